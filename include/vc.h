@@ -1,0 +1,290 @@
+/*
+ * vc.h -- C ABI of the GB300 (sm_103a) hot path of VeriCache's lossless
+ * draft -> verify -> accept decode loop.
+ *
+ * Source of the method: "VeriCache: Turning Lossy KV Cache into Lossless LLM
+ * Inference" (gist.science/paper/2605.17613), Technical Summary:
+ *   - Core Algorithm: draft with the compressed KV, verify with one forward
+ *     pass over the full KV, accept up to the first mismatch (+ bonus token);
+ *   - Key System Innovations (1): drafting is HBM-bound, verification is
+ *     interconnect-bound; requests are staggered so the two overlap;
+ *   - Architecture Support: compressed KV in GPU memory, full KV in CPU
+ *     memory loaded over the CPU-GPU link for verification; a uniform
+ *     compressor interface for token-dropping and quantisation methods
+ *     (KIVI, SnapKV named).
+ *
+ * Five shared libraries implement this header:
+ *   libvc_core.so         status strings, last-error text (used by the others)
+ *   libvc_quant_kv.so     compressors: KIVI-style pack / append, SnapKV-style
+ *                         score / select / gather
+ *   libvc_draft_attn.so   decode attention over the packed draft cache
+ *   libvc_verify_attn.so  verify attention over the full KV streamed from
+ *                         pinned host memory, commit of accepted tokens
+ *   libvc_accept.so       argmax / first-mismatch / bonus token
+ *
+ * Conventions (all entry points):
+ *   - Every call returns vc_status_t.  Argument errors are detected on the
+ *     host and returned before anything is launched; vc_last_error() then
+ *     holds a one-line reason (thread-local).  No exception crosses the ABI.
+ *   - Compute calls are asynchronous on the stream given (NULL = the legacy
+ *     default stream).  A fault inside a kernel surfaces at the caller's next
+ *     synchronisation.  Kernels that wait on a barrier give up after a bounded
+ *     time and raise a device error flag, read with vc_*_device_status().
+ *   - The caller owns every buffer (device memory, pinned host memory); the
+ *     libraries allocate nothing per call.  Scratch space is passed in as a
+ *     workspace whose size the *_workspace_size() query returns.
+ *   - Pointers are plain addresses: "device" = memory the GPU can address
+ *     (cudaMalloc / PyTorch CUDA tensors); "pinned host" = cudaHostAlloc'd
+ *     memory.  All tensor pointers must be 16-byte aligned.
+ *   - bf16 tensors are passed as uint16_t bit patterns, fp16 as uint16_t.
+ *   - GQA: query head h reads KV head h / G, G = Hq / Hkv (contiguous groups).
+ */
+#ifndef VC_H_
+#define VC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* vc_stream_t; /* ABI-identical to cudaStream_t */
+
+typedef enum {
+  VC_OK = 0,
+  VC_ERR_INVALID_ARG = 1, /* NULL / misaligned pointer, negative or inconsistent size */
+  VC_ERR_UNSUPPORTED = 2, /* valid but not built: bits not in {2,4}, d not in {64,128}, G > 8 ... */
+  VC_ERR_CUDA = 3,        /* a CUDA runtime call failed (text in vc_last_error) */
+  VC_ERR_TIMEOUT = 4,     /* a bounded wait expired (host event wait or device barrier) */
+  VC_ERR_WORKSPACE = 5,   /* workspace pointer NULL or smaller than *_workspace_size() */
+  VC_ERR_CAPACITY = 6     /* a length would exceed the capacity the caller allocated */
+} vc_status_t;
+
+/* Attention shape shared by the calls below.  Fields a call does not use are
+ * ignored (each call lists the ones it reads). */
+typedef struct {
+  int32_t B;             /* requests in the batch */
+  int32_t Hq;            /* query heads */
+  int32_t Hkv;           /* KV heads, Hq % Hkv == 0, G = Hq / Hkv <= 8 */
+  int32_t d;             /* head dim: 64 or 128 */
+  int32_t k;             /* draft length; verify has k + 1 rows per request */
+  int32_t bits;          /* KIVI code width: 2 or 4 */
+  float softmax_scale;   /* logits = softmax_scale * q . k */
+} vc_shape_t;
+
+/* ------------------------------------------------------------ libvc_core */
+
+/* Static text for a status code. */
+const char* vc_status_str(vc_status_t s);
+/* Reason of the last failing call on this thread ("" if none).  The pointer
+ * stays valid until the next failing call on the same thread. */
+const char* vc_last_error(void);
+
+/* ------------------------------------------------------- libvc_quant_kv
+ * KIVI-style quantiser (VeriCache, Architecture Support: KIVI is one of the
+ * quantisation methods the compressor interface takes).  Per group of 32
+ * values: s = fp16((max - min) / (2^b - 1)), z = fp16(min),
+ * code = clamp(rint((x - z) / s), 0, 2^b - 1) with round-half-even (0 if
+ * s == 0); dequantised x^ = fma(code, s, z) in fp32.  Keys group along 32
+ * tokens of one channel, values along 32 channels of one token.
+ *
+ * Packed draft cache of capacity T_cap tokens (T_cap % 32 == 0),
+ * W = d * bits / 32 words per token, NG = T_cap / 32:
+ *   kc  uint32 [B, Hkv, NG, W, 32]  word (g, w, t): token 32g + t, channels
+ *                                   w*(32/bits) + j at bits [bits*j, bits*j + bits)
+ *   ksz fp16   [B, Hkv, NG, d, 2]   (scale, zero) of channel c in group g
+ *   vc  uint32 [B, Hkv, NG, W, 32]  same packing for values
+ *   vsz fp16   [B, Hkv, NG, d/32, 32, 2]  (scale, zero) of token 32g + t over
+ *                                   channels 32cg .. 32cg + 31
+ * Bytes per token per KV head: d*bits/4 (codes) + d/4 (metadata).
+ */
+
+/* Byte sizes of the four packed arrays for B, Hkv, d, bits and T_cap. */
+vc_status_t vc_quant_packed_bytes(const vc_shape_t* s, int32_t T_cap, size_t* kc_bytes,
+                                  size_t* ksz_bytes, size_t* vc_bytes, size_t* vsz_bytes);
+
+/* Quantise and pack the first T tokens (T % 32 == 0, T <= T_cap) of
+ * K, V bf16 [B, Hkv, T, d] (device, contiguous) into groups 0 .. T/32 - 1 of
+ * the packed cache (device).  Reads B, Hkv, d, bits. */
+vc_status_t vc_quant_kv_pack(const vc_shape_t* s, int32_t T, int32_t T_cap, const uint16_t* K,
+                             const uint16_t* V, uint32_t* kc, uint16_t* ksz, uint32_t* vc,
+                             uint16_t* vsz, vc_stream_t stream);
+
+/* Dequantise groups 0 .. T/32 - 1 of a packed cache into fp32
+ * K_hat, V_hat [B, Hkv, T, d] (device).  For tests and inspection. */
+vc_status_t vc_quant_kv_unpack(const vc_shape_t* s, int32_t T, int32_t T_cap, const uint32_t* kc,
+                               const uint16_t* ksz, const uint32_t* vc, const uint16_t* vsz,
+                               float* K_hat, float* V_hat, vc_stream_t stream);
+
+/* Commit the accepted tokens to the draft cache and pack full groups
+ * (VeriCache, Core Algorithm: the loop repeats from the last accepted token).
+ * For every request b (device arrays):
+ *   1. append the exact K/V of the n_acc[b] + 1 committed verify inputs,
+ *      k_new/v_new bf16 [B, k+1, Hkv, d] rows 0 .. n_acc[b], to the bf16
+ *      tail [B, Hkv, tail_cap, d] at tail_len[b] (draft-time entries past
+ *      tail_len[b] are overwritten: they are dropped);
+ *   2. while the tail holds >= 32 tokens, quantise its oldest 32 into group
+ *      packed_len[b] / 32 of the packed cache, packed_len[b] += 32, and shift
+ *      the tail down by 32.
+ * tail_len and packed_len (int32 [B], device) are updated in place.  If a
+ * request would overflow tail_cap or T_cap, it is left unchanged and the
+ * device status flag is raised (vc_quant_kv_device_status).
+ * n_acc may be NULL to append all k + 1 rows.  Reads B, Hkv, d, k, bits. */
+vc_status_t vc_quant_kv_append(const vc_shape_t* s, const uint16_t* k_new, const uint16_t* v_new,
+                               const int32_t* n_acc, uint16_t* tail_k, uint16_t* tail_v,
+                               int32_t* tail_len, int32_t tail_cap, uint32_t* kc, uint16_t* ksz,
+                               uint32_t* vc, uint16_t* vsz, int32_t* packed_len, int32_t T_cap,
+                               vc_stream_t stream);
+
+/* SnapKV-style token score (VeriCache, Architecture Support: SnapKV is one
+ * of the token-dropping methods the interface takes).  For each request b
+ * and KV head: score[t] = sum over the G query heads of the group and over
+ * the n_obs observation queries i of softmax_i(t), where query i sits at
+ * position T - n_obs + i and sees keys 0 .. T - n_obs + i.
+ * q_obs bf16 [B, Hq, n_obs, d], K bf16 [B, Hkv, T, d] -> score fp32
+ * [B, Hkv, T] (all device).  fp32 arithmetic on CUDA cores.  n_obs <= 32,
+ * G * n_obs a multiple of 16, T >= n_obs.
+ * Reads B, Hq, Hkv, d, softmax_scale. */
+vc_status_t vc_token_score_workspace_size(const vc_shape_t* s, int32_t T, int32_t n_obs,
+                                          size_t* bytes);
+vc_status_t vc_token_score(const vc_shape_t* s, int32_t T, int32_t n_obs, const uint16_t* q_obs,
+                           const uint16_t* K, float* score, void* workspace,
+                           size_t workspace_bytes, vc_stream_t stream);
+
+/* Token selection: pooled[t] = max(score[t - pool/2 .. t + pool/2]) (window
+ * clipped at the ends); keep the last keep_last tokens and the
+ * keep - keep_last tokens of 0 .. T - keep_last - 1 with the largest pooled
+ * score (ties -> lower index).  idx int32 [B, Hkv, keep] ascending (device).
+ * pool odd, 1 <= pool <= 15; keep_last <= keep <= T. */
+vc_status_t vc_token_select_workspace_size(int32_t B, int32_t Hkv, int32_t T, size_t* bytes);
+vc_status_t vc_token_select(int32_t B, int32_t Hkv, int32_t T, const float* score, int32_t keep,
+                            int32_t keep_last, int32_t pool, int32_t* idx, void* workspace,
+                            size_t workspace_bytes, vc_stream_t stream);
+
+/* Gather kept tokens: out[b, h, j] = X[b, h, idx[b, h, j]] for K and V,
+ * bf16 [B, Hkv, T, d] -> [B, Hkv, keep, d] (device).  Indices must lie in
+ * [0, T); an out-of-range index raises the device status flag and writes
+ * zeros.  Reads B, Hkv, d. */
+vc_status_t vc_gather_kv(const vc_shape_t* s, int32_t T, int32_t keep, const int32_t* idx,
+                         const uint16_t* K, const uint16_t* V, uint16_t* K_out, uint16_t* V_out,
+                         vc_stream_t stream);
+
+/* Device status of libvc_quant_kv kernels since the last call: 0 = none.
+ * Synchronises the device; clears the flag. */
+vc_status_t vc_quant_kv_device_status(uint32_t* status);
+
+/* ------------------------------------------------------ libvc_draft_attn
+ * Draft decode attention over the compressed cache (VeriCache, Core
+ * Algorithm, Drafting; Key System Innovations: drafting is bound by HBM
+ * bandwidth).  For request b and query head h:
+ *   o = softmax(scale * q . [K^ ; tail_k[0 : tail_len[b] + step] ; k_cur]^T)
+ *       [V^ ; tail_v[...] ; v_cur]
+ * with K^, V^ the dequantised packed tokens 0 .. packed_len[b] - 1.
+ * If k_cur/v_cur (bf16 [B, Hkv, d]) are given, they are also stored at tail
+ * position tail_len[b] + step (for the following draft steps); if NULL, the
+ * current token is not added and the tail is not written.
+ * q bf16 [B, Hq, d] -> out bf16 [B, Hq, d].  packed_len, tail_len: int32 [B]
+ * device.  max_packed: an upper bound of packed_len over the batch (host).
+ * Split-KV over 32-token groups, log-sum-exp combine, fp32 accumulation.
+ * Reads B, Hq, Hkv, d, bits, softmax_scale. */
+vc_status_t vc_draft_attn_workspace_size(const vc_shape_t* s, int32_t max_packed, size_t* bytes);
+vc_status_t vc_draft_attn(const vc_shape_t* s, const uint16_t* q, const uint16_t* k_cur,
+                          const uint16_t* v_cur, const uint32_t* kc, const uint16_t* ksz,
+                          const uint32_t* vc, const uint16_t* vsz, const int32_t* packed_len,
+                          int32_t max_packed, int32_t T_cap, uint16_t* tail_k, uint16_t* tail_v,
+                          const int32_t* tail_len, int32_t tail_cap, int32_t step, uint16_t* out,
+                          void* workspace, size_t workspace_bytes, vc_stream_t stream);
+/* Device status (barrier time-outs) since the last call; synchronises. */
+vc_status_t vc_draft_attn_device_status(uint32_t* status);
+
+/* ----------------------------------------------------- libvc_verify_attn
+ * Verify attention (VeriCache, Core Algorithm, Verification: one forward
+ * pass over the full KV checks all drafted tokens at once).  Verify row j in
+ * 0 .. k (inputs [t_last, d_0 .. d_{k-1}]) of request b, query head h:
+ *   o = softmax(scale * q_j . [K[0 : prefix_len[b]] ; k_new[0 .. j]]^T) [V ; v_new]
+ * The full KV lives in pinned host memory (Architecture Support) in chunks
+ * of C tokens, chunk-major:
+ *   host_kv bf16 [n_chunks_cap][2 (K, V)][B][Hkv][C][d]
+ * so that one chunk is one contiguous host->device copy into a device slot
+ * bf16 [2][B][Hkv][C][d].
+ * q bf16 [B, k+1, Hq, d]; k_new, v_new bf16 [B, k+1, Hkv, d]; out bf16
+ * [B, k+1, Hq, d].  Rows per KV head M = (k+1) * G <= 512.  Tensor-core
+ * (bf16 MMA, fp32 accumulate) QK^T and PV; split-KV partials merged with a
+ * log-sum-exp rule.  Reads B, Hq, Hkv, d, k, softmax_scale.
+ *
+ * Workspace: parts_per_chunk running partial states + one for the new tokens.
+ */
+vc_status_t vc_verify_attn_workspace_size(const vc_shape_t* s, int32_t parts_per_chunk, size_t* bytes);
+
+/* Low-level, one chunk already in device memory: merge its tokens
+ * [chunk_start, chunk_start + C) of every request (only those below
+ * prefix_len[b]) into the running partial state.  first != 0 starts a new
+ * pass (overwrites the state). */
+vc_status_t vc_verify_attn_chunk(const vc_shape_t* s, const uint16_t* q, const uint16_t* kv_slot,
+                                 int32_t C, int32_t chunk_start, const int32_t* prefix_len,
+                                 int32_t parts_per_chunk, int32_t first, void* workspace,
+                                 size_t workspace_bytes, vc_stream_t stream);
+/* The causal block of the k + 1 new tokens, then the final combine -> out. */
+vc_status_t vc_verify_attn_finish(const vc_shape_t* s, const uint16_t* q, const uint16_t* k_new,
+                                  const uint16_t* v_new, int32_t parts_per_chunk,
+                                  int32_t any_chunk, uint16_t* out, void* workspace,
+                                  size_t workspace_bytes, vc_stream_t stream);
+
+/* Streamed pipeline: events for a ring of n_slots device slots. */
+typedef struct vc_verify_pipeline* vc_verify_pipeline_t;
+vc_status_t vc_verify_pipeline_create(int32_t n_slots, vc_verify_pipeline_t* p);
+vc_status_t vc_verify_pipeline_destroy(vc_verify_pipeline_t p);
+
+/* Host-side prefetch of chunks [0, n_chunks) on the copy stream into ring
+ * slots, as far as free slots allow, without the compute side.  Lets a
+ * caller start the transfer before the verify queries exist (e.g. while
+ * drafting).  Tokens at or beyond max_prefix are not copied. */
+vc_status_t vc_verify_prefetch(vc_verify_pipeline_t p, const vc_shape_t* s,
+                               const uint16_t* host_kv, int32_t C, int32_t max_prefix,
+                               uint16_t* dev_slots, vc_stream_t copy_stream);
+
+/* Whole verify for one layer: streams chunks 0 .. ceil(max_prefix / C) - 1
+ * of host_kv (pinned) through the ring dev_slots (device, n_slots slots of
+ * 2*B*Hkv*C*d bf16 each) on copy_stream, runs the chunk kernels on
+ * compute_stream as chunks land (CUDA events, no host waits), then the new
+ * tokens and the combine.  max_prefix (host) bounds prefix_len[b] (device). */
+vc_status_t vc_verify_attn_streamed(vc_verify_pipeline_t p, const vc_shape_t* s,
+                                    const uint16_t* q, const uint16_t* host_kv, int32_t C,
+                                    int32_t max_prefix, const int32_t* prefix_len,
+                                    uint16_t* dev_slots, const uint16_t* k_new,
+                                    const uint16_t* v_new, uint16_t* out, int32_t parts_per_chunk,
+                                    void* workspace, size_t workspace_bytes,
+                                    vc_stream_t compute_stream, vc_stream_t copy_stream);
+
+/* Commit the exact K/V of the n_acc[b] + 1 accepted verify inputs (rows
+ * 0 .. n_acc[b] of k_new/v_new) into the pinned host store at token
+ * prefix_len[b] and advance prefix_len[b] (device, in place).  The kernel
+ * writes host memory directly (mapped pinned memory).  A request that would
+ * pass T_cap (= n_chunks_cap * C) is left unchanged and raises the device
+ * status flag.  n_acc may be NULL (commit all k + 1 rows). */
+vc_status_t vc_verify_commit(const vc_shape_t* s, const uint16_t* k_new, const uint16_t* v_new,
+                             const int32_t* n_acc, int32_t* prefix_len, uint16_t* host_kv,
+                             int32_t C, int32_t T_cap, vc_stream_t stream);
+
+/* Device status of libvc_verify_attn kernels since the last call; synchronises. */
+vc_status_t vc_verify_attn_device_status(uint32_t* status);
+
+/* ------------------------------------------------------------ libvc_accept
+ * Acceptance (VeriCache, Core Algorithm, Acceptance).  For request b:
+ * a_i = argmax_v logits[b, i, v] (ties -> lowest v, IEEE comparisons) for
+ * i in 0 .. k; n_acc[b] = first i < k with a_i != draft[b, i], else k;
+ * next_tok[b] = a_{n_acc[b]} (the bonus token when n_acc == k, the full-KV
+ * correction otherwise).  logits fp32 [B, k+1, V], draft int32 [B, k];
+ * outputs int32 (device); argmax int32 [B, k+1] optional (NULL to skip).
+ * NaN logits are unsupported.  The workspace must be zero-filled before its
+ * first use; every call leaves it zero-filled again. */
+vc_status_t vc_accept_workspace_size(int32_t B, int32_t k, int32_t V, size_t* bytes);
+vc_status_t vc_accept(int32_t B, int32_t k, int32_t V, const float* logits, const int32_t* draft,
+                      int32_t* n_acc, int32_t* next_tok, int32_t* argmax, void* workspace,
+                      size_t workspace_bytes, vc_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VC_H_ */

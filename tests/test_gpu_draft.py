@@ -1,0 +1,147 @@
+"""vc_draft_attn on the GPU vs the oracle (fp64): max-abs <= 2e-2, mean-abs <= 2e-3."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import attention as oatt
+from oracle import kivi
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def vc():
+    from verify_compressed_kv_gb300 import _lib
+    return _lib
+
+
+def run_draft(vc, w, K, V, packed_len, tail_k, tail_v, tail_len, q, scale, k_cur=None, v_cur=None, step=0,
+              T_cap=None, tail_cap=None):
+    """Pack K/V on the GPU, run one draft step, return (out bf16 -> f64, tail after the call)."""
+    from gpu_util import dev, zeros_bytes, bf16_to_f64, DEV
+    B, H, T, d = K.shape
+    T_cap = T if T_cap is None else T_cap
+    tail_cap = tail_k.shape[2] if tail_cap is None else tail_cap
+    s = vc.shape(B, w.Hq, H, d, bits=w.bits, softmax_scale=scale)
+    kcb, kszb, vcb, vszb = vc.vc_quant_packed_bytes(s, T_cap)
+    kc = torch.zeros(kcb // 4, dtype=torch.int32, device=DEV)
+    ksz = torch.zeros(kszb // 2, dtype=torch.int16, device=DEV)
+    vcc = torch.zeros(vcb // 4, dtype=torch.int32, device=DEV)
+    vsz = torch.zeros(vszb // 2, dtype=torch.int16, device=DEV)
+    vc.vc_quant_kv_pack(s, T, T_cap, dev(K), dev(V), kc, ksz, vcc, vsz)
+    max_packed = int(max(packed_len))
+    wsb = vc.vc_draft_attn_workspace_size(s, max_packed)
+    ws = zeros_bytes(wsb)
+    out = torch.empty((B, w.Hq, d), dtype=torch.int16, device=DEV)
+    tk, tv = dev(tail_k), dev(tail_v)
+    vc.vc_draft_attn(s, dev(q), None if k_cur is None else dev(k_cur), None if v_cur is None else dev(v_cur),
+                     kc, ksz, vcc, vsz, dev(np.asarray(packed_len, np.int32)), max_packed, T_cap, tk, tv,
+                     dev(np.asarray(tail_len, np.int32)), tail_cap, step, out, ws, wsb)
+    torch.cuda.synchronize()
+    assert vc.vc_draft_attn_device_status() == 0
+    return bf16_to_f64(out), tk.cpu().numpy().view(np.uint16), tv.cpu().numpy().view(np.uint16)
+
+
+CASES = [
+    # name, overrides, packed_len per request, tail_len per request, step, with current token
+    ("tiny", dict(), [512], [0], 0, True),
+    ("tiny_tail", dict(), [480], [17], 2, True),
+    ("mistral_small", dict(B=3, T=2048), [2048, 1024, 32], [0, 5, 31], 3, True),
+    ("mistral_ragged_splits", dict(B=2, T=1600), [1600, 544], [1, 0], 0, False),
+    ("qwen_small", dict(B=2, T=1024, keep_frac=1.0), [1024, 992], [3, 0], 1, True),
+    ("llama_small", dict(B=2, T=1024, layers=1), [1024, 512], [0, 9], 0, True),
+    ("g1_d64_b2", dict(B=1, Hq=2, Hkv=2, d=64, bits=2, T=640), [640], [4], 0, True),
+    ("g2_d128_b4", dict(B=1, Hq=4, Hkv=2, d=128, bits=4, T=256), [256], [0], 0, True),
+]
+
+
+@pytest.mark.parametrize("name,ov,plen,tlen,step,cur", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("scale_kind", ["one", "rsqrt_d"])
+def test_draft_parity(vc, name, ov, plen, tlen, step, cur, scale_kind):
+    base = name.split("_")[0] if name.split("_")[0] in synth.WORKLOADS else "mistral"
+    w = synth.get(base, **ov)
+    scale = 1.0 if scale_kind == "one" else 1.0 / math.sqrt(w.d)
+    K, V = synth.kv(w)
+    rng = np.random.default_rng(len(name))
+    tail_cap = 32 + w.k + 1
+    tail_k = synth.bf16_bits(rng.standard_normal((w.B, w.Hkv, tail_cap, w.d)).astype(np.float32))
+    tail_v = synth.bf16_bits(rng.standard_normal((w.B, w.Hkv, tail_cap, w.d)).astype(np.float32))
+    q = synth.draft_q(w, 0, step)
+    k_cur, v_cur = synth.draft_kv_cur(w, 0, step) if cur else (None, None)
+    got, tk, tv = run_draft(vc, w, K, V, plen, tail_k, tail_v, tlen, q, scale, k_cur, v_cur, step)
+    packed = kivi.quant_pack(K, V, w.bits)
+    want = oatt.draft_attention(q, *packed, plen, tail_k, tail_v, tlen, w.bits, scale,
+                                k_cur=k_cur, v_cur=v_cur, step=step)
+    from gpu_util import assert_attn_close
+    assert_attn_close(got, want, what=name)
+    if cur:        # the current token was stored at tail position tail_len + step
+        for b in range(w.B):
+            assert np.array_equal(tk[b, :, tlen[b] + step], k_cur[b])
+            assert np.array_equal(tv[b, :, tlen[b] + step], v_cur[b])
+
+
+def test_draft_tail_only_equals_textbook(vc):
+    """packed_len = 0: pure bf16 attention over the tail and the current token."""
+    w = synth.get("mistral", B=2, T=32)
+    K, V = synth.kv(w)
+    rng = np.random.default_rng(0)
+    tail_cap = 49
+    tail_k = synth.bf16_bits(rng.standard_normal((2, 8, tail_cap, 128)).astype(np.float32))
+    tail_v = synth.bf16_bits(rng.standard_normal((2, 8, tail_cap, 128)).astype(np.float32))
+    q = synth.draft_q(w, 0, 0)
+    got, _, _ = run_draft(vc, w, K, V, [0, 0], tail_k, tail_v, [40, 7], q, 1 / math.sqrt(128))
+    G = w.G
+    want = np.empty_like(got)
+    for b, n in enumerate([40, 7]):
+        for h in range(w.Hq):
+            want[b, h] = oatt.softmax_attend(synth.bf16_to_f32(q[b, h]).astype(np.float64),
+                                             synth.bf16_to_f32(tail_k[b, h // G, :n]).astype(np.float64),
+                                             synth.bf16_to_f32(tail_v[b, h // G, :n]).astype(np.float64),
+                                             1 / math.sqrt(128))
+    from gpu_util import assert_attn_close
+    assert_attn_close(got, want, what="tail only")
+
+
+@pytest.mark.parametrize("name", ["mistral", "qwen", "llama", "stagger"])
+def test_draft_full_size_sampled(vc, name):
+    """Full-size layer (all requests, all heads in one launch, the bench's launch
+    configuration); sampled (request, KV head) slices against the oracle."""
+    w = synth.get(name)
+    T = w.T_keep if name == "qwen" else w.T        # Qwen drafts over the kept quarter
+    K, V = synth.kv(w, T=T)
+    tail_cap = 32 + w.k + 1
+    rng = np.random.default_rng(1)
+    tlen = rng.integers(0, 32, size=w.B)
+    tail_k = synth.bf16_bits(rng.standard_normal((w.B, w.Hkv, tail_cap, w.d)).astype(np.float32))
+    tail_v = synth.bf16_bits(rng.standard_normal((w.B, w.Hkv, tail_cap, w.d)).astype(np.float32))
+    q = synth.draft_q(w, 0, 0)
+    k_cur, v_cur = synth.draft_kv_cur(w, 0, 0)
+    plen = [T] * w.B
+    got, _, _ = run_draft(vc, w, K, V, plen, tail_k, tail_v, tlen, q, 1.0, k_cur, v_cur, 0)
+    from gpu_util import assert_attn_close
+    G = w.G
+    for (b, h) in [(0, 0), (w.B - 1, w.Hkv - 1), (w.B // 2, 3)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        packed = kivi.quant_pack(K[sl], V[sl], w.bits)
+        want = oatt.draft_attention(q[b:b + 1, h * G:(h + 1) * G], *packed, [T], tail_k[sl], tail_v[sl],
+                                    tlen[b:b + 1], w.bits, 1.0, k_cur=k_cur[sl], v_cur=v_cur[sl], step=0)
+        assert_attn_close(got[b, h * G:(h + 1) * G], want[0], what=f"{name} b{b} h{h}")
+
+
+def test_draft_argument_errors(vc):
+    from gpu_util import DEV
+    s = vc.shape(1, 4, 1, 96, bits=2)
+    with pytest.raises(vc.VcError) as e:
+        vc.vc_draft_attn_workspace_size(s, 64)
+    assert e.value.status == 2
+    s = vc.shape(1, 4, 1, 64, bits=3)
+    with pytest.raises(vc.VcError) as e:
+        vc.vc_draft_attn_workspace_size(s, 64)
+    assert e.value.status == 2
+    s = vc.shape(1, 4, 1, 64, bits=2)
+    with pytest.raises(vc.VcError) as e:
+        vc.vc_draft_attn_workspace_size(s, 65)
+    assert e.value.status == 1

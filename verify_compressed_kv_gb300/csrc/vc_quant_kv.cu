@@ -1,0 +1,814 @@
+// libvc_quant_kv: the draft-cache compressors behind VeriCache's uniform
+// compressor interface (gist.science/paper/2605.17613, Technical Summary,
+// Architecture Support: token-dropping and quantisation methods, e.g. KIVI
+// and SnapKV, plug in without touching scheduling or verification).
+//
+//   * KIVI-style quantiser: int2/int4 codes, keys per channel over 32 tokens,
+//     values per token over 32 channels, fp16 scale/zero from min/max,
+//     round-half-even.  pack (prefill), append (commit of accepted tokens +
+//     packing of full tail groups), unpack (tests).
+//   * SnapKV-style token dropping: score (attention mass from the last n_obs
+//     prompt queries, causal), select (7-wide max-pool, top-k + last tokens,
+//     ascending), gather.
+//
+// The quantiser's arithmetic is the exact fp32 sequence of the recipe
+// (separate correctly rounded subtract and divide, rintf, fp16 RNE), so the
+// codes are reproducible bit for bit.  Packed layout: include/vc.h.
+#include <cfloat>
+
+#include "vc_internal.h"
+
+namespace {
+
+__device__ uint32_t g_quant_status = 0;
+
+constexpr int kGroup = 32;
+
+// ------------------------------------------------------------------ quantiser
+
+// Quantise one 32-token tile held in shared memory.
+//   k_s, v_s : bf16 tiles [32][ld] (rows = tokens), ld >= d
+//   codes_s  : scratch uint8 [32][d + 4] (padded: conflict-free column reads)
+// Writes the tile's words and metadata into group `g` of (b, h)'s packed
+// arrays (already offset to the (b, h) slice).  All threads of the CTA call it.
+template <int BITS>
+__device__ void quantize_tile(const uint16_t* k_s, const uint16_t* v_s, int ld, int d,
+                              uint8_t* codes_s, int g, uint32_t* kc, uint16_t* ksz, uint32_t* vc,
+                              uint16_t* vsz) {
+  constexpr int QMAX = (1 << BITS) - 1;
+  constexpr int CPW = 32 / BITS;            // codes per 32-bit word
+  const int W = d / CPW;                    // words per token
+  const float qmax = static_cast<float>(QMAX);
+
+  // ---- keys: one thread per channel, group = 32 tokens of that channel
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    float mn = FLT_MAX, mx = -FLT_MAX;
+    for (int t = 0; t < kGroup; ++t) {
+      float x = vc_bf16_to_f32(k_s[t * ld + c]);
+      mn = fminf(mn, x);
+      mx = fmaxf(mx, x);
+    }
+    const uint16_t s16 = vc_f32_to_f16_rn(__fdiv_rn(__fsub_rn(mx, mn), qmax));
+    const uint16_t z16 = vc_f32_to_f16_rn(mn);
+    const float sf = vc_f16_to_f32(s16), zf = vc_f16_to_f32(z16);
+    for (int t = 0; t < kGroup; ++t) {
+      int code = 0;
+      if (sf != 0.0f) {
+        float r = rintf(__fdiv_rn(__fsub_rn(vc_bf16_to_f32(k_s[t * ld + c]), zf), sf));
+        r = fminf(fmaxf(r, 0.0f), qmax);
+        code = static_cast<int>(r);
+      }
+      codes_s[t * (d + 4) + c] = static_cast<uint8_t>(code);
+    }
+    const size_t m = (static_cast<size_t>(g) * d + c) * 2;
+    ksz[m] = s16;
+    ksz[m + 1] = z16;
+  }
+  __syncthreads();
+  // pack key words: word (w, t), consecutive threads -> consecutive t
+  for (int i = threadIdx.x; i < W * kGroup; i += blockDim.x) {
+    const int w = i / kGroup, t = i % kGroup;
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < CPW; ++j) word |= static_cast<uint32_t>(codes_s[t * (d + 4) + w * CPW + j]) << (BITS * j);
+    kc[(static_cast<size_t>(g) * W + w) * kGroup + t] = word;
+  }
+  // ---- values: one thread per (channel group, token), group = 32 channels
+  const int NC = d / kGroup;
+  for (int i = threadIdx.x; i < NC * kGroup; i += blockDim.x) {
+    const int cg = i / kGroup, t = i % kGroup;
+    const uint16_t* row = v_s + t * ld + cg * kGroup;
+    float mn = FLT_MAX, mx = -FLT_MAX;
+    for (int c = 0; c < kGroup; ++c) {
+      float x = vc_bf16_to_f32(row[c]);
+      mn = fminf(mn, x);
+      mx = fmaxf(mx, x);
+    }
+    const uint16_t s16 = vc_f32_to_f16_rn(__fdiv_rn(__fsub_rn(mx, mn), qmax));
+    const uint16_t z16 = vc_f32_to_f16_rn(mn);
+    const float sf = vc_f16_to_f32(s16), zf = vc_f16_to_f32(z16);
+    constexpr int WPG = kGroup / CPW;       // words per channel group
+#pragma unroll
+    for (int ww = 0; ww < WPG; ++ww) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int j = 0; j < CPW; ++j) {
+        int code = 0;
+        if (sf != 0.0f) {
+          float r = rintf(__fdiv_rn(__fsub_rn(vc_bf16_to_f32(row[ww * CPW + j]), zf), sf));
+          r = fminf(fmaxf(r, 0.0f), qmax);
+          code = static_cast<int>(r);
+        }
+        word |= static_cast<uint32_t>(code) << (BITS * j);
+      }
+      const int w = cg * WPG + ww;
+      vc[(static_cast<size_t>(g) * W + w) * kGroup + t] = word;
+    }
+    const size_t m = ((static_cast<size_t>(g) * NC + cg) * kGroup + t) * 2;
+    vsz[m] = s16;
+    vsz[m + 1] = z16;
+  }
+  __syncthreads();
+}
+
+// Load rows [0, 32) of a [*, d] bf16 matrix into a [32][ld] smem tile
+// (16-byte vectors; d multiple of 8).
+__device__ void load_tile(uint16_t* dst, int ld, const uint16_t* src, int d) {
+  const int vec = d / 8;
+  for (int i = threadIdx.x; i < kGroup * vec; i += blockDim.x) {
+    const int t = i / vec, v = i % vec;
+    const uint4 x = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(t) * d + v * 8);
+    uint32_t* o = reinterpret_cast<uint32_t*>(dst + t * ld + v * 8);
+    o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
+  }
+}
+
+struct Packed {
+  uint32_t* kc;
+  uint16_t* ksz;
+  uint32_t* vc;
+  uint16_t* vsz;
+};
+
+// Offsets of (b, h)'s slice in each packed array.
+__host__ __device__ inline Packed slice(Packed p, int bh, int T_cap, int d, int bits) {
+  const int NG = T_cap / kGroup;
+  const int W = d * bits / 32;
+  Packed r;
+  r.kc = p.kc + static_cast<size_t>(bh) * NG * W * kGroup;
+  r.vc = p.vc + static_cast<size_t>(bh) * NG * W * kGroup;
+  r.ksz = p.ksz + static_cast<size_t>(bh) * NG * d * 2;
+  r.vsz = p.vsz + static_cast<size_t>(bh) * NG * d * 2;
+  return r;
+}
+
+constexpr int kPackThreads = 128;
+
+// grid (T/32, B*Hkv): one 32-token group of one (b, h) per CTA.
+template <int BITS>
+__global__ void __launch_bounds__(kPackThreads) pack_kernel(const uint16_t* __restrict__ K,
+                                                            const uint16_t* __restrict__ V, int T,
+                                                            int T_cap, int d, Packed p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int ld = d + 2;                      // odd word stride: conflict-free row reads
+  uint16_t* k_s = reinterpret_cast<uint16_t*>(smem);
+  uint16_t* v_s = k_s + kGroup * ld;
+  uint8_t* codes_s = reinterpret_cast<uint8_t*>(v_s + kGroup * ld);
+  const int g = blockIdx.x, bh = blockIdx.y;
+  const size_t base = (static_cast<size_t>(bh) * T + static_cast<size_t>(g) * kGroup) * d;
+  load_tile(k_s, ld, K + base, d);
+  load_tile(v_s, ld, V + base, d);
+  __syncthreads();
+  Packed s = slice(p, bh, T_cap, d, BITS);
+  quantize_tile<BITS>(k_s, v_s, ld, d, codes_s, g, s.kc, s.ksz, s.vc, s.vsz);
+}
+
+size_t pack_smem(int d) { return 2 * kGroup * (d + 2) * sizeof(uint16_t) + kGroup * (d + 4); }
+
+// One CTA per request: append rows 0..n of k_new/v_new to the tail, then pack
+// whole groups from the tail's front (all KV heads of the request).
+template <int BITS>
+__global__ void __launch_bounds__(kPackThreads) append_kernel(
+    const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
+    const int32_t* __restrict__ n_acc, int k, int Hkv, int d, uint16_t* tail_k, uint16_t* tail_v,
+    int32_t* tail_len, int tail_cap, Packed p, int32_t* packed_len, int T_cap) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int ld = d + 2;
+  uint16_t* k_s = reinterpret_cast<uint16_t*>(smem);
+  uint16_t* v_s = k_s + kGroup * ld;
+  uint8_t* codes_s = reinterpret_cast<uint8_t*>(v_s + kGroup * ld);
+  const int b = blockIdx.x;
+  const int n = n_acc ? n_acc[b] : k;
+  int len = tail_len[b];
+  int plen = packed_len[b];
+  const int add = n + 1;
+  if (n < 0 || n > k || len < 0 || len + add > tail_cap) {
+    if (threadIdx.x == 0) atomicOr(&g_quant_status, VC_DEV_CAPACITY);
+    return;
+  }
+  const int total = len + add;
+  const int n_pack = total / kGroup;
+  if (plen + n_pack * kGroup > T_cap) {
+    if (threadIdx.x == 0) atomicOr(&g_quant_status, VC_DEV_CAPACITY);
+    return;
+  }
+  const int vec = d / 8;
+  // 1. append: tail[b, h, len + r] = new[b, r, h] for r <= n
+  for (int i = threadIdx.x; i < add * Hkv * vec; i += blockDim.x) {
+    const int v = i % vec, h = (i / vec) % Hkv, r = i / (vec * Hkv);
+    const size_t src = ((static_cast<size_t>(b) * (k + 1) + r) * Hkv + h) * d + v * 8;
+    const size_t dst = ((static_cast<size_t>(b) * Hkv + h) * tail_cap + len + r) * d + v * 8;
+    *reinterpret_cast<uint4*>(tail_k + dst) = *reinterpret_cast<const uint4*>(k_new + src);
+    *reinterpret_cast<uint4*>(tail_v + dst) = *reinterpret_cast<const uint4*>(v_new + src);
+  }
+  __syncthreads();
+  __threadfence_block();
+  // 2. pack whole groups from the front of the tail
+  for (int grp = 0; grp < n_pack; ++grp) {
+    for (int h = 0; h < Hkv; ++h) {
+      const size_t tb = (static_cast<size_t>(b) * Hkv + h) * tail_cap * d;
+      load_tile(k_s, ld, tail_k + tb + static_cast<size_t>(grp) * kGroup * d, d);
+      load_tile(v_s, ld, tail_v + tb + static_cast<size_t>(grp) * kGroup * d, d);
+      __syncthreads();
+      Packed s = slice(p, b * Hkv + h, T_cap, d, BITS);
+      quantize_tile<BITS>(k_s, v_s, ld, d, codes_s, plen / kGroup + grp, s.kc, s.ksz, s.vc, s.vsz);
+    }
+  }
+  // 3. shift the remaining (total - 32*n_pack < 32) tail tokens to the front
+  const int shift = n_pack * kGroup;
+  const int rest = total - shift;
+  if (shift > 0 && rest > 0) {
+    for (int h = 0; h < Hkv; ++h) {
+      const size_t tb = (static_cast<size_t>(b) * Hkv + h) * tail_cap * d;
+      // rest < 32 rows: stage through smem (rows overlap when shift < rest)
+      for (int i = threadIdx.x; i < rest * vec; i += blockDim.x) {
+        const int t = i / vec, v = i % vec;
+        const uint4 a = *reinterpret_cast<const uint4*>(tail_k + tb + static_cast<size_t>(shift + t) * d + v * 8);
+        const uint4 c = *reinterpret_cast<const uint4*>(tail_v + tb + static_cast<size_t>(shift + t) * d + v * 8);
+        uint32_t* ok = reinterpret_cast<uint32_t*>(k_s + t * ld + v * 8);
+        uint32_t* ov = reinterpret_cast<uint32_t*>(v_s + t * ld + v * 8);
+        ok[0] = a.x; ok[1] = a.y; ok[2] = a.z; ok[3] = a.w;
+        ov[0] = c.x; ov[1] = c.y; ov[2] = c.z; ov[3] = c.w;
+      }
+      __syncthreads();
+      for (int i = threadIdx.x; i < rest * vec; i += blockDim.x) {
+        const int t = i / vec, v = i % vec;
+        const uint32_t* ik = reinterpret_cast<const uint32_t*>(k_s + t * ld + v * 8);
+        const uint32_t* iv = reinterpret_cast<const uint32_t*>(v_s + t * ld + v * 8);
+        *reinterpret_cast<uint4*>(tail_k + tb + static_cast<size_t>(t) * d + v * 8) = make_uint4(ik[0], ik[1], ik[2], ik[3]);
+        *reinterpret_cast<uint4*>(tail_v + tb + static_cast<size_t>(t) * d + v * 8) = make_uint4(iv[0], iv[1], iv[2], iv[3]);
+      }
+      __syncthreads();
+    }
+  }
+  if (threadIdx.x == 0) {
+    tail_len[b] = rest;
+    packed_len[b] = plen + shift;
+  }
+}
+
+// grid (T/32, B*Hkv), thread per (token, channel) pairs.
+template <int BITS>
+__global__ void unpack_kernel(int T, int T_cap, int d, Packed p, float* K_hat, float* V_hat) {
+  constexpr int CPW = 32 / BITS;
+  constexpr uint32_t MASK = (1u << BITS) - 1u;
+  const int W = d / CPW;
+  const int g = blockIdx.x, bh = blockIdx.y;
+  Packed s = slice(p, bh, T_cap, d, BITS);
+  for (int i = threadIdx.x; i < kGroup * d; i += blockDim.x) {
+    const int t = i / d, c = i % d;
+    const int w = c / CPW, j = c % CPW;
+    const uint32_t kw = s.kc[(static_cast<size_t>(g) * W + w) * kGroup + t];
+    const uint32_t vw = s.vc[(static_cast<size_t>(g) * W + w) * kGroup + t];
+    const float kcode = static_cast<float>((kw >> (BITS * j)) & MASK);
+    const float vcode = static_cast<float>((vw >> (BITS * j)) & MASK);
+    const size_t km = (static_cast<size_t>(g) * d + c) * 2;
+    const size_t vm = ((static_cast<size_t>(g) * (d / kGroup) + c / kGroup) * kGroup + t) * 2;
+    const size_t o = (static_cast<size_t>(bh) * T + static_cast<size_t>(g) * kGroup + t) * d + c;
+    K_hat[o] = fmaf(kcode, vc_f16_to_f32(s.ksz[km]), vc_f16_to_f32(s.ksz[km + 1]));
+    V_hat[o] = fmaf(vcode, vc_f16_to_f32(s.vsz[vm]), vc_f16_to_f32(s.vsz[vm + 1]));
+  }
+}
+
+// ------------------------------------------------------------------ token score
+//
+// Two passes over q_obs . K^T on CUDA cores (fp32), CTA tile = all NR = G*n_obs
+// rows of one KV head x 128 tokens, d in shared memory transposed.
+//   pass 1: per row, (max, sum exp) over its visible tokens, per token range;
+//   pass 2: merge the ranges' (max, sum), then score[t] = sum_r p_r(t).
+constexpr int kScoreThreads = 256;    // 16 (row lanes) x 16 (token lanes)
+constexpr int kTT = 128;              // tokens per tile
+constexpr int kTilesPerRange = 4;     // pass-1 CTA covers 4 tiles = 512 tokens
+
+struct ScoreArgs {
+  const uint16_t* q;    // [B, Hq, n_obs, d]
+  const uint16_t* K;    // [B, Hkv, T, d]
+  int T, n_obs, Hq, Hkv, d;
+  float scale_log2;     // softmax_scale * log2(e)
+  float2* stats;        // [B*Hkv, n_ranges, NR] (max, sum) in log2 units
+  int n_ranges;
+  float* score;         // [B, Hkv, T]
+};
+
+// Shared memory: qT [d][NR] fp32, kT [d][kTT + 1] fp32.
+template <int RPT>
+__device__ void load_q(const ScoreArgs& a, int b, int kvh, float* qT) {
+  const int NR = RPT * 16;
+  const int G = a.Hq / a.Hkv;
+  for (int i = threadIdx.x; i < NR * a.d; i += blockDim.x) {
+    const int r = i / a.d, c = i % a.d;
+    const int g = r / a.n_obs, o = r % a.n_obs;
+    const size_t src = ((static_cast<size_t>(b) * a.Hq + kvh * G + g) * a.n_obs + o) * a.d + c;
+    qT[c * NR + r] = vc_bf16_to_f32(a.q[src]) * a.scale_log2;
+  }
+}
+
+__device__ void load_kT(const ScoreArgs& a, int bh, int t0, float* kT) {
+  for (int i = threadIdx.x; i < kTT * a.d; i += blockDim.x) {
+    const int t = i / a.d, c = i % a.d;
+    float x = 0.0f;
+    if (t0 + t < a.T) x = vc_bf16_to_f32(a.K[(static_cast<size_t>(bh) * a.T + t0 + t) * a.d + c]);
+    kT[c * (kTT + 1) + t] = x;
+  }
+}
+
+// acc[i][j] = q_row(ty + 16 i) . k_tok(tx + 16 j), log2-scaled.
+template <int RPT>
+__device__ __forceinline__ void tile_dots(const float* qT, const float* kT, int d, int ty, int tx,
+                                          float (&acc)[RPT][8]) {
+  const int NR = RPT * 16;
+#pragma unroll
+  for (int i = 0; i < RPT; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+  for (int c = 0; c < d; ++c) {
+    float qv[RPT], kv[8];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) qv[i] = qT[c * NR + ty + 16 * i];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) kv[j] = kT[c * (kTT + 1) + tx + 16 * j];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(qv[i], kv[j], acc[i][j]);
+  }
+}
+
+// grid (n_ranges, B*Hkv)
+template <int RPT>
+__global__ void __launch_bounds__(kScoreThreads) score_pass1(ScoreArgs a) {
+  extern __shared__ __align__(16) float fsm[];
+  const int NR = RPT * 16;
+  float* qT = fsm;
+  float* kT = qT + NR * a.d;
+  const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh % a.Hkv;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  load_q<RPT>(a, b, kvh, qT);
+  float m[RPT], s[RPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) { m[i] = -INFINITY; s[i] = 0.0f; }
+  for (int tile = 0; tile < kTilesPerRange; ++tile) {
+    const int t0 = (blockIdx.x * kTilesPerRange + tile) * kTT;
+    if (t0 >= a.T) break;
+    __syncthreads();
+    load_kT(a, bh, t0, kT);
+    __syncthreads();
+    float acc[RPT][8];
+    tile_dots<RPT>(qT, kT, a.d, ty, tx, acc);
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const int r = ty + 16 * i;
+      const int last = a.T - a.n_obs + (r % a.n_obs);        // inclusive visible limit
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int t = t0 + tx + 16 * j;
+        if (t > last) acc[i][j] = -INFINITY;
+        tmax = fmaxf(tmax, acc[i][j]);
+      }
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+      const float mn = fmaxf(m[i], tmax);
+      if (mn == -INFINITY) continue;
+      float add = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) add += exp2f(acc[i][j] - mn);
+      s[i] = s[i] * exp2f(m[i] - mn) + add;
+      m[i] = mn;
+    }
+  }
+  // sum the 16 token lanes (all hold the same m)
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) s[i] += __shfl_xor_sync(0xffffffffu, s[i], off);
+    if (tx == 0) {
+      const int r = ty + 16 * i;
+      a.stats[(static_cast<size_t>(bh) * a.n_ranges + blockIdx.x) * NR + r] = make_float2(m[i], s[i]);
+    }
+  }
+}
+
+// grid (ceil(T / kTT), B*Hkv)
+template <int RPT>
+__global__ void __launch_bounds__(kScoreThreads) score_pass2(ScoreArgs a) {
+  extern __shared__ __align__(16) float fsm[];
+  const int NR = RPT * 16;
+  float* qT = fsm;
+  float* kT = qT + NR * a.d;
+  float* red = kT + a.d * (kTT + 1);            // [16][kTT]
+  float* rowm = red + 16 * kTT;                 // [NR]
+  float* rowinv = rowm + NR;                    // [NR]
+  const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh % a.Hkv;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int t0 = blockIdx.x * kTT;
+  load_q<RPT>(a, b, kvh, qT);
+  // merge the per-range statistics of every row
+  for (int r = threadIdx.x; r < NR; r += blockDim.x) {
+    float M = -INFINITY;
+    for (int x = 0; x < a.n_ranges; ++x)
+      M = fmaxf(M, a.stats[(static_cast<size_t>(bh) * a.n_ranges + x) * NR + r].x);
+    float S = 0.0f;
+    for (int x = 0; x < a.n_ranges; ++x) {
+      const float2 st = a.stats[(static_cast<size_t>(bh) * a.n_ranges + x) * NR + r];
+      if (st.x != -INFINITY) S += st.y * exp2f(st.x - M);
+    }
+    rowm[r] = M;
+    rowinv[r] = 1.0f / S;
+  }
+  load_kT(a, bh, t0, kT);
+  __syncthreads();
+  float acc[RPT][8];
+  tile_dots<RPT>(qT, kT, a.d, ty, tx, acc);
+  float col[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) col[j] = 0.0f;
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int r = ty + 16 * i;
+    const int last = a.T - a.n_obs + (r % a.n_obs);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int t = t0 + tx + 16 * j;
+      if (t <= last) col[j] += exp2f(acc[i][j] - rowm[r]) * rowinv[r];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) red[ty * kTT + tx + 16 * j] = col[j];
+  __syncthreads();
+  for (int t = threadIdx.x; t < kTT; t += blockDim.x) {
+    if (t0 + t >= a.T) continue;
+    float sum = 0.0f;
+    for (int y = 0; y < 16; ++y) sum += red[y * kTT + t];
+    a.score[static_cast<size_t>(bh) * a.T + t0 + t] = sum;
+  }
+}
+
+size_t score_smem(int NR, int d, bool pass2) {
+  size_t f = static_cast<size_t>(NR) * d + static_cast<size_t>(d) * (kTT + 1);
+  if (pass2) f += 16 * kTT + 2 * NR;
+  return f * sizeof(float);
+}
+
+// ------------------------------------------------------------------ select
+constexpr int kSelThreads = 1024;
+
+// Order-preserving map of fp32 to uint32 (larger float -> larger key).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// pooled keys: grid (ceil(T/256), B*Hkv)
+__global__ void pool_kernel(const float* __restrict__ score, int T, int pool, uint32_t* __restrict__ keys) {
+  const int bh = blockIdx.y;
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  const int r = pool / 2;
+  const float* s = score + static_cast<size_t>(bh) * T;
+  float m = -INFINITY;
+  const int lo = max(0, t - r), hi = min(T - 1, t + r);
+  for (int u = lo; u <= hi; ++u) m = fmaxf(m, s[u]);
+  keys[static_cast<size_t>(bh) * T + t] = float_key(m);
+}
+
+// Block-wide exclusive scan of one int per thread (kSelThreads threads).
+__device__ int block_exclusive_scan(int v, int* tmp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) tmp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < kSelThreads / 32) ? tmp[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    tmp[lane] = w;                      // inclusive per warp
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? tmp[warp - 1] : 0) + x - v;
+  if (total) *total = tmp[kSelThreads / 32 - 1];
+  __syncthreads();
+  return before;
+}
+
+// One CTA per (b, h): radix-select the n_top-th largest key among candidates
+// [0, cand), then emit, in index order, keys above it plus the lowest-index
+// keys equal to it, then the keep_last tail tokens.
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const uint32_t* __restrict__ keys_all, int T,
+                                                             int keep, int keep_last,
+                                                             int32_t* __restrict__ idx) {
+  __shared__ int hist[256];
+  __shared__ int tmp[32];
+  __shared__ uint32_t prefix_s;
+  __shared__ int remain_s;
+  const int bh = blockIdx.x;
+  const uint32_t* keys = keys_all + static_cast<size_t>(bh) * T;
+  const int cand = T - keep_last;
+  const int n_top = keep - keep_last;
+  int32_t* out = idx + static_cast<size_t>(bh) * keep;
+  uint32_t prefix = 0, mask = 0;
+  int remain = n_top;                    // rank (1-based) still to find inside the prefix
+  if (n_top > 0) {
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+      __syncthreads();
+      for (int t = threadIdx.x; t < cand; t += blockDim.x) {
+        const uint32_t k = keys[t];
+        if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int acc = 0, bin = 255;
+        for (; bin >= 0; --bin) {
+          if (acc + hist[bin] >= remain) break;
+          acc += hist[bin];
+        }
+        prefix_s = prefix | (static_cast<uint32_t>(bin) << shift);
+        remain_s = remain - acc;
+      }
+      __syncthreads();
+      prefix = prefix_s;
+      remain = remain_s;
+      mask |= 255u << shift;
+      __syncthreads();
+    }
+  }
+  const uint32_t thr = prefix;           // the n_top-th largest key
+  const int need_eq = remain;            // how many keys == thr to take (lowest index first)
+  // contiguous chunk per thread, in index order
+  const int per = (cand + kSelThreads - 1) / kSelThreads;
+  const int lo = min(cand, threadIdx.x * per), hi = min(cand, lo + per);
+  int n_eq = 0;
+  if (n_top > 0)
+    for (int t = lo; t < hi; ++t) n_eq += (keys[t] == thr);
+  const int eq_before = block_exclusive_scan(n_eq, tmp, nullptr);
+  int n_sel = 0;
+  if (n_top > 0) {
+    int e = eq_before;
+    for (int t = lo; t < hi; ++t) {
+      const uint32_t k = keys[t];
+      const bool sel = k > thr || (k == thr && e < need_eq);
+      e += (k == thr);
+      n_sel += sel;
+    }
+  }
+  int total = 0;
+  int pos = block_exclusive_scan(n_sel, tmp, &total);
+  if (n_top > 0) {
+    int e = eq_before;
+    for (int t = lo; t < hi; ++t) {
+      const uint32_t k = keys[t];
+      const bool sel = k > thr || (k == thr && e < need_eq);
+      e += (k == thr);
+      if (sel) out[pos++] = t;
+    }
+  }
+  for (int j = threadIdx.x; j < keep_last; j += blockDim.x) out[n_top + j] = cand + j;
+}
+
+// ------------------------------------------------------------------ gather
+__global__ void gather_kernel(const int32_t* __restrict__ idx, int T, int keep, int d,
+                              const uint16_t* __restrict__ K, const uint16_t* __restrict__ V,
+                              uint16_t* __restrict__ Ko, uint16_t* __restrict__ Vo) {
+  const int bh = blockIdx.y;
+  const int vec = d / 8;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= keep * vec) return;
+  const int j = i / vec, v = i % vec;
+  const int t = idx[static_cast<size_t>(bh) * keep + j];
+  const size_t o = (static_cast<size_t>(bh) * keep + j) * d + v * 8;
+  if (t < 0 || t >= T) {
+    atomicOr(&g_quant_status, VC_DEV_BAD_INDEX);
+    *reinterpret_cast<uint4*>(Ko + o) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(Vo + o) = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const size_t s = (static_cast<size_t>(bh) * T + t) * d + v * 8;
+  *reinterpret_cast<uint4*>(Ko + o) = *reinterpret_cast<const uint4*>(K + s);
+  *reinterpret_cast<uint4*>(Vo + o) = *reinterpret_cast<const uint4*>(V + s);
+}
+
+vc_status_t check_shape(const vc_shape_t* s, bool need_bits) {
+  VC_REQUIRE(s != nullptr, "shape is NULL");
+  VC_REQUIRE(s->B >= 1 && s->Hkv >= 1, "need B >= 1 and Hkv >= 1");
+  if (s->d != 64 && s->d != 128) VC_FAIL(VC_ERR_UNSUPPORTED, "head dim %d not in {64, 128}", s->d);
+  if (need_bits && s->bits != 2 && s->bits != 4) VC_FAIL(VC_ERR_UNSUPPORTED, "bits %d not in {2, 4}", s->bits);
+  return VC_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" vc_status_t vc_quant_packed_bytes(const vc_shape_t* s, int32_t T_cap, size_t* kc_bytes,
+                                             size_t* ksz_bytes, size_t* vc_bytes, size_t* vsz_bytes) {
+  vc_status_t st = check_shape(s, true);
+  if (st != VC_OK) return st;
+  VC_REQUIRE(T_cap >= 0 && T_cap % kGroup == 0, "T_cap must be a non-negative multiple of 32 (got %d)", T_cap);
+  const size_t tok = static_cast<size_t>(s->B) * s->Hkv * T_cap;
+  if (kc_bytes) *kc_bytes = tok * s->d * s->bits / 8;
+  if (vc_bytes) *vc_bytes = tok * s->d * s->bits / 8;
+  if (ksz_bytes) *ksz_bytes = tok / kGroup * s->d * 4;
+  if (vsz_bytes) *vsz_bytes = tok * (s->d / kGroup) * 4;
+  return VC_OK;
+}
+
+extern "C" vc_status_t vc_quant_kv_pack(const vc_shape_t* s, int32_t T, int32_t T_cap, const uint16_t* K,
+                                        const uint16_t* V, uint32_t* kc, uint16_t* ksz, uint32_t* vc,
+                                        uint16_t* vsz, vc_stream_t stream) {
+  vc_status_t st = check_shape(s, true);
+  if (st != VC_OK) return st;
+  VC_REQUIRE(T >= 0 && T % kGroup == 0 && T <= T_cap && T_cap % kGroup == 0,
+             "need 0 <= T <= T_cap, both multiples of 32 (T=%d, T_cap=%d)", T, T_cap);
+  VC_REQUIRE(K && V && kc && ksz && vc && vsz, "NULL pointer");
+  VC_REQUIRE(vc_aligned16(K) && vc_aligned16(V) && vc_aligned16(kc) && vc_aligned16(ksz) && vc_aligned16(vc) &&
+                 vc_aligned16(vsz), "pointers must be 16-byte aligned");
+  if (T == 0) return VC_OK;
+  VC_REQUIRE(static_cast<int64_t>(s->B) * s->Hkv <= 65535, "B*Hkv <= 65535");
+  dim3 grid(T / kGroup, s->B * s->Hkv);
+  Packed p{kc, ksz, vc, vsz};
+  const size_t sm = pack_smem(s->d);
+  auto cs = reinterpret_cast<cudaStream_t>(stream);
+  if (s->bits == 2)
+    pack_kernel<2><<<grid, kPackThreads, sm, cs>>>(K, V, T, T_cap, s->d, p);
+  else
+    pack_kernel<4><<<grid, kPackThreads, sm, cs>>>(K, V, T, T_cap, s->d, p);
+  VC_LAUNCH_CHECK("pack_kernel");
+  return VC_OK;
+}
+
+extern "C" vc_status_t vc_quant_kv_unpack(const vc_shape_t* s, int32_t T, int32_t T_cap, const uint32_t* kc,
+                                          const uint16_t* ksz, const uint32_t* vc, const uint16_t* vsz,
+                                          float* K_hat, float* V_hat, vc_stream_t stream) {
+  vc_status_t st = check_shape(s, true);
+  if (st != VC_OK) return st;
+  VC_REQUIRE(T >= 0 && T % kGroup == 0 && T <= T_cap && T_cap % kGroup == 0, "bad T / T_cap");
+  VC_REQUIRE(kc && ksz && vc && vsz && K_hat && V_hat, "NULL pointer");
+  if (T == 0) return VC_OK;
+  dim3 grid(T / kGroup, s->B * s->Hkv);
+  Packed p{const_cast<uint32_t*>(kc), const_cast<uint16_t*>(ksz), const_cast<uint32_t*>(vc),
+           const_cast<uint16_t*>(vsz)};
+  auto cs = reinterpret_cast<cudaStream_t>(stream);
+  if (s->bits == 2)
+    unpack_kernel<2><<<grid, 256, 0, cs>>>(T, T_cap, s->d, p, K_hat, V_hat);
+  else
+    unpack_kernel<4><<<grid, 256, 0, cs>>>(T, T_cap, s->d, p, K_hat, V_hat);
+  VC_LAUNCH_CHECK("unpack_kernel");
+  return VC_OK;
+}
+
+extern "C" vc_status_t vc_quant_kv_append(const vc_shape_t* s, const uint16_t* k_new, const uint16_t* v_new,
+                                          const int32_t* n_acc, uint16_t* tail_k, uint16_t* tail_v,
+                                          int32_t* tail_len, int32_t tail_cap, uint32_t* kc, uint16_t* ksz,
+                                          uint32_t* vc, uint16_t* vsz, int32_t* packed_len, int32_t T_cap,
+                                          vc_stream_t stream) {
+  vc_status_t st = check_shape(s, true);
+  if (st != VC_OK) return st;
+  VC_REQUIRE(s->k >= 0, "k >= 0");
+  VC_REQUIRE(tail_cap >= s->k + 1 && T_cap % kGroup == 0 && T_cap >= 0, "tail_cap >= k+1 and T_cap % 32 == 0");
+  VC_REQUIRE(k_new && v_new && tail_k && tail_v && tail_len && kc && ksz && vc && vsz && packed_len, "NULL pointer");
+  VC_REQUIRE(vc_aligned16(k_new) && vc_aligned16(v_new) && vc_aligned16(tail_k) && vc_aligned16(tail_v),
+             "bf16 pointers must be 16-byte aligned");
+  Packed p{kc, ksz, vc, vsz};
+  const size_t sm = pack_smem(s->d);
+  auto cs = reinterpret_cast<cudaStream_t>(stream);
+  if (s->bits == 2)
+    append_kernel<2><<<s->B, kPackThreads, sm, cs>>>(k_new, v_new, n_acc, s->k, s->Hkv, s->d, tail_k, tail_v,
+                                                      tail_len, tail_cap, p, packed_len, T_cap);
+  else
+    append_kernel<4><<<s->B, kPackThreads, sm, cs>>>(k_new, v_new, n_acc, s->k, s->Hkv, s->d, tail_k, tail_v,
+                                                      tail_len, tail_cap, p, packed_len, T_cap);
+  VC_LAUNCH_CHECK("append_kernel");
+  return VC_OK;
+}
+
+namespace {
+int score_ranges(int T) { return (T + kTT * kTilesPerRange - 1) / (kTT * kTilesPerRange); }
+
+vc_status_t check_score(const vc_shape_t* s, int T, int n_obs, int* NR) {
+  vc_status_t st = check_shape(s, false);
+  if (st != VC_OK) return st;
+  VC_REQUIRE(s->Hq >= 1 && s->Hq % s->Hkv == 0, "Hq must be a multiple of Hkv");
+  const int G = s->Hq / s->Hkv;
+  if (G > 8) VC_FAIL(VC_ERR_UNSUPPORTED, "G = %d > 8", G);
+  VC_REQUIRE(n_obs >= 1 && n_obs <= 32 && T >= n_obs, "need 1 <= n_obs <= 32 and T >= n_obs");
+  *NR = G * n_obs;
+  if (*NR % 16 != 0) VC_FAIL(VC_ERR_UNSUPPORTED, "G * n_obs = %d must be a multiple of 16", *NR);
+  return VC_OK;
+}
+}  // namespace
+
+extern "C" vc_status_t vc_token_score_workspace_size(const vc_shape_t* s, int32_t T, int32_t n_obs, size_t* bytes) {
+  int NR = 0;
+  vc_status_t st = check_score(s, T, n_obs, &NR);
+  if (st != VC_OK) return st;
+  VC_REQUIRE(bytes, "bytes is NULL");
+  *bytes = static_cast<size_t>(s->B) * s->Hkv * score_ranges(T) * NR * sizeof(float2);
+  return VC_OK;
+}
+
+extern "C" vc_status_t vc_token_score(const vc_shape_t* s, int32_t T, int32_t n_obs, const uint16_t* q_obs,
+                                      const uint16_t* K, float* score, void* workspace, size_t workspace_bytes,
+                                      vc_stream_t stream) {
+  int NR = 0;
+  vc_status_t st = check_score(s, T, n_obs, &NR);
+  if (st != VC_OK) return st;
+  VC_REQUIRE(q_obs && K && score, "NULL pointer");
+  size_t need = 0;
+  vc_token_score_workspace_size(s, T, n_obs, &need);
+  if (!workspace || workspace_bytes < need)
+    VC_FAIL(VC_ERR_WORKSPACE, "score workspace needs %zu bytes (got %zu)", need, workspace_bytes);
+  ScoreArgs a;
+  a.q = q_obs; a.K = K; a.T = T; a.n_obs = n_obs; a.Hq = s->Hq; a.Hkv = s->Hkv; a.d = s->d;
+  a.scale_log2 = s->softmax_scale * 1.4426950408889634f;
+  a.stats = static_cast<float2*>(workspace);
+  a.n_ranges = score_ranges(T);
+  a.score = score;
+  const int RPT = NR / 16;
+  auto cs = reinterpret_cast<cudaStream_t>(stream);
+  dim3 g1(a.n_ranges, s->B * s->Hkv), g2((T + kTT - 1) / kTT, s->B * s->Hkv);
+  const size_t sm1 = score_smem(NR, s->d, false), sm2 = score_smem(NR, s->d, true);
+#define VC_SCORE_CASE(R)                                                                          \
+  case R:                                                                                         \
+    cudaFuncSetAttribute(score_pass1<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1);  \
+    cudaFuncSetAttribute(score_pass2<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);  \
+    score_pass1<R><<<g1, kScoreThreads, sm1, cs>>>(a);                                            \
+    score_pass2<R><<<g2, kScoreThreads, sm2, cs>>>(a);                                            \
+    break;
+  switch (RPT) {
+    VC_SCORE_CASE(1)
+    VC_SCORE_CASE(2)
+    VC_SCORE_CASE(4)
+    VC_SCORE_CASE(6)
+    VC_SCORE_CASE(8)
+    VC_SCORE_CASE(10)
+    VC_SCORE_CASE(12)
+    VC_SCORE_CASE(14)
+    VC_SCORE_CASE(16)
+    default:
+      VC_FAIL(VC_ERR_UNSUPPORTED, "G * n_obs = %d not built (need 16 * {1,2,4,6,...,16})", NR);
+  }
+#undef VC_SCORE_CASE
+  VC_LAUNCH_CHECK("token score");
+  return VC_OK;
+}
+
+extern "C" vc_status_t vc_token_select_workspace_size(int32_t B, int32_t Hkv, int32_t T, size_t* bytes) {
+  VC_REQUIRE(B >= 1 && Hkv >= 1 && T >= 1 && bytes, "bad arguments");
+  *bytes = static_cast<size_t>(B) * Hkv * T * sizeof(uint32_t);
+  return VC_OK;
+}
+
+extern "C" vc_status_t vc_token_select(int32_t B, int32_t Hkv, int32_t T, const float* score, int32_t keep,
+                                       int32_t keep_last, int32_t pool, int32_t* idx, void* workspace,
+                                       size_t workspace_bytes, vc_stream_t stream) {
+  VC_REQUIRE(B >= 1 && Hkv >= 1 && T >= 1, "need B, Hkv, T >= 1");
+  VC_REQUIRE(keep_last >= 0 && keep_last <= keep && keep <= T, "need 0 <= keep_last <= keep <= T");
+  VC_REQUIRE(pool >= 1 && pool <= 15 && (pool & 1), "pool must be odd, 1..15");
+  VC_REQUIRE(score && idx, "NULL pointer");
+  const size_t need = static_cast<size_t>(B) * Hkv * T * sizeof(uint32_t);
+  if (!workspace || workspace_bytes < need)
+    VC_FAIL(VC_ERR_WORKSPACE, "select workspace needs %zu bytes (got %zu)", need, workspace_bytes);
+  auto cs = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t* keys = static_cast<uint32_t*>(workspace);
+  pool_kernel<<<dim3((T + 255) / 256, B * Hkv), 256, 0, cs>>>(score, T, pool, keys);
+  VC_LAUNCH_CHECK("pool_kernel");
+  select_kernel<<<B * Hkv, kSelThreads, 0, cs>>>(keys, T, keep, keep_last, idx);
+  VC_LAUNCH_CHECK("select_kernel");
+  return VC_OK;
+}
+
+extern "C" vc_status_t vc_gather_kv(const vc_shape_t* s, int32_t T, int32_t keep, const int32_t* idx,
+                                    const uint16_t* K, const uint16_t* V, uint16_t* K_out, uint16_t* V_out,
+                                    vc_stream_t stream) {
+  vc_status_t st = check_shape(s, false);
+  if (st != VC_OK) return st;
+  VC_REQUIRE(T >= 1 && keep >= 0, "need T >= 1, keep >= 0");
+  VC_REQUIRE(idx && K && V && K_out && V_out, "NULL pointer");
+  VC_REQUIRE(vc_aligned16(K) && vc_aligned16(V) && vc_aligned16(K_out) && vc_aligned16(V_out),
+             "pointers must be 16-byte aligned");
+  if (keep == 0) return VC_OK;
+  const int vec = s->d / 8;
+  dim3 grid((keep * vec + 255) / 256, s->B * s->Hkv);
+  gather_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(idx, T, keep, s->d, K, V, K_out, V_out);
+  VC_LAUNCH_CHECK("gather_kernel");
+  return VC_OK;
+}
+
+extern "C" vc_status_t vc_quant_kv_device_status(uint32_t* status) {
+  VC_REQUIRE(status, "status is NULL");
+  VC_CUDA_CHECK(cudaDeviceSynchronize());
+  uint32_t v = 0, zero = 0;
+  VC_CUDA_CHECK(cudaMemcpyFromSymbol(&v, g_quant_status, sizeof(v)));
+  VC_CUDA_CHECK(cudaMemcpyToSymbol(g_quant_status, &zero, sizeof(zero)));
+  *status = v;
+  return VC_OK;
+}
