@@ -1,0 +1,588 @@
+"""Benchmark of the draft -> verify -> accept round on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mistral|qwen|llama|stagger|tiny]
+                    [--impl ours|reference] [--schedule staggered|lockstep]
+
+One step = one decode round of the whole hot path on one batch of synthetic
+inputs: k draft steps over the packed cache (every layer), the full KV of every
+layer streamed host->device in chunks (overlapped with drafting), verify
+attention, accept, and the commit of the accepted tokens to the full-KV store
+and the draft cache (with packing of full tail groups).  Per-round inputs
+(queries, the new tokens' K/V, logits) are device-resident for ``value`` and
+copied from pinned host memory inside the timed region for ``e2e``.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead (the reference arm).
+Under torchrun each rank runs an independent replica (no data-path
+collective); value = total over ranks, timed as max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified tokens/s/layer"
+PCIE_GEN5_GBS = 64.0
+L2_BYTES = 129 * 2 ** 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d.get("hbm_gbs", 6800.0), "bf16_tflops": d.get("bf16_tflops", 1900.0),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", 1700.0),
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks sampler
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- inputs
+def make_round_inputs(w, rnd, group, device, layers):
+    import numpy as np
+    import torch
+
+    import synth
+    from verify_compressed_kv_gb300.runtime import RoundInputs
+
+    def t(a, dt=None):
+        a = np.ascontiguousarray(a)
+        v = {np.dtype(np.uint16): np.int16}.get(a.dtype, a.dtype)
+        return torch.from_numpy(a.view(v))
+
+    qd = np.stack([np.stack([synth.draft_q(w, rnd, i, l, group) for i in range(w.k)]) for l in range(layers)])
+    kc = [[synth.draft_kv_cur(w, rnd, i, l, group) for i in range(w.k)] for l in range(layers)]
+    kvc = np.stack([np.stack([np.stack([kc[l][i][j] for i in range(w.k)]) for l in range(layers)]) for j in range(2)])
+    qv = np.stack([synth.verify_q(w, rnd, l, group) for l in range(layers)])
+    kn = [synth.kv_new(w, rnd, l, group) for l in range(layers)]
+    kvn = np.stack([np.stack([kn[l][j] for l in range(layers)]) for j in range(2)])
+    logits, drafts, _ = synth.logits_and_drafts(w, rnd, group)
+    host = RoundInputs(t(qd), t(kvc), t(qv), t(kvn), t(logits), t(drafts))
+    return host
+
+
+def to_device(inp, device, pinned=False):
+    from verify_compressed_kv_gb300.runtime import RoundInputs
+    f = (lambda x: x.pin_memory()) if pinned else (lambda x: x.to(device))
+    return RoundInputs(*[f(getattr(inp, n)) for n in ("q_draft", "kv_cur", "q_verify", "kv_new", "logits", "drafts")])
+
+
+def copy_inputs(dst, src, stream):
+    import torch
+    with torch.cuda.stream(stream):
+        for n in ("q_draft", "kv_cur", "q_verify", "kv_new", "logits", "drafts"):
+            getattr(dst, n).copy_(getattr(src, n), non_blocking=True)
+
+
+def input_bytes(inp):
+    return sum(getattr(inp, n).numel() * getattr(inp, n).element_size()
+               for n in ("q_draft", "kv_cur", "q_verify", "kv_new", "logits", "drafts"))
+
+
+def build_group(w, layers, device, rounds_total, n_slots, group_index=0):
+    import numpy as np
+    import torch
+
+    import synth
+    from verify_compressed_kv_gb300.runtime import Group
+
+    from verify_compressed_kv_gb300 import _lib as vc
+
+    drop = w.keep_frac < 1.0
+    g = Group(w.B, w.Hq, w.Hkv, w.d, w.k, w.bits, w.V, w.C, w.T, layers=layers,
+              extra_tokens=(rounds_total + 2) * (w.k + 1), n_slots=n_slots, softmax_scale=1.0, device=device,
+              packed_T0=w.T_keep if drop else None)
+    for l in range(layers):
+        K, V = synth.kv(w, layer=l, group=group_index, threads=16)
+        Kd = torch.from_numpy(K.view(np.int16)).to(device)
+        Vd = torch.from_numpy(V.view(np.int16)).to(device)
+        if not drop:
+            g.load_prefix(l, Kd, Vd)
+        else:
+            # token dropping (score -> select -> gather), then 4-bit packing of the kept tokens
+            keep = w.T_keep
+            qo = torch.from_numpy(synth.q_obs(w, group=group_index).view(np.int16)).to(device)
+            score = torch.empty((w.B, w.Hkv, w.T), dtype=torch.float32, device=device)
+            wsb = vc.vc_token_score_workspace_size(g.shape, w.T, 32)
+            ws = torch.empty(wsb, dtype=torch.uint8, device=device)
+            vc.vc_token_score(g.shape, w.T, 32, qo, Kd, score, ws, wsb)
+            wsb2 = vc.vc_token_select_workspace_size(w.B, w.Hkv, w.T)
+            ws2 = torch.empty(wsb2, dtype=torch.uint8, device=device)
+            idx = torch.empty((w.B, w.Hkv, keep), dtype=torch.int32, device=device)
+            vc.vc_token_select(w.B, w.Hkv, w.T, score, keep, 32, 7, idx, ws2, wsb2)
+            Kk = torch.empty((w.B, w.Hkv, keep, w.d), dtype=torch.int16, device=device)
+            Vk = torch.empty_like(Kk)
+            vc.vc_gather_kv(g.shape, w.T, keep, idx, Kd, Vd, Kk, Vk)
+            g.load_packed_only(l, Kk, Vk)
+            g.write_store(l, Kd, Vd)
+            del Kk, Vk, score, ws, ws2
+        del Kd, Vd
+    torch.cuda.synchronize()
+    return g
+
+
+# ---------------------------------------------------------------- our arm
+def algorithmic_draft_bytes(w, P):
+    """Bytes one draft call must move: packed K/V codes + metadata of P tokens per
+    (request, KV head), plus q in and o out (the bf16 tail is < 1%: ignored)."""
+    per_tok = 2 * w.d * w.bits // 8 + 2 * (w.d // 32) * 4
+    return w.B * w.Hkv * P * per_tok + 2 * w.B * w.Hq * w.d * 2
+
+
+def source_hash(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel_file, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel (else None)."""
+    prof = os.path.join(ROOT, "profiles", f"draft_attn_{workload}.md")
+    if not os.path.exists(prof):
+        return None
+    kv = {}
+    for line in open(prof):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("source_sha256_16") != source_hash(kernel_file):
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import synth
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    from verify_compressed_kv_gb300 import runtime as rt
+
+    w = synth.get(args.workload)
+    layers = w.layers
+    n_groups = w.groups
+    rounds_total = args.warmup + args.steps + 1
+    n_inp = min(3, rounds_total)
+    n_slots = args.slots
+    cs = torch.cuda.Stream(device)
+    xs = torch.cuda.Stream(device)
+    groups = [build_group(w, layers, device, rounds_total, n_slots, gi) for gi in range(n_groups)]
+    host_inputs = [[make_round_inputs(w, r, gi, device, layers) for r in range(n_inp)] for gi in range(n_groups)]
+    dev_inputs = [[to_device(x, device) for x in hi] for hi in host_inputs]
+    pin_inputs = [[to_device(x, device, pinned=True) for x in hi] for hi in host_inputs]
+    # device buffers the e2e leg copies into every round
+    e2e_bufs = [to_device(hi[0], device) for hi in host_inputs]
+    torch.cuda.synchronize()
+
+    # ---- prefill rows timed once: quantise + pack of the full prefix (layer 0)
+    K0, V0 = synth.kv(w, layer=0, group=0, threads=16)
+    K0d = torch.from_numpy(K0.view(np.int16)).to(device)
+    V0d = torch.from_numpy(V0.view(np.int16)).to(device)
+    from verify_compressed_kv_gb300 import _lib as vc
+    g0 = groups[0]
+    sb = vc.vc_quant_packed_bytes(g0.shape, w.T)         # scratch packed arrays for the timing
+    scratch = [torch.empty(n, dtype=torch.uint8, device=device) for n in sb]
+    for _ in range(3):
+        vc.vc_quant_kv_pack(g0.shape, w.T, w.T, K0d, V0d, *scratch, cs)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cs)
+    for _ in range(5):
+        vc.vc_quant_kv_pack(g0.shape, w.T, w.T, K0d, V0d, *scratch, cs)
+    e1.record(cs)
+    e1.synchronize()
+    pack_ms = e0.elapsed_time(e1) / 5
+    pack_bytes = 2 * w.B * w.Hkv * w.T * w.d * 2 + sum(sb)
+    del K0d, V0d, scratch
+    torch.cuda.synchronize()
+
+    state = {"round": 0}
+
+    def one_round(e2e=False, timeline=None):
+        r = state["round"]
+        state["round"] += 1
+        if n_groups == 1:
+            g = groups[0]
+            inp = dev_inputs[0][r % n_inp]
+            if e2e:
+                copy_inputs(e2e_bufs[0], pin_inputs[0][r % n_inp], cs)
+                inp = e2e_bufs[0]
+            tl = rt.round_single(g, inp, cs, xs, timeline)
+            return tl, [g]
+        X, Y = (groups[0], groups[1]) if r % 2 == 0 else (groups[1], groups[0])
+        ix = 0 if r % 2 == 0 else 1
+        iy = 1 - ix
+        inp_x = dev_inputs[ix][r % n_inp]
+        inp_y = dev_inputs[iy][r % n_inp]
+        if e2e:
+            copy_inputs(e2e_bufs[ix], pin_inputs[ix][r % n_inp], cs)
+            copy_inputs(e2e_bufs[iy], pin_inputs[iy][r % n_inp], cs)
+            inp_x, inp_y = e2e_bufs[ix], e2e_bufs[iy]
+        if args.schedule == "lockstep":
+            tl = rt.round_lockstep([X, Y], [inp_x, inp_y], cs, xs, timeline)
+            return tl, [X, Y]
+        tl = rt.round_staggered(X, Y, inp_x, inp_y, cs, xs, timeline)
+        return tl, [Y]
+
+    def finish(tl, done):
+        tl.ev["end"].synchronize()
+        return sum(g.after_round() for g in done)
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        tl, done = one_round()
+        finish(tl, done)
+    torch.cuda.synchronize()
+
+    # ---- timed region (device-resident per-round inputs)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    launches0 = sum(g.launches for g in groups)
+    clocks = Clocks(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(cs)
+    tokens = 0
+    tls = []
+    h2d_bytes = 0
+    for _ in range(args.steps):
+        h2d_bytes += sum(g.h2d_bytes() for g in (groups if (n_groups == 1 or args.schedule == "lockstep")
+                                                 else [groups[1] if state["round"] % 2 == 0 else groups[0]]))
+        tl, done = one_round()
+        tokens += finish(tl, done)
+        tls.append(tl)
+    t_end.record(cs)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    dist_barrier(world)
+    launches = sum(g.launches for g in groups) - launches0
+    total_ms = t_start.elapsed_time(t_end)
+    layer_tokens = tokens * layers
+    value_local = layer_tokens / (total_ms / 1e3)
+
+    # per-round breakdown from the timelines
+    def med(xs_):
+        return statistics.median(xs_) if xs_ else None
+    draft_span = [tl.ms("draft_start", "draft_end") for tl in tls]
+    copy_span = [tl.ms("copy_start", "copy_end") for tl in tls]
+    overlap = []
+    for tl in tls:
+        a0, a1 = tl.ms("start", "draft_start"), tl.ms("start", "draft_end")
+        b0, b1 = tl.ms("start", "copy_start"), tl.ms("start", "copy_end")
+        inter = max(0.0, min(a1, b1) - max(a0, b0))
+        overlap.append(inter / max(1e-9, b1 - b0))
+    round_ms = [tl.ms("start", "end") for tl in tls]
+
+    # ---- the draft call alone, timed on its stream (CUDA events, L2 > inputs)
+    g = groups[0]
+    inp = dev_inputs[0][0]
+    n_draft = 20
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for i in range(3):
+        g.draft_step(inp, 0, 0, cs)
+    ev[0].record(cs)
+    for i in range(n_draft):
+        g.draft_step(inp, 0, 0, cs)
+    ev[1].record(cs)
+    ev[1].synchronize()
+    draft_call_ms = ev[0].elapsed_time(ev[1]) / n_draft
+    P = int(g.packed_len[0].max().item())
+    alg_bytes = algorithmic_draft_bytes(w, P)
+    peaks = load_peaks()
+    achieved_gbs = alg_bytes / (draft_call_ms / 1e3) / 1e9
+    # inside the timed rounds: average draft call = draft span / (k * layers)
+    draft_in_round_ms = med(draft_span) / (w.k * layers)
+
+    # ---- e2e: same rounds, inputs copied from pinned host memory every round, result read back
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    e2e_tokens = 0
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(cs)
+    for _ in range(args.steps):
+        tl, done = one_round(e2e=True)
+        e2e_tokens += finish(tl, done)
+    s1.record(cs)
+    torch.cuda.synchronize()
+    e2e_ms = s0.elapsed_time(s1)
+    e2e_local = e2e_tokens * layers / (e2e_ms / 1e3)
+    per_round_in = input_bytes(pin_inputs[0][0]) * (2 if n_groups > 1 else 1)
+    per_round_out = 4 * w.B
+
+    # ---- reduce over ranks (replicas): value = sum, time = max
+    value, e2e_value, t_max = value_local, e2e_local, total_ms
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([value_local, e2e_local, total_ms], dtype=torch.float64)
+        vals = [torch.zeros(3, dtype=torch.float64) for _ in range(world)]
+        dist.all_gather(vals, tt)
+        t_max = max(float(v[2]) for v in vals)
+        # whole-job throughput: all ranks' tokens over the slowest rank's time
+        value = sum(float(v[0]) * float(v[2]) for v in vals) / t_max
+        e2e_value = sum(float(v[1]) for v in vals)
+
+    draft_src = os.path.join(ROOT, "verify_compressed_kv_gb300", "csrc", "vc_draft_attn.cu")
+    traffic = ncu_traffic(draft_src, args.workload)
+    link_peak = args.link_peak_gbs
+    h2d_rate = (h2d_bytes / args.steps) / (med(copy_span) / 1e3) / 1e9 if copy_span else None
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s/layer",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t_max / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16/int%d->f32" % w.bits,
+        "data": "synthetic (seeded; shapes and distributions of the workload; no weights)",
+        "config": {"workload": workload_name(w), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "T": w.T,
+                   "k": w.k, "bits": w.bits, "layers": layers, "groups": n_groups, "V": w.V, "chunk": w.C,
+                   "schedule": "single" if n_groups == 1 else args.schedule, "slots": n_slots,
+                   "l2": "inputs larger than L2 (packed cache %d MiB, full KV %d MiB per round)" % (
+                       alg_bytes // 2 ** 20, g.h2d_bytes() // 2 ** 20),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "e2e": {"value": e2e_value, "unit": "tokens/s/layer", "h2d_bytes_per_step": per_round_in,
+                "d2h_bytes_per_step": per_round_out},
+        "gpu_launches": launches,
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "vc_draft_attn (split-KV + tail + combine), alone on its stream",
+                     "bytes_per_launch": alg_bytes, "ms_per_launch": draft_call_ms,
+                     "ms_per_launch_in_round": draft_in_round_ms, "peak_source": peaks["source"]},
+        "h2d": {"gbs": h2d_rate, "bytes_per_round": h2d_bytes / args.steps, "copy_ms": med(copy_span),
+                "frac_of_measured_link": (h2d_rate / link_peak) if h2d_rate else None,
+                "measured_link_gbs": link_peak, "frac_of_pcie_gen5_64": (h2d_rate / PCIE_GEN5_GBS) if h2d_rate else None,
+                "overlap_with_draft": med(overlap)},
+        "round_ms": {"median": med(round_ms), "draft": med(draft_span), "copy": med(copy_span)},
+        "prefill_pack": {"ms": pack_ms, "gbs": pack_bytes / (pack_ms / 1e3) / 1e9},
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.workload)
+    for gg in groups:
+        gg.close()
+    return out
+
+
+def workload_name(w):
+    names = {"tiny": "tiny 1x(Hq4,Hkv1,d64) T512 k4 int4",
+             "mistral": "Mistral-24B-shaped layer: B8 Hq32 Hkv8 d128 T32768 k16 int2",
+             "qwen": "Qwen-32B-shaped layer: B16 Hq40 Hkv8 d128 T65536 (keep 25%) k32 int4",
+             "llama": "Llama-70B-shaped 8 layers: B4 Hq64 Hkv8 d128 T131072 k32 int2",
+             "stagger": "staggered mix: 2x B32 Hq32 Hkv8 d128 T32768 k24 int2"}
+    return names.get(w.name, w.name)
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+ORACLE_SAMPLE = r"""
+import json, sys, time, os
+sys.path.insert(0, {root!r})
+import numpy as np
+import synth
+from oracle import kivi, attention, accept
+w = synth.get({wl!r})
+b = 0
+# one request (all its KV heads), one round: k draft steps, verify, accept
+Ks, Vs = [], []
+T = w.T_keep if w.name == 'qwen' else w.T
+for h in range(w.Hkv):
+    k_, v_ = synth.kv_slice(w, b, h, T=T)
+    Ks.append(k_); Vs.append(v_)
+K = np.stack(Ks)[None]; V = np.stack(Vs)[None]
+t0 = time.perf_counter()
+packed = kivi.quant_pack(K, V, w.bits)
+t_pack = time.perf_counter() - t0
+tail = np.zeros((1, w.Hkv, 32 + w.k + 1, w.d), np.uint16)
+t0 = time.perf_counter()
+for i in range({steps}):
+    q = synth.draft_q(w, 0, i)[b:b+1]
+    kc, vc_ = synth.draft_kv_cur(w, 0, i)
+    attention.draft_attention(q, *packed, [T], tail, tail, [0], w.bits, 1.0, k_cur=kc[b:b+1], v_cur=vc_[b:b+1], step=i)
+t_draft = (time.perf_counter() - t0) * w.k / {steps}
+qv = synth.verify_q(w, 0)[b:b+1]
+kn, vn = synth.kv_new(w, 0)
+t0 = time.perf_counter()
+attention.verify_attention(qv, K, V, kn[b:b+1], vn[b:b+1], [T], 1.0)
+t_verify = time.perf_counter() - t0
+logits, drafts, L = synth.logits_and_drafts(w, 0)
+t0 = time.perf_counter()
+n, nxt, _ = accept.accept(logits[b:b+1], drafts[b:b+1])
+t_accept = time.perf_counter() - t0
+tokens = (int(n[0]) + 1) * w.layers
+t_round = (t_draft + t_verify + t_accept) * w.layers
+print(json.dumps(dict(t_round=t_round, tokens=tokens, t_pack=t_pack, t_draft=t_draft, t_verify=t_verify,
+                      t_accept=t_accept, draft_steps_run={steps})))
+"""
+
+
+def cpu_baseline(workload, steps=None):
+    """Time the oracle, as it stands, on one request of one round (all its KV
+    heads; 1 BLAS thread) and scale to the metric's unit."""
+    import synth
+    w = synth.get(workload)
+    steps = steps if steps is not None else (2 if w.T * w.layers > 100000 else 4)
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ORACLE_SAMPLE.format(root=ROOT, wl=workload, steps=steps)
+    t0 = time.time()
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        return {"value": None, "unit": "tokens/s/layer", "cores": 1, "kind": "oracle",
+                "sample": "failed: " + r.stderr[-300:]}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    # the whole batch = B requests, each processed like the sampled one
+    value = d["tokens"] / d["t_round"]        # tokens/s/layer for one request at a time on 1 core
+    return {"value": value, "unit": "tokens/s/layer", "cores": 1, "kind": "oracle",
+            "sample": (f"request 0 of round 0, all {w.Hkv} KV heads: {d['draft_steps_run']} of {w.k} draft steps "
+                       f"timed and scaled to {w.k}, one verify pass over T={w.T if w.name != 'qwen' else w.T_keep}, "
+                       f"accept; {w.layers} layer(s) by scaling; 1 thread"),
+            "seconds": {k: d[k] for k in ("t_round", "t_pack", "t_draft", "t_verify", "t_accept")},
+            "wall_s": time.time() - t0}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import synth
+    w = synth.get(args.workload)
+    vals = []
+    cb = None
+    t_all = time.time()
+    for _ in range(args.warmup):
+        pass                     # the oracle has no warm state to build
+    for s in range(args.steps):
+        cb = cpu_baseline(args.workload, steps=1)
+        if cb["value"] is None:
+            break
+        vals.append(cb["value"])
+    v = statistics.median(vals) if vals else None
+    wall = time.time() - t_all
+    out = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s/layer", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall * 1e3 / max(1, args.steps),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+           "data": "synthetic (seeded)",
+           "config": {"workload": workload_name(w), "B": w.B, "T": w.T, "k": w.k, "bits": w.bits,
+                      "layers": w.layers, "groups": w.groups},
+           "cpu_baseline": {"value": v, "unit": "tokens/s/layer", "cores": 1, "kind": "oracle",
+                            "sample": (cb or {}).get("sample")},
+           "e2e": {"value": v, "unit": "tokens/s/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    return out
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    return rank, world, local
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="mistral", choices=["tiny", "mistral", "qwen", "llama", "stagger"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--schedule", default="staggered", choices=["staggered", "lockstep"])
+    ap.add_argument("--slots", type=int, default=4)
+    ap.add_argument("--link-peak-gbs", type=float, default=211.0,
+                    help="measured pinned host->device copy peak of the box (GB/s)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_ours(args, rank, world, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

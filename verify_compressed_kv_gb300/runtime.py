@@ -1,0 +1,284 @@
+"""Device-side state of a request group and the round driver.
+
+VeriCache (gist.science/paper/2605.17613), Technical Summary:
+  * Core Algorithm: draft k tokens with the compressed KV, verify them with
+    one pass over the full KV, accept up to the first mismatch (+ the full-KV
+    token there), repeat from the last accepted token;
+  * Key System Innovations (1), cross-resource staggering: drafting uses HBM,
+    verification uses the CPU-GPU link; staggering request groups overlaps
+    the two instead of running them in lock-step;
+  * Architecture Support: compressed KV in GPU memory, full KV in CPU memory.
+
+Everything here is orchestration: buffers, streams, events and calls into the
+C ABI (``_lib``).  Every step of the path runs in the CUDA libraries.
+
+A ``Group`` is one batch of requests with L attention layers.  Per layer it
+owns the packed draft cache, the bf16 tail, the pinned chunk-major full-KV
+store and the per-request lengths; the group shares a verify slot ring and
+workspaces across layers.  Model work outside attention (projections,
+sampling) is not part of this path: a round takes its queries, the new
+tokens' K/V and the verify logits as inputs (``RoundInputs``).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+from . import _lib as vc
+
+GROUP = 32
+
+
+def _i16(shape, device):
+    return torch.empty(shape, dtype=torch.int16, device=device)
+
+
+@dataclasses.dataclass
+class RoundInputs:
+    """Per-round device inputs of one group (bf16 tensors are int16 bit views).
+
+    q_draft [L, k, B, Hq, d], kv_cur [2, L, k, B, Hkv, d], q_verify [L, B, k+1, Hq, d],
+    kv_new [2, L, B, k+1, Hkv, d], logits fp32 [B, k+1, V], drafts int32 [B, k].
+    """
+    q_draft: torch.Tensor
+    kv_cur: torch.Tensor
+    q_verify: torch.Tensor
+    kv_new: torch.Tensor
+    logits: torch.Tensor
+    drafts: torch.Tensor
+
+
+class Group:
+    def __init__(self, B, Hq, Hkv, d, k, bits, V, C, T0, layers=1, extra_tokens=None, n_slots=4,
+                 parts_per_chunk=1, softmax_scale=1.0, device="cuda", packed_T0=None):
+        self.B, self.Hq, self.Hkv, self.d, self.k, self.bits, self.V = B, Hq, Hkv, d, k, bits, V
+        self.C, self.L = C, layers
+        self.device = torch.device(device)
+        self.shape = vc.shape(B, Hq, Hkv, d, k=k, bits=bits, softmax_scale=softmax_scale)
+        extra = extra_tokens if extra_tokens is not None else 64 * (k + 1)
+        self.T_cap = int(math.ceil((T0 + extra) / C) * C)          # host store capacity (tokens)
+        self.P0 = T0 if packed_T0 is None else packed_T0             # tokens in the draft cache at start
+        self.P_cap = int(math.ceil((self.P0 + extra) / GROUP) * GROUP)
+        self.tail_cap = GROUP + k + 1
+        self.parts = parts_per_chunk
+        dev = self.device
+        # ---- draft caches, one per layer
+        kcb, kszb, vcb, vszb = vc.vc_quant_packed_bytes(self.shape, self.P_cap)
+        self.kc = [torch.zeros(kcb // 4, dtype=torch.int32, device=dev) for _ in range(layers)]
+        self.ksz = [torch.zeros(kszb // 2, dtype=torch.int16, device=dev) for _ in range(layers)]
+        self.vc = [torch.zeros(vcb // 4, dtype=torch.int32, device=dev) for _ in range(layers)]
+        self.vsz = [torch.zeros(vszb // 2, dtype=torch.int16, device=dev) for _ in range(layers)]
+        self.tail_k = [torch.zeros((B, Hkv, self.tail_cap, d), dtype=torch.int16, device=dev) for _ in range(layers)]
+        self.tail_v = [torch.zeros((B, Hkv, self.tail_cap, d), dtype=torch.int16, device=dev) for _ in range(layers)]
+        self.packed_len = [torch.zeros(B, dtype=torch.int32, device=dev) for _ in range(layers)]
+        self.tail_len = [torch.zeros(B, dtype=torch.int32, device=dev) for _ in range(layers)]
+        # ---- full KV: pinned, chunk-major, one store per layer
+        self.n_chunks_cap = self.T_cap // C
+        self.chunk_elems = 2 * B * Hkv * C * d
+        self.host_kv = [torch.empty(self.n_chunks_cap * self.chunk_elems, dtype=torch.int16, pin_memory=True)
+                        for _ in range(layers)]
+        self.prefix_len = [torch.zeros(B, dtype=torch.int32, device=dev) for _ in range(layers)]
+        self.max_prefix = 0          # host-side bound of prefix_len (exact: read back every round)
+        # ---- verify ring + workspaces
+        self.n_slots = n_slots
+        self.slots = _i16(n_slots * self.chunk_elems, dev)
+        self.ws_verify_bytes = vc.vc_verify_attn_workspace_size(self.shape, self.parts)
+        self.ws_verify = torch.zeros(self.ws_verify_bytes, dtype=torch.uint8, device=dev)
+        self.ws_draft_bytes = vc.vc_draft_attn_workspace_size(self.shape, self.P_cap)
+        self.ws_draft = torch.zeros(self.ws_draft_bytes, dtype=torch.uint8, device=dev)
+        self.ws_accept_bytes = vc.vc_accept_workspace_size(B, k, V)
+        self.ws_accept = torch.zeros(self.ws_accept_bytes, dtype=torch.uint8, device=dev)
+        # one ring for all layers: its per-slot events order slot reuse across layers too
+        self.pipe = vc.vc_verify_pipeline_create(n_slots)
+        self.launches = 0                      # kernels launched through this group
+        # ---- per-round outputs
+        self.draft_out = _i16((B, Hq, d), dev)
+        self.verify_out = _i16((B, k + 1, Hq, d), dev)
+        self.n_acc = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.next_tok = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.n_acc_host = torch.zeros(B, dtype=torch.int32, pin_memory=True)
+
+    def close(self):
+        if self.pipe:
+            vc.vc_verify_pipeline_destroy(self.pipe)
+        self.pipe = None
+
+    # ---------------------------------------------------------------- prefill
+    def load_prefix(self, layer, K, V, stream=None):
+        """Prefix K/V of a layer, bf16 [B, Hkv, T0, d] int16 tensors on the device:
+        quantise + pack into the draft cache and copy into the pinned store."""
+        T0 = K.shape[2]
+        assert T0 % GROUP == 0 and T0 <= self.P_cap
+        vc.vc_quant_kv_pack(self.shape, T0, self.P_cap, K, V, self.kc[layer], self.ksz[layer], self.vc[layer],
+                            self.vsz[layer], stream)
+        self.packed_len[layer].fill_(T0)
+        self.tail_len[layer].zero_()
+        self.write_store(layer, K, V)
+        self.prefix_len[layer].fill_(T0)
+        self.max_prefix = T0
+
+    def load_packed_only(self, layer, K, V, stream=None):
+        """Draft cache from an already-compressed (e.g. token-dropped) prefix."""
+        T = K.shape[2]
+        vc.vc_quant_kv_pack(self.shape, T, self.P_cap, K, V, self.kc[layer], self.ksz[layer], self.vc[layer],
+                            self.vsz[layer], stream)
+        self.packed_len[layer].fill_(T)
+        self.tail_len[layer].zero_()
+
+    def write_store(self, layer, K, V):
+        """Full prefix K/V [B, Hkv, T, d] (device or host) -> pinned chunk-major store."""
+        T = K.shape[2]
+        st = self.host_kv[layer].view(self.n_chunks_cap, 2, self.B, self.Hkv, self.C, self.d)
+        for c in range((T + self.C - 1) // self.C):
+            n = min(self.C, T - c * self.C)
+            st[c, 0, :, :, :n].copy_(K[:, :, c * self.C:c * self.C + n])
+            st[c, 1, :, :, :n].copy_(V[:, :, c * self.C:c * self.C + n])
+        self.prefix_len[layer].fill_(T)
+        self.max_prefix = T
+
+    # ---------------------------------------------------------------- the round's steps
+    def prefetch(self, layer, copy_stream):
+        vc.vc_verify_prefetch(self.pipe, self.shape, self.host_kv[layer], self.C, self.max_prefix,
+                              self.slots, copy_stream)
+
+    def draft_step(self, inp: RoundInputs, layer: int, step: int, stream):
+        vc.vc_draft_attn(self.shape, inp.q_draft[layer, step], inp.kv_cur[0, layer, step], inp.kv_cur[1, layer, step],
+                         self.kc[layer], self.ksz[layer], self.vc[layer], self.vsz[layer], self.packed_len[layer],
+                         self.P_cap, self.P_cap, self.tail_k[layer], self.tail_v[layer], self.tail_len[layer],
+                         self.tail_cap, step, self.draft_out, self.ws_draft, self.ws_draft_bytes, stream)
+        self.launches += 3                     # split-KV, tail, combine
+
+    def verify(self, inp: RoundInputs, layer: int, compute_stream, copy_stream):
+        vc.vc_verify_attn_streamed(self.pipe, self.shape, inp.q_verify[layer], self.host_kv[layer], self.C,
+                                   self.max_prefix, self.prefix_len[layer], self.slots, inp.kv_new[0, layer],
+                                   inp.kv_new[1, layer], self.verify_out, self.parts, self.ws_verify,
+                                   self.ws_verify_bytes, compute_stream, copy_stream)
+        self.launches += self.chunks() + 1     # one kernel per chunk, then the new-token block + merge
+
+    def accept(self, inp: RoundInputs, stream):
+        vc.vc_accept(self.B, self.k, self.V, inp.logits, inp.drafts, self.n_acc, self.next_tok, None,
+                     self.ws_accept, self.ws_accept_bytes, stream)
+        self.launches += 1
+
+    def commit(self, inp: RoundInputs, stream):
+        for l in range(self.L):
+            vc.vc_verify_commit(self.shape, inp.kv_new[0, l], inp.kv_new[1, l], self.n_acc, self.prefix_len[l],
+                                self.host_kv[l], self.C, self.T_cap, stream)
+            vc.vc_quant_kv_append(self.shape, inp.kv_new[0, l], inp.kv_new[1, l], self.n_acc, self.tail_k[l],
+                                  self.tail_v[l], self.tail_len[l], self.tail_cap, self.kc[l], self.ksz[l],
+                                  self.vc[l], self.vsz[l], self.packed_len[l], self.P_cap, stream)
+            self.launches += 2
+
+    def chunks(self):
+        return (self.max_prefix + self.C - 1) // self.C
+
+    def h2d_bytes(self):
+        """Full-KV bytes one verify pass moves over the link (all layers)."""
+        return self.L * 2 * self.B * self.Hkv * self.max_prefix * self.d * 2
+
+    def read_back(self, stream):
+        """Device -> host copy of the accepted lengths (the round's result)."""
+        with torch.cuda.stream(stream):
+            self.n_acc_host.copy_(self.n_acc, non_blocking=True)
+
+    def after_round(self):
+        """Host bookkeeping once the read-back has landed."""
+        n = self.n_acc_host
+        self.max_prefix += int(n.max()) + 1
+        return int(n.sum()) + self.B          # tokens produced this round
+
+
+class Timeline:
+    """CUDA events (with timing) recorded on the streams of one round."""
+
+    def __init__(self):
+        self.ev = {}
+
+    def mark(self, name, stream):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        self.ev[name] = e
+        return e
+
+    def ms(self, a, b):
+        return self.ev[a].elapsed_time(self.ev[b])
+
+
+def round_single(g: Group, inp: RoundInputs, cs, xs, tl: Timeline | None = None):
+    """One round of one group: the full KV of layer 0 starts streaming while the
+    group drafts (prefix chunks do not depend on the drafts), then verify,
+    accept, commit.  Returns nothing; call g.after_round() after syncing."""
+    tl = tl or Timeline()
+    tl.mark("start", cs)
+    xs.wait_event(tl.ev["start"])
+    tl.mark("copy_start", xs)
+    g.prefetch(0, xs)
+    tl.mark("draft_start", cs)
+    for i in range(g.k):
+        for l in range(g.L):
+            g.draft_step(inp, l, i, cs)
+    tl.mark("draft_end", cs)
+    for l in range(g.L):
+        g.verify(inp, l, cs, xs)
+    tl.mark("copy_end", xs)
+    tl.mark("verify_end", cs)
+    g.accept(inp, cs)
+    g.commit(inp, cs)
+    cs.wait_event(tl.ev["copy_end"])
+    g.read_back(cs)
+    tl.mark("end", cs)
+    return tl
+
+
+def round_staggered(X: Group, Y: Group, inp_x: RoundInputs, inp_y: RoundInputs, cs, xs, tl: Timeline | None = None):
+    """Cross-resource staggering: X drafts (HBM) while Y's full KV streams over
+    the link and Y verifies, accepts and commits.  Roles swap every round."""
+    tl = tl or Timeline()
+    tl.mark("start", cs)
+    xs.wait_event(tl.ev["start"])
+    tl.mark("copy_start", xs)
+    Y.prefetch(0, xs)
+    tl.mark("draft_start", cs)
+    for i in range(X.k):
+        for l in range(X.L):
+            X.draft_step(inp_x, l, i, cs)
+    tl.mark("draft_end", cs)
+    for l in range(Y.L):
+        Y.verify(inp_y, l, cs, xs)
+    tl.mark("copy_end", xs)
+    tl.mark("verify_end", cs)
+    Y.accept(inp_y, cs)
+    Y.commit(inp_y, cs)
+    cs.wait_event(tl.ev["copy_end"])
+    Y.read_back(cs)
+    tl.mark("end", cs)
+    return tl
+
+
+def round_lockstep(groups, inps, cs, xs, tl: Timeline | None = None):
+    """The comparison schedule: every group drafts, then every group verifies;
+    no transfer starts before drafting ends."""
+    tl = tl or Timeline()
+    tl.mark("start", cs)
+    tl.mark("draft_start", cs)
+    for g, inp in zip(groups, inps):
+        for i in range(g.k):
+            for l in range(g.L):
+                g.draft_step(inp, l, i, cs)
+    tl.mark("draft_end", cs)
+    xs.wait_event(tl.ev["draft_end"])
+    tl.mark("copy_start", xs)
+    for g, inp in zip(groups, inps):
+        for l in range(g.L):
+            g.verify(inp, l, cs, xs)
+        g.accept(inp, cs)
+        g.commit(inp, cs)
+    tl.mark("copy_end", xs)
+    tl.mark("verify_end", cs)
+    cs.wait_event(tl.ev["copy_end"])
+    for g in groups:
+        g.read_back(cs)
+    tl.mark("end", cs)
+    return tl
