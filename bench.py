@@ -565,7 +565,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="mistral", choices=["tiny", "mistral", "qwen", "llama", "stagger"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--schedule", default="staggered", choices=["staggered", "lockstep"])
-    ap.add_argument("--slots", type=int, default=4)
+    ap.add_argument("--slots", type=int, default=8)
     ap.add_argument("--link-peak-gbs", type=float, default=211.0,
                     help="measured pinned host->device copy peak of the box (GB/s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -186,7 +186,14 @@ vc_status_t vc_quant_kv_device_status(uint32_t* status);
  * current token is not added and the tail is not written.
  * q bf16 [B, Hq, d] -> out bf16 [B, Hq, d].  packed_len, tail_len: int32 [B]
  * device.  max_packed: an upper bound of packed_len over the batch (host).
- * Split-KV over 32-token groups, log-sum-exp combine, fp32 accumulation.
+ * One launch: the packed groups of all (request, KV head) slices are split
+ * evenly over a persistent grid sized to the current device (stream-K), the
+ * partials are merged with a log-sum-exp rule by the last CTA of each slice.
+ * fp32 accumulation.  The workspace holds the partials and one arrival
+ * counter per slice: it must be zero-filled before its first use, and every
+ * call leaves the counters at zero again.  Its size depends on the device
+ * (SM count, occupancy): query it with the same device current.  Calls that
+ * share a workspace must not overlap on the GPU.
  * Reads B, Hq, Hkv, d, bits, softmax_scale. */
 vc_status_t vc_draft_attn_workspace_size(const vc_shape_t* s, int32_t max_packed, size_t* bytes);
 vc_status_t vc_draft_attn(const vc_shape_t* s, const uint16_t* q, const uint16_t* k_cur,

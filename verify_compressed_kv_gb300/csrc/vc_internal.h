@@ -97,6 +97,11 @@ __device__ __forceinline__ bool vc_mbar_wait_bounded(uint64_t* bar, uint32_t par
   }
   return true;
 }
+// Order this thread's earlier generic-proxy shared-memory accesses before its
+// later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void vc_fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 // Bulk (non-tensor) async copy global -> this CTA's shared memory; completion
 // is signalled on `bar` as transaction bytes.  dst, src 16-byte aligned,
 // bytes a multiple of 16.
