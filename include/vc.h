@@ -291,6 +291,28 @@ vc_status_t vc_accept(int32_t B, int32_t k, int32_t V, const float* logits, cons
                       int32_t* n_acc, int32_t* next_tok, int32_t* argmax, void* workspace,
                       size_t workspace_bytes, vc_stream_t stream);
 
+/* vc_accept without a workspace argument and without any allocation.  The
+ * paper has no counterpart: this exists for callers that cannot allocate
+ * device memory, such as a plugin that a serving framework gives only its
+ * input and output buffers (the framework owns all device memory), or a
+ * latency-critical loop where cudaMalloc, which may synchronise the device,
+ * is not allowed.  Same inputs, outputs and results as vc_accept.
+ *
+ * Scratch lives in a fixed 64 KiB array in the library's device memory, which
+ * every GPU that loads libvc_accept.so holds until the process exits.  Limits:
+ * B <= 4096 and B*(k+1)*S <= 6144, S = splits per row = min(ceil(1216 /
+ * (B*(k+1))), ceil(V / 2048)), at least 1 (e.g. B=8, k=16, V=32768 uses
+ * 1224); larger calls return VC_ERR_CAPACITY with the reason.  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress) for
+ * that device: make that first call before any stream capture.  Each call
+ * zeroes the counters it needs on the stream before its kernel.  All calls
+ * share the one array: calls that overlap on the GPU (other streams, other
+ * host threads) race and return wrong results.  No cudaMalloc / cudaFree or
+ * allocating library routine is called. */
+vc_status_t vc_accept_noalloc(int32_t B, int32_t k, int32_t V, const float* logits,
+                              const int32_t* draft, int32_t* n_acc, int32_t* next_tok,
+                              int32_t* argmax, vc_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -92,6 +92,7 @@ _SIGS = {
     "vc_accept": {
         "vc_accept_workspace_size": [I32, I32, I32, POINTER(c_size_t)],
         "vc_accept": [I32, I32, I32, P, P, P, P, P, P, SZ, P],
+        "vc_accept_noalloc": [I32, I32, I32, P, P, P, P, P, P],
     },
 }
 
@@ -287,3 +288,8 @@ def vc_accept_workspace_size(B, k, V):
 def vc_accept(B, k, V, logits, draft, n_acc, next_tok, argmax, ws, ws_bytes, stream=None):
     _call("vc_accept", B, k, V, _ptr(logits), _ptr(draft), _ptr(n_acc), _ptr(next_tok), _ptr(argmax),
           _ptr(ws), ws_bytes, _stream(stream))
+
+
+def vc_accept_noalloc(B, k, V, logits, draft, n_acc, next_tok, argmax, stream=None):
+    _call("vc_accept_noalloc", B, k, V, _ptr(logits), _ptr(draft), _ptr(n_acc), _ptr(next_tok), _ptr(argmax),
+          _stream(stream))

@@ -13,6 +13,7 @@
 // folds the partials in split order, so ties resolve to the lowest index,
 // and writes n_acc / next_tok / argmax.  HBM-bound: B*(k+1)*V*4 bytes read.
 #include <cfloat>
+#include <mutex>
 
 #include "vc_internal.h"
 
@@ -186,5 +187,83 @@ extern "C" vc_status_t vc_accept(int32_t B, int32_t k, int32_t V, const float* l
   accept_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       logits, draft, k, V, S, part_v, part_i, counter, n_acc, next_tok, argmax);
   VC_LAUNCH_CHECK("accept_kernel");
+  return VC_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.
+//
+// Some callers of this library cannot allocate device memory at all: a plugin
+// that a serving framework hands only its input and output buffers (the
+// framework owns every byte of device memory and its budget), or a
+// latency-critical loop where a cudaMalloc (which may synchronise the device)
+// is not allowed.  For them vc_accept_noalloc keeps its scratch (the per-split
+// partial maxima and the per-request arrival counters) in a fixed array that
+// lives in the library's own device memory, loaded with the library.
+//
+// Limits: B * (k + 1) * S <= kNoAllocParts partials, where S is the number of
+// splits per row (see accept_splits), and B <= kNoAllocRequests.  Every GPU
+// that loads this library holds the 64 KiB array until the process exits.
+// All calls share the array: two calls that overlap on the GPU (different
+// streams, or different threads) race and give wrong results.
+namespace {
+constexpr int kNoAllocParts = 6144;
+constexpr int kNoAllocRequests = 4096;
+struct NoAllocScratch {
+  float part_v[kNoAllocParts];
+  int part_i[kNoAllocParts];
+  unsigned int counter[kNoAllocRequests];
+};
+static __device__ __align__(256) NoAllocScratch g_accept_scratch;
+
+// Device address of g_accept_scratch for each device, looked up on first use.
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+vc_status_t scratch_address(NoAllocScratch** out) {
+  int dev = 0;
+  VC_CUDA_CHECK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) VC_FAIL(VC_ERR_UNSUPPORTED, "device index %d >= %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_accept_scratch);
+    if (e != cudaSuccess) VC_FAIL(VC_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    g_scratch_addr[dev] = p;
+  }
+  *out = static_cast<NoAllocScratch*>(g_scratch_addr[dev]);
+  return VC_OK;
+}
+}  // namespace
+
+extern "C" vc_status_t vc_accept_noalloc(int32_t B, int32_t k, int32_t V, const float* logits,
+                                         const int32_t* draft, int32_t* n_acc, int32_t* next_tok,
+                                         int32_t* argmax, vc_stream_t stream) {
+  VC_REQUIRE(B >= 1 && k >= 0 && V >= 1, "need B >= 1, k >= 0, V >= 1 (got %d, %d, %d)", B, k, V);
+  VC_REQUIRE(k + 1 <= 64, "k + 1 <= 64 rows per request (got k = %d)", k);
+  VC_REQUIRE(logits && n_acc && next_tok, "logits, n_acc and next_tok must not be NULL");
+  VC_REQUIRE(k == 0 || draft, "draft must not be NULL when k > 0");
+  VC_REQUIRE(vc_aligned16(logits), "logits must be 16-byte aligned");
+  const int rows = B * (k + 1);
+  const int S = accept_splits(rows, V);
+  if (B > kNoAllocRequests)
+    VC_FAIL(VC_ERR_CAPACITY, "vc_accept_noalloc: B = %d exceeds the fixed scratch limit of %d requests", B,
+            kNoAllocRequests);
+  if (static_cast<int64_t>(rows) * S > kNoAllocParts)
+    VC_FAIL(VC_ERR_CAPACITY,
+            "vc_accept_noalloc: B*(k+1)*splits = %d*%d exceeds the fixed scratch limit of %d partials "
+            "(use vc_accept with a caller-provided workspace)",
+            rows, S, kNoAllocParts);
+  NoAllocScratch* sp = nullptr;
+  vc_status_t st = scratch_address(&sp);
+  if (st != VC_OK) return st;
+  auto cs = reinterpret_cast<cudaStream_t>(stream);
+  // the arrival counters must start at zero for every call
+  VC_CUDA_CHECK(cudaMemsetAsync(sp->counter, 0, sizeof(unsigned int) * B, cs));
+  dim3 grid(S, rows);
+  accept_kernel<<<grid, kThreads, 0, cs>>>(logits, draft, k, V, S, sp->part_v, sp->part_i, sp->counter, n_acc,
+                                           next_tok, argmax);
+  VC_LAUNCH_CHECK("accept_kernel (no-alloc)");
   return VC_OK;
 }
