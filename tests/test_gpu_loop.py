@@ -1,0 +1,133 @@
+"""The lossless invariant on the GPU (VeriCache, Technical Summary, Experimental
+Results, Correctness: outputs identical to full-KV decoding under greedy).
+
+A tiny random-init 2-layer decoder (Hq=4, Hkv=1, d=64, vocab 1024) runs the
+draft/verify/accept loop through the C ABI (drafting over the packed cache,
+verification over the full KV streamed from pinned host memory, accept,
+commit) and must reproduce, token for token, plain greedy decoding through
+the same verify kernel with k = 0, for every compressor (int4, int2, token
+drop + int4) and for drafters of any quality.  The GPU greedy stream is also
+compared with the oracle's fp64 greedy stream; a difference there is allowed
+only at a numeric near-tie of the oracle's logits.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.loop as oloop
+from tiny_model import TinyDecoder
+
+pytestmark = pytest.mark.gpu
+
+PROMPT_LEN = 512
+N_NEW = 256
+K_DRAFT = 4
+
+
+@pytest.fixture(scope="module")
+def setup():
+    from verify_compressed_kv_gb300.loop import GpuSpeculativeDecoder
+    m = TinyDecoder()
+    prompt = np.random.default_rng(11).integers(0, m.vocab, PROMPT_LEN)
+    store = oloop.FullKV(m.n_layers)
+    qs = [None] * m.n_layers
+    full = oloop.full_attention_fn(store, m.scale)
+
+    def prefill_attend(layer, q, k, v):
+        qs[layer] = q
+        return full(layer, q, k, v)
+
+    logits, ks, vs = m.forward(prompt, np.arange(PROMPT_LEN), prefill_attend)
+    K = [np.ascontiguousarray(ks[l].transpose(1, 0, 2)) for l in range(m.n_layers)]
+    V = [np.ascontiguousarray(vs[l].transpose(1, 0, 2)) for l in range(m.n_layers)]
+    first = int(np.argmax(logits[-1]))
+
+    def make(bits):
+        return GpuSpeculativeDecoder(m.n_layers, m.Hq, m.Hkv, m.d, m.vocab, K_DRAFT, bits, m.scale, C=128,
+                                     max_tokens=PROMPT_LEN + N_NEW + 64)
+
+    g = make(4)
+    g.load_prompt(K, V)
+    ref = g.greedy(m, first, PROMPT_LEN, N_NEW)
+    g.close()
+    return dict(m=m, K=K, V=V, qs=qs, first=first, ref=ref, make=make, prompt=prompt)
+
+
+def token_drop_on_gpu(s, K, V, qs, m):
+    """Score / select / gather on the GPU: keep T/4 tokens incl. the last 32."""
+    from verify_compressed_kv_gb300 import _lib as vc
+    dK, dV = [], []
+    T = K[0].shape[1]
+    keep = T // 4
+    sh = vc.shape(1, m.Hq, m.Hkv, m.d, softmax_scale=m.scale)
+    for l in range(m.n_layers):
+        Kd = torch.from_numpy(K[l][None].view(np.int16)).cuda()
+        Vd = torch.from_numpy(V[l][None].view(np.int16)).cuda()
+        qo = np.ascontiguousarray(qs[l][-32:].transpose(1, 0, 2)[None])             # [1, Hq, 32, d]
+        score = torch.empty((1, m.Hkv, T), dtype=torch.float32, device="cuda")
+        wsb = vc.vc_token_score_workspace_size(sh, T, 32)
+        ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+        vc.vc_token_score(sh, T, 32, torch.from_numpy(qo.view(np.int16)).cuda(), Kd, score, ws, wsb)
+        wsb2 = vc.vc_token_select_workspace_size(1, m.Hkv, T)
+        ws2 = torch.zeros(wsb2, dtype=torch.uint8, device="cuda")
+        idx = torch.empty((1, m.Hkv, keep), dtype=torch.int32, device="cuda")
+        vc.vc_token_select(1, m.Hkv, T, score, keep, 32, 7, idx, ws2, wsb2)
+        Ko = torch.empty((1, m.Hkv, keep, m.d), dtype=torch.int16, device="cuda")
+        Vo = torch.empty_like(Ko)
+        vc.vc_gather_kv(sh, T, keep, idx, Kd, Vd, Ko, Vo)
+        dK.append(Ko[0].cpu().numpy().view(np.uint16))
+        dV.append(Vo[0].cpu().numpy().view(np.uint16))
+    return dK, dV
+
+
+@pytest.mark.parametrize("bits,drop", [(4, False), (2, False), (4, True)], ids=["int4", "int2", "drop+int4"])
+def test_lossless_with_compressed_drafter(setup, bits, drop):
+    S = setup
+    dec = S["make"](bits)
+    try:
+        if drop:
+            dK, dV = token_drop_on_gpu(dec.sh, S["K"], S["V"], S["qs"], S["m"])
+            dec.load_prompt(S["K"], S["V"], dK, dV)
+        else:
+            dec.load_prompt(S["K"], S["V"])
+        out, acc = dec.generate(S["m"], S["first"], PROMPT_LEN, N_NEW)
+    finally:
+        dec.close()
+    assert out == S["ref"], f"diverged at {next(i for i, (a, b) in enumerate(zip(out, S['ref'])) if a != b)}"
+    # drafting from the compressed cache does accept tokens: fewer rounds than tokens
+    assert len(acc) < N_NEW and np.mean(acc) > 0.5
+
+
+@pytest.mark.parametrize("drafter", ["wrong", "perfect", "random"])
+def test_lossless_with_any_drafter(setup, drafter):
+    S = setup
+    dec = S["make"](4)
+    try:
+        dec.load_prompt(S["K"], S["V"])
+        out, acc = dec.generate(S["m"], S["first"], PROMPT_LEN, N_NEW, drafter=drafter, reference=S["ref"],
+                                rng=np.random.default_rng(3))
+    finally:
+        dec.close()
+    assert out == S["ref"]
+    if drafter == "wrong":
+        assert all(a == 0 for a in acc)
+    if drafter == "perfect":
+        assert all(a == K_DRAFT for a in acc[:-1])
+
+
+def test_gpu_greedy_matches_oracle_greedy(setup):
+    """GPU (fp32 accumulate, bf16 attention output) vs oracle (fp64): equal up to
+    a numeric near-tie of the oracle's top-2 logits at the first difference."""
+    S = setup
+    m = S["m"]
+    ref_cpu = oloop.greedy_decode(m, S["prompt"], 64, m.scale)
+    gpu = S["ref"][:64]
+    if gpu != ref_cpu:
+        i = next(i for i, (a, b) in enumerate(zip(gpu, ref_cpu)) if a != b)
+        # margin of the oracle's logits at step i
+        store = oloop.FullKV(m.n_layers)
+        full = oloop.full_attention_fn(store, m.scale)
+        toks = list(S["prompt"]) + ref_cpu[:i]
+        lg, _, _ = m.forward(np.asarray(toks), np.arange(len(toks)), full)
+        top = np.sort(lg[-1])[-2:]
+        assert top[1] - top[0] < 1e-2, f"diverged at {i} with oracle margin {top[1] - top[0]}"
