@@ -275,18 +275,34 @@ def run_ours(args, rank, world, local_rank):
                 inp = e2e_bufs[0]
             tl = rt.round_single(g, inp, cs, xs, timeline)
             return tl, [g]
-        X, Y = (groups[0], groups[1]) if r % 2 == 0 else (groups[1], groups[0])
-        ix = 0 if r % 2 == 0 else 1
-        iy = 1 - ix
-        inp_x = dev_inputs[ix][r % n_inp]
-        inp_y = dev_inputs[iy][r % n_inp]
-        if e2e:
-            copy_inputs(e2e_bufs[ix], pin_inputs[ix][r % n_inp], cs)
-            copy_inputs(e2e_bufs[iy], pin_inputs[iy][r % n_inp], cs)
-            inp_x, inp_y = e2e_bufs[ix], e2e_bufs[iy]
         if args.schedule == "lockstep":
-            tl = rt.round_lockstep([X, Y], [inp_x, inp_y], cs, xs, timeline)
-            return tl, [X, Y]
+            # every group drafts cycle r, then every group verifies it
+            inps = [dev_inputs[gi][r % n_inp] for gi in range(2)]
+            if e2e:
+                for gi in range(2):
+                    copy_inputs(e2e_bufs[gi], pin_inputs[gi][r % n_inp], cs)
+                inps = e2e_bufs
+            tl = rt.round_lockstep(groups, inps, cs, xs, timeline)
+            return tl, list(groups)
+        # staggered: round r, group r % 2 drafts its cycle r // 2 while the other
+        # group verifies its cycle (r - 1) // 2; round 0 is the prologue (draft only)
+        ix, iy = r % 2, (r + 1) % 2
+        X, Y = groups[ix], groups[iy]
+        dc, vcyc = r // 2, (r - 1) // 2
+        inp_x = dev_inputs[ix][dc % n_inp]
+        if r == 0:
+            tl = rt.Timeline()
+            tl.mark("start", cs)
+            for i in range(X.k):
+                for l in range(X.L):
+                    X.draft_step(inp_x, l, i, cs)
+            tl.mark("end", cs)
+            return tl, []
+        inp_y = dev_inputs[iy][vcyc % n_inp]
+        if e2e:
+            copy_inputs(e2e_bufs[ix], pin_inputs[ix][dc % n_inp], cs)
+            copy_inputs(e2e_bufs[iy], pin_inputs[iy][vcyc % n_inp], cs)
+            inp_x, inp_y = e2e_bufs[ix], e2e_bufs[iy]
         tl = rt.round_staggered(X, Y, inp_x, inp_y, cs, xs, timeline)
         return tl, [Y]
 
