@@ -394,16 +394,7 @@ def run_ours(args, rank, world, local_rank):
     per_round_out = 4 * w.B
 
     # ---- reduce over ranks (replicas): value = sum, time = max
-    value, e2e_value, t_max = value_local, e2e_local, total_ms
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([value_local, e2e_local, total_ms], dtype=torch.float64)
-        vals = [torch.zeros(3, dtype=torch.float64) for _ in range(world)]
-        dist.all_gather(vals, tt)
-        t_max = max(float(v[2]) for v in vals)
-        # whole-job throughput: all ranks' tokens over the slowest rank's time
-        value = sum(float(v[0]) * float(v[2]) for v in vals) / t_max
-        e2e_value = sum(float(v[1]) for v in vals)
+    value, e2e_value, t_max = reduce_over_ranks(value_local, e2e_local, total_ms, world)
 
     draft_src = os.path.join(ROOT, "verify_compressed_kv_gb300", "csrc", "vc_draft_attn.cu")
     traffic = ncu_traffic(draft_src, args.workload)
@@ -440,7 +431,9 @@ def run_ours(args, rank, world, local_rank):
                 "frac_of_measured_link": (h2d_rate / link_peak) if h2d_rate else None,
                 "measured_link_gbs": link_peak, "frac_of_pcie_gen5_64": (h2d_rate / PCIE_GEN5_GBS) if h2d_rate else None,
                 "overlap_with_draft": med(overlap)},
-        "round_ms": {"median": med(round_ms), "draft": med(draft_span), "copy": med(copy_span)},
+        "round_ms": {"median": med(round_ms), "draft": med(draft_span), "copy": med(copy_span),
+                     "all": [round(x, 3) for x in round_ms],
+                     "host_gap_total": round(total_ms - sum(round_ms), 3)},
         "prefill_pack": {"ms": pack_ms, "gbs": pack_bytes / (pack_ms / 1e3) / 1e9},
         "clocks": clk,
     }
@@ -565,6 +558,28 @@ def dist_setup():
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         dist.init_process_group("gloo", rank=rank, world_size=world)
     return rank, world, local
+
+
+def combine_rank_results(rows):
+    """rows = [(value, e2e, timed_ms)] per rank -> (whole-job value, e2e, max ms).
+
+    Replicas: every rank processed its own requests in its timed region, so
+    the job's throughput is all ranks' tokens (value * ms) over the slowest
+    rank's time; e2e throughputs add up."""
+    t_max = max(r[2] for r in rows)
+    value = sum(r[0] * r[2] for r in rows) / t_max
+    return value, sum(r[1] for r in rows), t_max
+
+
+def reduce_over_ranks(value_local, e2e_local, ms_local, world):
+    if world <= 1:
+        return value_local, e2e_local, ms_local
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([value_local, e2e_local, ms_local], dtype=torch.float64)
+    vals = [torch.zeros(3, dtype=torch.float64) for _ in range(world)]
+    dist.all_gather(vals, tt)
+    return combine_rank_results([(float(v[0]), float(v[1]), float(v[2])) for v in vals])
 
 
 def dist_barrier(world):

@@ -165,22 +165,24 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const uint16_t* __re
 
 size_t pack_smem(int d) { return 2 * kGroup * (d + 2) * sizeof(uint16_t) + kGroup * (d + 4); }
 
-// One CTA per request: append rows 0..n of k_new/v_new to the tail, then pack
-// whole groups from the tail's front (all KV heads of the request).
+// The commit of one request's accepted tokens for one KV head (grid (Hkv, B)):
+// append rows 0..n of k_new/v_new to the tail, pack whole groups from the
+// tail's front, shift the rest down.  Lengths are read here and written by
+// append_lengths_kernel afterwards, so no CTA sees another's update.
 template <int BITS>
 __global__ void __launch_bounds__(kPackThreads) append_kernel(
     const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
     const int32_t* __restrict__ n_acc, int k, int Hkv, int d, uint16_t* tail_k, uint16_t* tail_v,
-    int32_t* tail_len, int tail_cap, Packed p, int32_t* packed_len, int T_cap) {
+    const int32_t* tail_len, int tail_cap, Packed p, const int32_t* packed_len, int T_cap) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int ld = d + 2;
   uint16_t* k_s = reinterpret_cast<uint16_t*>(smem);
   uint16_t* v_s = k_s + kGroup * ld;
   uint8_t* codes_s = reinterpret_cast<uint8_t*>(v_s + kGroup * ld);
-  const int b = blockIdx.x;
+  const int h = blockIdx.x, b = blockIdx.y;
   const int n = n_acc ? n_acc[b] : k;
-  int len = tail_len[b];
-  int plen = packed_len[b];
+  const int len = tail_len[b];
+  const int plen = packed_len[b];
   const int add = n + 1;
   if (n < 0 || n > k || len < 0 || len + add > tail_cap) {
     if (threadIdx.x == 0) atomicOr(&g_quant_status, VC_DEV_CAPACITY);
@@ -193,56 +195,60 @@ __global__ void __launch_bounds__(kPackThreads) append_kernel(
     return;
   }
   const int vec = d / 8;
+  const size_t tb = (static_cast<size_t>(b) * Hkv + h) * tail_cap * d;
   // 1. append: tail[b, h, len + r] = new[b, r, h] for r <= n
-  for (int i = threadIdx.x; i < add * Hkv * vec; i += blockDim.x) {
-    const int v = i % vec, h = (i / vec) % Hkv, r = i / (vec * Hkv);
+  for (int i = threadIdx.x; i < add * vec; i += blockDim.x) {
+    const int v = i % vec, r = i / vec;
     const size_t src = ((static_cast<size_t>(b) * (k + 1) + r) * Hkv + h) * d + v * 8;
-    const size_t dst = ((static_cast<size_t>(b) * Hkv + h) * tail_cap + len + r) * d + v * 8;
+    const size_t dst = tb + static_cast<size_t>(len + r) * d + v * 8;
     *reinterpret_cast<uint4*>(tail_k + dst) = *reinterpret_cast<const uint4*>(k_new + src);
     *reinterpret_cast<uint4*>(tail_v + dst) = *reinterpret_cast<const uint4*>(v_new + src);
   }
   __syncthreads();
-  __threadfence_block();
   // 2. pack whole groups from the front of the tail
+  Packed s = slice(p, b * Hkv + h, T_cap, d, BITS);
   for (int grp = 0; grp < n_pack; ++grp) {
-    for (int h = 0; h < Hkv; ++h) {
-      const size_t tb = (static_cast<size_t>(b) * Hkv + h) * tail_cap * d;
-      load_tile(k_s, ld, tail_k + tb + static_cast<size_t>(grp) * kGroup * d, d);
-      load_tile(v_s, ld, tail_v + tb + static_cast<size_t>(grp) * kGroup * d, d);
-      __syncthreads();
-      Packed s = slice(p, b * Hkv + h, T_cap, d, BITS);
-      quantize_tile<BITS>(k_s, v_s, ld, d, codes_s, plen / kGroup + grp, s.kc, s.ksz, s.vc, s.vsz);
-    }
+    load_tile(k_s, ld, tail_k + tb + static_cast<size_t>(grp) * kGroup * d, d);
+    load_tile(v_s, ld, tail_v + tb + static_cast<size_t>(grp) * kGroup * d, d);
+    __syncthreads();
+    quantize_tile<BITS>(k_s, v_s, ld, d, codes_s, plen / kGroup + grp, s.kc, s.ksz, s.vc, s.vsz);
   }
   // 3. shift the remaining (total - 32*n_pack < 32) tail tokens to the front
   const int shift = n_pack * kGroup;
   const int rest = total - shift;
   if (shift > 0 && rest > 0) {
-    for (int h = 0; h < Hkv; ++h) {
-      const size_t tb = (static_cast<size_t>(b) * Hkv + h) * tail_cap * d;
-      // rest < 32 rows: stage through smem (rows overlap when shift < rest)
-      for (int i = threadIdx.x; i < rest * vec; i += blockDim.x) {
-        const int t = i / vec, v = i % vec;
-        const uint4 a = *reinterpret_cast<const uint4*>(tail_k + tb + static_cast<size_t>(shift + t) * d + v * 8);
-        const uint4 c = *reinterpret_cast<const uint4*>(tail_v + tb + static_cast<size_t>(shift + t) * d + v * 8);
-        uint32_t* ok = reinterpret_cast<uint32_t*>(k_s + t * ld + v * 8);
-        uint32_t* ov = reinterpret_cast<uint32_t*>(v_s + t * ld + v * 8);
-        ok[0] = a.x; ok[1] = a.y; ok[2] = a.z; ok[3] = a.w;
-        ov[0] = c.x; ov[1] = c.y; ov[2] = c.z; ov[3] = c.w;
-      }
-      __syncthreads();
-      for (int i = threadIdx.x; i < rest * vec; i += blockDim.x) {
-        const int t = i / vec, v = i % vec;
-        const uint32_t* ik = reinterpret_cast<const uint32_t*>(k_s + t * ld + v * 8);
-        const uint32_t* iv = reinterpret_cast<const uint32_t*>(v_s + t * ld + v * 8);
-        *reinterpret_cast<uint4*>(tail_k + tb + static_cast<size_t>(t) * d + v * 8) = make_uint4(ik[0], ik[1], ik[2], ik[3]);
-        *reinterpret_cast<uint4*>(tail_v + tb + static_cast<size_t>(t) * d + v * 8) = make_uint4(iv[0], iv[1], iv[2], iv[3]);
-      }
-      __syncthreads();
+    // stage through smem: the source and destination rows may overlap
+    for (int i = threadIdx.x; i < rest * vec; i += blockDim.x) {
+      const int t = i / vec, v = i % vec;
+      const uint4 a = *reinterpret_cast<const uint4*>(tail_k + tb + static_cast<size_t>(shift + t) * d + v * 8);
+      const uint4 c = *reinterpret_cast<const uint4*>(tail_v + tb + static_cast<size_t>(shift + t) * d + v * 8);
+      uint32_t* ok = reinterpret_cast<uint32_t*>(k_s + t * ld + v * 8);
+      uint32_t* ov = reinterpret_cast<uint32_t*>(v_s + t * ld + v * 8);
+      ok[0] = a.x; ok[1] = a.y; ok[2] = a.z; ok[3] = a.w;
+      ov[0] = c.x; ov[1] = c.y; ov[2] = c.z; ov[3] = c.w;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < rest * vec; i += blockDim.x) {
+      const int t = i / vec, v = i % vec;
+      const uint32_t* ik = reinterpret_cast<const uint32_t*>(k_s + t * ld + v * 8);
+      const uint32_t* iv = reinterpret_cast<const uint32_t*>(v_s + t * ld + v * 8);
+      *reinterpret_cast<uint4*>(tail_k + tb + static_cast<size_t>(t) * d + v * 8) = make_uint4(ik[0], ik[1], ik[2], ik[3]);
+      *reinterpret_cast<uint4*>(tail_v + tb + static_cast<size_t>(t) * d + v * 8) = make_uint4(iv[0], iv[1], iv[2], iv[3]);
     }
   }
-  if (threadIdx.x == 0) {
-    tail_len[b] = rest;
+}
+
+// New lengths after append_kernel (same checks, so a rejected request keeps its lengths).
+__global__ void append_lengths_kernel(const int32_t* __restrict__ n_acc, int B, int k, int32_t* tail_len,
+                                      int tail_cap, int32_t* packed_len, int T_cap) {
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int n = n_acc ? n_acc[b] : k;
+    const int len = tail_len[b], plen = packed_len[b];
+    if (n < 0 || n > k || len < 0 || len + n + 1 > tail_cap) continue;
+    const int total = len + n + 1;
+    const int shift = (total / kGroup) * kGroup;
+    if (plen + shift > T_cap) continue;
+    tail_len[b] = total - shift;
     packed_len[b] = plen + shift;
   }
 }
@@ -681,12 +687,14 @@ extern "C" vc_status_t vc_quant_kv_append(const vc_shape_t* s, const uint16_t* k
   const size_t sm = pack_smem(s->d);
   auto cs = reinterpret_cast<cudaStream_t>(stream);
   if (s->bits == 2)
-    append_kernel<2><<<s->B, kPackThreads, sm, cs>>>(k_new, v_new, n_acc, s->k, s->Hkv, s->d, tail_k, tail_v,
-                                                      tail_len, tail_cap, p, packed_len, T_cap);
+    append_kernel<2><<<dim3(s->Hkv, s->B), kPackThreads, sm, cs>>>(k_new, v_new, n_acc, s->k, s->Hkv, s->d, tail_k,
+                                                                     tail_v, tail_len, tail_cap, p, packed_len, T_cap);
   else
-    append_kernel<4><<<s->B, kPackThreads, sm, cs>>>(k_new, v_new, n_acc, s->k, s->Hkv, s->d, tail_k, tail_v,
-                                                      tail_len, tail_cap, p, packed_len, T_cap);
+    append_kernel<4><<<dim3(s->Hkv, s->B), kPackThreads, sm, cs>>>(k_new, v_new, n_acc, s->k, s->Hkv, s->d, tail_k,
+                                                                     tail_v, tail_len, tail_cap, p, packed_len, T_cap);
   VC_LAUNCH_CHECK("append_kernel");
+  append_lengths_kernel<<<1, 256, 0, cs>>>(n_acc, s->B, s->k, tail_len, tail_cap, packed_len, T_cap);
+  VC_LAUNCH_CHECK("append_lengths_kernel");
   return VC_OK;
 }
 

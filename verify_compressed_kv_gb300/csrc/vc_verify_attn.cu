@@ -676,10 +676,11 @@ extern "C" vc_status_t vc_verify_attn_streamed(vc_verify_pipeline_t p, const vc_
   const size_t need = ws_bytes(s, parts_per_chunk);
   if (!workspace || workspace_bytes < need)
     VC_FAIL(VC_ERR_WORKSPACE, "verify workspace needs %zu bytes (got %zu)", need, workspace_bytes);
-  if ((st = check_pinned(host_kv)) != VC_OK) return st;
+  // host-side fault injection for tests: fail before touching CUDA
   if (const char* f = std::getenv("VC_FAULT")) {
     if (std::string(f) == "h2d_fail") VC_FAIL(VC_ERR_CUDA, "injected host-to-device failure (VC_FAULT=h2d_fail)");
   }
+  if ((st = check_pinned(host_kv)) != VC_OK) return st;
   auto cs = reinterpret_cast<cudaStream_t>(compute_stream);
   auto xs = reinterpret_cast<cudaStream_t>(copy_stream);
   const int n_chunks = (max_prefix + C - 1) / C;

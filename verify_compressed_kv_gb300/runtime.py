@@ -52,7 +52,7 @@ class RoundInputs:
 
 class Group:
     def __init__(self, B, Hq, Hkv, d, k, bits, V, C, T0, layers=1, extra_tokens=None, n_slots=4,
-                 parts_per_chunk=1, softmax_scale=1.0, device="cuda", packed_T0=None):
+                 parts_per_chunk=None, softmax_scale=1.0, device="cuda", packed_T0=None):
         self.B, self.Hq, self.Hkv, self.d, self.k, self.bits, self.V = B, Hq, Hkv, d, k, bits, V
         self.C, self.L = C, layers
         self.device = torch.device(device)
@@ -62,6 +62,13 @@ class Group:
         self.P0 = T0 if packed_T0 is None else packed_T0             # tokens in the draft cache at start
         self.P_cap = int(math.ceil((self.P0 + extra) / GROUP) * GROUP)
         self.tail_cap = GROUP + k + 1
+        if parts_per_chunk is None:
+            # split each chunk so one chunk launch gives about two CTAs per SM:
+            # CTAs = parts * B * Hkv * row blocks of up to 128 query rows
+            rows = (k + 1) * (Hq // Hkv)
+            row_blocks = -(-(-(-rows // 16)) // 8)
+            sms = torch.cuda.get_device_properties(torch.device(device)).multi_processor_count
+            parts_per_chunk = max(1, min(8, -(-2 * sms // (B * Hkv * row_blocks))))
         self.parts = parts_per_chunk
         dev = self.device
         # ---- draft caches, one per layer
@@ -169,7 +176,7 @@ class Group:
             vc.vc_quant_kv_append(self.shape, inp.kv_new[0, l], inp.kv_new[1, l], self.n_acc, self.tail_k[l],
                                   self.tail_v[l], self.tail_len[l], self.tail_cap, self.kc[l], self.ksz[l],
                                   self.vc[l], self.vsz[l], self.packed_len[l], self.P_cap, stream)
-            self.launches += 2
+            self.launches += 3                 # commit, append, append lengths
 
     def chunks(self):
         return (self.max_prefix + self.C - 1) // self.C
