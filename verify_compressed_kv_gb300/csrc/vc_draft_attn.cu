@@ -38,7 +38,14 @@ __device__ uint32_t g_draft_status = 0;
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kGroup = 32;
-constexpr int kStageGroups = kWarps;       // one group per warp per stage
+// Head split: with many heads per KV head (G = 8) two warps share a group,
+// each taking G/2 heads, so a warp's registers stay those of the G = 4 case.
+template <int G>
+struct HeadSplit {
+  static constexpr int HS = G >= 8 ? 2 : 1;   // warps per group
+  static constexpr int GW = G / HS;           // heads per warp
+  static constexpr int SG = kWarps / HS;      // groups per stage
+};
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
 #ifndef VC_DRAFT_QK_TB
@@ -101,16 +108,18 @@ __host__ __device__ inline void ctas_of(int bh, const DraftArgs& a, int& first, 
 template <int D, int BITS, int G>
 struct Plan {
   static constexpr int W = D * BITS / 32;
-  static constexpr size_t kc = static_cast<size_t>(kStageGroups) * W * kGroup * 4;
-  static constexpr size_t meta = static_cast<size_t>(kStageGroups) * D * 4;
+  static constexpr int GW = HeadSplit<G>::GW, SG = HeadSplit<G>::SG;
+  static constexpr size_t kc = static_cast<size_t>(SG) * W * kGroup * 4;
+  static constexpr size_t meta = static_cast<size_t>(SG) * D * 4;
   static constexpr size_t stage = 2 * kc + 2 * meta;             // K codes, K meta, V codes, V meta
-  static constexpr int NS = stage * 3 <= 80 * 1024 ? 3 : 2;       // ring depth
+  // ring depth: about 72 KB of stages in flight, at least double buffering
+  static constexpr int NS = (72 * 1024 / stage) < 2 ? 2 : ((72 * 1024 / stage) > 6 ? 6 : static_cast<int>(72 * 1024 / stage));
   static constexpr size_t ring = stage * NS;
-  static constexpr size_t red = static_cast<size_t>(kWarps) * G * D * 4;   // warp merge (aliases the ring)
+  static constexpr size_t red = static_cast<size_t>(kWarps) * GW * D * 4;  // warp merge (aliases the ring)
   static constexpr size_t body = ring > red ? ring : red;
-  static constexpr size_t sc = static_cast<size_t>(kWarps) * G * kGroup * 4;  // per-warp scores
+  static constexpr size_t sc = static_cast<size_t>(kWarps) * GW * kGroup * 4;  // per-warp scores
   static constexpr size_t q = static_cast<size_t>(G) * D * 4;
-  static constexpr size_t wstat = static_cast<size_t>(kWarps) * G * 2 * 4;  // per-warp (max, sum)
+  static constexpr size_t wstat = static_cast<size_t>(kWarps) * (GW > 8 ? GW : 8) * 2 * 4;  // per-warp (max, sum)
   static constexpr size_t off_sc = body;
   static constexpr size_t off_q = off_sc + sc;
   static constexpr size_t off_wstat = off_q + q;
@@ -360,20 +369,23 @@ __device__ __forceinline__ void pv_group(const uint32_t* vc_g, const uint16_t* v
 // Partial of this CTA for slice bh: merge the warps' (max, sum, output) in
 // shared memory and write one normalised partial + log2-sum-exp per head.
 template <int D, int BITS, int G>
-__device__ void write_partial(const DraftArgs& a, uint8_t* smem, int bh, int slot, float (&m)[G], float (&l)[G],
-                              float2 (&acc)[G][PvLayout<D, BITS, G>::CPL / 2], float (&zacc)[G]) {
+__device__ void write_partial(const DraftArgs& a, uint8_t* smem, int bh, int slot,
+                              float (&m)[HeadSplit<G>::GW], float (&l)[HeadSplit<G>::GW],
+                              float2 (&acc)[HeadSplit<G>::GW][PvLayout<D, BITS, HeadSplit<G>::GW>::CPL / 2],
+                              float (&zacc)[HeadSplit<G>::GW]) {
   using P = Plan<D, BITS, G>;
-  using L = PvLayout<D, BITS, G>;
+  constexpr int GW = HeadSplit<G>::GW, HS = HeadSplit<G>::HS;
+  using L = PvLayout<D, BITS, GW>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* red = reinterpret_cast<float*>(smem);                          // [warp][G][D], aliases the ring
-  float* wstat = reinterpret_cast<float*>(smem + P::off_wstat);         // [warp][G][2]
+  float* red = reinterpret_cast<float*>(smem);                          // [warp][GW][D], aliases the ring
+  float* wstat = reinterpret_cast<float*>(smem + P::off_wstat);         // [warp][GW][2]
   const int wr = lane / L::TSR, tsr = lane % L::TSR;
   const int w = wr / L::SUB, sub = wr % L::SUB;
   // fold the token rows of the PV layout (the low lane bits)
 #pragma unroll
   for (int o = 1; o < L::TSR; o <<= 1)
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+    for (int h = 0; h < GW; ++h) {
       zacc[h] += __shfl_xor_sync(0xffffffffu, zacc[h], o);
 #pragma unroll
       for (int jp = 0; jp < L::CPL / 2; ++jp) {
@@ -382,7 +394,7 @@ __device__ void write_partial(const DraftArgs& a, uint8_t* smem, int bh, int slo
       }
     }
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
+  for (int h = 0; h < GW; ++h) {
     float s = l[h];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
@@ -391,29 +403,30 @@ __device__ void write_partial(const DraftArgs& a, uint8_t* smem, int bh, int slo
   __syncthreads();                                 // every warp is done with the ring
   if (tsr == 0) {
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int h = 0; h < GW; ++h)
 #pragma unroll
       for (int jp = 0; jp < L::CPL / 2; ++jp) {
         const int jl = 2 * jp;
         const int jj = (L::SUB == 1) ? (jl % L::HALF) : jl;
-        float* dst = red + (warp * G + h) * D + w * L::CPW + sub * L::CPL + jl;
+        float* dst = red + (warp * GW + h) * D + w * L::CPW + sub * L::CPL + jl;
         dst[0] = fmaf(acc[h][jp].x, pow2neg(BITS * jj), zacc[h]);
         dst[1] = fmaf(acc[h][jp].y, pow2neg(BITS * (jj + 1)), zacc[h]);
       }
   }
   if (lane == 0)
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      wstat[(warp * G + h) * 2] = m[h];
-      wstat[(warp * G + h) * 2 + 1] = l[h];
+    for (int h = 0; h < GW; ++h) {
+      wstat[(warp * GW + h) * 2] = m[h];
+      wstat[(warp * GW + h) * 2 + 1] = l[h];
     }
   __syncthreads();
   const int b = bh / a.Hkv, kvh = bh % a.Hkv;
   for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
     const int h = i / D, c = i % D;
+    const int half = h / GW, hl = h % GW;             // warps x with x % HS == half hold head h
     float M = -INFINITY;
 #pragma unroll
-    for (int x = 0; x < kWarps; ++x) M = fmaxf(M, wstat[(x * G + h) * 2]);
+    for (int x = half; x < kWarps; x += HS) M = fmaxf(M, wstat[(x * GW + hl) * 2]);
     const size_t row = static_cast<size_t>(b * a.Hq + kvh * G + h) * a.max_parts + slot;
     if (M == -INFINITY) {
       if (c == 0) a.part_lse[row] = -INFINITY;
@@ -421,12 +434,12 @@ __device__ void write_partial(const DraftArgs& a, uint8_t* smem, int bh, int slo
     }
     float o = 0.0f, Ls = 0.0f;
 #pragma unroll
-    for (int x = 0; x < kWarps; ++x) {
-      const float mx = wstat[(x * G + h) * 2];
+    for (int x = half; x < kWarps; x += HS) {
+      const float mx = wstat[(x * GW + hl) * 2];
       if (mx == -INFINITY) continue;
       const float wgt = exp2f(mx - M);
-      o = fmaf(wgt, red[(x * G + h) * D + c], o);
-      Ls = fmaf(wgt, wstat[(x * G + h) * 2 + 1], Ls);
+      o = fmaf(wgt, red[(x * GW + hl) * D + c], o);
+      Ls = fmaf(wgt, wstat[(x * GW + hl) * 2 + 1], Ls);
     }
     a.part_o[row * D + c] = o / Ls;
     if (c == 0) a.part_lse[row] = M + log2f(Ls);
@@ -471,10 +484,11 @@ __device__ void arrive_and_combine(const DraftArgs& a, unsigned int* flag, int b
 template <int D, int BITS, int G>
 __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
   using P = Plan<D, BITS, G>;
-  using L = PvLayout<D, BITS, G>;
+  constexpr int GW = HeadSplit<G>::GW, HS = HeadSplit<G>::HS, SG = HeadSplit<G>::SG;
+  using L = PvLayout<D, BITS, GW>;
   constexpr int W = P::W, NS = P::NS, NC = D / kGroup;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* sc = reinterpret_cast<float*>(smem + P::off_sc) + warp * G * kGroup;
+  float* sc = reinterpret_cast<float*>(smem + P::off_sc) + warp * GW * kGroup;
   float* q_s = reinterpret_cast<float*>(smem + P::off_q);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P::off_bar);
   unsigned int* flag = reinterpret_cast<unsigned int*>(smem + P::off_flag);
@@ -498,7 +512,7 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
       ng_req = a.NGmax;
     }
     const int n_valid = max(0, min(ge, ng_req) - gs);
-    const int n_st = (n_valid + kStageGroups - 1) / kStageGroups;
+    const int n_st = (n_valid + SG - 1) / SG;
     int first, last;
     ctas_of(bh, a, first, last);
     // ---- prologue: fill the ring (the proxy fence orders earlier generic
@@ -507,15 +521,15 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
     if (threadIdx.x == 0)
       for (int i = 0; i < NS && i < n_st; ++i) {
         const int buf = static_cast<int>((gstage + i) % NS);
-        issue_stage<D, BITS, G>(a, smem + buf * P::stage, bars + buf, bh, gs + i * kStageGroups,
-                                min(kStageGroups, n_valid - i * kStageGroups));
+        issue_stage<D, BITS, G>(a, smem + buf * P::stage, bars + buf, bh, gs + i * SG,
+                                min(SG, n_valid - i * SG));
       }
     load_q<D, G>(a, b, kvh, q_s);
     __syncthreads();
-    float m[G], l[G], zacc[G];
-    float2 acc[G][L::CPL / 2];
+    float m[GW], l[GW], zacc[GW];
+    float2 acc[GW][L::CPL / 2];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+    for (int h = 0; h < GW; ++h) {
       m[h] = -INFINITY;
       l[h] = 0.0f;
       zacc[h] = 0.0f;
@@ -530,31 +544,32 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
       ok = __syncthreads_and(mine) != 0;
       if (!ok) break;
       const uint8_t* base = smem + buf * P::stage;
-      const int gl = warp;                                   // this warp's group in the stage
-      if (st * kStageGroups + gl < n_valid) {
+      const int gl = warp / HS;                              // this warp's group in the stage
+      const float* q_w = q_s + (warp % HS) * GW * D;         // ... and its heads
+      if (st * SG + gl < n_valid) {
         const uint32_t* kc_g = reinterpret_cast<const uint32_t*>(base) + gl * W * kGroup;
         const uint16_t* ksz_g = reinterpret_cast<const uint16_t*>(base + P::kc) + gl * D * 2;
         const uint32_t* vc_g = reinterpret_cast<const uint32_t*>(base + P::kc + P::meta) + gl * W * kGroup;
         const uint16_t* vsz_g = reinterpret_cast<const uint16_t*>(base + 2 * P::kc + P::meta) + gl * NC * kGroup * 2;
-        qk_group<D, BITS, G>(kc_g, ksz_g, q_s, sc, lane);
+        qk_group<D, BITS, GW>(kc_g, ksz_g, q_w, sc, lane);
         __syncwarp();
-        float alpha[G];
-        if (softmax_group<G>(sc, m, l, alpha, lane)) {
+        float alpha[GW];
+        if (softmax_group<GW>(sc, m, l, alpha, lane)) {
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
+          for (int h = 0; h < GW; ++h) {
             zacc[h] *= alpha[h];
 #pragma unroll
             for (int jp = 0; jp < L::CPL / 2; ++jp) acc[h][jp] = __fmul2_rn(acc[h][jp], make_float2(alpha[h], alpha[h]));
           }
         }
         __syncwarp();
-        pv_group<D, BITS, G>(vc_g, vsz_g, sc, acc, zacc, lane);
+        pv_group<D, BITS, GW>(vc_g, vsz_g, sc, acc, zacc, lane);
         __syncwarp();
       }
       __syncthreads();                                      // stage `buf` fully consumed
       if (threadIdx.x == 0 && st + NS < n_st)
-        issue_stage<D, BITS, G>(a, smem + buf * P::stage, bars + buf, bh, gs + (st + NS) * kStageGroups,
-                                min(kStageGroups, n_valid - (st + NS) * kStageGroups));
+        issue_stage<D, BITS, G>(a, smem + buf * P::stage, bars + buf, bh, gs + (st + NS) * SG,
+                                min(SG, n_valid - (st + NS) * SG));
     }
     gstage += n_st;
     if (!ok) {
@@ -715,7 +730,7 @@ vc_status_t plan_t(const vc_shape_t* s, int max_packed, LaunchPlan* lp) {
   const long long NGmax = max_packed / kGroup;
   lp->total = static_cast<long long>(s->B) * s->Hkv * NGmax;
   long long n = static_cast<long long>(occ) * sms;
-  const long long by_work = lp->total / kStageGroups;          // at least one stage per CTA
+  const long long by_work = lp->total / HeadSplit<G>::SG;      // at least one stage per CTA
   if (n > by_work) n = by_work;
   if (n < 1 && lp->total > 0) n = 1;
   lp->n_stream = static_cast<int>(lp->total > 0 ? n : 0);
