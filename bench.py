@@ -72,9 +72,10 @@ class Clocks:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
+        """Stop sampling; summarise the samples that arrived in [t0, t1] (wall time)."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -84,7 +85,9 @@ class Clocks:
             self.proc.kill()
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ts, ln in self.lines:
+            if t0 is not None and not (t0 - 0.25 <= ts <= t1 + 0.25):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -241,6 +244,23 @@ def run_ours(args, rank, world, local_rank):
     e2e_bufs = [to_device(hi[0], device) for hi in host_inputs]
     torch.cuda.synchronize()
 
+    # ---- the link's own peak: best pinned host->device copy of 512 MiB (the
+    # roofline of the H2D stream), measured on this machine at this moment
+    link_buf_h = torch.empty(512 * 2 ** 20, dtype=torch.uint8, pin_memory=True)
+    link_buf_h.fill_(1)
+    link_buf_d = torch.empty_like(link_buf_h, device=device)
+    link_best = 0.0
+    for _ in range(4):
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(xs):
+            l0.record(xs)
+            link_buf_d.copy_(link_buf_h, non_blocking=True)
+            l1.record(xs)
+        l1.synchronize()
+        link_best = max(link_best, link_buf_h.numel() / l0.elapsed_time(l1) / 1e6)
+    del link_buf_h, link_buf_d
+    measured_link = link_best if args.link_peak_gbs <= 0 else args.link_peak_gbs
+
     # ---- prefill rows timed once: quantise + pack of the full prefix (layer 0)
     K0, V0 = synth.kv(w, layer=0, group=0, threads=16)
     K0d = torch.from_numpy(K0.view(np.int16)).to(device)
@@ -310,7 +330,11 @@ def run_ours(args, rank, world, local_rank):
         tl.ev["end"].synchronize()
         return sum(g.after_round() for g in done)
 
-    # ---- warm-up
+    # ---- warm-up (the clock sampler starts first: its start-up must not fall
+    # inside the timed region)
+    clocks = Clocks(local_rank)
+    clocks.start()
+    time.sleep(0.5)
     for _ in range(args.warmup):
         tl, done = one_round()
         finish(tl, done)
@@ -320,9 +344,7 @@ def run_ours(args, rank, world, local_rank):
     dist_barrier(world)
     torch.cuda.synchronize()
     launches0 = sum(g.launches for g in groups)
-    clocks = Clocks(local_rank)
-    clocks.start()
-    time.sleep(0.3)
+    wall0 = time.time()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(cs)
@@ -337,7 +359,8 @@ def run_ours(args, rank, world, local_rank):
         tls.append(tl)
     t_end.record(cs)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    wall1 = time.time()
+    clk = clocks.stop(wall0, wall1)
     dist_barrier(world)
     launches = sum(g.launches for g in groups) - launches0
     total_ms = t_start.elapsed_time(t_end)
@@ -377,6 +400,33 @@ def run_ours(args, rank, world, local_rank):
     # inside the timed rounds: average draft call = draft span / (k * layers)
     draft_in_round_ms = med(draft_span) / (w.k * layers)
 
+    # ---- context: plain full-KV decoding (one token per request per step), the
+    # full KV of every layer streamed from pinned host memory each step as in the
+    # pages' long-context scenario, through the same streamed verify kernel (k = 0)
+    g = groups[0]
+    inp0 = dev_inputs[0][0]
+    q1 = inp0.q_verify[:, :, :1].contiguous()
+    kv1 = inp0.kv_new[:, :, :, :1].contiguous()
+    out1 = torch.empty((w.B, 1, w.Hq, w.d), dtype=torch.int16, device=device)
+    n_dec = 3
+    for _ in range(2):
+        for l in range(layers):
+            g.decode_full_kv(q1[l], kv1[:, l], out1, l, cs, xs)
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    d0.record(cs)
+    for _ in range(n_dec):
+        for l in range(layers):
+            g.decode_full_kv(q1[l], kv1[:, l], out1, l, cs, xs)
+    ex = torch.cuda.Event()
+    ex.record(xs)
+    cs.wait_event(ex)
+    d1.record(cs)
+    d1.synchronize()
+    dec_ms = d0.elapsed_time(d1) / n_dec
+    full_kv = {"value": w.B * layers / (dec_ms / 1e3), "unit": "tokens/s/layer", "ms_per_step": dec_ms,
+               "what": "greedy decoding with the full KV streamed host->device every step (same kernels, k = 0)"}
+
     # ---- e2e: same rounds, inputs copied from pinned host memory every round, result read back
     dist_barrier(world)
     torch.cuda.synchronize()
@@ -398,7 +448,7 @@ def run_ours(args, rank, world, local_rank):
 
     draft_src = os.path.join(ROOT, "verify_compressed_kv_gb300", "csrc", "vc_draft_attn.cu")
     traffic = ncu_traffic(draft_src, args.workload)
-    link_peak = args.link_peak_gbs
+    link_peak = measured_link
     h2d_rate = (h2d_bytes / args.steps) / (med(copy_span) / 1e3) / 1e9 if copy_span else None
     out = {
         "metric": METRIC,
@@ -429,12 +479,14 @@ def run_ours(args, rank, world, local_rank):
                      "ms_per_launch_in_round": draft_in_round_ms, "peak_source": peaks["source"]},
         "h2d": {"gbs": h2d_rate, "bytes_per_round": h2d_bytes / args.steps, "copy_ms": med(copy_span),
                 "frac_of_measured_link": (h2d_rate / link_peak) if h2d_rate else None,
-                "measured_link_gbs": link_peak, "frac_of_pcie_gen5_64": (h2d_rate / PCIE_GEN5_GBS) if h2d_rate else None,
+                "measured_link_gbs": link_peak, "link_peak_source": "measured at start-up (best of 4 x 512 MiB)"
+                if args.link_peak_gbs <= 0 else "given on the command line", "frac_of_pcie_gen5_64": (h2d_rate / PCIE_GEN5_GBS) if h2d_rate else None,
                 "overlap_with_draft": med(overlap)},
         "round_ms": {"median": med(round_ms), "draft": med(draft_span), "copy": med(copy_span),
                      "all": [round(x, 3) for x in round_ms],
                      "host_gap_total": round(total_ms - sum(round_ms), 3)},
         "prefill_pack": {"ms": pack_ms, "gbs": pack_bytes / (pack_ms / 1e3) / 1e9},
+        "full_kv_decode": dict(full_kv, speedup_of_value=value_local / full_kv["value"]),
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -597,8 +649,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--schedule", default="staggered", choices=["staggered", "lockstep"])
     ap.add_argument("--slots", type=int, default=8)
-    ap.add_argument("--link-peak-gbs", type=float, default=211.0,
-                    help="measured pinned host->device copy peak of the box (GB/s)")
+    ap.add_argument("--link-peak-gbs", type=float, default=0.0,
+                    help="pinned host->device peak in GB/s (default 0: measure it at start-up)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

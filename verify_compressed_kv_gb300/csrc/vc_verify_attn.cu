@@ -404,33 +404,37 @@ __global__ void __launch_bounds__(kMaxWarps * 32) verify_finish_kernel(VerifyArg
   }
 }
 
-// Commit: grid B.  Writes rows 0..n of k_new / v_new into the host store.
+// Commit: grid (2 * Hkv, B), one CTA per (K|V, KV head, request).  Writes rows
+// 0..n of k_new / v_new into the host store (mapped pinned memory) at the
+// request's prefix length; commit_lengths_kernel advances the lengths after.
 __global__ void commit_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
-                              const int32_t* __restrict__ n_acc, int32_t* prefix_len, uint16_t* host_kv, int B,
+                              const int32_t* __restrict__ n_acc, const int32_t* prefix_len, uint16_t* host_kv, int B,
                               int R, int Hkv, int D, int C, int T_cap) {
-  const int b = blockIdx.x;
+  const int kv = blockIdx.x / Hkv, h = blockIdx.x % Hkv, b = blockIdx.y;
   const int n = n_acc ? n_acc[b] : R - 1;
   const int len = prefix_len[b];
   if (n < 0 || n >= R || len < 0 || len + n + 1 > T_cap) {
-    if (threadIdx.x == 0) atomicOr(&g_verify_status, VC_DEV_CAPACITY);
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(&g_verify_status, VC_DEV_CAPACITY);
     return;
   }
   const int vec = D / 8;
-  const int total = (n + 1) * 2 * Hkv * vec;
-  for (int i = threadIdx.x; i < total; i += blockDim.x) {
-    const int v = i % vec;
-    const int h = (i / vec) % Hkv;
-    const int kv = (i / (vec * Hkv)) % 2;
-    const int r = i / (vec * Hkv * 2);
+  const uint16_t* base = kv ? v_new : k_new;
+  for (int i = threadIdx.x; i < (n + 1) * vec; i += blockDim.x) {
+    const int v = i % vec, r = i / vec;
     const int pos = len + r;
     const int chunk = pos / C, t = pos % C;
-    const uint16_t* src = (kv ? v_new : k_new) + ((static_cast<size_t>(b) * R + r) * Hkv + h) * D + v * 8;
+    const uint16_t* src = base + ((static_cast<size_t>(b) * R + r) * Hkv + h) * D + v * 8;
     uint16_t* dst = host_kv + ((((static_cast<size_t>(chunk) * 2 + kv) * B + b) * Hkv + h) * C + t) * D + v * 8;
     *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence_system();
+}
+
+__global__ void commit_lengths_kernel(const int32_t* __restrict__ n_acc, int32_t* prefix_len, int B, int R, int T_cap) {
+  __threadfence_system();
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int n = n_acc ? n_acc[b] : R - 1;
+    const int len = prefix_len[b];
+    if (n < 0 || n >= R || len < 0 || len + n + 1 > T_cap) continue;
     prefix_len[b] = len + n + 1;
   }
 }
@@ -710,9 +714,12 @@ extern "C" vc_status_t vc_verify_commit(const vc_shape_t* s, const uint16_t* k_n
   if ((st = check_pinned(host_kv)) != VC_OK) return st;
   void* dptr = nullptr;
   VC_CUDA_CHECK(cudaHostGetDevicePointer(&dptr, const_cast<uint16_t*>(host_kv), 0));
-  commit_kernel<<<s->B, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      k_new, v_new, n_acc, prefix_len, static_cast<uint16_t*>(dptr), s->B, s->k + 1, s->Hkv, s->d, C, T_cap);
+  auto cs = reinterpret_cast<cudaStream_t>(stream);
+  commit_kernel<<<dim3(2 * s->Hkv, s->B), 128, 0, cs>>>(k_new, v_new, n_acc, prefix_len, static_cast<uint16_t*>(dptr),
+                                                        s->B, s->k + 1, s->Hkv, s->d, C, T_cap);
   VC_LAUNCH_CHECK("commit_kernel");
+  commit_lengths_kernel<<<1, 256, 0, cs>>>(n_acc, prefix_len, s->B, s->k + 1, T_cap);
+  VC_LAUNCH_CHECK("commit_lengths_kernel");
   return VC_OK;
 }
 

@@ -164,6 +164,20 @@ class Group:
                                    self.ws_verify_bytes, compute_stream, copy_stream)
         self.launches += self.chunks() + 1     # one kernel per chunk, then the new-token block + merge
 
+    def decode_full_kv(self, q1, kv1, out1, layer, compute_stream, copy_stream):
+        """One plain decoding step over the full KV (the baseline the pages
+        compare against): the same streamed verify path with one row (k = 0).
+        q1 [B, 1, Hq, d], kv1 [2, B, 1, Hkv, d], out1 [B, 1, Hq, d]."""
+        if not hasattr(self, "_shape0"):
+            self._shape0 = vc.shape(self.B, self.Hq, self.Hkv, self.d, k=0, bits=self.bits,
+                                    softmax_scale=self.shape.softmax_scale)
+            self._ws0_bytes = vc.vc_verify_attn_workspace_size(self._shape0, self.parts)
+            self._ws0 = torch.zeros(self._ws0_bytes, dtype=torch.uint8, device=self.device)
+        vc.vc_verify_attn_streamed(self.pipe, self._shape0, q1, self.host_kv[layer], self.C, self.max_prefix,
+                                   self.prefix_len[layer], self.slots, kv1[0], kv1[1], out1, self.parts, self._ws0,
+                                   self._ws0_bytes, compute_stream, copy_stream)
+        self.launches += self.chunks() + 1
+
     def accept(self, inp: RoundInputs, stream):
         vc.vc_accept(self.B, self.k, self.V, inp.logits, inp.drafts, self.n_acc, self.next_tok, None,
                      self.ws_accept, self.ws_accept_bytes, stream)
@@ -176,7 +190,7 @@ class Group:
             vc.vc_quant_kv_append(self.shape, inp.kv_new[0, l], inp.kv_new[1, l], self.n_acc, self.tail_k[l],
                                   self.tail_v[l], self.tail_len[l], self.tail_cap, self.kc[l], self.ksz[l],
                                   self.vc[l], self.vsz[l], self.packed_len[l], self.P_cap, stream)
-            self.launches += 3                 # commit, append, append lengths
+            self.launches += 4                 # commit, commit lengths, append, append lengths
 
     def chunks(self):
         return (self.max_prefix + self.C - 1) // self.C
