@@ -63,7 +63,7 @@ class Clocks:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -514,59 +514,65 @@ import synth
 from oracle import kivi, attention, accept
 w = synth.get({wl!r})
 b = 0
-# one request (all its KV heads), one round: k draft steps, verify, accept
+heads = {heads!r}                    # the KV heads of request 0 timed in this sample
+G = w.G
+qh = np.concatenate([np.arange(h * G, (h + 1) * G) for h in heads])
 Ks, Vs = [], []
 T = w.T_keep if w.name == 'qwen' else w.T
-for h in range(w.Hkv):
+for h in heads:
     k_, v_ = synth.kv_slice(w, b, h, T=T)
     Ks.append(k_); Vs.append(v_)
 K = np.stack(Ks)[None]; V = np.stack(Vs)[None]
 t0 = time.perf_counter()
 packed = kivi.quant_pack(K, V, w.bits)
 t_pack = time.perf_counter() - t0
-tail = np.zeros((1, w.Hkv, 32 + w.k + 1, w.d), np.uint16)
+tail = np.zeros((1, len(heads), 32 + w.k + 1, w.d), np.uint16)
 t0 = time.perf_counter()
 for i in range({steps}):
-    q = synth.draft_q(w, 0, i)[b:b+1]
+    q = synth.draft_q(w, 0, i)[b:b+1][:, qh]
     kc, vc_ = synth.draft_kv_cur(w, 0, i)
-    attention.draft_attention(q, *packed, [T], tail, tail, [0], w.bits, 1.0, k_cur=kc[b:b+1], v_cur=vc_[b:b+1], step=i)
+    attention.draft_attention(q, *packed, [T], tail, tail, [0], w.bits, 1.0, k_cur=kc[b:b+1][:, heads],
+                              v_cur=vc_[b:b+1][:, heads], step=i)
 t_draft = (time.perf_counter() - t0) * w.k / {steps}
-qv = synth.verify_q(w, 0)[b:b+1]
+qv = synth.verify_q(w, 0)[b:b+1][:, :, qh]
 kn, vn = synth.kv_new(w, 0)
 t0 = time.perf_counter()
-attention.verify_attention(qv, K, V, kn[b:b+1], vn[b:b+1], [T], 1.0)
+attention.verify_attention(qv, K, V, kn[b:b+1][:, :, heads], vn[b:b+1][:, :, heads], [T], 1.0)
 t_verify = time.perf_counter() - t0
 logits, drafts, L = synth.logits_and_drafts(w, 0)
 t0 = time.perf_counter()
 n, nxt, _ = accept.accept(logits[b:b+1], drafts[b:b+1])
 t_accept = time.perf_counter() - t0
+scale = w.Hkv / len(heads)           # attention work of the request's other KV heads
 tokens = (int(n[0]) + 1) * w.layers
-t_round = (t_draft + t_verify + t_accept) * w.layers
-print(json.dumps(dict(t_round=t_round, tokens=tokens, t_pack=t_pack, t_draft=t_draft, t_verify=t_verify,
-                      t_accept=t_accept, draft_steps_run={steps})))
+t_round = ((t_draft + t_verify) * scale + t_accept) * w.layers
+print(json.dumps(dict(t_round=t_round, tokens=tokens, t_pack=t_pack * scale, t_draft=t_draft * scale,
+                      t_verify=t_verify * scale, t_accept=t_accept, draft_steps_run={steps}, heads=heads)))
 """
 
 
-def cpu_baseline(workload, steps=None):
-    """Time the oracle, as it stands, on one request of one round (all its KV
-    heads; 1 BLAS thread) and scale to the metric's unit."""
+def cpu_baseline(workload, steps=None, heads=None):
+    """Time the oracle, as it stands, on request 0 of one round (the given KV
+    heads, all of them by default; 1 BLAS thread) and scale to the metric's
+    unit (tokens of the request over the time of its whole round)."""
     import synth
     w = synth.get(workload)
     steps = steps if steps is not None else (2 if w.T * w.layers > 100000 else 4)
+    heads = list(range(w.Hkv)) if heads is None else list(heads)
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    code = ORACLE_SAMPLE.format(root=ROOT, wl=workload, steps=steps)
+    code = ORACLE_SAMPLE.format(root=ROOT, wl=workload, steps=steps, heads=heads)
     t0 = time.time()
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
     if r.returncode != 0:
         return {"value": None, "unit": "tokens/s/layer", "cores": 1, "kind": "oracle",
                 "sample": "failed: " + r.stderr[-300:]}
     d = json.loads(r.stdout.strip().splitlines()[-1])
-    # the whole batch = B requests, each processed like the sampled one
-    value = d["tokens"] / d["t_round"]        # tokens/s/layer for one request at a time on 1 core
+    value = d["tokens"] / d["t_round"]        # one request at a time on one core
+    T = w.T_keep if w.name == "qwen" else w.T
     return {"value": value, "unit": "tokens/s/layer", "cores": 1, "kind": "oracle",
-            "sample": (f"request 0 of round 0, all {w.Hkv} KV heads: {d['draft_steps_run']} of {w.k} draft steps "
-                       f"timed and scaled to {w.k}, one verify pass over T={w.T if w.name != 'qwen' else w.T_keep}, "
-                       f"accept; {w.layers} layer(s) by scaling; 1 thread"),
+            "sample": (f"request 0 of round 0, KV heads {heads} of {w.Hkv} (time scaled to all heads): "
+                       f"{d['draft_steps_run']} of {w.k} draft steps timed and scaled to {w.k}, one verify pass "
+                       f"over T={T}, accept; {w.layers} layer(s) by scaling; 1 thread"),
             "seconds": {k: d[k] for k in ("t_round", "t_pack", "t_draft", "t_verify", "t_accept")},
             "wall_s": time.time() - t0}
 
@@ -582,7 +588,8 @@ def run_reference(args, rank, world):
     for _ in range(args.warmup):
         pass                     # the oracle has no warm state to build
     for s in range(args.steps):
-        cb = cpu_baseline(args.workload, steps=1)
+        # each step: one KV head of request 0 (rotating), scaled to the whole request
+        cb = cpu_baseline(args.workload, steps=1, heads=[s % w.Hkv])
         if cb["value"] is None:
             break
         vals.append(cb["value"])
@@ -643,7 +650,7 @@ def dist_barrier(world):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="mistral", choices=["tiny", "mistral", "qwen", "llama", "stagger"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
