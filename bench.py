@@ -55,20 +55,29 @@ class Clocks:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, interval_ms=50):
         self.gpu = gpu_index
+        self.interval_ms = interval_ms
         self.proc = None
         self.lines = []
 
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def wait_ready(self, n=3, timeout=10.0):
+        """Block until the sampler has printed ``n`` samples: its start-up (driver
+        initialisation) stalls the GPU's host interface for tens of ms and must
+        not land inside the timed region."""
+        t_end = time.time() + timeout
+        while self.proc is not None and len(self.lines) < n and time.time() < t_end:
+            time.sleep(0.01)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -332,8 +341,9 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- warm-up (the clock sampler starts first: its start-up must not fall
     # inside the timed region)
-    clocks = Clocks(local_rank)
+    clocks = Clocks(local_rank, args.clock_ms)
     clocks.start()
+    clocks.wait_ready()
     time.sleep(0.5)
     for _ in range(args.warmup):
         tl, done = one_round()
@@ -650,12 +660,13 @@ def dist_barrier(world):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="mistral", choices=["tiny", "mistral", "qwen", "llama", "stagger"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--schedule", default="staggered", choices=["staggered", "lockstep"])
     ap.add_argument("--slots", type=int, default=8)
+    ap.add_argument("--clock-ms", type=int, default=50, help="nvidia-smi sampling interval during the timed region")
     ap.add_argument("--link-peak-gbs", type=float, default=0.0,
                     help="pinned host->device peak in GB/s (default 0: measure it at start-up)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

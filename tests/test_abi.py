@@ -84,3 +84,23 @@ def test_size_queries_match_the_layout(vc):
     kc, ksz, vcb, vsz = vc.vc_quant_packed_bytes(s4, 16384)
     assert (kc + ksz + vcb + vsz) // (16 * 8 * 16384) == 160
     assert vc.vc_accept_workspace_size(8, 16, 32768) > 0
+
+
+def test_misaligned_and_null_pointers_are_rejected_before_launch(vc):
+    s = vc.shape(1, 4, 1, 64, k=2, bits=4)
+    with pytest.raises(vc.VcError) as e:                      # logits not 16-byte aligned
+        vc.vc_accept(1, 2, 16, 0x1004, 0x2000, 0x3000, 0x4000, None, 0x5000, 1 << 20, stream=0)
+    assert e.value.status == 1 and "aligned" in str(e.value)
+    with pytest.raises(vc.VcError) as e:
+        vc.vc_quant_kv_pack(s, 64, 64, 0x1008, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, stream=0)
+    assert e.value.status == 1 and "aligned" in str(e.value)
+    with pytest.raises(vc.VcError) as e:
+        vc.vc_quant_kv_pack(s, 48, 64, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, stream=0)   # T % 32
+    assert e.value.status == 1
+    with pytest.raises(vc.VcError) as e:
+        vc.vc_gather_kv(s, 10, 4, None, 0x1000, 0x2000, 0x3000, 0x4000, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(vc.VcError) as e:                      # k_cur without v_cur
+        vc.vc_draft_attn(s, 0x1000, 0x2000, None, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 64, 64, 0x8000, 0x9000,
+                         0xa000, 8, 0, 0xb000, 0xc000, 1 << 20, stream=0)
+    assert e.value.status == 1
