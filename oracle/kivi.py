@@ -16,15 +16,16 @@ Summary, Architecture Support).  The recipe, step by step, for one group of
 Keys form their groups along 32 consecutive tokens of one channel; values
 along 32 consecutive channels of one token.
 
-Packed layout (the library's format; the oracle writes it from this text):
-W = d*b/32 32-bit words per token.
+Packed layout (the library's format; written out from the rules next to
+the packing functions below).  Per (request, KV head) and group of 32
+tokens:
 
-* K codes uint32 [B, Hkv, T/32, W, 32]: word (g, w, t) holds token 32g+t,
-  channels w*(32/b) + j for j < 32/b, code j at bits [b*j, b*j+b).
-* K meta fp16 [B, Hkv, T/32, d, 2]: (scale, zero) of channel c in group g.
-* V codes uint32 [B, Hkv, T/32, W, 32]: same packing as K codes.
-* V meta fp16 [B, Hkv, T/32, d/32, 32, 2]: (scale, zero) of token 32g+t over
-  channels 32cg .. 32cg+31.
+* K codes uint32 [B, Hkv, T/32, d*b] and V codes uint32 [B, Hkv, T/32, d*b]:
+  32 lanes x d*b/32 words, each code a b-bit field at a position given by its
+  token and channel (K and V use different maps).
+* K meta fp16 [B, Hkv, T/32, 2, d]: scales of the group's channels, then zeros.
+* V meta fp16 [B, Hkv, T/32, d/32, 2, 32]: per channel group, the 32 tokens'
+  scales, then zeros, tokens in a fixed permuted order.
 
 Numbers are numpy arrays.  bf16 inputs are uint16 bit patterns.
 """
@@ -109,62 +110,168 @@ def dequantize_kv(kcode, kscale, kzero, vcode, vscale, vzero):
 
 
 # ------------------------------------------------------------ packed layout
+#
+# The bit placement below is this library's own format (the quantiser fixes
+# only the codes and the fp16 scale/zero).  It follows the register fragments
+# of the 16x8x16 half-precision tensor-core product that consumes it, so that a
+# lane finds each pair of codes it feeds to one operand register 16 bits apart
+# in one word.  Written out per group of 32 tokens; d channels, b bits.
 
-def pack_codes(code: np.ndarray, bits: int) -> np.ndarray:
-    """Logical codes uint8 [B,H,T,d] -> words uint32 [B,H,T/32,W,32]."""
+def _field_pos(bits: int, u: int, r: int, e: int) -> int:
+    """Lowest bit of a field.  b = 2: slot (u, r, e) starts at (8 - 2r + 16e + 4u)
+    mod 32.  b = 4: slot (u, e) starts at (6 + 16e + 4u) mod 32 (r unused); its
+    four bits run upwards and wrap from bit 31 to bit 0."""
+    if bits == 2:
+        return (8 - 2 * r + 16 * e + 4 * u) % 32
+    return (6 + 16 * e + 4 * u) % 32
+
+
+def _word_index(L: int, w: int) -> int:
+    """Word w of lane L sits at (w // 4) * 128 + 4 L + w % 4 within the group."""
+    return (w // 4) * 128 + 4 * L + w % 4
+
+
+def _slot(bits: int, i: int, r: int):
+    """Fragment index i of a lane (and its r) -> (word, u) of its field."""
+    if bits == 2:
+        return i // 4, i % 4
+    i2 = 2 * i + r
+    return i2 // 4, i2 % 4
+
+
+def _k_fields(d: int, bits: int):
+    """(word index, field start, token, channel) of every K code of one group.
+
+    Lane L = 4a + c holds tokens 4a + j (j < 4) and channels (d/4) c + 4k + 2r + e
+    (k < d/16, r, e < 2); its fragment index is i = j*(d/16) + k."""
+    KS = d // 16
+    rows = []
+    for L in range(32):
+        a, c = divmod(L, 4)
+        for j in range(4):
+            for k in range(KS):
+                for r in range(2):
+                    for e in range(2):
+                        w, u = _slot(bits, j * KS + k, r)
+                        rows.append((_word_index(L, w), _field_pos(bits, u, r, e),
+                                     4 * a + j, (d // 4) * c + 4 * k + 2 * r + e))
+    return np.array(rows, dtype=np.int64)
+
+
+def _v_fields(d: int, bits: int):
+    """(word index, field start, token, channel) of every V code of one group.
+
+    Lane L = 4a + c holds tokens 8c + 4e + 2s + r (s, r, e < 2) and channels
+    8n + a (n < d/8); its fragment index is i = s*(d/8) + n."""
+    NT = d // 8
+    rows = []
+    for L in range(32):
+        a, c = divmod(L, 4)
+        for s in range(2):
+            for n in range(NT):
+                for r in range(2):
+                    for e in range(2):
+                        w, u = _slot(bits, s * NT + n, r)
+                        rows.append((_word_index(L, w), _field_pos(bits, u, r, e),
+                                     8 * c + 4 * e + 2 * s + r, 8 * n + a))
+    return np.array(rows, dtype=np.int64)
+
+
+def _rotl(x, s):
+    x = x.astype(np.uint64)
+    s = np.asarray(s, dtype=np.uint64)
+    return ((x << s) | (x >> ((np.uint64(32) - s) % np.uint64(32)))) & np.uint64(0xFFFFFFFF)
+
+
+def _pack(code: np.ndarray, bits: int, fields) -> np.ndarray:
+    """Logical codes uint8 [B,H,T,d] -> words uint32 [B,H,T/32,d*b]."""
     B, H, T, d = code.shape
-    per = 32 // bits
-    W = d // per
-    c = code.reshape(B, H, T // GROUP, GROUP, W, per).astype(np.uint32)
-    words = np.zeros((B, H, T // GROUP, GROUP, W), np.uint32)
-    for j in range(per):
-        words |= c[..., j] << np.uint32(bits * j)
-    return np.ascontiguousarray(words.transpose(0, 1, 2, 4, 3))
+    c = code.reshape(B, H, T // GROUP, GROUP, d)
+    order = np.argsort(fields[:, 0], kind="stable")          # group fields by word
+    f = fields[order]
+    vals = c[..., f[:, 2], f[:, 3]]                          # [B,H,NG,F]
+    placed = _rotl(vals, f[:, 1])
+    n_words = d * bits
+    per = f.shape[0] // n_words
+    words = np.bitwise_or.reduce(placed.reshape(B, H, T // GROUP, n_words, per), axis=-1)
+    return words.astype(np.uint32)
 
 
-def unpack_codes(words: np.ndarray, bits: int, d: int) -> np.ndarray:
-    """Words uint32 [B,H,T/32,W,32] -> logical codes uint8 [B,H,T,d]."""
-    B, H, NG, W, _ = words.shape
-    per = 32 // bits
-    assert W * per == d
-    w = words.transpose(0, 1, 2, 4, 3)                 # [B,H,NG,32,W]
-    mask = np.uint32((1 << bits) - 1)
-    parts = [((w >> np.uint32(bits * j)) & mask) for j in range(per)]
-    c = np.stack(parts, axis=-1)                       # [B,H,NG,32,W,per]
-    return c.reshape(B, H, NG * GROUP, d).astype(np.uint8)
+def _unpack(words: np.ndarray, bits: int, d: int, fields) -> np.ndarray:
+    B, H, NG, n_words = words.shape
+    assert n_words == d * bits
+    w = words[..., fields[:, 0]].astype(np.uint64)           # [B,H,NG,F]
+    s = fields[:, 1].astype(np.uint64)
+    rot = ((w >> s) | (w << ((np.uint64(32) - s) % np.uint64(32)))) & np.uint64(0xFFFFFFFF)
+    vals = (rot & np.uint64((1 << bits) - 1)).astype(np.uint8)
+    code = np.zeros((B, H, NG, GROUP, d), np.uint8)
+    code[..., fields[:, 2], fields[:, 3]] = vals
+    return code.reshape(B, H, NG * GROUP, d)
+
+
+def pack_kcodes(code, bits: int):
+    """K codes uint8 [B,H,T,d] -> words uint32 [B,H,T/32,d*b]."""
+    return _pack(code, bits, _k_fields(code.shape[-1], bits))
+
+
+def unpack_kcodes(words, bits: int, d: int):
+    return _unpack(words, bits, d, _k_fields(d, bits))
+
+
+def pack_vcodes(code, bits: int):
+    """V codes uint8 [B,H,T,d] -> words uint32 [B,H,T/32,d*b]."""
+    return _pack(code, bits, _v_fields(code.shape[-1], bits))
+
+
+def unpack_vcodes(words, bits: int, d: int):
+    return _unpack(words, bits, d, _v_fields(d, bits))
 
 
 def pack_kmeta(kscale, kzero):
-    """fp16 [B,H,T/32,d] x2 -> fp16 [B,H,T/32,d,2]."""
-    return np.ascontiguousarray(np.stack([kscale, kzero], axis=-1))
+    """fp16 [B,H,T/32,d] x2 -> fp16 [B,H,T/32,2,d] (scales, then zeros)."""
+    return np.ascontiguousarray(np.stack([kscale, kzero], axis=-2))
+
+
+def unpack_kmeta(ksz):
+    return ksz[..., 0, :], ksz[..., 1, :]
+
+
+def _vmeta_token_of_entry():
+    """Entry p = 8c + 4s + 2r + e of a 32-entry row holds token 8c + 4e + 2s + r."""
+    p = np.arange(GROUP)
+    c, s, r, e = p // 8, (p // 4) % 2, (p // 2) % 2, p % 2
+    return 8 * c + 4 * e + 2 * s + r
 
 
 def pack_vmeta(vscale, vzero):
-    """fp16 [B,H,T,d/32] x2 -> fp16 [B,H,T/32,d/32,32,2]."""
+    """fp16 [B,H,T,d/32] x2 -> fp16 [B,H,T/32,d/32,2,32]."""
     B, H, T, NC = vscale.shape
     m = np.stack([vscale, vzero], axis=-1).reshape(B, H, T // GROUP, GROUP, NC, 2)
-    return np.ascontiguousarray(m.transpose(0, 1, 2, 4, 3, 5))
+    m = m.transpose(0, 1, 2, 4, 5, 3)                        # [B,H,NG,NC,2,32 tokens]
+    return np.ascontiguousarray(m[..., _vmeta_token_of_entry()])
 
 
 def unpack_vmeta(vsz):
-    """fp16 [B,H,T/32,d/32,32,2] -> (scale, zero) fp16 [B,H,T,d/32]."""
+    """fp16 [B,H,T/32,d/32,2,32] -> (scale, zero) fp16 [B,H,T,d/32]."""
     B, H, NG, NC, _, _ = vsz.shape
-    m = vsz.transpose(0, 1, 2, 4, 3, 5).reshape(B, H, NG * GROUP, NC, 2)
+    m = np.empty_like(vsz)
+    m[..., _vmeta_token_of_entry()] = vsz                    # back to token order
+    m = m.transpose(0, 1, 2, 5, 3, 4).reshape(B, H, NG * GROUP, NC, 2)
     return m[..., 0], m[..., 1]
 
 
 def quant_pack(K, V, bits: int):
     """bf16 K/V [B,Hkv,T,d] -> packed (kc, ksz, vc, vsz) in the library layout."""
     kcode, ks, kz, vcode, vs, vz = quantize_kv(K, V, bits)
-    return (pack_codes(kcode, bits), pack_kmeta(ks, kz),
-            pack_codes(vcode, bits), pack_vmeta(vs, vz))
+    return (pack_kcodes(kcode, bits), pack_kmeta(ks, kz),
+            pack_vcodes(vcode, bits), pack_vmeta(vs, vz))
 
 
 def unpack_dequant(kc, ksz, vc, vsz, bits: int, d: int, T: int | None = None):
     """Packed cache -> fp32 K^, V^ [B,Hkv,T,d] (first T tokens)."""
-    kcode = unpack_codes(kc, bits, d)
-    vcode = unpack_codes(vc, bits, d)
-    ks, kz = ksz[..., 0], ksz[..., 1]
+    kcode = unpack_kcodes(kc, bits, d)
+    vcode = unpack_vcodes(vc, bits, d)
+    ks, kz = unpack_kmeta(ksz)
     vs, vz = unpack_vmeta(vsz)
     Kh, Vh = dequantize_kv(kcode, ks, kz, vcode, vs, vz)
     if T is not None:

@@ -86,47 +86,107 @@ def test_grouping_axes():
     assert np.all(ks2 > 0)
 
 
-def test_packed_word_by_hand():
-    """d=32, b=4: token t, channel c has code c % 16.  Word w of a token holds
-    channels 8w..8w+7, code j at bits 4j..4j+3: w=0 -> 0x76543210, w=1 ->
-    0xFEDCBA98, w=2 -> 0x76543210, w=3 -> 0xFEDCBA98."""
-    code = np.broadcast_to((np.arange(32) % 16).astype(np.uint8), (1, 1, 64, 32)).copy()
-    words = kivi.pack_codes(code, 4)
-    assert words.shape == (1, 1, 2, 4, 32)
-    assert np.all(words[0, 0, :, 0, :] == 0x76543210)
-    assert np.all(words[0, 0, :, 1, :] == 0xFEDCBA98)
-    assert np.all(words[0, 0, :, 2, :] == 0x76543210)
-    # b=2: channel c code c % 4 -> 16 codes per word: 0b11100100 repeated = 0xE4E4E4E4
-    code2 = np.broadcast_to((np.arange(32) % 4).astype(np.uint8), (1, 1, 32, 32)).copy()
-    assert np.all(kivi.pack_codes(code2, 2) == 0xE4E4E4E4)
-    # the word index runs over tokens fastest: token t lands in lane t
-    code3 = np.zeros((1, 1, 32, 32), np.uint8)
-    code3[0, 0, 5, 9] = 3                                  # token 5, channel 9 (word 1 at b=4, j=1)
-    w3 = kivi.pack_codes(code3, 4)
-    assert w3[0, 0, 0, 1, 5] == 3 << 4 and np.count_nonzero(w3) == 1
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("d", [64, 128])
+def test_field_tables_are_bijections(bits, d):
+    """Every (token, channel) of a group has one field, and the fields of each
+    word tile its 32 bits exactly once."""
+    for fields in (kivi._k_fields(d, bits), kivi._v_fields(d, bits)):
+        assert fields.shape == (32 * d, 4)
+        tc = fields[:, 2] * d + fields[:, 3]
+        assert np.array_equal(np.sort(tc), np.arange(32 * d))
+        cover = np.zeros((d * bits, 32), np.int64)
+        for w, p in zip(fields[:, 0], fields[:, 1]):
+            for k in range(bits):
+                cover[w, (p + k) % 32] += 1
+        assert np.all(cover == 1)
+
+
+def _const_words(pack, code_fn, bits, d):
+    t = np.arange(32)[:, None]
+    c = np.arange(d)[None, :]
+    code = np.broadcast_to(code_fn(t, c), (32, d)).astype(np.uint8)[None, None]
+    return pack(code.copy(), bits)
+
+
+def test_packed_words_by_hand():
+    """Words worked out by hand from the field rules.
+
+    b = 2, fields (u, r, e) start at 8 - 2r + 16e + 4u (mod 32):
+      e = 1 fields: r = 0 -> 24, 28, 0, 4; r = 1 -> 22, 26, 30, 2.
+      A code of 1 in every e = 1 field -> bits {0,2,4,22,24,26,28,30} = 0x55400015.
+      r = 1 fields: 6, 10, 14, 18 (e = 0), 22, 26, 30, 2 (e = 1) -> 0x44444444.
+    For K, e is the channel's bit 0 and r its bit 1; for V, r is the token's
+    bit 0 and e its bit 2.
+    b = 4, fields (u, e) start at 6 + 16e + 4u (mod 32): the e = 1 fields cover
+      bits 22-25, 26-29, 30-31 + 0-1, 2-5, so code 15 there -> 0xFFC0003F and
+      code 1 there -> bits 22, 26, 30, 2 -> 0x44400004."""
+    for d in (64, 128):
+        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: c % 2, 2, d) == 0x55400015)
+        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: (c // 2) % 2, 2, d) == 0x44444444)
+        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: t % 2, 2, d) == 0x44444444)
+        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: (t // 4) % 2, 2, d) == 0x55400015)
+        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: 15 * (c % 2), 4, d) == 0xFFC0003F)
+        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: c % 2, 4, d) == 0x44400004)
+        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: (t // 4) % 2, 4, d) == 0x44400004)
+        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: 3 + 0 * c, 2, d) == 0xFFFFFFFF)
+
+
+def test_single_codes_land_where_the_rules_say():
+    """Three codes placed by hand (d = 128 unless noted).
+
+    K, b = 2, token 5, channel 37: a = 1, j = 1; 37 = 32*1 + 4*1 + 2*0 + 1 so
+      c = 1, k = 1, r = 0, e = 1; lane 4a + c = 5; fragment j*8 + k = 9 -> word 2,
+      u = 1; start 8 + 16 + 4 = 28; stored at (2 // 4)*128 + 4*5 + 2 = 22.
+    V, b = 2, token 13, channel 42: 13 = 8*1 + 4*1 + 2*0 + 1 so c = 1, e = 1,
+      s = 0, r = 1; 42 = 8*5 + 2 so n = 5, a = 2; lane 9; fragment 0*16 + 5 ->
+      word 1, u = 1; start 8 - 2 + 16 + 4 = 26; stored at 0 + 36 + 1 = 37.
+    K, b = 4, d = 64, token 0, channel 5: a = c = j = 0, k = 1, r = 0, e = 1;
+      index 2*(0*4 + 1) + 0 = 2 -> word 0, u = 2; start 6 + 16 + 8 = 30, so the
+      field is bits 30, 31, 0, 1: code 11 = 0b1011 -> bits 30, 31, 1 = 0xC0000002."""
+    code = np.zeros((1, 1, 32, 128), np.uint8)
+    code[0, 0, 5, 37] = 3
+    w = kivi.pack_kcodes(code, 2)[0, 0, 0]
+    assert w[22] == 0x30000000 and np.count_nonzero(w) == 1
+    code = np.zeros((1, 1, 32, 128), np.uint8)
+    code[0, 0, 13, 42] = 2
+    w = kivi.pack_vcodes(code, 2)[0, 0, 0]
+    assert w[37] == 0x08000000 and np.count_nonzero(w) == 1
+    code = np.zeros((1, 1, 32, 64), np.uint8)
+    code[0, 0, 0, 5] = 11
+    w = kivi.pack_kcodes(code, 4)[0, 0, 0]
+    assert w[0] == 0xC0000002 and np.count_nonzero(w) == 1
 
 
 @pytest.mark.parametrize("bits", [2, 4])
 def test_pack_unpack_bijection(bits):
     rng = np.random.default_rng(11)
     code = rng.integers(0, 1 << bits, size=(2, 3, 96, 128)).astype(np.uint8)
-    words = kivi.pack_codes(code, bits)
-    assert np.array_equal(kivi.unpack_codes(words, bits, 128), code)
-    # and every word is reachable: unpack then pack
-    w = rng.integers(0, 2 ** 32, size=words.shape, dtype=np.uint64).astype(np.uint32)
-    assert np.array_equal(kivi.pack_codes(kivi.unpack_codes(w, bits, 128), bits), w)
+    for pack, unpack in ((kivi.pack_kcodes, kivi.unpack_kcodes), (kivi.pack_vcodes, kivi.unpack_vcodes)):
+        words = pack(code, bits)
+        assert words.shape == (2, 3, 3, 128 * bits)
+        assert np.array_equal(unpack(words, bits, 128), code)
+        w = rng.integers(0, 2 ** 32, size=words.shape, dtype=np.uint64).astype(np.uint32)
+        assert np.array_equal(pack(unpack(w, bits, 128), bits), w)
 
 
-def test_vmeta_layout_roundtrip():
+def test_meta_layouts():
+    """V meta entry p = 8c + 4s + 2r + e holds token 8c + 4e + 2s + r: entry 5
+    (c 0, s 1, r 0, e 1) is token 6, entry 19 (c 2, s 0, r 1, e 1) is token 21.
+    K meta holds the scales of all channels, then the zeros."""
     rng = np.random.default_rng(5)
     s = rng.standard_normal((2, 2, 64, 4)).astype(np.float16)
     z = rng.standard_normal((2, 2, 64, 4)).astype(np.float16)
     m = kivi.pack_vmeta(s, z)
-    assert m.shape == (2, 2, 2, 4, 32, 2)
-    # (g, cg, t) holds token 32g+t of channel group cg
-    assert m[1, 0, 1, 3, 7, 0] == s[1, 0, 32 + 7, 3] and m[1, 0, 1, 3, 7, 1] == z[1, 0, 39, 3]
+    assert m.shape == (2, 2, 2, 4, 2, 32)
+    assert m[1, 0, 1, 3, 0, 5] == s[1, 0, 32 + 6, 3] and m[1, 0, 1, 3, 1, 5] == z[1, 0, 32 + 6, 3]
+    assert m[0, 1, 0, 2, 0, 19] == s[0, 1, 21, 2] and m[0, 1, 0, 2, 1, 19] == z[0, 1, 21, 2]
     s2, z2 = kivi.unpack_vmeta(m)
     assert np.array_equal(s2, s) and np.array_equal(z2, z)
+    ks = rng.standard_normal((1, 2, 3, 128)).astype(np.float16)
+    kz = rng.standard_normal((1, 2, 3, 128)).astype(np.float16)
+    km = kivi.pack_kmeta(ks, kz)
+    assert km.shape == (1, 2, 3, 2, 128) and km[0, 1, 2, 0, 77] == ks[0, 1, 2, 77] and km[0, 1, 2, 1, 77] == kz[0, 1, 2, 77]
 
 
 def test_quant_pack_roundtrip_and_bound_on_workload_inputs():
@@ -135,7 +195,7 @@ def test_quant_pack_roundtrip_and_bound_on_workload_inputs():
     kc, ksz, vc, vsz = kivi.quant_pack(K, V, w.bits)
     Kh, Vh = kivi.unpack_dequant(kc, ksz, vc, vsz, w.bits, w.d)
     Kf, Vf = synth.bf16_to_f32(K), synth.bf16_to_f32(V)
-    ks = np.repeat(ksz[..., 0], 32, axis=2).astype(np.float32)
+    ks = np.repeat(kivi.unpack_kmeta(ksz)[0], 32, axis=2).astype(np.float32)
     vs, _ = kivi.unpack_vmeta(vsz)
     vs = np.repeat(vs, 32, axis=3).astype(np.float32)
     assert np.all(np.abs(Kh - Kf) <= ks / 2 * 1.001 + 1e-3)
