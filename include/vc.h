@@ -89,14 +89,23 @@ const char* vc_last_error(void);
  * s == 0); dequantised x^ = fma(code, s, z) in fp32.  Keys group along 32
  * tokens of one channel, values along 32 channels of one token.
  *
- * Packed draft cache of capacity T_cap tokens (T_cap % 32 == 0),
- * W = d * bits / 32 words per token, NG = T_cap / 32:
- *   kc  uint32 [B, Hkv, NG, W, 32]  word (g, w, t): token 32g + t, channels
- *                                   w*(32/bits) + j at bits [bits*j, bits*j + bits)
- *   ksz fp16   [B, Hkv, NG, d, 2]   (scale, zero) of channel c in group g
- *   vc  uint32 [B, Hkv, NG, W, 32]  same packing for values
- *   vsz fp16   [B, Hkv, NG, d/32, 32, 2]  (scale, zero) of token 32g + t over
- *                                   channels 32cg .. 32cg + 31
+ * Packed draft cache of capacity T_cap tokens (T_cap % 32 == 0), NG = T_cap / 32
+ * groups of 32 tokens.  The bit placement is this library's own format: it
+ * follows the operand fragments of the 16x8x16 fp16 tensor-core product that
+ * reads it (two codes an operand register needs sit 16 bits apart in one word).
+ *   kc  uint32 [B, Hkv, NG, d*bits]     K codes of a group: 32 lanes x d*bits/32 words,
+ *                                       word w of lane L at (w/4)*128 + 4L + w%4
+ *   ksz fp16   [B, Hkv, NG, 2, d]       scales of the group's channels, then zeros
+ *   vc  uint32 [B, Hkv, NG, d*bits]     V codes, same word order, other field map
+ *   vsz fp16   [B, Hkv, NG, d/32, 2, 32]  per channel group: scales, then zeros,
+ *                                       entry 8c + 4s + 2r + e = token 8c + 4e + 2s + r
+ * Fields (bit 0 = least significant; a 4-bit field wraps from bit 31 to bit 0):
+ *   bits = 2: slot (u, r, e) starts at (8 - 2r + 16e + 4u) mod 32;
+ *   bits = 4: slot (u, e) starts at (6 + 16e + 4u) mod 32.
+ * Lane L = 4a + c.  K: tokens 4a + j (j < 4), channels (d/4)c + 4k + 2r + e
+ * (k < d/16), fragment i = j*(d/16) + k.  V: tokens 8c + 4e + 2s + r, channels
+ * 8n + a (n < d/8), fragment i = s*(d/8) + n.  bits = 2: word i/4, u = i%4;
+ * bits = 4: i2 = 2i + r, word i2/4, u = i2%4.
  * Bytes per token per KV head: d*bits/4 (codes) + d/4 (metadata).
  */
 
@@ -189,7 +198,12 @@ vc_status_t vc_quant_kv_device_status(uint32_t* status);
  * One launch: the packed groups of all (request, KV head) slices are split
  * evenly over a persistent grid sized to the current device (stream-K), the
  * partials are merged with a log-sum-exp rule by the last CTA of each slice.
- * fp32 accumulation.  The workspace holds the partials and one arrival
+ * The packed tokens go through fp16 tensor-core products with fp32
+ * accumulation: key scales fold into the query and value scales into the
+ * softmax weights, each fold kept as an fp16 (hi, lo) pair (~22 bits).  Range
+ * limits of those fp16 operands: |q| * key scale * 16 and 128 * value scale *
+ * 16 must stay below 65504.  G = Hq / Hkv in {1, 2, 4, 5, 8}; softmax_scale > 0.
+ * The workspace holds the partials and one arrival
  * counter per slice: it must be zero-filled before its first use, and every
  * call leaves the counters at zero again.  Its size depends on the device
  * (SM count, occupancy): query it with the same device current.  Calls that

@@ -43,12 +43,11 @@ def gpu_pack(vc, K, V, bits, T_cap=None):
 
 def to_np(packed, B, H, T_cap, d, bits):
     kc, ksz, vcc, vsz = packed
-    W = d * bits // 32
     NG = T_cap // 32
-    return (kc.cpu().numpy().view(np.uint32).reshape(B, H, NG, W, 32),
-            ksz.cpu().numpy().view(np.float16).reshape(B, H, NG, d, 2),
-            vcc.cpu().numpy().view(np.uint32).reshape(B, H, NG, W, 32),
-            vsz.cpu().numpy().view(np.float16).reshape(B, H, NG, d // 32, 32, 2))
+    return (kc.cpu().numpy().view(np.uint32).reshape(B, H, NG, d * bits),
+            ksz.cpu().numpy().view(np.float16).reshape(B, H, NG, 2, d),
+            vcc.cpu().numpy().view(np.uint32).reshape(B, H, NG, d * bits),
+            vsz.cpu().numpy().view(np.float16).reshape(B, H, NG, d // 32, 2, 32))
 
 
 def assert_packed_equal(got, want, NG=None):
@@ -87,12 +86,14 @@ def test_pack_hand_worked_groups(vc):
         Kb, Vb = synth.bf16_bits(K), synth.bf16_bits(V)
         _, packed = gpu_pack(vc, Kb, Vb, c["bits"])
         kc, ksz, vcc, vsz = to_np(packed, 1, 1, 32, d, c["bits"])
-        kcode = kivi.unpack_codes(kc, c["bits"], d)
-        vcode = kivi.unpack_codes(vcc, c["bits"], d)
+        kcode = kivi.unpack_kcodes(kc, c["bits"], d)
+        vcode = kivi.unpack_vcodes(vcc, c["bits"], d)
         assert kcode[0, 0, :, 5].tolist() == c["codes"], c["name"]
         assert vcode[0, 0, 7, 32:].tolist() == c["codes"], c["name"]
-        assert ksz[0, 0, 0, 5, 0] == np.float16(c["scale"]) and ksz[0, 0, 0, 5, 1] == np.float16(c["zero"])
-        assert vsz[0, 0, 0, 1, 7, 0] == np.float16(c["scale"]) and vsz[0, 0, 0, 1, 7, 1] == np.float16(c["zero"])
+        ks, kz = kivi.unpack_kmeta(ksz)
+        vs, vz = kivi.unpack_vmeta(vsz)
+        assert ks[0, 0, 0, 5] == np.float16(c["scale"]) and kz[0, 0, 0, 5] == np.float16(c["zero"])
+        assert vs[0, 0, 7, 1] == np.float16(c["scale"]) and vz[0, 0, 7, 1] == np.float16(c["zero"])
 
 
 @pytest.mark.parametrize("bits", [2, 4])
@@ -159,8 +160,8 @@ def test_append_matches_oracle_commit(vc, bits, k):
     for b in range(B):
         c = caches[b]
         assert pl[b] == c.packed_len and tl[b] == c.tail_k.shape[1]
-        want = (kivi.pack_codes(c.kcode, bits), kivi.pack_kmeta(c.ks, c.kz),
-                kivi.pack_codes(c.vcode, bits), kivi.pack_vmeta(c.vs, c.vz))
+        want = (kivi.pack_kcodes(c.kcode, bits), kivi.pack_kmeta(c.ks, c.kz),
+                kivi.pack_vcodes(c.vcode, bits), kivi.pack_vmeta(c.vs, c.vz))
         NG = c.packed_len // 32
         assert_packed_equal([g[b:b + 1, :, :NG] for g in got], want)
         assert np.array_equal(tk[b, :, :tl[b]], c.tail_k) and np.array_equal(tv[b, :, :tl[b]], c.tail_v)

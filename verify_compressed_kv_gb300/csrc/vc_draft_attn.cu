@@ -17,9 +17,13 @@
 //     by bulk async copies (cp.async.bulk + mbarrier transaction counts, bounded
 //     waits) while the 8 warps compute on earlier stages;
 //   * each warp owns one group per stage and keeps its own online-softmax
-//     state (max, sum) and output accumulators; QK dequantises exactly
-//     (fma(code, s, z), the quantiser's definition) with f32x2 FMAs; PV folds
-//     the per-token value scale into the softmax weight;
+//     state (max, sums) and output accumulators, all G heads of the KV head as
+//     rows of 16x8x16 tensor-core products: the packed codes become operand
+//     registers with one shift and one logic op per pair (1 + code/f is exact
+//     in fp16), the key scales fold into the query and the value scales into
+//     the softmax weights, each fold carried as an fp16 (hi, lo) pair so the
+//     products keep ~22 bits, and the zero points enter through two narrow
+//     correction products (group_mma below);
 //   * at the end of a segment the warps are merged (log-sum-exp) into one
 //     partial per query head; the last CTA to finish a (request, KV head)
 //     (arrival counter in the workspace, reset by that CTA) merges all its
@@ -35,27 +39,12 @@ namespace {
 
 __device__ uint32_t g_draft_status = 0;
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarps = 8;                       // consumer warps of a stream CTA (one group each per stage)
+constexpr int kConsumers = kWarps * 32;
+constexpr int kThreads = kConsumers + 32;        // + one producer warp
 constexpr int kGroup = 32;
-// Head split: with many heads per KV head (G = 8) two warps share a group,
-// each taking G/2 heads, so a warp's registers stay those of the G = 4 case.
-template <int G>
-struct HeadSplit {
-  static constexpr int HS = G >= 8 ? 2 : 1;   // warps per group
-  static constexpr int GW = G / HS;           // heads per warp
-  static constexpr int SG = kWarps / HS;      // groups per stage
-};
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
-#ifndef VC_DRAFT_QK_TB
-#define VC_DRAFT_QK_TB 8                           // QK tokens per lane per pass
-#endif
-
-__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
-// 2^-e as an exact float constant (0 <= e <= 30)
-__host__ __device__ constexpr float pow2neg(int e) { return 1.0f / static_cast<float>(1u << e); }
-
 struct DraftArgs {
   const uint16_t* q;        // [B, Hq, D]
   const uint16_t* k_cur;    // [B, Hkv, D] or null
@@ -107,29 +96,28 @@ __host__ __device__ inline void ctas_of(int bh, const DraftArgs& a, int& first, 
 // ------------------------------------------------------------------ shared memory plan
 template <int D, int BITS, int G>
 struct Plan {
-  static constexpr int W = D * BITS / 32;
-  static constexpr int GW = HeadSplit<G>::GW, SG = HeadSplit<G>::SG;
-  static constexpr size_t kc = static_cast<size_t>(SG) * W * kGroup * 4;
-  static constexpr size_t meta = static_cast<size_t>(SG) * D * 4;
-  static constexpr size_t stage = 2 * kc + 2 * meta;             // K codes, K meta, V codes, V meta
+  static constexpr size_t codes = static_cast<size_t>(D) * BITS * 4;   // bytes of one group's K (or V) codes
+  static constexpr size_t meta = static_cast<size_t>(D) * 4;           // bytes of one group's K (or V) meta
+  static constexpr size_t kc = kWarps * codes;                         // a stage holds kWarps groups
+  static constexpr size_t mt = kWarps * meta;
+  static constexpr size_t stage = 2 * kc + 2 * mt;                      // K codes, K meta, V codes, V meta
   // ring depth: about 72 KB of stages in flight, at least double buffering
   static constexpr int NS = (72 * 1024 / stage) < 2 ? 2 : ((72 * 1024 / stage) > 6 ? 6 : static_cast<int>(72 * 1024 / stage));
   static constexpr size_t ring = stage * NS;
-  static constexpr size_t red = static_cast<size_t>(kWarps) * GW * D * 4;  // warp merge (aliases the ring)
-  static constexpr size_t body = ring > red ? ring : red;
-  static constexpr size_t sc = static_cast<size_t>(kWarps) * GW * kGroup * 4;  // per-warp scores
-  static constexpr size_t q = static_cast<size_t>(G) * D * 4;
-  static constexpr size_t wstat = static_cast<size_t>(kWarps) * (GW > 8 ? GW : 8) * 2 * 4;  // per-warp (max, sum)
-  static constexpr size_t off_sc = body;
-  static constexpr size_t off_q = off_sc + sc;
+  static constexpr size_t red = static_cast<size_t>(kWarps) * G * D * 4;   // warp merge
+  static constexpr size_t off_red = ring;
+  static constexpr size_t body = ring + red;
+  static constexpr size_t q = static_cast<size_t>(G) * D * 4;             // tail CTA: fp32 queries
+  static constexpr size_t wstat = static_cast<size_t>(kWarps) * 8 * 2 * 4;  // per-warp (max, sum) per head
+  static constexpr size_t off_q = body;
   static constexpr size_t off_wstat = off_q + q;
-  static constexpr size_t off_bar = (off_wstat + wstat + 15) & ~size_t(15);
-  static constexpr size_t off_flag = off_bar + 8 * NS;
+  static constexpr size_t off_bar = (off_wstat + wstat + 15) & ~size_t(15);   // full[NS], empty[NS]
+  static constexpr size_t off_flag = off_bar + 16 * NS;                      // combine flag, abort flag
   static constexpr size_t total = off_flag + 16;
 };
 
 // Shared memory the tail CTA needs inside the same allocation (rows of the tail
-// K/V plus its scores); checked on the host against Plan::total.
+// K/V plus its scores); checked on the host against Plan::off_q.
 template <int D, int G>
 __host__ __device__ inline size_t tail_smem(int tail_cap) {
   return 2 * static_cast<size_t>(tail_cap + 1) * D * 2 + static_cast<size_t>(G) * (tail_cap + 1) * 4 + 64;
@@ -147,220 +135,231 @@ __device__ __forceinline__ void load_q(const DraftArgs& a, int b, int kvh, float
 template <int D, int BITS, int G>
 __device__ __forceinline__ void issue_stage(const DraftArgs& a, uint8_t* buf, uint64_t* bar, int bh, int g, int n) {
   using P = Plan<D, BITS, G>;
-  constexpr int W = P::W;
   const size_t gb = static_cast<size_t>(bh) * a.NG + g;
-  const uint32_t code_bytes = static_cast<uint32_t>(n) * W * kGroup * 4;
-  const uint32_t meta_bytes = static_cast<uint32_t>(n) * D * 4;
+  const uint32_t code_bytes = static_cast<uint32_t>(n * P::codes);
+  const uint32_t meta_bytes = static_cast<uint32_t>(n * P::meta);
   vc_mbar_arrive_expect_tx(bar, 2 * code_bytes + 2 * meta_bytes);
-  vc_bulk_g2s(buf, a.kc + gb * W * kGroup, code_bytes, bar);
-  vc_bulk_g2s(buf + P::kc, a.ksz + gb * D * 2, meta_bytes, bar);
-  vc_bulk_g2s(buf + P::kc + P::meta, a.vc + gb * W * kGroup, code_bytes, bar);
-  vc_bulk_g2s(buf + 2 * P::kc + P::meta, a.vsz + gb * D * 2, meta_bytes, bar);
+  vc_bulk_g2s(buf, a.kc + gb * D * BITS, code_bytes, bar);
+  vc_bulk_g2s(buf + P::kc, a.ksz + gb * 2 * D, meta_bytes, bar);
+  vc_bulk_g2s(buf + P::kc + P::mt, a.vc + gb * D * BITS, code_bytes, bar);
+  vc_bulk_g2s(buf + 2 * P::kc + P::mt, a.vsz + gb * 2 * D, meta_bytes, bar);
 }
 
-// ------------------------------------------------------------------ one group, one warp
-// Load N consecutive 32-bit words (N % 4 == 0) starting at `src` into out[],
-// issuing the 16-byte chunks in an order rotated by `rot`.  A word column is
-// 128 bytes, so lanes of a quarter-warp that sit in different columns would
-// otherwise hit the same bank slot; rotating by the column index spreads them.
-template <int N>
-__device__ __forceinline__ void load_words_rotated(const uint32_t* src, int rot, uint32_t (&out)[N]) {
-  constexpr int NCH = N / 4;
-  uint4 tmp[NCH];
-#pragma unroll
-  for (int k = 0; k < NCH; ++k) tmp[k] = *reinterpret_cast<const uint4*>(src + ((k + rot) % NCH) * 4);
-#pragma unroll
-  for (int c = 0; c < NCH; ++c) {
-    uint4 v = tmp[0];
-#pragma unroll
-    for (int k = 1; k < NCH; ++k)
-      if ((k + rot) % NCH == c) v = tmp[k];
-    out[4 * c] = v.x; out[4 * c + 1] = v.y; out[4 * c + 2] = v.z; out[4 * c + 3] = v.w;
+// ------------------------------------------------------------------ tensor-core pieces
+// 16x8x16 products, fp16 operands, fp32 accumulators.  Lane = 4*gid + tig.
+// A rows: gid = head gid (leading part), gid + 8 = the same head (remainder
+// part), so that hi + lo carry ~22 significant bits of a product that fp16
+// alone would round to 11.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 2^x (ex2.approx.ftz: relative error ~2^-22; results below 2^-126 flush to 0)
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// (hi, lo) of x*y: hi = fp16(x*y), lo = fp16(x*y - hi) (the residual of the
+// exact product; exact itself when x and y carry <= 22 significant bits).
+__device__ __forceinline__ void split_mul(__half2 x, __half2 y, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __hmul2(x, y);
+  hi = h2u(h);
+  lo = h2u(__hfma2(x, y, __hneg2(h)));
+}
+
+// Operand value of a packed code field: OR the field (moved to the top
+// mantissa bits) into the bit pattern of 1.0, giving 1 + code/f exactly.
+//   b = 2, r = 0: bits 8-9 of each half -> 1 + code/4   (f = 4)
+//   b = 2, r = 1: bits 6-7              -> 1 + code/16  (f = 16)
+//   b = 4:        bits 6-9              -> 1 + code/16  (f = 16)
+template <int BITS>
+__device__ __forceinline__ uint32_t field_value(uint32_t x, int r) {
+  if (BITS == 2) return r == 0 ? ((x & 0x03000300u) | 0x3C003C00u) : ((x & 0x00C000C0u) | 0x3C003C00u);
+  return (x & 0x03C003C0u) | 0x3C003C00u;
+}
+template <int BITS>
+__host__ __device__ constexpr float field_scale(int r) { return (BITS == 2 && r == 0) ? 4.0f : 16.0f; }
+template <int BITS>
+__host__ __device__ constexpr float field_log2(int r) { return (BITS == 2 && r == 0) ? 2.0f : 4.0f; }
+
+// Operand register r of fragment (word set w[], fragment index i) — the
+// field rules of the packed words (include/vc.h): b = 2: word i/4 rotated by
+// 4*(i%4); b = 4: i2 = 2i + r, word i2/4 rotated by 4*(i2%4).
+template <int BITS, int WPL>
+__device__ __forceinline__ void fragment(const uint32_t (&w)[WPL], int i, uint32_t& b0, uint32_t& b1) {
+  if (BITS == 2) {
+    const uint32_t x = (i % 4) ? __funnelshift_r(w[i / 4], w[i / 4], 4 * (i % 4)) : w[i / 4];
+    b0 = field_value<2>(x, 0);
+    b1 = field_value<2>(x, 1);
+  } else {
+    const int i0 = 2 * i, i1 = 2 * i + 1;
+    const uint32_t x0 = (i0 % 4) ? __funnelshift_r(w[i0 / 4], w[i0 / 4], 4 * (i0 % 4)) : w[i0 / 4];
+    const uint32_t x1 = __funnelshift_r(w[i1 / 4], w[i1 / 4], 4 * (i1 % 4));
+    b0 = field_value<4>(x0, 0);
+    b1 = field_value<4>(x1, 1);
   }
 }
 
-// Lane layout for QK: lane = w * TS + ts holds word column w (CPW channels) of
-// TPL = W tokens (rows ts * W .. ts * W + W - 1 of the group), TS = 32 / W.
-//
-// Code j of a word sits at bits [BITS*j, BITS*j + BITS); channels j < HALF
-// come from the low 16 bits, the rest from the high 16 bits.  OR-ing the
-// masked code (still at position BITS*jj) into the mantissa of 2^23 and
-// subtracting 2^23 gives code * 2^(BITS*jj) exactly; folding 2^(-BITS*jj) into
-// the channel's fp32 scale makes fma(code * 2^(BITS*jj), s * 2^(-BITS*jj), z)
-// bit-identical to fma(code, s, z).  Channel pairs go through f32x2 FMAs.
-template <int D, int BITS, int G>
-__device__ __forceinline__ void qk_group(const uint32_t* kc_g, const uint16_t* ksz_g, const float* q_s,
-                                         float* sc, int lane) {
-  constexpr int W = D * BITS / 32, CPW = 32 / BITS, HALF = CPW / 2, TPL = W;
-  constexpr uint32_t MASK = (1u << BITS) - 1u;
-  constexpr int TB = TPL < VC_DRAFT_QK_TB ? TPL : VC_DRAFT_QK_TB, NTB = TPL / TB;
-  constexpr int LOGW = ilog2(W), LOGTB = ilog2(TB);
-  constexpr int HB = (2 * G * TB <= 80) ? G : (G + 1) / 2;     // heads per pass (register budget)
-  constexpr int NHB = (G + HB - 1) / HB;
-  static_assert(LOGTB <= LOGW, "token block wider than the word row");
-  constexpr int TS = 32 / W;
-  const int w = lane / TS, ts = lane % TS;
-  uint32_t lo[TPL], hi[TPL];
-  load_words_rotated<TPL>(kc_g + w * kGroup + ts * TPL, w, lo);
+// The lane's words of one group: word w at (w/4)*128 + 4*lane + w%4.
+template <int WPL>
+__device__ __forceinline__ void load_lane_words(const uint32_t* g, int lane, uint32_t (&w)[WPL]) {
 #pragma unroll
-  for (int tl = 0; tl < TPL; ++tl) hi[tl] = lo[tl] >> 16;
-  const uint16_t* kmeta = ksz_g + w * CPW * 2;                    // the lane's CPW (s, z) pairs
-#pragma unroll
-  for (int tb = 0; tb < NTB; ++tb) {
-#pragma unroll
-    for (int hb = 0; hb < NHB; ++hb) {
-      float2 acc[HB][TB];
-#pragma unroll
-      for (int h = 0; h < HB; ++h)
-#pragma unroll
-        for (int tl = 0; tl < TB; ++tl) acc[h][tl] = make_float2(0.0f, 0.0f);
-#pragma unroll
-      for (int cp = 0; cp < CPW / 2; ++cp) {
-        const int j0 = 2 * cp;
-        const bool upper = j0 >= HALF;
-        const int jj = j0 % HALF;
-        const uint32_t m0 = MASK << (BITS * jj), m1 = MASK << (BITS * (jj + 1));
-        const uint2 raw = *reinterpret_cast<const uint2*>(kmeta + j0 * 2);
-        const float2 sz0 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-        const float2 sz1 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-        const float2 s2 = make_float2(sz0.x * pow2neg(BITS * jj), sz1.x * pow2neg(BITS * (jj + 1)));
-        const float2 z2 = make_float2(sz0.y, sz1.y);
-        float2 q2[HB];
-#pragma unroll
-        for (int h = 0; h < HB; ++h)
-          q2[h] = (hb * HB + h < G) ? *reinterpret_cast<const float2*>(q_s + (hb * HB + h) * D + w * CPW + j0)
-                                    : make_float2(0.0f, 0.0f);
-#pragma unroll
-        for (int tl = 0; tl < TB; ++tl) {
-          const uint32_t src = upper ? hi[tb * TB + tl] : lo[tb * TB + tl];
-          float2 f = make_float2(__uint_as_float(0x4B000000u | (src & m0)),
-                                 __uint_as_float(0x4B000000u | (src & m1)));
-          f = __fadd2_rn(f, make_float2(-8388608.0f, -8388608.0f));
-          const float2 k2 = __ffma2_rn(f, s2, z2);
-#pragma unroll
-          for (int h = 0; h < HB; ++h) acc[h][tl] = __ffma2_rn(q2[h], k2, acc[h][tl]);
-        }
-      }
-      float part[HB][TB];
-#pragma unroll
-      for (int h = 0; h < HB; ++h)
-#pragma unroll
-        for (int tl = 0; tl < TB; ++tl) part[h][tl] = acc[h][tl].x + acc[h][tl].y;
-      // fold the W lanes of the token row: recursive halving over the TB token
-      // slots, then an all-reduce over the remaining lane bits
-#pragma unroll
-      for (int step = 0; step < LOGW; ++step) {
-        const int o = W >> (step + 1);                    // bit of w; lanes differ by o * TS
-        if (step < LOGTB) {
-          const int half = TB >> (step + 1);
-          const bool up = (w & o) != 0;
-#pragma unroll
-          for (int i = 0; i < TB / 2; ++i) {
-            if (i < half) {
-#pragma unroll
-              for (int h = 0; h < HB; ++h) {
-                const float send = up ? part[h][i] : part[h][i + half];
-                const float keep = up ? part[h][i + half] : part[h][i];
-                part[h][i] = keep + __shfl_xor_sync(0xffffffffu, send, o * TS);
-              }
-            }
-          }
-        } else {
-#pragma unroll
-          for (int h = 0; h < HB; ++h) part[h][0] += __shfl_xor_sync(0xffffffffu, part[h][0], o * TS);
-        }
-      }
-      if ((w & ((1 << (LOGW - LOGTB)) - 1)) == 0) {
-        const int t = ts * TPL + tb * TB + (w >> (LOGW - LOGTB));
-#pragma unroll
-        for (int h = 0; h < HB; ++h)
-          if (hb * HB + h < G) sc[(hb * HB + h) * kGroup + t] = part[h][0];
-      }
-    }
+  for (int c = 0; c < WPL / 4; ++c) {
+    const uint4 v = *reinterpret_cast<const uint4*>(g + c * 128 + 4 * lane);
+    w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
   }
 }
 
-// Warp-level online softmax over one group's 32 scores per head (sc[h][t],
-// log2 units): running max m (warp-uniform), per-lane partial sums l, the
-// rescale factor of the earlier accumulators, and p written back over sc.
-template <int G>
-__device__ __forceinline__ bool softmax_group(float* sc, float (&m)[G], float (&l)[G], float (&alpha)[G], int lane) {
-  bool rescale = false;
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const float s = sc[h * kGroup + lane];
-    float gm = s;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, off));
-    const float mn = fmaxf(m[h], gm);
-    alpha[h] = exp2f(m[h] - mn);          // m = -inf at the start: alpha = 0, nothing to keep
-    rescale |= (alpha[h] != 1.0f);
-    const float p = exp2f(s - mn);
-    sc[h * kGroup + lane] = p;
-    l[h] = fmaf(l[h], alpha[h], p);
-    m[h] = mn;
-  }
-  return rescale;
-}
-
-// PV lane layout: SUB lanes share a word (SUB = 2 halves the per-lane channels
-// when G is large); lane = wr * TSR + tsr with WR = W * SUB lanes per token row.
-template <int D, int BITS, int G>
-struct PvLayout {
-  static constexpr int W = D * BITS / 32, CPW = 32 / BITS, HALF = CPW / 2;
-  static constexpr int SUB = (G * CPW > 64) ? 2 : 1;
-  static constexpr int CPL = CPW / SUB;        // channels per lane
-  static constexpr int WR = W * SUB;           // lanes per token row
-  static constexpr int TSR = 32 / WR;          // token rows per warp
-  static constexpr int TPLR = WR;              // tokens per lane per group
-  static_assert(SUB == 1 || CPL == HALF, "a lane's channels lie in one half word");
-  static_assert(TSR >= 1 && TPLR % 4 == 0, "lane layout");
+// Per-warp running state of one segment: rows = the lane's head gid.
+template <int D>
+struct WarpState {
+  static constexpr int NT = D / 8;
+  float o[NT][4];       // PV accumulators: cols 8nt + 2tig (+1), rows gid / gid+8
+  float oz[4];          // correction columns (2g: zeros, 2g+1: scales) of group g = tig
+  float l0, l1;         // sums of the softmax weights of r = 0 / r = 1 tokens (times f_r)
+  float m;              // running max (log2 units) the weights are relative to
 };
 
-// sum_t p_t (c_t s_t + z_t) = sum_t (p_t s_t) c_t + sum_t p_t z_t: raw codes
-// (times 2^(BITS*jj), undone at the end) accumulate against p_t s_t.
-template <int D, int BITS, int G>
-__device__ __forceinline__ void pv_group(const uint32_t* vc_g, const uint16_t* vsz_g, const float* sc,
-                                         float2 (&acc)[G][PvLayout<D, BITS, G>::CPL / 2], float (&zacc)[G],
-                                         int lane) {
-  using L = PvLayout<D, BITS, G>;
-  constexpr uint32_t MASK = (1u << BITS) - 1u;
-  const int wr = lane / L::TSR, tsr = lane % L::TSR;
-  const int w = wr / L::SUB, sub = wr % L::SUB;
-  const int cgrp = (w * L::CPW) / kGroup;
-  uint32_t wv[L::TPLR];
-  load_words_rotated<L::TPLR>(vc_g + w * kGroup + tsr * L::TPLR, w, wv);
+// Rescale threshold (log2 units): the running max is raised only when a group's
+// max exceeds it by more than this, so weights stay <= 2^kLazy * 16.
+constexpr float kLazy = 3.0f;
+
+// One group of 32 tokens for the lane's head (row gid), all on tensor cores.
+//
+//   score(t) = sum_c q_c (s_c code_tc + z_c)
+//            = sum_c (f_c q_c s_c)(1 + code_tc / f_c) + sum_c q_c (z_c - f_c s_c)
+// The first sum is one product per n-tile with A = f q s split into (hi, lo)
+// fp16 rows and B = the codes' operand values; the second ("bias") is one
+// product per k-step with A = f q (exact in fp16) and B columns z / f and -s.
+//   out_h = sum_t p_t (sv_t code_tc + zv_t)
+//         = sum_t (f_t p_t sv_t)(1 + code_tc / f_t) + sum_t (f_t p_t)(zv_t / f_t - sv_t)
+// likewise with one A per channel group (sv depends on the group) and one
+// correction product whose columns are (zv / f, -sv) per channel group.
+template <int D, int BITS>
+__device__ __forceinline__ void group_mma(const uint32_t* kc_g, const uint16_t* ksz_g, const uint32_t* vc_g,
+                                          const uint16_t* vsz_g, const uint32_t (&qf)[D / 16][2],
+                                          uint32_t bias_mul0, uint32_t bias_mul1,
+                                          uint32_t zcol_mul0, uint32_t zcol_mul1, int zcol_off, float cs,
+                                          WarpState<D>& st, int lane) {
+  constexpr int KS = D / 16, NT = D / 8, NCG = D / 32, WPL = D * BITS / 32;
+  const int gid = lane >> 2, tig = lane & 3;
+  // ---------------- QK
+  uint32_t kw[WPL];
+  load_lane_words<WPL>(kc_g, lane, kw);
+  // scales of the lane's channels (D/4) tig + 4ks + 2r + {0, 1}: one half2 per (ks, r)
+  const uint32_t* srow = reinterpret_cast<const uint32_t*>(ksz_g) + (D / 8) * tig;
+  const uint32_t* zrow = reinterpret_cast<const uint32_t*>(ksz_g) + (gid == 0 ? D / 2 : 0) + (D / 8) * tig;
+  float c[4][4];
 #pragma unroll
-  for (int tl = 0; tl < L::TPLR; ++tl) {
-    const int t = tsr * L::TPLR + tl;
-    const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(vsz_g + (cgrp * kGroup + t) * 2));
-    float2 w2[G];
+  for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
+  float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float p = sc[h * kGroup + t];
-      const float wgt = p * sz.x;
-      w2[h] = make_float2(wgt, wgt);
-      zacc[h] = fmaf(p, sz.y, zacc[h]);
-    }
-    const uint32_t lo = wv[tl], hi = lo >> 16;
+  for (int kq = 0; kq < KS / 2; ++kq) {
+    const uint4 s4 = *reinterpret_cast<const uint4*>(srow + 4 * kq);     // (ks, r) = (2kq, 0), (2kq, 1), (2kq+1, 0), (2kq+1, 1)
+    const uint4 z4 = *reinterpret_cast<const uint4*>(zrow + 4 * kq);
+    const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
+    const uint32_t zv[4] = {z4.x, z4.y, z4.z, z4.w};
 #pragma unroll
-    for (int jp = 0; jp < L::CPL / 2; ++jp) {
-      // lane channel j = sub * CPL + 2 jp (+1); with SUB == 2 a lane owns one half word
-      const int jl = 2 * jp;
-      uint32_t src;
-      int jj;
-      if (L::SUB == 1) {
-        src = (jl >= L::HALF) ? hi : lo;
-        jj = jl % L::HALF;
-      } else {
-        src = sub ? hi : lo;
-        jj = jl;
+    for (int h = 0; h < 2; ++h) {
+      const int ks = 2 * kq + h;
+      uint32_t a0, a1, a2, a3;
+      split_mul(u2h(qf[ks][0]), u2h(sv[2 * h]), a0, a1);
+      split_mul(u2h(qf[ks][1]), u2h(sv[2 * h + 1]), a2, a3);
+      mma16816(cb, qf[ks][0], 0u, qf[ks][1], 0u, h2u(__hmul2(u2h(zv[2 * h]), u2h(bias_mul0))),
+               h2u(__hmul2(u2h(zv[2 * h + 1]), u2h(bias_mul1))));
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t b0, b1;
+        fragment<BITS, WPL>(kw, j * KS + ks, b0, b1);
+        mma16816(c[j], a0, a1, a2, a3, b0, b1);
       }
-      float2 f = make_float2(__uint_as_float(0x4B000000u | (src & (MASK << (BITS * jj)))),
-                             __uint_as_float(0x4B000000u | (src & (MASK << (BITS * (jj + 1))))));
-      f = __fadd2_rn(f, make_float2(-8388608.0f, -8388608.0f));
+    }
+  }
+  // bias of row gid: columns 0 (q.z) and 1 (-q.f s) live in the quad's tig 0 lane
+  const float bias = __shfl_sync(0xffffffffu, cb[0] + cb[1], lane & ~3);
+  // ---------------- online softmax (row gid; tokens 8 tig + 4e + j)
+  float y[4][2];
+  float my = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < G; ++h) acc[h][jp] = __ffma2_rn(w2[h], f, acc[h][jp]);
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      y[j][e] = c[j][e] + c[j][2 + e];
+      my = fmaxf(my, y[j][e]);
+    }
+  my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 1));
+  my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 2));
+  const float mx = (my + bias) * cs;
+  const bool need = !(mx <= st.m + kLazy);
+  if (__any_sync(0xffffffffu, need)) {
+    const float mn = need ? mx : st.m;
+    const float alpha = fast_exp2(st.m - mn);          // m = -inf at the start: alpha = 0
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) st.o[nt][k] *= alpha;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) st.oz[k] *= alpha;
+    st.l0 *= alpha;
+    st.l1 *= alpha;
+    st.m = mn;
+  }
+  const float k0 = fmaf(bias, cs, -st.m);
+  // weights times f_r (r = j % 2), split into fp16 (hi, lo)
+  uint32_t ph[4], pl[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float kk = k0 + field_log2<BITS>(j & 1);
+    const float p0 = fast_exp2(fmaf(y[j][0], cs, kk));
+    const float p1 = fast_exp2(fmaf(y[j][1], cs, kk));
+    if (j & 1) st.l1 += p0 + p1; else st.l0 += p0 + p1;
+    const __half2 h = __floats2half2_rn(p0, p1);
+    const float2 hf = __half22float2(h);
+    ph[j] = h2u(h);
+    pl[j] = h2u(__floats2half2_rn(p0 - hf.x, p1 - hf.y));
+  }
+  // ---------------- PV
+  uint32_t vw[WPL];
+  load_lane_words<WPL>(vc_g, lane, vw);
+  // correction columns: lane gid feeds column gid = (group gid/2, zeros | scales)
+  {
+    const uint4 r4 = *reinterpret_cast<const uint4*>(vsz_g + zcol_off + 8 * tig);
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const uint32_t b0 = h2u(__hmul2(u2h(s ? r4.z : r4.x), u2h(zcol_mul0)));
+      const uint32_t b1 = h2u(__hmul2(u2h(s ? r4.w : r4.y), u2h(zcol_mul1)));
+      mma16816(st.oz, ph[2 * s], pl[2 * s], ph[2 * s + 1], pl[2 * s + 1], b0, b1);
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < NCG; ++g) {
+    const uint4 s4 = *reinterpret_cast<const uint4*>(vsz_g + g * 64 + 8 * tig);   // (s, r) = (0,0), (0,1), (1,0), (1,1)
+    const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      uint32_t a[4];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const __half2 x = u2h(ph[2 * s + r]), sc = u2h(sv[2 * s + r]);
+        const __half2 h = __hmul2(x, sc);
+        a[2 * r] = h2u(h);
+        a[2 * r + 1] = h2u(__hfma2(u2h(pl[2 * s + r]), sc, __hfma2(x, sc, __hneg2(h))));
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int nt = 4 * g + u;
+        uint32_t b0, b1;
+        fragment<BITS, WPL>(vw, s * NT + nt, b0, b1);
+        mma16816(st.o[nt], a[0], a[1], a[2], a[3], b0, b1);
+      }
     }
   }
 }
@@ -369,64 +368,41 @@ __device__ __forceinline__ void pv_group(const uint32_t* vc_g, const uint16_t* v
 // Partial of this CTA for slice bh: merge the warps' (max, sum, output) in
 // shared memory and write one normalised partial + log2-sum-exp per head.
 template <int D, int BITS, int G>
-__device__ void write_partial(const DraftArgs& a, uint8_t* smem, int bh, int slot,
-                              float (&m)[HeadSplit<G>::GW], float (&l)[HeadSplit<G>::GW],
-                              float2 (&acc)[HeadSplit<G>::GW][PvLayout<D, BITS, HeadSplit<G>::GW>::CPL / 2],
-                              float (&zacc)[HeadSplit<G>::GW]) {
+__device__ void write_partial(const DraftArgs& a, uint8_t* smem, int bh, int slot, WarpState<D>& st) {
   using P = Plan<D, BITS, G>;
-  constexpr int GW = HeadSplit<G>::GW, HS = HeadSplit<G>::HS;
-  using L = PvLayout<D, BITS, GW>;
+  constexpr int NT = D / 8, NCG = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* red = reinterpret_cast<float*>(smem);                          // [warp][GW][D], aliases the ring
-  float* wstat = reinterpret_cast<float*>(smem + P::off_wstat);         // [warp][GW][2]
-  const int wr = lane / L::TSR, tsr = lane % L::TSR;
-  const int w = wr / L::SUB, sub = wr % L::SUB;
-  // fold the token rows of the PV layout (the low lane bits)
+  const int gid = lane >> 2, tig = lane & 3;
+  float* red = reinterpret_cast<float*>(smem + P::off_red);             // [warp][G][D]
+  float* wstat = reinterpret_cast<float*>(smem + P::off_wstat);         // [warp][8][2]
+  // correction of channel group g for row gid sits in lane (gid, g)
+  const float ozl = st.oz[0] + st.oz[1] + st.oz[2] + st.oz[3];
+  float ozg[NCG];
 #pragma unroll
-  for (int o = 1; o < L::TSR; o <<= 1)
+  for (int g = 0; g < NCG; ++g) ozg[g] = __shfl_sync(0xffffffffu, ozl, (lane & ~3) | g);
+  float l = st.l0 * (1.0f / field_scale<BITS>(0)) + st.l1 * (1.0f / field_scale<BITS>(1));
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  if (gid < G) {
 #pragma unroll
-    for (int h = 0; h < GW; ++h) {
-      zacc[h] += __shfl_xor_sync(0xffffffffu, zacc[h], o);
-#pragma unroll
-      for (int jp = 0; jp < L::CPL / 2; ++jp) {
-        acc[h][jp].x += __shfl_xor_sync(0xffffffffu, acc[h][jp].x, o);
-        acc[h][jp].y += __shfl_xor_sync(0xffffffffu, acc[h][jp].y, o);
-      }
+    for (int nt = 0; nt < NT; ++nt) {
+      float2 v;
+      v.x = st.o[nt][0] + st.o[nt][2] + ozg[nt / 4];
+      v.y = st.o[nt][1] + st.o[nt][3] + ozg[nt / 4];
+      *reinterpret_cast<float2*>(red + (warp * G + gid) * D + 8 * nt + 2 * tig) = v;
     }
-#pragma unroll
-  for (int h = 0; h < GW; ++h) {
-    float s = l[h];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    l[h] = s;
-  }
-  __syncthreads();                                 // every warp is done with the ring
-  if (tsr == 0) {
-#pragma unroll
-    for (int h = 0; h < GW; ++h)
-#pragma unroll
-      for (int jp = 0; jp < L::CPL / 2; ++jp) {
-        const int jl = 2 * jp;
-        const int jj = (L::SUB == 1) ? (jl % L::HALF) : jl;
-        float* dst = red + (warp * GW + h) * D + w * L::CPW + sub * L::CPL + jl;
-        dst[0] = fmaf(acc[h][jp].x, pow2neg(BITS * jj), zacc[h]);
-        dst[1] = fmaf(acc[h][jp].y, pow2neg(BITS * (jj + 1)), zacc[h]);
-      }
-  }
-  if (lane == 0)
-#pragma unroll
-    for (int h = 0; h < GW; ++h) {
-      wstat[(warp * GW + h) * 2] = m[h];
-      wstat[(warp * GW + h) * 2 + 1] = l[h];
+    if (tig == 0) {
+      wstat[(warp * 8 + gid) * 2] = st.m;
+      wstat[(warp * 8 + gid) * 2 + 1] = l;
     }
-  __syncthreads();
+  }
+  vc_bar_sync(1, kConsumers);
   const int b = bh / a.Hkv, kvh = bh % a.Hkv;
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+  for (int i = threadIdx.x; i < G * D; i += kConsumers) {
     const int h = i / D, c = i % D;
-    const int half = h / GW, hl = h % GW;             // warps x with x % HS == half hold head h
     float M = -INFINITY;
 #pragma unroll
-    for (int x = half; x < kWarps; x += HS) M = fmaxf(M, wstat[(x * GW + hl) * 2]);
+    for (int x = 0; x < kWarps; ++x) M = fmaxf(M, wstat[(x * 8 + h) * 2]);
     const size_t row = static_cast<size_t>(b * a.Hq + kvh * G + h) * a.max_parts + slot;
     if (M == -INFINITY) {
       if (c == 0) a.part_lse[row] = -INFINITY;
@@ -434,12 +410,12 @@ __device__ void write_partial(const DraftArgs& a, uint8_t* smem, int bh, int slo
     }
     float o = 0.0f, Ls = 0.0f;
 #pragma unroll
-    for (int x = half; x < kWarps; x += HS) {
-      const float mx = wstat[(x * GW + hl) * 2];
+    for (int x = 0; x < kWarps; ++x) {
+      const float mx = wstat[(x * 8 + h) * 2];
       if (mx == -INFINITY) continue;
       const float wgt = exp2f(mx - M);
-      o = fmaf(wgt, red[(x * GW + hl) * D + c], o);
-      Ls = fmaf(wgt, wstat[(x * GW + hl) * 2 + 1], Ls);
+      o = fmaf(wgt, red[(x * G + h) * D + c], o);
+      Ls = fmaf(wgt, wstat[(x * 8 + h) * 2 + 1], Ls);
     }
     a.part_o[row * D + c] = o / Ls;
     if (c == 0) a.part_lse[row] = M + log2f(Ls);
@@ -448,19 +424,25 @@ __device__ void write_partial(const DraftArgs& a, uint8_t* smem, int bh, int slo
 
 // Count this CTA's partial for slice bh; the last of the n_parts arrivals
 // merges all partials of the slice and writes its bf16 output.
+// `nthr` threads take part: the consumer warps of a stream CTA (named barrier
+// 1) or the whole tail CTA.
+__device__ __forceinline__ void sync_part(int nthr) {
+  if (nthr == kConsumers) vc_bar_sync(1, kConsumers); else __syncthreads();
+}
+
 template <int G, int D>
-__device__ void arrive_and_combine(const DraftArgs& a, unsigned int* flag, int bh, int n_parts) {
+__device__ void arrive_and_combine(const DraftArgs& a, unsigned int* flag, int bh, int n_parts, int nthr) {
   __threadfence();
-  __syncthreads();
+  sync_part(nthr);
   if (threadIdx.x == 0) {
     const unsigned int prev = atomicAdd(a.counter + bh, 1u);
     *flag = (prev + 1 == static_cast<unsigned int>(n_parts)) ? 1u : 0u;
   }
-  __syncthreads();
+  sync_part(nthr);
   if (*flag == 0u) return;
   __threadfence();
   const int b = bh / a.Hkv, kvh = bh % a.Hkv;
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+  for (int i = threadIdx.x; i < G * D; i += nthr) {
     const int h = i / D, c = i % D;
     const size_t row = static_cast<size_t>(b * a.Hq + kvh * G + h) * a.max_parts;
     float M = -INFINITY;
@@ -481,104 +463,135 @@ __device__ void arrive_and_combine(const DraftArgs& a, unsigned int* flag, int b
 }
 
 // ------------------------------------------------------------------ stream CTA
+// Segments of stream CTA c: consecutive calls walk [range_lo(c), range_lo(c+1)).
+struct Segment {
+  int bh, gs, n_valid, n_st;
+};
+__device__ __forceinline__ bool next_segment(const DraftArgs& a, long long& pos, long long hi, Segment& sg,
+                                             bool& over_capacity) {
+  if (pos >= hi) return false;
+  sg.bh = static_cast<int>(pos / a.NGmax);
+  sg.gs = static_cast<int>(pos % a.NGmax);
+  const int ge = static_cast<int>(min(static_cast<long long>(a.NGmax), sg.gs + (hi - pos)));
+  pos += ge - sg.gs;
+  int ng_req = a.packed_len[sg.bh / a.Hkv] / kGroup;
+  over_capacity = ng_req > a.NGmax;
+  if (over_capacity) ng_req = a.NGmax;
+  sg.n_valid = max(0, min(ge, ng_req) - sg.gs);
+  sg.n_st = (sg.n_valid + kWarps - 1) / kWarps;
+  return true;
+}
+
+// Producer warp (lane 0): fills the ring stage by stage, across segments,
+// each stage once all consumer warps released its previous use.
+template <int D, int BITS, int G>
+__device__ void produce(const DraftArgs& a, uint8_t* smem, int c, uint64_t* full, uint64_t* empty,
+                        volatile uint32_t* abort) {
+  using P = Plan<D, BITS, G>;
+  long long k = 0;                              // stage uses issued so far (ring position, phase)
+  const long long hi = range_lo(c + 1, a.total, a.n_stream);
+  long long pos = range_lo(c, a.total, a.n_stream);
+  Segment sg;
+  bool over;
+  while (next_segment(a, pos, hi, sg, over)) {
+    for (int s = 0; s < sg.n_st; ++s, ++k) {
+      const int buf = static_cast<int>(k % P::NS);
+      const long long use = k / P::NS;
+      if (use > 0 && !vc_mbar_wait_or_abort(empty + buf, static_cast<uint32_t>((use - 1) & 1), abort, kWaitCycles))
+        return;
+      issue_stage<D, BITS, G>(a, smem + buf * P::stage, full + buf, sg.bh, sg.gs + s * kWarps,
+                              min(kWarps, sg.n_valid - s * kWarps));
+    }
+  }
+}
+
 template <int D, int BITS, int G>
 __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
   using P = Plan<D, BITS, G>;
-  constexpr int GW = HeadSplit<G>::GW, HS = HeadSplit<G>::HS, SG = HeadSplit<G>::SG;
-  using L = PvLayout<D, BITS, GW>;
-  constexpr int W = P::W, NS = P::NS, NC = D / kGroup;
+  constexpr int NS = P::NS, KS = D / 16, NT = D / 8, NCG = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* sc = reinterpret_cast<float*>(smem + P::off_sc) + warp * GW * kGroup;
-  float* q_s = reinterpret_cast<float*>(smem + P::off_q);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P::off_bar);
+  const int gid = lane >> 2, tig = lane & 3;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + P::off_bar);
+  uint64_t* empty = full + NS;
   unsigned int* flag = reinterpret_cast<unsigned int*>(smem + P::off_flag);
+  volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(flag + 1);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NS; ++i) vc_mbar_init(bars + i, 1);
+    for (int i = 0; i < NS; ++i) {
+      vc_mbar_init(full + i, 1);
+      vc_mbar_init(empty + i, kWarps);
+    }
+    *abort = 0u;
     vc_fence_mbar_init();
   }
   __syncthreads();
-  long long gstage = 0;                        // stages consumed by this CTA (ring position, phase)
+  if (warp == kWarps) {                         // producer warp
+    if (lane == 0) produce<D, BITS, G>(a, smem, c, full, empty, abort);
+    return;
+  }
+  // lane constants: bias columns (gid 0: zeros / f, gid 1: -scales) and
+  // correction columns (gid = 2g: zeros / f, gid = 2g + 1: -scales of channel
+  // group g; a V meta row pair holds the scales first, then the zeros)
+  const float f0 = field_scale<BITS>(0), f1 = field_scale<BITS>(1);
+  const uint32_t bias_mul0 = h2u(__float2half2_rn(gid == 0 ? 1.0f / f0 : (gid == 1 ? -1.0f : 0.0f)));
+  const uint32_t bias_mul1 = h2u(__float2half2_rn(gid == 0 ? 1.0f / f1 : (gid == 1 ? -1.0f : 0.0f)));
+  const bool zc = gid < 2 * NCG;
+  const uint32_t zcol_mul0 = h2u(__float2half2_rn(!zc ? 0.0f : ((gid & 1) ? -1.0f : 1.0f / f0)));
+  const uint32_t zcol_mul1 = h2u(__float2half2_rn(!zc ? 0.0f : ((gid & 1) ? -1.0f : 1.0f / f1)));
+  const int zcol_off = zc ? 32 * (gid ^ 1) : 0;
+  long long k = 0;                              // stage uses consumed so far
   const long long hi = range_lo(c + 1, a.total, a.n_stream);
   long long pos = range_lo(c, a.total, a.n_stream);
-  while (pos < hi) {
-    const int bh = static_cast<int>(pos / a.NGmax);
-    const int gs = static_cast<int>(pos % a.NGmax);
-    const int ge = static_cast<int>(min(static_cast<long long>(a.NGmax), gs + (hi - pos)));
-    pos += ge - gs;
-    const int b = bh / a.Hkv, kvh = bh % a.Hkv;
-    int ng_req = a.packed_len[b] / kGroup;
-    if (ng_req > a.NGmax) {
-      if (threadIdx.x == 0) atomicOr(&g_draft_status, VC_DEV_CAPACITY);
-      ng_req = a.NGmax;
-    }
-    const int n_valid = max(0, min(ge, ng_req) - gs);
-    const int n_st = (n_valid + SG - 1) / SG;
+  Segment sg;
+  bool over;
+  while (next_segment(a, pos, hi, sg, over)) {
+    if (over && threadIdx.x == 0) atomicOr(&g_draft_status, VC_DEV_CAPACITY);
+    const int b = sg.bh / a.Hkv, kvh = sg.bh % a.Hkv;
     int first, last;
-    ctas_of(bh, a, first, last);
-    // ---- prologue: fill the ring (the proxy fence orders earlier generic
-    // writes to the ring, the previous segment's warp merge, before the copies)
-    if (threadIdx.x == 0) vc_fence_proxy_async_smem();
-    if (threadIdx.x == 0)
-      for (int i = 0; i < NS && i < n_st; ++i) {
-        const int buf = static_cast<int>((gstage + i) % NS);
-        issue_stage<D, BITS, G>(a, smem + buf * P::stage, bars + buf, bh, gs + i * SG,
-                                min(SG, n_valid - i * SG));
+    ctas_of(sg.bh, a, first, last);
+    // query fragments of head gid, times f_r: channels (D/4) tig + 4ks + 2r + {0, 1}
+    uint32_t qf[KS][2];
+    {
+      const uint16_t* qrow = a.q + (static_cast<size_t>(b) * a.Hq + kvh * G + (gid < G ? gid : 0)) * D + (D / 4) * tig;
+      const float on = gid < G ? 1.0f : 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(qrow + 4 * ks);
+        const float q0 = vc_bf16_to_f32(static_cast<uint16_t>(raw.x)), q1 = vc_bf16_to_f32(static_cast<uint16_t>(raw.x >> 16));
+        const float q2 = vc_bf16_to_f32(static_cast<uint16_t>(raw.y)), q3 = vc_bf16_to_f32(static_cast<uint16_t>(raw.y >> 16));
+        qf[ks][0] = h2u(__floats2half2_rn(q0 * on * f0, q1 * on * f0));
+        qf[ks][1] = h2u(__floats2half2_rn(q2 * on * f1, q3 * on * f1));
       }
-    load_q<D, G>(a, b, kvh, q_s);
-    __syncthreads();
-    float m[GW], l[GW], zacc[GW];
-    float2 acc[GW][L::CPL / 2];
-#pragma unroll
-    for (int h = 0; h < GW; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.0f;
-      zacc[h] = 0.0f;
-#pragma unroll
-      for (int jp = 0; jp < L::CPL / 2; ++jp) acc[h][jp] = make_float2(0.0f, 0.0f);
     }
-    bool ok = true;
-    for (int st = 0; st < n_st; ++st) {
-      const int buf = static_cast<int>((gstage + st) % NS);
-      const uint32_t parity = static_cast<uint32_t>(((gstage + st) / NS) & 1);
-      const bool mine = vc_mbar_wait_bounded(bars + buf, parity, kWaitCycles);
-      ok = __syncthreads_and(mine) != 0;
-      if (!ok) break;
-      const uint8_t* base = smem + buf * P::stage;
-      const int gl = warp / HS;                              // this warp's group in the stage
-      const float* q_w = q_s + (warp % HS) * GW * D;         // ... and its heads
-      if (st * SG + gl < n_valid) {
-        const uint32_t* kc_g = reinterpret_cast<const uint32_t*>(base) + gl * W * kGroup;
-        const uint16_t* ksz_g = reinterpret_cast<const uint16_t*>(base + P::kc) + gl * D * 2;
-        const uint32_t* vc_g = reinterpret_cast<const uint32_t*>(base + P::kc + P::meta) + gl * W * kGroup;
-        const uint16_t* vsz_g = reinterpret_cast<const uint16_t*>(base + 2 * P::kc + P::meta) + gl * NC * kGroup * 2;
-        qk_group<D, BITS, GW>(kc_g, ksz_g, q_w, sc, lane);
-        __syncwarp();
-        float alpha[GW];
-        if (softmax_group<GW>(sc, m, l, alpha, lane)) {
+    WarpState<D> st;
 #pragma unroll
-          for (int h = 0; h < GW; ++h) {
-            zacc[h] *= alpha[h];
-#pragma unroll
-            for (int jp = 0; jp < L::CPL / 2; ++jp) acc[h][jp] = __fmul2_rn(acc[h][jp], make_float2(alpha[h], alpha[h]));
-          }
-        }
-        __syncwarp();
-        pv_group<D, BITS, GW>(vc_g, vsz_g, sc, acc, zacc, lane);
-        __syncwarp();
+    for (int nt = 0; nt < NT; ++nt) st.o[nt][0] = st.o[nt][1] = st.o[nt][2] = st.o[nt][3] = 0.0f;
+    st.oz[0] = st.oz[1] = st.oz[2] = st.oz[3] = 0.0f;
+    st.l0 = st.l1 = 0.0f;
+    st.m = -INFINITY;
+    for (int s = 0; s < sg.n_st; ++s, ++k) {
+      const int buf = static_cast<int>(k % NS);
+      const bool ok = __all_sync(0xffffffffu, vc_mbar_wait_or_abort(full + buf, static_cast<uint32_t>((k / NS) & 1),
+                                                                   abort, kWaitCycles));
+      if (ok && s * kWarps + warp < sg.n_valid) {
+        const uint8_t* base = smem + buf * P::stage;
+        const uint32_t* kc_g = reinterpret_cast<const uint32_t*>(base + warp * P::codes);
+        const uint16_t* ksz_g = reinterpret_cast<const uint16_t*>(base + P::kc + warp * P::meta);
+        const uint32_t* vc_g = reinterpret_cast<const uint32_t*>(base + P::kc + P::mt + warp * P::codes);
+        const uint16_t* vsz_g = reinterpret_cast<const uint16_t*>(base + 2 * P::kc + P::mt + warp * P::meta);
+        group_mma<D, BITS>(kc_g, ksz_g, vc_g, vsz_g, qf, bias_mul0, bias_mul1, zcol_mul0, zcol_mul1, zcol_off,
+                           a.scale_log2, st, lane);
       }
-      __syncthreads();                                      // stage `buf` fully consumed
-      if (threadIdx.x == 0 && st + NS < n_st)
-        issue_stage<D, BITS, G>(a, smem + buf * P::stage, bars + buf, bh, gs + (st + NS) * SG,
-                                min(SG, n_valid - (st + NS) * SG));
+      __syncwarp();
+      if (lane == 0) vc_mbar_arrive(empty + buf);          // this warp is done with the stage
     }
-    gstage += n_st;
-    if (!ok) {
+    // every consumer thread takes the same branch: the OR of the abort flag
+    if (vc_bar_red_or(1, kConsumers, *abort != 0u)) {
       if (threadIdx.x == 0) atomicOr(&g_draft_status, VC_DEV_BARRIER_TIMEOUT);
       return;                                               // outputs of this call are invalid
     }
-    write_partial<D, BITS, G>(a, smem, bh, c - first, m, l, acc, zacc);
-    arrive_and_combine<G, D>(a, flag, bh, last - first + 2);
-    __syncthreads();                                        // smem (red / q) reused by the next segment
+    write_partial<D, BITS, G>(a, smem, sg.bh, c - first, st);
+    arrive_and_combine<G, D>(a, flag, sg.bh, last - first + 2, kConsumers);
+    vc_bar_sync(1, kConsumers);                             // red / flag reused by the next segment
   }
 }
 
@@ -604,7 +617,7 @@ __device__ void tail_cta(const DraftArgs& a, uint8_t* smem, int bh) {
   if (bad || n_tok == 0) {
     for (int h = threadIdx.x; h < G; h += blockDim.x)
       a.part_lse[static_cast<size_t>(b * a.Hq + kvh * G + h) * a.max_parts + slot] = -INFINITY;
-    arrive_and_combine<G, D>(a, flag, bh, n_c + 1);
+    arrive_and_combine<G, D>(a, flag, bh, n_c + 1, blockDim.x);
     return;
   }
   uint16_t* krow = reinterpret_cast<uint16_t*>(smem);                      // [n_tok][D]
@@ -622,7 +635,8 @@ __device__ void tail_cta(const DraftArgs& a, uint8_t* smem, int bh) {
   load_q<D, G>(a, b, kvh, q_s);
   __syncthreads();
   // scores: warp per token, lanes over channel pairs
-  for (int t = warp; t < n_tok; t += kWarps) {
+  const int nw = blockDim.x / 32;
+  for (int t = warp; t < n_tok; t += nw) {
     float part[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) part[h] = 0.0f;
@@ -639,7 +653,7 @@ __device__ void tail_cta(const DraftArgs& a, uint8_t* smem, int bh) {
     }
   }
   __syncthreads();
-  for (int h = warp; h < G; h += kWarps) {
+  for (int h = warp; h < G; h += nw) {
     float mx = -INFINITY;
     for (int t = lane; t < n_tok; t += 32) mx = fmaxf(mx, sc[h * n_tok + t]);
 #pragma unroll
@@ -678,7 +692,7 @@ __device__ void tail_cta(const DraftArgs& a, uint8_t* smem, int bh) {
           *reinterpret_cast<const uint4*>(vrow + n_tail * D + i * 8);
     }
   }
-  arrive_and_combine<G, D>(a, flag, bh, n_c + 1);
+  arrive_and_combine<G, D>(a, flag, bh, n_c + 1, blockDim.x);
 }
 
 template <int D, int BITS, int G, int MINB>
@@ -699,16 +713,15 @@ vc_status_t check(const vc_shape_t* s) {
   if (s->bits != 2 && s->bits != 4) VC_FAIL(VC_ERR_UNSUPPORTED, "bits %d not in {2, 4}", s->bits);
   const int G = s->Hq / s->Hkv;
   if (G != 1 && G != 2 && G != 4 && G != 5 && G != 8) VC_FAIL(VC_ERR_UNSUPPORTED, "G = %d not in {1,2,4,5,8}", G);
+  VC_REQUIRE(s->softmax_scale > 0.0f, "softmax_scale must be positive");
   return VC_OK;
 }
 
-#ifndef VC_DRAFT_MINB
-#define VC_DRAFT_MINB 1
-#endif
+// One CTA of 256 threads per SM: the warps keep the whole per-head output
+// (D/8 accumulator tiles) and the query fragments in registers.
 template <int G>
 struct MinBlocks {
-  // CTAs per SM the register allocation targets (2 caps registers at 128)
-  static constexpr int value = G <= 5 ? VC_DRAFT_MINB : 1;
+  static constexpr int value = 1;
 };
 
 struct LaunchPlan {
@@ -730,7 +743,7 @@ vc_status_t plan_t(const vc_shape_t* s, int max_packed, LaunchPlan* lp) {
   const long long NGmax = max_packed / kGroup;
   lp->total = static_cast<long long>(s->B) * s->Hkv * NGmax;
   long long n = static_cast<long long>(occ) * sms;
-  const long long by_work = lp->total / HeadSplit<G>::SG;      // at least one stage per CTA
+  const long long by_work = lp->total / kWarps;                 // at least one stage per CTA
   if (n > by_work) n = by_work;
   if (n < 1 && lp->total > 0) n = 1;
   lp->n_stream = static_cast<int>(lp->total > 0 ? n : 0);
@@ -764,7 +777,7 @@ size_t ws_bytes(const vc_shape_t* s, const LaunchPlan& lp) {
 
 template <int D, int BITS, int G>
 vc_status_t launch_t(const DraftArgs& a, const LaunchPlan& lp, cudaStream_t cs) {
-  if (tail_smem<D, G>(a.tail_cap) > Plan<D, BITS, G>::off_sc)
+  if (tail_smem<D, G>(a.tail_cap) > Plan<D, BITS, G>::off_q)
     VC_FAIL(VC_ERR_UNSUPPORTED, "tail_cap %d too large for the shared-memory plan", a.tail_cap);
   const int grid = a.B * a.Hkv + lp.n_stream;
   draft_kernel<D, BITS, G, MinBlocks<G>::value><<<grid, kThreads, lp.smem, cs>>>(a);

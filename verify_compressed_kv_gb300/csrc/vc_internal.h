@@ -97,6 +97,43 @@ __device__ __forceinline__ bool vc_mbar_wait_bounded(uint64_t* bar, uint32_t par
   }
   return true;
 }
+// Plain arrival (no transaction bytes) on an mbarrier.
+__device__ __forceinline__ void vc_mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(vc_smem_addr(bar)) : "memory");
+}
+// Bounded wait that also gives up as soon as *abort is non-zero (another warp
+// already gave up); on its own timeout it sets *abort.  Returns true once
+// phase `parity` completed.
+__device__ __forceinline__ bool vc_mbar_wait_or_abort(uint64_t* bar, uint32_t parity, volatile uint32_t* abort,
+                                                      long long limit_cycles) {
+  if (vc_mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!vc_mbar_try_wait(bar, parity)) {
+    if (*abort != 0u) return false;
+    if (clock64() - t0 > limit_cycles) {
+      *abort = 1u;
+      return false;
+    }
+  }
+  return true;
+}
+// Barrier over the first `count` threads of the CTA (named barrier `id`, 1..15).
+__device__ __forceinline__ void vc_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Barrier over the first `count` threads returning the OR of `pred` over them.
+__device__ __forceinline__ bool vc_bar_red_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n"
+      " setp.ne.u32 p, %1, 0;\n"
+      " bar.red.or.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
 // Order this thread's earlier generic-proxy shared-memory accesses before its
 // later async-proxy (bulk copy) accesses.
 __device__ __forceinline__ void vc_fence_proxy_async_smem() {

@@ -26,9 +26,65 @@ constexpr int kGroup = 32;
 
 // ------------------------------------------------------------------ quantiser
 
+// ------------------------------------------------------------------ packed layout
+// Field rules of the packed words (the library's format; include/vc.h): per
+// group, 32 lanes x d*b/32 words; word w of lane L at (w/4)*128 + 4L + w%4.
+// b = 2: slot (u, r, e) starts at bit (8 - 2r + 16e + 4u) mod 32;
+// b = 4: slot (u, e) starts at (6 + 16e + 4u) mod 32, bits taken cyclically.
+__device__ __forceinline__ int field_pos(int bits, int u, int r, int e) {
+  return bits == 2 ? ((8 - 2 * r + 16 * e + 4 * u) & 31) : ((6 + 16 * e + 4 * u) & 31);
+}
+
+// Word `idx` of a group's K codes (V codes when IS_V) from a code tile
+// codes[t * ld + c].  K: lane L = 4a + c holds tokens 4a + j, channels
+// (d/4) c + 4k + 2r + e, fragment i = j*(d/16) + k.  V: tokens 8c + 4e + 2s + r,
+// channels 8n + a, fragment i = s*(d/8) + n.  b = 2: word i/4, u = i%4;
+// b = 4: i2 = 2i + r, word i2/4, u = i2%4.
+template <int BITS, bool IS_V>
+__device__ uint32_t build_word(const uint8_t* codes, int ld, int d, int idx) {
+  const int L = (idx % 128) / 4, w = (idx / 128) * 4 + idx % 4;
+  const int a = L / 4, c = L % 4;
+  const int per = IS_V ? d / 8 : d / 16;          // fragments per j (K) or per s (V)
+  uint32_t word = 0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      int i;
+      if (BITS == 2) {
+        i = 4 * w + u;
+      } else {
+        const int i2 = 4 * w + u;
+        if ((i2 & 1) != r) continue;              // b = 4: slot u carries one r
+        i = i2 >> 1;
+      }
+      const int hi = i / per, lo = i % per;         // (j, k) for K, (s, n) for V
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        int t, ch;
+        if (IS_V) {
+          t = 8 * c + 4 * e + 2 * hi + r;
+          ch = 8 * lo + a;
+        } else {
+          t = 4 * a + hi;
+          ch = (d / 4) * c + 4 * lo + 2 * r + e;
+        }
+        const uint32_t code = codes[t * ld + ch];
+        word |= __funnelshift_l(code, code, field_pos(BITS, u, r, e));
+      }
+    }
+  return word;
+}
+
+// Entry of a V meta row (32 entries, one per token) that holds token t:
+// entry 8c + 4s + 2r + e holds token 8c + 4e + 2s + r.
+__device__ __forceinline__ int vmeta_entry(int t) {
+  return (t & ~7) | (((t >> 1) & 1) << 2) | ((t & 1) << 1) | ((t >> 2) & 1);
+}
+
 // Quantise one 32-token tile held in shared memory.
 //   k_s, v_s : bf16 tiles [32][ld] (rows = tokens), ld >= d
-//   codes_s  : scratch uint8 [32][d + 4] (padded: conflict-free column reads)
+//   codes_s  : scratch uint8 2 x [32][d + 4] (K codes, then V codes)
 // Writes the tile's words and metadata into group `g` of (b, h)'s packed
 // arrays (already offset to the (b, h) slice).  All threads of the CTA call it.
 template <int BITS>
@@ -36,8 +92,9 @@ __device__ void quantize_tile(const uint16_t* k_s, const uint16_t* v_s, int ld, 
                               uint8_t* codes_s, int g, uint32_t* kc, uint16_t* ksz, uint32_t* vc,
                               uint16_t* vsz) {
   constexpr int QMAX = (1 << BITS) - 1;
-  constexpr int CPW = 32 / BITS;            // codes per 32-bit word
-  const int W = d / CPW;                    // words per token
+  const int cld = d + 4;
+  uint8_t* kcodes = codes_s;
+  uint8_t* vcodes = codes_s + kGroup * cld;
   const float qmax = static_cast<float>(QMAX);
 
   // ---- keys: one thread per channel, group = 32 tokens of that channel
@@ -58,20 +115,10 @@ __device__ void quantize_tile(const uint16_t* k_s, const uint16_t* v_s, int ld, 
         r = fminf(fmaxf(r, 0.0f), qmax);
         code = static_cast<int>(r);
       }
-      codes_s[t * (d + 4) + c] = static_cast<uint8_t>(code);
+      kcodes[t * cld + c] = static_cast<uint8_t>(code);
     }
-    const size_t m = (static_cast<size_t>(g) * d + c) * 2;
-    ksz[m] = s16;
-    ksz[m + 1] = z16;
-  }
-  __syncthreads();
-  // pack key words: word (w, t), consecutive threads -> consecutive t
-  for (int i = threadIdx.x; i < W * kGroup; i += blockDim.x) {
-    const int w = i / kGroup, t = i % kGroup;
-    uint32_t word = 0;
-#pragma unroll
-    for (int j = 0; j < CPW; ++j) word |= static_cast<uint32_t>(codes_s[t * (d + 4) + w * CPW + j]) << (BITS * j);
-    kc[(static_cast<size_t>(g) * W + w) * kGroup + t] = word;
+    ksz[static_cast<size_t>(g) * 2 * d + c] = s16;          // scales row, then zeros row
+    ksz[static_cast<size_t>(g) * 2 * d + d + c] = z16;
   }
   // ---- values: one thread per (channel group, token), group = 32 channels
   const int NC = d / kGroup;
@@ -87,26 +134,25 @@ __device__ void quantize_tile(const uint16_t* k_s, const uint16_t* v_s, int ld, 
     const uint16_t s16 = vc_f32_to_f16_rn(__fdiv_rn(__fsub_rn(mx, mn), qmax));
     const uint16_t z16 = vc_f32_to_f16_rn(mn);
     const float sf = vc_f16_to_f32(s16), zf = vc_f16_to_f32(z16);
-    constexpr int WPG = kGroup / CPW;       // words per channel group
-#pragma unroll
-    for (int ww = 0; ww < WPG; ++ww) {
-      uint32_t word = 0;
-#pragma unroll
-      for (int j = 0; j < CPW; ++j) {
-        int code = 0;
-        if (sf != 0.0f) {
-          float r = rintf(__fdiv_rn(__fsub_rn(vc_bf16_to_f32(row[ww * CPW + j]), zf), sf));
-          r = fminf(fmaxf(r, 0.0f), qmax);
-          code = static_cast<int>(r);
-        }
-        word |= static_cast<uint32_t>(code) << (BITS * j);
+    for (int c = 0; c < kGroup; ++c) {
+      int code = 0;
+      if (sf != 0.0f) {
+        float r = rintf(__fdiv_rn(__fsub_rn(vc_bf16_to_f32(row[c]), zf), sf));
+        r = fminf(fmaxf(r, 0.0f), qmax);
+        code = static_cast<int>(r);
       }
-      const int w = cg * WPG + ww;
-      vc[(static_cast<size_t>(g) * W + w) * kGroup + t] = word;
+      vcodes[t * cld + cg * kGroup + c] = static_cast<uint8_t>(code);
     }
-    const size_t m = ((static_cast<size_t>(g) * NC + cg) * kGroup + t) * 2;
+    const size_t m = ((static_cast<size_t>(g) * NC + cg) * 2) * kGroup + vmeta_entry(t);
     vsz[m] = s16;
-    vsz[m + 1] = z16;
+    vsz[m + kGroup] = z16;
+  }
+  __syncthreads();
+  // ---- words: consecutive threads -> consecutive words
+  const int n_words = d * BITS;
+  for (int idx = threadIdx.x; idx < n_words; idx += blockDim.x) {
+    kc[static_cast<size_t>(g) * n_words + idx] = build_word<BITS, false>(kcodes, cld, d, idx);
+    vc[static_cast<size_t>(g) * n_words + idx] = build_word<BITS, true>(vcodes, cld, d, idx);
   }
   __syncthreads();
 }
@@ -163,7 +209,7 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const uint16_t* __re
   quantize_tile<BITS>(k_s, v_s, ld, d, codes_s, g, s.kc, s.ksz, s.vc, s.vsz);
 }
 
-size_t pack_smem(int d) { return 2 * kGroup * (d + 2) * sizeof(uint16_t) + kGroup * (d + 4); }
+size_t pack_smem(int d) { return 2 * kGroup * (d + 2) * sizeof(uint16_t) + 2 * kGroup * (d + 4); }
 
 // The commit of one request's accepted tokens for one KV head (grid (Hkv, B)):
 // append rows 0..n of k_new/v_new to the tail, pack whole groups from the
@@ -253,26 +299,60 @@ __global__ void append_lengths_kernel(const int32_t* __restrict__ n_acc, int B, 
   }
 }
 
+// Position of code (t, ch) of a group: word index and field start.
+template <int BITS, bool IS_V>
+__device__ __forceinline__ void locate(int t, int ch, int d, int& idx, int& pos) {
+  int L, i, r, e;
+  if (IS_V) {
+    const int c = t / 8, s = (t >> 1) & 1;
+    e = (t >> 2) & 1;
+    r = t & 1;
+    const int a = ch % 8, n = ch / 8;
+    L = 4 * a + c;
+    i = s * (d / 8) + n;
+  } else {
+    const int a = t / 4, j = t % 4;
+    const int c = ch / (d / 4), rem = ch % (d / 4);
+    const int k = rem / 4;
+    r = (rem >> 1) & 1;
+    e = rem & 1;
+    L = 4 * a + c;
+    i = j * (d / 16) + k;
+  }
+  int w, u;
+  if (BITS == 2) {
+    w = i / 4;
+    u = i % 4;
+  } else {
+    const int i2 = 2 * i + r;
+    w = i2 / 4;
+    u = i2 % 4;
+  }
+  idx = (w / 4) * 128 + 4 * L + w % 4;
+  pos = field_pos(BITS, u, r, e);
+}
+
 // grid (T/32, B*Hkv), thread per (token, channel) pairs.
 template <int BITS>
 __global__ void unpack_kernel(int T, int T_cap, int d, Packed p, float* K_hat, float* V_hat) {
-  constexpr int CPW = 32 / BITS;
   constexpr uint32_t MASK = (1u << BITS) - 1u;
-  const int W = d / CPW;
   const int g = blockIdx.x, bh = blockIdx.y;
   Packed s = slice(p, bh, T_cap, d, BITS);
+  const int n_words = d * BITS;
   for (int i = threadIdx.x; i < kGroup * d; i += blockDim.x) {
     const int t = i / d, c = i % d;
-    const int w = c / CPW, j = c % CPW;
-    const uint32_t kw = s.kc[(static_cast<size_t>(g) * W + w) * kGroup + t];
-    const uint32_t vw = s.vc[(static_cast<size_t>(g) * W + w) * kGroup + t];
-    const float kcode = static_cast<float>((kw >> (BITS * j)) & MASK);
-    const float vcode = static_cast<float>((vw >> (BITS * j)) & MASK);
-    const size_t km = (static_cast<size_t>(g) * d + c) * 2;
-    const size_t vm = ((static_cast<size_t>(g) * (d / kGroup) + c / kGroup) * kGroup + t) * 2;
+    int ki, kp, vi, vp;
+    locate<BITS, false>(t, c, d, ki, kp);
+    locate<BITS, true>(t, c, d, vi, vp);
+    const uint32_t kw = s.kc[static_cast<size_t>(g) * n_words + ki];
+    const uint32_t vw = s.vc[static_cast<size_t>(g) * n_words + vi];
+    const float kcode = static_cast<float>(__funnelshift_r(kw, kw, kp) & MASK);
+    const float vcode = static_cast<float>(__funnelshift_r(vw, vw, vp) & MASK);
+    const size_t km = static_cast<size_t>(g) * 2 * d + c;
+    const size_t vm = ((static_cast<size_t>(g) * (d / kGroup) + c / kGroup) * 2) * kGroup + vmeta_entry(t);
     const size_t o = (static_cast<size_t>(bh) * T + static_cast<size_t>(g) * kGroup + t) * d + c;
-    K_hat[o] = fmaf(kcode, vc_f16_to_f32(s.ksz[km]), vc_f16_to_f32(s.ksz[km + 1]));
-    V_hat[o] = fmaf(vcode, vc_f16_to_f32(s.vsz[vm]), vc_f16_to_f32(s.vsz[vm + 1]));
+    K_hat[o] = fmaf(kcode, vc_f16_to_f32(s.ksz[km]), vc_f16_to_f32(s.ksz[km + d]));
+    V_hat[o] = fmaf(vcode, vc_f16_to_f32(s.vsz[vm]), vc_f16_to_f32(s.vsz[vm + kGroup]));
   }
 }
 
