@@ -22,7 +22,7 @@ tokens:
 
 * K codes uint32 [B, Hkv, T/32, d*b] and V codes uint32 [B, Hkv, T/32, d*b]:
   32 lanes x d*b/32 words, each code a b-bit field at a position given by its
-  token and channel (K and V use different maps).
+  token and channel (K and V use different maps); no field crosses bit 31.
 * K meta fp16 [B, Hkv, T/32, 2, d]: scales of the group's channels, then zeros.
 * V meta fp16 [B, Hkv, T/32, d/32, 2, 32]: per channel group, the 32 tokens'
   scales, then zeros, tokens in a fixed permuted order.
@@ -118,12 +118,12 @@ def dequantize_kv(kcode, kscale, kzero, vcode, vscale, vzero):
 # in one word.  Written out per group of 32 tokens; d channels, b bits.
 
 def _field_pos(bits: int, u: int, r: int, e: int) -> int:
-    """Lowest bit of a field.  b = 2: slot (u, r, e) starts at (8 - 2r + 16e + 4u)
-    mod 32.  b = 4: slot (u, e) starts at (6 + 16e + 4u) mod 32 (r unused); its
-    four bits run upwards and wrap from bit 31 to bit 0."""
+    """Lowest bit of a field.  b = 2: slot (u, r, e) starts at 16e + 4u + 2(1 - r).
+    b = 4: slot (u, e) starts at 16e + 4u (r unused).  The e = 1 field of a
+    slot sits exactly 16 bits above its e = 0 field, in the high half-word."""
     if bits == 2:
-        return (8 - 2 * r + 16 * e + 4 * u) % 32
-    return (6 + 16 * e + 4 * u) % 32
+        return 16 * e + 4 * u + 2 * (1 - r)
+    return 16 * e + 4 * u
 
 
 def _word_index(L: int, w: int) -> int:
@@ -177,12 +177,6 @@ def _v_fields(d: int, bits: int):
     return np.array(rows, dtype=np.int64)
 
 
-def _rotl(x, s):
-    x = x.astype(np.uint64)
-    s = np.asarray(s, dtype=np.uint64)
-    return ((x << s) | (x >> ((np.uint64(32) - s) % np.uint64(32)))) & np.uint64(0xFFFFFFFF)
-
-
 def _pack(code: np.ndarray, bits: int, fields) -> np.ndarray:
     """Logical codes uint8 [B,H,T,d] -> words uint32 [B,H,T/32,d*b]."""
     B, H, T, d = code.shape
@@ -190,7 +184,7 @@ def _pack(code: np.ndarray, bits: int, fields) -> np.ndarray:
     order = np.argsort(fields[:, 0], kind="stable")          # group fields by word
     f = fields[order]
     vals = c[..., f[:, 2], f[:, 3]]                          # [B,H,NG,F]
-    placed = _rotl(vals, f[:, 1])
+    placed = vals.astype(np.uint64) << f[:, 1].astype(np.uint64)
     n_words = d * bits
     per = f.shape[0] // n_words
     words = np.bitwise_or.reduce(placed.reshape(B, H, T // GROUP, n_words, per), axis=-1)
@@ -201,9 +195,7 @@ def _unpack(words: np.ndarray, bits: int, d: int, fields) -> np.ndarray:
     B, H, NG, n_words = words.shape
     assert n_words == d * bits
     w = words[..., fields[:, 0]].astype(np.uint64)           # [B,H,NG,F]
-    s = fields[:, 1].astype(np.uint64)
-    rot = ((w >> s) | (w << ((np.uint64(32) - s) % np.uint64(32)))) & np.uint64(0xFFFFFFFF)
-    vals = (rot & np.uint64((1 << bits) - 1)).astype(np.uint8)
+    vals = ((w >> fields[:, 1].astype(np.uint64)) & np.uint64((1 << bits) - 1)).astype(np.uint8)
     code = np.zeros((B, H, NG, GROUP, d), np.uint8)
     code[..., fields[:, 2], fields[:, 3]] = vals
     return code.reshape(B, H, NG * GROUP, d)

@@ -112,23 +112,22 @@ def _const_words(pack, code_fn, bits, d):
 def test_packed_words_by_hand():
     """Words worked out by hand from the field rules.
 
-    b = 2, fields (u, r, e) start at 8 - 2r + 16e + 4u (mod 32):
-      e = 1 fields: r = 0 -> 24, 28, 0, 4; r = 1 -> 22, 26, 30, 2.
-      A code of 1 in every e = 1 field -> bits {0,2,4,22,24,26,28,30} = 0x55400015.
-      r = 1 fields: 6, 10, 14, 18 (e = 0), 22, 26, 30, 2 (e = 1) -> 0x44444444.
+    b = 2, slot (u, r, e) starts at 16e + 4u + 2(1 - r):
+      e = 1 fields: bits 16, 18, ..., 30; a code of 1 in each -> 0x55550000.
+      r = 1 fields: 16e + 4u = 0, 4, 8, 12, 16, 20, 24, 28 -> 0x11111111.
     For K, e is the channel's bit 0 and r its bit 1; for V, r is the token's
     bit 0 and e its bit 2.
-    b = 4, fields (u, e) start at 6 + 16e + 4u (mod 32): the e = 1 fields cover
-      bits 22-25, 26-29, 30-31 + 0-1, 2-5, so code 15 there -> 0xFFC0003F and
-      code 1 there -> bits 22, 26, 30, 2 -> 0x44400004."""
+    b = 4, slot (u, e) starts at 16e + 4u: the e = 1 fields fill bits 16-31,
+      so code 15 there -> 0xFFFF0000 and code 1 there -> bits 16, 20, 24, 28 =
+      0x11110000."""
     for d in (64, 128):
-        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: c % 2, 2, d) == 0x55400015)
-        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: (c // 2) % 2, 2, d) == 0x44444444)
-        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: t % 2, 2, d) == 0x44444444)
-        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: (t // 4) % 2, 2, d) == 0x55400015)
-        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: 15 * (c % 2), 4, d) == 0xFFC0003F)
-        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: c % 2, 4, d) == 0x44400004)
-        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: (t // 4) % 2, 4, d) == 0x44400004)
+        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: c % 2, 2, d) == 0x55550000)
+        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: (c // 2) % 2, 2, d) == 0x11111111)
+        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: t % 2, 2, d) == 0x11111111)
+        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: (t // 4) % 2, 2, d) == 0x55550000)
+        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: 15 * (c % 2), 4, d) == 0xFFFF0000)
+        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: c % 2, 4, d) == 0x11110000)
+        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: (t // 4) % 2, 4, d) == 0x11110000)
         assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: 3 + 0 * c, 2, d) == 0xFFFFFFFF)
 
 
@@ -137,25 +136,25 @@ def test_single_codes_land_where_the_rules_say():
 
     K, b = 2, token 5, channel 37: a = 1, j = 1; 37 = 32*1 + 4*1 + 2*0 + 1 so
       c = 1, k = 1, r = 0, e = 1; lane 4a + c = 5; fragment j*8 + k = 9 -> word 2,
-      u = 1; start 8 + 16 + 4 = 28; stored at (2 // 4)*128 + 4*5 + 2 = 22.
+      u = 1; start 16 + 4 + 2 = 22; stored at (2 // 4)*128 + 4*5 + 2 = 22.
     V, b = 2, token 13, channel 42: 13 = 8*1 + 4*1 + 2*0 + 1 so c = 1, e = 1,
       s = 0, r = 1; 42 = 8*5 + 2 so n = 5, a = 2; lane 9; fragment 0*16 + 5 ->
-      word 1, u = 1; start 8 - 2 + 16 + 4 = 26; stored at 0 + 36 + 1 = 37.
+      word 1, u = 1; start 16 + 4 + 0 = 20; stored at 0 + 36 + 1 = 37.
     K, b = 4, d = 64, token 0, channel 5: a = c = j = 0, k = 1, r = 0, e = 1;
-      index 2*(0*4 + 1) + 0 = 2 -> word 0, u = 2; start 6 + 16 + 8 = 30, so the
-      field is bits 30, 31, 0, 1: code 11 = 0b1011 -> bits 30, 31, 1 = 0xC0000002."""
+      index 2*(0*4 + 1) + 0 = 2 -> word 0, u = 2; start 16 + 8 = 24:
+      code 11 -> 0x0B000000."""
     code = np.zeros((1, 1, 32, 128), np.uint8)
     code[0, 0, 5, 37] = 3
     w = kivi.pack_kcodes(code, 2)[0, 0, 0]
-    assert w[22] == 0x30000000 and np.count_nonzero(w) == 1
+    assert w[22] == 0x00C00000 and np.count_nonzero(w) == 1
     code = np.zeros((1, 1, 32, 128), np.uint8)
     code[0, 0, 13, 42] = 2
     w = kivi.pack_vcodes(code, 2)[0, 0, 0]
-    assert w[37] == 0x08000000 and np.count_nonzero(w) == 1
+    assert w[37] == 0x00200000 and np.count_nonzero(w) == 1
     code = np.zeros((1, 1, 32, 64), np.uint8)
     code[0, 0, 0, 5] = 11
     w = kivi.pack_kcodes(code, 4)[0, 0, 0]
-    assert w[0] == 0xC0000002 and np.count_nonzero(w) == 1
+    assert w[0] == 0x0B000000 and np.count_nonzero(w) == 1
 
 
 @pytest.mark.parametrize("bits", [2, 4])
