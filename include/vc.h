@@ -99,9 +99,9 @@ const char* vc_last_error(void);
  *   vc  uint32 [B, Hkv, NG, d*bits]     V codes, same word order, other field map
  *   vsz fp16   [B, Hkv, NG, d/32, 2, 32]  per channel group: scales, then zeros,
  *                                       entry 8c + 4s + 2r + e = token 8c + 4e + 2s + r
- * Fields (bit 0 = least significant; a 4-bit field wraps from bit 31 to bit 0):
- *   bits = 2: slot (u, r, e) starts at (8 - 2r + 16e + 4u) mod 32;
- *   bits = 4: slot (u, e) starts at (6 + 16e + 4u) mod 32.
+ * Fields (bit 0 = least significant):
+ *   bits = 2: slot (u, r, e) starts at 16e + 4u + 2(1 - r);
+ *   bits = 4: slot (u, e) starts at 16e + 4u.
  * Lane L = 4a + c.  K: tokens 4a + j (j < 4), channels (d/4)c + 4k + 2r + e
  * (k < d/16), fragment i = j*(d/16) + k.  V: tokens 8c + 4e + 2s + r, channels
  * 8n + a (n < d/8), fragment i = s*(d/8) + n.  bits = 2: word i/4, u = i%4;

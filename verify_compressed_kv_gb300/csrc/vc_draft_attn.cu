@@ -12,7 +12,7 @@
 //     laid end to end and each stream CTA takes an equal contiguous range, so
 //     the work is balanced whatever B*Hkv is; a range may span two heads
 //     (segments);
-//   * a segment is streamed through a ring of shared-memory stages (8 groups
+//   * a segment is streamed through a ring of shared-memory stages (11 groups
 //     of 32 tokens each: K codes, K scale/zero, V codes, V scale/zero), filled
 //     by bulk async copies (cp.async.bulk + mbarrier transaction counts, bounded
 //     waits) while the 8 warps compute on earlier stages;
@@ -39,7 +39,9 @@ namespace {
 
 __device__ uint32_t g_draft_status = 0;
 
-constexpr int kWarps = 8;                       // consumer warps of a stream CTA (one group each per stage)
+// 11 consumer warps + 1 producer: three warps per scheduler, the same
+// register budget (168) as 8 + 1.
+constexpr int kWarps = 11;                      // consumer warps of a stream CTA (one group each per stage)
 constexpr int kConsumers = kWarps * 32;
 constexpr int kThreads = kConsumers + 32;        // + one producer warp
 constexpr int kGroup = 32;
@@ -101,8 +103,8 @@ struct Plan {
   static constexpr size_t kc = kWarps * codes;                         // a stage holds kWarps groups
   static constexpr size_t mt = kWarps * meta;
   static constexpr size_t stage = 2 * kc + 2 * mt;                      // K codes, K meta, V codes, V meta
-  // ring depth: about 72 KB of stages in flight, at least double buffering
-  static constexpr int NS = (72 * 1024 / stage) < 2 ? 2 : ((72 * 1024 / stage) > 6 ? 6 : static_cast<int>(72 * 1024 / stage));
+  // ring depth: about 100 KB of stages in flight, at least double buffering
+  static constexpr int NS = (100 * 1024 / stage) < 2 ? 2 : ((100 * 1024 / stage) > 6 ? 6 : static_cast<int>(100 * 1024 / stage));
   static constexpr size_t ring = stage * NS;
   static constexpr size_t red = static_cast<size_t>(kWarps) * G * D * 4;   // warp merge
   static constexpr size_t off_red = ring;
@@ -176,7 +178,7 @@ __device__ __forceinline__ void split_mul(__half2 x, __half2 y, uint32_t& hi, ui
 }
 
 // Operand value of a packed code field: OR the field (moved to the top
-// mantissa bits) into the bit pattern of 1.0, giving 1 + code/f exactly.
+// mantissa bits by slot_shift) into the bit pattern of 1.0: 1 + code/f exactly.
 //   b = 2, r = 0: bits 8-9 of each half -> 1 + code/4   (f = 4)
 //   b = 2, r = 1: bits 6-7              -> 1 + code/16  (f = 16)
 //   b = 4:        bits 6-9              -> 1 + code/16  (f = 16)
@@ -190,21 +192,27 @@ __host__ __device__ constexpr float field_scale(int r) { return (BITS == 2 && r 
 template <int BITS>
 __host__ __device__ constexpr float field_log2(int r) { return (BITS == 2 && r == 0) ? 2.0f : 4.0f; }
 
-// Operand register r of fragment (word set w[], fragment index i) — the
-// field rules of the packed words (include/vc.h): b = 2: word i/4 rotated by
-// 4*(i%4); b = 4: i2 = 2i + r, word i2/4 rotated by 4*(i2%4).
+// Word w moved so that slot u's fields land in the operand windows: the e = 0
+// field of slot u starts at 4u + 2(1 - r) (b = 2) or 4u (b = 4), so a shift by
+// 4u - 6 brings it to bit 8 (r = 0) / bit 6 (r = 1, b = 4); the e = 1 field,
+// 16 bits higher, lands 16 bits higher too.  One plain shift, nothing wraps.
+__device__ __forceinline__ uint32_t slot_shift(uint32_t w, int u) {
+  return u == 0 ? (w << 6) : u == 1 ? (w << 2) : u == 2 ? (w >> 2) : (w >> 6);
+}
+
+// Operand registers (r = 0, 1) of fragment index i — the field rules of the
+// packed words (include/vc.h): b = 2: word i/4, slot u = i%4; b = 4: i2 = 2i + r,
+// word i2/4, slot u = i2%4.
 template <int BITS, int WPL>
 __device__ __forceinline__ void fragment(const uint32_t (&w)[WPL], int i, uint32_t& b0, uint32_t& b1) {
   if (BITS == 2) {
-    const uint32_t x = (i % 4) ? __funnelshift_r(w[i / 4], w[i / 4], 4 * (i % 4)) : w[i / 4];
+    const uint32_t x = slot_shift(w[i / 4], i % 4);
     b0 = field_value<2>(x, 0);
     b1 = field_value<2>(x, 1);
   } else {
     const int i0 = 2 * i, i1 = 2 * i + 1;
-    const uint32_t x0 = (i0 % 4) ? __funnelshift_r(w[i0 / 4], w[i0 / 4], 4 * (i0 % 4)) : w[i0 / 4];
-    const uint32_t x1 = __funnelshift_r(w[i1 / 4], w[i1 / 4], 4 * (i1 % 4));
-    b0 = field_value<4>(x0, 0);
-    b1 = field_value<4>(x1, 1);
+    b0 = field_value<4>(slot_shift(w[i0 / 4], i0 % 4), 0);
+    b1 = field_value<4>(slot_shift(w[i1 / 4], i1 % 4), 1);
   }
 }
 
@@ -488,19 +496,24 @@ template <int D, int BITS, int G>
 __device__ void produce(const DraftArgs& a, uint8_t* smem, int c, uint64_t* full, uint64_t* empty,
                         volatile uint32_t* abort) {
   using P = Plan<D, BITS, G>;
-  long long k = 0;                              // stage uses issued so far (ring position, phase)
+  int buf = 0;                                  // ring position of the next stage use
+  uint32_t phase = 0;                           // completed wraps of the ring, mod 2
+  bool wrapped = false;                         // every buffer used at least once
   const long long hi = range_lo(c + 1, a.total, a.n_stream);
   long long pos = range_lo(c, a.total, a.n_stream);
   Segment sg;
   bool over;
   while (next_segment(a, pos, hi, sg, over)) {
-    for (int s = 0; s < sg.n_st; ++s, ++k) {
-      const int buf = static_cast<int>(k % P::NS);
-      const long long use = k / P::NS;
-      if (use > 0 && !vc_mbar_wait_or_abort(empty + buf, static_cast<uint32_t>((use - 1) & 1), abort, kWaitCycles))
-        return;
+    for (int s = 0; s < sg.n_st; ++s) {
+      // the previous use of `buf` (one wrap earlier) must have been released
+      if (wrapped && !vc_mbar_wait_or_abort(empty + buf, phase ^ 1u, abort, kWaitCycles)) return;
       issue_stage<D, BITS, G>(a, smem + buf * P::stage, full + buf, sg.bh, sg.gs + s * kWarps,
                               min(kWarps, sg.n_valid - s * kWarps));
+      if (++buf == P::NS) {
+        buf = 0;
+        phase ^= 1u;
+        wrapped = true;
+      }
     }
   }
 }
@@ -538,7 +551,8 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
   const uint32_t zcol_mul0 = h2u(__float2half2_rn(!zc ? 0.0f : ((gid & 1) ? -1.0f : 1.0f / f0)));
   const uint32_t zcol_mul1 = h2u(__float2half2_rn(!zc ? 0.0f : ((gid & 1) ? -1.0f : 1.0f / f1)));
   const int zcol_off = zc ? 32 * (gid ^ 1) : 0;
-  long long k = 0;                              // stage uses consumed so far
+  int buf = 0;                                  // ring position and phase of the next stage use
+  uint32_t phase = 0;
   const long long hi = range_lo(c + 1, a.total, a.n_stream);
   long long pos = range_lo(c, a.total, a.n_stream);
   Segment sg;
@@ -568,10 +582,8 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
     st.oz[0] = st.oz[1] = st.oz[2] = st.oz[3] = 0.0f;
     st.l0 = st.l1 = 0.0f;
     st.m = -INFINITY;
-    for (int s = 0; s < sg.n_st; ++s, ++k) {
-      const int buf = static_cast<int>(k % NS);
-      const bool ok = __all_sync(0xffffffffu, vc_mbar_wait_or_abort(full + buf, static_cast<uint32_t>((k / NS) & 1),
-                                                                   abort, kWaitCycles));
+    for (int s = 0; s < sg.n_st; ++s) {
+      const bool ok = __all_sync(0xffffffffu, vc_mbar_wait_or_abort(full + buf, phase, abort, kWaitCycles));
       if (ok && s * kWarps + warp < sg.n_valid) {
         const uint8_t* base = smem + buf * P::stage;
         const uint32_t* kc_g = reinterpret_cast<const uint32_t*>(base + warp * P::codes);
@@ -583,6 +595,10 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
       }
       __syncwarp();
       if (lane == 0) vc_mbar_arrive(empty + buf);          // this warp is done with the stage
+      if (++buf == NS) {
+        buf = 0;
+        phase ^= 1u;
+      }
     }
     // every consumer thread takes the same branch: the OR of the abort flag
     if (vc_bar_red_or(1, kConsumers, *abort != 0u)) {

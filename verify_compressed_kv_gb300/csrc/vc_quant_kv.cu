@@ -29,10 +29,10 @@ constexpr int kGroup = 32;
 // ------------------------------------------------------------------ packed layout
 // Field rules of the packed words (the library's format; include/vc.h): per
 // group, 32 lanes x d*b/32 words; word w of lane L at (w/4)*128 + 4L + w%4.
-// b = 2: slot (u, r, e) starts at bit (8 - 2r + 16e + 4u) mod 32;
-// b = 4: slot (u, e) starts at (6 + 16e + 4u) mod 32, bits taken cyclically.
+// b = 2: slot (u, r, e) starts at bit 16e + 4u + 2(1 - r);
+// b = 4: slot (u, e) starts at 16e + 4u.  No field crosses bit 31.
 __device__ __forceinline__ int field_pos(int bits, int u, int r, int e) {
-  return bits == 2 ? ((8 - 2 * r + 16 * e + 4 * u) & 31) : ((6 + 16 * e + 4 * u) & 31);
+  return bits == 2 ? (16 * e + 4 * u + 2 * (1 - r)) : (16 * e + 4 * u);
 }
 
 // Word `idx` of a group's K codes (V codes when IS_V) from a code tile
@@ -70,7 +70,7 @@ __device__ uint32_t build_word(const uint8_t* codes, int ld, int d, int idx) {
           ch = (d / 4) * c + 4 * lo + 2 * r + e;
         }
         const uint32_t code = codes[t * ld + ch];
-        word |= __funnelshift_l(code, code, field_pos(BITS, u, r, e));
+        word |= code << field_pos(BITS, u, r, e);
       }
     }
   return word;
@@ -346,8 +346,8 @@ __global__ void unpack_kernel(int T, int T_cap, int d, Packed p, float* K_hat, f
     locate<BITS, true>(t, c, d, vi, vp);
     const uint32_t kw = s.kc[static_cast<size_t>(g) * n_words + ki];
     const uint32_t vw = s.vc[static_cast<size_t>(g) * n_words + vi];
-    const float kcode = static_cast<float>(__funnelshift_r(kw, kw, kp) & MASK);
-    const float vcode = static_cast<float>(__funnelshift_r(vw, vw, vp) & MASK);
+    const float kcode = static_cast<float>((kw >> kp) & MASK);
+    const float vcode = static_cast<float>((vw >> vp) & MASK);
     const size_t km = static_cast<size_t>(g) * 2 * d + c;
     const size_t vm = ((static_cast<size_t>(g) * (d / kGroup) + c / kGroup) * 2) * kGroup + vmeta_entry(t);
     const size_t o = (static_cast<size_t>(bh) * T + static_cast<size_t>(g) * kGroup + t) * d + c;
