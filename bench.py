@@ -227,6 +227,26 @@ def ncu_traffic(kernel_file, workload):
         return None
 
 
+def measure_link_gbs(device, stream, mib=512, reps=4):
+    """The link's own peak: best pinned host->device copy of `mib` MiB (the
+    roofline of the H2D stream), measured on this machine at this moment."""
+    import torch
+    h = torch.empty(mib * 2 ** 20, dtype=torch.uint8, pin_memory=True)
+    h.fill_(1)
+    d = torch.empty_like(h, device=device)
+    best = 0.0
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            d.copy_(h, non_blocking=True)
+            e1.record(stream)
+        e1.synchronize()
+        best = max(best, h.numel() / e0.elapsed_time(e1) / 1e6)
+    del h, d
+    return best
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -253,21 +273,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_bufs = [to_device(hi[0], device) for hi in host_inputs]
     torch.cuda.synchronize()
 
-    # ---- the link's own peak: best pinned host->device copy of 512 MiB (the
-    # roofline of the H2D stream), measured on this machine at this moment
-    link_buf_h = torch.empty(512 * 2 ** 20, dtype=torch.uint8, pin_memory=True)
-    link_buf_h.fill_(1)
-    link_buf_d = torch.empty_like(link_buf_h, device=device)
-    link_best = 0.0
-    for _ in range(4):
-        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(xs):
-            l0.record(xs)
-            link_buf_d.copy_(link_buf_h, non_blocking=True)
-            l1.record(xs)
-        l1.synchronize()
-        link_best = max(link_best, link_buf_h.numel() / l0.elapsed_time(l1) / 1e6)
-    del link_buf_h, link_buf_d
+    link_best = measure_link_gbs(device, xs)
     measured_link = link_best if args.link_peak_gbs <= 0 else args.link_peak_gbs
 
     # ---- prefill rows timed once: quantise + pack of the full prefix (layer 0)
@@ -618,6 +624,107 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------- distributed plumbing
+def run_adaptive(args, local_rank):
+    """Fixed draft length (the workload's k) against a per-round draft length
+    chosen by the controller from the previous rounds' measured spans, on one
+    group whose buffers hold up to --k-max draft tokens.  Same process, same
+    prefix, alternating blocks of rounds."""
+    import dataclasses
+
+    import torch
+
+    import synth
+    from verify_compressed_kv_gb300 import runtime as rt
+    from verify_compressed_kv_gb300.schedule import DraftLengthController
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    w = synth.get(args.workload)
+    if w.groups != 1 or w.keep_frac < 1.0:
+        raise SystemExit("--adaptive runs the single-group workloads without token dropping")
+    k_max = max(args.k_max, w.k)
+    choices = sorted({w.k, k_max} | {c for c in range(4, k_max + 1, 4)})
+    rounds_total = args.warmup + 2 * args.steps + 4
+    g = build_group(dataclasses.replace(w, k=k_max), w.layers, device, rounds_total, args.slots)
+    n_inp = 3
+    inputs = {k: [to_device(make_round_inputs(dataclasses.replace(w, k=k), r, 0, device, w.layers), device)
+                  for r in range(n_inp)] for k in choices}
+    cs, xs = torch.cuda.Stream(), torch.cuda.Stream()
+    ctl = DraftLengthController(k_max=k_max, k_min=choices[0], choices=tuple(choices))
+
+    link_gbs = measure_link_gbs(device, xs)
+
+    # verify compute per row: the chunk kernel alone on a resident slot, at the
+    # smallest and the largest draft length (slope = cost of one more row)
+    from verify_compressed_kv_gb300 import _lib as vc
+    g.slots[:g.chunk_elems].copy_(g.host_kv[0][:g.chunk_elems])     # chunk 0 of layer 0 into slot 0
+    torch.cuda.synchronize()
+
+    def chunk_ms(k, reps=20):
+        sh = g.shape_k(k)
+        q = inputs[k][0].q_verify[0]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for i in range(reps + 3):
+            if i == 3:
+                e0.record(cs)
+            vc.vc_verify_attn_chunk(sh, q, g.slots, g.C, 0, g.prefix_len[0], g.parts, True, g.ws_verify,
+                                    g.ws_verify_bytes, cs)
+        e1.record(cs)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps
+    k_lo, k_hi = choices[0], choices[-1]
+    row_chunk_ms = max(0.0, (chunk_ms(k_hi) - chunk_ms(k_lo)) / (k_hi - k_lo))
+    rate = {"bytes_per_ms": link_gbs * 1e6}
+
+    def one(k, r):
+        h2d_bytes = g.h2d_bytes()
+        pf_bytes = g.prefetch_bytes()
+        tl = rt.round_single(g, inputs[k][r % n_inp], cs, xs)
+        tl.ev["end"].synchronize()
+        toks = g.after_round()
+        d_ms, r_ms = tl.ms("draft_start", "draft_end"), tl.ms("start", "end")
+        v_end = tl.ms("start", "verify_end")
+        t_tail = max(0.0, r_ms - v_end)
+        # the transfer alone, at the rate of this round's first slot copies (they
+        # never wait for a slot; the whole span stretches when slots wait for the verify)
+        pf_ms = tl.ms("copy_start", "prefetch_end")
+        if pf_ms > 0 and pf_bytes > 0:
+            rate["bytes_per_ms"] = pf_bytes / pf_ms
+        t_copy = h2d_bytes / rate["bytes_per_ms"]
+        # verify compute of k + 1 rows over every chunk of every layer (calibrated slope)
+        t_verify = (k + 1) * row_chunk_ms * g.chunks() * g.L
+        ctl.observe(g.n_acc_host.numpy(), k, t_step=d_ms / k, t_copy=t_copy, t_tail=t_tail, t_verify=t_verify)
+        return toks, r_ms
+
+    for r in range(args.warmup):
+        one(w.k, r)
+    res = {"fixed": [0, 0.0], "adaptive": [0, 0.0]}
+    chosen = {}
+    r = args.warmup
+    for blk in range(2 * args.steps // 10):                 # blocks of 10 rounds, alternating
+        mode = "fixed" if blk % 2 == 0 else "adaptive"
+        for _ in range(10):
+            k = w.k if mode == "fixed" else ctl.next_k()
+            if mode == "adaptive":
+                chosen[k] = chosen.get(k, 0) + 1
+            toks, ms = one(k, r)
+            res[mode][0] += toks * w.layers
+            res[mode][1] += ms
+            r += 1
+    g.close()
+    val = {m: v[0] / (v[1] / 1e3) for m, v in res.items()}
+    return {"metric": "verified tokens/s/layer", "value": val["adaptive"], "unit": "tokens/s/layer",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "bf16/int%d->f32" % w.bits, "data": "synthetic (seeded)",
+            "config": {"workload": workload_name(w), "schedule": "adaptive draft length", "k_fixed": w.k,
+                       "k_max": k_max, "choices": choices},
+            "fixed_k_value": val["fixed"], "adaptive_over_fixed": val["adaptive"] / val["fixed"],
+            "k_chosen": chosen, "acceptance_estimate": ctl.acceptance(),
+            "measured": {"t_step_ms": ctl.t_step, "t_copy_ms": ctl.t_copy, "t_tail_ms": ctl.t_tail,
+                         "t_verify_row_ms": ctl.t_row, "link_peak_gbs": link_gbs,
+                         "copy_gbs": rate["bytes_per_ms"] / 1e6, "verify_row_chunk_ms": row_chunk_ms}}
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -670,12 +777,17 @@ def main(argv=None):
     ap.add_argument("--link-peak-gbs", type=float, default=0.0,
                     help="pinned host->device peak in GB/s (default 0: measure it at start-up)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--adaptive", action="store_true",
+                    help="compare the fixed draft length with a per-round length chosen by the controller")
+    ap.add_argument("--k-max", type=int, default=60, help="largest draft length of --adaptive (accept takes k + 1 <= 64)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_setup()
     if args.impl == "reference":
         out = run_reference(args, rank, world)
+    elif args.adaptive:
+        out = run_adaptive(args, local) if rank == 0 else None
     else:
         out = run_ours(args, rank, world, local)
     if rank == 0 and out is not None:

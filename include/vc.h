@@ -298,8 +298,11 @@ vc_status_t vc_verify_attn_device_status(uint32_t* status);
  * next_tok[b] = a_{n_acc[b]} (the bonus token when n_acc == k, the full-KV
  * correction otherwise).  logits fp32 [B, k+1, V], draft int32 [B, k];
  * outputs int32 (device); argmax int32 [B, k+1] optional (NULL to skip).
- * NaN logits are unsupported.  The workspace must be zero-filled before its
- * first use; every call leaves it zero-filled again. */
+ * NaN logits are unsupported.  The workspace starts with B per-request
+ * arrival counters at a fixed place: zero-fill the workspace before its first
+ * use; every call leaves the counters at zero, so one workspace, sized for the
+ * largest need, serves calls with any k and V for the same B (the size is not
+ * monotone in k: query it for every k that will be used). */
 vc_status_t vc_accept_workspace_size(int32_t B, int32_t k, int32_t V, size_t* bytes);
 vc_status_t vc_accept(int32_t B, int32_t k, int32_t V, const float* logits, const int32_t* draft,
                       int32_t* n_acc, int32_t* next_tok, int32_t* argmax, void* workspace,

@@ -115,6 +115,36 @@ def test_lossless_with_any_drafter(setup, drafter):
         assert all(a == K_DRAFT for a in acc[:-1])
 
 
+@pytest.mark.parametrize("policy", ["cycle", "controller"])
+def test_lossless_with_a_draft_length_per_round(setup, policy):
+    """The verification period may change every round (Key System Innovations (2)):
+    rounds of 3, 1, 4, 2 draft tokens, or a controller fed a slow transfer and
+    expensive drafting, must leave the output identical."""
+    from verify_compressed_kv_gb300.schedule import DraftLengthController
+    S = setup
+    dec = S["make"](4)
+    lengths = []
+    if policy == "cycle":
+        def pol(r):
+            lengths.append((3, 1, 4, 2)[r % 4])
+            return lengths[-1]
+    else:
+        class Recording(DraftLengthController):
+            def next_k(self):
+                lengths.append(super().next_k())
+                return lengths[-1]
+        pol = Recording(k_max=K_DRAFT, k_min=1)
+        pol.observe([], K_DRAFT, t_step=3.0, t_copy=1.0, t_tail=1.0)     # costs seen on an earlier round
+    try:
+        dec.load_prompt(S["K"], S["V"])
+        out, acc = dec.generate(S["m"], S["first"], PROMPT_LEN, N_NEW, k_policy=pol)
+    finally:
+        dec.close()
+    assert out == S["ref"]
+    assert all(0 <= a <= k for a, k in zip(acc, lengths))
+    assert len(set(lengths)) > 1 if policy == "cycle" else min(lengths) < K_DRAFT
+
+
 def test_gpu_greedy_matches_oracle_greedy(setup):
     """GPU (fp32 accumulate, bf16 attention output) vs oracle (fp64): equal up to
     a numeric near-tie of the oracle's top-2 logits at the first difference."""

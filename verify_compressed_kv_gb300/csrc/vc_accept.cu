@@ -139,15 +139,18 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(
   }
 }
 
+// Workspace: the B arrival counters first (their place does not depend on k
+// or V, so one zero-filled workspace serves calls with any k and V for the
+// same B), then the partial maxima and their indices.
+size_t counter_bytes(int B) { return (static_cast<size_t>(B) * sizeof(unsigned int) + 255) & ~size_t(255); }
+
 size_t ws_bytes(int B, int k, int V) {
   const int rows = B * (k + 1);
   const int S = accept_splits(rows, V);
   size_t part = static_cast<size_t>(rows) * S;
-  size_t bytes = part * sizeof(float);
+  size_t bytes = counter_bytes(B) + part * sizeof(float);
   bytes = (bytes + 255) & ~size_t(255);
   bytes += part * sizeof(int);
-  bytes = (bytes + 255) & ~size_t(255);
-  bytes += static_cast<size_t>(B) * sizeof(unsigned int);
   return bytes;
 }
 
@@ -178,11 +181,11 @@ extern "C" vc_status_t vc_accept(int32_t B, int32_t k, int32_t V, const float* l
   const int rows = B * (k + 1);
   const int S = accept_splits(rows, V);
   char* ws = static_cast<char*>(workspace);
-  float* part_v = reinterpret_cast<float*>(ws);
-  size_t off = (static_cast<size_t>(rows) * S * sizeof(float) + 255) & ~size_t(255);
+  unsigned int* counter = reinterpret_cast<unsigned int*>(ws);
+  size_t off = counter_bytes(B);
+  float* part_v = reinterpret_cast<float*>(ws + off);
+  off = (off + static_cast<size_t>(rows) * S * sizeof(float) + 255) & ~size_t(255);
   int* part_i = reinterpret_cast<int*>(ws + off);
-  off = (off + static_cast<size_t>(rows) * S * sizeof(int) + 255) & ~size_t(255);
-  unsigned int* counter = reinterpret_cast<unsigned int*>(ws + off);
   dim3 grid(S, rows);
   accept_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       logits, draft, k, V, S, part_v, part_i, counter, n_acc, next_tok, argmax);

@@ -91,7 +91,7 @@ class GpuSpeculativeDecoder:
         self.ws_draft = torch.zeros(self.ws_draft_bytes, dtype=torch.uint8, device=self.device)
         self.ws_v_bytes = vc.vc_verify_attn_workspace_size(self.sh, 1)
         self.ws_v = torch.zeros(self.ws_v_bytes, dtype=torch.uint8, device=self.device)
-        self.ws_a_bytes = vc.vc_accept_workspace_size(1, k, vocab)
+        self.ws_a_bytes = max(vc.vc_accept_workspace_size(1, kk, vocab) for kk in range(1, k + 1))
         self.ws_a = torch.zeros(self.ws_a_bytes, dtype=torch.uint8, device=self.device)
         self.k_new = [None] * n_layers
         self.v_new = [None] * n_layers
@@ -165,7 +165,7 @@ class GpuSpeculativeDecoder:
         dr = torch.from_numpy(np.ascontiguousarray(np.asarray(drafts, np.int32)[None])).to(self.device)
         n = torch.empty(1, dtype=torch.int32, device=self.device)
         nxt = torch.empty(1, dtype=torch.int32, device=self.device)
-        vc.vc_accept(1, self.k, self.V, lg, dr, n, nxt, None, self.ws_a, self.ws_a_bytes, self.cs)
+        vc.vc_accept(1, len(drafts), self.V, lg, dr, n, nxt, None, self.ws_a, self.ws_a_bytes, self.cs)
         self.cs.synchronize()
         return int(n.item()), int(nxt.item())
 
@@ -184,17 +184,44 @@ class GpuSpeculativeDecoder:
         self.max_prefix += n_acc + 1
 
     # ------------------------------------------------------------ decoding
-    def generate(self, model, first_token, pos0, n_new, drafter="compressed", reference=None, rng=None):
+    def _shape_k(self, k):
+        """Shape struct for a round that drafts k tokens (k <= the k buffers were sized for)."""
+        if k == self.k:
+            return self.sh
+        if not hasattr(self, "_shapes"):
+            self._shapes = {}
+        if k not in self._shapes:
+            s = self.sh
+            self._shapes[k] = vc.shape(1, s.Hq, s.Hkv, s.d, k=k, bits=s.bits, softmax_scale=s.softmax_scale)
+        return self._shapes[k]
+
+    def generate(self, model, first_token, pos0, n_new, drafter="compressed", reference=None, rng=None,
+                 k_policy=None):
         """Speculative decoding from the last prompt token's prediction
-        ``first_token``; returns (tokens, accepted lengths)."""
+        ``first_token``; returns (tokens, accepted lengths).
+
+        k_policy sets each round's draft length (1 <= k <= the decoder's k): None
+        keeps the decoder's k; an object with next_k() / observe(n_acc, k) (a
+        DraftLengthController) is asked before and told after every round; any
+        other callable is called with the round index."""
         out = [int(first_token)]
         accepted = []
         pos = pos0
+        rnd = 0
         while len(out) < n_new:
+            if k_policy is None:
+                kr = self.k
+            elif hasattr(k_policy, "next_k"):
+                kr = int(k_policy.next_k())
+            else:
+                kr = int(k_policy(rnd))
+            if not 1 <= kr <= self.k:
+                raise ValueError(f"draft length {kr} outside [1, {self.k}]")
+            sh = self._shape_k(kr)
             t_last = out[-1]
             drafts = []
             cur = t_last
-            for i in range(self.k):
+            for i in range(kr):
                 lg, _, _ = model.forward(np.asarray([cur]), np.asarray([pos + i]),
                                          lambda l, q, kk, vv, _i=i: self.draft_attend(l, q, kk, vv, _i))
                 if drafter == "compressed":
@@ -211,10 +238,14 @@ class GpuSpeculativeDecoder:
                     raise ValueError(drafter)
                 drafts.append(cur)
             inputs = np.asarray([t_last] + drafts)
-            vlg, _, _ = model.forward(inputs, pos + np.arange(self.k + 1), self.verify_attend)
+            vlg, _, _ = model.forward(inputs, pos + np.arange(kr + 1),
+                                      lambda l, q, kk, vv: self.verify_attend(l, q, kk, vv, sh=sh))
             n, nxt = self.accept(vlg, drafts)
             accepted.append(n)
-            self.commit(n)
+            if hasattr(k_policy, "observe"):
+                k_policy.observe([n], kr)
+            self.commit(n, sh=sh)
+            rnd += 1
             pos += n + 1
             out.extend(drafts[:n])
             out.append(nxt)

@@ -49,6 +49,11 @@ class RoundInputs:
     logits: torch.Tensor
     drafts: torch.Tensor
 
+    @property
+    def k(self) -> int:
+        """Draft length of this round (<= the group's k)."""
+        return int(self.drafts.shape[1])
+
 
 class Group:
     def __init__(self, B, Hq, Hkv, d, k, bits, V, C, T0, layers=1, extra_tokens=None, n_slots=4,
@@ -91,11 +96,13 @@ class Group:
         # ---- verify ring + workspaces
         self.n_slots = n_slots
         self.slots = _i16(n_slots * self.chunk_elems, dev)
-        self.ws_verify_bytes = vc.vc_verify_attn_workspace_size(self.shape, self.parts)
+        # sized for every draft length a round may use (1 .. k): the needs are not monotone in k
+        self.ws_verify_bytes = max(vc.vc_verify_attn_workspace_size(
+            vc.shape(B, Hq, Hkv, d, k=kk, bits=bits, softmax_scale=softmax_scale), self.parts) for kk in range(1, k + 1))
         self.ws_verify = torch.zeros(self.ws_verify_bytes, dtype=torch.uint8, device=dev)
         self.ws_draft_bytes = vc.vc_draft_attn_workspace_size(self.shape, self.P_cap)
         self.ws_draft = torch.zeros(self.ws_draft_bytes, dtype=torch.uint8, device=dev)
-        self.ws_accept_bytes = vc.vc_accept_workspace_size(B, k, V)
+        self.ws_accept_bytes = max(vc.vc_accept_workspace_size(B, kk, V) for kk in range(1, k + 1))
         self.ws_accept = torch.zeros(self.ws_accept_bytes, dtype=torch.uint8, device=dev)
         # one ring for all layers: its per-slot events order slot reuse across layers too
         self.pipe = vc.vc_verify_pipeline_create(n_slots)
@@ -106,6 +113,25 @@ class Group:
         self.n_acc = torch.zeros(B, dtype=torch.int32, device=dev)
         self.next_tok = torch.zeros(B, dtype=torch.int32, device=dev)
         self.n_acc_host = torch.zeros(B, dtype=torch.int32, pin_memory=True)
+        self._shapes = {}
+
+    def shape_k(self, k):
+        """Shape struct of a round drafting k <= self.k tokens (buffers and
+        workspaces sized for self.k fit every smaller k)."""
+        if k == self.k:
+            return self.shape
+        if not 1 <= k <= self.k:
+            raise ValueError(f"draft length {k} outside [1, {self.k}]")
+        if k not in self._shapes:
+            s = self.shape
+            self._shapes[k] = vc.shape(self.B, self.Hq, self.Hkv, self.d, k=k, bits=self.bits,
+                                       softmax_scale=s.softmax_scale)
+        return self._shapes[k]
+
+    def verify_out_k(self, k):
+        """verify_out viewed as [B, k+1, Hq, d] (its leading elements)."""
+        n = self.B * (k + 1) * self.Hq * self.d
+        return self.verify_out.view(-1)[:n].view(self.B, k + 1, self.Hq, self.d)
 
     def close(self):
         if self.pipe:
@@ -158,9 +184,9 @@ class Group:
         self.launches += 3                     # split-KV, tail, combine
 
     def verify(self, inp: RoundInputs, layer: int, compute_stream, copy_stream):
-        vc.vc_verify_attn_streamed(self.pipe, self.shape, inp.q_verify[layer], self.host_kv[layer], self.C,
+        vc.vc_verify_attn_streamed(self.pipe, self.shape_k(inp.k), inp.q_verify[layer], self.host_kv[layer], self.C,
                                    self.max_prefix, self.prefix_len[layer], self.slots, inp.kv_new[0, layer],
-                                   inp.kv_new[1, layer], self.verify_out, self.parts, self.ws_verify,
+                                   inp.kv_new[1, layer], self.verify_out_k(inp.k), self.parts, self.ws_verify,
                                    self.ws_verify_bytes, compute_stream, copy_stream)
         self.launches += self.chunks() + 1     # one kernel per chunk, then the new-token block + merge
 
@@ -179,18 +205,26 @@ class Group:
         self.launches += self.chunks() + 1
 
     def accept(self, inp: RoundInputs, stream):
-        vc.vc_accept(self.B, self.k, self.V, inp.logits, inp.drafts, self.n_acc, self.next_tok, None,
+        vc.vc_accept(self.B, inp.k, self.V, inp.logits, inp.drafts, self.n_acc, self.next_tok, None,
                      self.ws_accept, self.ws_accept_bytes, stream)
         self.launches += 1
 
     def commit(self, inp: RoundInputs, stream):
+        sh = self.shape_k(inp.k)
         for l in range(self.L):
-            vc.vc_verify_commit(self.shape, inp.kv_new[0, l], inp.kv_new[1, l], self.n_acc, self.prefix_len[l],
+            vc.vc_verify_commit(sh, inp.kv_new[0, l], inp.kv_new[1, l], self.n_acc, self.prefix_len[l],
                                 self.host_kv[l], self.C, self.T_cap, stream)
-            vc.vc_quant_kv_append(self.shape, inp.kv_new[0, l], inp.kv_new[1, l], self.n_acc, self.tail_k[l],
+            vc.vc_quant_kv_append(sh, inp.kv_new[0, l], inp.kv_new[1, l], self.n_acc, self.tail_k[l],
                                   self.tail_v[l], self.tail_len[l], self.tail_cap, self.kc[l], self.ksz[l],
                                   self.vc[l], self.vsz[l], self.packed_len[l], self.P_cap, stream)
             self.launches += 4                 # commit, commit lengths, append, append lengths
+
+    def prefetch_bytes(self):
+        """Bytes prefetch() moves: the first min(n_slots, chunks) chunks of one layer."""
+        total = 0
+        for c in range(min(self.n_slots, self.chunks())):
+            total += 2 * self.B * self.Hkv * min(self.C, self.max_prefix - c * self.C) * self.d * 2
+        return total
 
     def chunks(self):
         return (self.max_prefix + self.C - 1) // self.C
@@ -236,8 +270,9 @@ def round_single(g: Group, inp: RoundInputs, cs, xs, tl: Timeline | None = None)
     xs.wait_event(tl.ev["start"])
     tl.mark("copy_start", xs)
     g.prefetch(0, xs)
+    tl.mark("prefetch_end", xs)            # the first slots' copies: they never wait for a slot
     tl.mark("draft_start", cs)
-    for i in range(g.k):
+    for i in range(inp.k):
         for l in range(g.L):
             g.draft_step(inp, l, i, cs)
     tl.mark("draft_end", cs)
@@ -262,7 +297,7 @@ def round_staggered(X: Group, Y: Group, inp_x: RoundInputs, inp_y: RoundInputs, 
     tl.mark("copy_start", xs)
     Y.prefetch(0, xs)
     tl.mark("draft_start", cs)
-    for i in range(X.k):
+    for i in range(inp_x.k):
         for l in range(X.L):
             X.draft_step(inp_x, l, i, cs)
     tl.mark("draft_end", cs)
@@ -285,7 +320,7 @@ def round_lockstep(groups, inps, cs, xs, tl: Timeline | None = None):
     tl.mark("start", cs)
     tl.mark("draft_start", cs)
     for g, inp in zip(groups, inps):
-        for i in range(g.k):
+        for i in range(inp.k):
             for l in range(g.L):
                 g.draft_step(inp, l, i, cs)
     tl.mark("draft_end", cs)
