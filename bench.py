@@ -725,6 +725,67 @@ def run_adaptive(args, local_rank):
                          "copy_gbs": rate["bytes_per_ms"] / 1e6, "verify_row_chunk_ms": row_chunk_ms}}
 
 
+def run_remote(args, local_rank):
+    """Remote prefix caching, emulated on one GPU: every layer's packed prefix
+    arrives over a slow link paced at --remote-prefix GB/s (real copies through
+    vc_quant_kv_stage_groups), then rounds run as usual with the full KV over
+    the fast local link.  Compared with shipping the full prefix over the same
+    slow link (bytes / rate)."""
+    import torch
+
+    import synth
+    from verify_compressed_kv_gb300 import runtime as rt
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    w = synth.get(args.workload)
+    if w.groups != 1 or w.keep_frac < 1.0:
+        raise SystemExit("--remote-prefix runs the single-group workloads without token dropping")
+    rate = args.remote_prefix
+    rounds = args.warmup + args.steps
+    g = build_group(w, w.layers, device, rounds + 2, args.slots)
+    host = [g.export_packed(l, w.T) for l in range(w.layers)]
+    for l in range(w.layers):                     # the draft cache now only exists remotely
+        for x in (g.kc, g.ksz, g.vc, g.vsz):
+            x[l].zero_()
+        g.packed_len[l].zero_()
+    comp_bytes = sum(h.numel() * h.element_size() for hs in host for h in hs)
+    full_bytes = g.h2d_bytes()
+    inputs = [to_device(make_round_inputs(w, r, 0, device, w.layers), device) for r in range(3)]
+    cs, xs = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for l in range(w.layers):
+        g.stage_packed_remote(l, host[l], w.T, rate, xs)
+    xs.synchronize()
+    stage_ms = (time.perf_counter() - t0) * 1e3
+    t1 = time.perf_counter()
+    tl = rt.round_single(g, inputs[0], cs, xs)
+    tl.ev["end"].synchronize()
+    first_round_ms = (time.perf_counter() - t1) * 1e3
+    first_tokens = g.after_round() * w.layers
+    ms, toks = [], 0
+    for r in range(1, rounds):
+        tl = rt.round_single(g, inputs[r % 3], cs, xs)
+        tl.ev["end"].synchronize()
+        t = g.after_round()
+        if r >= args.warmup:
+            ms.append(tl.ms("start", "end"))
+            toks += t * w.layers
+    g.close()
+    full_ms = full_bytes / (rate * 1e6)
+    ttfr = stage_ms + first_round_ms
+    return {"metric": "time to the first verified round", "value": ttfr, "unit": "ms", "higher_is_better": False,
+            "n_gpus": 1, "data": "synthetic (seeded)",
+            "config": {"workload": workload_name(w), "schedule": "remote prefix caching (emulated, one GPU)",
+                       "slow_link_gbs": rate},
+            "compressed_bytes": comp_bytes, "full_bytes": full_bytes, "bytes_ratio": full_bytes / comp_bytes,
+            "stage_ms": stage_ms, "stage_ms_at_rate": comp_bytes / (rate * 1e6), "first_round_ms": first_round_ms,
+            "first_round_tokens": first_tokens, "full_prefix_over_slow_link_ms": full_ms,
+            "speedup_vs_full_prefix": (full_ms + first_round_ms) / ttfr,
+            "steady_value": toks / (sum(ms) / 1e3) if ms else None, "steady_unit": "tokens/s/layer"}
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -779,6 +840,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--adaptive", action="store_true",
                     help="compare the fixed draft length with a per-round length chosen by the controller")
+    ap.add_argument("--remote-prefix", type=float, default=0.0, metavar="GBS",
+                    help="emulate remote prefix caching: the packed prefix arrives over a link paced at GBS GB/s")
     ap.add_argument("--k-max", type=int, default=60, help="largest draft length of --adaptive (accept takes k + 1 <= 64)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -788,6 +851,8 @@ def main(argv=None):
         out = run_reference(args, rank, world)
     elif args.adaptive:
         out = run_adaptive(args, local) if rank == 0 else None
+    elif args.remote_prefix > 0:
+        out = run_remote(args, local) if rank == 0 else None
     else:
         out = run_ours(args, rank, world, local)
     if rank == 0 and out is not None:

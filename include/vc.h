@@ -179,6 +179,21 @@ vc_status_t vc_gather_kv(const vc_shape_t* s, int32_t T, int32_t keep, const int
                          const uint16_t* K, const uint16_t* V, uint16_t* K_out, uint16_t* V_out,
                          vc_stream_t stream);
 
+/* Staging of a packed cache from pinned host memory (VeriCache, Architecture
+ * Support, Remote Prefix Caching: the compressed KV is what travels over the
+ * slow link to the GPU that drafts).  Copies groups [g0, g1) of every
+ * (request, KV head) from host arrays laid out like the device arrays but with
+ * host_ng groups per (b, h) (kc, vc: d*bits words per group; ksz, vsz: 2*d
+ * fp16 per group) into the device arrays of capacity T_cap: four 2-D
+ * host-to-device copies on `stream`, no kernel.  The host arrays must be
+ * pinned (checked) and stay untouched until the copies complete.  Sets no
+ * lengths: the caller sets packed_len once the groups it needs have landed.
+ * Reads B, Hkv, d, bits. */
+vc_status_t vc_quant_kv_stage_groups(const vc_shape_t* s, const uint32_t* host_kc, const uint16_t* host_ksz,
+                                     const uint32_t* host_vc, const uint16_t* host_vsz, int32_t host_ng,
+                                     int32_t g0, int32_t g1, int32_t T_cap, uint32_t* kc, uint16_t* ksz,
+                                     uint32_t* vc, uint16_t* vsz, vc_stream_t stream);
+
 /* Device status of libvc_quant_kv kernels since the last call: 0 = none.
  * Synchronises the device; clears the flag. */
 vc_status_t vc_quant_kv_device_status(uint32_t* status);

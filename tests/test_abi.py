@@ -104,3 +104,19 @@ def test_misaligned_and_null_pointers_are_rejected_before_launch(vc):
         vc.vc_draft_attn(s, 0x1000, 0x2000, None, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 64, 64, 0x8000, 0x9000,
                          0xa000, 8, 0, 0xb000, 0xc000, 1 << 20, stream=0)
     assert e.value.status == 1
+
+
+def test_stage_groups_checks_ranges_before_any_copy(vc):
+    s = vc.shape(2, 8, 2, 128, bits=2)
+    args = (0x1000, 0x2000, 0x3000, 0x4000)
+    dev = (0x5000, 0x6000, 0x7000, 0x8000)
+    with pytest.raises(vc.VcError) as e:                     # g1 beyond the host store
+        vc.vc_quant_kv_stage_groups(s, *args, 4, 0, 5, 1024, *dev, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(vc.VcError) as e:                     # g1 beyond the device capacity
+        vc.vc_quant_kv_stage_groups(s, *args, 64, 0, 40, 1024, *dev, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(vc.VcError) as e:
+        vc.vc_quant_kv_stage_groups(s, None, *args[1:], 4, 0, 1, 1024, *dev, stream=0)
+    assert e.value.status == 1
+    vc.vc_quant_kv_stage_groups(s, *args, 4, 2, 2, 1024, *dev, stream=0)   # empty range: nothing to do

@@ -71,6 +71,7 @@ _SIGS = {
         "vc_token_select_workspace_size": [I32, I32, I32, POINTER(c_size_t)],
         "vc_token_select": [I32, I32, I32, P, I32, I32, I32, P, P, SZ, P],
         "vc_gather_kv": [S, I32, I32, P, P, P, P, P, P],
+        "vc_quant_kv_stage_groups": [S, P, P, P, P, I32, I32, I32, I32, P, P, P, P, P],
         "vc_quant_kv_device_status": [POINTER(c_uint32)],
     },
     "vc_draft_attn": {
@@ -197,6 +198,12 @@ def vc_token_select(B, Hkv, T, score, keep, keep_last, pool, idx, ws, ws_bytes, 
 def vc_gather_kv(s, T, keep, idx, K, V, K_out, V_out, stream=None):
     _call("vc_gather_kv", ctypes.byref(s), T, keep, _ptr(idx), _ptr(K), _ptr(V), _ptr(K_out),
           _ptr(V_out), _stream(stream))
+
+
+def vc_quant_kv_stage_groups(s, host_kc, host_ksz, host_vc, host_vsz, host_ng, g0, g1, T_cap, kc, ksz, vc, vsz,
+                             stream=None):
+    _call("vc_quant_kv_stage_groups", ctypes.byref(s), _ptr(host_kc), _ptr(host_ksz), _ptr(host_vc), _ptr(host_vsz),
+          host_ng, g0, g1, T_cap, _ptr(kc), _ptr(ksz), _ptr(vc), _ptr(vsz), _stream(stream))
 
 
 def vc_quant_kv_device_status() -> int:

@@ -891,6 +891,44 @@ extern "C" vc_status_t vc_gather_kv(const vc_shape_t* s, int32_t T, int32_t keep
   return VC_OK;
 }
 
+// Groups [g0, g1) of every (request, KV head) of a packed cache held in pinned
+// host memory (layout of the device arrays with host_ng groups per (b, h)) into
+// the device arrays of capacity T_cap: one 2-D copy per array.
+extern "C" vc_status_t vc_quant_kv_stage_groups(const vc_shape_t* s, const uint32_t* host_kc, const uint16_t* host_ksz,
+                                                const uint32_t* host_vc, const uint16_t* host_vsz, int32_t host_ng,
+                                                int32_t g0, int32_t g1, int32_t T_cap, uint32_t* kc, uint16_t* ksz,
+                                                uint32_t* vc, uint16_t* vsz, vc_stream_t stream) {
+  vc_status_t st = check_shape(s, true);
+  if (st != VC_OK) return st;
+  VC_REQUIRE(host_kc && host_ksz && host_vc && host_vsz && kc && ksz && vc && vsz, "NULL pointer");
+  VC_REQUIRE(T_cap >= 0 && T_cap % kGroup == 0, "T_cap must be a non-negative multiple of 32 (got %d)", T_cap);
+  const int NG = T_cap / kGroup;
+  VC_REQUIRE(0 <= g0 && g0 <= g1 && g1 <= host_ng && g1 <= NG, "need 0 <= g0 <= g1 <= min(host_ng, T_cap/32)");
+  if (g0 == g1) return VC_OK;
+  for (const void* p : {static_cast<const void*>(host_kc), static_cast<const void*>(host_ksz),
+                        static_cast<const void*>(host_vc), static_cast<const void*>(host_vsz)}) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess || at.type != cudaMemoryTypeHost) {
+      cudaGetLastError();
+      VC_FAIL(VC_ERR_INVALID_ARG, "the host store must be pinned host memory (cudaHostAlloc / pin_memory)");
+    }
+  }
+  const size_t rows = static_cast<size_t>(s->B) * s->Hkv;
+  const size_t code_g = static_cast<size_t>(s->d) * s->bits * 4;    // bytes of one group's codes
+  const size_t meta_g = static_cast<size_t>(s->d) * 4;              // bytes of one group's metadata
+  auto cs = reinterpret_cast<cudaStream_t>(stream);
+  auto copy2d = [&](void* dst, const void* src, size_t gb) -> cudaError_t {
+    return cudaMemcpy2DAsync(static_cast<char*>(dst) + g0 * gb, NG * gb, static_cast<const char*>(src) + g0 * gb,
+                             static_cast<size_t>(host_ng) * gb, static_cast<size_t>(g1 - g0) * gb, rows,
+                             cudaMemcpyHostToDevice, cs);
+  };
+  VC_CUDA_CHECK(copy2d(kc, host_kc, code_g));
+  VC_CUDA_CHECK(copy2d(ksz, host_ksz, meta_g));
+  VC_CUDA_CHECK(copy2d(vc, host_vc, code_g));
+  VC_CUDA_CHECK(copy2d(vsz, host_vsz, meta_g));
+  return VC_OK;
+}
+
 extern "C" vc_status_t vc_quant_kv_device_status(uint32_t* status) {
   VC_REQUIRE(status, "status is NULL");
   VC_CUDA_CHECK(cudaDeviceSynchronize());

@@ -23,6 +23,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import time
 
 import torch
 
@@ -159,6 +160,46 @@ class Group:
                             self.vsz[layer], stream)
         self.packed_len[layer].fill_(T)
         self.tail_len[layer].zero_()
+
+    # ---------------------------------------------------------------- remote prefix (emulated)
+    def export_packed(self, layer, T):
+        """The packed groups of tokens [0, T) of a layer, in pinned host memory:
+        the store a remote prefix cache would hold (kc, ksz, vc, vsz arrays laid
+        out like the device ones with T/32 groups per (request, KV head))."""
+        ng, NGc, BH = T // GROUP, self.P_cap // GROUP, self.B * self.Hkv
+        out = []
+        for x in (self.kc, self.ksz, self.vc, self.vsz):
+            v = x[layer].view(BH, NGc, -1)[:, :ng].contiguous()
+            out.append(v.cpu().pin_memory())
+        return out
+
+    def stage_packed_remote(self, layer, host, T, link_gbs, stream, groups_per_copy=32):
+        """Stream a remote packed store into the layer's draft cache over an
+        emulated slow link: the copies go out in pieces of `groups_per_copy`
+        groups, each issued no earlier than the time the link would have
+        delivered the bytes before it at `link_gbs` GB/s (host pacing; the copy
+        engine itself runs at the local link's speed).  Returns the host wall
+        time at which the last piece was issued; packed_len is set on `stream`
+        after the last piece."""
+        ng = T // GROUP
+        per_group = sum(h[0, 0].numel() * h.element_size() for h in host) * self.B * self.Hkv
+        t0 = time.perf_counter()
+        sent = 0
+        for g0 in range(0, ng, groups_per_copy):
+            g1 = min(ng, g0 + groups_per_copy)
+            wait = sent / (link_gbs * 1e9) - (time.perf_counter() - t0)
+            if wait > 0:
+                time.sleep(wait)
+            vc.vc_quant_kv_stage_groups(self.shape, host[0], host[1], host[2], host[3], ng, g0, g1, self.P_cap,
+                                        self.kc[layer], self.ksz[layer], self.vc[layer], self.vsz[layer], stream)
+            sent += (g1 - g0) * per_group
+        wait = sent / (link_gbs * 1e9) - (time.perf_counter() - t0)
+        if wait > 0:
+            time.sleep(wait)
+        with torch.cuda.stream(stream):
+            self.packed_len[layer].fill_(T)
+            self.tail_len[layer].zero_()
+        return time.perf_counter() - t0
 
     def write_store(self, layer, K, V):
         """Full prefix K/V [B, Hkv, T, d] (device or host) -> pinned chunk-major store."""
