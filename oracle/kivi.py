@@ -5,7 +5,7 @@ quantisation methods its compressor interface takes (VeriCache, Technical
 Summary, Architecture Support).  The recipe, step by step, for one group of
 32 bf16 values x (widened exactly to fp32):
 
-1. mn = min(x), mx = max(x)
+1. mn = min(x), mx = max(x)                 (b = 2, 4 or 8)
 2. s32 = (mx - mn) / (2^b - 1)             fp32, correctly rounded
 3. s = fp16(s32), z = fp16(mn)             round to nearest even
 4. code = clamp(rint((x - float(z)) / float(s)), 0, 2^b - 1)
@@ -119,11 +119,12 @@ def dequantize_kv(kcode, kscale, kzero, vcode, vscale, vzero):
 
 def _field_pos(bits: int, u: int, r: int, e: int) -> int:
     """Lowest bit of a field.  b = 2: slot (u, r, e) starts at 16e + 4u + 2(1 - r).
-    b = 4: slot (u, e) starts at 16e + 4u (r unused).  The e = 1 field of a
-    slot sits exactly 16 bits above its e = 0 field, in the high half-word."""
+    b = 4: slot (u, e) starts at 16e + 4u; b = 8: slot (u, e) at 16e + 8u (r
+    unused for b = 4, 8).  The e = 1 field of a slot sits exactly 16 bits above
+    its e = 0 field, in the high half-word."""
     if bits == 2:
         return 16 * e + 4 * u + 2 * (1 - r)
-    return 16 * e + 4 * u
+    return 16 * e + bits * u
 
 
 def _word_index(L: int, w: int) -> int:
@@ -132,11 +133,14 @@ def _word_index(L: int, w: int) -> int:
 
 
 def _slot(bits: int, i: int, r: int):
-    """Fragment index i of a lane (and its r) -> (word, u) of its field."""
+    """Fragment index i of a lane (and its r) -> (word, u) of its field.
+    b = 2: word i // 4, u = i % 4.  b = 4, 8: i2 = 2i + r, and a word holds
+    32 / (2b) slots: word i2 // (16 / b), u = i2 % (16 / b)."""
     if bits == 2:
         return i // 4, i % 4
     i2 = 2 * i + r
-    return i2 // 4, i2 % 4
+    per = 16 // bits
+    return i2 // per, i2 % per
 
 
 def _k_fields(d: int, bits: int):

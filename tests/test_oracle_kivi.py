@@ -86,7 +86,7 @@ def test_grouping_axes():
     assert np.all(ks2 > 0)
 
 
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 @pytest.mark.parametrize("d", [64, 128])
 def test_field_tables_are_bijections(bits, d):
     """Every (token, channel) of a group has one field, and the fields of each
@@ -157,7 +157,7 @@ def test_single_codes_land_where_the_rules_say():
     assert w[0] == 0x0B000000 and np.count_nonzero(w) == 1
 
 
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 def test_pack_unpack_bijection(bits):
     rng = np.random.default_rng(11)
     code = rng.integers(0, 1 << bits, size=(2, 3, 96, 128)).astype(np.uint8)
@@ -199,3 +199,20 @@ def test_quant_pack_roundtrip_and_bound_on_workload_inputs():
     vs = np.repeat(vs, 32, axis=3).astype(np.float32)
     assert np.all(np.abs(Kh - Kf) <= ks / 2 * 1.001 + 1e-3)
     assert np.all(np.abs(Vh - Vf) <= vs / 2 * 1.001 + 1e-3)
+
+
+def test_eight_bit_words_by_hand():
+    """b = 8: slot (u, e) starts at 16e + 8u, two slots per word.
+    K codes equal to the channel's bit 0 (e) put a 1 at bits 16 and 24: 0x01010000;
+    code 255 in every e = 1 field: 0xFFFF0000.  One code: K, d = 128, token 5,
+    channel 37 -> lane 5, j = 1, k = 1, r = 0, e = 1; fragment i = 9, i2 = 2*9 + 0 =
+    18 -> word 18 // 2 = 9, u = 0; start 16; stored at (9 // 4)*128 + 4*5 + 9 % 4 = 277:
+    code 200 -> 0x00C80000."""
+    for d in (64, 128):
+        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: c % 2, 8, d) == 0x01010000)
+        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: 255 * (c % 2), 8, d) == 0xFFFF0000)
+        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: (t // 4) % 2, 8, d) == 0x01010000)
+    code = np.zeros((1, 1, 32, 128), np.uint8)
+    code[0, 0, 5, 37] = 200
+    w = kivi.pack_kcodes(code, 8)[0, 0, 0]
+    assert w.shape == (1024,) and w[277] == 0x00C80000 and np.count_nonzero(w) == 1
