@@ -69,7 +69,7 @@ typedef struct {
   int32_t Hkv;           /* KV heads, Hq % Hkv == 0, G = Hq / Hkv <= 8 */
   int32_t d;             /* head dim: 64 or 128 */
   int32_t k;             /* draft length; verify has k + 1 rows per request */
-  int32_t bits;          /* KIVI code width: 2 or 4 */
+  int32_t bits;          /* KIVI code width: 2, 4 or 8 */
   float softmax_scale;   /* logits = softmax_scale * q . k */
 } vc_shape_t;
 
@@ -101,11 +101,11 @@ const char* vc_last_error(void);
  *                                       entry 8c + 4s + 2r + e = token 8c + 4e + 2s + r
  * Fields (bit 0 = least significant):
  *   bits = 2: slot (u, r, e) starts at 16e + 4u + 2(1 - r);
- *   bits = 4: slot (u, e) starts at 16e + 4u.
+ *   bits = 4: slot (u, e) starts at 16e + 4u;  bits = 8: at 16e + 8u.
  * Lane L = 4a + c.  K: tokens 4a + j (j < 4), channels (d/4)c + 4k + 2r + e
  * (k < d/16), fragment i = j*(d/16) + k.  V: tokens 8c + 4e + 2s + r, channels
  * 8n + a (n < d/8), fragment i = s*(d/8) + n.  bits = 2: word i/4, u = i%4;
- * bits = 4: i2 = 2i + r, word i2/4, u = i2%4.
+ * bits = 4, 8: i2 = 2i + r, SPW = 16/bits slots per word, word i2/SPW, u = i2%SPW.
  * Bytes per token per KV head: d*bits/4 (codes) + d/4 (metadata).
  */
 
@@ -216,8 +216,9 @@ vc_status_t vc_quant_kv_device_status(uint32_t* status);
  * The packed tokens go through fp16 tensor-core products with fp32
  * accumulation: key scales fold into the query and value scales into the
  * softmax weights, each fold kept as an fp16 (hi, lo) pair (~22 bits).  Range
- * limits of those fp16 operands: |q| * key scale * 16 and 128 * value scale *
- * 16 must stay below 65504.  G = Hq / Hkv in {1, 2, 4, 5, 8}; softmax_scale > 0.
+ * limits of those fp16 operands, with f = 16 (bits 2, 4) or 256 (bits 8):
+ * |q| * key scale * f and 8 * f * value scale must stay below 65504.
+ * G = Hq / Hkv in {1, 2, 4, 5, 8}; softmax_scale > 0.
  * The workspace holds the partials and one arrival
  * counter per slice: it must be zero-filled before its first use, and every
  * call leaves the counters at zero again.  Its size depends on the device

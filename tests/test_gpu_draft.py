@@ -55,6 +55,8 @@ CASES = [
     ("llama_small", dict(B=2, T=1024, layers=1), [1024, 512], [0, 9], 0, True),
     ("g1_d64_b2", dict(B=1, Hq=2, Hkv=2, d=64, bits=2, T=640), [640], [4], 0, True),
     ("g2_d128_b4", dict(B=1, Hq=4, Hkv=2, d=128, bits=4, T=256), [256], [0], 0, True),
+    ("mistral_int8", dict(B=2, T=1024, bits=8), [1024, 480], [3, 0], 1, True),
+    ("g8_d64_b8", dict(B=1, Hq=8, Hkv=1, d=64, bits=8, T=320), [320], [5], 0, True),
 ]
 
 

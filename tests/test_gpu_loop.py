@@ -5,10 +5,10 @@ A tiny random-init 2-layer decoder (Hq=4, Hkv=1, d=64, vocab 1024) runs the
 draft/verify/accept loop through the C ABI (drafting over the packed cache,
 verification over the full KV streamed from pinned host memory, accept,
 commit) and must reproduce, token for token, plain greedy decoding through
-the same verify kernel with k = 0, for every compressor (int4, int2, token
-drop + int4) and for drafters of any quality.  The GPU greedy stream is also
-compared with the oracle's fp64 greedy stream; a difference there is allowed
-only at a numeric near-tie of the oracle's logits.
+the same verify kernel with k = 0, for every compressor (int4, int2, int8,
+token drop + int4 or int2) and for drafters of any quality.  The GPU greedy
+stream is also compared with the oracle's fp64 greedy stream; a difference
+there is allowed only at a numeric near-tie of the oracle's logits.
 """
 import numpy as np
 import pytest
@@ -80,7 +80,8 @@ def token_drop_on_gpu(s, K, V, qs, m):
     return dK, dV
 
 
-@pytest.mark.parametrize("bits,drop", [(4, False), (2, False), (4, True)], ids=["int4", "int2", "drop+int4"])
+@pytest.mark.parametrize("bits,drop", [(4, False), (2, False), (8, False), (4, True), (2, True)],
+                         ids=["int4", "int2", "int8", "drop+int4", "drop+int2"])
 def test_lossless_with_compressed_drafter(setup, bits, drop):
     S = setup
     dec = S["make"](bits)

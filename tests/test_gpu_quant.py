@@ -63,7 +63,7 @@ def assert_packed_equal(got, want, NG=None):
 
 
 @pytest.mark.parametrize("B,H,T,d,bits", [(1, 1, 512, 64, 4), (2, 2, 1024, 128, 2), (2, 3, 96, 128, 4),
-                                          (1, 2, 64, 64, 2)])
+                                          (1, 2, 64, 64, 2), (2, 2, 256, 128, 8), (1, 1, 96, 64, 8)])
 def test_pack_bit_exact(vc, B, H, T, d, bits):
     w = synth.get("mistral", B=B, Hkv=H, Hq=H, T=T, d=d, bits=bits)
     K, V = synth.kv(w)
@@ -96,7 +96,7 @@ def test_pack_hand_worked_groups(vc):
         assert vs[0, 0, 7, 1] == np.float16(c["scale"]) and vz[0, 0, 7, 1] == np.float16(c["zero"])
 
 
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 def test_unpack_bit_exact(vc, bits):
     from gpu_util import DEV
     w = synth.get("mistral", B=2, Hkv=2, Hq=2, T=256, bits=bits)
@@ -121,7 +121,7 @@ def test_pack_full_size_sampled(vc):
         assert_packed_equal([g[b:b + 1, h:h + 1] for g in got], want)
 
 
-@pytest.mark.parametrize("bits,k", [(4, 4), (2, 16), (2, 33)])
+@pytest.mark.parametrize("bits,k", [(4, 4), (2, 16), (2, 33), (8, 7)])
 def test_append_matches_oracle_commit(vc, bits, k):
     from gpu_util import dev, DEV
     B, H, d = 3, 2, 64 if bits == 4 else 128

@@ -182,15 +182,21 @@ __device__ __forceinline__ void split_mul(__half2 x, __half2 y, uint32_t& hi, ui
 //   b = 2, r = 0: bits 8-9 of each half -> 1 + code/4   (f = 4)
 //   b = 2, r = 1: bits 6-7              -> 1 + code/16  (f = 16)
 //   b = 4:        bits 6-9              -> 1 + code/16  (f = 16)
+//   b = 8:        bits 2-9              -> 1 + code/256 (f = 256)
 template <int BITS>
 __device__ __forceinline__ uint32_t field_value(uint32_t x, int r) {
   if (BITS == 2) return r == 0 ? ((x & 0x03000300u) | 0x3C003C00u) : ((x & 0x00C000C0u) | 0x3C003C00u);
+  if (BITS == 8) return (x & 0x03FC03FCu) | 0x3C003C00u;
   return (x & 0x03C003C0u) | 0x3C003C00u;
 }
 template <int BITS>
-__host__ __device__ constexpr float field_scale(int r) { return (BITS == 2 && r == 0) ? 4.0f : 16.0f; }
+__host__ __device__ constexpr float field_scale(int r) {
+  return BITS == 8 ? 256.0f : ((BITS == 2 && r == 0) ? 4.0f : 16.0f);
+}
 template <int BITS>
-__host__ __device__ constexpr float field_log2(int r) { return (BITS == 2 && r == 0) ? 2.0f : 4.0f; }
+__host__ __device__ constexpr float field_log2(int r) {
+  return BITS == 8 ? 8.0f : ((BITS == 2 && r == 0) ? 2.0f : 4.0f);
+}
 
 // Word w moved so that slot u's fields land in the operand windows: the e = 0
 // field of slot u starts at 4u + 2(1 - r) (b = 2) or 4u (b = 4), so a shift by
@@ -199,20 +205,25 @@ __host__ __device__ constexpr float field_log2(int r) { return (BITS == 2 && r =
 __device__ __forceinline__ uint32_t slot_shift(uint32_t w, int u) {
   return u == 0 ? (w << 6) : u == 1 ? (w << 2) : u == 2 ? (w >> 2) : (w >> 6);
 }
+// b = 8: the e = 0 field of slot u starts at 8u; a shift by 8u - 2 brings it to bit 2.
+__device__ __forceinline__ uint32_t slot_shift8(uint32_t w, int u) { return u == 0 ? (w << 2) : (w >> 6); }
 
 // Operand registers (r = 0, 1) of fragment index i — the field rules of the
 // packed words (include/vc.h): b = 2: word i/4, slot u = i%4; b = 4: i2 = 2i + r,
-// word i2/4, slot u = i2%4.
+// word i2/4, slot u = i2%4; b = 8: word (2i + r)/2 = i, slot u = r.
 template <int BITS, int WPL>
 __device__ __forceinline__ void fragment(const uint32_t (&w)[WPL], int i, uint32_t& b0, uint32_t& b1) {
   if (BITS == 2) {
     const uint32_t x = slot_shift(w[i / 4], i % 4);
     b0 = field_value<2>(x, 0);
     b1 = field_value<2>(x, 1);
-  } else {
+  } else if (BITS == 4) {
     const int i0 = 2 * i, i1 = 2 * i + 1;
     b0 = field_value<4>(slot_shift(w[i0 / 4], i0 % 4), 0);
     b1 = field_value<4>(slot_shift(w[i1 / 4], i1 % 4), 1);
+  } else {                                   // b = 8: word i holds slots u = 0 (r = 0) and 1 (r = 1)
+    b0 = field_value<8>(slot_shift8(w[i], 0), 0);
+    b1 = field_value<8>(slot_shift8(w[i], 1), 1);
   }
 }
 
@@ -726,7 +737,7 @@ vc_status_t check(const vc_shape_t* s) {
   VC_REQUIRE(s != nullptr, "shape is NULL");
   VC_REQUIRE(s->B >= 1 && s->Hkv >= 1 && s->Hq >= s->Hkv && s->Hq % s->Hkv == 0, "bad B/Hq/Hkv");
   if (s->d != 64 && s->d != 128) VC_FAIL(VC_ERR_UNSUPPORTED, "head dim %d not in {64, 128}", s->d);
-  if (s->bits != 2 && s->bits != 4) VC_FAIL(VC_ERR_UNSUPPORTED, "bits %d not in {2, 4}", s->bits);
+  if (s->bits != 2 && s->bits != 4 && s->bits != 8) VC_FAIL(VC_ERR_UNSUPPORTED, "bits %d not in {2, 4, 8}", s->bits);
   const int G = s->Hq / s->Hkv;
   if (G != 1 && G != 2 && G != 4 && G != 5 && G != 8) VC_FAIL(VC_ERR_UNSUPPORTED, "G = %d not in {1,2,4,5,8}", G);
   VC_REQUIRE(s->softmax_scale > 0.0f, "softmax_scale must be positive");
@@ -778,7 +789,7 @@ vc_status_t plan(const vc_shape_t* s, int max_packed, LaunchPlan* lp) {
 #define VC_PLAN(D_, B_, G_) \
   if (s->d == D_ && s->bits == B_ && G == G_) return plan_t<D_, B_, G_>(s, max_packed, lp);
 #define VC_PLAN_G(D_, B_) VC_PLAN(D_, B_, 1) VC_PLAN(D_, B_, 2) VC_PLAN(D_, B_, 4) VC_PLAN(D_, B_, 5) VC_PLAN(D_, B_, 8)
-  VC_PLAN_G(128, 2) VC_PLAN_G(128, 4) VC_PLAN_G(64, 2) VC_PLAN_G(64, 4)
+  VC_PLAN_G(128, 2) VC_PLAN_G(128, 4) VC_PLAN_G(128, 8) VC_PLAN_G(64, 2) VC_PLAN_G(64, 4) VC_PLAN_G(64, 8)
 #undef VC_PLAN_G
 #undef VC_PLAN
   VC_FAIL(VC_ERR_UNSUPPORTED, "no kernel for d=%d bits=%d G=%d", s->d, s->bits, G);
@@ -806,7 +817,7 @@ vc_status_t launch(const vc_shape_t* s, const DraftArgs& a, const LaunchPlan& lp
 #define VC_L(D_, B_, G_) \
   if (s->d == D_ && s->bits == B_ && G == G_) return launch_t<D_, B_, G_>(a, lp, cs);
 #define VC_L_G(D_, B_) VC_L(D_, B_, 1) VC_L(D_, B_, 2) VC_L(D_, B_, 4) VC_L(D_, B_, 5) VC_L(D_, B_, 8)
-  VC_L_G(128, 2) VC_L_G(128, 4) VC_L_G(64, 2) VC_L_G(64, 4)
+  VC_L_G(128, 2) VC_L_G(128, 4) VC_L_G(128, 8) VC_L_G(64, 2) VC_L_G(64, 4) VC_L_G(64, 8)
 #undef VC_L_G
 #undef VC_L
   VC_FAIL(VC_ERR_UNSUPPORTED, "no kernel for d=%d bits=%d G=%d", s->d, s->bits, G);

@@ -3,7 +3,7 @@
 // Architecture Support: token-dropping and quantisation methods, e.g. KIVI
 // and SnapKV, plug in without touching scheduling or verification).
 //
-//   * KIVI-style quantiser: int2/int4 codes, keys per channel over 32 tokens,
+//   * KIVI-style quantiser: int2/int4/int8 codes, keys per channel over 32 tokens,
 //     values per token over 32 channels, fp16 scale/zero from min/max,
 //     round-half-even.  pack (prefill), append (commit of accepted tokens +
 //     packing of full tail groups), unpack (tests).
@@ -30,32 +30,33 @@ constexpr int kGroup = 32;
 // Field rules of the packed words (the library's format; include/vc.h): per
 // group, 32 lanes x d*b/32 words; word w of lane L at (w/4)*128 + 4L + w%4.
 // b = 2: slot (u, r, e) starts at bit 16e + 4u + 2(1 - r);
-// b = 4: slot (u, e) starts at 16e + 4u.  No field crosses bit 31.
+// b = 4: slot (u, e) starts at 16e + 4u; b = 8: at 16e + 8u.  No field crosses bit 31.
 __device__ __forceinline__ int field_pos(int bits, int u, int r, int e) {
-  return bits == 2 ? (16 * e + 4 * u + 2 * (1 - r)) : (16 * e + 4 * u);
+  return bits == 2 ? (16 * e + 4 * u + 2 * (1 - r)) : (16 * e + bits * u);
 }
 
 // Word `idx` of a group's K codes (V codes when IS_V) from a code tile
 // codes[t * ld + c].  K: lane L = 4a + c holds tokens 4a + j, channels
 // (d/4) c + 4k + 2r + e, fragment i = j*(d/16) + k.  V: tokens 8c + 4e + 2s + r,
 // channels 8n + a, fragment i = s*(d/8) + n.  b = 2: word i/4, u = i%4;
-// b = 4: i2 = 2i + r, word i2/4, u = i2%4.
+// b = 4, 8: i2 = 2i + r, SPW = 16/b slots per word, word i2/SPW, u = i2%SPW.
 template <int BITS, bool IS_V>
 __device__ uint32_t build_word(const uint8_t* codes, int ld, int d, int idx) {
   const int L = (idx % 128) / 4, w = (idx / 128) * 4 + idx % 4;
   const int a = L / 4, c = L % 4;
   const int per = IS_V ? d / 8 : d / 16;          // fragments per j (K) or per s (V)
+  constexpr int SPW = BITS == 2 ? 4 : 16 / BITS;   // slots per word
   uint32_t word = 0;
 #pragma unroll
-  for (int u = 0; u < 4; ++u)
+  for (int u = 0; u < SPW; ++u)
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       int i;
       if (BITS == 2) {
         i = 4 * w + u;
       } else {
-        const int i2 = 4 * w + u;
-        if ((i2 & 1) != r) continue;              // b = 4: slot u carries one r
+        const int i2 = SPW * w + u;
+        if ((i2 & 1) != r) continue;              // b = 4, 8: slot u carries one r
         i = i2 >> 1;
       }
       const int hi = i / per, lo = i % per;         // (j, k) for K, (s, n) for V
@@ -324,9 +325,10 @@ __device__ __forceinline__ void locate(int t, int ch, int d, int& idx, int& pos)
     w = i / 4;
     u = i % 4;
   } else {
+    constexpr int SPW = 16 / BITS;
     const int i2 = 2 * i + r;
-    w = i2 / 4;
-    u = i2 % 4;
+    w = i2 / SPW;
+    u = i2 % SPW;
   }
   idx = (w / 4) * 128 + 4 * L + w % 4;
   pos = field_pos(BITS, u, r, e);
@@ -686,7 +688,8 @@ vc_status_t check_shape(const vc_shape_t* s, bool need_bits) {
   VC_REQUIRE(s != nullptr, "shape is NULL");
   VC_REQUIRE(s->B >= 1 && s->Hkv >= 1, "need B >= 1 and Hkv >= 1");
   if (s->d != 64 && s->d != 128) VC_FAIL(VC_ERR_UNSUPPORTED, "head dim %d not in {64, 128}", s->d);
-  if (need_bits && s->bits != 2 && s->bits != 4) VC_FAIL(VC_ERR_UNSUPPORTED, "bits %d not in {2, 4}", s->bits);
+  if (need_bits && s->bits != 2 && s->bits != 4 && s->bits != 8)
+    VC_FAIL(VC_ERR_UNSUPPORTED, "bits %d not in {2, 4, 8}", s->bits);
   return VC_OK;
 }
 
@@ -725,8 +728,10 @@ extern "C" vc_status_t vc_quant_kv_pack(const vc_shape_t* s, int32_t T, int32_t 
   auto cs = reinterpret_cast<cudaStream_t>(stream);
   if (s->bits == 2)
     pack_kernel<2><<<grid, kPackThreads, sm, cs>>>(K, V, T, T_cap, s->d, p);
-  else
+  else if (s->bits == 4)
     pack_kernel<4><<<grid, kPackThreads, sm, cs>>>(K, V, T, T_cap, s->d, p);
+  else
+    pack_kernel<8><<<grid, kPackThreads, sm, cs>>>(K, V, T, T_cap, s->d, p);
   VC_LAUNCH_CHECK("pack_kernel");
   return VC_OK;
 }
@@ -745,8 +750,10 @@ extern "C" vc_status_t vc_quant_kv_unpack(const vc_shape_t* s, int32_t T, int32_
   auto cs = reinterpret_cast<cudaStream_t>(stream);
   if (s->bits == 2)
     unpack_kernel<2><<<grid, 256, 0, cs>>>(T, T_cap, s->d, p, K_hat, V_hat);
-  else
+  else if (s->bits == 4)
     unpack_kernel<4><<<grid, 256, 0, cs>>>(T, T_cap, s->d, p, K_hat, V_hat);
+  else
+    unpack_kernel<8><<<grid, 256, 0, cs>>>(T, T_cap, s->d, p, K_hat, V_hat);
   VC_LAUNCH_CHECK("unpack_kernel");
   return VC_OK;
 }
@@ -769,8 +776,11 @@ extern "C" vc_status_t vc_quant_kv_append(const vc_shape_t* s, const uint16_t* k
   if (s->bits == 2)
     append_kernel<2><<<dim3(s->Hkv, s->B), kPackThreads, sm, cs>>>(k_new, v_new, n_acc, s->k, s->Hkv, s->d, tail_k,
                                                                      tail_v, tail_len, tail_cap, p, packed_len, T_cap);
-  else
+  else if (s->bits == 4)
     append_kernel<4><<<dim3(s->Hkv, s->B), kPackThreads, sm, cs>>>(k_new, v_new, n_acc, s->k, s->Hkv, s->d, tail_k,
+                                                                     tail_v, tail_len, tail_cap, p, packed_len, T_cap);
+  else
+    append_kernel<8><<<dim3(s->Hkv, s->B), kPackThreads, sm, cs>>>(k_new, v_new, n_acc, s->k, s->Hkv, s->d, tail_k,
                                                                      tail_v, tail_len, tail_cap, p, packed_len, T_cap);
   VC_LAUNCH_CHECK("append_kernel");
   append_lengths_kernel<<<1, 256, 0, cs>>>(n_acc, s->B, s->k, tail_len, tail_cap, packed_len, T_cap);
