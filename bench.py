@@ -257,7 +257,7 @@ def run_ours(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     from verify_compressed_kv_gb300 import runtime as rt
 
-    w = synth.get(args.workload)
+    w = workload_of(args)
     layers = w.layers
     n_groups = w.groups
     rounds_total = args.warmup + args.steps + 1
@@ -512,13 +512,23 @@ def run_ours(args, rank, world, local_rank):
     return out
 
 
+def workload_of(args):
+    """The workload, with --bits overriding its code width."""
+    import synth
+    return synth.get(args.workload, **({"bits": args.bits} if args.bits else {}))
+
+
 def workload_name(w):
     names = {"tiny": "tiny 1x(Hq4,Hkv1,d64) T512 k4 int4",
              "mistral": "Mistral-24B-shaped layer: B8 Hq32 Hkv8 d128 T32768 k16 int2",
              "qwen": "Qwen-32B-shaped layer: B16 Hq40 Hkv8 d128 T65536 (keep 25%) k32 int4",
              "llama": "Llama-70B-shaped 8 layers: B4 Hq64 Hkv8 d128 T131072 k32 int2",
              "stagger": "staggered mix: 2x B32 Hq32 Hkv8 d128 T32768 k24 int2"}
-    return names.get(w.name, w.name)
+    name = names.get(w.name, w.name)
+    own = {"tiny": 4, "mistral": 2, "qwen": 4, "llama": 2, "stagger": 2}.get(w.name)
+    if own is not None and w.bits != own:
+        name = name.replace(f"int{own}", f"int{w.bits}")
+    return name
 
 
 # ---------------------------------------------------------------- CPU oracle leg
@@ -639,7 +649,7 @@ def run_adaptive(args, local_rank):
 
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
-    w = synth.get(args.workload)
+    w = workload_of(args)
     if w.groups != 1 or w.keep_frac < 1.0:
         raise SystemExit("--adaptive runs the single-group workloads without token dropping")
     k_max = max(args.k_max, w.k)
@@ -738,7 +748,7 @@ def run_remote(args, local_rank):
 
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
-    w = synth.get(args.workload)
+    w = workload_of(args)
     if w.groups != 1 or w.keep_frac < 1.0:
         raise SystemExit("--remote-prefix runs the single-group workloads without token dropping")
     rate = args.remote_prefix
@@ -840,6 +850,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--adaptive", action="store_true",
                     help="compare the fixed draft length with a per-round length chosen by the controller")
+    ap.add_argument("--bits", type=int, default=0, choices=[0, 2, 4, 8],
+                    help="KIVI code width instead of the workload's own (0: keep it)")
     ap.add_argument("--remote-prefix", type=float, default=0.0, metavar="GBS",
                     help="emulate remote prefix caching: the packed prefix arrives over a link paced at GBS GB/s")
     ap.add_argument("--k-max", type=int, default=60, help="largest draft length of --adaptive (accept takes k + 1 <= 64)")
