@@ -247,6 +247,57 @@ def measure_link_gbs(device, stream, mib=512, reps=4):
     return best
 
 
+def time_kernel(fn, stream, reps=20, warm=3):
+    """Average CUDA-event time (ms) of fn() on `stream`."""
+    import torch
+    for _ in range(warm):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def alu_peak_tflops(peaks):
+    """fp32 CUDA-core peak: 152 SMs x 128 lanes x 2 flops per FMA x the maximum SM clock."""
+    return 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+
+
+def time_token_drop(w, shape, Kd, Vd, device, cs):
+    """Score, select and gather of the token-dropping compressor on layer 0,
+    each timed alone against its roofline."""
+    import numpy as np
+    import torch
+
+    import synth
+    from verify_compressed_kv_gb300 import _lib as vc
+    peaks = load_peaks()
+    keep = w.T_keep
+    qo = torch.from_numpy(synth.q_obs(w).view(np.int16)).to(device)
+    score = torch.empty((w.B, w.Hkv, w.T), dtype=torch.float32, device=device)
+    wsb = vc.vc_token_score_workspace_size(shape, w.T, 32)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=device)
+    t_score = time_kernel(lambda: vc.vc_token_score(shape, w.T, 32, qo, Kd, score, ws, wsb, cs), cs, reps=5)
+    flops = 4.0 * w.B * w.Hq * 32 * w.T * w.d            # QK in both passes, 2 flops per multiply-add
+    wsb2 = vc.vc_token_select_workspace_size(w.B, w.Hkv, w.T)
+    ws2 = torch.empty(wsb2, dtype=torch.uint8, device=device)
+    idx = torch.empty((w.B, w.Hkv, keep), dtype=torch.int32, device=device)
+    t_sel = time_kernel(lambda: vc.vc_token_select(w.B, w.Hkv, w.T, score, keep, 32, 7, idx, ws2, wsb2, cs), cs, reps=5)
+    Ko = torch.empty((w.B, w.Hkv, keep, w.d), dtype=torch.int16, device=device)
+    Vo = torch.empty_like(Ko)
+    t_gat = time_kernel(lambda: vc.vc_gather_kv(shape, w.T, keep, idx, Kd, Vd, Ko, Vo, cs), cs, reps=10)
+    gat_bytes = 2 * 2 * w.B * w.Hkv * keep * w.d * 2
+    return {"a3_token_score": {"ms": t_score, "tflops": flops / (t_score / 1e3) / 1e12, "bound": "alu",
+                               "peak_tflops": alu_peak_tflops(peaks),
+                               "frac": flops / (t_score / 1e3) / 1e12 / alu_peak_tflops(peaks)},
+            "a4_token_select": {"ms": t_sel, "bound": "latency (6 passes over the pooled scores)"},
+            "a4_gather": {"ms": t_gat, "gbs": gat_bytes / (t_gat / 1e3) / 1e9, "bound": "hbm",
+                          "frac": gat_bytes / (t_gat / 1e3) / 1e9 / peaks["hbm_gbs"]}}
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -294,6 +345,9 @@ def run_ours(args, rank, world, local_rank):
     e1.synchronize()
     pack_ms = e0.elapsed_time(e1) / 5
     pack_bytes = 2 * w.B * w.Hkv * w.T * w.d * 2 + sum(sb)
+    prefill_rows = {}
+    if w.keep_frac < 1.0:
+        prefill_rows = time_token_drop(w, g0.shape, K0d, V0d, device, cs)
     del K0d, V0d, scratch
     torch.cuda.synchronize()
 
@@ -416,6 +470,26 @@ def run_ours(args, rank, world, local_rank):
     # inside the timed rounds: average draft call = draft span / (k * layers)
     draft_in_round_ms = med(draft_span) / (w.k * layers)
 
+    # ---- the other rows of the path, each timed alone against its roofline
+    g.slots[:g.chunk_elems].copy_(g.host_kv[0][:g.chunk_elems])       # one resident chunk
+    torch.cuda.synchronize()
+    t_ver = time_kernel(lambda: vc.vc_verify_attn_chunk(g.shape, inp.q_verify[0], g.slots, g.C, 0, g.prefix_len[0],
+                                                        g.parts, True, g.ws_verify, g.ws_verify_bytes, cs), cs)
+    ver_flops = 4.0 * w.B * w.Hq * (w.k + 1) * w.C * w.d               # QK and PV of (k+1)*Hq rows x C tokens
+    t_acc = time_kernel(lambda: g.accept(inp, cs), cs)
+    acc_bytes = w.B * (w.k + 1) * w.V * 4
+    rows = {
+        "a1_pack": {"ms": pack_ms, "gbs": pack_bytes / (pack_ms / 1e3) / 1e9, "bound": "hbm",
+                    "frac": pack_bytes / (pack_ms / 1e3) / 1e9 / peaks["hbm_gbs"]},
+        "a5_draft": {"ms": draft_call_ms, "gbs": achieved_gbs, "bound": "hbm", "frac": achieved_gbs / peaks["hbm_gbs"]},
+        "a7_verify_chunk": {"ms": t_ver, "tflops": ver_flops / (t_ver / 1e3) / 1e12, "bound": "tensor (bf16)",
+                            "frac": ver_flops / (t_ver / 1e3) / 1e12 / peaks["bf16_tflops"],
+                            "chunk_transfer_ms": g.chunk_elems * 2 / (measured_link * 1e6)},
+        "a8_accept": {"ms": t_acc, "gbs": acc_bytes / (t_acc / 1e3) / 1e9, "bound": "hbm",
+                      "frac": acc_bytes / (t_acc / 1e3) / 1e9 / peaks["hbm_gbs"]},
+    }
+    rows.update(prefill_rows)
+
     # ---- context: plain full-KV decoding (one token per request per step), the
     # full KV of every layer streamed from pinned host memory each step as in the
     # pages' long-context scenario, through the same streamed verify kernel (k = 0)
@@ -502,6 +576,7 @@ def run_ours(args, rank, world, local_rank):
                      "all": [round(x, 3) for x in round_ms],
                      "host_gap_total": round(total_ms - sum(round_ms), 3)},
         "prefill_pack": {"ms": pack_ms, "gbs": pack_bytes / (pack_ms / 1e3) / 1e9},
+        "rows": rows,
         "full_kv_decode": dict(full_kv, speedup_of_value=value_local / full_kv["value"]),
         "clocks": clk,
     }
