@@ -73,6 +73,37 @@ def test_pack_bit_exact(vc, B, H, T, d, bits):
     assert_packed_equal(got, want, NG=T // 32)
 
 
+def tie_grid(rng, shape, bits, step, group_axis):
+    """bf16 bits of values on a grid of half a scale step, with every 32-group's min
+    and max pinned to 0 and qmax*step: (x - z)/s is an exact half-integer for half
+    of the elements, so round-half-even decides their codes."""
+    qmax = (1 << bits) - 1
+    m = rng.integers(0, min(2 * qmax, 256) + 1, size=shape)          # <= 8 significant bits
+    x = m.astype(np.float32) * np.float32(step / 2)
+    x = np.moveaxis(x, group_axis, -1).copy()
+    grp = x.reshape(*x.shape[:-1], -1, 32)
+    grp[..., 0] = 0.0
+    grp[..., 1] = qmax * step
+    x = np.moveaxis(grp.reshape(x.shape), -1, group_axis)
+    b = x.astype(np.float32).view(np.uint32)
+    assert np.all((b & 0xFFFF) == 0), "grid values must be exact in bf16"
+    return np.ascontiguousarray((b >> 16).astype(np.uint16))
+
+
+@pytest.mark.parametrize("bits,step", [(2, 0.5), (2, 1.5), (4, 0.125), (4, 0.375), (8, 0.0625)])
+def test_pack_bit_exact_at_exact_ties(vc, bits, step):
+    """Quotients that are exact half-integers (and their neighbours on the grid)
+    must round half to even exactly as the oracle's fp32 division does."""
+    B, H, T, d = 2, 2, 256, 128
+    rng = np.random.default_rng(bits * 100 + int(step * 64))
+    K = tie_grid(rng, (B, H, T, d), bits, step, group_axis=2)     # keys: groups along tokens
+    V = tie_grid(rng, (B, H, T, d), bits, step, group_axis=3)     # values: groups along channels
+    _, packed = gpu_pack(vc, K, V, bits)
+    got = to_np(packed, B, H, T, d, bits)
+    want = kivi.quant_pack(K, V, bits)
+    assert_packed_equal(got, want)
+
+
 def test_pack_hand_worked_groups(vc):
     """The golden groups, placed as key channels and as value channel groups."""
     cases = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "kivi_cases.json")))["cases"]

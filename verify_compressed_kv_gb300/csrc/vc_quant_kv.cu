@@ -40,11 +40,11 @@ __device__ __forceinline__ int field_pos(int bits, int u, int r, int e) {
 // (d/4) c + 4k + 2r + e, fragment i = j*(d/16) + k.  V: tokens 8c + 4e + 2s + r,
 // channels 8n + a, fragment i = s*(d/8) + n.  b = 2: word i/4, u = i%4;
 // b = 4, 8: i2 = 2i + r, SPW = 16/b slots per word, word i2/SPW, u = i2%SPW.
-template <int BITS, bool IS_V>
-__device__ uint32_t build_word(const uint8_t* codes, int ld, int d, int idx) {
+template <int BITS, bool IS_V, int D>
+__device__ __forceinline__ uint32_t build_word(const uint8_t* codes, int ld, int idx) {
   const int L = (idx % 128) / 4, w = (idx / 128) * 4 + idx % 4;
   const int a = L / 4, c = L % 4;
-  const int per = IS_V ? d / 8 : d / 16;          // fragments per j (K) or per s (V)
+  constexpr int per = IS_V ? D / 8 : D / 16;      // fragments per j (K) or per s (V)
   constexpr int SPW = BITS == 2 ? 4 : 16 / BITS;   // slots per word
   uint32_t word = 0;
 #pragma unroll
@@ -55,9 +55,8 @@ __device__ uint32_t build_word(const uint8_t* codes, int ld, int d, int idx) {
       if (BITS == 2) {
         i = 4 * w + u;
       } else {
-        const int i2 = SPW * w + u;
-        if ((i2 & 1) != r) continue;              // b = 4, 8: slot u carries one r
-        i = i2 >> 1;
+        if ((u & 1) != r) continue;               // b = 4, 8: slot u carries r = u % 2 (SPW even)
+        i = (SPW * w + u) >> 1;
       }
       const int hi = i / per, lo = i % per;         // (j, k) for K, (s, n) for V
 #pragma unroll
@@ -68,7 +67,7 @@ __device__ uint32_t build_word(const uint8_t* codes, int ld, int d, int idx) {
           ch = 8 * lo + a;
         } else {
           t = 4 * a + hi;
-          ch = (d / 4) * c + 4 * lo + 2 * r + e;
+          ch = (D / 4) * c + 4 * lo + 2 * r + e;
         }
         const uint32_t code = codes[t * ld + ch];
         word |= code << field_pos(BITS, u, r, e);
@@ -83,91 +82,213 @@ __device__ __forceinline__ int vmeta_entry(int t) {
   return (t & ~7) | (((t >> 1) & 1) << 2) | ((t & 1) << 1) | ((t >> 2) & 1);
 }
 
-// Quantise one 32-token tile held in shared memory.
-//   k_s, v_s : bf16 tiles [32][ld] (rows = tokens), ld >= d
-//   codes_s  : scratch uint8 2 x [32][d + 4] (K codes, then V codes)
-// Writes the tile's words and metadata into group `g` of (b, h)'s packed
-// arrays (already offset to the (b, h) slice).  All threads of the CTA call it.
-template <int BITS>
-__device__ void quantize_tile(const uint16_t* k_s, const uint16_t* v_s, int ld, int d,
-                              uint8_t* codes_s, int g, uint32_t* kc, uint16_t* ksz, uint32_t* vc,
-                              uint16_t* vsz) {
-  constexpr int QMAX = (1 << BITS) - 1;
-  const int cld = d + 4;
-  uint8_t* kcodes = codes_s;
-  uint8_t* vcodes = codes_s + kGroup * cld;
-  const float qmax = static_cast<float>(QMAX);
+// Quantisation parameters of one group (KIVI recipe): scale s = fp16((max - min) / qmax),
+// zero z = fp16(min), both applied in fp32.
+struct QParams {
+  float s, z;
+  float y;        // RN(1 / s) when `fast`
+  bool fast;      // s > 0 and finite, z finite
+  uint16_t s16, z16;
+};
 
-  // ---- keys: one thread per channel, group = 32 tokens of that channel
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    float mn = FLT_MAX, mx = -FLT_MAX;
-    for (int t = 0; t < kGroup; ++t) {
-      float x = vc_bf16_to_f32(k_s[t * ld + c]);
-      mn = fminf(mn, x);
-      mx = fmaxf(mx, x);
-    }
-    const uint16_t s16 = vc_f32_to_f16_rn(__fdiv_rn(__fsub_rn(mx, mn), qmax));
-    const uint16_t z16 = vc_f32_to_f16_rn(mn);
-    const float sf = vc_f16_to_f32(s16), zf = vc_f16_to_f32(z16);
-    for (int t = 0; t < kGroup; ++t) {
-      int code = 0;
-      if (sf != 0.0f) {
-        float r = rintf(__fdiv_rn(__fsub_rn(vc_bf16_to_f32(k_s[t * ld + c]), zf), sf));
-        r = fminf(fmaxf(r, 0.0f), qmax);
-        code = static_cast<int>(r);
-      }
-      kcodes[t * cld + c] = static_cast<uint8_t>(code);
-    }
-    ksz[static_cast<size_t>(g) * 2 * d + c] = s16;          // scales row, then zeros row
-    ksz[static_cast<size_t>(g) * 2 * d + d + c] = z16;
+template <int QMAX>
+__device__ __forceinline__ QParams qparams(float mn, float mx) {
+  QParams p;
+  p.s16 = vc_f32_to_f16_rn(__fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(QMAX)));
+  p.z16 = vc_f32_to_f16_rn(mn);
+  p.s = vc_f16_to_f32(p.s16);
+  p.z = vc_f16_to_f32(p.z16);
+  p.fast = p.s > 0.0f && isfinite(p.s) && isfinite(p.z);
+  p.y = p.fast ? __frcp_rn(p.s) : 0.0f;
+  return p;
+}
+
+// QParams travel between lanes as (s16 | z16 << 16, y); y = 0 marks a slow group.
+__device__ __forceinline__ uint32_t share_sz(const QParams& p) {
+  return p.s16 | (static_cast<uint32_t>(p.z16) << 16);
+}
+__device__ __forceinline__ QParams unshare(uint32_t sz, float y) {
+  QParams p;
+  p.s16 = static_cast<uint16_t>(sz & 0xFFFFu);
+  p.z16 = static_cast<uint16_t>(sz >> 16);
+  p.s = vc_f16_to_f32(p.s16);
+  p.z = vc_f16_to_f32(p.z16);
+  p.y = y;
+  p.fast = y > 0.0f;
+  return p;
+}
+
+// The recipe's code: clamp(rint((x - z) / s), 0, qmax), correctly rounded subtract
+// and divide; 0 when s = 0.
+template <int QMAX>
+__device__ __noinline__ uint32_t code_exact(float x, QParams p) {
+  if (p.s == 0.0f) return 0u;
+  float r = rintf(__fdiv_rn(__fsub_rn(x, p.z), p.s));
+  r = fminf(fmaxf(r, 0.0f), static_cast<float>(QMAX));
+  return static_cast<uint32_t>(r);
+}
+
+// The same code without a division per element (p.fast only).  With y = RN(1/s),
+// q = RN(a y) lies within |a/s| 2^-23 of a/s and RN(a/s) within |a/s| 2^-24, so for
+// |a/s| <= 512 they are less than 2^-13 apart: unless q is within 2^-12 of a
+// half-integer, both round to the same integer (beyond 512 both clamp to qmax, below
+// zero both clamp to 0).  Such near-ties take the exact division.  Rounding after
+// the clamp equals clamping after it (integer bounds, monotone rounding); adding
+// 2^23 rounds a value in [0, 2^22) to an integer, ties to even, in the low bits.
+template <int QMAX>
+__device__ __forceinline__ uint32_t code_fast(float x, const QParams& p) {
+  const float a = __fsub_rn(x, p.z);
+  const float q = __fmul_rn(a, p.y);
+  if (fabsf(__fsub_rn(q, floorf(q)) - 0.5f) <= 0x1p-12f) return code_exact<QMAX>(x, p);
+  const float c = fminf(fmaxf(q, 0.0f), static_cast<float>(QMAX));
+  return __float_as_uint(__fadd_rn(c, 0x1p23f)) & 0xFFu;
+}
+
+template <int QMAX>
+__device__ __forceinline__ uint32_t code_of(float x, const QParams& p, bool fast) {
+  return fast ? code_fast<QMAX>(x, p) : code_exact<QMAX>(x, p);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+constexpr int kPackThreads = 128;
+
+// Quantise one 32-token group: Kg, Vg point at its 32 rows of d bf16 (row stride
+// D) in global memory.  Writes the group's words and metadata into group `g` of the
+// (b, h) slice of the packed arrays.  All kPackThreads threads of the CTA call it;
+// codes_s is 2 x [32][D + 4] bytes of shared memory.
+//   keys:   thread = (channel pair, slice of 32/TQ tokens); the TQ slices of a pair
+//           sit in one warp and combine min/max by shuffles.
+//   values: a lane holds 4 channels of one token row; 8 lanes = one 32-channel group.
+// All loads of the group are issued before the first use.
+template <int BITS, int D>
+__device__ __forceinline__ void quantize_group(const uint16_t* Kg, const uint16_t* Vg, uint8_t* codes_s, int g,
+                                               uint32_t* kc, uint16_t* ksz, uint32_t* vc, uint16_t* vsz) {
+  static_assert(D == 64 || D == 128, "head dim");
+  constexpr int QMAX = (1 << BITS) - 1;
+  constexpr int CLD = D + 4;                         // code tile row stride (bytes)
+  constexpr int TQ = 2 * kPackThreads / D;           // token slices per channel pair
+  constexpr int TPT = kGroup / TQ;                   // tokens per slice
+  constexpr int PPW = 32 / TQ;                       // channel pairs per warp
+  constexpr int LPR = D / 4;                         // lanes per V row
+  constexpr int NPI = kGroup * LPR / kPackThreads;   // V row pieces per thread
+  constexpr int NC = D / kGroup;                     // V channel groups per token
+  uint8_t* kcodes = codes_s;
+  uint8_t* vcodes = codes_s + kGroup * CLD;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cp = warp * PPW + lane % PPW, sl = lane / PPW;
+
+  uint32_t kx[TPT];
+#pragma unroll
+  for (int j = 0; j < TPT; ++j) kx[j] = *reinterpret_cast<const uint32_t*>(Kg + (sl * TPT + j) * D + 2 * cp);
+  uint2 vx[NPI];
+#pragma unroll
+  for (int it = 0; it < NPI; ++it) {
+    const int pi = it * kPackThreads + tid;
+    vx[it] = *reinterpret_cast<const uint2*>(Vg + (pi / LPR) * D + 4 * (pi % LPR));
   }
-  // ---- values: one thread per (channel group, token), group = 32 channels
-  const int NC = d / kGroup;
-  for (int i = threadIdx.x; i < NC * kGroup; i += blockDim.x) {
-    const int cg = i / kGroup, t = i % kGroup;
-    const uint16_t* row = v_s + t * ld + cg * kGroup;
-    float mn = FLT_MAX, mx = -FLT_MAX;
-    for (int c = 0; c < kGroup; ++c) {
-      float x = vc_bf16_to_f32(row[c]);
-      mn = fminf(mn, x);
-      mx = fmaxf(mx, x);
+
+  // ---- keys: channels 2cp, 2cp + 1 over the group's 32 tokens
+  {
+    float mn0 = FLT_MAX, mx0 = -FLT_MAX, mn1 = FLT_MAX, mx1 = -FLT_MAX;
+#pragma unroll
+    for (int j = 0; j < TPT; ++j) {
+      mn0 = fminf(mn0, bf16_lo(kx[j]));
+      mx0 = fmaxf(mx0, bf16_lo(kx[j]));
+      mn1 = fminf(mn1, bf16_hi(kx[j]));
+      mx1 = fmaxf(mx1, bf16_hi(kx[j]));
     }
-    const uint16_t s16 = vc_f32_to_f16_rn(__fdiv_rn(__fsub_rn(mx, mn), qmax));
-    const uint16_t z16 = vc_f32_to_f16_rn(mn);
-    const float sf = vc_f16_to_f32(s16), zf = vc_f16_to_f32(z16);
-    for (int c = 0; c < kGroup; ++c) {
-      int code = 0;
-      if (sf != 0.0f) {
-        float r = rintf(__fdiv_rn(__fsub_rn(vc_bf16_to_f32(row[c]), zf), sf));
-        r = fminf(fmaxf(r, 0.0f), qmax);
-        code = static_cast<int>(r);
+#pragma unroll
+    for (int o = PPW; o < 32; o <<= 1) {
+      mn0 = fminf(mn0, __shfl_xor_sync(0xFFFFFFFFu, mn0, o));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));
+      mn1 = fminf(mn1, __shfl_xor_sync(0xFFFFFFFFu, mn1, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
+    }
+    // odd slices derive channel 2cp + 1's parameters, even ones 2cp's; swap across slices
+    const bool odd = sl & 1;
+    const QParams mine = qparams<QMAX>(odd ? mn1 : mn0, odd ? mx1 : mx0);
+    const QParams other = unshare(__shfl_xor_sync(0xFFFFFFFFu, share_sz(mine), PPW),
+                                  __shfl_xor_sync(0xFFFFFFFFu, mine.y, PPW));
+    const QParams p0 = odd ? other : mine, p1 = odd ? mine : other;
+    if (sl == 0) {                                   // scales row, then zeros row
+      uint32_t* m = reinterpret_cast<uint32_t*>(ksz + static_cast<size_t>(g) * 2 * D);
+      m[cp] = p0.s16 | (static_cast<uint32_t>(p1.s16) << 16);
+      m[D / 2 + cp] = p0.z16 | (static_cast<uint32_t>(p1.z16) << 16);
+    }
+    const bool fast = p0.fast && p1.fast;
+#pragma unroll
+    for (int j = 0; j < TPT; ++j) {
+      const uint32_t c0 = code_of<QMAX>(bf16_lo(kx[j]), p0, fast);
+      const uint32_t c1 = code_of<QMAX>(bf16_hi(kx[j]), p1, fast);
+      *reinterpret_cast<uint16_t*>(kcodes + (sl * TPT + j) * CLD + 2 * cp) = static_cast<uint16_t>(c0 | (c1 << 8));
+    }
+  }
+  // ---- values: 4 channels of token t per lane; the 8 lanes of a 32-channel group
+  // reduce-scatter their NPI partial min/max, so each lane derives the parameters of
+  // one (piece, group) and the group's lanes fetch them by shuffle.
+  {
+    constexpr int LOG_NPI = NPI == 8 ? 3 : 2;
+    float vmn[NPI], vmx[NPI];
+#pragma unroll
+    for (int it = 0; it < NPI; ++it) {
+      vmn[it] = fminf(fminf(bf16_lo(vx[it].x), bf16_hi(vx[it].x)), fminf(bf16_lo(vx[it].y), bf16_hi(vx[it].y)));
+      vmx[it] = fmaxf(fmaxf(bf16_lo(vx[it].x), bf16_hi(vx[it].x)), fmaxf(bf16_lo(vx[it].y), bf16_hi(vx[it].y)));
+    }
+    // halving exchanges at lane offsets 4, 2, 1: a lane with the offset bit set keeps
+    // the upper half; once one value is left, the remaining stages are all-reduces
+#pragma unroll
+    for (int st = 0, n = NPI; st < 3; ++st) {
+      const int o = 4 >> st;
+      const bool up = lane & o;
+      if (n > 1) {
+        const int half = n / 2;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+          const float smn = up ? vmn[i] : vmn[i + half], kmn = up ? vmn[i + half] : vmn[i];
+          const float smx = up ? vmx[i] : vmx[i + half], kmx = up ? vmx[i + half] : vmx[i];
+          vmn[i] = fminf(kmn, __shfl_xor_sync(0xFFFFFFFFu, smn, o));
+          vmx[i] = fmaxf(kmx, __shfl_xor_sync(0xFFFFFFFFu, smx, o));
+        }
+        n = half;
+      } else {
+        vmn[0] = fminf(vmn[0], __shfl_xor_sync(0xFFFFFFFFu, vmn[0], o));
+        vmx[0] = fmaxf(vmx[0], __shfl_xor_sync(0xFFFFFFFFu, vmx[0], o));
       }
-      vcodes[t * cld + cg * kGroup + c] = static_cast<uint8_t>(code);
     }
-    const size_t m = ((static_cast<size_t>(g) * NC + cg) * 2) * kGroup + vmeta_entry(t);
-    vsz[m] = s16;
-    vsz[m + kGroup] = z16;
+    const int own = (lane & 7) >> (3 - LOG_NPI);     // the piece this lane's parameters belong to
+    const QParams po = qparams<QMAX>(vmn[0], vmx[0]);
+    {
+      const int pi = own * kPackThreads + tid, t = pi / LPR, q4 = pi % LPR;
+      if (((lane & 7) & ((8 >> LOG_NPI) - 1)) == 0) {
+        const size_t m = ((static_cast<size_t>(g) * NC + q4 / 8) * 2) * kGroup + vmeta_entry(t);
+        vsz[m] = po.s16;
+        vsz[m + kGroup] = po.z16;
+      }
+    }
+    const uint32_t sz_own = share_sz(po);
+#pragma unroll
+    for (int it = 0; it < NPI; ++it) {
+      const int src = (lane & ~7) | (it << (3 - LOG_NPI));
+      const QParams p = unshare(__shfl_sync(0xFFFFFFFFu, sz_own, src), __shfl_sync(0xFFFFFFFFu, po.y, src));
+      const int pi = it * kPackThreads + tid, t = pi / LPR, q4 = pi % LPR;
+      const float x[4] = {bf16_lo(vx[it].x), bf16_hi(vx[it].x), bf16_lo(vx[it].y), bf16_hi(vx[it].y)};
+      uint32_t packed = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) packed |= code_of<QMAX>(x[e], p, p.fast) << (8 * e);
+      *reinterpret_cast<uint32_t*>(vcodes + t * CLD + 4 * q4) = packed;
+    }
   }
   __syncthreads();
   // ---- words: consecutive threads -> consecutive words
-  const int n_words = d * BITS;
-  for (int idx = threadIdx.x; idx < n_words; idx += blockDim.x) {
-    kc[static_cast<size_t>(g) * n_words + idx] = build_word<BITS, false>(kcodes, cld, d, idx);
-    vc[static_cast<size_t>(g) * n_words + idx] = build_word<BITS, true>(vcodes, cld, d, idx);
+  constexpr int n_words = D * BITS;
+#pragma unroll
+  for (int idx = tid; idx < n_words; idx += kPackThreads) {
+    kc[static_cast<size_t>(g) * n_words + idx] = build_word<BITS, false, D>(kcodes, CLD, idx);
+    vc[static_cast<size_t>(g) * n_words + idx] = build_word<BITS, true, D>(vcodes, CLD, idx);
   }
   __syncthreads();
-}
-
-// Load rows [0, 32) of a [*, d] bf16 matrix into a [32][ld] smem tile
-// (16-byte vectors; d multiple of 8).
-__device__ void load_tile(uint16_t* dst, int ld, const uint16_t* src, int d) {
-  const int vec = d / 8;
-  for (int i = threadIdx.x; i < kGroup * vec; i += blockDim.x) {
-    const int t = i / vec, v = i % vec;
-    const uint4 x = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(t) * d + v * 8);
-    uint32_t* o = reinterpret_cast<uint32_t*>(dst + t * ld + v * 8);
-    o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
-  }
 }
 
 struct Packed {
@@ -189,40 +310,34 @@ __host__ __device__ inline Packed slice(Packed p, int bh, int T_cap, int d, int 
   return r;
 }
 
-constexpr int kPackThreads = 128;
-
 // grid (T/32, B*Hkv): one 32-token group of one (b, h) per CTA.
-template <int BITS>
+template <int BITS, int D>
 __global__ void __launch_bounds__(kPackThreads) pack_kernel(const uint16_t* __restrict__ K,
                                                             const uint16_t* __restrict__ V, int T,
-                                                            int T_cap, int d, Packed p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int ld = d + 2;                      // odd word stride: conflict-free row reads
-  uint16_t* k_s = reinterpret_cast<uint16_t*>(smem);
-  uint16_t* v_s = k_s + kGroup * ld;
-  uint8_t* codes_s = reinterpret_cast<uint8_t*>(v_s + kGroup * ld);
+                                                            int T_cap, Packed p) {
+  __shared__ __align__(16) uint8_t codes_s[2 * kGroup * (D + 4)];
   const int g = blockIdx.x, bh = blockIdx.y;
-  const size_t base = (static_cast<size_t>(bh) * T + static_cast<size_t>(g) * kGroup) * d;
-  load_tile(k_s, ld, K + base, d);
-  load_tile(v_s, ld, V + base, d);
-  __syncthreads();
-  Packed s = slice(p, bh, T_cap, d, BITS);
-  quantize_tile<BITS>(k_s, v_s, ld, d, codes_s, g, s.kc, s.ksz, s.vc, s.vsz);
+  const size_t base = (static_cast<size_t>(bh) * T + static_cast<size_t>(g) * kGroup) * D;
+  Packed s = slice(p, bh, T_cap, D, BITS);
+  quantize_group<BITS, D>(K + base, V + base, codes_s, g, s.kc, s.ksz, s.vc, s.vsz);
 }
 
-size_t pack_smem(int d) { return 2 * kGroup * (d + 2) * sizeof(uint16_t) + 2 * kGroup * (d + 4); }
+// append_kernel's shared memory: two bf16 [32][d + 2] staging tiles for the tail
+// shift, then the code tiles.
+size_t append_smem(int d) { return 2 * kGroup * (d + 2) * sizeof(uint16_t) + 2 * kGroup * (d + 4); }
 
 // The commit of one request's accepted tokens for one KV head (grid (Hkv, B)):
 // append rows 0..n of k_new/v_new to the tail, pack whole groups from the
 // tail's front, shift the rest down.  Lengths are read here and written by
 // append_lengths_kernel afterwards, so no CTA sees another's update.
-template <int BITS>
+template <int BITS, int D>
 __global__ void __launch_bounds__(kPackThreads) append_kernel(
     const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
-    const int32_t* __restrict__ n_acc, int k, int Hkv, int d, uint16_t* tail_k, uint16_t* tail_v,
+    const int32_t* __restrict__ n_acc, int k, int Hkv, uint16_t* tail_k, uint16_t* tail_v,
     const int32_t* tail_len, int tail_cap, Packed p, const int32_t* packed_len, int T_cap) {
   extern __shared__ __align__(16) uint8_t smem[];
-  const int ld = d + 2;
+  constexpr int d = D;
+  constexpr int ld = d + 2;
   uint16_t* k_s = reinterpret_cast<uint16_t*>(smem);
   uint16_t* v_s = k_s + kGroup * ld;
   uint8_t* codes_s = reinterpret_cast<uint8_t*>(v_s + kGroup * ld);
@@ -254,12 +369,10 @@ __global__ void __launch_bounds__(kPackThreads) append_kernel(
   __syncthreads();
   // 2. pack whole groups from the front of the tail
   Packed s = slice(p, b * Hkv + h, T_cap, d, BITS);
-  for (int grp = 0; grp < n_pack; ++grp) {
-    load_tile(k_s, ld, tail_k + tb + static_cast<size_t>(grp) * kGroup * d, d);
-    load_tile(v_s, ld, tail_v + tb + static_cast<size_t>(grp) * kGroup * d, d);
-    __syncthreads();
-    quantize_tile<BITS>(k_s, v_s, ld, d, codes_s, plen / kGroup + grp, s.kc, s.ksz, s.vc, s.vsz);
-  }
+  for (int grp = 0; grp < n_pack; ++grp)
+    quantize_group<BITS, D>(tail_k + tb + static_cast<size_t>(grp) * kGroup * d,
+                            tail_v + tb + static_cast<size_t>(grp) * kGroup * d, codes_s, plen / kGroup + grp, s.kc,
+                            s.ksz, s.vc, s.vsz);
   // 3. shift the remaining (total - 32*n_pack < 32) tail tokens to the front
   const int shift = n_pack * kGroup;
   const int rest = total - shift;
@@ -724,14 +837,18 @@ extern "C" vc_status_t vc_quant_kv_pack(const vc_shape_t* s, int32_t T, int32_t 
   VC_REQUIRE(static_cast<int64_t>(s->B) * s->Hkv <= 65535, "B*Hkv <= 65535");
   dim3 grid(T / kGroup, s->B * s->Hkv);
   Packed p{kc, ksz, vc, vsz};
-  const size_t sm = pack_smem(s->d);
   auto cs = reinterpret_cast<cudaStream_t>(stream);
-  if (s->bits == 2)
-    pack_kernel<2><<<grid, kPackThreads, sm, cs>>>(K, V, T, T_cap, s->d, p);
-  else if (s->bits == 4)
-    pack_kernel<4><<<grid, kPackThreads, sm, cs>>>(K, V, T, T_cap, s->d, p);
-  else
-    pack_kernel<8><<<grid, kPackThreads, sm, cs>>>(K, V, T, T_cap, s->d, p);
+#define VC_PACK(BITS, D) pack_kernel<BITS, D><<<grid, kPackThreads, 0, cs>>>(K, V, T, T_cap, p)
+  if (s->d == 128) {
+    if (s->bits == 2) VC_PACK(2, 128);
+    else if (s->bits == 4) VC_PACK(4, 128);
+    else VC_PACK(8, 128);
+  } else {
+    if (s->bits == 2) VC_PACK(2, 64);
+    else if (s->bits == 4) VC_PACK(4, 64);
+    else VC_PACK(8, 64);
+  }
+#undef VC_PACK
   VC_LAUNCH_CHECK("pack_kernel");
   return VC_OK;
 }
@@ -771,17 +888,21 @@ extern "C" vc_status_t vc_quant_kv_append(const vc_shape_t* s, const uint16_t* k
   VC_REQUIRE(vc_aligned16(k_new) && vc_aligned16(v_new) && vc_aligned16(tail_k) && vc_aligned16(tail_v),
              "bf16 pointers must be 16-byte aligned");
   Packed p{kc, ksz, vc, vsz};
-  const size_t sm = pack_smem(s->d);
+  const size_t sm = append_smem(s->d);
   auto cs = reinterpret_cast<cudaStream_t>(stream);
-  if (s->bits == 2)
-    append_kernel<2><<<dim3(s->Hkv, s->B), kPackThreads, sm, cs>>>(k_new, v_new, n_acc, s->k, s->Hkv, s->d, tail_k,
-                                                                     tail_v, tail_len, tail_cap, p, packed_len, T_cap);
-  else if (s->bits == 4)
-    append_kernel<4><<<dim3(s->Hkv, s->B), kPackThreads, sm, cs>>>(k_new, v_new, n_acc, s->k, s->Hkv, s->d, tail_k,
-                                                                     tail_v, tail_len, tail_cap, p, packed_len, T_cap);
-  else
-    append_kernel<8><<<dim3(s->Hkv, s->B), kPackThreads, sm, cs>>>(k_new, v_new, n_acc, s->k, s->Hkv, s->d, tail_k,
-                                                                     tail_v, tail_len, tail_cap, p, packed_len, T_cap);
+#define VC_APPEND(BITS, D)                                                                                    \
+  append_kernel<BITS, D><<<dim3(s->Hkv, s->B), kPackThreads, sm, cs>>>(k_new, v_new, n_acc, s->k, s->Hkv, tail_k, \
+                                                                       tail_v, tail_len, tail_cap, p, packed_len, T_cap)
+  if (s->d == 128) {
+    if (s->bits == 2) VC_APPEND(2, 128);
+    else if (s->bits == 4) VC_APPEND(4, 128);
+    else VC_APPEND(8, 128);
+  } else {
+    if (s->bits == 2) VC_APPEND(2, 64);
+    else if (s->bits == 4) VC_APPEND(4, 64);
+    else VC_APPEND(8, 64);
+  }
+#undef VC_APPEND
   VC_LAUNCH_CHECK("append_kernel");
   append_lengths_kernel<<<1, 256, 0, cs>>>(n_acc, s->B, s->k, tail_len, tail_cap, packed_len, T_cap);
   VC_LAUNCH_CHECK("append_lengths_kernel");
