@@ -104,6 +104,30 @@ def test_pack_bit_exact_at_exact_ties(vc, bits, step):
     assert_packed_equal(got, want)
 
 
+def wide_range(rng, shape, group_axis):
+    """bf16 bits of groups with magnitudes 2^-24 .. 2^10 and offsets of a few
+    magnitudes: scales from fp16 subnormals (and zero) to large, every exponent of
+    the quotient path."""
+    x = rng.standard_normal(shape).astype(np.float32)
+    x = np.moveaxis(x, group_axis, -1)
+    g = x.reshape(*x.shape[:-1], -1, 32)
+    mag = np.exp2(rng.uniform(-24, 10, size=g.shape[:-1] + (1,))).astype(np.float32)
+    off = (rng.standard_normal(g.shape[:-1] + (1,)) * 4).astype(np.float32) * mag
+    x = np.moveaxis((g * mag + off).reshape(x.shape), -1, group_axis)
+    b = np.ascontiguousarray(x).view(np.uint32)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)        # RNE to bf16
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_pack_bit_exact_wide_value_range(vc, bits):
+    B, H, T, d = 1, 4, 2048, 128
+    rng = np.random.default_rng(40 + bits)
+    K = wide_range(rng, (B, H, T, d), 2)
+    V = wide_range(rng, (B, H, T, d), 3)
+    _, packed = gpu_pack(vc, K, V, bits)
+    assert_packed_equal(to_np(packed, B, H, T, d, bits), kivi.quant_pack(K, V, bits))
+
+
 def test_pack_hand_worked_groups(vc):
     """The golden groups, placed as key channels and as value channel groups."""
     cases = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "kivi_cases.json")))["cases"]

@@ -86,8 +86,7 @@ __device__ __forceinline__ int vmeta_entry(int t) {
 // zero z = fp16(min), both applied in fp32.
 struct QParams {
   float s, z;
-  float y;        // RN(1 / s) when `fast`
-  bool fast;      // s > 0 and finite, z finite
+  float y;        // RN(1 / s) when s > 0 and finite and z finite; else 0 (exact path)
   uint16_t s16, z16;
 };
 
@@ -98,8 +97,7 @@ __device__ __forceinline__ QParams qparams(float mn, float mx) {
   p.z16 = vc_f32_to_f16_rn(mn);
   p.s = vc_f16_to_f32(p.s16);
   p.z = vc_f16_to_f32(p.z16);
-  p.fast = p.s > 0.0f && isfinite(p.s) && isfinite(p.z);
-  p.y = p.fast ? __frcp_rn(p.s) : 0.0f;
+  p.y = (p.s > 0.0f && isfinite(p.s) && isfinite(p.z)) ? __frcp_rn(p.s) : 0.0f;
   return p;
 }
 
@@ -114,43 +112,99 @@ __device__ __forceinline__ QParams unshare(uint32_t sz, float y) {
   p.s = vc_f16_to_f32(p.s16);
   p.z = vc_f16_to_f32(p.z16);
   p.y = y;
-  p.fast = y > 0.0f;
   return p;
 }
 
 // The recipe's code: clamp(rint((x - z) / s), 0, qmax), correctly rounded subtract
 // and divide; 0 when s = 0.
 template <int QMAX>
-__device__ __noinline__ uint32_t code_exact(float x, QParams p) {
-  if (p.s == 0.0f) return 0u;
-  float r = rintf(__fdiv_rn(__fsub_rn(x, p.z), p.s));
+__device__ __forceinline__ uint32_t code_exact(float x, float s, float z) {
+  if (s == 0.0f) return 0u;
+  float r = rintf(__fdiv_rn(__fsub_rn(x, z), s));
   r = fminf(fmaxf(r, 0.0f), static_cast<float>(QMAX));
   return static_cast<uint32_t>(r);
 }
 
-// The same code without a division per element (p.fast only).  With y = RN(1/s),
-// q = RN(a y) lies within |a/s| 2^-23 of a/s and RN(a/s) within |a/s| 2^-24, so for
-// |a/s| <= 512 they are less than 2^-13 apart: unless q is within 2^-12 of a
-// half-integer, both round to the same integer (beyond 512 both clamp to qmax, below
-// zero both clamp to 0).  Such near-ties take the exact division.  Rounding after
-// the clamp equals clamping after it (integer bounds, monotone rounding); adding
-// 2^23 rounds a value in [0, 2^22) to an integer, ties to even, in the low bits.
-template <int QMAX>
-__device__ __forceinline__ uint32_t code_fast(float x, const QParams& p) {
-  const float a = __fsub_rn(x, p.z);
-  const float q = __fmul_rn(a, p.y);
-  if (fabsf(__fsub_rn(q, floorf(q)) - 0.5f) <= 0x1p-12f) return code_exact<QMAX>(x, p);
-  const float c = fminf(fmaxf(q, 0.0f), static_cast<float>(QMAX));
-  return __float_as_uint(__fadd_rn(c, 0x1p23f)) & 0xFFu;
+// Two fp32 values in one 64-bit register; add / sub / mul act on both lanes with
+// IEEE round-to-nearest (sm_100 family f32x2 instructions).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float f2lo(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float f2hi(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
 }
 
+// The codes of two elements without a division, for groups with y = RN(1/s) > 0.
+// A code can only depend on where c = clamp(q, 0, qmax) lies against the
+// half-integers 1/2 .. qmax - 1/2, so only |q| < qmax + 1 <= 2^b matters.  There
+// q = RN((x - z) y) lies within |a/s| (2^-23 + 2^-47) of a/s (a = x - z), and
+// RN(a/s) within |a/s| 2^-24, so the two are less than 2^(b-22) apart: unless c is
+// within kTieWindow = 2^(b-21) of a half-integer, both give the same code.  Such
+// near-ties set `tie` and the caller redoes them with the exact division.  Rounding
+// after the clamp equals clamping after it (integer bounds, monotone rounding);
+// 2^23 + c rounds c in [0, 2^22) to an integer, ties to even, in the low bits, and
+// c - rint(c) is exact.  Returns code(x.lo) | code(x.hi) << 8.
 template <int QMAX>
-__device__ __forceinline__ uint32_t code_of(float x, const QParams& p, bool fast) {
-  return fast ? code_fast<QMAX>(x, p) : code_exact<QMAX>(x, p);
+__device__ __forceinline__ uint32_t code_pair(uint64_t x, uint64_t z, uint64_t y, bool& tie) {
+  const float qmax = static_cast<float>(QMAX);
+  const uint64_t q = f2_mul(f2_sub(x, z), y);
+  const uint64_t c = f2(fminf(fmaxf(f2lo(q), 0.0f), qmax), fminf(fmaxf(f2hi(q), 0.0f), qmax));
+  const uint64_t big = f2(0x1p23f, 0x1p23f);
+  const uint64_t m = f2_add(c, big);
+  const uint64_t frac = f2_sub(c, f2_sub(m, big));
+  constexpr float kTieWindow = static_cast<float>(QMAX + 1) * 0x1p-21f;
+  tie |= (fabsf(f2lo(frac)) >= 0.5f - kTieWindow) | (fabsf(f2hi(frac)) >= 0.5f - kTieWindow);
+  return (__float_as_uint(f2lo(m)) & 0xFFu) | ((__float_as_uint(f2hi(m)) & 0xFFu) << 8);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// One element's code where its pair flagged a near-tie: the fast code unless this
+// element is itself near a tie (or its group has no reciprocal), else the exact one.
+template <int QMAX>
+__device__ __forceinline__ uint32_t code_recheck(float x, float s, float z, float y) {
+  bool tie = !(y > 0.0f);
+  const uint32_t c = code_pair<QMAX>(f2(x, x), f2(z, z), f2(y, y), tie) & 0xFFu;
+  return tie ? code_exact<QMAX>(x, s, z) : c;
+}
+
+// Codes of one thread's key elements (channels 2cp, 2cp + 1, tokens t0 .. t0 + TPT
+// - 1) re-read from global memory, each near-tie by the exact division: the rare
+// path after code_pair flagged one.
+template <int QMAX, int D, int TPT>
+__device__ __noinline__ void k_codes_exact(const uint16_t* Kg, int t0, int cp, QParams p0, QParams p1,
+                                           uint8_t* kcodes) {
+  for (int j = 0; j < TPT; ++j) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(Kg + (t0 + j) * D + 2 * cp);
+    const uint32_t c = code_recheck<QMAX>(bf16_lo(w), p0.s, p0.z, p0.y) |
+                       (code_recheck<QMAX>(bf16_hi(w), p1.s, p1.z, p1.y) << 8);
+    *reinterpret_cast<uint16_t*>(kcodes + (t0 + j) * (D + 4) + 2 * cp) = static_cast<uint16_t>(c);
+  }
+}
+
+// Codes of 4 value elements (one lane's piece of a token row), each near-tie by
+// the exact division.
+template <int QMAX>
+__device__ __noinline__ uint32_t v_codes_exact(uint2 w, QParams p) {
+  return code_recheck<QMAX>(bf16_lo(w.x), p.s, p.z, p.y) | (code_recheck<QMAX>(bf16_hi(w.x), p.s, p.z, p.y) << 8) |
+         (code_recheck<QMAX>(bf16_lo(w.y), p.s, p.z, p.y) << 16) |
+         (code_recheck<QMAX>(bf16_hi(w.y), p.s, p.z, p.y) << 24);
+}
 
 constexpr int kPackThreads = 128;
 
@@ -217,13 +271,14 @@ __device__ __forceinline__ void quantize_group(const uint16_t* Kg, const uint16_
       m[cp] = p0.s16 | (static_cast<uint32_t>(p1.s16) << 16);
       m[D / 2 + cp] = p0.z16 | (static_cast<uint32_t>(p1.z16) << 16);
     }
-    const bool fast = p0.fast && p1.fast;
+    bool tie = !(p0.y > 0.0f) | !(p1.y > 0.0f);
+    const uint64_t z2 = f2(p0.z, p1.z), y2 = f2(p0.y, p1.y);
 #pragma unroll
     for (int j = 0; j < TPT; ++j) {
-      const uint32_t c0 = code_of<QMAX>(bf16_lo(kx[j]), p0, fast);
-      const uint32_t c1 = code_of<QMAX>(bf16_hi(kx[j]), p1, fast);
-      *reinterpret_cast<uint16_t*>(kcodes + (sl * TPT + j) * CLD + 2 * cp) = static_cast<uint16_t>(c0 | (c1 << 8));
+      const uint32_t c = code_pair<QMAX>(f2(bf16_lo(kx[j]), bf16_hi(kx[j])), z2, y2, tie);
+      *reinterpret_cast<uint16_t*>(kcodes + (sl * TPT + j) * CLD + 2 * cp) = static_cast<uint16_t>(c);
     }
+    if (tie) k_codes_exact<QMAX, D, TPT>(Kg, sl * TPT, cp, p0, p1, kcodes);
   }
   // ---- values: 4 channels of token t per lane; the 8 lanes of a 32-channel group
   // reduce-scatter their NPI partial min/max, so each lane derives the parameters of
@@ -273,10 +328,11 @@ __device__ __forceinline__ void quantize_group(const uint16_t* Kg, const uint16_
       const int src = (lane & ~7) | (it << (3 - LOG_NPI));
       const QParams p = unshare(__shfl_sync(0xFFFFFFFFu, sz_own, src), __shfl_sync(0xFFFFFFFFu, po.y, src));
       const int pi = it * kPackThreads + tid, t = pi / LPR, q4 = pi % LPR;
-      const float x[4] = {bf16_lo(vx[it].x), bf16_hi(vx[it].x), bf16_lo(vx[it].y), bf16_hi(vx[it].y)};
-      uint32_t packed = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) packed |= code_of<QMAX>(x[e], p, p.fast) << (8 * e);
+      bool tie = !(p.y > 0.0f);
+      const uint64_t z2 = f2(p.z, p.z), y2 = f2(p.y, p.y);
+      uint32_t packed = code_pair<QMAX>(f2(bf16_lo(vx[it].x), bf16_hi(vx[it].x)), z2, y2, tie) |
+                        (code_pair<QMAX>(f2(bf16_lo(vx[it].y), bf16_hi(vx[it].y)), z2, y2, tie) << 16);
+      if (tie) packed = v_codes_exact<QMAX>(vx[it], p);
       *reinterpret_cast<uint32_t*>(vcodes + t * CLD + 4 * q4) = packed;
     }
   }
@@ -312,7 +368,7 @@ __host__ __device__ inline Packed slice(Packed p, int bh, int T_cap, int d, int 
 
 // grid (T/32, B*Hkv): one 32-token group of one (b, h) per CTA.
 template <int BITS, int D>
-__global__ void __launch_bounds__(kPackThreads) pack_kernel(const uint16_t* __restrict__ K,
+__global__ void __launch_bounds__(kPackThreads, 8) pack_kernel(const uint16_t* __restrict__ K,
                                                             const uint16_t* __restrict__ V, int T,
                                                             int T_cap, Packed p) {
   __shared__ __align__(16) uint8_t codes_s[2 * kGroup * (D + 4)];
