@@ -70,7 +70,7 @@ __device__ __forceinline__ uint32_t build_word(const uint8_t* codes, int ld, int
           ch = (D / 4) * c + 4 * lo + 2 * r + e;
         }
         const uint32_t code = codes[t * ld + ch];
-        word |= code << field_pos(BITS, u, r, e);
+        word += code << field_pos(BITS, u, r, e);      // disjoint fields: + == |
       }
     }
   return word;
@@ -86,10 +86,14 @@ __device__ __forceinline__ int vmeta_entry(int t) {
 // zero z = fp16(min), both applied in fp32.
 struct QParams {
   float s, z;
-  float y;        // RN(1 / s) when s > 0 and finite and z finite; else 0 (exact path)
+  float y;        // RN(1/s) for a fast group (see qparams), else 0: every code exact
   uint16_t s16, z16;
 };
 
+// A group is fast when s > 0 and finite, z finite, and every q = RN(RN(x - z) y)
+// of its elements lies in (-1/4, qmax + 1/4): q is monotone in x (each step rounds
+// monotonically and y > 0), so the group's min and max bound it.  Then
+// rint(q) is already in [0, qmax] and no element needs the clamp.
 template <int QMAX>
 __device__ __forceinline__ QParams qparams(float mn, float mx) {
   QParams p;
@@ -97,11 +101,16 @@ __device__ __forceinline__ QParams qparams(float mn, float mx) {
   p.z16 = vc_f32_to_f16_rn(mn);
   p.s = vc_f16_to_f32(p.s16);
   p.z = vc_f16_to_f32(p.z16);
-  p.y = (p.s > 0.0f && isfinite(p.s) && isfinite(p.z)) ? __frcp_rn(p.s) : 0.0f;
+  p.y = 0.0f;
+  if (p.s > 0.0f && isfinite(p.s) && isfinite(p.z)) {
+    const float y = __frcp_rn(p.s);
+    const float qlo = __fmul_rn(__fsub_rn(mn, p.z), y), qhi = __fmul_rn(__fsub_rn(mx, p.z), y);
+    if (qlo > -0.25f && qhi < static_cast<float>(QMAX) + 0.25f) p.y = y;
+  }
   return p;
 }
 
-// QParams travel between lanes as (s16 | z16 << 16, y); y = 0 marks a slow group.
+// QParams travel between lanes as (s16 | z16 << 16, y).
 __device__ __forceinline__ uint32_t share_sz(const QParams& p) {
   return p.s16 | (static_cast<uint32_t>(p.z16) << 16);
 }
@@ -148,44 +157,66 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   return r;
 }
 
-// The codes of two elements without a division, for groups with y = RN(1/s) > 0.
-// A code can only depend on where c = clamp(q, 0, qmax) lies against the
-// half-integers 1/2 .. qmax - 1/2, so only |q| < qmax + 1 <= 2^b matters.  There
-// q = RN((x - z) y) lies within |a/s| (2^-23 + 2^-47) of a/s (a = x - z), and
-// RN(a/s) within |a/s| 2^-24, so the two are less than 2^(b-22) apart: unless c is
-// within kTieWindow = 2^(b-21) of a half-integer, both give the same code.  Such
-// near-ties set `tie` and the caller redoes them with the exact division.  Rounding
-// after the clamp equals clamping after it (integer bounds, monotone rounding);
-// 2^23 + c rounds c in [0, 2^22) to an integer, ties to even, in the low bits, and
-// c - rint(c) is exact.  Returns code(x.lo) | code(x.hi) << 8.
-template <int QMAX>
-__device__ __forceinline__ uint32_t code_pair(uint64_t x, uint64_t z, uint64_t y, bool& tie) {
-  const float qmax = static_cast<float>(QMAX);
-  const uint64_t q = f2_mul(f2_sub(x, z), y);
-  const uint64_t c = f2(fminf(fmaxf(f2lo(q), 0.0f), qmax), fminf(fmaxf(f2hi(q), 0.0f), qmax));
-  const uint64_t big = f2(0x1p23f, 0x1p23f);
-  const uint64_t m = f2_add(c, big);
-  const uint64_t frac = f2_sub(c, f2_sub(m, big));
-  constexpr float kTieWindow = static_cast<float>(QMAX + 1) * 0x1p-21f;
-  tie |= (fabsf(f2lo(frac)) >= 0.5f - kTieWindow) | (fabsf(f2hi(frac)) >= 0.5f - kTieWindow);
-  return (__float_as_uint(f2lo(m)) & 0xFFu) | ((__float_as_uint(f2hi(m)) & 0xFFu) << 8);
+// Paired bf16 min / max (a NaN operand yields the other) and byte permute.
+__device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// One element's code where its pair flagged a near-tie: the fast code unless this
-// element is itself near a tie (or its group has no reciprocal), else the exact one.
+// Codes are decided exactly unless c = rint-candidate lies within this distance of
+// a half-integer.  A code depends only on where q sits against 1/2 .. qmax - 1/2,
+// so only |q| < 2^b matters; there q = RN((x - z) y) is within |a/s| (2^-23 + 2^-47)
+// of a/s (a = x - z, y = RN(1/s)) and RN(a/s) within |a/s| 2^-24, so the two are
+// less than 2^(b-22) apart and round to the same integer outside the window.
+template <int QMAX>
+__device__ __forceinline__ constexpr float tie_window() { return static_cast<float>(QMAX + 1) * 0x1p-21f; }
+
+// The codes of two elements of fast groups (y > 0) without a division.  2^23 + q
+// rounds q in (-1/4, 2^22) to an integer, ties to even, in the low bits, and
+// q - rint(q) is exact.  A near-tie (or a NaN) sets `tie`; the caller redoes the
+// pair's elements with code_recheck.  Returns code(x.lo) | code(x.hi) << 8 in the
+// low half (the high half is unspecified).
+template <int QMAX>
+__device__ __forceinline__ uint32_t code_pair(uint64_t x, uint64_t z, uint64_t y, bool& tie) {
+  const uint64_t big = f2(0x1p23f, 0x1p23f);
+  const uint64_t q = f2_mul(f2_sub(x, z), y);
+  const uint64_t m = f2_add(q, big);
+  const uint64_t frac = f2_sub(q, f2_sub(m, big));
+  tie |= !(fabsf(f2lo(frac)) < 0.5f - tie_window<QMAX>()) | !(fabsf(f2hi(frac)) < 0.5f - tie_window<QMAX>());
+  return prmt(static_cast<uint32_t>(m), static_cast<uint32_t>(m >> 32), 0x0040u);
+}
+
+// One element's exact code by the cheapest sure route: the reciprocal product when
+// its group is fast and it is not near a tie (clamped, so it also serves groups
+// whose range test failed), else the division.
 template <int QMAX>
 __device__ __forceinline__ uint32_t code_recheck(float x, float s, float z, float y) {
-  bool tie = !(y > 0.0f);
-  const uint32_t c = code_pair<QMAX>(f2(x, x), f2(z, z), f2(y, y), tie) & 0xFFu;
-  return tie ? code_exact<QMAX>(x, s, z) : c;
+  if (y > 0.0f) {
+    const float q = __fmul_rn(__fsub_rn(x, z), y);
+    const float c = fminf(fmaxf(q, 0.0f), static_cast<float>(QMAX));
+    const float r = __fsub_rn(__fadd_rn(c, 0x1p23f), 0x1p23f);
+    if (fabsf(__fsub_rn(c, r)) < 0.5f - tie_window<QMAX>()) return static_cast<uint32_t>(r);
+  }
+  return code_exact<QMAX>(x, s, z);
 }
 
 // Codes of one thread's key elements (channels 2cp, 2cp + 1, tokens t0 .. t0 + TPT
-// - 1) re-read from global memory, each near-tie by the exact division: the rare
-// path after code_pair flagged one.
+// - 1) re-read from global memory: the rare path after code_pair flagged one, or
+// for a group that is not fast.
 template <int QMAX, int D, int TPT>
 __device__ __noinline__ void k_codes_exact(const uint16_t* Kg, int t0, int cp, QParams p0, QParams p1,
                                            uint8_t* kcodes) {
@@ -197,8 +228,7 @@ __device__ __noinline__ void k_codes_exact(const uint16_t* Kg, int t0, int cp, Q
   }
 }
 
-// Codes of 4 value elements (one lane's piece of a token row), each near-tie by
-// the exact division.
+// Codes of 4 value elements (one lane's piece of a token row), the same way.
 template <int QMAX>
 __device__ __noinline__ uint32_t v_codes_exact(uint2 w, QParams p) {
   return code_recheck<QMAX>(bf16_lo(w.x), p.s, p.z, p.y) | (code_recheck<QMAX>(bf16_hi(w.x), p.s, p.z, p.y) << 8) |
@@ -215,7 +245,8 @@ constexpr int kPackThreads = 128;
 //   keys:   thread = (channel pair, slice of 32/TQ tokens); the TQ slices of a pair
 //           sit in one warp and combine min/max by shuffles.
 //   values: a lane holds 4 channels of one token row; 8 lanes = one 32-channel group.
-// All loads of the group are issued before the first use.
+// All loads of the group are issued before the first use.  Min and max are taken
+// on the bf16 inputs themselves (exact).
 template <int BITS, int D>
 __device__ __forceinline__ void quantize_group(const uint16_t* Kg, const uint16_t* Vg, uint8_t* codes_s, int g,
                                                uint32_t* kc, uint16_t* ksz, uint32_t* vc, uint16_t* vsz) {
@@ -245,24 +276,20 @@ __device__ __forceinline__ void quantize_group(const uint16_t* Kg, const uint16_
 
   // ---- keys: channels 2cp, 2cp + 1 over the group's 32 tokens
   {
-    float mn0 = FLT_MAX, mx0 = -FLT_MAX, mn1 = FLT_MAX, mx1 = -FLT_MAX;
+    uint32_t kmn = kx[0], kmx = kx[0];
 #pragma unroll
-    for (int j = 0; j < TPT; ++j) {
-      mn0 = fminf(mn0, bf16_lo(kx[j]));
-      mx0 = fmaxf(mx0, bf16_lo(kx[j]));
-      mn1 = fminf(mn1, bf16_hi(kx[j]));
-      mx1 = fmaxf(mx1, bf16_hi(kx[j]));
+    for (int j = 1; j < TPT; ++j) {
+      kmn = bmin2(kmn, kx[j]);
+      kmx = bmax2(kmx, kx[j]);
     }
 #pragma unroll
     for (int o = PPW; o < 32; o <<= 1) {
-      mn0 = fminf(mn0, __shfl_xor_sync(0xFFFFFFFFu, mn0, o));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));
-      mn1 = fminf(mn1, __shfl_xor_sync(0xFFFFFFFFu, mn1, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
+      kmn = bmin2(kmn, __shfl_xor_sync(0xFFFFFFFFu, kmn, o));
+      kmx = bmax2(kmx, __shfl_xor_sync(0xFFFFFFFFu, kmx, o));
     }
     // odd slices derive channel 2cp + 1's parameters, even ones 2cp's; swap across slices
     const bool odd = sl & 1;
-    const QParams mine = qparams<QMAX>(odd ? mn1 : mn0, odd ? mx1 : mx0);
+    const QParams mine = odd ? qparams<QMAX>(bf16_hi(kmn), bf16_hi(kmx)) : qparams<QMAX>(bf16_lo(kmn), bf16_lo(kmx));
     const QParams other = unshare(__shfl_xor_sync(0xFFFFFFFFu, share_sz(mine), PPW),
                                   __shfl_xor_sync(0xFFFFFFFFu, mine.y, PPW));
     const QParams p0 = odd ? other : mine, p1 = odd ? mine : other;
@@ -280,16 +307,17 @@ __device__ __forceinline__ void quantize_group(const uint16_t* Kg, const uint16_
     }
     if (tie) k_codes_exact<QMAX, D, TPT>(Kg, sl * TPT, cp, p0, p1, kcodes);
   }
-  // ---- values: 4 channels of token t per lane; the 8 lanes of a 32-channel group
-  // reduce-scatter their NPI partial min/max, so each lane derives the parameters of
-  // one (piece, group) and the group's lanes fetch them by shuffle.
+  // ---- values: 4 channels of token t per lane.  Each piece's partial (min, -max)
+  // travels as one bf16 pair; the 8 lanes of a 32-channel group reduce-scatter
+  // their NPI pairs, so each lane derives the parameters of one (piece, group) and
+  // the group's lanes fetch them by shuffle.
   {
     constexpr int LOG_NPI = NPI == 8 ? 3 : 2;
-    float vmn[NPI], vmx[NPI];
+    uint32_t pr[NPI];
 #pragma unroll
     for (int it = 0; it < NPI; ++it) {
-      vmn[it] = fminf(fminf(bf16_lo(vx[it].x), bf16_hi(vx[it].x)), fminf(bf16_lo(vx[it].y), bf16_hi(vx[it].y)));
-      vmx[it] = fmaxf(fmaxf(bf16_lo(vx[it].x), bf16_hi(vx[it].x)), fmaxf(bf16_lo(vx[it].y), bf16_hi(vx[it].y)));
+      const uint32_t a = bmin2(vx[it].x, vx[it].y), b = bmax2(vx[it].x, vx[it].y) ^ 0x80008000u;
+      pr[it] = bmin2(prmt(a, b, 0x5410u), prmt(a, b, 0x7632u));     // (min, -max)
     }
     // halving exchanges at lane offsets 4, 2, 1: a lane with the offset bit set keeps
     // the upper half; once one value is left, the remaining stages are all-reduces
@@ -301,19 +329,16 @@ __device__ __forceinline__ void quantize_group(const uint16_t* Kg, const uint16_
         const int half = n / 2;
 #pragma unroll
         for (int i = 0; i < half; ++i) {
-          const float smn = up ? vmn[i] : vmn[i + half], kmn = up ? vmn[i + half] : vmn[i];
-          const float smx = up ? vmx[i] : vmx[i + half], kmx = up ? vmx[i + half] : vmx[i];
-          vmn[i] = fminf(kmn, __shfl_xor_sync(0xFFFFFFFFu, smn, o));
-          vmx[i] = fmaxf(kmx, __shfl_xor_sync(0xFFFFFFFFu, smx, o));
+          const uint32_t send = up ? pr[i] : pr[i + half], keep = up ? pr[i + half] : pr[i];
+          pr[i] = bmin2(keep, __shfl_xor_sync(0xFFFFFFFFu, send, o));
         }
         n = half;
       } else {
-        vmn[0] = fminf(vmn[0], __shfl_xor_sync(0xFFFFFFFFu, vmn[0], o));
-        vmx[0] = fmaxf(vmx[0], __shfl_xor_sync(0xFFFFFFFFu, vmx[0], o));
+        pr[0] = bmin2(pr[0], __shfl_xor_sync(0xFFFFFFFFu, pr[0], o));
       }
     }
     const int own = (lane & 7) >> (3 - LOG_NPI);     // the piece this lane's parameters belong to
-    const QParams po = qparams<QMAX>(vmn[0], vmx[0]);
+    const QParams po = qparams<QMAX>(bf16_lo(pr[0]), -bf16_hi(pr[0]));
     {
       const int pi = own * kPackThreads + tid, t = pi / LPR, q4 = pi % LPR;
       if (((lane & 7) & ((8 >> LOG_NPI) - 1)) == 0) {
@@ -330,8 +355,8 @@ __device__ __forceinline__ void quantize_group(const uint16_t* Kg, const uint16_
       const int pi = it * kPackThreads + tid, t = pi / LPR, q4 = pi % LPR;
       bool tie = !(p.y > 0.0f);
       const uint64_t z2 = f2(p.z, p.z), y2 = f2(p.y, p.y);
-      uint32_t packed = code_pair<QMAX>(f2(bf16_lo(vx[it].x), bf16_hi(vx[it].x)), z2, y2, tie) |
-                        (code_pair<QMAX>(f2(bf16_lo(vx[it].y), bf16_hi(vx[it].y)), z2, y2, tie) << 16);
+      uint32_t packed = prmt(code_pair<QMAX>(f2(bf16_lo(vx[it].x), bf16_hi(vx[it].x)), z2, y2, tie),
+                             code_pair<QMAX>(f2(bf16_lo(vx[it].y), bf16_hi(vx[it].y)), z2, y2, tie), 0x5410u);
       if (tie) packed = v_codes_exact<QMAX>(vx[it], p);
       *reinterpret_cast<uint32_t*>(vcodes + t * CLD + 4 * q4) = packed;
     }
