@@ -554,182 +554,323 @@ __global__ void unpack_kernel(int T, int T_cap, int d, Packed p, float* K_hat, f
 
 // ------------------------------------------------------------------ token score
 //
-// Two passes over q_obs . K^T on CUDA cores (fp32), CTA tile = all NR = G*n_obs
-// rows of one KV head x 128 tokens, d in shared memory transposed.
-//   pass 1: per row, (max, sum exp) over its visible tokens, per token range;
-//   pass 2: merge the ranges' (max, sum), then score[t] = sum_r p_r(t).
-constexpr int kScoreThreads = 256;    // 16 (row lanes) x 16 (token lanes)
-constexpr int kTT = 128;              // tokens per tile
-constexpr int kTilesPerRange = 4;     // pass-1 CTA covers 4 tiles = 512 tokens
+// S = q_obs . K^T per KV head on the tensor cores (mma.sync m16n8k16, bf16
+// operands, fp32 accumulate; the products of bf16 values are exact), log2
+// softmax scale applied to the fp32 sums.  A CTA covers kScoreRange = 1024
+// tokens of one (b, KV head) in kScoreTile = 128-token K tiles, double-buffered
+// with cp.async; all NR = G * n_obs rows sit in shared memory.  Warp w owns the
+// 32-token quarter w % 4 of each tile (its B fragments stay in registers for the
+// tile) and the 16-row m-tiles w / 4 + 4 k.
+//   pass 1: per row, (max, sum exp2) over the row's visible tokens of the range;
+//   merge:  per row, (M, 1 / S) over all ranges;
+//   pass 2: score[t] = sum_r exp2(s_rt - M_r) / S_r.
+constexpr int kScoreThreads = 512;                 // 16 warps
+constexpr int kScoreMG = kScoreThreads / 128;      // m-tile groups (warps per token quarter)
+constexpr int kScoreTile = 128;
+constexpr int kScoreTilesPerRange = 8;
+constexpr int kScoreRange = kScoreTilesPerRange * kScoreTile;
 
 struct ScoreArgs {
   const uint16_t* q;    // [B, Hq, n_obs, d]
   const uint16_t* K;    // [B, Hkv, T, d]
-  int T, n_obs, Hq, Hkv, d;
+  int T, n_obs, Hq, Hkv;
   float scale_log2;     // softmax_scale * log2(e)
-  float2* stats;        // [B*Hkv, n_ranges, NR] (max, sum) in log2 units
+  float2* stats;        // [B*Hkv, n_ranges, NR] (max, sum) per range, log2 units
+  float2* rowstat;      // [B*Hkv, NR] (M, 1 / S)
   int n_ranges;
   float* score;         // [B, Hkv, T]
 };
 
-// Shared memory: qT [d][NR] fp32, kT [d][kTT + 1] fp32.
-template <int RPT>
-__device__ void load_q(const ScoreArgs& a, int b, int kvh, float* qT) {
-  const int NR = RPT * 16;
+__device__ __forceinline__ void sc_cp_async16(void* smem, const void* gmem, bool valid) {
+  const int n = valid ? 16 : 0;                    // src-size 0: zero fill
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(vc_smem_addr(smem)), "l"(gmem), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void sc_cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void sc_cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void sc_ldsm_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(vc_smem_addr(p)));
+}
+// 2^x (ex2.approx.ftz: relative error ~2^-22; results below 2^-126 flush to 0)
+__device__ __forceinline__ float sc_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32
+__device__ __forceinline__ void sc_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int MT, int D>
+struct ScoreCfg {
+  static constexpr int NR = 16 * MT;               // rows = G * n_obs
+  static constexpr int LD = D + 8;                 // padded smem row (bf16): conflict-free ldmatrix
+  static constexpr int KS = D / 16;                // k-steps
+  static constexpr int MTW = (MT + kScoreMG - 1) / kScoreMG;   // m-tiles per warp (at most)
+  static constexpr size_t q_bytes = static_cast<size_t>(NR) * LD * 2;
+  static constexpr size_t k_bytes = 2ull * kScoreTile * LD * 2;
+  // pass 1: 4 x NR float2 quarter statistics; pass 2: NR float2 row stats + kScoreMG x 128 column sums
+  static constexpr size_t red_p2 = NR * 8 + kScoreMG * kScoreTile * 4;
+  static constexpr size_t red_bytes = (4 * NR * 8 > red_p2) ? 4 * NR * 8 : red_p2;
+  static constexpr size_t smem = q_bytes + k_bytes + red_bytes;
+};
+
+// Q rows of KV head kvh (row r = g * n_obs + o is query head kvh*G + g, obs o)
+// and the range's first K tile, by cp.async; the caller commits.
+template <int MT, int D>
+__device__ __forceinline__ void score_load_q(const ScoreArgs& a, int b, int kvh, uint16_t* q_s) {
+  using C = ScoreCfg<MT, D>;
+  constexpr int VEC = D / 8;
   const int G = a.Hq / a.Hkv;
-  for (int i = threadIdx.x; i < NR * a.d; i += blockDim.x) {
-    const int r = i / a.d, c = i % a.d;
+  for (int i = threadIdx.x; i < C::NR * VEC; i += blockDim.x) {
+    const int r = i / VEC, v = i % VEC;
     const int g = r / a.n_obs, o = r % a.n_obs;
-    const size_t src = ((static_cast<size_t>(b) * a.Hq + kvh * G + g) * a.n_obs + o) * a.d + c;
-    qT[c * NR + r] = vc_bf16_to_f32(a.q[src]) * a.scale_log2;
+    const uint16_t* src = a.q + ((static_cast<size_t>(b) * a.Hq + kvh * G + g) * a.n_obs + o) * D + v * 8;
+    sc_cp_async16(q_s + r * C::LD + v * 8, src, true);
   }
 }
 
-__device__ void load_kT(const ScoreArgs& a, int bh, int t0, float* kT) {
-  for (int i = threadIdx.x; i < kTT * a.d; i += blockDim.x) {
-    const int t = i / a.d, c = i % a.d;
-    float x = 0.0f;
-    if (t0 + t < a.T) x = vc_bf16_to_f32(a.K[(static_cast<size_t>(bh) * a.T + t0 + t) * a.d + c]);
-    kT[c * (kTT + 1) + t] = x;
+template <int MT, int D>
+__device__ __forceinline__ void score_load_k(const ScoreArgs& a, int bh, int t0, uint16_t* k_s) {
+  using C = ScoreCfg<MT, D>;
+  constexpr int VEC = D / 8;
+  for (int i = threadIdx.x; i < kScoreTile * VEC; i += blockDim.x) {
+    const int t = i / VEC, v = i % VEC;
+    const bool ok = t0 + t < a.T;
+    const uint16_t* src = a.K + (ok ? ((static_cast<size_t>(bh) * a.T + t0 + t) * D + v * 8) : 0);
+    sc_cp_async16(k_s + t * C::LD + v * 8, src, ok);
   }
 }
 
-// acc[i][j] = q_row(ty + 16 i) . k_tok(tx + 16 j), log2-scaled.
-template <int RPT>
-__device__ __forceinline__ void tile_dots(const float* qT, const float* kT, int d, int ty, int tx,
-                                          float (&acc)[RPT][8]) {
-  const int NR = RPT * 16;
+// The quarter's B fragments: kb[ks][np] covers tokens quarter*32 + np*16 .. +15
+// (n-tiles 2np, 2np + 1), channels ks*16 .. +15.
+template <int MT, int D>
+__device__ __forceinline__ void score_b_frags(const uint16_t* kt, int quarter, int lane,
+                                              uint32_t (&kb)[ScoreCfg<MT, D>::KS][2][4]) {
+  using C = ScoreCfg<MT, D>;
 #pragma unroll
-  for (int i = 0; i < RPT; ++i)
+  for (int ks = 0; ks < C::KS; ++ks)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
-  for (int c = 0; c < d; ++c) {
-    float qv[RPT], kv[8];
+    for (int np = 0; np < 2; ++np)
+      sc_ldsm_x4(kb[ks][np], kt + (quarter * 32 + np * 16 + (lane & 7) + ((lane >> 4) << 3)) * C::LD + ks * 16 +
+                                     ((lane >> 3) & 1) * 8);
+}
+
+// s[nt][e] = q.k (unscaled) of row mt*16 + gid + 8 (e >> 1), token quarter*32 +
+// nt*8 + 2 tig + (e & 1) of the tile; -inf where the row does not see it.
+template <int MT, int D>
+__device__ __forceinline__ void score_item(const ScoreArgs& a, const uint16_t* q_s,
+                                           const uint32_t (&kb)[ScoreCfg<MT, D>::KS][2][4], int mt, int tq0,
+                                           int lane, float (&s)[4][4]) {
+  using C = ScoreCfg<MT, D>;
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) qv[i] = qT[c * NR + ty + 16 * i];
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) kv[j] = kT[c * (kTT + 1) + tx + 16 * j];
+    for (int e = 0; e < 4; ++e) s[nt][e] = 0.0f;
 #pragma unroll
-    for (int i = 0; i < RPT; ++i)
+  for (int ks = 0; ks < C::KS; ++ks) {
+    uint32_t qa[4];
+    sc_ldsm_x4(qa, q_s + (mt * 16 + (lane & 15)) * C::LD + ks * 16 + (lane >> 4) * 8);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(qv[i], kv[j], acc[i][j]);
+    for (int np = 0; np < 2; ++np) {
+      sc_mma(s[2 * np], qa, kb[ks][np][0], kb[ks][np][1]);
+      sc_mma(s[2 * np + 1], qa, kb[ks][np][2], kb[ks][np][3]);
+    }
+  }
+  // row r sees tokens t <= T - n_obs + r % n_obs: only quarters that reach the
+  // observation window (or run past T) need the mask
+  if (tq0 + 32 > a.T - a.n_obs) {
+    const int r0 = mt * 16 + (lane >> 2);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int last = a.T - a.n_obs + (r0 + 8 * h) % a.n_obs;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          if (tq0 + nt * 8 + (lane & 3) * 2 + c > last) s[nt][2 * h + c] = -INFINITY;
+    }
   }
 }
 
 // grid (n_ranges, B*Hkv)
-template <int RPT>
+template <int MT, int D>
 __global__ void __launch_bounds__(kScoreThreads) score_pass1(ScoreArgs a) {
-  extern __shared__ __align__(16) float fsm[];
-  const int NR = RPT * 16;
-  float* qT = fsm;
-  float* kT = qT + NR * a.d;
+  using C = ScoreCfg<MT, D>;
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint16_t* q_s = reinterpret_cast<uint16_t*>(smem);
+  uint16_t* k_s = reinterpret_cast<uint16_t*>(smem + C::q_bytes);
+  float2* red = reinterpret_cast<float2*>(smem + C::q_bytes + C::k_bytes);    // [4][NR]
   const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh % a.Hkv;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  load_q<RPT>(a, b, kvh, qT);
-  float m[RPT], s[RPT];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3;
+  const int r0 = blockIdx.x * kScoreRange;
+  const int n_tiles = min(kScoreTilesPerRange, (a.T - r0 + kScoreTile - 1) / kScoreTile);
+  score_load_q<MT, D>(a, b, kvh, q_s);
+  score_load_k<MT, D>(a, bh, r0, k_s);
+  sc_cp_async_commit();
+  float m[C::MTW][2], l[C::MTW][2];
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) { m[i] = -INFINITY; s[i] = 0.0f; }
-  for (int tile = 0; tile < kTilesPerRange; ++tile) {
-    const int t0 = (blockIdx.x * kTilesPerRange + tile) * kTT;
-    if (t0 >= a.T) break;
+  for (int k = 0; k < C::MTW; ++k) m[k][0] = m[k][1] = -INFINITY, l[k][0] = l[k][1] = 0.0f;
+  for (int it = 0; it < n_tiles; ++it) {
+    if (it + 1 < n_tiles) {
+      score_load_k<MT, D>(a, bh, r0 + (it + 1) * kScoreTile, k_s + ((it + 1) & 1) * kScoreTile * C::LD);
+      sc_cp_async_commit();
+      sc_cp_async_wait<1>();
+    } else {
+      sc_cp_async_wait<0>();
+    }
     __syncthreads();
-    load_kT(a, bh, t0, kT);
-    __syncthreads();
-    float acc[RPT][8];
-    tile_dots<RPT>(qT, kT, a.d, ty, tx, acc);
+    uint32_t kb[C::KS][2][4];
+    score_b_frags<MT, D>(k_s + (it & 1) * kScoreTile * C::LD, quarter, lane, kb);
+    const int tq0 = r0 + it * kScoreTile + quarter * 32;
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-      const int r = ty + 16 * i;
-      const int last = a.T - a.n_obs + (r % a.n_obs);        // inclusive visible limit
-      float tmax = -INFINITY;
+    for (int k = 0; k < C::MTW; ++k) {
+      const int mt = (warp >> 2) + kScoreMG * k;
+      if (mt >= MT) break;
+      float s[4][4];
+      score_item<MT, D>(a, q_s, kb, mt, tq0, lane, s);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int t = t0 + tx + 16 * j;
-        if (t > last) acc[i][j] = -INFINITY;
-        tmax = fmaxf(tmax, acc[i][j]);
+      for (int h = 0; h < 2; ++h) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) mx = fmaxf(mx, fmaxf(s[nt][2 * h], s[nt][2 * h + 1]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+        const float mn = fmaxf(m[k][h], mx * a.scale_log2);     // log2 units (scale > 0)
+        if (mn == -INFINITY) continue;             // nothing visible yet (quad-uniform)
+        float add = 0.0f;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) add += sc_exp2(fmaf(s[nt][2 * h + c], a.scale_log2, -mn));
+        l[k][h] = l[k][h] * sc_exp2(m[k][h] - mn) + add;
+        m[k][h] = mn;
       }
+    }
+    __syncthreads();                               // buffer it & 1 is refilled next
+  }
+  // quad sums, then the 4 quarters of every row
 #pragma unroll
-      for (int off = 8; off > 0; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
-      const float mn = fmaxf(m[i], tmax);
-      if (mn == -INFINITY) continue;
-      float add = 0.0f;
+  for (int k = 0; k < C::MTW; ++k) {
+    const int mt = (warp >> 2) + kScoreMG * k;
+    if (mt >= MT) break;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) add += exp2f(acc[i][j] - mn);
-      s[i] = s[i] * exp2f(m[i] - mn) + add;
-      m[i] = mn;
+    for (int h = 0; h < 2; ++h) {
+      float x = l[k][h];
+      x += __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+      x += __shfl_xor_sync(0xFFFFFFFFu, x, 2);
+      if ((lane & 3) == 0) red[quarter * C::NR + mt * 16 + (lane >> 2) + 8 * h] = make_float2(m[k][h], x);
     }
   }
-  // sum the 16 token lanes (all hold the same m)
+  __syncthreads();
+  for (int r = threadIdx.x; r < C::NR; r += blockDim.x) {
+    float M = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) {
+    for (int q = 0; q < 4; ++q) M = fmaxf(M, red[q * C::NR + r].x);
+    float S = 0.0f;
+    if (M != -INFINITY) {
 #pragma unroll
-    for (int off = 8; off > 0; off >>= 1) s[i] += __shfl_xor_sync(0xffffffffu, s[i], off);
-    if (tx == 0) {
-      const int r = ty + 16 * i;
-      a.stats[(static_cast<size_t>(bh) * a.n_ranges + blockIdx.x) * NR + r] = make_float2(m[i], s[i]);
+      for (int q = 0; q < 4; ++q) {
+        const float2 st = red[q * C::NR + r];
+        if (st.x != -INFINITY) S += st.y * exp2f(st.x - M);
+      }
     }
+    a.stats[(static_cast<size_t>(bh) * a.n_ranges + blockIdx.x) * C::NR + r] = make_float2(M, S);
   }
 }
 
-// grid (ceil(T / kTT), B*Hkv)
-template <int RPT>
-__global__ void __launch_bounds__(kScoreThreads) score_pass2(ScoreArgs a) {
-  extern __shared__ __align__(16) float fsm[];
-  const int NR = RPT * 16;
-  float* qT = fsm;
-  float* kT = qT + NR * a.d;
-  float* red = kT + a.d * (kTT + 1);            // [16][kTT]
-  float* rowm = red + 16 * kTT;                 // [NR]
-  float* rowinv = rowm + NR;                    // [NR]
-  const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh % a.Hkv;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  const int t0 = blockIdx.x * kTT;
-  load_q<RPT>(a, b, kvh, qT);
-  // merge the per-range statistics of every row
+// grid (B*Hkv): per row, (M, 1/S) over the ranges.
+__global__ void score_merge(ScoreArgs a, int NR) {
+  const int bh = blockIdx.x;
   for (int r = threadIdx.x; r < NR; r += blockDim.x) {
+    const float2* st = a.stats + static_cast<size_t>(bh) * a.n_ranges * NR + r;
     float M = -INFINITY;
-    for (int x = 0; x < a.n_ranges; ++x)
-      M = fmaxf(M, a.stats[(static_cast<size_t>(bh) * a.n_ranges + x) * NR + r].x);
+    for (int x = 0; x < a.n_ranges; ++x) M = fmaxf(M, st[static_cast<size_t>(x) * NR].x);
     float S = 0.0f;
     for (int x = 0; x < a.n_ranges; ++x) {
-      const float2 st = a.stats[(static_cast<size_t>(bh) * a.n_ranges + x) * NR + r];
-      if (st.x != -INFINITY) S += st.y * exp2f(st.x - M);
+      const float2 v = st[static_cast<size_t>(x) * NR];
+      if (v.x != -INFINITY) S += v.y * exp2f(v.x - M);
     }
-    rowm[r] = M;
-    rowinv[r] = 1.0f / S;
-  }
-  load_kT(a, bh, t0, kT);
-  __syncthreads();
-  float acc[RPT][8];
-  tile_dots<RPT>(qT, kT, a.d, ty, tx, acc);
-  float col[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) col[j] = 0.0f;
-#pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    const int r = ty + 16 * i;
-    const int last = a.T - a.n_obs + (r % a.n_obs);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int t = t0 + tx + 16 * j;
-      if (t <= last) col[j] += exp2f(acc[i][j] - rowm[r]) * rowinv[r];
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) red[ty * kTT + tx + 16 * j] = col[j];
-  __syncthreads();
-  for (int t = threadIdx.x; t < kTT; t += blockDim.x) {
-    if (t0 + t >= a.T) continue;
-    float sum = 0.0f;
-    for (int y = 0; y < 16; ++y) sum += red[y * kTT + t];
-    a.score[static_cast<size_t>(bh) * a.T + t0 + t] = sum;
+    a.rowstat[static_cast<size_t>(bh) * NR + r] = make_float2(M, 1.0f / S);
   }
 }
 
-size_t score_smem(int NR, int d, bool pass2) {
-  size_t f = static_cast<size_t>(NR) * d + static_cast<size_t>(d) * (kTT + 1);
-  if (pass2) f += 16 * kTT + 2 * NR;
-  return f * sizeof(float);
+// grid (n_ranges, B*Hkv)
+template <int MT, int D>
+__global__ void __launch_bounds__(kScoreThreads) score_pass2(ScoreArgs a) {
+  using C = ScoreCfg<MT, D>;
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint16_t* q_s = reinterpret_cast<uint16_t*>(smem);
+  uint16_t* k_s = reinterpret_cast<uint16_t*>(smem + C::q_bytes);
+  float2* rs = reinterpret_cast<float2*>(smem + C::q_bytes + C::k_bytes);    // [NR] (M, 1/S)
+  float* col = reinterpret_cast<float*>(rs + C::NR);                            // [kScoreMG][128]
+  const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh % a.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3;
+  const int r0 = blockIdx.x * kScoreRange;
+  const int n_tiles = min(kScoreTilesPerRange, (a.T - r0 + kScoreTile - 1) / kScoreTile);
+  score_load_q<MT, D>(a, b, kvh, q_s);
+  score_load_k<MT, D>(a, bh, r0, k_s);
+  sc_cp_async_commit();
+  for (int r = threadIdx.x; r < C::NR; r += blockDim.x) rs[r] = a.rowstat[static_cast<size_t>(bh) * C::NR + r];
+  for (int it = 0; it < n_tiles; ++it) {
+    if (it + 1 < n_tiles) {
+      score_load_k<MT, D>(a, bh, r0 + (it + 1) * kScoreTile, k_s + ((it + 1) & 1) * kScoreTile * C::LD);
+      sc_cp_async_commit();
+      sc_cp_async_wait<1>();
+    } else {
+      sc_cp_async_wait<0>();
+    }
+    __syncthreads();
+    uint32_t kb[C::KS][2][4];
+    score_b_frags<MT, D>(k_s + (it & 1) * kScoreTile * C::LD, quarter, lane, kb);
+    const int tq0 = r0 + it * kScoreTile + quarter * 32;
+    float cs[4][2];                                // column partial sums of this thread's rows
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) cs[nt][0] = cs[nt][1] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < C::MTW; ++k) {
+      const int mt = (warp >> 2) + kScoreMG * k;
+      if (mt >= MT) break;
+      float s[4][4];
+      score_item<MT, D>(a, q_s, kb, mt, tq0, lane, s);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float2 st = rs[mt * 16 + (lane >> 2) + 8 * h];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) cs[nt][c] = fmaf(sc_exp2(fmaf(s[nt][2 * h + c], a.scale_log2, -st.x)), st.y, cs[nt][c]);
+      }
+    }
+    // sum over the 8 row groups of the warp, then over the kScoreMG warps of the quarter
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float x = cs[nt][c];
+        x += __shfl_xor_sync(0xFFFFFFFFu, x, 4);
+        x += __shfl_xor_sync(0xFFFFFFFFu, x, 8);
+        x += __shfl_xor_sync(0xFFFFFFFFu, x, 16);
+        if (lane < 4) col[(warp >> 2) * kScoreTile + quarter * 32 + nt * 8 + lane * 2 + c] = x;
+      }
+    __syncthreads();
+    if (threadIdx.x < kScoreTile) {
+      const int t = r0 + it * kScoreTile + threadIdx.x;
+      float x = 0.0f;
+#pragma unroll
+      for (int g = 0; g < kScoreMG; ++g) x += col[g * kScoreTile + threadIdx.x];
+      if (t < a.T) a.score[static_cast<size_t>(bh) * a.T + t] = x;
+    }
+    __syncthreads();                               // buffer it & 1 and col are reused next
+  }
 }
 
 // ------------------------------------------------------------------ select
@@ -991,7 +1132,7 @@ extern "C" vc_status_t vc_quant_kv_append(const vc_shape_t* s, const uint16_t* k
 }
 
 namespace {
-int score_ranges(int T) { return (T + kTT * kTilesPerRange - 1) / (kTT * kTilesPerRange); }
+int score_ranges(int T) { return (T + kScoreRange - 1) / kScoreRange; }
 
 vc_status_t check_score(const vc_shape_t* s, int T, int n_obs, int* NR) {
   vc_status_t st = check_shape(s, false);
@@ -1011,7 +1152,7 @@ extern "C" vc_status_t vc_token_score_workspace_size(const vc_shape_t* s, int32_
   vc_status_t st = check_score(s, T, n_obs, &NR);
   if (st != VC_OK) return st;
   VC_REQUIRE(bytes, "bytes is NULL");
-  *bytes = static_cast<size_t>(s->B) * s->Hkv * score_ranges(T) * NR * sizeof(float2);
+  *bytes = static_cast<size_t>(s->B) * s->Hkv * (score_ranges(T) + 1) * NR * sizeof(float2);
   return VC_OK;
 }
 
@@ -1027,35 +1168,45 @@ extern "C" vc_status_t vc_token_score(const vc_shape_t* s, int32_t T, int32_t n_
   if (!workspace || workspace_bytes < need)
     VC_FAIL(VC_ERR_WORKSPACE, "score workspace needs %zu bytes (got %zu)", need, workspace_bytes);
   ScoreArgs a;
-  a.q = q_obs; a.K = K; a.T = T; a.n_obs = n_obs; a.Hq = s->Hq; a.Hkv = s->Hkv; a.d = s->d;
+  a.q = q_obs; a.K = K; a.T = T; a.n_obs = n_obs; a.Hq = s->Hq; a.Hkv = s->Hkv;
   a.scale_log2 = s->softmax_scale * 1.4426950408889634f;
-  a.stats = static_cast<float2*>(workspace);
   a.n_ranges = score_ranges(T);
+  a.stats = static_cast<float2*>(workspace);
+  a.rowstat = a.stats + static_cast<size_t>(s->B) * s->Hkv * a.n_ranges * NR;
   a.score = score;
-  const int RPT = NR / 16;
   auto cs = reinterpret_cast<cudaStream_t>(stream);
-  dim3 g1(a.n_ranges, s->B * s->Hkv), g2((T + kTT - 1) / kTT, s->B * s->Hkv);
-  const size_t sm1 = score_smem(NR, s->d, false), sm2 = score_smem(NR, s->d, true);
-#define VC_SCORE_CASE(R)                                                                          \
-  case R:                                                                                         \
-    cudaFuncSetAttribute(score_pass1<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1);  \
-    cudaFuncSetAttribute(score_pass2<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);  \
-    score_pass1<R><<<g1, kScoreThreads, sm1, cs>>>(a);                                            \
-    score_pass2<R><<<g2, kScoreThreads, sm2, cs>>>(a);                                            \
-    break;
-  switch (RPT) {
-    VC_SCORE_CASE(1)
-    VC_SCORE_CASE(2)
-    VC_SCORE_CASE(4)
-    VC_SCORE_CASE(6)
-    VC_SCORE_CASE(8)
-    VC_SCORE_CASE(10)
-    VC_SCORE_CASE(12)
-    VC_SCORE_CASE(14)
-    VC_SCORE_CASE(16)
-    default:
-      VC_FAIL(VC_ERR_UNSUPPORTED, "G * n_obs = %d not built (need 16 * {1,2,4,6,...,16})", NR);
+  const dim3 grid(a.n_ranges, s->B * s->Hkv);
+  const int bhs = s->B * s->Hkv;
+#define VC_SCORE_CASE(M, D)                                                                          \
+  case M: {                                                                                          \
+    const int sm = static_cast<int>(ScoreCfg<M, D>::smem);                                           \
+    cudaFuncSetAttribute(score_pass1<M, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);        \
+    cudaFuncSetAttribute(score_pass2<M, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);        \
+    score_pass1<M, D><<<grid, kScoreThreads, sm, cs>>>(a);                                           \
+    score_merge<<<bhs, 256, 0, cs>>>(a, NR);                                                         \
+    score_pass2<M, D><<<grid, kScoreThreads, sm, cs>>>(a);                                           \
+    break;                                                                                           \
   }
+#define VC_SCORE_SWITCH(D)                                                                           \
+  switch (NR / 16) {                                                                                 \
+    VC_SCORE_CASE(1, D)                                                                              \
+    VC_SCORE_CASE(2, D)                                                                              \
+    VC_SCORE_CASE(4, D)                                                                              \
+    VC_SCORE_CASE(6, D)                                                                              \
+    VC_SCORE_CASE(8, D)                                                                              \
+    VC_SCORE_CASE(10, D)                                                                             \
+    VC_SCORE_CASE(12, D)                                                                             \
+    VC_SCORE_CASE(14, D)                                                                             \
+    VC_SCORE_CASE(16, D)                                                                             \
+    default:                                                                                         \
+      VC_FAIL(VC_ERR_UNSUPPORTED, "G * n_obs = %d not built (need 16 * {1,2,4,6,...,16})", NR);      \
+  }
+  if (s->d == 128) {
+    VC_SCORE_SWITCH(128)
+  } else {
+    VC_SCORE_SWITCH(64)
+  }
+#undef VC_SCORE_SWITCH
 #undef VC_SCORE_CASE
   VC_LAUNCH_CHECK("token score");
   return VC_OK;
