@@ -261,11 +261,6 @@ def time_kernel(fn, stream, reps=20, warm=3):
     return e0.elapsed_time(e1) / reps
 
 
-def alu_peak_tflops(peaks):
-    """fp32 CUDA-core peak: 152 SMs x 128 lanes x 2 flops per FMA x the maximum SM clock."""
-    return 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
-
-
 def time_token_drop(w, shape, Kd, Vd, device, cs):
     """Score, select and gather of the token-dropping compressor on layer 0,
     each timed alone against its roofline."""
@@ -290,12 +285,53 @@ def time_token_drop(w, shape, Kd, Vd, device, cs):
     Vo = torch.empty_like(Ko)
     t_gat = time_kernel(lambda: vc.vc_gather_kv(shape, w.T, keep, idx, Kd, Vd, Ko, Vo, cs), cs, reps=10)
     gat_bytes = 2 * 2 * w.B * w.Hkv * keep * w.d * 2
-    return {"a3_token_score": {"ms": t_score, "tflops": flops / (t_score / 1e3) / 1e12, "bound": "alu",
-                               "peak_tflops": alu_peak_tflops(peaks),
-                               "frac": flops / (t_score / 1e3) / 1e12 / alu_peak_tflops(peaks)},
+    # logits on the tensor cores (mma.sync bf16): against the measured dense bf16 peak
+    return {"a3_token_score": {"ms": t_score, "tflops": flops / (t_score / 1e3) / 1e12, "bound": "tensor",
+                               "peak_tflops": peaks["bf16_tflops"],
+                               "frac": flops / (t_score / 1e3) / 1e12 / peaks["bf16_tflops"]},
             "a4_token_select": {"ms": t_sel, "bound": "latency (6 passes over the pooled scores)"},
             "a4_gather": {"ms": t_gat, "gbs": gat_bytes / (t_gat / 1e3) / 1e9, "bound": "hbm",
                           "frac": gat_bytes / (t_gat / 1e3) / 1e9 / peaks["hbm_gbs"]}}
+
+
+def time_prefill_rows(w, shape, device, cs):
+    """The prefill rows of layer 0, each timed alone: quantise + pack of the full
+    prefix and, for the token-dropping compressor, score / select / gather."""
+    import numpy as np
+    import torch
+
+    import synth
+    from verify_compressed_kv_gb300 import _lib as vc
+    peaks = load_peaks()
+    K0, V0 = synth.kv(w, layer=0, group=0, threads=16)
+    K0d = torch.from_numpy(K0.view(np.int16)).to(device)
+    V0d = torch.from_numpy(V0.view(np.int16)).to(device)
+    sb = vc.vc_quant_packed_bytes(shape, w.T)             # scratch packed arrays for the timing
+    scratch = [torch.empty(n, dtype=torch.uint8, device=device) for n in sb]
+    pack_ms = time_kernel(lambda: vc.vc_quant_kv_pack(shape, w.T, w.T, K0d, V0d, *scratch, cs), cs, reps=5)
+    pack_bytes = 2 * w.B * w.Hkv * w.T * w.d * 2 + sum(sb)
+    rows = {"a1_pack": {"ms": pack_ms, "gbs": pack_bytes / (pack_ms / 1e3) / 1e9, "bound": "hbm",
+                        "frac": pack_bytes / (pack_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}}
+    if w.keep_frac < 1.0:
+        rows.update(time_token_drop(w, shape, K0d, V0d, device, cs))
+    del K0d, V0d, scratch
+    torch.cuda.synchronize()
+    return rows
+
+
+def run_rows(args, local_rank):
+    """--rows-only: the prefill rows of one layer, without the decode loop (a small
+    device footprint, e.g. for kernel captures)."""
+    import torch
+
+    from verify_compressed_kv_gb300 import _lib as vc
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    w = workload_of(args)
+    shape = vc.shape(w.B, w.Hq, w.Hkv, w.d, w.k, w.bits, 1.0)
+    cs = torch.cuda.Stream(device)
+    rows = time_prefill_rows(w, shape, device, cs)
+    return {"workload": workload_name(w), "mode": "rows-only", "data": "synthetic", "rows": rows}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -327,29 +363,8 @@ def run_ours(args, rank, world, local_rank):
     link_best = measure_link_gbs(device, xs)
     measured_link = link_best if args.link_peak_gbs <= 0 else args.link_peak_gbs
 
-    # ---- prefill rows timed once: quantise + pack of the full prefix (layer 0)
-    K0, V0 = synth.kv(w, layer=0, group=0, threads=16)
-    K0d = torch.from_numpy(K0.view(np.int16)).to(device)
-    V0d = torch.from_numpy(V0.view(np.int16)).to(device)
-    from verify_compressed_kv_gb300 import _lib as vc
-    g0 = groups[0]
-    sb = vc.vc_quant_packed_bytes(g0.shape, w.T)         # scratch packed arrays for the timing
-    scratch = [torch.empty(n, dtype=torch.uint8, device=device) for n in sb]
-    for _ in range(3):
-        vc.vc_quant_kv_pack(g0.shape, w.T, w.T, K0d, V0d, *scratch, cs)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(cs)
-    for _ in range(5):
-        vc.vc_quant_kv_pack(g0.shape, w.T, w.T, K0d, V0d, *scratch, cs)
-    e1.record(cs)
-    e1.synchronize()
-    pack_ms = e0.elapsed_time(e1) / 5
-    pack_bytes = 2 * w.B * w.Hkv * w.T * w.d * 2 + sum(sb)
-    prefill_rows = {}
-    if w.keep_frac < 1.0:
-        prefill_rows = time_token_drop(w, g0.shape, K0d, V0d, device, cs)
-    del K0d, V0d, scratch
-    torch.cuda.synchronize()
+    # ---- prefill rows timed once (layer 0)
+    prefill_rows = time_prefill_rows(w, groups[0].shape, device, cs)
 
     state = {"round": 0}
 
@@ -479,8 +494,6 @@ def run_ours(args, rank, world, local_rank):
     t_acc = time_kernel(lambda: g.accept(inp, cs), cs)
     acc_bytes = w.B * (w.k + 1) * w.V * 4
     rows = {
-        "a1_pack": {"ms": pack_ms, "gbs": pack_bytes / (pack_ms / 1e3) / 1e9, "bound": "hbm",
-                    "frac": pack_bytes / (pack_ms / 1e3) / 1e9 / peaks["hbm_gbs"]},
         "a5_draft": {"ms": draft_call_ms, "gbs": achieved_gbs, "bound": "hbm", "frac": achieved_gbs / peaks["hbm_gbs"]},
         "a7_verify_chunk": {"ms": t_ver, "tflops": ver_flops / (t_ver / 1e3) / 1e12, "bound": "tensor (bf16)",
                             "frac": ver_flops / (t_ver / 1e3) / 1e12 / peaks["bf16_tflops"],
@@ -575,7 +588,6 @@ def run_ours(args, rank, world, local_rank):
         "round_ms": {"median": med(round_ms), "draft": med(draft_span), "copy": med(copy_span),
                      "all": [round(x, 3) for x in round_ms],
                      "host_gap_total": round(total_ms - sum(round_ms), 3)},
-        "prefill_pack": {"ms": pack_ms, "gbs": pack_bytes / (pack_ms / 1e3) / 1e9},
         "rows": rows,
         "full_kv_decode": dict(full_kv, speedup_of_value=value_local / full_kv["value"]),
         "clocks": clk,
@@ -930,12 +942,16 @@ def main(argv=None):
     ap.add_argument("--remote-prefix", type=float, default=0.0, metavar="GBS",
                     help="emulate remote prefix caching: the packed prefix arrives over a link paced at GBS GB/s")
     ap.add_argument("--k-max", type=int, default=60, help="largest draft length of --adaptive (accept takes k + 1 <= 64)")
+    ap.add_argument("--rows-only", action="store_true",
+                    help="time only the prefill rows (pack, token score / select / gather) of one layer")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_setup()
     if args.impl == "reference":
         out = run_reference(args, rank, world)
+    elif args.rows_only:
+        out = run_rows(args, local) if rank == 0 else None
     elif args.adaptive:
         out = run_adaptive(args, local) if rank == 0 else None
     elif args.remote_prefix > 0:
