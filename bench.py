@@ -342,6 +342,7 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
+    from verify_compressed_kv_gb300 import _lib as vc
     from verify_compressed_kv_gb300 import runtime as rt
 
     w = workload_of(args)
