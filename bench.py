@@ -294,6 +294,21 @@ def time_token_drop(w, shape, Kd, Vd, device, cs):
                           "frac": gat_bytes / (t_gat / 1e3) / 1e9 / peaks["hbm_gbs"]}}
 
 
+def verify_row(t_ms, flops, chunk_bytes, peaks, link_gbs):
+    """The verify chunk kernel against its roofline: HBM when its arithmetic
+    intensity (flops per byte of the chunk it reads) is below the bf16 ridge point
+    (tensor peak / HBM peak), else the tensor peak."""
+    tflops = flops / (t_ms / 1e3) / 1e12
+    gbs = chunk_bytes / (t_ms / 1e3) / 1e9
+    intensity = flops / chunk_bytes
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    hbm = intensity < ridge
+    return {"ms": t_ms, "tflops": tflops, "gbs": gbs, "flop_per_byte": intensity, "ridge_flop_per_byte": ridge,
+            "bound": "hbm" if hbm else "tensor (bf16)",
+            "frac": gbs / peaks["hbm_gbs"] if hbm else tflops / peaks["bf16_tflops"],
+            "chunk_transfer_ms": chunk_bytes / (link_gbs * 1e6)}
+
+
 def time_prefill_rows(w, shape, device, cs):
     """The prefill rows of layer 0, each timed alone: quantise + pack of the full
     prefix and, for the token-dropping compressor, score / select / gather."""
@@ -496,9 +511,7 @@ def run_ours(args, rank, world, local_rank):
     acc_bytes = w.B * (w.k + 1) * w.V * 4
     rows = {
         "a5_draft": {"ms": draft_call_ms, "gbs": achieved_gbs, "bound": "hbm", "frac": achieved_gbs / peaks["hbm_gbs"]},
-        "a7_verify_chunk": {"ms": t_ver, "tflops": ver_flops / (t_ver / 1e3) / 1e12, "bound": "tensor (bf16)",
-                            "frac": ver_flops / (t_ver / 1e3) / 1e12 / peaks["bf16_tflops"],
-                            "chunk_transfer_ms": g.chunk_elems * 2 / (measured_link * 1e6)},
+        "a7_verify_chunk": verify_row(t_ver, ver_flops, g.chunk_elems * 2, peaks, measured_link),
         "a8_accept": {"ms": t_acc, "gbs": acc_bytes / (t_acc / 1e3) / 1e9, "bound": "hbm",
                       "frac": acc_bytes / (t_acc / 1e3) / 1e9 / peaks["hbm_gbs"]},
     }
