@@ -257,6 +257,13 @@ vc_status_t vc_draft_attn_device_status(uint32_t* status);
  */
 vc_status_t vc_verify_attn_workspace_size(const vc_shape_t* s, int32_t parts_per_chunk, size_t* bytes);
 
+/* Parts per chunk (split-KV partitions of one chunk launch) for this shape
+ * and chunk length C on the current device: chosen from the chunk kernel's
+ * occupancy so the launch's CTAs fill the SMs in whole waves, with the fewest
+ * tiles per CTA (1 <= parts <= 16).  Pass the result as parts_per_chunk.
+ * Host-only: queries the device, launches nothing. */
+vc_status_t vc_verify_attn_parts(const vc_shape_t* s, int32_t C, int32_t* parts);
+
 /* Low-level, one chunk already in device memory: merge its tokens
  * [chunk_start, chunk_start + C) of every request (only those below
  * prefix_len[b]) into the running partial state.  first != 0 starts a new

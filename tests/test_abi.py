@@ -70,6 +70,9 @@ def test_host_side_argument_checks(vc):
     with pytest.raises(vc.VcError) as e:
         vc.vc_token_select(1, 1, 100, None, 10, 32, 7, None, None, 0, stream=0)   # keep_last > keep
     assert e.value.status == 1
+    with pytest.raises(vc.VcError) as e:
+        vc.vc_verify_attn_parts(s, 0)                                           # C = 0
+    assert e.value.status == 1
 
 
 def test_size_queries_match_the_layout(vc):

@@ -183,10 +183,12 @@ def test_verify_full_size_sampled(vc, name):
     from gpu_util import dev, zeros_bytes, bf16_to_f64, pinned, DEV, assert_attn_close
     w = synth.get(name)
     K, V = synth.kv(w)
-    C, parts, n_slots = w.C, 1, 2
+    C, n_slots = w.C, 2
     n_chunks = w.T // C
     st = pinned(host_store(K, V, C, n_chunks))
     s = vc.shape(w.B, w.Hq, w.Hkv, w.d, k=w.k, softmax_scale=1.0)
+    parts = vc.vc_verify_attn_parts(s, C)                   # as the runtime plans it
+    assert 1 <= parts <= 16
     slots = torch.empty(n_slots * 2 * w.B * w.Hkv * C * w.d, dtype=torch.int16, device=DEV)
     wsb = vc.vc_verify_attn_workspace_size(s, parts)
     ws = zeros_bytes(wsb)

@@ -81,6 +81,7 @@ _SIGS = {
     },
     "vc_verify_attn": {
         "vc_verify_attn_workspace_size": [S, I32, POINTER(c_size_t)],
+        "vc_verify_attn_parts": [S, I32, POINTER(c_int32)],
         "vc_verify_attn_chunk": [S, P, P, I32, I32, P, I32, I32, P, SZ, P],
         "vc_verify_attn_finish": [S, P, P, P, I32, I32, P, P, SZ, P],
         "vc_verify_pipeline_create": [I32, POINTER(c_void_p)],
@@ -238,6 +239,12 @@ def vc_draft_attn_device_status() -> int:
 def vc_verify_attn_workspace_size(s, parts_per_chunk):
     n = c_size_t()
     _call("vc_verify_attn_workspace_size", ctypes.byref(s), parts_per_chunk, ctypes.byref(n))
+    return n.value
+
+
+def vc_verify_attn_parts(s, C):
+    n = c_int32()
+    _call("vc_verify_attn_parts", ctypes.byref(s), C, ctypes.byref(n))
     return n.value
 
 

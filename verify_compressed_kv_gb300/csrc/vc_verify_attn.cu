@@ -37,6 +37,11 @@ __device__ uint32_t g_verify_status = 0;
 
 constexpr int kTile = 64;              // tokens per K/V tile
 constexpr int kMaxWarps = 8;           // 16 query rows per warp
+// Launch bound of the attention kernels: 384 threads caps registers at 168, so three
+// warps fit per scheduler and two CTAs of up to 6 warps share an SM (they launch
+// with at most kMaxWarps warps)
+constexpr int kBoundThreads = 384;
+constexpr int kMaxPlannedParts = 16;   // vc_verify_attn_parts searches 1 .. 16
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------------ PTX helpers
@@ -259,7 +264,7 @@ __device__ __forceinline__ void finish_l(float (&l)[2]) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kMaxWarps * 32) verify_chunk_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(kBoundThreads) verify_chunk_kernel(VerifyArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   constexpr int LD = Cfg<D>::LD;
   const int nw = blockDim.x >> 5;
@@ -335,7 +340,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) verify_chunk_kernel(VerifyArgs
 // New-token causal block + merge of every part state -> bf16 output.
 // grid (row blocks, B*Hkv).
 template <int D>
-__global__ void __launch_bounds__(kMaxWarps * 32) verify_finish_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(kBoundThreads) verify_finish_kernel(VerifyArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   constexpr int LD = Cfg<D>::LD;
   const int nw = blockDim.x >> 5;
@@ -483,6 +488,8 @@ template <int D>
 vc_status_t launch_chunk(const VerifyArgs& a, const Geometry& g, cudaStream_t cs) {
   const size_t sm = smem_bytes<D>(g.nw);
   VC_CUDA_CHECK(cudaFuncSetAttribute(verify_chunk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+  VC_CUDA_CHECK(cudaFuncSetAttribute(verify_chunk_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared));   // two CTAs per SM
   verify_chunk_kernel<D><<<dim3(a.parts, g.row_blocks, a.B * a.Hkv), g.nw * 32, sm, cs>>>(a);
   VC_LAUNCH_CHECK("verify_chunk_kernel");
   return VC_OK;
@@ -581,6 +588,51 @@ extern "C" vc_status_t vc_verify_attn_workspace_size(const vc_shape_t* s, int32_
   VC_REQUIRE(bytes, "bytes is NULL");
   VC_REQUIRE(parts_per_chunk >= 1 && parts_per_chunk <= 64, "1 <= parts_per_chunk <= 64");
   *bytes = ws_bytes(s, parts_per_chunk);
+  return VC_OK;
+}
+
+// Parts per chunk for a chunk launch: the CTAs that fit at once (occupancy of
+// the chunk kernel x SMs) run in waves, and each CTA walks ceil(tiles / parts)
+// 64-token tiles and then merges its state (about one tile's worth of traffic);
+// pick the parts with the least waves x (tiles per part + 1), fewest on ties.
+namespace {
+template <int D>
+vc_status_t plan_parts(const vc_shape_t* s, int C, int* parts) {
+  const Geometry g = geometry(s);
+  const size_t sm = smem_bytes<D>(g.nw);
+  VC_CUDA_CHECK(cudaFuncSetAttribute(verify_chunk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+  VC_CUDA_CHECK(cudaFuncSetAttribute(verify_chunk_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared));   // two CTAs per SM
+  int per_sm = 0, dev = 0, sms = 0;
+  VC_CUDA_CHECK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_chunk_kernel<D>, g.nw * 32, sm));
+  VC_CUDA_CHECK(cudaGetDevice(&dev));
+  VC_CUDA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t slots = static_cast<int64_t>(per_sm > 0 ? per_sm : 1) * sms;
+  const int64_t units = static_cast<int64_t>(s->B) * s->Hkv * g.row_blocks;
+  const int tiles = (C + kTile - 1) / kTile;
+  int best = 1;
+  int64_t best_cost = INT64_MAX;
+  for (int p = 1; p <= kMaxPlannedParts && p <= tiles; ++p) {
+    const int64_t waves = (units * p + slots - 1) / slots;
+    const int64_t cost = waves * ((tiles + p - 1) / p + 1);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = p;
+    }
+  }
+  *parts = best;
+  return VC_OK;
+}
+}  // namespace
+
+extern "C" vc_status_t vc_verify_attn_parts(const vc_shape_t* s, int32_t C, int32_t* parts) {
+  vc_status_t st = check(s);
+  if (st != VC_OK) return st;
+  VC_REQUIRE(C >= 1 && parts, "need C >= 1 and parts != NULL");
+  int p = 1;
+  st = s->d == 128 ? plan_parts<128>(s, C, &p) : plan_parts<64>(s, C, &p);
+  if (st != VC_OK) return st;
+  *parts = p;
   return VC_OK;
 }
 

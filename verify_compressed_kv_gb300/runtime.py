@@ -69,12 +69,8 @@ class Group:
         self.P_cap = int(math.ceil((self.P0 + extra) / GROUP) * GROUP)
         self.tail_cap = GROUP + k + 1
         if parts_per_chunk is None:
-            # split each chunk so one chunk launch gives about two CTAs per SM:
-            # CTAs = parts * B * Hkv * row blocks of up to 128 query rows
-            rows = (k + 1) * (Hq // Hkv)
-            row_blocks = -(-(-(-rows // 16)) // 8)
-            sms = torch.cuda.get_device_properties(torch.device(device)).multi_processor_count
-            parts_per_chunk = max(1, min(8, -(-2 * sms // (B * Hkv * row_blocks))))
+            # the library plans the split from its chunk kernel's occupancy (whole waves)
+            parts_per_chunk = vc.vc_verify_attn_parts(self.shape, C)
         self.parts = parts_per_chunk
         dev = self.device
         # ---- draft caches, one per layer
