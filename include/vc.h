@@ -87,7 +87,11 @@ const char* vc_last_error(void);
  * values: s = fp16((max - min) / (2^b - 1)), z = fp16(min),
  * code = clamp(rint((x - z) / s), 0, 2^b - 1) with round-half-even (0 if
  * s == 0); dequantised x^ = fma(code, s, z) in fp32.  Keys group along 32
- * tokens of one channel, values along 32 channels of one token.
+ * tokens of one channel, values along 32 channels of one token.  The codes
+ * are those of this recipe in fp32 with a correctly rounded subtract and
+ * divide, bit for bit (the kernel reaches them through a per-group reciprocal
+ * and takes the division itself only near a rounding tie).  Inputs are
+ * expected finite; a NaN element gets code 0.
  *
  * Packed draft cache of capacity T_cap tokens (T_cap % 32 == 0), NG = T_cap / 32
  * groups of 32 tokens.  The bit placement is this library's own format: it
