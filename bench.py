@@ -365,7 +365,7 @@ def run_ours(args, rank, world, local_rank):
     n_groups = w.groups
     rounds_total = args.warmup + args.steps + 1
     n_inp = min(3, rounds_total)
-    n_slots = args.slots
+    n_slots = args.slots or None
     cs = torch.cuda.Stream(device)
     xs = torch.cuda.Stream(device)
     groups = [build_group(w, layers, device, rounds_total, n_slots, gi) for gi in range(n_groups)]
@@ -502,9 +502,9 @@ def run_ours(args, rank, world, local_rank):
     draft_in_round_ms = med(draft_span) / (w.k * layers)
 
     # ---- the other rows of the path, each timed alone against its roofline
-    g.slots[:g.chunk_elems].copy_(g.host_kv[0][:g.chunk_elems])       # one resident chunk
+    g.ring[0][:g.chunk_elems].copy_(g.host_kv[0][:g.chunk_elems])     # one resident chunk
     torch.cuda.synchronize()
-    t_ver = time_kernel(lambda: vc.vc_verify_attn_chunk(g.shape, inp.q_verify[0], g.slots, g.C, 0, g.prefix_len[0],
+    t_ver = time_kernel(lambda: vc.vc_verify_attn_chunk(g.shape, inp.q_verify[0], g.ring[0], g.C, 0, g.prefix_len[0],
                                                         g.parts, True, g.ws_verify, g.ws_verify_bytes, cs), cs)
     ver_flops = 4.0 * w.B * w.Hq * (w.k + 1) * w.C * w.d               # QK and PV of (k+1)*Hq rows x C tokens
     t_acc = time_kernel(lambda: g.accept(inp, cs), cs)
@@ -582,7 +582,7 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded; shapes and distributions of the workload; no weights)",
         "config": {"workload": workload_name(w), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "T": w.T,
                    "k": w.k, "bits": w.bits, "layers": layers, "groups": n_groups, "V": w.V, "chunk": w.C,
-                   "schedule": "single" if n_groups == 1 else args.schedule, "slots": n_slots,
+                   "schedule": "single" if n_groups == 1 else args.schedule, "slots_per_layer": groups[0].n_slots,
                    "l2": "inputs larger than L2 (packed cache %d MiB, full KV %d MiB per round)" % (
                        alg_bytes // 2 ** 20, g.h2d_bytes() // 2 ** 20),
                    "parallelism": "replicas" if world > 1 else "single"},
@@ -756,7 +756,7 @@ def run_adaptive(args, local_rank):
     k_max = max(args.k_max, w.k)
     choices = sorted({w.k, k_max} | {c for c in range(4, k_max + 1, 4)})
     rounds_total = args.warmup + 2 * args.steps + 4
-    g = build_group(dataclasses.replace(w, k=k_max), w.layers, device, rounds_total, args.slots)
+    g = build_group(dataclasses.replace(w, k=k_max), w.layers, device, rounds_total, args.slots or None)
     n_inp = 3
     inputs = {k: [to_device(make_round_inputs(dataclasses.replace(w, k=k), r, 0, device, w.layers), device)
                   for r in range(n_inp)] for k in choices}
@@ -768,7 +768,7 @@ def run_adaptive(args, local_rank):
     # verify compute per row: the chunk kernel alone on a resident slot, at the
     # smallest and the largest draft length (slope = cost of one more row)
     from verify_compressed_kv_gb300 import _lib as vc
-    g.slots[:g.chunk_elems].copy_(g.host_kv[0][:g.chunk_elems])     # chunk 0 of layer 0 into slot 0
+    g.ring[0][:g.chunk_elems].copy_(g.host_kv[0][:g.chunk_elems])   # chunk 0 of layer 0 into slot 0
     torch.cuda.synchronize()
 
     def chunk_ms(k, reps=20):
@@ -778,7 +778,7 @@ def run_adaptive(args, local_rank):
         for i in range(reps + 3):
             if i == 3:
                 e0.record(cs)
-            vc.vc_verify_attn_chunk(sh, q, g.slots, g.C, 0, g.prefix_len[0], g.parts, True, g.ws_verify,
+            vc.vc_verify_attn_chunk(sh, q, g.ring[0], g.C, 0, g.prefix_len[0], g.parts, True, g.ws_verify,
                                     g.ws_verify_bytes, cs)
         e1.record(cs)
         e1.synchronize()
@@ -854,7 +854,7 @@ def run_remote(args, local_rank):
         raise SystemExit("--remote-prefix runs the single-group workloads without token dropping")
     rate = args.remote_prefix
     rounds = args.warmup + args.steps
-    g = build_group(w, w.layers, device, rounds + 2, args.slots)
+    g = build_group(w, w.layers, device, rounds + 2, args.slots or None)
     host = [g.export_packed(l, w.T) for l in range(w.layers)]
     for l in range(w.layers):                     # the draft cache now only exists remotely
         for x in (g.kc, g.ksz, g.vc, g.vsz):
@@ -944,7 +944,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="mistral", choices=["tiny", "mistral", "qwen", "llama", "stagger"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--schedule", default="staggered", choices=["staggered", "lockstep"])
-    ap.add_argument("--slots", type=int, default=8)
+    ap.add_argument("--slots", type=int, default=0,
+                    help="verify ring slots per layer (0: as many as the layer's chunks, within a 32 GiB budget)")
     ap.add_argument("--clock-ms", type=int, default=50, help="nvidia-smi sampling interval during the timed region")
     ap.add_argument("--link-peak-gbs", type=float, default=0.0,
                     help="pinned host->device peak in GB/s (default 0: measure it at start-up)")

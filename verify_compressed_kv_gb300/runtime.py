@@ -57,8 +57,9 @@ class RoundInputs:
 
 
 class Group:
-    def __init__(self, B, Hq, Hkv, d, k, bits, V, C, T0, layers=1, extra_tokens=None, n_slots=4,
-                 parts_per_chunk=None, softmax_scale=1.0, device="cuda", packed_T0=None):
+    def __init__(self, B, Hq, Hkv, d, k, bits, V, C, T0, layers=1, extra_tokens=None, n_slots=None,
+                 parts_per_chunk=None, softmax_scale=1.0, device="cuda", packed_T0=None,
+                 ring_budget_bytes=32 << 30):
         self.B, self.Hq, self.Hkv, self.d, self.k, self.bits, self.V = B, Hq, Hkv, d, k, bits, V
         self.C, self.L = C, layers
         self.device = torch.device(device)
@@ -90,9 +91,15 @@ class Group:
                         for _ in range(layers)]
         self.prefix_len = [torch.zeros(B, dtype=torch.int32, device=dev) for _ in range(layers)]
         self.max_prefix = 0          # host-side bound of prefix_len (exact: read back every round)
-        # ---- verify ring + workspaces
-        self.n_slots = n_slots
-        self.slots = _i16(n_slots * self.chunk_elems, dev)
+        # ---- verify rings (one per layer) + workspaces.  A round prefetches every
+        # layer's first chunks while the group drafts, so the link is busy from the
+        # start of the round; by default each ring holds all of its layer's chunks
+        # when the rings of all layers fit the HBM budget.
+        if n_slots is None:
+            per_layer = ring_budget_bytes // (layers * self.chunk_elems * 2)
+            n_slots = int(max(2, min(self.n_chunks_cap, per_layer)))
+        self.n_slots = n_slots                 # per layer
+        self.ring = [_i16(n_slots * self.chunk_elems, dev) for _ in range(layers)]
         # sized for every draft length a round may use (1 .. k): the needs are not monotone in k
         self.ws_verify_bytes = max(vc.vc_verify_attn_workspace_size(
             vc.shape(B, Hq, Hkv, d, k=kk, bits=bits, softmax_scale=softmax_scale), self.parts) for kk in range(1, k + 1))
@@ -101,8 +108,7 @@ class Group:
         self.ws_draft = torch.zeros(self.ws_draft_bytes, dtype=torch.uint8, device=dev)
         self.ws_accept_bytes = max(vc.vc_accept_workspace_size(B, kk, V) for kk in range(1, k + 1))
         self.ws_accept = torch.zeros(self.ws_accept_bytes, dtype=torch.uint8, device=dev)
-        # one ring for all layers: its per-slot events order slot reuse across layers too
-        self.pipe = vc.vc_verify_pipeline_create(n_slots)
+        self.pipes = [vc.vc_verify_pipeline_create(n_slots) for _ in range(layers)]
         self.launches = 0                      # kernels launched through this group
         # ---- per-round outputs
         self.draft_out = _i16((B, Hq, d), dev)
@@ -131,9 +137,9 @@ class Group:
         return self.verify_out.view(-1)[:n].view(self.B, k + 1, self.Hq, self.d)
 
     def close(self):
-        if self.pipe:
-            vc.vc_verify_pipeline_destroy(self.pipe)
-        self.pipe = None
+        for p in self.pipes:
+            vc.vc_verify_pipeline_destroy(p)
+        self.pipes = []
 
     # ---------------------------------------------------------------- prefill
     def load_prefix(self, layer, K, V, stream=None):
@@ -210,8 +216,13 @@ class Group:
 
     # ---------------------------------------------------------------- the round's steps
     def prefetch(self, layer, copy_stream):
-        vc.vc_verify_prefetch(self.pipe, self.shape, self.host_kv[layer], self.C, self.max_prefix,
-                              self.slots, copy_stream)
+        vc.vc_verify_prefetch(self.pipes[layer], self.shape, self.host_kv[layer], self.C, self.max_prefix,
+                              self.ring[layer], copy_stream)
+
+    def prefetch_all(self, copy_stream):
+        """Every layer's first n_slots chunks, in layer order, on the copy stream."""
+        for layer in range(self.L):
+            self.prefetch(layer, copy_stream)
 
     def draft_step(self, inp: RoundInputs, layer: int, step: int, stream):
         vc.vc_draft_attn(self.shape, inp.q_draft[layer, step], inp.kv_cur[0, layer, step], inp.kv_cur[1, layer, step],
@@ -221,8 +232,8 @@ class Group:
         self.launches += 3                     # split-KV, tail, combine
 
     def verify(self, inp: RoundInputs, layer: int, compute_stream, copy_stream):
-        vc.vc_verify_attn_streamed(self.pipe, self.shape_k(inp.k), inp.q_verify[layer], self.host_kv[layer], self.C,
-                                   self.max_prefix, self.prefix_len[layer], self.slots, inp.kv_new[0, layer],
+        vc.vc_verify_attn_streamed(self.pipes[layer], self.shape_k(inp.k), inp.q_verify[layer], self.host_kv[layer],
+                                   self.C, self.max_prefix, self.prefix_len[layer], self.ring[layer], inp.kv_new[0, layer],
                                    inp.kv_new[1, layer], self.verify_out_k(inp.k), self.parts, self.ws_verify,
                                    self.ws_verify_bytes, compute_stream, copy_stream)
         self.launches += self.chunks() + 1     # one kernel per chunk, then the new-token block + merge
@@ -236,8 +247,8 @@ class Group:
                                     softmax_scale=self.shape.softmax_scale)
             self._ws0_bytes = vc.vc_verify_attn_workspace_size(self._shape0, self.parts)
             self._ws0 = torch.zeros(self._ws0_bytes, dtype=torch.uint8, device=self.device)
-        vc.vc_verify_attn_streamed(self.pipe, self._shape0, q1, self.host_kv[layer], self.C, self.max_prefix,
-                                   self.prefix_len[layer], self.slots, kv1[0], kv1[1], out1, self.parts, self._ws0,
+        vc.vc_verify_attn_streamed(self.pipes[layer], self._shape0, q1, self.host_kv[layer], self.C, self.max_prefix,
+                                   self.prefix_len[layer], self.ring[layer], kv1[0], kv1[1], out1, self.parts, self._ws0,
                                    self._ws0_bytes, compute_stream, copy_stream)
         self.launches += self.chunks() + 1
 
@@ -257,11 +268,11 @@ class Group:
             self.launches += 4                 # commit, commit lengths, append, append lengths
 
     def prefetch_bytes(self):
-        """Bytes prefetch() moves: the first min(n_slots, chunks) chunks of one layer."""
+        """Bytes prefetch_all() moves: the first min(n_slots, chunks) chunks of every layer."""
         total = 0
         for c in range(min(self.n_slots, self.chunks())):
             total += 2 * self.B * self.Hkv * min(self.C, self.max_prefix - c * self.C) * self.d * 2
-        return total
+        return total * self.L
 
     def chunks(self):
         return (self.max_prefix + self.C - 1) // self.C
@@ -299,14 +310,15 @@ class Timeline:
 
 
 def round_single(g: Group, inp: RoundInputs, cs, xs, tl: Timeline | None = None):
-    """One round of one group: the full KV of layer 0 starts streaming while the
-    group drafts (prefix chunks do not depend on the drafts), then verify,
-    accept, commit.  Returns nothing; call g.after_round() after syncing."""
+    """One round of one group: the first chunks of every layer's full KV start
+    streaming while the group drafts (prefix chunks do not depend on the
+    drafts), then verify, accept, commit.  Returns the round's timeline; call
+    g.after_round() after syncing."""
     tl = tl or Timeline()
     tl.mark("start", cs)
     xs.wait_event(tl.ev["start"])
     tl.mark("copy_start", xs)
-    g.prefetch(0, xs)
+    g.prefetch_all(xs)
     tl.mark("prefetch_end", xs)            # the first slots' copies: they never wait for a slot
     tl.mark("draft_start", cs)
     for i in range(inp.k):
@@ -332,7 +344,7 @@ def round_staggered(X: Group, Y: Group, inp_x: RoundInputs, inp_y: RoundInputs, 
     tl.mark("start", cs)
     xs.wait_event(tl.ev["start"])
     tl.mark("copy_start", xs)
-    Y.prefetch(0, xs)
+    Y.prefetch_all(xs)
     tl.mark("draft_start", cs)
     for i in range(inp_x.k):
         for l in range(X.L):
