@@ -383,7 +383,220 @@ __device__ __forceinline__ void group_mma(const uint32_t* kc_g, const uint16_t* 
   }
 }
 
+// ------------------------------------------------------------------ transposed group product (G = 4)
+// With G = 4 the 16 rows of a product above carry only 8 of 16 (hi, lo) query
+// rows.  Here the roles swap: S^T = codes . Q'^T and O^T = V^T . P'^T, with
+// the codes as the A operand (16 tokens or 16 channels per tile) and the
+// 4 heads' hi and lo parts as the 8 columns: 16 QK + 16 PV products per group
+// instead of 32 + 32.  The packed words need no change: the B fragment of
+// n-tile j is the top (b0) / bottom (b1) register pair of an A fragment whose
+// rows are the tokens of n-tiles j and j' (a0 = b0 of j, a1 = b0 of j',
+// a2 = b1 of j, a3 = b1 of j').  The QK accumulator block of tokens 4 gid + j
+// (j = 2 mt + half), transposed in registers (movmatrix), is the PV B fragment
+// of k-step s = j / 2, register r = j % 2.
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Per-warp running state of one segment, transposed: the lane's heads are
+// h0 = 2 (tig & 1) and h0 + 1.
+template <int D>
+struct WarpStateT {
+  static constexpr int MT = D / 16;
+  float o[MT][4];       // O^T: rows = channels 16 mt + gid (+ 8), cols 2 tig (+1) = (lo if tig >= 2) of heads h0 (+1)
+  float oz[4];          // correction: rows = P' columns (gid: lo if >= 4, head gid & 3), cols = (channel group tig, zeros | scales)
+  float l0[2], l1[2];   // per head: sums of the weights of r = 0 / r = 1 tokens (times f_r)
+  float m[2];           // per head: running max (log2 units)
+};
+
+template <int D, int G>
+struct StateOf {
+  using type = WarpState<D>;
+};
+template <int D>
+struct StateOf<D, 4> {
+  using type = WarpStateT<D>;
+};
+
+template <int D>
+__device__ __forceinline__ void init_state(WarpState<D>& st) {
+#pragma unroll
+  for (int nt = 0; nt < D / 8; ++nt) st.o[nt][0] = st.o[nt][1] = st.o[nt][2] = st.o[nt][3] = 0.0f;
+  st.oz[0] = st.oz[1] = st.oz[2] = st.oz[3] = 0.0f;
+  st.l0 = st.l1 = 0.0f;
+  st.m = -INFINITY;
+}
+template <int D>
+__device__ __forceinline__ void init_state(WarpStateT<D>& st) {
+#pragma unroll
+  for (int m = 0; m < D / 16; ++m) st.o[m][0] = st.o[m][1] = st.o[m][2] = st.o[m][3] = 0.0f;
+  st.oz[0] = st.oz[1] = st.oz[2] = st.oz[3] = 0.0f;
+  st.l0[0] = st.l0[1] = st.l1[0] = st.l1[1] = 0.0f;
+  st.m[0] = st.m[1] = -INFINITY;
+}
+
+template <int D, int BITS>
+__device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t* ksz_g, const uint32_t* vc_g,
+                                            const uint16_t* vsz_g, const uint32_t (&qf)[D / 16][2],
+                                            uint32_t bias_mul0, uint32_t bias_mul1,
+                                            uint32_t zcol_mul0, uint32_t zcol_mul1, int zcol_off, float cs,
+                                            WarpStateT<D>& st, int lane) {
+  constexpr int KS = D / 16, NT = D / 8, NCG = D / 32, WPL = D * BITS / 32;
+  const int gid = lane >> 2, tig = lane & 3;
+  const bool lo_q = gid >= 4;                   // Q'^T column gid: the remainder part of head gid & 3
+  const bool lo_p = tig >= 2;                   // P block columns 2 tig (+1): remainder parts
+  const int h0 = 2 * (tig & 1);
+  // ---------------- S^T = codes . Q'^T
+  uint32_t kw[WPL];
+  load_lane_words<WPL>(kc_g, lane, kw);
+  const uint32_t* srow = reinterpret_cast<const uint32_t*>(ksz_g) + (D / 8) * tig;
+  const uint32_t* zrow = reinterpret_cast<const uint32_t*>(ksz_g) + (gid == 0 ? D / 2 : 0) + (D / 8) * tig;
+  float c[2][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) c[mt][0] = c[mt][1] = c[mt][2] = c[mt][3] = 0.0f;
+  float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int kq = 0; kq < KS / 2; ++kq) {
+    const uint4 s4 = *reinterpret_cast<const uint4*>(srow + 4 * kq);
+    const uint4 z4 = *reinterpret_cast<const uint4*>(zrow + 4 * kq);
+    const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
+    const uint32_t zv[4] = {z4.x, z4.y, z4.z, z4.w};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int ks = 2 * kq + h;
+      uint32_t hi0, lo0, hi1, lo1;
+      split_mul(u2h(qf[ks][0]), u2h(sv[2 * h]), hi0, lo0);
+      split_mul(u2h(qf[ks][1]), u2h(sv[2 * h + 1]), hi1, lo1);
+      const uint32_t qb0 = lo_q ? lo0 : hi0, qb1 = lo_q ? lo1 : hi1;
+      mma16816(cb, qf[ks][0], 0u, qf[ks][1], 0u, h2u(__hmul2(u2h(zv[2 * h]), u2h(bias_mul0))),
+               h2u(__hmul2(u2h(zv[2 * h + 1]), u2h(bias_mul1))));
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        fragment<BITS, WPL>(kw, (2 * mt) * KS + ks, a0, a2);
+        fragment<BITS, WPL>(kw, (2 * mt + 1) * KS + ks, a1, a3);
+        mma16816(c[mt], a0, a1, a2, a3, qb0, qb1);
+      }
+    }
+  }
+  // bias of head h: row h of the bias product, columns 0 (q.z) and 1 (-q.f s) in lane 4 h
+  const float cbs = cb[0] + cb[1];
+  const float bias[2] = {__shfl_sync(0xffffffffu, cbs, 4 * h0), __shfl_sync(0xffffffffu, cbs, 4 * h0 + 4)};
+  // hi + lo columns; y[mt][2 half + hh] = score of token 4 gid + 2 mt + half, head h0 + hh
+  float y[2][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) y[mt][e] = c[mt][e] + __shfl_xor_sync(0xffffffffu, c[mt][e], 2);
+  // ---------------- online softmax, one state per head
+  float mx[2];
+  bool need[2];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    float my = fmaxf(fmaxf(y[0][hh], y[0][2 + hh]), fmaxf(y[1][hh], y[1][2 + hh]));
+    my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 4));
+    my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 8));
+    my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 16));
+    mx[hh] = (my + bias[hh]) * cs;
+    need[hh] = !(mx[hh] <= st.m[hh] + kLazy);
+  }
+  if (__any_sync(0xffffffffu, need[0] || need[1])) {
+    float alpha[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float mn = need[hh] ? mx[hh] : st.m[hh];
+      alpha[hh] = fast_exp2(st.m[hh] - mn);     // m = -inf at the start: alpha = 0
+      st.l0[hh] *= alpha[hh];
+      st.l1[hh] *= alpha[hh];
+      st.m[hh] = mn;
+    }
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      st.o[mt][0] *= alpha[0];
+      st.o[mt][1] *= alpha[1];
+      st.o[mt][2] *= alpha[0];
+      st.o[mt][3] *= alpha[1];
+    }
+    // correction rows belong to head gid & 3: its factor sits in lane (gid, (gid & 3) >> 1)
+    const float a_g = (gid & 1) ? alpha[1] : alpha[0];
+    const float a_oz = __shfl_sync(0xffffffffu, a_g, 4 * gid + ((gid & 3) >> 1));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) st.oz[k] *= a_oz;
+  }
+  const float kk[2] = {fmaf(bias[0], cs, -st.m[0]), fmaf(bias[1], cs, -st.m[1])};
+  // weights times f_r (r = token parity = half), split into fp16 (hi, lo); block j = 2 mt + half
+  uint32_t ph[4], pl[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int mt = j >> 1, half = j & 1;
+    const float lf = field_log2<BITS>(half);
+    const float p0 = fast_exp2(fmaf(y[mt][2 * half], cs, kk[0] + lf));
+    const float p1 = fast_exp2(fmaf(y[mt][2 * half + 1], cs, kk[1] + lf));
+    if (half) {
+      st.l1[0] += p0;
+      st.l1[1] += p1;
+    } else {
+      st.l0[0] += p0;
+      st.l0[1] += p1;
+    }
+    const __half2 h = __floats2half2_rn(p0, p1);
+    const float2 hf = __half22float2(h);
+    ph[j] = h2u(h);
+    pl[j] = h2u(__floats2half2_rn(p0 - hf.x, p1 - hf.y));
+  }
+  // ---------------- correction: A = P' blocks transposed (rows = P' columns), B = meta columns
+  {
+    uint32_t pu[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) pu[j] = movmatrix_t(lo_p ? pl[j] : ph[j]);
+    const uint4 r4 = *reinterpret_cast<const uint4*>(vsz_g + zcol_off + 8 * tig);
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const uint32_t b0 = h2u(__hmul2(u2h(s ? r4.z : r4.x), u2h(zcol_mul0)));
+      const uint32_t b1 = h2u(__hmul2(u2h(s ? r4.w : r4.y), u2h(zcol_mul1)));
+      mma16816(st.oz, pu[2 * s], 0u, pu[2 * s + 1], 0u, b0, b1);
+    }
+  }
+  // ---------------- O^T += V^T . P'^T, one P'^T per channel group (the value scales of its tokens)
+  uint32_t vw[WPL];
+  load_lane_words<WPL>(vc_g, lane, vw);
+#pragma unroll
+  for (int g = 0; g < NCG; ++g) {
+    // scales of tokens 4 gid + j: entry 8 (gid >> 1) + 2 j + (gid & 1) of the group's scale row
+    const uint4 s4 = *reinterpret_cast<const uint4*>(vsz_g + g * 64 + 8 * (gid >> 1));
+    const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w};
+    const uint32_t sel = (gid & 1) ? 0x3232u : 0x1010u;
+    uint32_t pb[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t sv2;
+      asm("prmt.b32 %0, %1, %1, %2;" : "=r"(sv2) : "r"(sw[j]), "r"(sel));   // (sv, sv) of token 4 gid + j
+      const __half2 x = u2h(ph[j]), sc = u2h(sv2);
+      const __half2 h = __hmul2(x, sc);
+      const __half2 l = __hfma2(u2h(pl[j]), sc, __hfma2(x, sc, __hneg2(h)));
+      pb[j] = movmatrix_t(h2u(lo_p ? l : h));
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int m = 2 * g + u;                  // channels 16 m .. 16 m + 15 = n-tiles 2 m, 2 m + 1
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        uint32_t a0, a1, a2, a3;
+        fragment<BITS, WPL>(vw, s * NT + 2 * m, a0, a2);
+        fragment<BITS, WPL>(vw, s * NT + 2 * m + 1, a1, a3);
+        mma16816(st.o[m], a0, a1, a2, a3, pb[2 * s], pb[2 * s + 1]);
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ merge / arrive / combine
+template <int D, int BITS, int G>
+__device__ void merge_partials(const DraftArgs& a, uint8_t* smem, int bh, int slot);
+
 // Partial of this CTA for slice bh: merge the warps' (max, sum, output) in
 // shared memory and write one normalised partial + log2-sum-exp per head.
 template <int D, int BITS, int G>
@@ -416,6 +629,17 @@ __device__ void write_partial(const DraftArgs& a, uint8_t* smem, int bh, int slo
     }
   }
   vc_bar_sync(1, kConsumers);
+  merge_partials<D, BITS, G>(a, smem, bh, slot);
+}
+
+// The warps' (max, sum, output) of slice bh, left in `red` / `wstat` by the
+// consumer warps (after a consumer barrier), merged into one normalised
+// partial + log2-sum-exp per head.
+template <int D, int BITS, int G>
+__device__ void merge_partials(const DraftArgs& a, uint8_t* smem, int bh, int slot) {
+  using P = Plan<D, BITS, G>;
+  const float* red = reinterpret_cast<const float*>(smem + P::off_red);
+  const float* wstat = reinterpret_cast<const float*>(smem + P::off_wstat);
   const int b = bh / a.Hkv, kvh = bh % a.Hkv;
   for (int i = threadIdx.x; i < G * D; i += kConsumers) {
     const int h = i / D, c = i % D;
@@ -439,6 +663,62 @@ __device__ void write_partial(const DraftArgs& a, uint8_t* smem, int bh, int slo
     a.part_o[row * D + c] = o / Ls;
     if (c == 0) a.part_lse[row] = M + log2f(Ls);
   }
+}
+
+// write_partial for the transposed state: per head the hi + lo columns, the
+// correction of each channel group, the softmax sum over the warp's tokens.
+template <int D, int BITS, int G>
+__device__ void write_partial_t(const DraftArgs& a, uint8_t* smem, int bh, int slot, WarpStateT<D>& st) {
+  using P = Plan<D, BITS, G>;
+  static_assert(G == 4, "the transposed product carries 4 heads");
+  constexpr int MT = D / 16, NCG = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int h0 = 2 * (tig & 1);
+  float* red = reinterpret_cast<float*>(smem + P::off_red);             // [warp][G][D]
+  float* wstat = reinterpret_cast<float*>(smem + P::off_wstat);         // [warp][8][2]
+  // correction of (head gid & 3, channel group tig): hi row gid + lo row gid ^ 4
+  float cz = st.oz[0] + st.oz[1] + st.oz[2] + st.oz[3];
+  cz += __shfl_xor_sync(0xffffffffu, cz, 16);
+  float corr[2][NCG];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+    for (int g = 0; g < NCG; ++g) corr[hh][g] = __shfl_sync(0xffffffffu, cz, 4 * (h0 + hh) + g);
+  float l[2];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    float x = st.l0[hh] * (1.0f / field_scale<BITS>(0)) + st.l1[hh] * (1.0f / field_scale<BITS>(1));
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    x += __shfl_xor_sync(0xffffffffu, x, 8);
+    x += __shfl_xor_sync(0xffffffffu, x, 16);
+    l[hh] = x;
+  }
+  float v[MT][4];
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[m][e] = st.o[m][e] + __shfl_xor_sync(0xffffffffu, st.o[m][e], 2);
+  if (tig < 2) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      const int c0 = 16 * m + gid, g = m / 2;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        red[(warp * G + h0 + hh) * D + c0] = v[m][hh] + corr[hh][g];
+        red[(warp * G + h0 + hh) * D + c0 + 8] = v[m][2 + hh] + corr[hh][g];
+      }
+    }
+    if (gid == 0) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        wstat[(warp * 8 + h0 + hh) * 2] = st.m[hh];
+        wstat[(warp * 8 + h0 + hh) * 2 + 1] = l[hh];
+      }
+    }
+  }
+  vc_bar_sync(1, kConsumers);
+  merge_partials<D, BITS, G>(a, smem, bh, slot);
 }
 
 // Count this CTA's partial for slice bh; the last of the n_parts arrivals
@@ -532,7 +812,7 @@ __device__ void produce(const DraftArgs& a, uint8_t* smem, int c, uint64_t* full
 template <int D, int BITS, int G>
 __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
   using P = Plan<D, BITS, G>;
-  constexpr int NS = P::NS, KS = D / 16, NT = D / 8, NCG = D / 32;
+  constexpr int NS = P::NS, KS = D / 16, NCG = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + P::off_bar);
@@ -574,10 +854,13 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
     int first, last;
     ctas_of(sg.bh, a, first, last);
     // query fragments of head gid, times f_r: channels (D/4) tig + 4ks + 2r + {0, 1}
+    // (the transposed product, G = 4: lanes gid and gid + 4 both hold head gid & 3)
     uint32_t qf[KS][2];
     {
-      const uint16_t* qrow = a.q + (static_cast<size_t>(b) * a.Hq + kvh * G + (gid < G ? gid : 0)) * D + (D / 4) * tig;
-      const float on = gid < G ? 1.0f : 0.0f;
+      constexpr bool kT = G == 4;
+      const int head = kT ? (gid & 3) : (gid < G ? gid : 0);
+      const uint16_t* qrow = a.q + (static_cast<size_t>(b) * a.Hq + kvh * G + head) * D + (D / 4) * tig;
+      const float on = (kT || gid < G) ? 1.0f : 0.0f;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const uint2 raw = *reinterpret_cast<const uint2*>(qrow + 4 * ks);
@@ -587,12 +870,8 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
         qf[ks][1] = h2u(__floats2half2_rn(q2 * on * f1, q3 * on * f1));
       }
     }
-    WarpState<D> st;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) st.o[nt][0] = st.o[nt][1] = st.o[nt][2] = st.o[nt][3] = 0.0f;
-    st.oz[0] = st.oz[1] = st.oz[2] = st.oz[3] = 0.0f;
-    st.l0 = st.l1 = 0.0f;
-    st.m = -INFINITY;
+    typename StateOf<D, G>::type st;
+    init_state(st);
     for (int s = 0; s < sg.n_st; ++s) {
       const bool ok = __all_sync(0xffffffffu, vc_mbar_wait_or_abort(full + buf, phase, abort, kWaitCycles));
       if (ok && s * kWarps + warp < sg.n_valid) {
@@ -601,8 +880,12 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
         const uint16_t* ksz_g = reinterpret_cast<const uint16_t*>(base + P::kc + warp * P::meta);
         const uint32_t* vc_g = reinterpret_cast<const uint32_t*>(base + P::kc + P::mt + warp * P::codes);
         const uint16_t* vsz_g = reinterpret_cast<const uint16_t*>(base + 2 * P::kc + P::mt + warp * P::meta);
-        group_mma<D, BITS>(kc_g, ksz_g, vc_g, vsz_g, qf, bias_mul0, bias_mul1, zcol_mul0, zcol_mul1, zcol_off,
-                           a.scale_log2, st, lane);
+        if constexpr (G == 4)
+          group_mma_t<D, BITS>(kc_g, ksz_g, vc_g, vsz_g, qf, bias_mul0, bias_mul1, zcol_mul0, zcol_mul1, zcol_off,
+                               a.scale_log2, st, lane);
+        else
+          group_mma<D, BITS>(kc_g, ksz_g, vc_g, vsz_g, qf, bias_mul0, bias_mul1, zcol_mul0, zcol_mul1, zcol_off,
+                             a.scale_log2, st, lane);
       }
       __syncwarp();
       if (lane == 0) vc_mbar_arrive(empty + buf);          // this warp is done with the stage
@@ -616,7 +899,10 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
       if (threadIdx.x == 0) atomicOr(&g_draft_status, VC_DEV_BARRIER_TIMEOUT);
       return;                                               // outputs of this call are invalid
     }
-    write_partial<D, BITS, G>(a, smem, sg.bh, c - first, st);
+    if constexpr (G == 4)
+      write_partial_t<D, BITS, G>(a, smem, sg.bh, c - first, st);
+    else
+      write_partial<D, BITS, G>(a, smem, sg.bh, c - first, st);
     arrive_and_combine<G, D>(a, flag, sg.bh, last - first + 2, kConsumers);
     vc_bar_sync(1, kConsumers);                             // red / flag reused by the next segment
   }
