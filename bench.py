@@ -205,7 +205,13 @@ def algorithmic_draft_bytes(w, P):
 
 
 def source_hash(path):
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    """Hash of a kernel source's code: comments and whitespace removed, so edits to
+    the comments keep a capture valid and any change to the code does not."""
+    import re
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256("".join(text.split()).encode()).hexdigest()[:16]
 
 
 def ncu_traffic(kernel_file, workload):

@@ -15,7 +15,7 @@
 //   * a segment is streamed through a ring of shared-memory stages (11 groups
 //     of 32 tokens each: K codes, K scale/zero, V codes, V scale/zero), filled
 //     by bulk async copies (cp.async.bulk + mbarrier transaction counts, bounded
-//     waits) while the 8 warps compute on earlier stages;
+//     waits) while the 11 consumer warps compute on earlier stages;
 //   * each warp owns one group per stage and keeps its own online-softmax
 //     state (max, sums) and output accumulators, all G heads of the KV head as
 //     rows of 16x8x16 tensor-core products: the packed codes become operand
@@ -23,7 +23,9 @@
 //     in fp16), the key scales fold into the query and the value scales into
 //     the softmax weights, each fold carried as an fp16 (hi, lo) pair so the
 //     products keep ~22 bits, and the zero points enter through two narrow
-//     correction products (group_mma below);
+//     correction products (group_mma below); with G = 4 the roles swap
+//     (codes as the A operand, the heads' (hi, lo) parts as the 8 columns,
+//     group_mma_t), which halves the QK and PV products;
 //   * at the end of a segment the warps are merged (log-sum-exp) into one
 //     partial per query head; the last CTA to finish a (request, KV head)
 //     (arrival counter in the workspace, reset by that CTA) merges all its
