@@ -57,6 +57,10 @@ CASES = [
     ("g2_d128_b4", dict(B=1, Hq=4, Hkv=2, d=128, bits=4, T=256), [256], [0], 0, True),
     ("mistral_int8", dict(B=2, T=1024, bits=8), [1024, 480], [3, 0], 1, True),
     ("g8_d64_b8", dict(B=1, Hq=8, Hkv=1, d=64, bits=8, T=320), [320], [5], 0, True),
+    # G = 4 takes the transposed group product: every code width and head dim
+    ("g4_d128_b4", dict(B=2, Hq=8, Hkv=2, d=128, bits=4, T=768), [768, 352], [2, 0], 1, True),
+    ("g4_d64_b2", dict(B=1, Hq=4, Hkv=1, d=64, bits=2, T=512), [512], [7], 0, True),
+    ("g4_d64_b8", dict(B=2, Hq=8, Hkv=2, d=64, bits=8, T=384), [384, 64], [0, 3], 2, True),
 ]
 
 
