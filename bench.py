@@ -136,6 +136,34 @@ def make_round_inputs(w, rnd, group, device, layers):
     return host
 
 
+def round_drafts(w, host_inputs, n_rounds, group):
+    """Draft tokens int32 [B, k] of rounds 0 .. n_rounds - 1 of one group, over the
+    logits of input slot r % n_inp: the slot's row argmaxes (lowest index) below the
+    round's accepted length L, drawn from the workload's distribution
+    (synth.accept_lengths(w, r)), and a mismatch from L on.  A few input slots then
+    still give the distribution's mean accepted length; the accept kernel finds n = L
+    from the logits."""
+    import numpy as np
+    import torch
+
+    import synth
+    amax = [hi.logits.numpy().argmax(-1).astype(np.int64) for hi in host_inputs]     # [B, k+1] per slot
+    out = []
+    for r in range(n_rounds):
+        A = amax[r % len(amax)]
+        L = synth.accept_lengths(w, r, group)
+        d = ((A[:, :w.k] + 1) % w.V).astype(np.int32)          # mismatches everywhere ...
+        for b in range(w.B):
+            d[b, :int(L[b])] = A[b, :int(L[b])]                # ... except below L
+        out.append(torch.from_numpy(d))
+    return out
+
+
+def with_drafts(inp, drafts):
+    import dataclasses
+    return dataclasses.replace(inp, drafts=drafts)
+
+
 def to_device(inp, device, pinned=False):
     from verify_compressed_kv_gb300.runtime import RoundInputs
     f = (lambda x: x.pin_memory()) if pinned else (lambda x: x.to(device))
@@ -414,6 +442,11 @@ def run_ours(args, rank, world, local_rank):
     pin_inputs = [[to_device(x, device, pinned=True) for x in hi] for hi in host_inputs]
     # device buffers the e2e leg copies into every round
     e2e_bufs = [to_device(hi[0], device) for hi in host_inputs]
+    # per-round draft tokens (accepted lengths drawn per round, see round_drafts)
+    n_draft_rounds = args.warmup + 2 * args.steps + 8
+    host_drafts = [round_drafts(w, host_inputs[gi], n_draft_rounds, gi) for gi in range(n_groups)]
+    dev_drafts = [[x.to(device) for x in hd] for hd in host_drafts]
+    pin_drafts = [[x.pin_memory() for x in hd] for hd in host_drafts]
     torch.cuda.synchronize()
 
     link_best = measure_link_gbs(device, xs)
@@ -429,18 +462,18 @@ def run_ours(args, rank, world, local_rank):
         state["round"] += 1
         if n_groups == 1:
             g = groups[0]
-            inp = dev_inputs[0][r % n_inp]
+            inp = with_drafts(dev_inputs[0][r % n_inp], dev_drafts[0][r])
             if e2e:
-                copy_inputs(e2e_bufs[0], pin_inputs[0][r % n_inp], cs)
+                copy_inputs(e2e_bufs[0], with_drafts(pin_inputs[0][r % n_inp], pin_drafts[0][r]), cs)
                 inp = e2e_bufs[0]
             tl = rt.round_single(g, inp, cs, xs, timeline)
             return tl, [g]
         if args.schedule == "lockstep":
             # every group drafts cycle r, then every group verifies it
-            inps = [dev_inputs[gi][r % n_inp] for gi in range(2)]
+            inps = [with_drafts(dev_inputs[gi][r % n_inp], dev_drafts[gi][r]) for gi in range(2)]
             if e2e:
                 for gi in range(2):
-                    copy_inputs(e2e_bufs[gi], pin_inputs[gi][r % n_inp], cs)
+                    copy_inputs(e2e_bufs[gi], with_drafts(pin_inputs[gi][r % n_inp], pin_drafts[gi][r]), cs)
                 inps = e2e_bufs
             tl = rt.round_lockstep(groups, inps, cs, xs, timeline)
             return tl, list(groups)
@@ -449,7 +482,7 @@ def run_ours(args, rank, world, local_rank):
         ix, iy = r % 2, (r + 1) % 2
         X, Y = groups[ix], groups[iy]
         dc, vcyc = r // 2, (r - 1) // 2
-        inp_x = dev_inputs[ix][dc % n_inp]
+        inp_x = with_drafts(dev_inputs[ix][dc % n_inp], dev_drafts[ix][dc])
         if r == 0:
             tl = rt.Timeline()
             tl.mark("start", cs)
@@ -458,10 +491,10 @@ def run_ours(args, rank, world, local_rank):
                     X.draft_step(inp_x, l, i, cs)
             tl.mark("end", cs)
             return tl, []
-        inp_y = dev_inputs[iy][vcyc % n_inp]
+        inp_y = with_drafts(dev_inputs[iy][vcyc % n_inp], dev_drafts[iy][vcyc])
         if e2e:
-            copy_inputs(e2e_bufs[ix], pin_inputs[ix][dc % n_inp], cs)
-            copy_inputs(e2e_bufs[iy], pin_inputs[iy][vcyc % n_inp], cs)
+            copy_inputs(e2e_bufs[ix], with_drafts(pin_inputs[ix][dc % n_inp], pin_drafts[ix][dc]), cs)
+            copy_inputs(e2e_bufs[iy], with_drafts(pin_inputs[iy][vcyc % n_inp], pin_drafts[iy][vcyc]), cs)
             inp_x, inp_y = e2e_bufs[ix], e2e_bufs[iy]
         tl = rt.round_staggered(X, Y, inp_x, inp_y, cs, xs, timeline)
         return tl, [Y]
