@@ -690,9 +690,14 @@ def run_ours(args, rank, world, local_rank):
 
 
 def workload_of(args):
-    """The workload, with --bits overriding its code width."""
+    """The workload, with --bits / --k overriding its code width / draft length."""
     import synth
-    return synth.get(args.workload, **({"bits": args.bits} if args.bits else {}))
+    ov = {}
+    if args.bits:
+        ov["bits"] = args.bits
+    if getattr(args, "k", 0):
+        ov["k"] = args.k
+    return synth.get(args.workload, **ov)
 
 
 def workload_name(w):
@@ -705,6 +710,9 @@ def workload_name(w):
     own = {"tiny": 4, "mistral": 2, "qwen": 4, "llama": 2, "stagger": 2}.get(w.name)
     if own is not None and w.bits != own:
         name = name.replace(f"int{own}", f"int{w.bits}")
+    own_k = {"tiny": 4, "mistral": 16, "qwen": 32, "llama": 32, "stagger": 24}.get(w.name)
+    if own_k is not None and w.k != own_k:
+        name = name.replace(f" k{own_k} ", f" k{w.k} ")
     return name
 
 
@@ -834,8 +842,12 @@ def run_adaptive(args, local_rank):
     rounds_total = args.warmup + 2 * args.steps + 4
     g = build_group(dataclasses.replace(w, k=k_max), w.layers, device, rounds_total, args.slots or None)
     n_inp = 3
-    inputs = {k: [to_device(make_round_inputs(dataclasses.replace(w, k=k), r, 0, device, w.layers), device)
-                  for r in range(n_inp)] for k in choices}
+    host_in = {k: [make_round_inputs(dataclasses.replace(w, k=k), r, 0, device, w.layers) for r in range(n_inp)]
+               for k in choices}
+    inputs = {k: [to_device(x, device) for x in host_in[k]] for k in choices}
+    n_rounds = rounds_total + 8
+    drafts = {k: [x.to(device) for x in round_drafts(dataclasses.replace(w, k=k), host_in[k], n_rounds, 0)]
+              for k in choices}
     cs, xs = torch.cuda.Stream(), torch.cuda.Stream()
     ctl = DraftLengthController(k_max=k_max, k_min=choices[0], choices=tuple(choices))
 
@@ -860,32 +872,41 @@ def run_adaptive(args, local_rank):
         e1.synchronize()
         return e0.elapsed_time(e1) / reps
     k_lo, k_hi = choices[0], choices[-1]
-    row_chunk_ms = max(0.0, (chunk_ms(k_hi) - chunk_ms(k_lo)) / (k_hi - k_lo))
+    # the chunk kernel timed at every candidate k: its cost steps with the launch
+    # geometry (rows per KV head decide warps per CTA and CTAs per SM), so a slope
+    # between two k would misjudge the rest
+    chunk_of_k = {k: chunk_ms(k) for k in choices}
+    row_chunk_ms = max(0.0, (chunk_of_k[k_hi] - chunk_of_k[k_lo]) / (k_hi - k_lo))
     rate = {"bytes_per_ms": link_gbs * 1e6}
 
     def one(k, r):
         h2d_bytes = g.h2d_bytes()
         pf_bytes = g.prefetch_bytes()
-        tl = rt.round_single(g, inputs[k][r % n_inp], cs, xs)
+        tl = rt.round_single(g, with_drafts(inputs[k][r % n_inp], drafts[k][r % n_rounds]), cs, xs)
         tl.ev["end"].synchronize()
         toks = g.after_round()
         d_ms, r_ms = tl.ms("draft_start", "draft_end"), tl.ms("start", "end")
         v_end = tl.ms("start", "verify_end")
         t_tail = max(0.0, r_ms - v_end)
-        # the transfer alone, at the rate of this round's first slot copies (they
-        # never wait for a slot; the whole span stretches when slots wait for the verify)
+        # the transfer alone, at the best rate the prefetched copies have reached (they
+        # never wait for a slot): the link's capacity, which an occasional stall of the
+        # shared host link must not move (a stalled round would make every later plan
+        # hide longer drafting behind a transfer that is not really that long)
         pf_ms = tl.ms("copy_start", "prefetch_end")
         if pf_ms > 0 and pf_bytes > 0:
-            rate["bytes_per_ms"] = pf_bytes / pf_ms
+            rate["bytes_per_ms"] = max(rate["bytes_per_ms"], pf_bytes / pf_ms)
         t_copy = h2d_bytes / rate["bytes_per_ms"]
-        # verify compute of k + 1 rows over every chunk of every layer (calibrated slope)
+        # verify compute of k + 1 rows over every chunk of every layer (calibrated slope),
+        # and the measured table for every candidate k
         t_verify = (k + 1) * row_chunk_ms * g.chunks() * g.L
         ctl.observe(g.n_acc_host.numpy(), k, t_step=d_ms / k, t_copy=t_copy, t_tail=t_tail, t_verify=t_verify)
+        ctl.t_verify = {kk: v * g.chunks() * g.L for kk, v in chunk_of_k.items()}
         return toks, r_ms
 
     for r in range(args.warmup):
         one(w.k, r)
     res = {"fixed": [0, 0.0], "adaptive": [0, 0.0]}
+    per_round = {"fixed": [], "adaptive": []}            # (tokens, ms) of every round
     chosen = {}
     r = args.warmup
     for blk in range(2 * args.steps // 10):                 # blocks of 10 rounds, alternating
@@ -897,15 +918,24 @@ def run_adaptive(args, local_rank):
             toks, ms = one(k, r)
             res[mode][0] += toks * w.layers
             res[mode][1] += ms
+            per_round[mode].append((toks * w.layers, ms))
             r += 1
     g.close()
     val = {m: v[0] / (v[1] / 1e3) for m, v in res.items()}
+    # the same with each mode's median round time (insensitive to the host link's
+    # occasional stalls, which land in either mode's blocks at random)
+    import statistics
+    val_med = {m: statistics.mean(t for t, _ in v) / (statistics.median(ms for _, ms in v) / 1e3)
+               for m, v in per_round.items() if v}
     return {"metric": "verified tokens/s/layer", "value": val["adaptive"], "unit": "tokens/s/layer",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
             "dtype": "bf16/int%d->f32" % w.bits, "data": "synthetic (seeded)",
             "config": {"workload": workload_name(w), "schedule": "adaptive draft length", "k_fixed": w.k,
                        "k_max": k_max, "choices": choices},
             "fixed_k_value": val["fixed"], "adaptive_over_fixed": val["adaptive"] / val["fixed"],
+            "at_median_round": {"fixed": val_med.get("fixed"), "adaptive": val_med.get("adaptive"),
+                                "adaptive_over_fixed": (val_med["adaptive"] / val_med["fixed"])
+                                if "fixed" in val_med and "adaptive" in val_med else None},
             "k_chosen": chosen, "acceptance_estimate": ctl.acceptance(),
             "measured": {"t_step_ms": ctl.t_step, "t_copy_ms": ctl.t_copy, "t_tail_ms": ctl.t_tail,
                          "t_verify_row_ms": ctl.t_row, "link_peak_gbs": link_gbs,
@@ -938,7 +968,9 @@ def run_remote(args, local_rank):
         g.packed_len[l].zero_()
     comp_bytes = sum(h.numel() * h.element_size() for hs in host for h in hs)
     full_bytes = g.h2d_bytes()
-    inputs = [to_device(make_round_inputs(w, r, 0, device, w.layers), device) for r in range(3)]
+    host_in = [make_round_inputs(w, r, 0, device, w.layers) for r in range(3)]
+    inputs = [to_device(x, device) for x in host_in]
+    drafts = [x.to(device) for x in round_drafts(w, host_in, rounds + 2, 0)]
     cs, xs = torch.cuda.Stream(), torch.cuda.Stream()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -947,13 +979,13 @@ def run_remote(args, local_rank):
     xs.synchronize()
     stage_ms = (time.perf_counter() - t0) * 1e3
     t1 = time.perf_counter()
-    tl = rt.round_single(g, inputs[0], cs, xs)
+    tl = rt.round_single(g, with_drafts(inputs[0], drafts[0]), cs, xs)
     tl.ev["end"].synchronize()
     first_round_ms = (time.perf_counter() - t1) * 1e3
     first_tokens = g.after_round() * w.layers
     ms, toks = [], 0
     for r in range(1, rounds):
-        tl = rt.round_single(g, inputs[r % 3], cs, xs)
+        tl = rt.round_single(g, with_drafts(inputs[r % 3], drafts[r]), cs, xs)
         tl.ev["end"].synchronize()
         t = g.after_round()
         if r >= args.warmup:
@@ -970,7 +1002,8 @@ def run_remote(args, local_rank):
             "stage_ms": stage_ms, "stage_ms_at_rate": comp_bytes / (rate * 1e6), "first_round_ms": first_round_ms,
             "first_round_tokens": first_tokens, "full_prefix_over_slow_link_ms": full_ms,
             "speedup_vs_full_prefix": (full_ms + first_round_ms) / ttfr,
-            "steady_value": toks / (sum(ms) / 1e3) if ms else None, "steady_unit": "tokens/s/layer"}
+            "steady_value": toks / (sum(ms) / 1e3) if ms else None, "steady_unit": "tokens/s/layer",
+            "steady_round_ms": [round(x, 3) for x in ms]}
 
 
 def dist_setup():
@@ -1033,6 +1066,7 @@ def main(argv=None):
     ap.add_argument("--remote-prefix", type=float, default=0.0, metavar="GBS",
                     help="emulate remote prefix caching: the packed prefix arrives over a link paced at GBS GB/s")
     ap.add_argument("--k-max", type=int, default=60, help="largest draft length of --adaptive (accept takes k + 1 <= 64)")
+    ap.add_argument("--k", type=int, default=0, help="draft length instead of the workload's own (0: keep it)")
     ap.add_argument("--rows-only", action="store_true",
                     help="time only the prefill rows (pack, token score / select / gather) of one layer")
     args = ap.parse_args(argv)

@@ -85,3 +85,27 @@ def test_verify_rows_cost_bounds_the_draft_length():
     c = DraftLengthController(k_max=60, k_min=4, choices=tuple(range(4, 61, 4)))
     c.observe([5] * 8, 48, t_step=0.107, t_copy=5.2, t_tail=0.5, t_verify=49 * 0.05)
     assert c.t_row == pytest.approx(0.05) and c.next_k() == k_rows
+
+
+def test_measured_verify_table_overrides_the_linear_row_term():
+    """A verify cost that steps up at large k (the chunk kernel's launch geometry
+    changes) must steer the choice away from those k, where the linear per-row
+    term would not."""
+    from verify_compressed_kv_gb300.schedule import best_k
+    a, t_step, t_copy, t_tail, t_row = 0.96, 1.4, 82.0, 0.25, 0.69
+    linear = best_k(a, t_step, t_copy, t_tail, 4, 60, choices=range(4, 61, 4), t_row=t_row)
+    table = {k: (k + 1) * t_row * (1.0 if k <= 32 else 1.8) for k in range(4, 61, 4)}
+    stepped = best_k(a, t_step, t_copy, t_tail, 4, 60, choices=range(4, 61, 4), t_row=t_row, t_verify=table)
+    assert linear > 32 and stepped <= 32
+    # a table equal to the linear term changes nothing
+    same = {k: (k + 1) * t_row for k in range(4, 61, 4)}
+    assert best_k(a, t_step, t_copy, t_tail, 4, 60, choices=range(4, 61, 4), t_row=t_row, t_verify=same) == linear
+
+
+def test_controller_passes_its_verify_table():
+    from verify_compressed_kv_gb300.schedule import DraftLengthController
+    c = DraftLengthController(k_max=60, k_min=4, choices=tuple(range(4, 61, 4)))
+    c.observe([30, 31, 28, 29], 32, t_step=1.4, t_copy=82.0, t_tail=0.25, t_verify=32 * 0.69)
+    free = c.next_k()
+    c.t_verify = {k: (k + 1) * 0.69 * (1.0 if k <= 32 else 1.8) for k in range(4, 61, 4)}
+    assert c.next_k() <= 32 < free

@@ -43,13 +43,19 @@ def round_time(k: int, t_step: float, t_copy: float, t_tail: float, t_row: float
 
 
 def best_k(a: float, t_step: float, t_copy: float, t_tail: float, k_min: int, k_max: int,
-           choices=None, t_row: float = 0.0) -> int:
+           choices=None, t_row: float = 0.0, t_verify=None) -> int:
     """The draft length in [k_min, k_max] (or among `choices`) with the most
-    tokens per second (the smallest such k on ties: fewer draft launches)."""
+    tokens per second (the smallest such k on ties: fewer draft launches).
+    t_verify: optional mapping k -> verify compute time of a round drafting k
+    tokens; where it has k, it replaces the linear (k + 1) * t_row."""
     ks = sorted(choices) if choices is not None else range(k_min, k_max + 1)
     best, best_rate = ks[0], -1.0
     for k in ks:
-        rate = (expected_accepted(a, k) + 1.0) / round_time(k, t_step, t_copy, t_tail, t_row)
+        if t_verify is not None and k in t_verify:
+            t = max(k * t_step + t_verify[k], t_copy) + t_tail
+        else:
+            t = round_time(k, t_step, t_copy, t_tail, t_row)
+        rate = (expected_accepted(a, k) + 1.0) / t
         if rate > best_rate * (1.0 + 1e-12):
             best, best_rate = k, rate
     return best
@@ -74,6 +80,7 @@ class DraftLengthController:
     t_tail: float | None = None
     t_row: float | None = None       # verify compute per row, learned from rounds it was not hidden in
     choices: tuple | None = None     # allowed draft lengths (default: every k in [k_min, k_max])
+    t_verify: dict | None = None     # optional k -> verify compute of a round (measured); overrides t_row
 
     def __post_init__(self):
         if not (1 <= self.k_min <= self.k_max):
@@ -112,4 +119,4 @@ class DraftLengthController:
         if self.t_step is None or self.t_copy is None:
             return self.k_max
         return best_k(self.acceptance(), self.t_step, self.t_copy, self.t_tail or 0.0, self.k_min, self.k_max,
-                      self.choices, self.t_row or 0.0)
+                      self.choices, self.t_row or 0.0, self.t_verify)
