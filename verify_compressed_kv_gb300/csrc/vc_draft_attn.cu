@@ -1032,8 +1032,8 @@ vc_status_t check(const vc_shape_t* s) {
   return VC_OK;
 }
 
-// One CTA of 256 threads per SM: the warps keep the whole per-head output
-// (D/8 accumulator tiles) and the query fragments in registers.
+// One CTA of kThreads (11 consumer warps + the producer) per SM: the warps keep
+// the output accumulators and the query fragments in registers.
 template <int G>
 struct MinBlocks {
   static constexpr int value = 1;
