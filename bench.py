@@ -170,16 +170,20 @@ def to_device(inp, device, pinned=False):
     return RoundInputs(*[f(getattr(inp, n)) for n in ("q_draft", "kv_cur", "q_verify", "kv_new", "logits", "drafts")])
 
 
-def copy_inputs(dst, src, stream):
+ALL_FIELDS = ("q_draft", "kv_cur", "q_verify", "kv_new", "logits", "drafts")
+DRAFT_FIELDS = ("q_draft", "kv_cur", "drafts")                  # what a drafting round reads
+VERIFY_FIELDS = ("q_verify", "kv_new", "logits", "drafts")      # what verify, accept and commit read
+
+
+def copy_inputs(dst, src, stream, fields=ALL_FIELDS):
     import torch
     with torch.cuda.stream(stream):
-        for n in ("q_draft", "kv_cur", "q_verify", "kv_new", "logits", "drafts"):
+        for n in fields:
             getattr(dst, n).copy_(getattr(src, n), non_blocking=True)
 
 
-def input_bytes(inp):
-    return sum(getattr(inp, n).numel() * getattr(inp, n).element_size()
-               for n in ("q_draft", "kv_cur", "q_verify", "kv_new", "logits", "drafts"))
+def input_bytes(inp, fields=ALL_FIELDS):
+    return sum(getattr(inp, n).numel() * getattr(inp, n).element_size() for n in fields)
 
 
 def build_group(w, layers, device, rounds_total, n_slots, group_index=0):
@@ -436,6 +440,7 @@ def run_ours(args, rank, world, local_rank):
     n_slots = args.slots or None
     cs = torch.cuda.Stream(device)
     xs = torch.cuda.Stream(device)
+    ins = torch.cuda.Stream(device)           # the e2e leg's per-round input copies
     groups = [build_group(w, layers, device, rounds_total, n_slots, gi) for gi in range(n_groups)]
     host_inputs = [[make_round_inputs(w, r, gi, device, layers) for r in range(n_inp)] for gi in range(n_groups)]
     dev_inputs = [[to_device(x, device) for x in hi] for hi in host_inputs]
@@ -463,10 +468,16 @@ def run_ours(args, rank, world, local_rank):
         if n_groups == 1:
             g = groups[0]
             inp = with_drafts(dev_inputs[0][r % n_inp], dev_drafts[0][r])
+            ready = None
             if e2e:
-                copy_inputs(e2e_bufs[0], with_drafts(pin_inputs[0][r % n_inp], pin_drafts[0][r]), cs)
+                # the round's inputs come over the link on their own stream; only the
+                # drafting waits for them, not the round's full-KV transfer
+                ins.wait_stream(cs)
+                copy_inputs(e2e_bufs[0], with_drafts(pin_inputs[0][r % n_inp], pin_drafts[0][r]), ins)
+                ready = torch.cuda.Event()
+                ready.record(ins)
                 inp = e2e_bufs[0]
-            tl = rt.round_single(g, inp, cs, xs, timeline)
+            tl = rt.round_single(g, inp, cs, xs, timeline, ready=ready)
             return tl, [g]
         if args.schedule == "lockstep":
             # every group drafts cycle r, then every group verifies it
@@ -492,11 +503,17 @@ def run_ours(args, rank, world, local_rank):
             tl.mark("end", cs)
             return tl, []
         inp_y = with_drafts(dev_inputs[iy][vcyc % n_inp], dev_drafts[iy][vcyc])
+        ready = None
         if e2e:
-            copy_inputs(e2e_bufs[ix], with_drafts(pin_inputs[ix][dc % n_inp], pin_drafts[ix][dc]), cs)
-            copy_inputs(e2e_bufs[iy], with_drafts(pin_inputs[iy][vcyc % n_inp], pin_drafts[iy][vcyc]), cs)
+            ins.wait_stream(cs)
+            # each group copies what its role in this round reads
+            copy_inputs(e2e_bufs[ix], with_drafts(pin_inputs[ix][dc % n_inp], pin_drafts[ix][dc]), ins, DRAFT_FIELDS)
+            copy_inputs(e2e_bufs[iy], with_drafts(pin_inputs[iy][vcyc % n_inp], pin_drafts[iy][vcyc]), ins,
+                        VERIFY_FIELDS)
+            ready = torch.cuda.Event()
+            ready.record(ins)
             inp_x, inp_y = e2e_bufs[ix], e2e_bufs[iy]
-        tl = rt.round_staggered(X, Y, inp_x, inp_y, cs, xs, timeline)
+        tl = rt.round_staggered(X, Y, inp_x, inp_y, cs, xs, timeline, ready=ready)
         return tl, [Y]
 
     def finish(tl, done):
@@ -631,7 +648,10 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = s0.elapsed_time(s1)
     e2e_local = e2e_tokens * layers / (e2e_ms / 1e3)
-    per_round_in = input_bytes(pin_inputs[0][0]) * (2 if n_groups > 1 else 1)
+    if n_groups == 1 or args.schedule == "lockstep":
+        per_round_in = input_bytes(pin_inputs[0][0]) * n_groups
+    else:                                       # staggered: one group's draft inputs, the other's verify inputs
+        per_round_in = input_bytes(pin_inputs[0][0], DRAFT_FIELDS) + input_bytes(pin_inputs[0][0], VERIFY_FIELDS)
     per_round_out = 4 * w.B
 
     # ---- reduce over ranks (replicas): value = sum, time = max

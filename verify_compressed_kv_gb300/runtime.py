@@ -309,17 +309,21 @@ class Timeline:
         return self.ev[a].elapsed_time(self.ev[b])
 
 
-def round_single(g: Group, inp: RoundInputs, cs, xs, tl: Timeline | None = None):
+def round_single(g: Group, inp: RoundInputs, cs, xs, tl: Timeline | None = None, ready=None):
     """One round of one group: the first chunks of every layer's full KV start
     streaming while the group drafts (prefix chunks do not depend on the
-    drafts), then verify, accept, commit.  Returns the round's timeline; call
-    g.after_round() after syncing."""
+    drafts), then verify, accept, commit.  `ready`: an event the round's inputs
+    wait for (e.g. their copy from host memory on another stream); the full-KV
+    stream does not.  Returns the round's timeline; call g.after_round() after
+    syncing."""
     tl = tl or Timeline()
     tl.mark("start", cs)
     xs.wait_event(tl.ev["start"])
     tl.mark("copy_start", xs)
     g.prefetch_all(xs)
     tl.mark("prefetch_end", xs)            # the first slots' copies: they never wait for a slot
+    if ready is not None:
+        cs.wait_event(ready)
     tl.mark("draft_start", cs)
     for i in range(inp.k):
         for l in range(g.L):
@@ -337,14 +341,18 @@ def round_single(g: Group, inp: RoundInputs, cs, xs, tl: Timeline | None = None)
     return tl
 
 
-def round_staggered(X: Group, Y: Group, inp_x: RoundInputs, inp_y: RoundInputs, cs, xs, tl: Timeline | None = None):
+def round_staggered(X: Group, Y: Group, inp_x: RoundInputs, inp_y: RoundInputs, cs, xs, tl: Timeline | None = None,
+                    ready=None):
     """Cross-resource staggering: X drafts (HBM) while Y's full KV streams over
-    the link and Y verifies, accepts and commits.  Roles swap every round."""
+    the link and Y verifies, accepts and commits.  Roles swap every round.
+    `ready` as in round_single."""
     tl = tl or Timeline()
     tl.mark("start", cs)
     xs.wait_event(tl.ev["start"])
     tl.mark("copy_start", xs)
     Y.prefetch_all(xs)
+    if ready is not None:
+        cs.wait_event(ready)
     tl.mark("draft_start", cs)
     for i in range(inp_x.k):
         for l in range(X.L):
