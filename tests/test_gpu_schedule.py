@@ -135,3 +135,44 @@ def test_first_verify_against_oracle():
                                  kn[b:b + 1, :, h:h + 1], vn[b:b + 1, :, h:h + 1], [W.T], 1.0)
     err = np.abs(got[b:b + 1, :, h * G:(h + 1) * G] - want)
     assert err.max() <= 2e-2 and err.mean() <= 2e-3
+
+
+def test_inputs_arriving_on_another_stream():
+    """round_single with `ready`: the round's inputs copied from pinned host
+    memory on their own stream while the full-KV transfer starts; the results
+    equal a round on device-resident inputs."""
+    from verify_compressed_kv_gb300 import runtime as rt
+    from verify_compressed_kv_gb300.runtime import RoundInputs
+    cs, xs, ins = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    res = []
+    for mode in ("resident", "copied"):
+        g, other = build()
+        other.close()
+        outs = []
+        for c in range(N_CYCLES):
+            inp = inputs(0, c)
+            ready = None
+            if mode == "copied":
+                host = RoundInputs(*[getattr(inp, n).cpu().pin_memory() for n in
+                                     ("q_draft", "kv_cur", "q_verify", "kv_new", "logits", "drafts")])
+                dst = RoundInputs(*[torch.empty_like(getattr(inp, n)) for n in
+                                    ("q_draft", "kv_cur", "q_verify", "kv_new", "logits", "drafts")])
+                torch.cuda.synchronize()
+                with torch.cuda.stream(ins):
+                    for n in ("q_draft", "kv_cur", "q_verify", "kv_new", "logits", "drafts"):
+                        getattr(dst, n).copy_(getattr(host, n), non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(ins)
+                inp = dst
+            tl = rt.round_single(g, inp, cs, xs, ready=ready)
+            tl.ev["end"].synchronize()
+            outs.append((g.verify_out.cpu().numpy().copy(), g.n_acc.cpu().numpy().copy(),
+                         g.next_tok.cpu().numpy().copy()))
+            g.after_round()
+        res.append(outs + [state(g)])
+        g.close()
+    for a, b in zip(res[0][:-1], res[1][:-1]):
+        for x, y in zip(a, b):
+            assert np.array_equal(x, y)
+    for x, y in zip(res[0][-1], res[1][-1]):
+        assert np.array_equal(x, y)
