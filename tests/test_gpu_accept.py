@@ -44,7 +44,9 @@ def test_golden(vc, case):
     assert n[0] == case["n_acc"] and nxt[0] == case["next"] and am[0].tolist() == case["argmax"]
 
 
-@pytest.mark.parametrize("B,k,V", [(1, 4, 1024), (3, 7, 1001), (8, 16, 32768), (2, 0, 77), (5, 3, 6)])
+@pytest.mark.parametrize("B,k,V", [(1, 4, 1024), (3, 7, 1001), (8, 16, 32768), (2, 0, 77), (5, 3, 6),
+                                   (2, 63, 500),     # the largest draft: 64 rows per request
+                                   (3, 5, 1)])       # a one-token vocabulary
 def test_random_with_ties(vc, B, k, V):
     rng = np.random.default_rng(B * 100 + V)
     logits = rng.integers(-4, 5, size=(B, k + 1, V)).astype(np.float32)   # many exact ties
