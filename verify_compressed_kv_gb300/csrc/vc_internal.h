@@ -148,6 +148,80 @@ __device__ __forceinline__ void vc_bulk_g2s(void* dst, const void* src, uint32_t
       ::"r"(vc_smem_addr(dst)), "l"(src), "r"(bytes), "r"(vc_smem_addr(bar))
       : "memory");
 }
+
+// ---------------------------------------------------------------- PTX: tcgen05 (tensor cores with TMEM accumulators)
+// Operand tiles live in shared memory as K-major core matrices without
+// swizzle: a core matrix is 8 rows x 16 bytes (8 bf16 of the K axis), 128
+// contiguous bytes; `lbo` is the byte distance between core matrices that
+// are neighbours along K, `sbo` the distance between neighbouring 8-row
+// groups.  Descriptor fields: start address >> 4 (bits 0-13), lbo >> 4
+// (16-29), sbo >> 4 (32-45), descriptor version 1 (bit 46), no swizzle.
+__device__ __forceinline__ uint64_t vc_tc_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+// Instruction descriptor of an M x N x 16 kind::f16 product: bf16 A and B,
+// fp32 D, both operands K-major (D format bit 4, A / B formats bits 7 / 10,
+// N >> 3 at bit 17, M >> 4 at bit 24).  M = 128: N a multiple of 16 in
+// [16, 256]; D row i is TMEM lane i, column j is TMEM column j.
+__host__ __device__ constexpr uint32_t vc_tc_idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+// TMEM allocation of `ncols` columns (a power of two >= 32) by one whole
+// warp; the base address is written to *slot (shared memory).
+__device__ __forceinline__ void vc_tc_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(vc_smem_addr(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void vc_tc_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D (TMEM) = A . B^T (+ D if acc), issued by one thread.
+__device__ __forceinline__ void vc_tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          bool acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc ? 1u : 0u)
+      : "memory");
+}
+// Arrive once on `bar` when every earlier tcgen05.mma of this thread completed.
+__device__ __forceinline__ void vc_tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   vc_smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ void vc_tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void vc_tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 8 / 16 consecutive fp32 columns of the warp's 32 TMEM lanes (lane quarter
+// warp % 4): thread i gets lane 32 (warp % 4) + i.  Load and wait in one
+// statement, so no use of the values can move above the wait.
+__device__ __forceinline__ void vc_tc_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void vc_tc_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
 #endif  // __CUDACC__
 
 #endif  // VC_INTERNAL_H_

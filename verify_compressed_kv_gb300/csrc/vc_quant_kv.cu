@@ -554,21 +554,28 @@ __global__ void unpack_kernel(int T, int T_cap, int d, Packed p, float* K_hat, f
 
 // ------------------------------------------------------------------ token score
 //
-// S = q_obs . K^T per KV head on the tensor cores (mma.sync m16n8k16, bf16
-// operands, fp32 accumulate; the products of bf16 values are exact), log2
-// softmax scale applied to the fp32 sums.  A CTA covers kScoreRange = 1024
-// tokens of one (b, KV head) in kScoreTile = 128-token K tiles, double-buffered
-// with cp.async; all NR = G * n_obs rows sit in shared memory.  Warp w owns the
-// 32-token quarter w % 4 of each tile (its B fragments stay in registers for the
-// tile) and the 16-row m-tiles w / 4 + 4 k.
-//   pass 1: per row, (max, sum exp2) over the row's visible tokens of the range;
+// S = q_obs . K^T per KV head on the tcgen05 tensor cores: bf16 operands in
+// shared memory, fp32 accumulators in TMEM (the products of bf16 values are
+// exact), log2 softmax scale applied to the fp32 sums.  A CTA covers
+// kScoreRange = 1024 tokens of one (b, KV head) in kScoreTile = 128-token K
+// tiles, double-buffered with cp.async; all NR = G * n_obs rows of q sit in
+// shared memory.  Q and the K tiles are K-major core-matrix tiles
+// (vc_tc_desc), so the same tiles serve both orientations:
+//   pass 1: D = Q . K_tile^T, one M = 128 product per 128 rows (rows in TMEM
+//           lanes): each thread folds its own row's (max, sum exp2) over the
+//           visible tokens of the range;
 //   merge:  per row, (M, 1 / S) over all ranges;
-//   pass 2: score[t] = sum_r exp2(s_rt - M_r) / S_r.
-constexpr int kScoreThreads = 512;                 // 16 warps
-constexpr int kScoreMG = kScoreThreads / 128;      // m-tile groups (warps per token quarter)
+//   pass 2: D = K_tile . Q^T, N = NR (tokens in TMEM lanes): each thread sums
+//           exp2(s_rt - M_r) / S_r over the rows for its own token.
+// One thread issues a tile's products and commits them to an mbarrier; the 8
+// warps read TMEM by lane quarter (warp % 4) and split the columns (warp / 4).
+// Shared memory is at least 100 KB, so at most two CTAs share an SM and each
+// allocates at most 256 of its 512 TMEM columns.
+constexpr int kScoreThreads = 256;
 constexpr int kScoreTile = 128;
 constexpr int kScoreTilesPerRange = 8;
 constexpr int kScoreRange = kScoreTilesPerRange * kScoreTile;
+constexpr long long kScoreWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
 
 struct ScoreArgs {
   const uint16_t* q;    // [B, Hq, n_obs, d]
@@ -589,202 +596,255 @@ __device__ __forceinline__ void sc_cp_async16(void* smem, const void* gmem, bool
 __device__ __forceinline__ void sc_cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void sc_cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-__device__ __forceinline__ void sc_ldsm_x4(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(vc_smem_addr(p)));
-}
 // 2^x (ex2.approx.ftz: relative error ~2^-22; results below 2^-126 flush to 0)
 __device__ __forceinline__ float sc_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32
-__device__ __forceinline__ void sc_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 
 template <int MT, int D>
 struct ScoreCfg {
   static constexpr int NR = 16 * MT;               // rows = G * n_obs
-  static constexpr int LD = D + 8;                 // padded smem row (bf16): conflict-free ldmatrix
-  static constexpr int KS = D / 16;                // k-steps
-  static constexpr int MTW = (MT + kScoreMG - 1) / kScoreMG;   // m-tiles per warp (at most)
-  static constexpr size_t q_bytes = static_cast<size_t>(NR) * LD * 2;
-  static constexpr size_t k_bytes = 2ull * kScoreTile * LD * 2;
-  // pass 1: 4 x NR float2 quarter statistics; pass 2: NR float2 row stats + kScoreMG x 128 column sums
-  static constexpr size_t red_p2 = NR * 8 + kScoreMG * kScoreTile * 4;
-  static constexpr size_t red_bytes = (4 * NR * 8 > red_p2) ? 4 * NR * 8 : red_p2;
-  static constexpr size_t smem = q_bytes + k_bytes + red_bytes;
+  static constexpr uint32_t GROUP = D * 16;        // bytes of one 8-row group (D / 8 core matrices)
+  static constexpr int KS = D / 16;                // products along the channel axis
+  static constexpr int NM = (NR + 127) / 128;      // pass-1 products (128 rows each)
+  static constexpr uint32_t q_bytes = NR * D * 2;
+  static constexpr uint32_t k_bytes = kScoreTile * D * 2;      // one K stage
+  static constexpr uint32_t off_k = q_bytes;                    // two stages
+  static constexpr uint32_t off_red = off_k + 2 * k_bytes;
+  // pass 1: [2][NR] (max, sum) halves; pass 2: [NR] row thresholds + [2 tiles][2 halves][128] token sums
+  static constexpr uint32_t red1 = 2 * NR * 8, red2 = NR * 4 + 4 * kScoreTile * 4;
+  static constexpr uint32_t off_bar = off_red + (red1 > red2 ? red1 : red2);
+  static constexpr uint32_t used = off_bar + 16;                // mbarrier + TMEM base
+  static constexpr uint32_t smem = used > 100 * 1024 ? used : 100 * 1024;
+  static constexpr uint32_t cols1 = NM * 128;
+  static constexpr uint32_t cols2 = NR <= 32 ? 32 : NR <= 64 ? 64 : NR <= 128 ? 128 : 256;
+  // pass 1 with NR > 128 reads rows up to 256 from the start of Q (the rows
+  // past NR are never used): they must lie inside the CTA's shared memory
+  static_assert(NM == 1 || 256u * D * 2 <= smem, "pass-1 row block outside shared memory");
 };
 
-// Q rows of KV head kvh (row r = g * n_obs + o is query head kvh*G + g, obs o)
-// and the range's first K tile, by cp.async; the caller commits.
+// Byte offset of the 16-byte chunk (row r, channels 8c .. 8c + 7) in a
+// K-major core-matrix tile with D channels.
+template <int D>
+__device__ __forceinline__ uint32_t sc_tile_off(int r, int c) {
+  return (r >> 3) * (D * 16) + c * 128 + (r & 7) * 16;
+}
+
+// Q rows of KV head kvh: row r = g * n_obs + o is query head kvh * G + g,
+// observation o; the rows are contiguous in q.  Plain loads; the caller fences
+// them for the tensor cores.
 template <int MT, int D>
-__device__ __forceinline__ void score_load_q(const ScoreArgs& a, int b, int kvh, uint16_t* q_s) {
-  using C = ScoreCfg<MT, D>;
-  constexpr int VEC = D / 8;
+__device__ __forceinline__ void score_load_q(const ScoreArgs& a, int b, int kvh, uint8_t* q_s) {
+  constexpr int VEC = D / 8, NR = 16 * MT;
   const int G = a.Hq / a.Hkv;
-  for (int i = threadIdx.x; i < C::NR * VEC; i += blockDim.x) {
-    const int r = i / VEC, v = i % VEC;
-    const int g = r / a.n_obs, o = r % a.n_obs;
-    const uint16_t* src = a.q + ((static_cast<size_t>(b) * a.Hq + kvh * G + g) * a.n_obs + o) * D + v * 8;
-    sc_cp_async16(q_s + r * C::LD + v * 8, src, true);
+  const uint16_t* base = a.q + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(kvh) * G) * a.n_obs * D;
+  for (int i = threadIdx.x; i < NR * VEC; i += kScoreThreads) {
+    const int c = (i >> 3) % VEC, r = (i / (8 * VEC)) * 8 + (i & 7);
+    const uint4 v = *reinterpret_cast<const uint4*>(base + static_cast<size_t>(r) * D + c * 8);
+    *reinterpret_cast<uint4*>(q_s + sc_tile_off<D>(r, c)) = v;
   }
 }
 
-template <int MT, int D>
-__device__ __forceinline__ void score_load_k(const ScoreArgs& a, int bh, int t0, uint16_t* k_s) {
-  using C = ScoreCfg<MT, D>;
+// One 128-token K tile (zero rows past T) into a K stage, by cp.async.
+template <int D>
+__device__ __forceinline__ void score_load_k(const ScoreArgs& a, int bh, int t0, uint8_t* k_s) {
   constexpr int VEC = D / 8;
-  for (int i = threadIdx.x; i < kScoreTile * VEC; i += blockDim.x) {
-    const int t = i / VEC, v = i % VEC;
+  for (int i = threadIdx.x; i < kScoreTile * VEC; i += kScoreThreads) {
+    const int c = (i >> 3) % VEC, t = (i / (8 * VEC)) * 8 + (i & 7);
     const bool ok = t0 + t < a.T;
-    const uint16_t* src = a.K + (ok ? ((static_cast<size_t>(bh) * a.T + t0 + t) * D + v * 8) : 0);
-    sc_cp_async16(k_s + t * C::LD + v * 8, src, ok);
+    const uint16_t* src = a.K + (ok ? ((static_cast<size_t>(bh) * a.T + t0 + t) * D + c * 8) : 0);
+    sc_cp_async16(k_s + sc_tile_off<D>(t, c), src, ok);
   }
 }
 
-// The quarter's B fragments: kb[ks][np] covers tokens quarter*32 + np*16 .. +15
-// (n-tiles 2np, 2np + 1), channels ks*16 .. +15.
-template <int MT, int D>
-__device__ __forceinline__ void score_b_frags(const uint16_t* kt, int quarter, int lane,
-                                              uint32_t (&kb)[ScoreCfg<MT, D>::KS][2][4]) {
+// The products of one tile, issued by one thread.
+template <int PASS, int MT, int D>
+__device__ __forceinline__ void score_issue(uint32_t tmem, uint32_t q_addr, uint32_t k_addr) {
   using C = ScoreCfg<MT, D>;
+  if (PASS == 1) {
+    constexpr uint32_t idesc = vc_tc_idesc_bf16(128, kScoreTile);
 #pragma unroll
-  for (int ks = 0; ks < C::KS; ++ks)
+    for (int mm = 0; mm < C::NM; ++mm)
 #pragma unroll
-    for (int np = 0; np < 2; ++np)
-      sc_ldsm_x4(kb[ks][np], kt + (quarter * 32 + np * 16 + (lane & 7) + ((lane >> 4) << 3)) * C::LD + ks * 16 +
-                                     ((lane >> 3) & 1) * 8);
-}
-
-// s[nt][e] = q.k (unscaled) of row mt*16 + gid + 8 (e >> 1), token quarter*32 +
-// nt*8 + 2 tig + (e & 1) of the tile; -inf where the row does not see it.
-template <int MT, int D>
-__device__ __forceinline__ void score_item(const ScoreArgs& a, const uint16_t* q_s,
-                                           const uint32_t (&kb)[ScoreCfg<MT, D>::KS][2][4], int mt, int tq0,
-                                           int lane, float (&s)[4][4]) {
-  using C = ScoreCfg<MT, D>;
+      for (int kk = 0; kk < C::KS; ++kk)
+        vc_tc_mma(tmem + mm * kScoreTile, vc_tc_desc(q_addr + mm * 128 * D * 2 + kk * 256, 128, C::GROUP),
+                  vc_tc_desc(k_addr + kk * 256, 128, C::GROUP), idesc, kk > 0);
+  } else {
+    constexpr uint32_t idesc = vc_tc_idesc_bf16(kScoreTile, C::NR);
 #pragma unroll
-  for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) s[nt][e] = 0.0f;
-#pragma unroll
-  for (int ks = 0; ks < C::KS; ++ks) {
-    uint32_t qa[4];
-    sc_ldsm_x4(qa, q_s + (mt * 16 + (lane & 15)) * C::LD + ks * 16 + (lane >> 4) * 8);
-#pragma unroll
-    for (int np = 0; np < 2; ++np) {
-      sc_mma(s[2 * np], qa, kb[ks][np][0], kb[ks][np][1]);
-      sc_mma(s[2 * np + 1], qa, kb[ks][np][2], kb[ks][np][3]);
-    }
-  }
-  // row r sees tokens t <= T - n_obs + r % n_obs: only quarters that reach the
-  // observation window (or run past T) need the mask
-  if (tq0 + 32 > a.T - a.n_obs) {
-    const int r0 = mt * 16 + (lane >> 2);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int last = a.T - a.n_obs + (r0 + 8 * h) % a.n_obs;
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-          if (tq0 + nt * 8 + (lane & 3) * 2 + c > last) s[nt][2 * h + c] = -INFINITY;
-    }
+    for (int kk = 0; kk < C::KS; ++kk)
+      vc_tc_mma(tmem, vc_tc_desc(k_addr + kk * 256, 128, C::GROUP), vc_tc_desc(q_addr + kk * 256, 128, C::GROUP),
+                idesc, kk > 0);
   }
 }
 
-// grid (n_ranges, B*Hkv)
-template <int MT, int D>
-__global__ void __launch_bounds__(kScoreThreads) score_pass1(ScoreArgs a) {
+// grid (n_ranges, B*Hkv).  PASS 1 writes the range statistics, PASS 2 the scores.
+template <int PASS, int MT, int D>
+__global__ void __launch_bounds__(kScoreThreads, 2) score_pass(ScoreArgs a) {
   using C = ScoreCfg<MT, D>;
+  constexpr int NR = C::NR;
+  constexpr uint32_t ncols = PASS == 1 ? C::cols1 : C::cols2;
   extern __shared__ __align__(16) uint8_t smem[];
-  uint16_t* q_s = reinterpret_cast<uint16_t*>(smem);
-  uint16_t* k_s = reinterpret_cast<uint16_t*>(smem + C::q_bytes);
-  float2* red = reinterpret_cast<float2*>(smem + C::q_bytes + C::k_bytes);    // [4][NR]
+  uint8_t* q_s = smem;
+  uint8_t* k_s = smem + C::off_k;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::off_bar);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(smem + C::off_bar + 8);
   const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh % a.Hkv;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, half = warp >> 2;
   const int r0 = blockIdx.x * kScoreRange;
   const int n_tiles = min(kScoreTilesPerRange, (a.T - r0 + kScoreTile - 1) / kScoreTile);
-  score_load_q<MT, D>(a, b, kvh, q_s);
-  score_load_k<MT, D>(a, bh, r0, k_s);
+
+  if (warp == 0) vc_tc_alloc(slot, ncols);
+  if (threadIdx.x == 32) {
+    vc_mbar_init(bar, 1);
+    vc_fence_mbar_init();
+  }
+  score_load_k<D>(a, bh, r0, k_s);
   sc_cp_async_commit();
-  float m[C::MTW][2], l[C::MTW][2];
-#pragma unroll
-  for (int k = 0; k < C::MTW; ++k) m[k][0] = m[k][1] = -INFINITY, l[k][0] = l[k][1] = 0.0f;
-  for (int it = 0; it < n_tiles; ++it) {
-    if (it + 1 < n_tiles) {
-      score_load_k<MT, D>(a, bh, r0 + (it + 1) * kScoreTile, k_s + ((it + 1) & 1) * kScoreTile * C::LD);
-      sc_cp_async_commit();
-      sc_cp_async_wait<1>();
-    } else {
-      sc_cp_async_wait<0>();
-    }
-    __syncthreads();
-    uint32_t kb[C::KS][2][4];
-    score_b_frags<MT, D>(k_s + (it & 1) * kScoreTile * C::LD, quarter, lane, kb);
-    const int tq0 = r0 + it * kScoreTile + quarter * 32;
-#pragma unroll
-    for (int k = 0; k < C::MTW; ++k) {
-      const int mt = (warp >> 2) + kScoreMG * k;
-      if (mt >= MT) break;
-      float s[4][4];
-      score_item<MT, D>(a, q_s, kb, mt, tq0, lane, s);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) mx = fmaxf(mx, fmaxf(s[nt][2 * h], s[nt][2 * h + 1]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-        const float mn = fmaxf(m[k][h], mx * a.scale_log2);     // log2 units (scale > 0)
-        if (mn == -INFINITY) continue;             // nothing visible yet (quad-uniform)
-        float add = 0.0f;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-          for (int c = 0; c < 2; ++c) add += sc_exp2(fmaf(s[nt][2 * h + c], a.scale_log2, -mn));
-        l[k][h] = l[k][h] * sc_exp2(m[k][h] - mn) + add;
-        m[k][h] = mn;
-      }
-    }
-    __syncthreads();                               // buffer it & 1 is refilled next
+  if (n_tiles > 1) {
+    score_load_k<D>(a, bh, r0 + kScoreTile, k_s + C::k_bytes);
+    sc_cp_async_commit();
   }
-  // quad sums, then the 4 quarters of every row
-#pragma unroll
-  for (int k = 0; k < C::MTW; ++k) {
-    const int mt = (warp >> 2) + kScoreMG * k;
-    if (mt >= MT) break;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float x = l[k][h];
-      x += __shfl_xor_sync(0xFFFFFFFFu, x, 1);
-      x += __shfl_xor_sync(0xFFFFFFFFu, x, 2);
-      if ((lane & 3) == 0) red[quarter * C::NR + mt * 16 + (lane >> 2) + 8 * h] = make_float2(m[k][h], x);
+  score_load_q<MT, D>(a, b, kvh, q_s);
+  float* red = reinterpret_cast<float*>(smem + C::off_red);
+  if (PASS == 2) {                                 // row thresholds M_r + log2 S_r
+    for (int r = threadIdx.x; r < NR; r += kScoreThreads) {
+      const float2 st = a.rowstat[static_cast<size_t>(bh) * NR + r];
+      red[r] = st.x - log2f(st.y);
     }
   }
+  vc_tc_fence_before();
   __syncthreads();
-  for (int r = threadIdx.x; r < C::NR; r += blockDim.x) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) M = fmaxf(M, red[q * C::NR + r].x);
-    float S = 0.0f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 st = red[q * C::NR + r];
-        if (st.x != -INFINITY) S += st.y * exp2f(st.x - M);
-      }
+  vc_tc_fence_after();
+  const uint32_t tmem = *slot;
+  const uint32_t q_addr = vc_smem_addr(q_s), k_addr = vc_smem_addr(k_s);
+  const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+
+  // pass 1: this thread's row and running (max, sum); NR <= 128: the two warp
+  // halves take 64 tokens of each tile, else half h takes rows 128 h .. 128 h + 127
+  constexpr bool SPLIT = C::NM == 1;
+  const int mm = SPLIT ? 0 : half;
+  const int row = mm * 128 + quarter * 32 + lane;
+  const bool rows_live = mm * 128 + quarter * 32 < NR;      // warp-uniform
+  const int last = a.T - a.n_obs + row % a.n_obs;          // last token the row sees
+  float m = -INFINITY, l = 0.0f;
+  float* tsum = red + NR;                                  // pass 2: [2][2][128]
+  bool alive = true;
+
+  for (int it = 0; it < n_tiles; ++it) {
+    const int t0 = r0 + it * kScoreTile;
+    const uint32_t ks = k_addr + (it & 1) * C::k_bytes;
+    if (it + 1 < n_tiles) sc_cp_async_wait<1>(); else sc_cp_async_wait<0>();
+    vc_fence_proxy_async_smem();                   // this thread's tile writes -> tensor-core reads
+    __syncthreads();                               // tile it complete; TMEM free (previous tile read)
+    if (PASS == 2 && it > 0 && threadIdx.x < kScoreTile) {   // scores of the previous tile
+      const int t = t0 - kScoreTile + threadIdx.x;
+      const float* ts = tsum + ((it - 1) & 1) * 2 * kScoreTile;
+      if (t < a.T) a.score[static_cast<size_t>(bh) * a.T + t] = ts[threadIdx.x] + ts[kScoreTile + threadIdx.x];
     }
-    a.stats[(static_cast<size_t>(bh) * a.n_ranges + blockIdx.x) * C::NR + r] = make_float2(M, S);
+    if (threadIdx.x == 0) {
+      vc_tc_fence_after();
+      score_issue<PASS, MT, D>(tmem, q_addr, ks);
+      vc_tc_commit(bar);
+    }
+    const bool ok = vc_mbar_wait_bounded(bar, static_cast<uint32_t>(it & 1), kScoreWaitCycles);
+    if (!__syncthreads_and(ok)) {
+      if (threadIdx.x == 0) atomicOr(&g_quant_status, VC_DEV_BARRIER_TIMEOUT);
+      alive = false;
+      break;
+    }
+    vc_tc_fence_after();
+    if (it + 2 < n_tiles) {                        // the products read this stage: refill it
+      score_load_k<D>(a, bh, t0 + 2 * kScoreTile, k_s + (it & 1) * C::k_bytes);
+      sc_cp_async_commit();
+    }
+    const bool masked = t0 + kScoreTile > a.T - a.n_obs;     // tile reaches the observation window
+    if (PASS == 1) {
+      if (rows_live) {
+        const int c_lo = SPLIT ? half * 64 : 0;
+#pragma unroll 1
+        for (int c0 = c_lo; c0 < c_lo + (SPLIT ? 64 : 128); c0 += 16) {
+          float s[16];
+          vc_tc_ld16(t_lane + mm * kScoreTile + c0, s);
+          if (masked) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (t0 + c0 + j > last) s[j] = -INFINITY;
+          }
+          float mx = s[0];
+#pragma unroll
+          for (int j = 1; j < 16; ++j) mx = fmaxf(mx, s[j]);
+          const float mn = fmaxf(m, mx * a.scale_log2);      // log2 units (scale > 0)
+          if (mn == -INFINITY) continue;                      // nothing visible yet
+          float add = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) add += sc_exp2(fmaf(s[j], a.scale_log2, -mn));
+          l = l * sc_exp2(m - mn) + add;
+          m = mn;
+        }
+      }
+    } else {
+      constexpr int HALF = NR / 2;
+      constexpr int CH = HALF % 16 == 0 ? 16 : 8;
+      const int t = t0 + quarter * 32 + lane;
+      float acc = 0.0f;
+#pragma unroll 1
+      for (int c0 = half * HALF; c0 < (half + 1) * HALF; c0 += CH) {
+        float s[CH];
+        if constexpr (CH == 16) vc_tc_ld16(t_lane + c0, s); else vc_tc_ld8(t_lane + c0, s);
+        float th[CH];
+#pragma unroll
+        for (int j = 0; j < CH; j += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(red + c0 + j);
+          th[j] = v.x; th[j + 1] = v.y; th[j + 2] = v.z; th[j + 3] = v.w;
+        }
+        if (masked) {
+#pragma unroll
+          for (int j = 0; j < CH; ++j)
+            if (t <= a.T - a.n_obs + (c0 + j) % a.n_obs) acc += sc_exp2(fmaf(s[j], a.scale_log2, -th[j]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < CH; ++j) acc += sc_exp2(fmaf(s[j], a.scale_log2, -th[j]));
+        }
+      }
+      tsum[(it & 1) * 2 * kScoreTile + half * kScoreTile + quarter * 32 + lane] = acc;
+    }
+    vc_tc_fence_before();                          // TMEM reads done before the next tile's products
   }
+  sc_cp_async_wait<0>();
+  __syncthreads();
+  if (alive) {
+    if (PASS == 1) {
+      float2* st = reinterpret_cast<float2*>(red);                 // [2][NR]
+      float2* out = a.stats + (static_cast<size_t>(bh) * a.n_ranges + blockIdx.x) * NR;
+      if (SPLIT) {
+        if (rows_live && row < NR) st[half * NR + row] = make_float2(m, l);
+        __syncthreads();
+        for (int r = threadIdx.x; r < NR; r += kScoreThreads) {
+          const float2 x = st[r], y = st[NR + r];
+          const float M = fmaxf(x.x, y.x);
+          float S = 0.0f;
+          if (M != -INFINITY) {
+            if (x.x != -INFINITY) S += x.y * exp2f(x.x - M);
+            if (y.x != -INFINITY) S += y.y * exp2f(y.x - M);
+          }
+          out[r] = make_float2(M, S);
+        }
+      } else if (rows_live && row < NR) {
+        out[row] = make_float2(m, l);
+      }
+    } else if (threadIdx.x < kScoreTile && n_tiles > 0) {
+      const int t = r0 + (n_tiles - 1) * kScoreTile + threadIdx.x;
+      const float* ts = tsum + ((n_tiles - 1) & 1) * 2 * kScoreTile;
+      if (t < a.T) a.score[static_cast<size_t>(bh) * a.T + t] = ts[threadIdx.x] + ts[kScoreTile + threadIdx.x];
+    }
+  }
+  vc_tc_fence_before();
+  __syncthreads();
+  vc_tc_fence_after();
+  if (warp == 0) vc_tc_dealloc(tmem, ncols);
 }
 
 // grid (B*Hkv): per row, (M, 1/S) over the ranges.
@@ -800,76 +860,6 @@ __global__ void score_merge(ScoreArgs a, int NR) {
       if (v.x != -INFINITY) S += v.y * exp2f(v.x - M);
     }
     a.rowstat[static_cast<size_t>(bh) * NR + r] = make_float2(M, 1.0f / S);
-  }
-}
-
-// grid (n_ranges, B*Hkv)
-template <int MT, int D>
-__global__ void __launch_bounds__(kScoreThreads) score_pass2(ScoreArgs a) {
-  using C = ScoreCfg<MT, D>;
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint16_t* q_s = reinterpret_cast<uint16_t*>(smem);
-  uint16_t* k_s = reinterpret_cast<uint16_t*>(smem + C::q_bytes);
-  float2* rs = reinterpret_cast<float2*>(smem + C::q_bytes + C::k_bytes);    // [NR] (M, 1/S)
-  float* col = reinterpret_cast<float*>(rs + C::NR);                            // [kScoreMG][128]
-  const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh % a.Hkv;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3;
-  const int r0 = blockIdx.x * kScoreRange;
-  const int n_tiles = min(kScoreTilesPerRange, (a.T - r0 + kScoreTile - 1) / kScoreTile);
-  score_load_q<MT, D>(a, b, kvh, q_s);
-  score_load_k<MT, D>(a, bh, r0, k_s);
-  sc_cp_async_commit();
-  for (int r = threadIdx.x; r < C::NR; r += blockDim.x) rs[r] = a.rowstat[static_cast<size_t>(bh) * C::NR + r];
-  for (int it = 0; it < n_tiles; ++it) {
-    if (it + 1 < n_tiles) {
-      score_load_k<MT, D>(a, bh, r0 + (it + 1) * kScoreTile, k_s + ((it + 1) & 1) * kScoreTile * C::LD);
-      sc_cp_async_commit();
-      sc_cp_async_wait<1>();
-    } else {
-      sc_cp_async_wait<0>();
-    }
-    __syncthreads();
-    uint32_t kb[C::KS][2][4];
-    score_b_frags<MT, D>(k_s + (it & 1) * kScoreTile * C::LD, quarter, lane, kb);
-    const int tq0 = r0 + it * kScoreTile + quarter * 32;
-    float cs[4][2];                                // column partial sums of this thread's rows
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) cs[nt][0] = cs[nt][1] = 0.0f;
-#pragma unroll
-    for (int k = 0; k < C::MTW; ++k) {
-      const int mt = (warp >> 2) + kScoreMG * k;
-      if (mt >= MT) break;
-      float s[4][4];
-      score_item<MT, D>(a, q_s, kb, mt, tq0, lane, s);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float2 st = rs[mt * 16 + (lane >> 2) + 8 * h];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-          for (int c = 0; c < 2; ++c) cs[nt][c] = fmaf(sc_exp2(fmaf(s[nt][2 * h + c], a.scale_log2, -st.x)), st.y, cs[nt][c]);
-      }
-    }
-    // sum over the 8 row groups of the warp, then over the kScoreMG warps of the quarter
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float x = cs[nt][c];
-        x += __shfl_xor_sync(0xFFFFFFFFu, x, 4);
-        x += __shfl_xor_sync(0xFFFFFFFFu, x, 8);
-        x += __shfl_xor_sync(0xFFFFFFFFu, x, 16);
-        if (lane < 4) col[(warp >> 2) * kScoreTile + quarter * 32 + nt * 8 + lane * 2 + c] = x;
-      }
-    __syncthreads();
-    if (threadIdx.x < kScoreTile) {
-      const int t = r0 + it * kScoreTile + threadIdx.x;
-      float x = 0.0f;
-#pragma unroll
-      for (int g = 0; g < kScoreMG; ++g) x += col[g * kScoreTile + threadIdx.x];
-      if (t < a.T) a.score[static_cast<size_t>(bh) * a.T + t] = x;
-    }
-    __syncthreads();                               // buffer it & 1 and col are reused next
   }
 }
 
@@ -1163,6 +1153,7 @@ extern "C" vc_status_t vc_token_score(const vc_shape_t* s, int32_t T, int32_t n_
   vc_status_t st = check_score(s, T, n_obs, &NR);
   if (st != VC_OK) return st;
   VC_REQUIRE(q_obs && K && score, "NULL pointer");
+  VC_REQUIRE(vc_aligned16(q_obs) && vc_aligned16(K), "q_obs and K must be 16-byte aligned");
   size_t need = 0;
   vc_token_score_workspace_size(s, T, n_obs, &need);
   if (!workspace || workspace_bytes < need)
@@ -1180,11 +1171,11 @@ extern "C" vc_status_t vc_token_score(const vc_shape_t* s, int32_t T, int32_t n_
 #define VC_SCORE_CASE(M, D)                                                                          \
   case M: {                                                                                          \
     const int sm = static_cast<int>(ScoreCfg<M, D>::smem);                                           \
-    cudaFuncSetAttribute(score_pass1<M, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);        \
-    cudaFuncSetAttribute(score_pass2<M, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);        \
-    score_pass1<M, D><<<grid, kScoreThreads, sm, cs>>>(a);                                           \
+    cudaFuncSetAttribute(score_pass<1, M, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);      \
+    cudaFuncSetAttribute(score_pass<2, M, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);      \
+    score_pass<1, M, D><<<grid, kScoreThreads, sm, cs>>>(a);                                         \
     score_merge<<<bhs, 256, 0, cs>>>(a, NR);                                                         \
-    score_pass2<M, D><<<grid, kScoreThreads, sm, cs>>>(a);                                           \
+    score_pass<2, M, D><<<grid, kScoreThreads, sm, cs>>>(a);                                         \
     break;                                                                                           \
   }
 #define VC_SCORE_SWITCH(D)                                                                           \
