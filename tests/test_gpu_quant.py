@@ -255,8 +255,11 @@ def gpu_scores(vc, q, K, scale, n_obs=32):
                                                 (1, 1, 1, 40, 128, 16),       # one m-tile, one partial tile
                                                 (1, 6, 1, 1029, 64, 32),      # 12 m-tiles, ragged 2nd range
                                                 (2, 14, 2, 2100, 128, 32),    # 14 m-tiles, 3 ranges
-                                                (1, 4, 1, 32, 64, 32)],       # T = n_obs: row i sees i + 1 keys
-                         ids=["g5", "g2_d64", "g8", "nr16_t40", "g6_ragged", "g7_3ranges", "t_eq_nobs"])
+                                                (1, 4, 1, 32, 64, 32),        # T = n_obs: row i sees i + 1 keys
+                                                (32, 40, 8, 200, 128, 32),    # 256 two-tile items: q reloaded per item
+                                                (4, 32, 8, 8192, 128, 32)],   # 256 items over the SMs: runs cross slices
+                         ids=["g5", "g2_d64", "g8", "nr16_t40", "g6_ragged", "g7_3ranges", "t_eq_nobs",
+                              "g5_many_items", "g4_runs_cross_slices"])
 def test_token_score(vc, B, Hq, Hkv, T, d, n_obs):
     w = synth.get("qwen", B=B, Hq=Hq, Hkv=Hkv, T=T, d=d)
     K, _ = synth.kv(w)

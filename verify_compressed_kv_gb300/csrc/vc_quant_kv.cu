@@ -16,6 +16,9 @@
 // codes are reproducible bit for bit.  Packed layout: include/vc.h.
 #include <cfloat>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "vc_internal.h"
 
 namespace {
@@ -556,298 +559,448 @@ __global__ void unpack_kernel(int T, int T_cap, int d, Packed p, float* K_hat, f
 //
 // S = q_obs . K^T per KV head on the tcgen05 tensor cores: bf16 operands in
 // shared memory, fp32 accumulators in TMEM (the products of bf16 values are
-// exact), log2 softmax scale applied to the fp32 sums.  A CTA covers
-// kScoreRange = 1024 tokens of one (b, KV head) in kScoreTile = 128-token K
-// tiles, double-buffered with cp.async; all NR = G * n_obs rows of q sit in
-// shared memory.  Q and the K tiles are K-major core-matrix tiles
-// (vc_tc_desc), so the same tiles serve both orientations:
-//   pass 1: D = Q . K_tile^T, one M = 128 product per 128 rows (rows in TMEM
-//           lanes): each thread folds its own row's (max, sum exp2) over the
-//           visible tokens of the range;
-//   merge:  per row, (M, 1 / S) over all ranges;
-//   pass 2: D = K_tile . Q^T, N = NR (tokens in TMEM lanes): each thread sums
-//           exp2(s_rt - M_r) / S_r over the rows for its own token.
-// One thread issues a tile's products and commits them to an mbarrier; the 8
-// warps read TMEM by lane quarter (warp % 4) and split the columns (warp / 4).
-// Shared memory is at least 100 KB, so at most two CTAs share an SM and each
-// allocates at most 256 of its 512 TMEM columns.
-constexpr int kScoreThreads = 256;
+// exact), log2 softmax scale applied to the fp32 sums.  The work is a list of
+// items, one per (b, KV head) and kScoreRange = 1024-token range; a
+// persistent CTA per SM takes a contiguous run of items and walks their
+// 128-token K tiles as one sequence.  Warp roles:
+//   * lane 0 of the last warp loads K tiles (and q when the KV head changes)
+//     with TMA tensor copies into a kScoreStages ring and issues each tile's
+//     products into one of two TMEM buffers;
+//   * 16 epilogue warps read a buffer (warp w: TMEM lane quarter w % 4) while
+//     the tensor cores fill the other.
+// They meet only on mbarriers: stage full (TMA bytes), stage empty and buffer
+// full (tcgen05.commit), buffer empty (16 warp arrivals).  Both operands are
+// K-major core-matrix tiles written by TMA boxes of 8 channels: chunk c of a
+// tile holds 8 channels of every row, 16 bytes per row, so neighbouring 8-row
+// groups are 128 bytes apart and neighbouring chunks rows * 16 bytes apart.
+//   pass 1: D = Q . K_tile^T (rows in TMEM lanes): each thread folds (max,
+//           sum exp2) of one row over 32 tokens of every tile; per item the
+//           4 partials of every row are merged into the range's statistics.
+//           Rows 0-127 are one M = 128 product; rows 128-255 either one more
+//           (NR > 224) or, for NR <= 224, one N = 32 product per 32-row block
+//           and lane quarter q whose A rows start at 128 + 32 x - 32 q, so
+//           block x lands in quarter q's lanes for tokens 32 q .. 32 q + 31
+//           and every quarter (scheduler) gets the same share;
+//   merge:  per row, the threshold M + log2 S over all ranges;
+//   pass 2: D = K_tile . Q^T (tokens in TMEM lanes, N = NR): each thread sums
+//           exp2(s_rt - threshold_r) over a quarter of the rows for its
+//           token; the quarters are added in shared memory.
+constexpr int kScoreEpiWarps = 16;
+constexpr int kScoreEpiThreads = kScoreEpiWarps * 32;
+constexpr int kScoreThreads = kScoreEpiThreads + 32;
 constexpr int kScoreTile = 128;
 constexpr int kScoreTilesPerRange = 8;
 constexpr int kScoreRange = kScoreTilesPerRange * kScoreTile;
+constexpr int kScoreStages = 4;
 constexpr long long kScoreWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
 
 struct ScoreArgs {
-  const uint16_t* q;    // [B, Hq, n_obs, d]
-  const uint16_t* K;    // [B, Hkv, T, d]
   int T, n_obs, Hq, Hkv;
   float scale_log2;     // softmax_scale * log2(e)
   float2* stats;        // [B*Hkv, n_ranges, NR] (max, sum) per range, log2 units
-  float2* rowstat;      // [B*Hkv, NR] (M, 1 / S)
+  float* thr;           // [B*Hkv, NR] M + log2 S per row
   int n_ranges;
-  float* score;         // [B, Hkv, T]
+  int n_items;          // B * Hkv * n_ranges
 };
 
-__device__ __forceinline__ void sc_cp_async16(void* smem, const void* gmem, bool valid) {
-  const int n = valid ? 16 : 0;                    // src-size 0: zero fill
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(vc_smem_addr(smem)), "l"(gmem), "r"(n)
-               : "memory");
-}
-__device__ __forceinline__ void sc_cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void sc_cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 // 2^x (ex2.approx.ftz: relative error ~2^-22; results below 2^-126 flush to 0)
 __device__ __forceinline__ float sc_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// TMA tensor copies into this CTA's shared memory, completion as transaction bytes on `bar`.
+__device__ __forceinline__ void sc_tma3(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(vc_smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(vc_smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void sc_tma2(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(vc_smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(vc_smem_addr(bar))
+      : "memory");
+}
 
 template <int MT, int D>
 struct ScoreCfg {
   static constexpr int NR = 16 * MT;               // rows = G * n_obs
-  static constexpr uint32_t GROUP = D * 16;        // bytes of one 8-row group (D / 8 core matrices)
   static constexpr int KS = D / 16;                // products along the channel axis
-  static constexpr int NM = (NR + 127) / 128;      // pass-1 products (128 rows each)
+  static constexpr int CHUNKS = D / 8;             // TMA boxes per tile
+  // pass 1 layout of rows 128 .. NR - 1
+  static constexpr bool FULL2 = NR > 128;          // a second M = 128 product over all tokens
+  static constexpr int NE = (NR <= 128 || FULL2) ? 0 : (NR - 128 + 31) / 32;   // spread 32-row blocks
+  static constexpr int cols1 = NR <= 128 ? 128 : FULL2 ? 256 : 128 + 128 * NE;
+  // TMEM buffer stride (a power of two) and count
+  static constexpr int stride1 = cols1 <= 128 ? 128 : cols1 <= 256 ? 256 : 512;
+  static constexpr int stride2 = NR <= 32 ? 32 : NR <= 64 ? 64 : NR <= 128 ? 128 : 256;
+  static constexpr int bufs1 = 2 * stride1 <= 512 ? 2 : 1;
+  static constexpr int bufs2 = 2 * stride2 <= 512 ? 2 : 1;
+  // pass 2: NCG column groups of CW rows of q (CW in 16 .. 64, a multiple of 8)
+  static constexpr int NCG = NR >= 64 ? 4 : NR / 16;
+  static constexpr int CW = NR / NCG;
+  // highest q row a pass-1 product reads (rows past NR feed unused lanes)
+  static constexpr int max_row = FULL2 ? 255 : NE > 0 ? 223 + 32 * NE : 127;
   static constexpr uint32_t q_bytes = NR * D * 2;
-  static constexpr uint32_t k_bytes = kScoreTile * D * 2;      // one K stage
-  static constexpr uint32_t off_k = q_bytes;                    // two stages
-  static constexpr uint32_t off_red = off_k + 2 * k_bytes;
-  // pass 1: [2][NR] (max, sum) halves; pass 2: [NR] row thresholds + [2 tiles][2 halves][128] token sums
-  static constexpr uint32_t red1 = 2 * NR * 8, red2 = NR * 4 + 4 * kScoreTile * 4;
-  static constexpr uint32_t off_bar = off_red + (red1 > red2 ? red1 : red2);
-  static constexpr uint32_t used = off_bar + 16;                // mbarrier + TMEM base
-  static constexpr uint32_t smem = used > 100 * 1024 ? used : 100 * 1024;
-  static constexpr uint32_t cols1 = NM * 128;
-  static constexpr uint32_t cols2 = NR <= 32 ? 32 : NR <= 64 ? 64 : NR <= 128 ? 128 : 256;
-  // pass 1 with NR > 128 reads rows up to 256 from the start of Q (the rows
-  // past NR are never used): they must lie inside the CTA's shared memory
-  static_assert(NM == 1 || 256u * D * 2 <= smem, "pass-1 row block outside shared memory");
+  // the last chunk's rows may run past the q tile: keep them inside the region
+  static constexpr uint32_t q_reach = (CHUNKS - 1) * NR * 16 + (max_row + 1) * 16;
+  static constexpr uint32_t q_region = ((q_reach > q_bytes ? q_reach : q_bytes) + 1023) / 1024 * 1024;
+  static constexpr uint32_t k_bytes = kScoreTile * D * 2;                  // one K stage
+  static constexpr uint32_t off_k = q_region;
+  static constexpr uint32_t off_red = off_k + kScoreStages * k_bytes;     // pass 1: [2][4][NR] float2
+  static constexpr uint32_t off_sum = off_red + 2 * 4 * NR * 8;           // pass 2: [2][4][128] float
+  static constexpr uint32_t off_thr = off_sum + 2 * 4 * kScoreTile * 4;   // pass 2: [NR] float
+  static constexpr uint32_t off_bar = off_thr + NR * 4;                   // 13 mbarriers, TMEM base, abort
+  static constexpr uint32_t smem = off_bar + 13 * 8 + 8 + 128;        // + alignment slack
+  static_assert(smem <= 227 * 1024, "shared memory");
+  static_assert(NE <= 3 && cols1 <= 512, "TMEM plan");
 };
 
-// Byte offset of the 16-byte chunk (row r, channels 8c .. 8c + 7) in a
-// K-major core-matrix tile with D channels.
-template <int D>
-__device__ __forceinline__ uint32_t sc_tile_off(int r, int c) {
-  return (r >> 3) * (D * 16) + c * 128 + (r & 7) * 16;
+__host__ __device__ constexpr uint32_t sc_pow2_cols(int c) {
+  return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512;
 }
 
-// Q rows of KV head kvh: row r = g * n_obs + o is query head kvh * G + g,
-// observation o; the rows are contiguous in q.  Plain loads; the caller fences
-// them for the tensor cores.
-template <int MT, int D>
-__device__ __forceinline__ void score_load_q(const ScoreArgs& a, int b, int kvh, uint8_t* q_s) {
-  constexpr int VEC = D / 8, NR = 16 * MT;
-  const int G = a.Hq / a.Hkv;
-  const uint16_t* base = a.q + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(kvh) * G) * a.n_obs * D;
-  for (int i = threadIdx.x; i < NR * VEC; i += kScoreThreads) {
-    const int c = (i >> 3) % VEC, r = (i / (8 * VEC)) * 8 + (i & 7);
-    const uint4 v = *reinterpret_cast<const uint4*>(base + static_cast<size_t>(r) * D + c * 8);
-    *reinterpret_cast<uint4*>(q_s + sc_tile_off<D>(r, c)) = v;
+// Position in a CTA's tile sequence: item (slice, range) and tile within it.
+struct ScoreCursor {
+  int item, tile, n_tiles, bh, t0;
+  __device__ __forceinline__ void set(const ScoreArgs& a, int it) {
+    item = it;
+    tile = 0;
+    bh = it / a.n_ranges;
+    const int r0 = (it % a.n_ranges) * kScoreRange;
+    n_tiles = min(kScoreTilesPerRange, (a.T - r0 + kScoreTile - 1) / kScoreTile);
+    t0 = r0;
   }
-}
-
-// One 128-token K tile (zero rows past T) into a K stage, by cp.async.
-template <int D>
-__device__ __forceinline__ void score_load_k(const ScoreArgs& a, int bh, int t0, uint8_t* k_s) {
-  constexpr int VEC = D / 8;
-  for (int i = threadIdx.x; i < kScoreTile * VEC; i += kScoreThreads) {
-    const int c = (i >> 3) % VEC, t = (i / (8 * VEC)) * 8 + (i & 7);
-    const bool ok = t0 + t < a.T;
-    const uint16_t* src = a.K + (ok ? ((static_cast<size_t>(bh) * a.T + t0 + t) * D + c * 8) : 0);
-    sc_cp_async16(k_s + sc_tile_off<D>(t, c), src, ok);
+  __device__ __forceinline__ void next(const ScoreArgs& a) {
+    if (++tile < n_tiles) {
+      t0 += kScoreTile;
+    } else {
+      set(a, item + 1);
+    }
   }
-}
+};
 
-// The products of one tile, issued by one thread.
+// The products of one tile into TMEM columns from `tmem`, issued by one
+// thread.  A descriptor moves with its start address: desc + (bytes >> 4)
+// (the address field cannot carry: shared addresses stay below 256 KB).
+//   K tile: chunk stride 128 * 16 = 2048 B, 8-row group stride 128 B;
+//   q:      chunk stride NR * 16 B,       8-row group stride 128 B.
 template <int PASS, int MT, int D>
 __device__ __forceinline__ void score_issue(uint32_t tmem, uint32_t q_addr, uint32_t k_addr) {
   using C = ScoreCfg<MT, D>;
+  constexpr uint32_t QC = C::NR * 16, KC = kScoreTile * 16;
+  const uint64_t dq = vc_tc_desc(q_addr, QC, 128), dk = vc_tc_desc(k_addr, KC, 128);
+  constexpr uint64_t qk = (2 * QC) >> 4, kk16 = (2 * KC) >> 4;     // one 16-channel step
   if (PASS == 1) {
-    constexpr uint32_t idesc = vc_tc_idesc_bf16(128, kScoreTile);
+    constexpr uint32_t id128 = vc_tc_idesc_bf16(128, kScoreTile), id32 = vc_tc_idesc_bf16(128, 32);
 #pragma unroll
-    for (int mm = 0; mm < C::NM; ++mm)
+    for (int kk = 0; kk < C::KS; ++kk) vc_tc_mma(tmem, dq + kk * qk, dk + kk * kk16, id128, kk > 0);
+    if (C::FULL2) {
 #pragma unroll
       for (int kk = 0; kk < C::KS; ++kk)
-        vc_tc_mma(tmem + mm * kScoreTile, vc_tc_desc(q_addr + mm * 128 * D * 2 + kk * 256, 128, C::GROUP),
-                  vc_tc_desc(k_addr + kk * 256, 128, C::GROUP), idesc, kk > 0);
+        vc_tc_mma(tmem + 128, dq + ((128 * 16) >> 4) + kk * qk, dk + kk * kk16, id128, kk > 0);
+    }
+#pragma unroll
+    for (int x = 0; x < C::NE; ++x)
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int kk = 0; kk < C::KS; ++kk)      // A rows from 128 + 32 x - 32 q; tokens 32 q .. 32 q + 31
+          vc_tc_mma(tmem + 128 + (4 * x + q) * 32, dq + (((128 + 32 * x - 32 * q) * 16) >> 4) + kk * qk,
+                    dk + ((32 * q * 16) >> 4) + kk * kk16, id32, kk > 0);
   } else {
     constexpr uint32_t idesc = vc_tc_idesc_bf16(kScoreTile, C::NR);
 #pragma unroll
-    for (int kk = 0; kk < C::KS; ++kk)
-      vc_tc_mma(tmem, vc_tc_desc(k_addr + kk * 256, 128, C::GROUP), vc_tc_desc(q_addr + kk * 256, 128, C::GROUP),
-                idesc, kk > 0);
+    for (int kk = 0; kk < C::KS; ++kk) vc_tc_mma(tmem, dk + kk * kk16, dq + kk * qk, idesc, kk > 0);
   }
 }
 
-// grid (n_ranges, B*Hkv).  PASS 1 writes the range statistics, PASS 2 the scores.
+// Online (max, sum exp2) of one row over 32 tokens first_t .. first_t + 31 (scores s).
+__device__ __forceinline__ void score_fold32(float* s, const ScoreArgs& a, bool masked, int first_t, int last,
+                                             float& m, float& l) {
+  if (masked) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (first_t + j > last) s[j] = -INFINITY;
+  }
+  float mx = s[0];
+#pragma unroll
+  for (int j = 1; j < 32; ++j) mx = fmaxf(mx, s[j]);
+  const float mn = fmaxf(m, mx * a.scale_log2);    // log2 units (scale > 0)
+  if (mn == -INFINITY) return;                     // nothing visible yet
+  float add = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) add += sc_exp2(fmaf(s[j], a.scale_log2, -mn));
+  l = l * sc_exp2(m - mn) + add;
+  m = mn;
+}
+
+// Columns [0, N) of the warp's TMEM lanes from taddr, in one statement.
+template <int N>
+__device__ __forceinline__ void score_ld(uint32_t taddr, float (&v)[N]) {
+  if constexpr (N == 8) vc_tc_ld8(taddr, v);
+  else if constexpr (N == 16) vc_tc_ld16(taddr, v);
+  else if constexpr (N == 24) vc_tc_ld24(taddr, v);
+  else if constexpr (N == 32) vc_tc_ld32(taddr, v);
+  else if constexpr (N == 40) vc_tc_ld40(taddr, v);
+  else if constexpr (N == 48) vc_tc_ld48(taddr, v);
+  else if constexpr (N == 56) vc_tc_ld56(taddr, v);
+  else vc_tc_ld64(taddr, v);
+}
+
+// Pass 2: acc += exp2(s_j * scale - threshold) over N columns from cbase for
+// token t, skipping the rows that do not see t.
+template <int N>
+__device__ __forceinline__ void score_acc(const float (&s)[N], const float* thr_s, int cbase, bool masked, int t,
+                                          const ScoreArgs& a, float& acc) {
+  if (masked) {                                    // row r sees t iff t <= T - n_obs + r % n_obs
+    const int lag = t - (a.T - a.n_obs);           // row r needs r % n_obs >= lag
+    int o = cbase % a.n_obs;
+#pragma unroll
+    for (int jj = 0; jj < N; ++jj) {
+      if (o >= lag) acc += sc_exp2(fmaf(s[jj], a.scale_log2, -thr_s[cbase + jj]));
+      o = o + 1 == a.n_obs ? 0 : o + 1;
+    }
+    return;
+  }
+#pragma unroll
+  for (int jj = 0; jj < N; jj += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(thr_s + cbase + jj);
+    acc += sc_exp2(fmaf(s[jj], a.scale_log2, -v.x));
+    acc += sc_exp2(fmaf(s[jj + 1], a.scale_log2, -v.y));
+    acc += sc_exp2(fmaf(s[jj + 2], a.scale_log2, -v.z));
+    acc += sc_exp2(fmaf(s[jj + 3], a.scale_log2, -v.w));
+  }
+}
+
+// grid = min(SMs, items), one CTA per SM.  PASS 1 writes the range statistics, PASS 2 the scores.
 template <int PASS, int MT, int D>
-__global__ void __launch_bounds__(kScoreThreads, 2) score_pass(ScoreArgs a) {
+__global__ void __launch_bounds__(kScoreThreads, 1)
+    score_pass(ScoreArgs a, const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tq,
+               float* __restrict__ score) {
   using C = ScoreCfg<MT, D>;
   constexpr int NR = C::NR;
-  constexpr uint32_t ncols = PASS == 1 ? C::cols1 : C::cols2;
-  extern __shared__ __align__(16) uint8_t smem[];
+  constexpr int COLS = PASS == 1 ? C::stride1 : C::stride2;    // TMEM buffer stride
+  constexpr int BUFS = PASS == 1 ? C::bufs1 : C::bufs2;
+  constexpr uint32_t NCOLS = sc_pow2_cols(COLS * BUFS);
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  // TMA destinations: 128-byte aligned (kScoreAlign bytes of slack are allocated)
+  uint8_t* smem = smem_raw + ((128u - (vc_smem_addr(smem_raw) & 127u)) & 127u);
   uint8_t* q_s = smem;
   uint8_t* k_s = smem + C::off_k;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::off_bar);
-  uint32_t* slot = reinterpret_cast<uint32_t*>(smem + C::off_bar + 8);
-  const int bh = blockIdx.y, b = bh / a.Hkv, kvh = bh % a.Hkv;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, half = warp >> 2;
-  const int r0 = blockIdx.x * kScoreRange;
-  const int n_tiles = min(kScoreTilesPerRange, (a.T - r0 + kScoreTile - 1) / kScoreTile);
+  float2* red = reinterpret_cast<float2*>(smem + C::off_red);
+  float* tsum = reinterpret_cast<float*>(smem + C::off_sum);
+  float* thr_s = reinterpret_cast<float*>(smem + C::off_thr);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::off_bar);   // [kScoreStages]
+  uint64_t* empty = full + kScoreStages;                              // [kScoreStages]
+  uint64_t* tfull = empty + kScoreStages;                             // [2]
+  uint64_t* tempty = tfull + 2;                                       // [2]
+  uint64_t* qbar = tempty + 2;
+  uint32_t* slot = reinterpret_cast<uint32_t*>(qbar + 1);
+  volatile uint32_t* abort = slot + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, grp = warp >> 2;
+  const int i0 = static_cast<int>(static_cast<long long>(blockIdx.x) * a.n_items / gridDim.x);
+  const int i1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * a.n_items / gridDim.x);
+  int n = 0;                                       // tiles in this CTA's sequence
+  for (int it = i0; it < i1; ++it) {
+    const int r0 = (it % a.n_ranges) * kScoreRange;
+    n += min(kScoreTilesPerRange, (a.T - r0 + kScoreTile - 1) / kScoreTile);
+  }
 
-  if (warp == 0) vc_tc_alloc(slot, ncols);
-  if (threadIdx.x == 32) {
-    vc_mbar_init(bar, 1);
-    vc_fence_mbar_init();
-  }
-  score_load_k<D>(a, bh, r0, k_s);
-  sc_cp_async_commit();
-  if (n_tiles > 1) {
-    score_load_k<D>(a, bh, r0 + kScoreTile, k_s + C::k_bytes);
-    sc_cp_async_commit();
-  }
-  score_load_q<MT, D>(a, b, kvh, q_s);
-  float* red = reinterpret_cast<float*>(smem + C::off_red);
-  if (PASS == 2) {                                 // row thresholds M_r + log2 S_r
-    for (int r = threadIdx.x; r < NR; r += kScoreThreads) {
-      const float2 st = a.rowstat[static_cast<size_t>(bh) * NR + r];
-      red[r] = st.x - log2f(st.y);
+  if (warp == 0) vc_tc_alloc(slot, NCOLS);
+  if (threadIdx.x == kScoreEpiThreads) {
+    for (int s = 0; s < kScoreStages; ++s) {
+      vc_mbar_init(full + s, 1);
+      vc_mbar_init(empty + s, 1);
     }
+    for (int b = 0; b < 2; ++b) {
+      vc_mbar_init(tfull + b, 1);
+      vc_mbar_init(tempty + b, kScoreEpiWarps);
+    }
+    vc_mbar_init(qbar, 1);
+    *abort = 0u;
+    vc_fence_mbar_init();
   }
   vc_tc_fence_before();
   __syncthreads();
   vc_tc_fence_after();
   const uint32_t tmem = *slot;
-  const uint32_t q_addr = vc_smem_addr(q_s), k_addr = vc_smem_addr(k_s);
-  const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
 
-  // pass 1: this thread's row and running (max, sum); NR <= 128: the two warp
-  // halves take 64 tokens of each tile, else half h takes rows 128 h .. 128 h + 127
-  constexpr bool SPLIT = C::NM == 1;
-  const int mm = SPLIT ? 0 : half;
-  const int row = mm * 128 + quarter * 32 + lane;
-  const bool rows_live = mm * 128 + quarter * 32 < NR;      // warp-uniform
-  const int last = a.T - a.n_obs + row % a.n_obs;          // last token the row sees
-  float m = -INFINITY, l = 0.0f;
-  float* tsum = red + NR;                                  // pass 2: [2][2][128]
-  bool alive = true;
-
-  for (int it = 0; it < n_tiles; ++it) {
-    const int t0 = r0 + it * kScoreTile;
-    const uint32_t ks = k_addr + (it & 1) * C::k_bytes;
-    if (it + 1 < n_tiles) sc_cp_async_wait<1>(); else sc_cp_async_wait<0>();
-    vc_fence_proxy_async_smem();                   // this thread's tile writes -> tensor-core reads
-    __syncthreads();                               // tile it complete; TMEM free (previous tile read)
-    if (PASS == 2 && it > 0 && threadIdx.x < kScoreTile) {   // scores of the previous tile
-      const int t = t0 - kScoreTile + threadIdx.x;
-      const float* ts = tsum + ((it - 1) & 1) * 2 * kScoreTile;
-      if (t < a.T) a.score[static_cast<size_t>(bh) * a.T + t] = ts[threadIdx.x] + ts[kScoreTile + threadIdx.x];
+  if (warp == kScoreEpiWarps) {
+    // ---------------- loads and products (one thread)
+    if (lane == 0 && n > 0) {
+      const int G = a.Hq / a.Hkv;
+      const uint32_t q_addr = vc_smem_addr(q_s), k_addr = vc_smem_addr(k_s);
+      auto load_q = [&](int bh) {
+        const int y = ((bh / a.Hkv) * a.Hq + (bh % a.Hkv) * G) * a.n_obs;
+        vc_mbar_arrive_expect_tx(qbar, C::q_bytes);
+        for (int c = 0; c < C::CHUNKS; ++c) sc_tma2(q_s + c * NR * 16, &tq, 8 * c, y, qbar);
+      };
+      auto load_k = [&](const ScoreCursor& cu, int stage) {
+        uint64_t* bar = full + stage;
+        vc_mbar_arrive_expect_tx(bar, C::k_bytes);
+        for (int c = 0; c < C::CHUNKS; ++c)
+          sc_tma3(k_s + stage * C::k_bytes + c * kScoreTile * 16, &tk, 8 * c, cu.t0, cu.bh, bar);
+      };
+      ScoreCursor mc, ld;
+      mc.set(a, i0);
+      ld = mc;
+      int q_bh = mc.bh;
+      uint32_t q_phase = 0;
+      load_q(q_bh);
+      for (int s = 0; s < kScoreStages && s < n; ++s) {
+        load_k(ld, s);
+        ld.next(a);
+      }
+      bool ok = vc_mbar_wait_or_abort(qbar, q_phase, abort, kScoreWaitCycles);
+      q_phase ^= 1u;
+      for (int j = 0; ok && j < n; ++j) {
+        const int s = j % kScoreStages, b = BUFS == 2 ? (j & 1) : 0;
+        if (mc.bh != q_bh) {                       // every earlier product done, then this slice's q
+          ok = vc_mbar_wait_or_abort(empty + (j - 1) % kScoreStages, ((j - 1) / kScoreStages) & 1, abort,
+                                     kScoreWaitCycles);
+          if (!ok) break;
+          q_bh = mc.bh;
+          load_q(q_bh);
+          ok = vc_mbar_wait_or_abort(qbar, q_phase, abort, kScoreWaitCycles);
+          q_phase ^= 1u;
+          if (!ok) break;
+        }
+        ok = vc_mbar_wait_or_abort(full + s, (j / kScoreStages) & 1, abort, kScoreWaitCycles);
+        // the buffer's previous tile p = j - BUFS has been read out (its
+        // epilogue arrives on tempty[p & 1], completing phase p / 2)
+        if (ok && j >= BUFS)
+          ok = vc_mbar_wait_or_abort(tempty + ((j - BUFS) & 1), ((j - BUFS) >> 1) & 1, abort, kScoreWaitCycles);
+        if (!ok) break;
+        vc_tc_fence_after();
+        score_issue<PASS, MT, D>(tmem + b * COLS, q_addr, k_addr + s * C::k_bytes);
+        vc_tc_commit(tfull + (j & 1));
+        vc_tc_commit(empty + s);
+        mc.next(a);
+        // refill the stage of tile j - 1 with tile j + kScoreStages - 1
+        if (j >= 1 && j + kScoreStages - 1 < n) {
+          const int sp = (j - 1) % kScoreStages;
+          ok = vc_mbar_wait_or_abort(empty + sp, ((j - 1) / kScoreStages) & 1, abort, kScoreWaitCycles);
+          if (!ok) break;
+          load_k(ld, sp);
+          ld.next(a);
+        }
+      }
+      if (!ok) *abort = 1u;
     }
-    if (threadIdx.x == 0) {
+  } else {
+    // ---------------- epilogue warps
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    // pass-1 pieces of this warp: A = 32 tokens (32 grp ..) of rows 0-127,
+    // B = rows 128+ (spread block grp, tokens 32 quarter ..; or the second
+    // product, tokens 32 grp ..)
+    const int rowA = quarter * 32 + lane;
+    const bool liveA = quarter * 32 < NR;
+    const int rowB = C::FULL2 ? 128 + quarter * 32 + lane : 128 + grp * 32 + lane;
+    const bool liveB = C::FULL2 ? 128 + quarter * 32 < NR : (grp < C::NE && 128 + grp * 32 < NR);
+    const int colB = C::FULL2 ? 128 + grp * 32 : 128 + (4 * grp + quarter) * 32;
+    const int tokB = C::FULL2 ? grp * 32 : quarter * 32;
+    const int slotB = C::FULL2 ? grp : quarter;
+    const int lastA = a.T - a.n_obs + rowA % a.n_obs, lastB = a.T - a.n_obs + rowB % a.n_obs;
+    float mA = -INFINITY, lA = 0.0f, mB = -INFINITY, lB = 0.0f;
+    int n_items_done = 0, thr_bh = -1;
+    ScoreCursor ec;
+    ec.set(a, i0);
+    for (int j = 0; j < n; ++j) {
+      const int b = j & 1;
+      // after an abort every warp still takes every named barrier below
+      bool live = *abort == 0u && vc_mbar_wait_or_abort(tfull + b, (j >> 1) & 1, abort, kScoreWaitCycles);
+      live = __all_sync(0xffffffffu, live);
       vc_tc_fence_after();
-      score_issue<PASS, MT, D>(tmem, q_addr, ks);
-      vc_tc_commit(bar);
-    }
-    const bool ok = vc_mbar_wait_bounded(bar, static_cast<uint32_t>(it & 1), kScoreWaitCycles);
-    if (!__syncthreads_and(ok)) {
-      if (threadIdx.x == 0) atomicOr(&g_quant_status, VC_DEV_BARRIER_TIMEOUT);
-      alive = false;
-      break;
-    }
-    vc_tc_fence_after();
-    if (it + 2 < n_tiles) {                        // the products read this stage: refill it
-      score_load_k<D>(a, bh, t0 + 2 * kScoreTile, k_s + (it & 1) * C::k_bytes);
-      sc_cp_async_commit();
-    }
-    const bool masked = t0 + kScoreTile > a.T - a.n_obs;     // tile reaches the observation window
-    if (PASS == 1) {
-      if (rows_live) {
-        const int c_lo = SPLIT ? half * 64 : 0;
-#pragma unroll 1
-        for (int c0 = c_lo; c0 < c_lo + (SPLIT ? 64 : 128); c0 += 16) {
-          float s[16];
-          vc_tc_ld16(t_lane + mm * kScoreTile + c0, s);
-          if (masked) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (t0 + c0 + j > last) s[j] = -INFINITY;
+      const uint32_t tb = t_lane + (BUFS == 2 ? b : 0) * COLS;
+      const bool masked = ec.t0 + kScoreTile > a.T - a.n_obs;   // tile reaches the observation window
+      if (PASS == 1) {
+        if (live && liveA && liveB) {              // both pieces in one TMEM round trip
+          float s[64];
+          vc_tc_ld32x2(tb + grp * 32, tb + colB, s);
+          score_fold32(s, a, masked, ec.t0 + grp * 32, lastA, mA, lA);
+          score_fold32(s + 32, a, masked, ec.t0 + tokB, lastB, mB, lB);
+        } else if (live && liveA) {
+          float s[32];
+          vc_tc_ld32(tb + grp * 32, s);
+          score_fold32(s, a, masked, ec.t0 + grp * 32, lastA, mA, lA);
+        }
+      } else {
+        if (ec.bh != thr_bh) {                     // this slice's row thresholds into shared memory
+          vc_bar_sync(1, kScoreEpiThreads);
+          for (int r = threadIdx.x; r < NR; r += kScoreEpiThreads) thr_s[r] = a.thr[static_cast<size_t>(ec.bh) * NR + r];
+          vc_bar_sync(1, kScoreEpiThreads);
+          thr_bh = ec.bh;
+        }
+        float acc = 0.0f;
+        if (live && grp < C::NCG) {
+          const int t = ec.t0 + quarter * 32 + lane;
+          const int c0 = grp * C::CW;
+          constexpr int H1 = C::CW > 32 ? 32 : C::CW, H2 = C::CW - H1;   // at most two TMEM round trips
+          {
+            float s[H1];
+            score_ld<H1>(tb + c0, s);
+            score_acc<H1>(s, thr_s, c0, masked, t, a, acc);
           }
-          float mx = s[0];
-#pragma unroll
-          for (int j = 1; j < 16; ++j) mx = fmaxf(mx, s[j]);
-          const float mn = fmaxf(m, mx * a.scale_log2);      // log2 units (scale > 0)
-          if (mn == -INFINITY) continue;                      // nothing visible yet
-          float add = 0.0f;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) add += sc_exp2(fmaf(s[j], a.scale_log2, -mn));
-          l = l * sc_exp2(m - mn) + add;
-          m = mn;
-        }
-      }
-    } else {
-      constexpr int HALF = NR / 2;
-      constexpr int CH = HALF % 16 == 0 ? 16 : 8;
-      const int t = t0 + quarter * 32 + lane;
-      float acc = 0.0f;
-#pragma unroll 1
-      for (int c0 = half * HALF; c0 < (half + 1) * HALF; c0 += CH) {
-        float s[CH];
-        if constexpr (CH == 16) vc_tc_ld16(t_lane + c0, s); else vc_tc_ld8(t_lane + c0, s);
-        float th[CH];
-#pragma unroll
-        for (int j = 0; j < CH; j += 4) {
-          const float4 v = *reinterpret_cast<const float4*>(red + c0 + j);
-          th[j] = v.x; th[j + 1] = v.y; th[j + 2] = v.z; th[j + 3] = v.w;
-        }
-        if (masked) {
-#pragma unroll
-          for (int j = 0; j < CH; ++j)
-            if (t <= a.T - a.n_obs + (c0 + j) % a.n_obs) acc += sc_exp2(fmaf(s[j], a.scale_log2, -th[j]));
-        } else {
-#pragma unroll
-          for (int j = 0; j < CH; ++j) acc += sc_exp2(fmaf(s[j], a.scale_log2, -th[j]));
-        }
-      }
-      tsum[(it & 1) * 2 * kScoreTile + half * kScoreTile + quarter * 32 + lane] = acc;
-    }
-    vc_tc_fence_before();                          // TMEM reads done before the next tile's products
-  }
-  sc_cp_async_wait<0>();
-  __syncthreads();
-  if (alive) {
-    if (PASS == 1) {
-      float2* st = reinterpret_cast<float2*>(red);                 // [2][NR]
-      float2* out = a.stats + (static_cast<size_t>(bh) * a.n_ranges + blockIdx.x) * NR;
-      if (SPLIT) {
-        if (rows_live && row < NR) st[half * NR + row] = make_float2(m, l);
-        __syncthreads();
-        for (int r = threadIdx.x; r < NR; r += kScoreThreads) {
-          const float2 x = st[r], y = st[NR + r];
-          const float M = fmaxf(x.x, y.x);
-          float S = 0.0f;
-          if (M != -INFINITY) {
-            if (x.x != -INFINITY) S += x.y * exp2f(x.x - M);
-            if (y.x != -INFINITY) S += y.y * exp2f(y.x - M);
+          if constexpr (H2 > 0) {
+            float s[H2];
+            score_ld<H2>(tb + c0 + H1, s);
+            score_acc<H2>(s, thr_s, c0 + H1, masked, t, a, acc);
           }
-          out[r] = make_float2(M, S);
         }
-      } else if (rows_live && row < NR) {
-        out[row] = make_float2(m, l);
+        if (grp < C::NCG) tsum[(j & 1) * 4 * kScoreTile + grp * kScoreTile + quarter * 32 + lane] = acc;
       }
-    } else if (threadIdx.x < kScoreTile && n_tiles > 0) {
-      const int t = r0 + (n_tiles - 1) * kScoreTile + threadIdx.x;
-      const float* ts = tsum + ((n_tiles - 1) & 1) * 2 * kScoreTile;
-      if (t < a.T) a.score[static_cast<size_t>(bh) * a.T + t] = ts[threadIdx.x] + ts[kScoreTile + threadIdx.x];
+      vc_tc_fence_before();                        // TMEM reads done before the buffer is refilled
+      __syncwarp();
+      if (lane == 0) vc_mbar_arrive(tempty + b);
+      if (PASS == 1) {
+        if (ec.tile + 1 == ec.n_tiles) {           // item done: merge the 4 partials of every row
+          float2* rd = red + (n_items_done & 1) * 4 * NR;
+          if (liveA && rowA < NR) rd[grp * NR + rowA] = make_float2(mA, lA);
+          if (liveB && rowB < NR) rd[slotB * NR + rowB] = make_float2(mB, lB);
+          vc_bar_sync(1, kScoreEpiThreads);
+          float2* out = a.stats + static_cast<size_t>(ec.item) * NR;   // item = bh * n_ranges + range
+          for (int r = threadIdx.x; r < NR && *abort == 0u; r += kScoreEpiThreads) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int s = 0; s < 4; ++s) M = fmaxf(M, rd[s * NR + r].x);
+            float S = 0.0f;
+            if (M != -INFINITY) {
+#pragma unroll
+              for (int s = 0; s < 4; ++s) {
+                const float2 v = rd[s * NR + r];
+                if (v.x != -INFINITY) S += v.y * exp2f(v.x - M);
+              }
+            }
+            out[r] = make_float2(M, S);
+          }
+          ++n_items_done;
+          mA = mB = -INFINITY;
+          lA = lB = 0.0f;
+        }
+      } else {
+        vc_bar_sync(1, kScoreEpiThreads);          // the 4 column groups of tile j are in tsum
+        if (threadIdx.x < kScoreTile && *abort == 0u) {
+          const int t = ec.t0 + threadIdx.x;
+          const float* ts = tsum + (j & 1) * 4 * kScoreTile;
+          float x = 0.0f;
+#pragma unroll
+          for (int g = 0; g < C::NCG; ++g) x += ts[g * kScoreTile + threadIdx.x];
+          if (t < a.T) score[static_cast<size_t>(ec.bh) * a.T + t] = x;
+        }
+      }
+      ec.next(a);
     }
   }
   vc_tc_fence_before();
   __syncthreads();
   vc_tc_fence_after();
-  if (warp == 0) vc_tc_dealloc(tmem, ncols);
+  if (threadIdx.x == 0 && *abort != 0u) atomicOr(&g_quant_status, VC_DEV_BARRIER_TIMEOUT);
+  if (warp == 0) vc_tc_dealloc(tmem, NCOLS);
 }
 
-// grid (B*Hkv): per row, (M, 1/S) over the ranges.
+// grid (B*Hkv): per row, the threshold M + log2 S over the ranges.
 __global__ void score_merge(ScoreArgs a, int NR) {
   const int bh = blockIdx.x;
   for (int r = threadIdx.x; r < NR; r += blockDim.x) {
@@ -859,7 +1012,7 @@ __global__ void score_merge(ScoreArgs a, int NR) {
       const float2 v = st[static_cast<size_t>(x) * NR];
       if (v.x != -INFINITY) S += v.y * exp2f(v.x - M);
     }
-    a.rowstat[static_cast<size_t>(bh) * NR + r] = make_float2(M, 1.0f / S);
+    a.thr[static_cast<size_t>(bh) * NR + r] = M + log2f(S);
   }
 }
 
@@ -1122,6 +1275,20 @@ extern "C" vc_status_t vc_quant_kv_append(const vc_shape_t* s, const uint16_t* k
 }
 
 namespace {
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link to
+// the driver library); null when the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
 int score_ranges(int T) { return (T + kScoreRange - 1) / kScoreRange; }
 
 vc_status_t check_score(const vc_shape_t* s, int T, int n_obs, int* NR) {
@@ -1159,23 +1326,48 @@ extern "C" vc_status_t vc_token_score(const vc_shape_t* s, int32_t T, int32_t n_
   if (!workspace || workspace_bytes < need)
     VC_FAIL(VC_ERR_WORKSPACE, "score workspace needs %zu bytes (got %zu)", need, workspace_bytes);
   ScoreArgs a;
-  a.q = q_obs; a.K = K; a.T = T; a.n_obs = n_obs; a.Hq = s->Hq; a.Hkv = s->Hkv;
+  a.T = T; a.n_obs = n_obs; a.Hq = s->Hq; a.Hkv = s->Hkv;
   a.scale_log2 = s->softmax_scale * 1.4426950408889634f;
   a.n_ranges = score_ranges(T);
+  a.n_items = s->B * s->Hkv * a.n_ranges;
   a.stats = static_cast<float2*>(workspace);
-  a.rowstat = a.stats + static_cast<size_t>(s->B) * s->Hkv * a.n_ranges * NR;
-  a.score = score;
+  a.thr = reinterpret_cast<float*>(a.stats + static_cast<size_t>(s->B) * s->Hkv * a.n_ranges * NR);
+  // TMA maps: K as [B*Hkv][T][d] in boxes of 8 channels x 128 tokens (zero
+  // past T), q as [B*Hq*n_obs][d] in boxes of 8 channels x NR rows
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) VC_FAIL(VC_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  CUtensorMap tk, tq;
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(s->d), static_cast<cuuint64_t>(T),
+                                static_cast<cuuint64_t>(s->B) * s->Hkv};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(s->d) * 2, static_cast<cuuint64_t>(T) * s->d * 2};
+    const cuuint32_t box[3] = {8, static_cast<cuuint32_t>(kScoreTile), 1}, es[3] = {1, 1, 1};
+    CUresult r = encode(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(K), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) VC_FAIL(VC_ERR_CUDA, "K tensor map: error %d", static_cast<int>(r));
+    const cuuint64_t qd[2] = {static_cast<cuuint64_t>(s->d), static_cast<cuuint64_t>(s->B) * s->Hq * n_obs};
+    const cuuint64_t qs[1] = {static_cast<cuuint64_t>(s->d) * 2};
+    const cuuint32_t qb[2] = {8, static_cast<cuuint32_t>(NR)};
+    r = encode(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(q_obs), qd, qs, qb, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) VC_FAIL(VC_ERR_CUDA, "q tensor map: error %d", static_cast<int>(r));
+  }
   auto cs = reinterpret_cast<cudaStream_t>(stream);
-  const dim3 grid(a.n_ranges, s->B * s->Hkv);
+  int dev = 0, sms = 0;
+  VC_CUDA_CHECK(cudaGetDevice(&dev));
+  VC_CUDA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const dim3 grid(a.n_items < sms ? a.n_items : sms);
   const int bhs = s->B * s->Hkv;
 #define VC_SCORE_CASE(M, D)                                                                          \
   case M: {                                                                                          \
     const int sm = static_cast<int>(ScoreCfg<M, D>::smem);                                           \
     cudaFuncSetAttribute(score_pass<1, M, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);      \
     cudaFuncSetAttribute(score_pass<2, M, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);      \
-    score_pass<1, M, D><<<grid, kScoreThreads, sm, cs>>>(a);                                         \
+    score_pass<1, M, D><<<grid, kScoreThreads, sm, cs>>>(a, tk, tq, score);                          \
     score_merge<<<bhs, 256, 0, cs>>>(a, NR);                                                         \
-    score_pass<2, M, D><<<grid, kScoreThreads, sm, cs>>>(a);                                         \
+    score_pass<2, M, D><<<grid, kScoreThreads, sm, cs>>>(a, tk, tq, score);                          \
     break;                                                                                           \
   }
 #define VC_SCORE_SWITCH(D)                                                                           \
