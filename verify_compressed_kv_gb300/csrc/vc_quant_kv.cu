@@ -576,11 +576,10 @@ __global__ void unpack_kernel(int T, int T_cap, int d, Packed p, float* K_hat, f
 //   pass 1: D = Q . K_tile^T (rows in TMEM lanes): each thread folds (max,
 //           sum exp2) of one row over 32 tokens of every tile; per item the
 //           4 partials of every row are merged into the range's statistics.
-//           Rows 0-127 are one M = 128 product; rows 128-255 either one more
-//           (NR > 224) or, for NR <= 224, one N = 32 product per 32-row block
-//           and lane quarter q whose A rows start at 128 + 32 x - 32 q, so
-//           block x lands in quarter q's lanes for tokens 32 q .. 32 q + 31
-//           and every quarter (scheduler) gets the same share;
+//           Rows 0-127 are one M = 128 product; for NR > 128 a second one
+//           takes rows NR - 128 .. NR - 1, so its new rows (128 and up) sit in
+//           the highest lane quarters, away from the issuing thread's
+//           scheduler (quarter 0), and no row past NR is read;
 //   merge:  per row, the threshold M + log2 S over all ranges;
 //   pass 2: D = K_tile . Q^T (tokens in TMEM lanes, N = NR): each thread sums
 //           exp2(s_rt - threshold_r) over a quarter of the rows for its
@@ -628,10 +627,10 @@ struct ScoreCfg {
   static constexpr int NR = 16 * MT;               // rows = G * n_obs
   static constexpr int KS = D / 16;                // products along the channel axis
   static constexpr int CHUNKS = D / 8;             // TMA boxes per tile
-  // pass 1 layout of rows 128 .. NR - 1
-  static constexpr bool FULL2 = NR > 128;          // a second M = 128 product over all tokens
-  static constexpr int NE = (NR <= 128 || FULL2) ? 0 : (NR - 128 + 31) / 32;   // spread 32-row blocks
-  static constexpr int cols1 = NR <= 128 ? 128 : FULL2 ? 256 : 128 + 128 * NE;
+  // pass 1: a second M = 128 product for rows NR - 128 .. NR - 1 when NR > 128
+  static constexpr bool TWO = NR > 128;
+  static constexpr int S2 = NR - 128;              // its first row
+  static constexpr int cols1 = TWO ? 256 : 128;
   // TMEM buffer stride (a power of two) and count
   static constexpr int stride1 = cols1 <= 128 ? 128 : cols1 <= 256 ? 256 : 512;
   static constexpr int stride2 = NR <= 32 ? 32 : NR <= 64 ? 64 : NR <= 128 ? 128 : 256;
@@ -640,8 +639,8 @@ struct ScoreCfg {
   // pass 2: NCG column groups of CW rows of q (CW in 16 .. 64, a multiple of 8)
   static constexpr int NCG = NR >= 64 ? 4 : NR / 16;
   static constexpr int CW = NR / NCG;
-  // highest q row a pass-1 product reads (rows past NR feed unused lanes)
-  static constexpr int max_row = FULL2 ? 255 : NE > 0 ? 223 + 32 * NE : 127;
+  // highest q row a pass-1 product reads (for NR < 128, rows past NR feed unused lanes)
+  static constexpr int max_row = TWO ? NR - 1 : 127;
   static constexpr uint32_t q_bytes = NR * D * 2;
   // the last chunk's rows may run past the q tile: keep them inside the region
   static constexpr uint32_t q_reach = (CHUNKS - 1) * NR * 16 + (max_row + 1) * 16;
@@ -654,7 +653,7 @@ struct ScoreCfg {
   static constexpr uint32_t off_bar = off_thr + NR * 4;                   // 13 mbarriers, TMEM base, abort
   static constexpr uint32_t smem = off_bar + 13 * 8 + 8 + 128;        // + alignment slack
   static_assert(smem <= 227 * 1024, "shared memory");
-  static_assert(NE <= 3 && cols1 <= 512, "TMEM plan");
+
 };
 
 __host__ __device__ constexpr uint32_t sc_pow2_cols(int c) {
@@ -693,22 +692,14 @@ __device__ __forceinline__ void score_issue(uint32_t tmem, uint32_t q_addr, uint
   const uint64_t dq = vc_tc_desc(q_addr, QC, 128), dk = vc_tc_desc(k_addr, KC, 128);
   constexpr uint64_t qk = (2 * QC) >> 4, kk16 = (2 * KC) >> 4;     // one 16-channel step
   if (PASS == 1) {
-    constexpr uint32_t id128 = vc_tc_idesc_bf16(128, kScoreTile), id32 = vc_tc_idesc_bf16(128, 32);
+    constexpr uint32_t id128 = vc_tc_idesc_bf16(128, kScoreTile);
 #pragma unroll
     for (int kk = 0; kk < C::KS; ++kk) vc_tc_mma(tmem, dq + kk * qk, dk + kk * kk16, id128, kk > 0);
-    if (C::FULL2) {
+    if constexpr (C::TWO) {
 #pragma unroll
       for (int kk = 0; kk < C::KS; ++kk)
-        vc_tc_mma(tmem + 128, dq + ((128 * 16) >> 4) + kk * qk, dk + kk * kk16, id128, kk > 0);
+        vc_tc_mma(tmem + 128, dq + static_cast<uint64_t>(C::S2) + kk * qk, dk + kk * kk16, id128, kk > 0);
     }
-#pragma unroll
-    for (int x = 0; x < C::NE; ++x)
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int kk = 0; kk < C::KS; ++kk)      // A rows from 128 + 32 x - 32 q; tokens 32 q .. 32 q + 31
-          vc_tc_mma(tmem + 128 + (4 * x + q) * 32, dq + (((128 + 32 * x - 32 * q) * 16) >> 4) + kk * qk,
-                    dk + ((32 * q * 16) >> 4) + kk * kk16, id32, kk > 0);
   } else {
     constexpr uint32_t idesc = vc_tc_idesc_bf16(kScoreTile, C::NR);
 #pragma unroll
@@ -892,16 +883,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   } else {
     // ---------------- epilogue warps
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    // pass-1 pieces of this warp: A = 32 tokens (32 grp ..) of rows 0-127,
-    // B = rows 128+ (spread block grp, tokens 32 quarter ..; or the second
-    // product, tokens 32 grp ..)
+    // pass-1 pieces of this warp, both over tokens 32 grp .. 32 grp + 31 of a
+    // tile: A = row quarter * 32 + lane of the first product, B = row
+    // S2 + quarter * 32 + lane of the second (only its rows >= 128 are new)
     const int rowA = quarter * 32 + lane;
     const bool liveA = quarter * 32 < NR;
-    const int rowB = C::FULL2 ? 128 + quarter * 32 + lane : 128 + grp * 32 + lane;
-    const bool liveB = C::FULL2 ? 128 + quarter * 32 < NR : (grp < C::NE && 128 + grp * 32 < NR);
-    const int colB = C::FULL2 ? 128 + grp * 32 : 128 + (4 * grp + quarter) * 32;
-    const int tokB = C::FULL2 ? grp * 32 : quarter * 32;
-    const int slotB = C::FULL2 ? grp : quarter;
+    const int rowB = C::S2 + quarter * 32 + lane;
+    const bool liveB = C::TWO && C::S2 + quarter * 32 + 31 >= 128;
+    const bool newB = liveB && rowB >= 128;
     const int lastA = a.T - a.n_obs + rowA % a.n_obs, lastB = a.T - a.n_obs + rowB % a.n_obs;
     float mA = -INFINITY, lA = 0.0f, mB = -INFINITY, lB = 0.0f;
     int n_items_done = 0, thr_bh = -1;
@@ -918,9 +907,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (PASS == 1) {
         if (live && liveA && liveB) {              // both pieces in one TMEM round trip
           float s[64];
-          vc_tc_ld32x2(tb + grp * 32, tb + colB, s);
+          vc_tc_ld32x2(tb + grp * 32, tb + 128 + grp * 32, s);
           score_fold32(s, a, masked, ec.t0 + grp * 32, lastA, mA, lA);
-          score_fold32(s + 32, a, masked, ec.t0 + tokB, lastB, mB, lB);
+          score_fold32(s + 32, a, masked, ec.t0 + grp * 32, lastB, mB, lB);
         } else if (live && liveA) {
           float s[32];
           vc_tc_ld32(tb + grp * 32, s);
@@ -958,7 +947,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if (ec.tile + 1 == ec.n_tiles) {           // item done: merge the 4 partials of every row
           float2* rd = red + (n_items_done & 1) * 4 * NR;
           if (liveA && rowA < NR) rd[grp * NR + rowA] = make_float2(mA, lA);
-          if (liveB && rowB < NR) rd[slotB * NR + rowB] = make_float2(mB, lB);
+          if (newB) rd[grp * NR + rowB] = make_float2(mB, lB);
           vc_bar_sync(1, kScoreEpiThreads);
           float2* out = a.stats + static_cast<size_t>(ec.item) * NR;   // item = bh * n_ranges + range
           for (int r = threadIdx.x; r < NR && *abort == 0u; r += kScoreEpiThreads) {
@@ -980,13 +969,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           lA = lB = 0.0f;
         }
       } else {
-        vc_bar_sync(1, kScoreEpiThreads);          // the 4 column groups of tile j are in tsum
-        if (threadIdx.x < kScoreTile && *abort == 0u) {
-          const int t = ec.t0 + threadIdx.x;
-          const float* ts = tsum + (j & 1) * 4 * kScoreTile;
+        vc_bar_sync(2 + quarter, 128);             // the column groups of this quarter's tokens are in tsum
+        if (grp == 0 && *abort == 0u) {
+          const int t = ec.t0 + quarter * 32 + lane;
+          const float* ts = tsum + (j & 1) * 4 * kScoreTile + quarter * 32 + lane;
           float x = 0.0f;
 #pragma unroll
-          for (int g = 0; g < C::NCG; ++g) x += ts[g * kScoreTile + threadIdx.x];
+          for (int g = 0; g < C::NCG; ++g) x += ts[g * kScoreTile];
           if (t < a.T) score[static_cast<size_t>(ec.bh) * a.T + t] = x;
         }
       }
