@@ -160,6 +160,15 @@ __device__ __forceinline__ uint64_t vc_tc_desc(uint32_t saddr, uint32_t lbo, uin
   return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
+// Descriptor of a K-major operand in the 128-byte-swizzled layout: rows of
+// 64 bf16 (128 B), 8-row atoms of 1024 B (1024-byte aligned) in which the
+// 16-byte chunk c of row r sits at chunk c ^ (r % 8), the layout a TMA copy
+// with 128-byte swizzle writes.  lbo = 16 (unused within a row), sbo = 1024,
+// swizzle code 2 (bits 61-63).  A 16-channel step inside the row is +32 bytes
+// on the start address.
+__device__ __forceinline__ uint64_t vc_tc_desc_sw128(uint32_t saddr) {
+  return vc_tc_desc(saddr, 16, 1024) | (2ull << 61);
+}
 // Instruction descriptor of an M x N x 16 kind::f16 product: bf16 A and B,
 // fp32 D, both operands K-major (D format bit 4, A / B formats bits 7 / 10,
 // N >> 3 at bit 17, M >> 4 at bit 24).  M = 128: N a multiple of 16 in

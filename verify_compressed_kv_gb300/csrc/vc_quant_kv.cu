@@ -569,10 +569,11 @@ __global__ void unpack_kernel(int T, int T_cap, int d, Packed p, float* K_hat, f
 //   * 16 epilogue warps read a buffer (warp w: TMEM lane quarter w % 4) while
 //     the tensor cores fill the other.
 // They meet only on mbarriers: stage full (TMA bytes), stage empty and buffer
-// full (tcgen05.commit), buffer empty (16 warp arrivals).  Both operands are
-// K-major core-matrix tiles written by TMA boxes of 8 channels: chunk c of a
-// tile holds 8 channels of every row, 16 bytes per row, so neighbouring 8-row
-// groups are 128 bytes apart and neighbouring chunks rows * 16 bytes apart.
+// full (tcgen05.commit), buffer empty (16 warp arrivals); with up to four
+// TMEM buffers the products run up to three tiles ahead of the epilogue.  Both
+// operands are K-major tiles in the 128-byte-swizzled layout (vc_tc_desc_sw128)
+// written by TMA boxes of 64 channels x all rows: region h of a tile holds
+// channels 64 h .. 64 h + 63, 128 bytes per row.
 //   pass 1: D = Q . K_tile^T (rows in TMEM lanes): each thread folds (max,
 //           sum exp2) of one row over 32 tokens of every tile; per item the
 //           4 partials of every row are merged into the range's statistics.
@@ -591,6 +592,7 @@ constexpr int kScoreTile = 128;
 constexpr int kScoreTilesPerRange = 8;
 constexpr int kScoreRange = kScoreTilesPerRange * kScoreTile;
 constexpr int kScoreStages = 4;
+constexpr int kScoreMaxBufs = 4;                   // TMEM accumulator buffers
 constexpr long long kScoreWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
 
 struct ScoreArgs {
@@ -626,32 +628,33 @@ template <int MT, int D>
 struct ScoreCfg {
   static constexpr int NR = 16 * MT;               // rows = G * n_obs
   static constexpr int KS = D / 16;                // products along the channel axis
-  static constexpr int CHUNKS = D / 8;             // TMA boxes per tile
+  static constexpr int REG = D / 64;               // 64-channel regions (TMA boxes) per tile
   // pass 1: a second M = 128 product for rows NR - 128 .. NR - 1 when NR > 128
   static constexpr bool TWO = NR > 128;
   static constexpr int S2 = NR - 128;              // its first row
   static constexpr int cols1 = TWO ? 256 : 128;
-  // TMEM buffer stride (a power of two) and count
-  static constexpr int stride1 = cols1 <= 128 ? 128 : cols1 <= 256 ? 256 : 512;
-  static constexpr int stride2 = NR <= 32 ? 32 : NR <= 64 ? 64 : NR <= 128 ? 128 : 256;
-  static constexpr int bufs1 = 2 * stride1 <= 512 ? 2 : 1;
-  static constexpr int bufs2 = 2 * stride2 <= 512 ? 2 : 1;
+  // TMEM buffers: stride a multiple of 32 columns (the allocation unit), as
+  // many as fit in 512 columns, at most kScoreMaxBufs
+  static constexpr int stride1 = cols1;
+  static constexpr int stride2 = (NR + 31) / 32 * 32;
+  static constexpr int bufs1 = 512 / stride1 < kScoreMaxBufs ? 512 / stride1 : kScoreMaxBufs;
+  static constexpr int bufs2 = 512 / stride2 < kScoreMaxBufs ? 512 / stride2 : kScoreMaxBufs;
   // pass 2: NCG column groups of CW rows of q (CW in 16 .. 64, a multiple of 8)
   static constexpr int NCG = NR >= 64 ? 4 : NR / 16;
   static constexpr int CW = NR / NCG;
   // highest q row a pass-1 product reads (for NR < 128, rows past NR feed unused lanes)
   static constexpr int max_row = TWO ? NR - 1 : 127;
   static constexpr uint32_t q_bytes = NR * D * 2;
-  // the last chunk's rows may run past the q tile: keep them inside the region
-  static constexpr uint32_t q_reach = (CHUNKS - 1) * NR * 16 + (max_row + 1) * 16;
+  // the last region's rows may run past the q tile: keep them inside the q region
+  static constexpr uint32_t q_reach = (REG - 1) * NR * 128 + (max_row + 1) * 128;
   static constexpr uint32_t q_region = ((q_reach > q_bytes ? q_reach : q_bytes) + 1023) / 1024 * 1024;
   static constexpr uint32_t k_bytes = kScoreTile * D * 2;                  // one K stage
   static constexpr uint32_t off_k = q_region;
   static constexpr uint32_t off_red = off_k + kScoreStages * k_bytes;     // pass 1: [2][4][NR] float2
   static constexpr uint32_t off_sum = off_red + 2 * 4 * NR * 8;           // pass 2: [2][4][128] float
   static constexpr uint32_t off_thr = off_sum + 2 * 4 * kScoreTile * 4;   // pass 2: [NR] float
-  static constexpr uint32_t off_bar = off_thr + NR * 4;                   // 13 mbarriers, TMEM base, abort
-  static constexpr uint32_t smem = off_bar + 13 * 8 + 8 + 128;        // + alignment slack
+  static constexpr uint32_t off_bar = off_thr + NR * 4;                   // 17 mbarriers, TMEM base, abort
+  static constexpr uint32_t smem = off_bar + 17 * 8 + 8 + 1024;       // + alignment slack
   static_assert(smem <= 227 * 1024, "shared memory");
 
 };
@@ -683,27 +686,33 @@ struct ScoreCursor {
 // The products of one tile into TMEM columns from `tmem`, issued by one
 // thread.  A descriptor moves with its start address: desc + (bytes >> 4)
 // (the address field cannot carry: shared addresses stay below 256 KB).
-//   K tile: chunk stride 128 * 16 = 2048 B, 8-row group stride 128 B;
-//   q:      chunk stride NR * 16 B,       8-row group stride 128 B.
+// Channel step kk: region kk / 4 (q: NR * 128 B, K tile: 128 * 128 B apart),
+// +32 B per step inside the region; row r: +128 r B.
+template <int PASS, int MT, int D>
+__device__ __forceinline__ uint64_t score_koff(int kk, uint32_t region_bytes) {
+  return static_cast<uint64_t>(((kk >> 2) * region_bytes + (kk & 3) * 32) >> 4);
+}
 template <int PASS, int MT, int D>
 __device__ __forceinline__ void score_issue(uint32_t tmem, uint32_t q_addr, uint32_t k_addr) {
   using C = ScoreCfg<MT, D>;
-  constexpr uint32_t QC = C::NR * 16, KC = kScoreTile * 16;
-  const uint64_t dq = vc_tc_desc(q_addr, QC, 128), dk = vc_tc_desc(k_addr, KC, 128);
-  constexpr uint64_t qk = (2 * QC) >> 4, kk16 = (2 * KC) >> 4;     // one 16-channel step
+  constexpr uint32_t QR = C::NR * 128, KR = kScoreTile * 128;
+  const uint64_t dq = vc_tc_desc_sw128(q_addr), dk = vc_tc_desc_sw128(k_addr);
   if (PASS == 1) {
     constexpr uint32_t id128 = vc_tc_idesc_bf16(128, kScoreTile);
 #pragma unroll
-    for (int kk = 0; kk < C::KS; ++kk) vc_tc_mma(tmem, dq + kk * qk, dk + kk * kk16, id128, kk > 0);
+    for (int kk = 0; kk < C::KS; ++kk)
+      vc_tc_mma(tmem, dq + score_koff<PASS, MT, D>(kk, QR), dk + score_koff<PASS, MT, D>(kk, KR), id128, kk > 0);
     if constexpr (C::TWO) {
 #pragma unroll
       for (int kk = 0; kk < C::KS; ++kk)
-        vc_tc_mma(tmem + 128, dq + static_cast<uint64_t>(C::S2) + kk * qk, dk + kk * kk16, id128, kk > 0);
+        vc_tc_mma(tmem + 128, dq + ((C::S2 * 128) >> 4) + score_koff<PASS, MT, D>(kk, QR),
+                  dk + score_koff<PASS, MT, D>(kk, KR), id128, kk > 0);
     }
   } else {
     constexpr uint32_t idesc = vc_tc_idesc_bf16(kScoreTile, C::NR);
 #pragma unroll
-    for (int kk = 0; kk < C::KS; ++kk) vc_tc_mma(tmem, dk + kk * kk16, dq + kk * qk, idesc, kk > 0);
+    for (int kk = 0; kk < C::KS; ++kk)
+      vc_tc_mma(tmem, dk + score_koff<PASS, MT, D>(kk, KR), dq + score_koff<PASS, MT, D>(kk, QR), idesc, kk > 0);
   }
 }
 
@@ -776,8 +785,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   constexpr int BUFS = PASS == 1 ? C::bufs1 : C::bufs2;
   constexpr uint32_t NCOLS = sc_pow2_cols(COLS * BUFS);
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  // TMA destinations: 128-byte aligned (kScoreAlign bytes of slack are allocated)
-  uint8_t* smem = smem_raw + ((128u - (vc_smem_addr(smem_raw) & 127u)) & 127u);
+  // swizzled tiles: 1024-byte aligned (1024 bytes of slack are allocated)
+  uint8_t* smem = smem_raw + ((1024u - (vc_smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* q_s = smem;
   uint8_t* k_s = smem + C::off_k;
   float2* red = reinterpret_cast<float2*>(smem + C::off_red);
@@ -785,9 +794,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   float* thr_s = reinterpret_cast<float*>(smem + C::off_thr);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::off_bar);   // [kScoreStages]
   uint64_t* empty = full + kScoreStages;                              // [kScoreStages]
-  uint64_t* tfull = empty + kScoreStages;                             // [2]
-  uint64_t* tempty = tfull + 2;                                       // [2]
-  uint64_t* qbar = tempty + 2;
+  uint64_t* tfull = empty + kScoreStages;                             // [kScoreMaxBufs]
+  uint64_t* tempty = tfull + kScoreMaxBufs;                           // [kScoreMaxBufs]
+  uint64_t* qbar = tempty + kScoreMaxBufs;
   uint32_t* slot = reinterpret_cast<uint32_t*>(qbar + 1);
   volatile uint32_t* abort = slot + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, grp = warp >> 2;
@@ -805,7 +814,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       vc_mbar_init(full + s, 1);
       vc_mbar_init(empty + s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kScoreMaxBufs; ++b) {
       vc_mbar_init(tfull + b, 1);
       vc_mbar_init(tempty + b, kScoreEpiWarps);
     }
@@ -826,13 +835,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       auto load_q = [&](int bh) {
         const int y = ((bh / a.Hkv) * a.Hq + (bh % a.Hkv) * G) * a.n_obs;
         vc_mbar_arrive_expect_tx(qbar, C::q_bytes);
-        for (int c = 0; c < C::CHUNKS; ++c) sc_tma2(q_s + c * NR * 16, &tq, 8 * c, y, qbar);
+        for (int h = 0; h < C::REG; ++h) sc_tma2(q_s + h * NR * 128, &tq, 64 * h, y, qbar);
       };
       auto load_k = [&](const ScoreCursor& cu, int stage) {
         uint64_t* bar = full + stage;
         vc_mbar_arrive_expect_tx(bar, C::k_bytes);
-        for (int c = 0; c < C::CHUNKS; ++c)
-          sc_tma3(k_s + stage * C::k_bytes + c * kScoreTile * 16, &tk, 8 * c, cu.t0, cu.bh, bar);
+        for (int h = 0; h < C::REG; ++h)
+          sc_tma3(k_s + stage * C::k_bytes + h * kScoreTile * 128, &tk, 64 * h, cu.t0, cu.bh, bar);
       };
       ScoreCursor mc, ld;
       mc.set(a, i0);
@@ -847,7 +856,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       bool ok = vc_mbar_wait_or_abort(qbar, q_phase, abort, kScoreWaitCycles);
       q_phase ^= 1u;
       for (int j = 0; ok && j < n; ++j) {
-        const int s = j % kScoreStages, b = BUFS == 2 ? (j & 1) : 0;
+        const int s = j % kScoreStages, b = j % BUFS;
         if (mc.bh != q_bh) {                       // every earlier product done, then this slice's q
           ok = vc_mbar_wait_or_abort(empty + (j - 1) % kScoreStages, ((j - 1) / kScoreStages) & 1, abort,
                                      kScoreWaitCycles);
@@ -860,13 +869,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         ok = vc_mbar_wait_or_abort(full + s, (j / kScoreStages) & 1, abort, kScoreWaitCycles);
         // the buffer's previous tile p = j - BUFS has been read out (its
-        // epilogue arrives on tempty[p & 1], completing phase p / 2)
+        // epilogue completes phase p / BUFS of tempty[b])
         if (ok && j >= BUFS)
-          ok = vc_mbar_wait_or_abort(tempty + ((j - BUFS) & 1), ((j - BUFS) >> 1) & 1, abort, kScoreWaitCycles);
+          ok = vc_mbar_wait_or_abort(tempty + b, ((j - BUFS) / BUFS) & 1, abort, kScoreWaitCycles);
         if (!ok) break;
         vc_tc_fence_after();
         score_issue<PASS, MT, D>(tmem + b * COLS, q_addr, k_addr + s * C::k_bytes);
-        vc_tc_commit(tfull + (j & 1));
+        vc_tc_commit(tfull + b);
         vc_tc_commit(empty + s);
         mc.next(a);
         // refill the stage of tile j - 1 with tile j + kScoreStages - 1
@@ -897,12 +906,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     ScoreCursor ec;
     ec.set(a, i0);
     for (int j = 0; j < n; ++j) {
-      const int b = j & 1;
+      const int b = j % BUFS;
       // after an abort every warp still takes every named barrier below
-      bool live = *abort == 0u && vc_mbar_wait_or_abort(tfull + b, (j >> 1) & 1, abort, kScoreWaitCycles);
+      bool live = *abort == 0u && vc_mbar_wait_or_abort(tfull + b, (j / BUFS) & 1, abort, kScoreWaitCycles);
       live = __all_sync(0xffffffffu, live);
       vc_tc_fence_after();
-      const uint32_t tb = t_lane + (BUFS == 2 ? b : 0) * COLS;
+      const uint32_t tb = t_lane + b * COLS;
       const bool masked = ec.t0 + kScoreTile > a.T - a.n_obs;   // tile reaches the observation window
       if (PASS == 1) {
         if (live && liveA && liveB) {              // both pieces in one TMEM round trip
@@ -1321,8 +1330,8 @@ extern "C" vc_status_t vc_token_score(const vc_shape_t* s, int32_t T, int32_t n_
   a.n_items = s->B * s->Hkv * a.n_ranges;
   a.stats = static_cast<float2*>(workspace);
   a.thr = reinterpret_cast<float*>(a.stats + static_cast<size_t>(s->B) * s->Hkv * a.n_ranges * NR);
-  // TMA maps: K as [B*Hkv][T][d] in boxes of 8 channels x 128 tokens (zero
-  // past T), q as [B*Hq*n_obs][d] in boxes of 8 channels x NR rows
+  // TMA maps (128-byte swizzle): K as [B*Hkv][T][d] in boxes of 64 channels x
+  // 128 tokens (zero past T), q as [B*Hq*n_obs][d] in boxes of 64 channels x NR rows
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) VC_FAIL(VC_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   CUtensorMap tk, tq;
@@ -1330,16 +1339,16 @@ extern "C" vc_status_t vc_token_score(const vc_shape_t* s, int32_t T, int32_t n_
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(s->d), static_cast<cuuint64_t>(T),
                                 static_cast<cuuint64_t>(s->B) * s->Hkv};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(s->d) * 2, static_cast<cuuint64_t>(T) * s->d * 2};
-    const cuuint32_t box[3] = {8, static_cast<cuuint32_t>(kScoreTile), 1}, es[3] = {1, 1, 1};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kScoreTile), 1}, es[3] = {1, 1, 1};
     CUresult r = encode(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(K), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) VC_FAIL(VC_ERR_CUDA, "K tensor map: error %d", static_cast<int>(r));
     const cuuint64_t qd[2] = {static_cast<cuuint64_t>(s->d), static_cast<cuuint64_t>(s->B) * s->Hq * n_obs};
     const cuuint64_t qs[1] = {static_cast<cuuint64_t>(s->d) * 2};
-    const cuuint32_t qb[2] = {8, static_cast<cuuint32_t>(NR)};
+    const cuuint32_t qb[2] = {64, static_cast<cuuint32_t>(NR)};
     r = encode(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(q_obs), qd, qs, qb, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) VC_FAIL(VC_ERR_CUDA, "q tensor map: error %d", static_cast<int>(r));
   }
