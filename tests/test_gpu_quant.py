@@ -275,6 +275,23 @@ def test_token_score(vc, B, Hq, Hkv, T, d, n_obs):
     assert np.allclose(got.sum(-1), (Hq // Hkv) * n_obs, rtol=1e-4)
 
 
+def test_token_score_full_size_sampled(vc):
+    """Qwen-32B-shaped prompt at full size (B16 Hq40 Hkv8 T65536 d128, 32
+    observation queries), scored in one call with the launch the bench times (one
+    persistent CTA per SM over 8192 items); sampled (request, KV head) slices
+    against the fp64 oracle, with the tolerance of test_token_score."""
+    w = synth.get("qwen")
+    K, _ = synth.kv(w)
+    q = synth.q_obs(w, n_obs=32)
+    got = gpu_scores(vc, q, K, 1.0, n_obs=32)
+    G = w.Hq // w.Hkv
+    for (b, h) in [(0, 0), (7, 3), (w.B - 1, w.Hkv - 1)]:
+        want = tokendrop.token_scores(q[b:b + 1, h * G:(h + 1) * G], K[b:b + 1, h:h + 1], 1.0)[0, 0]
+        err = np.abs(got[b, h] - want)
+        assert np.all(err <= 1e-3 * want + 1e-7 * G * 32), (b, h, err.max())
+        assert np.isclose(got[b, h].sum(), G * 32, rtol=1e-4)
+
+
 def check_selection(idx, pooled, keep, keep_last):
     """Kept set S valid: the last tokens present, ascending, and every kept candidate
     scores at least as high as every dropped one, up to 1e-4 * max(pooled): the
