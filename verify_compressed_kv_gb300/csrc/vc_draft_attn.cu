@@ -448,7 +448,6 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
                                             WarpStateT<D>& st, int lane) {
   constexpr int KS = D / 16, NT = D / 8, NCG = D / 32, WPL = D * BITS / 32;
   const int gid = lane >> 2, tig = lane & 3;
-  const bool lo_q = gid >= 4;                   // Q'^T column gid: the remainder part of head gid & 3
   const bool lo_p = tig >= 2;                   // P block columns 2 tig (+1): remainder parts
   const int h0 = 2 * (tig & 1);
   // ---------------- S^T = codes . Q'^T
@@ -469,10 +468,9 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int ks = 2 * kq + h;
-      uint32_t hi0, lo0, hi1, lo1;
-      split_mul(u2h(qf[ks][0]), u2h(sv[2 * h]), hi0, lo0);
-      split_mul(u2h(qf[ks][1]), u2h(sv[2 * h + 1]), hi1, lo1);
-      const uint32_t qb0 = lo_q ? lo0 : hi0, qb1 = lo_q ? lo1 : hi1;
+      // Q'^T columns gid and gid + 4 both carry head gid & 3 (fp16 f q s)
+      const uint32_t qb0 = h2u(__hmul2(u2h(qf[ks][0]), u2h(sv[2 * h])));
+      const uint32_t qb1 = h2u(__hmul2(u2h(qf[ks][1]), u2h(sv[2 * h + 1])));
       mma16816(cb, qf[ks][0], 0u, qf[ks][1], 0u, h2u(__hmul2(u2h(zv[2 * h]), u2h(bias_mul0))),
                h2u(__hmul2(u2h(zv[2 * h + 1]), u2h(bias_mul1))));
 #pragma unroll
@@ -487,12 +485,9 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
   // bias of head h: row h of the bias product, columns 0 (q.z) and 1 (-q.f s) in lane 4 h
   const float cbs = cb[0] + cb[1];
   const float bias[2] = {__shfl_sync(0xffffffffu, cbs, 4 * h0), __shfl_sync(0xffffffffu, cbs, 4 * h0 + 4)};
-  // hi + lo columns; y[mt][2 half + hh] = score of token 4 gid + 2 mt + half, head h0 + hh
-  float y[2][4];
-#pragma unroll
-  for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) y[mt][e] = c[mt][e] + __shfl_xor_sync(0xffffffffu, c[mt][e], 2);
+  // y[mt][2 half + hh] = score of token 4 gid + 2 mt + half, head h0 + hh (columns
+  // 2 tig, 2 tig + 1 hold heads h0, h0 + 1 in both column halves)
+  float (&y)[2][4] = c;
   // ---------------- online softmax, one state per head
   float mx[2];
   bool need[2];
@@ -529,8 +524,8 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
     for (int k = 0; k < 4; ++k) st.oz[k] *= a_oz;
   }
   const float kk[2] = {fmaf(bias[0], cs, -st.m[0]), fmaf(bias[1], cs, -st.m[1])};
-  // weights times f_r (r = token parity = half), split into fp16 (hi, lo); block j = 2 mt + half
-  uint32_t ph[4], pl[4];
+  // weights times f_r (r = token parity = half) in fp16; block j = 2 mt + half
+  uint32_t ph[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int mt = j >> 1, half = j & 1;
@@ -544,16 +539,13 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
       st.l0[0] += p0;
       st.l0[1] += p1;
     }
-    const __half2 h = __floats2half2_rn(p0, p1);
-    const float2 hf = __half22float2(h);
-    ph[j] = h2u(h);
-    pl[j] = h2u(__floats2half2_rn(p0 - hf.x, p1 - hf.y));
+    ph[j] = h2u(__floats2half2_rn(p0, p1));
   }
-  // ---------------- correction: A = P' blocks transposed (rows = P' columns), B = meta columns
+  // ---------------- correction: A = P' blocks transposed (rows = P' columns; rows 4-7 zero), B = meta columns
   {
     uint32_t pu[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) pu[j] = movmatrix_t(lo_p ? pl[j] : ph[j]);
+    for (int j = 0; j < 4; ++j) pu[j] = movmatrix_t(lo_p ? 0u : ph[j]);
     const uint4 r4 = *reinterpret_cast<const uint4*>(vsz_g + zcol_off + 8 * tig);
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
@@ -576,10 +568,7 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
     for (int j = 0; j < 4; ++j) {
       uint32_t sv2;
       asm("prmt.b32 %0, %1, %1, %2;" : "=r"(sv2) : "r"(sw[j]), "r"(sel));   // (sv, sv) of token 4 gid + j
-      const __half2 x = u2h(ph[j]), sc = u2h(sv2);
-      const __half2 h = __hmul2(x, sc);
-      const __half2 l = __hfma2(u2h(pl[j]), sc, __hfma2(x, sc, __hneg2(h)));
-      pb[j] = movmatrix_t(h2u(lo_p ? l : h));
+      pb[j] = movmatrix_t(lo_p ? 0u : h2u(__hmul2(u2h(ph[j]), u2h(sv2))));   // every lane transposes
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
