@@ -156,11 +156,13 @@ vc_status_t vc_quant_kv_append(const vc_shape_t* s, const uint16_t* k_new, const
  * the n_obs observation queries i of softmax_i(t), where query i sits at
  * position T - n_obs + i and sees keys 0 .. T - n_obs + i.
  * q_obs bf16 [B, Hq, n_obs, d], K bf16 [B, Hkv, T, d] -> score fp32
- * [B, Hkv, T] (all device).  Logits on the tensor cores (bf16 products,
- * exact, summed in fp32; softmax scale applied in fp32), softmax weights and
+ * [B, Hkv, T] (all device; q_obs and K 16-byte aligned, VC_ERR_INVALID_ARG
+ * otherwise).  Logits on the tcgen05 tensor cores (bf16 products, exact,
+ * summed in fp32 in TMEM; softmax scale applied in fp32), softmax weights and
  * their sums in fp32.  n_obs <= 32, G * n_obs in 16 * {1, 2, 4, 6, .., 16},
  * T >= n_obs.  Workspace: per (b, KV head) the (max, sum) of every
- * 1024-token range and the merged row statistics.
+ * 1024-token range and one threshold M + log2 S per row.  A driver without
+ * cuTensorMapEncodeTiled gives VC_ERR_CUDA.
  * Reads B, Hq, Hkv, d, softmax_scale. */
 vc_status_t vc_token_score_workspace_size(const vc_shape_t* s, int32_t T, int32_t n_obs,
                                           size_t* bytes);

@@ -24,8 +24,10 @@
 //     the softmax weights, each fold carried as an fp16 (hi, lo) pair so the
 //     products keep ~22 bits, and the zero points enter through two narrow
 //     correction products (group_mma below); with G = 4 the roles swap
-//     (codes as the A operand, the heads' (hi, lo) parts as the 8 columns,
-//     group_mma_t), which halves the QK and PV products;
+//     (codes as the A operand, the 4 heads as the 8 columns, group_mma_t),
+//     which halves the QK and PV products, and the folds are single fp16
+//     values (the draft is lossy by design: fp16 rounding of the folded
+//     operands sits far below the codes' own error);
 //   * at the end of a segment the warps are merged (log-sum-exp) into one
 //     partial per query head; the last CTA to finish a (request, KV head)
 //     (arrival counter in the workspace, reset by that CTA) merges all its
