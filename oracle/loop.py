@@ -32,6 +32,7 @@ import numpy as np
 
 from . import kivi
 from .accept import accept as accept_rule
+from .attention import round_bf16
 
 
 class DecoderModel(Protocol):
@@ -94,6 +95,22 @@ def commit_to_draft_cache(dc: DraftCache, k_new, v_new):
         dc.tail_v = dc.tail_v[:, 32:]
 
 
+def committed_kv(vk, vv, n: int, draft_k=None, draft_v=None):
+    """The K/V a round appends to one layer's draft cache ([Hkv, n+1, d] each).
+
+    They are the verify pass's exact K/V of t_last, d_0 .. d_{n-1} (vk/vv
+    [k+1, Hkv, d]); the draft pass's approximate K/V of the same tokens
+    (draft_k/draft_v, [Hkv, d] per draft step) are discarded.  The pages
+    leave the choice open (Core Algorithm: the next round "repeats from the
+    last accepted token"); exact K/V keep the draft cache equal to the
+    compression of the full cache.
+    """
+    del draft_k, draft_v
+    k = np.ascontiguousarray(np.asarray(vk)[:n + 1].transpose(1, 0, 2))
+    v = np.ascontiguousarray(np.asarray(vv)[:n + 1].transpose(1, 0, 2))
+    return k, v
+
+
 def _bf16_to_f64(b):
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
 
@@ -135,9 +152,17 @@ class FullKV:
         return 0 if self.K[0] is None else self.K[0].shape[1]
 
 
-def full_attention_fn(store: FullKV, scale: float):
-    """Attention of new tokens over the full cache + themselves (causal)."""
+def full_attention_fn(store: FullKV, scale: float, bf16_out: bool = False):
+    """Attention of new tokens over the full cache + themselves (causal).
+
+    bf16_out rounds the fp64 result to bf16 (nearest, ties to even), the
+    precision in which the attention kernels hand their output back.
+    """
     def attend(layer, q, k, v):
+        out = _attend_full(layer, q, k, v)
+        return round_bf16(out) if bf16_out else out
+
+    def _attend_full(layer, q, k, v):
         qf = _bf16_to_f64(q)
         T = store.length()
         Ks = _bf16_to_f64(k).transpose(1, 0, 2)
@@ -150,16 +175,18 @@ def full_attention_fn(store: FullKV, scale: float):
     return attend
 
 
-def greedy_decode(model: DecoderModel, prompt, n_new: int, scale: float):
+def greedy_decode(model: DecoderModel, prompt, n_new: int, scale: float, bf16_out: bool = False):
     """Plain greedy decoding with full-KV attention: the reference stream."""
     store = FullKV(model.n_layers)
-    logits, ks, vs = model.forward(np.asarray(prompt), np.arange(len(prompt)), full_attention_fn(store, scale))
+    logits, ks, vs = model.forward(np.asarray(prompt), np.arange(len(prompt)),
+                                   full_attention_fn(store, scale, bf16_out))
     for l in range(model.n_layers):
         store.append(l, ks[l], vs[l])
     out = [int(np.argmax(logits[-1]))]
     while len(out) < n_new:
         pos = store.length()
-        logits, ks, vs = model.forward(np.asarray([out[-1]]), np.asarray([pos]), full_attention_fn(store, scale))
+        logits, ks, vs = model.forward(np.asarray([out[-1]]), np.asarray([pos]),
+                                       full_attention_fn(store, scale, bf16_out))
         for l in range(model.n_layers):
             store.append(l, ks[l], vs[l])
         out.append(int(np.argmax(logits[-1])))
@@ -168,14 +195,17 @@ def greedy_decode(model: DecoderModel, prompt, n_new: int, scale: float):
 
 def speculative_decode(model: DecoderModel, prompt, n_new: int, k: int, bits: int,
                        scale: float, drafter: str = "compressed", rng=None,
-                       reference: list | None = None, compress: Callable | None = None):
+                       reference: list | None = None, compress: Callable | None = None,
+                       on_commit: Callable | None = None):
     """Draft with the compressed cache, verify with the full one, accept.
 
     drafter: "compressed" (the method), "wrong" (every draft is wrong),
     "perfect" (drafts copied from ``reference``), "random".  ``compress``
     optionally inserts a token-dropping step before quantisation: it maps
     (layer, K [Hkv,T,d], V, prompt queries [T,Hq,d]) to the (K, V) the draft
-    cache is built from.  Returns (tokens, accepted lengths per round).
+    cache is built from.  ``on_commit(store, caches)``, if given, sees the
+    full cache and every layer's draft cache after each round's commit.
+    Returns (tokens, accepted lengths per round).
     """
     L = model.n_layers
     store = FullKV(L)
@@ -244,9 +274,10 @@ def speculative_decode(model: DecoderModel, prompt, n_new: int, k: int, bits: in
         # ---- commit the exact K/V of t_last, d_0 .. d_{n-1}
         for l in range(L):
             store.append(l, vks[l][:n + 1], vvs[l][:n + 1])
-            kk = np.asarray(vks[l][:n + 1]).transpose(1, 0, 2)
-            vv = np.asarray(vvs[l][:n + 1]).transpose(1, 0, 2)
+            kk, vv = committed_kv(vks[l], vvs[l], n, extra_k[l], extra_v[l])
             commit_to_draft_cache(caches[l], kk, vv)
+        if on_commit is not None:
+            on_commit(store, caches)
         out.extend(drafts[:n])
         out.append(int(nxt[0]))
     return out[:n_new], accepted

@@ -7,8 +7,9 @@ verification over the full KV streamed from pinned host memory, accept,
 commit) and must reproduce, token for token, plain greedy decoding through
 the same verify kernel with k = 0, for every compressor (int4, int2, int8,
 token drop + int4 or int2) and for drafters of any quality.  The GPU greedy
-stream is also compared with the oracle's fp64 greedy stream; a difference
-there is allowed only at a numeric near-tie of the oracle's logits.
+stream is also compared with the oracle's greedy stream (fp64 attention
+rounded to bf16); a difference there is allowed only at a numeric tie
+(top-2 margin below 1e-3) of the oracle's logits.
 """
 import numpy as np
 import pytest
@@ -147,18 +148,23 @@ def test_lossless_with_a_draft_length_per_round(setup, policy):
 
 
 def test_gpu_greedy_matches_oracle_greedy(setup):
-    """GPU (fp32 accumulate, bf16 attention output) vs oracle (fp64): equal up to
-    a numeric near-tie of the oracle's top-2 logits at the first difference."""
+    """GPU (fp32 accumulate, bf16 attention output) vs oracle (fp64 attention
+    rounded to bf16, the output precision of the kernels): equal, except at a
+    numeric tie, a top-2 margin of the oracle's logits below 1e-3 at the first
+    difference.  With both outputs on the bf16 grid the two differ only where
+    the fp32 sum lands on the other side of a bf16 rounding boundary (one bf16
+    ulp in an element now and then), which moves the tiny model's logits by
+    ~1e-5, two orders below the tie line."""
     S = setup
     m = S["m"]
-    ref_cpu = oloop.greedy_decode(m, S["prompt"], 64, m.scale)
+    ref_cpu = oloop.greedy_decode(m, S["prompt"], 64, m.scale, bf16_out=True)
     gpu = S["ref"][:64]
     if gpu != ref_cpu:
         i = next(i for i, (a, b) in enumerate(zip(gpu, ref_cpu)) if a != b)
         # margin of the oracle's logits at step i
         store = oloop.FullKV(m.n_layers)
-        full = oloop.full_attention_fn(store, m.scale)
+        full = oloop.full_attention_fn(store, m.scale, bf16_out=True)
         toks = list(S["prompt"]) + ref_cpu[:i]
         lg, _, _ = m.forward(np.asarray(toks), np.arange(len(toks)), full)
         top = np.sort(lg[-1])[-2:]
-        assert top[1] - top[0] < 1e-2, f"diverged at {i} with oracle margin {top[1] - top[0]}"
+        assert top[1] - top[0] < 1e-3, f"diverged at {i} with oracle margin {top[1] - top[0]}"
