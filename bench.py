@@ -236,6 +236,19 @@ def algorithmic_draft_bytes(w, P):
     return w.B * w.Hkv * P * per_tok + 2 * w.B * w.Hq * w.d * 2
 
 
+def bench_config(w, args, world):
+    """The bench line's `config` (the same dict in both arms): the workload, its
+    schedule, and how the timed region stays clear of L2."""
+    P = w.T_keep if w.name == "qwen" else w.T
+    packed_mib = algorithmic_draft_bytes(w, P) * w.layers // 2 ** 20
+    full_mib = 2 * w.B * w.Hkv * w.T * w.d * 2 * w.layers // 2 ** 20
+    return {"workload": workload_name(w), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "T": w.T, "k": w.k,
+            "bits": w.bits, "layers": w.layers, "groups": w.groups, "V": w.V, "chunk": w.C,
+            "schedule": "single" if w.groups == 1 else args.schedule,
+            "l2": "inputs larger than L2 (packed cache %d MiB, full KV %d MiB per round)" % (packed_mib, full_mib),
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
 def source_hash(path):
     """Hash of a kernel source's code: comments and whitespace removed, so edits to
     the comments keep a capture valid and any change to the code does not."""
@@ -323,28 +336,33 @@ def time_token_drop(w, shape, Kd, Vd, device, cs):
     Vo = torch.empty_like(Ko)
     t_gat = time_kernel(lambda: vc.vc_gather_kv(shape, w.T, keep, idx, Kd, Vd, Ko, Vo, cs), cs, reps=10)
     gat_bytes = 2 * 2 * w.B * w.Hkv * keep * w.d * 2
-    # logits on the tensor cores (mma.sync bf16): against the measured dense bf16 peak
-    return {"a3_token_score": {"ms": t_score, "tflops": flops / (t_score / 1e3) / 1e12, "bound": "tensor",
-                               "peak_tflops": peaks["bf16_tflops"],
-                               "frac": flops / (t_score / 1e3) / 1e12 / peaks["bf16_tflops"]},
+    # K is read once per pass (2 bytes a channel), the scores written once: at
+    # 32*G flops per byte the score sits below the bf16 ridge, so HBM bounds it
+    score_bytes = 2 * w.B * w.Hkv * w.T * w.d * 2 + w.B * w.Hkv * w.T * 4
+    return {"a3_token_score": dict(intensity_row(t_score, flops, score_bytes, peaks), engine="tcgen05 bf16"),
             "a4_token_select": {"ms": t_sel, "bound": "latency (6 passes over the pooled scores)"},
             "a4_gather": {"ms": t_gat, "gbs": gat_bytes / (t_gat / 1e3) / 1e9, "bound": "hbm",
                           "frac": gat_bytes / (t_gat / 1e3) / 1e9 / peaks["hbm_gbs"]}}
 
 
-def verify_row(t_ms, flops, chunk_bytes, peaks, link_gbs):
-    """The verify chunk kernel against its roofline: HBM when its arithmetic
-    intensity (flops per byte of the chunk it reads) is below the bf16 ridge point
+def intensity_row(t_ms, flops, nbytes, peaks):
+    """A contraction kernel against its roofline: HBM when its arithmetic
+    intensity (flops per byte it must move) is below the bf16 ridge point
     (tensor peak / HBM peak), else the tensor peak."""
     tflops = flops / (t_ms / 1e3) / 1e12
-    gbs = chunk_bytes / (t_ms / 1e3) / 1e9
-    intensity = flops / chunk_bytes
+    gbs = nbytes / (t_ms / 1e3) / 1e9
+    intensity = flops / nbytes
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     hbm = intensity < ridge
     return {"ms": t_ms, "tflops": tflops, "gbs": gbs, "flop_per_byte": intensity, "ridge_flop_per_byte": ridge,
             "bound": "hbm" if hbm else "tensor (bf16)",
-            "frac": gbs / peaks["hbm_gbs"] if hbm else tflops / peaks["bf16_tflops"],
-            "chunk_transfer_ms": chunk_bytes / (link_gbs * 1e6)}
+            "frac": gbs / peaks["hbm_gbs"] if hbm else tflops / peaks["bf16_tflops"]}
+
+
+def verify_row(t_ms, flops, chunk_bytes, peaks, link_gbs):
+    """The verify chunk kernel against its roofline (intensity_row: the chunk's
+    bytes), plus the time the link takes to deliver that chunk."""
+    return dict(intensity_row(t_ms, flops, chunk_bytes, peaks), chunk_transfer_ms=chunk_bytes / (link_gbs * 1e6))
 
 
 def time_full_kv_resident(g, q1, kv1, out1, layers, cs, n_dec=3):
@@ -570,6 +588,7 @@ def run_ours(args, rank, world, local_rank):
         inter = max(0.0, min(a1, b1) - max(a0, b0))
         overlap.append(inter / max(1e-9, b1 - b0))
     round_ms = [tl.ms("start", "end") for tl in tls]
+    commit_span = [tl.ms("commit_start", "commit_end") for tl in tls if "commit_start" in tl.ev]
 
     # ---- the draft call alone, timed on its stream (CUDA events, L2 > inputs)
     g = groups[0]
@@ -674,12 +693,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16/int%d->f32" % w.bits,
         "data": "synthetic (seeded; shapes and distributions of the workload; no weights)",
-        "config": {"workload": workload_name(w), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "T": w.T,
-                   "k": w.k, "bits": w.bits, "layers": layers, "groups": n_groups, "V": w.V, "chunk": w.C,
-                   "schedule": "single" if n_groups == 1 else args.schedule, "slots_per_layer": groups[0].n_slots,
-                   "l2": "inputs larger than L2 (packed cache %d MiB, full KV %d MiB per round)" % (
-                       alg_bytes // 2 ** 20, g.h2d_bytes() // 2 ** 20),
-                   "parallelism": "replicas" if world > 1 else "single"},
+        "config": bench_config(w, args, world),
         "e2e": {"value": e2e_value, "unit": "tokens/s/layer", "h2d_bytes_per_step": per_round_in,
                 "d2h_bytes_per_step": per_round_out},
         "gpu_launches": launches,
@@ -689,11 +703,13 @@ def run_ours(args, rank, world, local_rank):
                      "bytes_per_launch": alg_bytes, "ms_per_launch": draft_call_ms,
                      "ms_per_launch_in_round": draft_in_round_ms, "peak_source": peaks["source"]},
         "h2d": {"gbs": h2d_rate, "bytes_per_round": h2d_bytes / args.steps, "copy_ms": med(copy_span),
+                "slots_per_layer": groups[0].n_slots,
                 "frac_of_measured_link": (h2d_rate / link_peak) if h2d_rate else None,
                 "measured_link_gbs": link_peak, "link_peak_source": "measured at start-up (best of 4 x 512 MiB)"
                 if args.link_peak_gbs <= 0 else "given on the command line", "frac_of_pcie_gen5_64": (h2d_rate / PCIE_GEN5_GBS) if h2d_rate else None,
                 "overlap_with_draft": med(overlap)},
         "round_ms": {"median": med(round_ms), "draft": med(draft_span), "copy": med(copy_span),
+                     "commit": med(commit_span), "commit_max": max(commit_span) if commit_span else None,
                      "all": [round(x, 3) for x in round_ms],
                      "host_gap_total": round(total_ms - sum(round_ms), 3)},
         "rows": rows,
@@ -703,7 +719,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(args.workload)
+        out["cpu_baseline"] = cpu_baseline(args.workload, w)
     for gg in groups:
         gg.close()
     return out
@@ -737,105 +753,227 @@ def workload_name(w):
 
 
 # ---------------------------------------------------------------- CPU oracle leg
-ORACLE_SAMPLE = r"""
-import json, sys, time, os
+# One unit of oracle work = one (request, KV head) of one round of one layer:
+# a draft step over the packed prefix (timed once, counted k times) and the
+# verify pass of the k+1 rows over the full prefix.  Both are linear in the
+# prefix length, so a unit is timed on the first T_SAMPLE tokens of its slice
+# and scaled to the workload's length.  Worker processes (one BLAS thread
+# each) build their units, report "ready", and time them when the parent
+# sends "go" to all of them at once: the all-cores figure is measured with
+# every core busy on the same work.
+T_SAMPLE = 32768
+
+ORACLE_WORKER = r"""
+import json, sys, time
 sys.path.insert(0, {root!r})
 import numpy as np
 import synth
-from oracle import kivi, attention, accept
+from oracle import kivi, attention
 w = synth.get({wl!r})
-b = 0
-heads = {heads!r}                    # the KV heads of request 0 timed in this sample
+T = {T_s}
 G = w.G
-qh = np.concatenate([np.arange(h * G, (h + 1) * G) for h in heads])
-Ks, Vs = [], []
-T = w.T_keep if w.name == 'qwen' else w.T
-for h in heads:
+prep = []
+for b, h in {units!r}:
     k_, v_ = synth.kv_slice(w, b, h, T=T)
-    Ks.append(k_); Vs.append(v_)
-K = np.stack(Ks)[None]; V = np.stack(Vs)[None]
-t0 = time.perf_counter()
-packed = kivi.quant_pack(K, V, w.bits)
-t_pack = time.perf_counter() - t0
-tail = np.zeros((1, len(heads), 32 + w.k + 1, w.d), np.uint16)
-t0 = time.perf_counter()
-for i in range({steps}):
-    q = synth.draft_q(w, 0, i)[b:b+1][:, qh]
-    kc, vc_ = synth.draft_kv_cur(w, 0, i)
-    attention.draft_attention(q, *packed, [T], tail, tail, [0], w.bits, 1.0, k_cur=kc[b:b+1][:, heads],
-                              v_cur=vc_[b:b+1][:, heads], step=i)
-t_draft = (time.perf_counter() - t0) * w.k / {steps}
-qv = synth.verify_q(w, 0)[b:b+1][:, :, qh]
-kn, vn = synth.kv_new(w, 0)
-t0 = time.perf_counter()
-attention.verify_attention(qv, K, V, kn[b:b+1][:, :, heads], vn[b:b+1][:, :, heads], [T], 1.0)
-t_verify = time.perf_counter() - t0
-logits, drafts, L = synth.logits_and_drafts(w, 0)
-t0 = time.perf_counter()
-n, nxt, _ = accept.accept(logits[b:b+1], drafts[b:b+1])
-t_accept = time.perf_counter() - t0
-scale = w.Hkv / len(heads)           # attention work of the request's other KV heads
-tokens = (int(n[0]) + 1) * w.layers
-t_round = ((t_draft + t_verify) * scale + t_accept) * w.layers
-print(json.dumps(dict(t_round=t_round, tokens=tokens, t_pack=t_pack * scale, t_draft=t_draft * scale,
-                      t_verify=t_verify * scale, t_accept=t_accept, draft_steps_run={steps}, heads=heads)))
+    K = k_[None, None]
+    V = v_[None, None]
+    qh = list(range(h * G, (h + 1) * G))
+    kc, vc_ = synth.draft_kv_cur(w, 0, 0)
+    kn, vn = synth.kv_new(w, 0)
+    prep.append(dict(K=K, V=V, packed=kivi.quant_pack(K, V, w.bits), q=synth.draft_q(w, 0, 0)[b:b + 1][:, qh],
+                     kc=kc[b:b + 1][:, [h]], vc=vc_[b:b + 1][:, [h]], qv=synth.verify_q(w, 0)[b:b + 1][:, :, qh],
+                     kn=kn[b:b + 1][:, :, [h]], vn=vn[b:b + 1][:, :, [h]]))
+tail = np.zeros((1, 1, 32 + w.k + 1, w.d), np.uint16)
+print("ready", flush=True)
+while sys.stdin.readline().strip() == "go":
+    t_start = time.time()
+    res = []
+    for u in prep:
+        t0 = time.perf_counter()
+        attention.draft_attention(u["q"], *u["packed"], [T], tail, tail, [0], w.bits, 1.0,
+                                  k_cur=u["kc"], v_cur=u["vc"], step=0)
+        t1 = time.perf_counter()
+        attention.verify_attention(u["qv"], u["K"], u["V"], u["kn"], u["vn"], [T], 1.0)
+        res.append((t1 - t0, time.perf_counter() - t1))
+    print(json.dumps(dict(units=res, t_start=t_start, t_end=time.time())), flush=True)
 """
 
 
-def cpu_baseline(workload, steps=None, heads=None):
-    """Time the oracle, as it stands, on request 0 of one round (the given KV
-    heads, all of them by default; 1 BLAS thread) and scale to the metric's
-    unit (tokens of the request over the time of its whole round)."""
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+class OracleSampler:
+    """Worker processes holding oracle units; run() times all of them together."""
+
+    def __init__(self, workload, unit_lists, T_s):
+        import tempfile
+        env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        self.procs, self.errs = [], []
+        for units in unit_lists:
+            code = ORACLE_WORKER.format(root=ROOT, wl=workload, T_s=T_s, units=[tuple(u) for u in units])
+            err = tempfile.TemporaryFile(mode="w+")
+            self.errs.append(err)
+            self.procs.append(subprocess.Popen([sys.executable, "-c", code], stdin=subprocess.PIPE,
+                                               stdout=subprocess.PIPE, stderr=err, text=True, env=env))
+        for i, p in enumerate(self.procs):
+            if p.stdout.readline().strip() != "ready":
+                self._fail(i)
+
+    def _fail(self, i):
+        self.errs[i].seek(0)
+        msg = self.errs[i].read()[-300:]
+        self.close()
+        raise RuntimeError("oracle worker failed: " + msg)
+
+    def run(self):
+        """Per-unit (draft step, verify) seconds of every worker, and the wall time of the slowest."""
+        for p in self.procs:
+            p.stdin.write("go\n")
+            p.stdin.flush()
+        res = []
+        for i, p in enumerate(self.procs):
+            line = p.stdout.readline()
+            if not line:
+                self._fail(i)
+            res.append(json.loads(line))
+        wall = max(r["t_end"] for r in res) - min(r["t_start"] for r in res)
+        return [u for r in res for u in r["units"]], wall
+
+    def close(self):
+        for p in self.procs:
+            try:
+                p.stdin.close()
+                p.wait(timeout=60)
+            except Exception:
+                p.kill()
+        for e in self.errs:
+            e.close()
+
+
+def oracle_round_units(w):
+    """The (request, KV head) units of one round of one layer, in a fixed order."""
+    return [(b, h) for h in range(w.Hkv) for b in range(w.B)]
+
+
+def oracle_value(w, units, workers, t_accept, tokens):
+    """tokens/s/layer of the oracle running a whole round on `workers` cores,
+    from unit times measured with that many cores busy.
+
+    A round of one layer is B*Hkv units (k draft steps + one verify pass each,
+    scaled from the sampled length to the workload's) spread over the workers,
+    plus the accept step of the B requests (one core)."""
+    T_d = w.T_keep if w.name == "qwen" else w.T          # drafting reads the kept tokens
+    T_s = min(w.T, T_SAMPLE)
+    per_unit = statistics.mean(w.k * td * (T_d / T_s) + tv * (w.T / T_s) for td, tv in units)
+    n_units = w.B * w.Hkv
+    round_layer = math.ceil(n_units / workers) * per_unit + t_accept
+    return tokens / round_layer, per_unit
+
+
+def oracle_accept(w):
+    """Tokens of round 0 (accepted lengths + 1, summed over requests) and the accept step's time."""
     import synth
-    w = synth.get(workload)
-    steps = steps if steps is not None else (2 if w.T * w.layers > 100000 else 4)
-    heads = list(range(w.Hkv)) if heads is None else list(heads)
-    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    code = ORACLE_SAMPLE.format(root=ROOT, wl=workload, steps=steps, heads=heads)
+    from oracle import accept as oacc
+    logits, drafts, _ = synth.logits_and_drafts(w, 0)
+    t0 = time.perf_counter()
+    n, _, _ = oacc.accept(logits, drafts)
+    return int((n + 1).sum()), time.perf_counter() - t0
+
+
+def cpu_baseline(workload, workload_obj=None):
+    """The oracle, as it stands, on the machine's host cores: the same seeded units
+    timed on 1 thread and on every core, scaled to the metric's unit."""
+    import synth
+    w = workload_obj or synth.get(workload)
+    cores = len(os.sched_getaffinity(0))
+    T_s = min(w.T, T_SAMPLE)
     t0 = time.time()
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
-    if r.returncode != 0:
-        return {"value": None, "unit": "tokens/s/layer", "cores": 1, "kind": "oracle",
-                "sample": "failed: " + r.stderr[-300:]}
-    d = json.loads(r.stdout.strip().splitlines()[-1])
-    value = d["tokens"] / d["t_round"]        # one request at a time on one core
-    T = w.T_keep if w.name == "qwen" else w.T
-    return {"value": value, "unit": "tokens/s/layer", "cores": 1, "kind": "oracle",
-            "sample": (f"request 0 of round 0, KV heads {heads} of {w.Hkv} (time scaled to all heads): "
-                       f"{d['draft_steps_run']} of {w.k} draft steps timed and scaled to {w.k}, one verify pass "
-                       f"over T={T}, accept; {w.layers} layer(s) by scaling; 1 thread"),
-            "seconds": {k: d[k] for k in ("t_round", "t_pack", "t_draft", "t_verify", "t_accept")},
+    order = oracle_round_units(w)
+    try:
+        tokens, t_acc = oracle_accept(w)
+        one = OracleSampler(w.name, [order[:2]], T_s)
+        u1, wall1 = one.run()
+        one.close()
+        n_par = min(cores, len(order))
+        par = OracleSampler(w.name, [[order[i]] for i in range(n_par)], T_s)
+        uc, wallc = par.run()
+        par.close()
+    except RuntimeError as e:
+        return {"value": None, "unit": "tokens/s/layer", "cores": cores, "kind": "oracle", "sample": str(e)}
+    v1, pu1 = oracle_value(w, u1, 1, t_acc, tokens)
+    vc, puc = oracle_value(w, uc, n_par, t_acc, tokens)
+    return {"value": vc, "unit": "tokens/s/layer", "cores": n_par, "kind": "oracle",
+            "value_1thread": v1, "cpu_model": cpu_model(), "cores_available": cores,
+            "sample": (f"round 0, one layer: (request, KV head) units, each a draft step (counted {w.k} times) and "
+                       f"the {w.k + 1}-row verify pass, timed on the first {T_s} tokens of the slice and scaled to "
+                       f"T={w.T_keep if w.name == 'qwen' else w.T} (draft) / T={w.T} (verify); 1 thread: 2 units "
+                       f"in one process; all cores: {n_par} units, one per process, started together; round = "
+                       f"{w.B * w.Hkv} units over the cores + accept of {w.B} requests ({tokens} tokens), x{w.layers} "
+                       f"layer(s); numpy fp64, 1 BLAS thread per process"),
+            "seconds": {"unit_1thread": pu1, "unit_all_cores": puc, "accept": t_acc,
+                        "sample_wall_1thread": wall1, "sample_wall_all_cores": wallc},
             "wall_s": time.time() - t0}
 
 
 def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step runs one all-cores sample of
+    the workload (one unit per core, started together) and converts it to
+    tokens/s/layer exactly as the default line's cpu_baseline does."""
     if rank != 0:
         return None
     import synth
-    w = synth.get(args.workload)
-    vals = []
-    cb = None
+    w = workload_of(args)
+    cores = len(os.sched_getaffinity(0))
+    T_s = min(w.T, T_SAMPLE)
+    order = oracle_round_units(w)
+    n_par = min(cores, len(order))
     t_all = time.time()
+    tokens, t_acc = oracle_accept(w)
+    one = OracleSampler(w.name, [order[:2]], T_s)
+    u1, _ = one.run()
+    one.close()
+    v1, _ = oracle_value(w, u1, 1, t_acc, tokens)
+    par = OracleSampler(w.name, [[order[i]] for i in range(n_par)], T_s)
     for _ in range(args.warmup):
-        pass                     # the oracle has no warm state to build
-    for s in range(args.steps):
-        # each step: one KV head of request 0 (rotating), scaled to the whole request
-        cb = cpu_baseline(args.workload, steps=1, heads=[s % w.Hkv])
-        if cb["value"] is None:
-            break
-        vals.append(cb["value"])
-    v = statistics.median(vals) if vals else None
-    wall = time.time() - t_all
-    out = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s/layer", "n_gpus": world,
-           "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall * 1e3 / max(1, args.steps),
-           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
-           "data": "synthetic (seeded)",
-           "config": {"workload": workload_name(w), "B": w.B, "T": w.T, "k": w.k, "bits": w.bits,
-                      "layers": w.layers, "groups": w.groups},
-           "cpu_baseline": {"value": v, "unit": "tokens/s/layer", "cores": 1, "kind": "oracle",
-                            "sample": (cb or {}).get("sample")},
-           "e2e": {"value": v, "unit": "tokens/s/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    return out
+        par.run()
+    vals, walls = [], []
+    for _ in range(args.steps):
+        uc, wall = par.run()
+        vals.append(oracle_value(w, uc, n_par, t_acc, tokens)[0])
+        walls.append(wall)
+    par.close()
+    v = statistics.median(vals)
+    cb = {"value": v, "unit": "tokens/s/layer", "cores": n_par, "kind": "oracle", "value_1thread": v1,
+          "cpu_model": cpu_model(), "cores_available": cores,
+          "sample": (f"per step: {n_par} (request, KV head) units of round 0, one per process, started together; "
+                     f"each a draft step (counted {w.k} times) and the {w.k + 1}-row verify pass on the first "
+                     f"{T_s} tokens, scaled to the workload's length; round = {w.B * w.Hkv} units over the cores "
+                     f"+ accept; median over steps")}
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s/layer", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(walls) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic (seeded)",
+            "config": bench_config(w, args, world),
+            "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": "tokens/s/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": time.time() - t_all}
 
 
 # ---------------------------------------------------------------- distributed plumbing
@@ -1070,7 +1208,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="mistral", choices=["tiny", "mistral", "qwen", "llama", "stagger"])
+    ap.add_argument("--workload", default="llama", choices=["tiny", "mistral", "qwen", "llama", "stagger"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--schedule", default="staggered", choices=["staggered", "lockstep"])
     ap.add_argument("--slots", type=int, default=0,

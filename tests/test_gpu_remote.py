@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import synth
+from oracle import kivi
 
 pytestmark = pytest.mark.gpu
 
@@ -59,6 +60,16 @@ def test_staged_remote_prefix_equals_local_pack_and_paces_the_link():
         x = a[0].view(W.B * W.Hkv, NGc, -1)[:, :ng]
         y = b[0].view(W.B * W.Hkv, NGc, -1)[:, :ng]
         assert torch.equal(x, y)
+    # and the staged cache is the oracle's packing of the same K/V, bit for bit
+    okc, oksz, ovc, ovsz = kivi.quant_pack(K, V, W.bits)
+    for dev, want, dt in ((remote.kc, okc, np.uint32), (remote.vc, ovc, np.uint32),
+                          (remote.ksz, oksz, np.float16), (remote.vsz, ovsz, np.float16)):
+        got = dev[0].view(W.B * W.Hkv, NGc, -1)[:, :ng].cpu().numpy().view(dt)
+        want = np.ascontiguousarray(want).reshape(W.B * W.Hkv, ng, -1)
+        if dt is np.float16:
+            assert np.array_equal(got.astype(np.float32), want.astype(np.float32))   # values (-0 == +0)
+        else:
+            assert np.array_equal(got, want.view(dt))
     assert remote.packed_len[0].tolist() == [W.T] * W.B and remote.tail_len[0].tolist() == [0] * W.B
     # one round on each: identical verify outputs and accepted lengths
     inp = _inputs()

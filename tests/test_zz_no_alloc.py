@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import synth
+from oracle import accept as oacc
 
 pytestmark = pytest.mark.gpu
 
@@ -51,6 +52,8 @@ def test_noalloc_matches_workspace_entry_point_twice(vc, name):
         logits, drafts, _ = synth.logits_and_drafts(w, rnd)
         (n0, x0, a0), (n1, x1, a1) = _run_both(vc, logits, drafts)
         assert np.array_equal(n0, n1) and np.array_equal(x0, x1) and np.array_equal(a0, a1)
+        on, ox, oa = oacc.accept(logits, drafts)
+        assert np.array_equal(n1, on) and np.array_equal(x1, ox) and np.array_equal(a1, oa)
 
 
 def test_noalloc_ties_and_small_vocab(vc):
@@ -60,6 +63,8 @@ def test_noalloc_ties_and_small_vocab(vc):
         drafts = rng.integers(0, V, size=(6, 4)).astype(np.int32)
         (n0, x0, a0), (n1, x1, a1) = _run_both(vc, logits, drafts)
         assert np.array_equal(n0, n1) and np.array_equal(x0, x1) and np.array_equal(a0, a1)
+        on, ox, oa = oacc.accept(logits, drafts)
+        assert np.array_equal(n1, on) and np.array_equal(x1, ox) and np.array_equal(a1, oa)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(vc):
@@ -70,3 +75,12 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(vc):
     with pytest.raises(vc.VcError) as e:
         vc.vc_accept_noalloc(B, k, V, lg, dr, o, o, None)
     assert e.value.status == 6 and "scratch limit" in str(e.value)
+
+
+def test_noalloc_rejects_more_requests_than_its_counters(vc):
+    B, k, V = 4097, 0, 1           # one row per request: 4097 partials fit, 4097 counters do not
+    lg = torch.zeros((B, k + 1, V), dtype=torch.float32, device="cuda")
+    o = torch.zeros(B, dtype=torch.int32, device="cuda")
+    with pytest.raises(vc.VcError) as e:
+        vc.vc_accept_noalloc(B, k, V, lg, None, o, o, None)
+    assert e.value.status == 6 and "4096 requests" in str(e.value)

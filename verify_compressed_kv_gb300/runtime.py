@@ -334,7 +334,9 @@ def round_single(g: Group, inp: RoundInputs, cs, xs, tl: Timeline | None = None,
     tl.mark("copy_end", xs)
     tl.mark("verify_end", cs)
     g.accept(inp, cs)
+    tl.mark("commit_start", cs)
     g.commit(inp, cs)
+    tl.mark("commit_end", cs)
     cs.wait_event(tl.ev["copy_end"])
     g.read_back(cs)
     tl.mark("end", cs)
@@ -363,7 +365,9 @@ def round_staggered(X: Group, Y: Group, inp_x: RoundInputs, inp_y: RoundInputs, 
     tl.mark("copy_end", xs)
     tl.mark("verify_end", cs)
     Y.accept(inp_y, cs)
+    tl.mark("commit_start", cs)
     Y.commit(inp_y, cs)
+    tl.mark("commit_end", cs)
     cs.wait_event(tl.ev["copy_end"])
     Y.read_back(cs)
     tl.mark("end", cs)
