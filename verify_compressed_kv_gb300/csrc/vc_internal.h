@@ -177,6 +177,13 @@ __host__ __device__ constexpr uint32_t vc_tc_idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
+// Instruction descriptor of an M x N x 16 kind::f16 product with fp16 A and B
+// and fp32 D (A/B format fields 0).  A is K-major (or in TMEM); B is K-major,
+// or MN-major when b_mn (bit 16).  M = 128: N a multiple of 16 in [16, 256].
+__host__ __device__ constexpr uint32_t vc_tc_idesc_f16(int M, int N, bool b_mn) {
+  return (1u << 4) | (b_mn ? (1u << 16) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
 // TMEM allocation of `ncols` columns (a power of two >= 32) by one whole
 // warp; the base address is written to *slot (shared memory).
 __device__ __forceinline__ void vc_tc_alloc(uint32_t* slot, uint32_t ncols) {
@@ -197,6 +204,29 @@ __device__ __forceinline__ void vc_tc_mma(uint32_t d_tmem, uint64_t a_desc, uint
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc ? 1u : 0u)
       : "memory");
 }
+// D (TMEM) = A . B^T (+ D if acc) with A in TMEM: lane m holds row m, a 32-bit
+// column holds two consecutive K elements (16-bit types), so one K = 16 step
+// spans 8 columns from a_tmem.  Issued by one thread.
+__device__ __forceinline__ void vc_tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             bool acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc ? 1u : 0u)
+      : "memory");
+}
+// 16 consecutive 32-bit columns of the warp's 32 TMEM lanes from registers:
+// thread i writes lane 32 (warp % 4) + i.  Asynchronous: tcgen05.wait::st
+// (vc_tc_wait_st) before the values are relied on.
+__device__ __forceinline__ void vc_tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void vc_tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // Arrive once on `bar` when every earlier tcgen05.mma of this thread completed.
 __device__ __forceinline__ void vc_tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
