@@ -94,20 +94,22 @@ const char* vc_last_error(void);
  * expected finite; a NaN element gets code 0.
  *
  * Packed draft cache of capacity T_cap tokens (T_cap % 32 == 0), NG = T_cap / 32
- * groups of 32 tokens.  The bit placement is this library's own format: K
- * codes are stored as token rows and V codes as channel rows, so that the
- * draft kernel's threads (one per token for K, one per channel for V) each
- * read one contiguous row, and the codes of row elements 2m and 2m + 1 sit
- * 16 bits apart in one word (one shift and one mask give both as the two
- * halves of a 16-bit pair).
- *   kc  uint32 [B, Hkv, NG, 32, d*bits/32]   K codes of a group: row t = token t
- *   ksz fp16   [B, Hkv, NG, 2, d]            scales of the group's channels, then zeros
- *   vc  uint32 [B, Hkv, NG, d, bits]         V codes of a group: row c = channel c
- *   vsz fp16   [B, Hkv, NG, d/32, 2, 32]     per 32-channel group: the 32 tokens'
- *                                            scales, then their zeros, in token order
- * Fields (bit 0 = least significant): word w of a row holds row elements
- * 2((16/bits)w + k) + e (channels of a K row, tokens of a V row), k < 16/bits,
- * e < 2, in the bits-wide field starting at bit 16e + bits*k.
+ * groups of 32 tokens.  The bit placement is this library's own format: it
+ * follows the operand fragments of the 16x8x16 fp16 tensor-core product that
+ * reads it (two codes an operand register needs sit 16 bits apart in one word).
+ *   kc  uint32 [B, Hkv, NG, d*bits]     K codes of a group: 32 lanes x d*bits/32 words,
+ *                                       word w of lane L at (w/4)*128 + 4L + w%4
+ *   ksz fp16   [B, Hkv, NG, 2, d]       scales of the group's channels, then zeros
+ *   vc  uint32 [B, Hkv, NG, d*bits]     V codes, same word order, other field map
+ *   vsz fp16   [B, Hkv, NG, d/32, 2, 32]  per channel group: scales, then zeros,
+ *                                       entry 8c + 4s + 2r + e = token 8c + 4e + 2s + r
+ * Fields (bit 0 = least significant):
+ *   bits = 2: slot (u, r, e) starts at 16e + 4u + 2(1 - r);
+ *   bits = 4: slot (u, e) starts at 16e + 4u;  bits = 8: at 16e + 8u.
+ * Lane L = 4a + c.  K: tokens 4a + j (j < 4), channels (d/4)c + 4k + 2r + e
+ * (k < d/16), fragment i = j*(d/16) + k.  V: tokens 8c + 4e + 2s + r, channels
+ * 8n + a (n < d/8), fragment i = s*(d/8) + n.  bits = 2: word i/4, u = i%4;
+ * bits = 4, 8: i2 = 2i + r, SPW = 16/bits slots per word, word i2/SPW, u = i2%SPW.
  * Bytes per token per KV head: d*bits/4 (codes) + d/4 (metadata).
  */
 

@@ -20,14 +20,12 @@ Packed layout (the library's format; written out from the rules next to
 the packing functions below).  Per (request, KV head) and group of 32
 tokens:
 
-* K codes uint32 [B, Hkv, T/32, d*b]: 32 token rows of d*b/32 words; V codes
-  uint32 [B, Hkv, T/32, d*b]: d channel rows of b words; rows stored in chunks
-  of up to 4 words (chunk-major).  Word w of a row holds elements
-  2((16/b)w + k) + e of the row (channels for K, tokens for V) in the b-bit
-  field at bit 16e + b*k; no field crosses bit 31.
+* K codes uint32 [B, Hkv, T/32, d*b] and V codes uint32 [B, Hkv, T/32, d*b]:
+  32 lanes x d*b/32 words, each code a b-bit field at a position given by its
+  token and channel (K and V use different maps); no field crosses bit 31.
 * K meta fp16 [B, Hkv, T/32, 2, d]: scales of the group's channels, then zeros.
 * V meta fp16 [B, Hkv, T/32, d/32, 2, 32]: per channel group, the 32 tokens'
-  scales, then zeros, in token order.
+  scales, then zeros, tokens in a fixed permuted order.
 
 Numbers are numpy arrays.  bf16 inputs are uint16 bit patterns.
 """
@@ -114,43 +112,73 @@ def dequantize_kv(kcode, kscale, kzero, vcode, vscale, vzero):
 # ------------------------------------------------------------ packed layout
 #
 # The bit placement below is this library's own format (the quantiser fixes
-# only the codes and the fp16 scale/zero).  Per group of 32 tokens, the K
-# codes are stored as 32 token rows and the V codes as d channel rows; along a
-# row, the codes of elements 2m and 2m + 1 sit in the same field of the low and
-# the high half-word of one 32-bit word, so that one shift and one mask give
-# both of them as the two halves of a packed 16-bit pair.  With b bits, a
-# half-word holds 16/b fields; field k of a half-word starts at bit b*k.
+# only the codes and the fp16 scale/zero).  It follows the register fragments
+# of the 16x8x16 half-precision tensor-core product that consumes it, so that a
+# lane finds each pair of codes it feeds to one operand register 16 bits apart
+# in one word.  Written out per group of 32 tokens; d channels, b bits.
 
-def _row_fields(bits: int, n_rows: int, row_len: int, rows_are_tokens: bool):
-    """(word index, field start, token, channel) of every code of one group.
+def _field_pos(bits: int, u: int, r: int, e: int) -> int:
+    """Lowest bit of a field.  b = 2: slot (u, r, e) starts at 16e + 4u + 2(1 - r).
+    b = 4: slot (u, e) starts at 16e + 4u; b = 8: slot (u, e) at 16e + 8u (r
+    unused for b = 4, 8).  The e = 1 field of a slot sits exactly 16 bits above
+    its e = 0 field, in the high half-word."""
+    if bits == 2:
+        return 16 * e + 4 * u + 2 * (1 - r)
+    return 16 * e + bits * u
 
-    Row r (a token for K, a channel for V) holds row_len codes in
-    W = row_len*bits/32 words, stored in chunks of CW = min(W, 4) words: word
-    w of row r sits at ((w // CW) * n_rows + r) * CW + w % CW (the chunks of
-    all rows come before the next chunk).  Field (k, e) of a word, at bit
-    16e + b*k (k < 16/b, e < 2), holds element 2*((16/b)*w + k) + e of the row."""
-    per_half = 16 // bits
-    W = row_len * bits // 32
-    CW = min(W, 4)
-    rows = []
-    for r in range(n_rows):
-        for w in range(W):
-            for k in range(per_half):
-                for e in range(2):
-                    x = 2 * (per_half * w + k) + e
-                    t, ch = (r, x) if rows_are_tokens else (x, r)
-                    rows.append((((w // CW) * n_rows + r) * CW + w % CW, 16 * e + bits * k, t, ch))
-    return np.array(rows, dtype=np.int64)
+
+def _word_index(L: int, w: int) -> int:
+    """Word w of lane L sits at (w // 4) * 128 + 4 L + w % 4 within the group."""
+    return (w // 4) * 128 + 4 * L + w % 4
+
+
+def _slot(bits: int, i: int, r: int):
+    """Fragment index i of a lane (and its r) -> (word, u) of its field.
+    b = 2: word i // 4, u = i % 4.  b = 4, 8: i2 = 2i + r, and a word holds
+    32 / (2b) slots: word i2 // (16 / b), u = i2 % (16 / b)."""
+    if bits == 2:
+        return i // 4, i % 4
+    i2 = 2 * i + r
+    per = 16 // bits
+    return i2 // per, i2 % per
 
 
 def _k_fields(d: int, bits: int):
-    """K codes: 32 token rows of d channels (d*b/32 words per token)."""
-    return _row_fields(bits, GROUP, d, True)
+    """(word index, field start, token, channel) of every K code of one group.
+
+    Lane L = 4a + c holds tokens 4a + j (j < 4) and channels (d/4) c + 4k + 2r + e
+    (k < d/16, r, e < 2); its fragment index is i = j*(d/16) + k."""
+    KS = d // 16
+    rows = []
+    for L in range(32):
+        a, c = divmod(L, 4)
+        for j in range(4):
+            for k in range(KS):
+                for r in range(2):
+                    for e in range(2):
+                        w, u = _slot(bits, j * KS + k, r)
+                        rows.append((_word_index(L, w), _field_pos(bits, u, r, e),
+                                     4 * a + j, (d // 4) * c + 4 * k + 2 * r + e))
+    return np.array(rows, dtype=np.int64)
 
 
 def _v_fields(d: int, bits: int):
-    """V codes: d channel rows of 32 tokens (b words per channel)."""
-    return _row_fields(bits, d, GROUP, False)
+    """(word index, field start, token, channel) of every V code of one group.
+
+    Lane L = 4a + c holds tokens 8c + 4e + 2s + r (s, r, e < 2) and channels
+    8n + a (n < d/8); its fragment index is i = s*(d/8) + n."""
+    NT = d // 8
+    rows = []
+    for L in range(32):
+        a, c = divmod(L, 4)
+        for s in range(2):
+            for n in range(NT):
+                for r in range(2):
+                    for e in range(2):
+                        w, u = _slot(bits, s * NT + n, r)
+                        rows.append((_word_index(L, w), _field_pos(bits, u, r, e),
+                                     8 * c + 4 * e + 2 * s + r, 8 * n + a))
+    return np.array(rows, dtype=np.int64)
 
 
 def _pack(code: np.ndarray, bits: int, fields) -> np.ndarray:
@@ -204,19 +232,28 @@ def unpack_kmeta(ksz):
     return ksz[..., 0, :], ksz[..., 1, :]
 
 
+def _vmeta_token_of_entry():
+    """Entry p = 8c + 4s + 2r + e of a 32-entry row holds token 8c + 4e + 2s + r."""
+    p = np.arange(GROUP)
+    c, s, r, e = p // 8, (p // 4) % 2, (p // 2) % 2, p % 2
+    return 8 * c + 4 * e + 2 * s + r
+
+
 def pack_vmeta(vscale, vzero):
-    """fp16 [B,H,T,d/32] x2 -> fp16 [B,H,T/32,d/32,2,32]: per 32-channel group,
-    the 32 tokens' scales, then their zeros, in token order."""
+    """fp16 [B,H,T,d/32] x2 -> fp16 [B,H,T/32,d/32,2,32]."""
     B, H, T, NC = vscale.shape
     m = np.stack([vscale, vzero], axis=-1).reshape(B, H, T // GROUP, GROUP, NC, 2)
-    return np.ascontiguousarray(m.transpose(0, 1, 2, 4, 5, 3))      # [B,H,NG,NC,2,32 tokens]
+    m = m.transpose(0, 1, 2, 4, 5, 3)                        # [B,H,NG,NC,2,32 tokens]
+    return np.ascontiguousarray(m[..., _vmeta_token_of_entry()])
 
 
 def unpack_vmeta(vsz):
     """fp16 [B,H,T/32,d/32,2,32] -> (scale, zero) fp16 [B,H,T,d/32]."""
     B, H, NG, NC, _, _ = vsz.shape
-    m = vsz.transpose(0, 1, 2, 5, 3, 4).reshape(B, H, NG * GROUP, NC, 2)
-    return np.ascontiguousarray(m[..., 0]), np.ascontiguousarray(m[..., 1])
+    m = np.empty_like(vsz)
+    m[..., _vmeta_token_of_entry()] = vsz                    # back to token order
+    m = m.transpose(0, 1, 2, 5, 3, 4).reshape(B, H, NG * GROUP, NC, 2)
+    return m[..., 0], m[..., 1]
 
 
 def quant_pack(K, V, bits: int):

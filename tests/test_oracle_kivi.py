@@ -110,59 +110,51 @@ def _const_words(pack, code_fn, bits, d):
 
 
 def test_packed_words_by_hand():
-    """Words worked out by hand from the field rules (field (k, e) of a word at
-    bit 16e + b*k holds row element 2((16/b)w + k) + e).
+    """Words worked out by hand from the field rules.
 
-    b = 2: e = 1 fields start at bits 16, 18, ..., 30, so a code of 1 wherever
-      the element index is odd gives 0x55550000 (K: odd channels; V: odd
-      tokens).  Element index // 2 = 8w + k is odd exactly when k is (8w is
-      even): fields k = 1, 3, 5, 7 of both halves start at bits 2, 6, 10, 14,
-      18, 22, 26, 30 -> 0x44444444.  Code 3 everywhere -> 0xFFFFFFFF.
-    b = 4: the e = 1 fields fill bits 16-31, so code 15 there -> 0xFFFF0000 and
-      code 1 there -> bits 16, 20, 24, 28 = 0x11110000; k odd (k = 1, 3) ->
-      bits 4, 12, 20, 28 = 0x10101010."""
+    b = 2, slot (u, r, e) starts at 16e + 4u + 2(1 - r):
+      e = 1 fields: bits 16, 18, ..., 30; a code of 1 in each -> 0x55550000.
+      r = 1 fields: 16e + 4u = 0, 4, 8, 12, 16, 20, 24, 28 -> 0x11111111.
+    For K, e is the channel's bit 0 and r its bit 1; for V, r is the token's
+    bit 0 and e its bit 2.
+    b = 4, slot (u, e) starts at 16e + 4u: the e = 1 fields fill bits 16-31,
+      so code 15 there -> 0xFFFF0000 and code 1 there -> bits 16, 20, 24, 28 =
+      0x11110000."""
     for d in (64, 128):
         assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: c % 2, 2, d) == 0x55550000)
-        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: t % 2, 2, d) == 0x55550000)
-        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: (c // 2) % 2, 2, d) == 0x44444444)
-        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: (t // 2) % 2, 2, d) == 0x44444444)
-        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: 3 + 0 * c, 2, d) == 0xFFFFFFFF)
+        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: (c // 2) % 2, 2, d) == 0x11111111)
+        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: t % 2, 2, d) == 0x11111111)
+        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: (t // 4) % 2, 2, d) == 0x55550000)
         assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: 15 * (c % 2), 4, d) == 0xFFFF0000)
         assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: c % 2, 4, d) == 0x11110000)
-        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: (t // 2) % 2, 4, d) == 0x10101010)
+        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: (t // 4) % 2, 4, d) == 0x11110000)
+        assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: 3 + 0 * c, 2, d) == 0xFFFFFFFF)
 
 
 def test_single_codes_land_where_the_rules_say():
-    """Codes placed by hand (d = 128 unless noted).
+    """Three codes placed by hand (d = 128 unless noted).
 
-    Word w of row r sits at ((w // CW) * rows + r) * CW + w % CW, CW = min(4,
-    words per row).
-    K, b = 2, token 5, channel 37: pair 18, e = 1; a word holds 8 pairs, so
-      w = 2, k = 2; 8 words a token row, CW = 4: index (0*32 + 5)*4 + 2 = 22,
-      start 16 + 2*2 = 20: code 3 -> 0x00300000.
-    V, b = 2, token 13, channel 42: pair 6, e = 1 -> w = 0, k = 6; 2 words a
-      channel row, CW = 2: index (0*128 + 42)*2 + 0 = 84, start 16 + 12 = 28:
-      code 2 -> 0x20000000.
-    K, b = 4, d = 64, token 0, channel 5: pair 2, e = 1; 4 pairs a word -> w = 0,
-      k = 2; index 0, start 16 + 8 = 24: code 11 -> 0x0B000000.
-    V, b = 4, token 31, channel 0: pair 15, e = 1 -> w = 3, k = 3; CW = 4:
-      index (0*128 + 0)*4 + 3 = 3, start 16 + 12 = 28: code 9 -> 0x90000000."""
+    K, b = 2, token 5, channel 37: a = 1, j = 1; 37 = 32*1 + 4*1 + 2*0 + 1 so
+      c = 1, k = 1, r = 0, e = 1; lane 4a + c = 5; fragment j*8 + k = 9 -> word 2,
+      u = 1; start 16 + 4 + 2 = 22; stored at (2 // 4)*128 + 4*5 + 2 = 22.
+    V, b = 2, token 13, channel 42: 13 = 8*1 + 4*1 + 2*0 + 1 so c = 1, e = 1,
+      s = 0, r = 1; 42 = 8*5 + 2 so n = 5, a = 2; lane 9; fragment 0*16 + 5 ->
+      word 1, u = 1; start 16 + 4 + 0 = 20; stored at 0 + 36 + 1 = 37.
+    K, b = 4, d = 64, token 0, channel 5: a = c = j = 0, k = 1, r = 0, e = 1;
+      index 2*(0*4 + 1) + 0 = 2 -> word 0, u = 2; start 16 + 8 = 24:
+      code 11 -> 0x0B000000."""
     code = np.zeros((1, 1, 32, 128), np.uint8)
     code[0, 0, 5, 37] = 3
     w = kivi.pack_kcodes(code, 2)[0, 0, 0]
-    assert w[22] == 0x00300000 and np.count_nonzero(w) == 1
+    assert w[22] == 0x00C00000 and np.count_nonzero(w) == 1
     code = np.zeros((1, 1, 32, 128), np.uint8)
     code[0, 0, 13, 42] = 2
     w = kivi.pack_vcodes(code, 2)[0, 0, 0]
-    assert w[84] == 0x20000000 and np.count_nonzero(w) == 1
+    assert w[37] == 0x00200000 and np.count_nonzero(w) == 1
     code = np.zeros((1, 1, 32, 64), np.uint8)
     code[0, 0, 0, 5] = 11
     w = kivi.pack_kcodes(code, 4)[0, 0, 0]
     assert w[0] == 0x0B000000 and np.count_nonzero(w) == 1
-    code = np.zeros((1, 1, 32, 128), np.uint8)
-    code[0, 0, 31, 0] = 9
-    w = kivi.pack_vcodes(code, 4)[0, 0, 0]
-    assert w[3] == 0x90000000 and np.count_nonzero(w) == 1
 
 
 @pytest.mark.parametrize("bits", [2, 4, 8])
@@ -178,16 +170,16 @@ def test_pack_unpack_bijection(bits):
 
 
 def test_meta_layouts():
-    """V meta: per 32-channel group, the 32 tokens' scales, then their zeros, in
-    token order (entry 6 of group 1 is token 32 + 6).  K meta holds the scales
-    of all channels, then the zeros."""
+    """V meta entry p = 8c + 4s + 2r + e holds token 8c + 4e + 2s + r: entry 5
+    (c 0, s 1, r 0, e 1) is token 6, entry 19 (c 2, s 0, r 1, e 1) is token 21.
+    K meta holds the scales of all channels, then the zeros."""
     rng = np.random.default_rng(5)
     s = rng.standard_normal((2, 2, 64, 4)).astype(np.float16)
     z = rng.standard_normal((2, 2, 64, 4)).astype(np.float16)
     m = kivi.pack_vmeta(s, z)
     assert m.shape == (2, 2, 2, 4, 2, 32)
-    assert m[1, 0, 1, 3, 0, 6] == s[1, 0, 32 + 6, 3] and m[1, 0, 1, 3, 1, 6] == z[1, 0, 32 + 6, 3]
-    assert m[0, 1, 0, 2, 0, 21] == s[0, 1, 21, 2] and m[0, 1, 0, 2, 1, 21] == z[0, 1, 21, 2]
+    assert m[1, 0, 1, 3, 0, 5] == s[1, 0, 32 + 6, 3] and m[1, 0, 1, 3, 1, 5] == z[1, 0, 32 + 6, 3]
+    assert m[0, 1, 0, 2, 0, 19] == s[0, 1, 21, 2] and m[0, 1, 0, 2, 1, 19] == z[0, 1, 21, 2]
     s2, z2 = kivi.unpack_vmeta(m)
     assert np.array_equal(s2, s) and np.array_equal(z2, z)
     ks = rng.standard_normal((1, 2, 3, 128)).astype(np.float16)
@@ -210,16 +202,16 @@ def test_quant_pack_roundtrip_and_bound_on_workload_inputs():
 
 
 def test_eight_bit_words_by_hand():
-    """b = 8: two fields a half-word, field (k, e) at 16e + 8k.
-    Codes equal to the element's bit 0 (e) put a 1 at bits 16 and 24: 0x01010000
-    (K: channel parity; V: token parity); code 255 in every e = 1 field:
-    0xFFFF0000.  One code: K, d = 128, token 5, channel 37 -> pair 18, e = 1;
-    2 pairs a word -> w = 9, k = 0; 32 words a token row in chunks of 4: index
-    ((9 // 4)*32 + 5)*4 + 9 % 4 = 277, start 16: code 200 -> 0x00C80000."""
+    """b = 8: slot (u, e) starts at 16e + 8u, two slots per word.
+    K codes equal to the channel's bit 0 (e) put a 1 at bits 16 and 24: 0x01010000;
+    code 255 in every e = 1 field: 0xFFFF0000.  One code: K, d = 128, token 5,
+    channel 37 -> lane 5, j = 1, k = 1, r = 0, e = 1; fragment i = 9, i2 = 2*9 + 0 =
+    18 -> word 18 // 2 = 9, u = 0; start 16; stored at (9 // 4)*128 + 4*5 + 9 % 4 = 277:
+    code 200 -> 0x00C80000."""
     for d in (64, 128):
         assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: c % 2, 8, d) == 0x01010000)
         assert np.all(_const_words(kivi.pack_kcodes, lambda t, c: 255 * (c % 2), 8, d) == 0xFFFF0000)
-        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: t % 2, 8, d) == 0x01010000)
+        assert np.all(_const_words(kivi.pack_vcodes, lambda t, c: (t // 4) % 2, 8, d) == 0x01010000)
     code = np.zeros((1, 1, 32, 128), np.uint8)
     code[0, 0, 5, 37] = 200
     w = kivi.pack_kcodes(code, 8)[0, 0, 0]

@@ -1,5 +1,4 @@
-// libvc_draft_attn: decode attention over the KIVI-packed draft cache, on the
-// tcgen05 tensor cores.
+// libvc_draft_attn: decode attention over the KIVI-packed draft cache.
 //
 // VeriCache (gist.science/paper/2605.17613), Technical Summary, Core
 // Algorithm (Drafting: candidate tokens come from the compressed KV) and Key
@@ -8,39 +7,34 @@
 // of a KV head share every byte read.
 //
 // One launch per draft step.  Grid = B*Hkv tail CTAs followed by a persistent
-// set of stream CTAs (one per SM):
+// set of stream CTAs (occupancy x SM count):
 //   * stream-K partition: the packed groups of every (request, KV head) are
 //     laid end to end and each stream CTA takes an equal contiguous range, so
-//     the work is balanced whatever B*Hkv is; a range may span slices
+//     the work is balanced whatever B*Hkv is; a range may span two heads
 //     (segments);
-//   * a segment is cut into tiles of 4 groups (128 tokens); a producer thread
-//     fills a ring of tile stages (K codes, K scale/zero, V codes, V
-//     scale/zero) with bulk async copies;
-//   * 4 token warps (one 32-token group each: TMEM lane quarter = group)
-//     dequantise their tokens' K rows into TMEM as fp16, and D/32 channel
-//     warps dequantise the tile's V rows (TMEM lane = channel, tokens along
-//     the row): the code field OR-ed into the mantissa of 1.0 gives
-//     y = 1 + code/f exactly, and x^ = fma(y - 1, f s, z) is the correctly
-//     rounded fp16 of code s + z, two elements per instruction;
-//   * one thread issues S = K^ . Q^T (M = 128 tokens, N = 16 columns for the
-//     G heads, K = d; A in TMEM, Q in shared memory) and O^T = V^T . P^T
-//     (M = channels, N = 16, K = the tile's 128 tokens; A in TMEM, P in
-//     shared memory), fp16 operands, fp32 accumulators in TMEM;
-//   * the token warps turn S into softmax weights against a running maximum
-//     that is raised only when a score exceeds it by more than 2^3 (the four
-//     warps agree once per tile on one barrier), write P as fp16 and keep the
-//     weight sums; the channel warps fold each tile's O into registers,
-//     rescaling when the maximum rose;
-//   * at the end of a segment the sums and outputs give one normalised
-//     partial + log2-sum-exp per head; the last CTA to finish a (request, KV
-//     head) (arrival counter in the workspace, reset by that CTA) merges all
-//     its partials and writes the bf16 output.
+//   * a segment is streamed through a ring of shared-memory stages (11 groups
+//     of 32 tokens each: K codes, K scale/zero, V codes, V scale/zero), filled
+//     by bulk async copies (cp.async.bulk + mbarrier transaction counts, bounded
+//     waits) while the 11 consumer warps compute on earlier stages;
+//   * each warp owns one group per stage and keeps its own online-softmax
+//     state (max, sums) and output accumulators, all G heads of the KV head as
+//     rows of 16x8x16 tensor-core products: the packed codes become operand
+//     registers with one shift and one logic op per pair (1 + code/f is exact
+//     in fp16), the key scales fold into the query and the value scales into
+//     the softmax weights, each fold carried as an fp16 (hi, lo) pair so the
+//     products keep ~22 bits, and the zero points enter through two narrow
+//     correction products (group_mma below); with G = 4 the roles swap
+//     (codes as the A operand, the 4 heads as the 8 columns, group_mma_t),
+//     which halves the QK and PV products, and the folds are single fp16
+//     values (the draft is lossy by design: fp16 rounding of the folded
+//     operands sits far below the codes' own error);
+//   * at the end of a segment the warps are merged (log-sum-exp) into one
+//     partial per query head; the last CTA to finish a (request, KV head)
+//     (arrival counter in the workspace, reset by that CTA) merges all its
+//     partials and writes the bf16 output.
 // The tail CTAs handle the bf16 tail (tokens committed since the last full
 // group plus earlier draft steps) and the current token, and store the
 // current token's K/V into the tail for the following steps.
-// Every wait is bounded (~2 s); a wait that runs out sets the device status
-// flag, the CTA drains its copies and products, frees its TMEM and returns,
-// and the call's outputs are invalid (vc_draft_attn_device_status).
 #include <cfloat>
 
 #include "vc_internal.h"
@@ -49,23 +43,22 @@ namespace {
 
 __device__ uint32_t g_draft_status = 0;
 
+// 11 consumer warps + 1 producer: three warps per scheduler, the same
+// register budget (168) as 8 + 1.
+constexpr int kWarps = 11;                      // consumer warps of a stream CTA (one group each per stage)
+constexpr int kConsumers = kWarps * 32;
+constexpr int kThreads = kConsumers + 32;        // + one producer warp
 constexpr int kGroup = 32;
-constexpr int kTileGroups = 4;                    // a tile: 4 groups = 128 tokens = the products' M
-constexpr int kTile = kTileGroups * kGroup;
-constexpr int kTokWarps = 4;                      // token warp q: group q of a tile, TMEM lanes 32q..
-constexpr int kN = 16;                            // N of both products: the G <= 16 heads, zero-padded
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
-constexpr float kLazy = 3.0f;                     // running max raised only past max + 2^3
-
 struct DraftArgs {
   const uint16_t* q;        // [B, Hq, D]
   const uint16_t* k_cur;    // [B, Hkv, D] or null
   const uint16_t* v_cur;
-  const uint32_t* kc;       // [B, Hkv, NG, D*BITS] words
-  const uint16_t* ksz;      // [B, Hkv, NG, 2, D]
-  const uint32_t* vc;       // [B, Hkv, NG, D*BITS] words
-  const uint16_t* vsz;      // [B, Hkv, NG, D/32, 2, 32]
+  const uint32_t* kc;       // [B, Hkv, NG, W, 32]
+  const uint16_t* ksz;      // [B, Hkv, NG, D, 2]
+  const uint32_t* vc;
+  const uint16_t* vsz;      // [B, Hkv, NG, D/32, 32, 2]
   const int32_t* packed_len;
   uint16_t* tail_k;         // [B, Hkv, tail_cap, D]
   uint16_t* tail_v;
@@ -106,200 +99,629 @@ __host__ __device__ inline void ctas_of(int bh, const DraftArgs& a, int& first, 
   last = static_cast<int>(d);
 }
 
-// Segments of stream CTA c: consecutive calls walk [range_lo(c), range_lo(c+1)).
-struct Segment {
-  int bh, gs, n_valid, n_tiles;
+// ------------------------------------------------------------------ shared memory plan
+template <int D, int BITS, int G>
+struct Plan {
+  static constexpr size_t codes = static_cast<size_t>(D) * BITS * 4;   // bytes of one group's K (or V) codes
+  static constexpr size_t meta = static_cast<size_t>(D) * 4;           // bytes of one group's K (or V) meta
+  static constexpr size_t kc = kWarps * codes;                         // a stage holds kWarps groups
+  static constexpr size_t mt = kWarps * meta;
+  static constexpr size_t stage = 2 * kc + 2 * mt;                      // K codes, K meta, V codes, V meta
+  // ring depth: about 100 KB of stages in flight, at least double buffering
+  static constexpr int NS = (100 * 1024 / stage) < 2 ? 2 : ((100 * 1024 / stage) > 6 ? 6 : static_cast<int>(100 * 1024 / stage));
+  static constexpr size_t ring = stage * NS;
+  static constexpr size_t red = static_cast<size_t>(kWarps) * G * D * 4;   // warp merge
+  static constexpr size_t off_red = ring;
+  static constexpr size_t body = ring + red;
+  static constexpr size_t q = static_cast<size_t>(G) * D * 4;             // tail CTA: fp32 queries
+  static constexpr size_t wstat = static_cast<size_t>(kWarps) * 8 * 2 * 4;  // per-warp (max, sum) per head
+  static constexpr size_t off_q = body;
+  static constexpr size_t off_wstat = off_q + q;
+  static constexpr size_t off_bar = (off_wstat + wstat + 15) & ~size_t(15);   // full[NS], empty[NS]
+  static constexpr size_t off_flag = off_bar + 16 * NS;                      // combine flag, abort flag
+  static constexpr size_t total = off_flag + 16;
 };
-__device__ __forceinline__ bool next_segment(const DraftArgs& a, long long& pos, long long hi, Segment& sg,
-                                             bool& over_capacity) {
-  if (pos >= hi) return false;
-  sg.bh = static_cast<int>(pos / a.NGmax);
-  sg.gs = static_cast<int>(pos % a.NGmax);
-  const int ge = static_cast<int>(min(static_cast<long long>(a.NGmax), sg.gs + (hi - pos)));
-  pos += ge - sg.gs;
-  int ng_req = a.packed_len[sg.bh / a.Hkv] / kGroup;
-  over_capacity = ng_req > a.NGmax;
-  if (over_capacity) ng_req = a.NGmax;
-  sg.n_valid = max(0, min(ge, ng_req) - sg.gs);
-  sg.n_tiles = (sg.n_valid + kTileGroups - 1) / kTileGroups;
-  return true;
+
+// Shared memory the tail CTA needs inside the same allocation (rows of the tail
+// K/V plus its scores); checked on the host against Plan::off_q.
+template <int D, int G>
+__host__ __device__ inline size_t tail_smem(int tail_cap) {
+  return 2 * static_cast<size_t>(tail_cap + 1) * D * 2 + static_cast<size_t>(G) * (tail_cap + 1) * 4 + 64;
 }
 
-// ------------------------------------------------------------------ roles and shared memory
-template <int D>
-struct Roles {
-  static constexpr int chan_warps = D / 32;                   // channel warp c: channels 32c.., TMEM lanes 32c..
-  static constexpr int compute_warps = kTokWarps + chan_warps;
-  static constexpr int compute_threads = 32 * compute_warps;
-  static constexpr int producer_warp = compute_warps;    // then the products' warp
-  static constexpr int threads = 32 * (compute_warps + 2);
-};
-
-template <int D, int BITS>
-struct Plan {
-  static constexpr uint32_t kcb = D * BITS * 4;               // one group's K codes (bytes)
-  static constexpr uint32_t kmb = D * 4;                      // one group's K scale/zero
-  static constexpr uint32_t vcb = D * BITS * 4;
-  static constexpr uint32_t vmb = D * 4;
-  static constexpr uint32_t off_kc = 0;
-  static constexpr uint32_t off_km = off_kc + kTileGroups * kcb;
-  static constexpr uint32_t off_vc = off_km + kTileGroups * kmb;
-  static constexpr uint32_t off_vm = off_vc + kTileGroups * vcb;
-  static constexpr uint32_t stage = off_vm + kTileGroups * vmb;
-  static constexpr int NS = (96 * 1024 / stage) < 2 ? 2 : ((96 * 1024 / stage) > 8 ? 8 : static_cast<int>(96 * 1024 / stage));
-  static constexpr uint32_t ring = stage * NS;
-  // B operands: Q [16 heads x D] K-major core matrices (8 rows x 16 B; K step
-  // 128 B, 8-row step 16 D B), P [128 tokens x 16 heads] MN-major (8 tokens x
-  // 8 heads per 128 B core matrix; head step 128 B, token step 256 B)
-  static constexpr uint32_t q_bytes = kN * D * 2;
-  static constexpr uint32_t p_bytes = kTile * kN * 2;
-  static constexpr uint32_t off_q = ring;                     // [2] by segment parity
-  static constexpr uint32_t off_p = off_q + 2 * q_bytes;      // [2] by tile parity
-  static constexpr uint32_t off_mt = off_p + 2 * p_bytes;                   // max of a tile [2][kN]
-  static constexpr uint32_t off_red = off_mt + 2 * kN * 4;                   // [4][kN] exchange
-  static constexpr uint32_t off_bar = off_red + kTokWarps * kN * 4;
-  // full[NS], empty[NS], then [2] each of: ak, sf, av, pr, of, ofree, mr; done
-  static constexpr int n_bars = 2 * NS + 15;
-  static constexpr uint32_t off_misc = off_bar + n_bars * 8;  // TMEM base, combine flag, abort flag
-  static constexpr uint32_t total = off_misc + 16;
-  static_assert(stage % 16 == 0 && off_bar % 8 == 0, "alignment");
-  static_assert(total <= 227 * 1024, "shared memory");
-};
-
-// TMEM columns: A_K[2] (D/2 each), A_V[2] (64 each), S[2], O[2] (16 each).
-template <int D>
-struct Cols {
-  static constexpr uint32_t ak = 0, av = D, s = D + 2 * (kTile / 2), o = s + 2 * kN;
-  static constexpr uint32_t used = o + 2 * kN;
-  static constexpr uint32_t alloc = used <= 256 ? 256 : 512;
-};
-
-// Shared memory the tail CTA uses (rows of the tail K/V, scores, fp32 queries,
-// per-head (max, sum), combine flag); checked on the host against Plan::total.
 template <int D, int G>
-struct TailPlan {
-  __host__ __device__ static size_t rows(int cap) { return 2 * static_cast<size_t>(cap + 1) * D * 2; }
-  __host__ __device__ static size_t off_sc(int cap) { return rows(cap); }
-  __host__ __device__ static size_t off_q(int cap) { return (off_sc(cap) + static_cast<size_t>(G) * (cap + 1) * 4 + 15) & ~size_t(15); }
-  __host__ __device__ static size_t off_ml(int cap) { return off_q(cap) + static_cast<size_t>(G) * D * 4; }
-  __host__ __device__ static size_t off_flag(int cap) { return off_ml(cap) + static_cast<size_t>(G) * 2 * 4; }
-  __host__ __device__ static size_t total(int cap) { return off_flag(cap) + 16; }
-};
+__device__ __forceinline__ void load_q(const DraftArgs& a, int b, int kvh, float* q_s) {
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    const int h = i / D, c = i % D;
+    q_s[i] = vc_bf16_to_f32(a.q[(static_cast<size_t>(b) * a.Hq + kvh * G + h) * D + c]) * a.scale_log2;
+  }
+}
 
-// ------------------------------------------------------------------ small device pieces
-__device__ __forceinline__ float fast_exp2(float x) {   // ex2.approx.ftz: relative error ~2^-22
+// Issue the bulk copies of one stage (groups [g, g + n) of slice bh) into `buf`.
+template <int D, int BITS, int G>
+__device__ __forceinline__ void issue_stage(const DraftArgs& a, uint8_t* buf, uint64_t* bar, int bh, int g, int n) {
+  using P = Plan<D, BITS, G>;
+  const size_t gb = static_cast<size_t>(bh) * a.NG + g;
+  const uint32_t code_bytes = static_cast<uint32_t>(n * P::codes);
+  const uint32_t meta_bytes = static_cast<uint32_t>(n * P::meta);
+  vc_mbar_arrive_expect_tx(bar, 2 * code_bytes + 2 * meta_bytes);
+  vc_bulk_g2s(buf, a.kc + gb * D * BITS, code_bytes, bar);
+  vc_bulk_g2s(buf + P::kc, a.ksz + gb * 2 * D, meta_bytes, bar);
+  vc_bulk_g2s(buf + P::kc + P::mt, a.vc + gb * D * BITS, code_bytes, bar);
+  vc_bulk_g2s(buf + 2 * P::kc + P::mt, a.vsz + gb * 2 * D, meta_bytes, bar);
+}
+
+// ------------------------------------------------------------------ tensor-core pieces
+// 16x8x16 products, fp16 operands, fp32 accumulators.  Lane = 4*gid + tig.
+// A rows: gid = head gid (leading part), gid + 8 = the same head (remainder
+// part), so that hi + lo carry ~22 significant bits of a product that fp16
+// alone would round to 11.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 2^x (ex2.approx.ftz: relative error ~2^-22; results below 2^-126 flush to 0)
+__device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
-// Operand pair of field k of packed word w: the field of both half-words moved
-// into the top mantissa bits of the fp16 pattern of f, giving y = f + code
-// exactly.  b = 2: field k at bit 2k; one shift puts the odd field of a nibble
-// at bits 8-9 (f = 4) and the even one at bits 6-7 (f = 16).  b = 4: bits 6-9
-// (f = 16).  b = 8: bits 2-9 (f = 256).
+
+// (hi, lo) of x*y: hi = fp16(x*y), lo = fp16(x*y - hi) (the residual of the
+// exact product; exact itself when x and y carry <= 22 significant bits).
+__device__ __forceinline__ void split_mul(__half2 x, __half2 y, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __hmul2(x, y);
+  hi = h2u(h);
+  lo = h2u(__hfma2(x, y, __hneg2(h)));
+}
+
+// Operand value of a packed code field: OR the field (moved to the top
+// mantissa bits by slot_shift) into the bit pattern of 1.0: 1 + code/f exactly.
+//   b = 2, r = 0: bits 8-9 of each half -> 1 + code/4   (f = 4)
+//   b = 2, r = 1: bits 6-7              -> 1 + code/16  (f = 16)
+//   b = 4:        bits 6-9              -> 1 + code/16  (f = 16)
+//   b = 8:        bits 2-9              -> 1 + code/256 (f = 256)
 template <int BITS>
-__device__ __forceinline__ uint32_t pair_operand(uint32_t w, int k) {
+__device__ __forceinline__ uint32_t field_value(uint32_t x, int r) {
+  if (BITS == 2) return r == 0 ? ((x & 0x03000300u) | 0x3C003C00u) : ((x & 0x00C000C0u) | 0x3C003C00u);
+  if (BITS == 8) return (x & 0x03FC03FCu) | 0x3C003C00u;
+  return (x & 0x03C003C0u) | 0x3C003C00u;
+}
+template <int BITS>
+__host__ __device__ constexpr float field_scale(int r) {
+  return BITS == 8 ? 256.0f : ((BITS == 2 && r == 0) ? 4.0f : 16.0f);
+}
+template <int BITS>
+__host__ __device__ constexpr float field_log2(int r) {
+  return BITS == 8 ? 8.0f : ((BITS == 2 && r == 0) ? 2.0f : 4.0f);
+}
+
+// Word w moved so that slot u's fields land in the operand windows: the e = 0
+// field of slot u starts at 4u + 2(1 - r) (b = 2) or 4u (b = 4), so a shift by
+// 4u - 6 brings it to bit 8 (r = 0) / bit 6 (r = 1, b = 4); the e = 1 field,
+// 16 bits higher, lands 16 bits higher too.  One plain shift, nothing wraps.
+__device__ __forceinline__ uint32_t slot_shift(uint32_t w, int u) {
+  return u == 0 ? (w << 6) : u == 1 ? (w << 2) : u == 2 ? (w >> 2) : (w >> 6);
+}
+// b = 8: the e = 0 field of slot u starts at 8u; a shift by 8u - 2 brings it to bit 2.
+__device__ __forceinline__ uint32_t slot_shift8(uint32_t w, int u) { return u == 0 ? (w << 2) : (w >> 6); }
+
+// Operand registers (r = 0, 1) of fragment index i — the field rules of the
+// packed words (include/vc.h): b = 2: word i/4, slot u = i%4; b = 4: i2 = 2i + r,
+// word i2/4, slot u = i2%4; b = 8: word (2i + r)/2 = i, slot u = r.
+template <int BITS, int WPL>
+__device__ __forceinline__ void fragment(const uint32_t (&w)[WPL], int i, uint32_t& b0, uint32_t& b1) {
   if (BITS == 2) {
-    const int u = k >> 1;
-    const uint32_t x = u == 0 ? (w << 6) : u == 1 ? (w << 2) : u == 2 ? (w >> 2) : (w >> 6);
-    return (k & 1) ? ((x & 0x03000300u) | 0x44004400u) : ((x & 0x00C000C0u) | 0x4C004C00u);
+    const uint32_t x = slot_shift(w[i / 4], i % 4);
+    b0 = field_value<2>(x, 0);
+    b1 = field_value<2>(x, 1);
   } else if (BITS == 4) {
-    const uint32_t x = k == 0 ? (w << 6) : k == 1 ? (w << 2) : k == 2 ? (w >> 2) : (w >> 6);
-    return (x & 0x03C003C0u) | 0x4C004C00u;
-  } else {
-    const uint32_t x = k == 0 ? (w << 2) : (w >> 6);
-    return (x & 0x03FC03FCu) | 0x5C005C00u;
-  }
-}
-// f of field k (the fp16 pattern pair_operand ORs the field into).
-template <int BITS>
-__host__ __device__ constexpr float field_f(int k) {
-  return BITS == 2 ? ((k & 1) ? 4.0f : 16.0f) : (BITS == 4 ? 16.0f : 256.0f);
-}
-// x^ = fma(y - f, s, z) for an operand pair y = f + code: y - f = code is exact,
-// so x^ is the correctly rounded fp16 of code s + z (two elements at once).
-template <int BITS>
-__device__ __forceinline__ uint32_t dequant2(uint32_t y, int k, uint32_t s, uint32_t z) {
-  return h2u(__hfma2(__hsub2(u2h(y), __float2half2_rn(field_f<BITS>(k))), u2h(s), u2h(z)));
-}
-
-// ------------------------------------------------------------------ token warp: K rows
-// Dequantise token t's K row into the warp's TMEM lanes of A_K at column ta
-// (pair m = channels 2m, 2m+1 at column m).  kc_g: the group's K codes, 32
-// token rows of W = D*BITS/32 words stored in chunks of 4 words (word w of
-// token t at ((w/4)*32 + t)*4 + w%4, so the warp's 16-byte loads cover
-// contiguous 512 bytes); km: the group's scales then zeros, fp16 pairs.
-template <int D, int BITS>
-__device__ __forceinline__ void dequant_k_row(const uint32_t* kc_g, const uint32_t* km, int t, uint32_t ta) {
-  constexpr int W = D * BITS / 32;
-  constexpr int PH = 16 / BITS;                  // pairs per word
-  uint32_t wv[W];
-#pragma unroll
-  for (int ch = 0; ch < W / 4; ++ch) {
-    const uint4 v = *reinterpret_cast<const uint4*>(kc_g + (ch * 32 + t) * 4);
-    wv[4 * ch] = v.x; wv[4 * ch + 1] = v.y; wv[4 * ch + 2] = v.z; wv[4 * ch + 3] = v.w;
-  }
-  uint32_t r[16];
-#pragma unroll
-  for (int m0 = 0; m0 < D / 2; m0 += 4) {        // 4 pairs: one 16-byte load of scales, one of zeros
-    const uint4 s4 = *reinterpret_cast<const uint4*>(km + m0);
-    const uint4 z4 = *reinterpret_cast<const uint4*>(km + D / 2 + m0);
-    const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w}, zv[4] = {z4.x, z4.y, z4.z, z4.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int m = m0 + i, k = m % PH;
-      r[m & 15] = dequant2<BITS>(pair_operand<BITS>(wv[m / PH], k), k, sv[i], zv[i]);
-    }
-    if (((m0 + 3) & 15) == 15) vc_tc_st16(ta + (m0 + 3 - 15), r);
+    const int i0 = 2 * i, i1 = 2 * i + 1;
+    b0 = field_value<4>(slot_shift(w[i0 / 4], i0 % 4), 0);
+    b1 = field_value<4>(slot_shift(w[i1 / 4], i1 % 4), 1);
+  } else {                                   // b = 8: word i holds slots u = 0 (r = 0) and 1 (r = 1)
+    b0 = field_value<8>(slot_shift8(w[i], 0), 0);
+    b1 = field_value<8>(slot_shift8(w[i], 1), 1);
   }
 }
 
-// ------------------------------------------------------------------ channel warp: V rows
-// Dequantise channel ch's V row of one group (its 32 tokens: pair m = tokens
-// 2m, 2m+1) into the warp's TMEM lanes at column ta .. ta + 15.  vc_g: the
-// group's V codes, D channel rows of BITS words in chunks of min(BITS, 4)
-// words; vm: the scales then zeros of the channel's 32-channel group, fp16 pairs.
+// The lane's words of one group: word w at (w/4)*128 + 4*lane + w%4.
+template <int WPL>
+__device__ __forceinline__ void load_lane_words(const uint32_t* g, int lane, uint32_t (&w)[WPL]) {
+#pragma unroll
+  for (int c = 0; c < WPL / 4; ++c) {
+    const uint4 v = *reinterpret_cast<const uint4*>(g + c * 128 + 4 * lane);
+    w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+  }
+}
+
+// Per-warp running state of one segment: rows = the lane's head gid.
+template <int D>
+struct WarpState {
+  static constexpr int NT = D / 8;
+  float o[NT][4];       // PV accumulators: cols 8nt + 2tig (+1), rows gid / gid+8
+  float oz[4];          // correction columns (2g: zeros, 2g+1: scales) of group g = tig
+  float l0, l1;         // sums of the softmax weights of r = 0 / r = 1 tokens (times f_r)
+  float m;              // running max (log2 units) the weights are relative to
+};
+
+// Rescale threshold (log2 units): the running max is raised only when a group's
+// max exceeds it by more than this, so weights stay <= 2^kLazy * 16.
+constexpr float kLazy = 3.0f;
+
+// One group of 32 tokens for the lane's head (row gid), all on tensor cores.
+//
+//   score(t) = sum_c q_c (s_c code_tc + z_c)
+//            = sum_c (f_c q_c s_c)(1 + code_tc / f_c) + sum_c q_c (z_c - f_c s_c)
+// The first sum is one product per n-tile with A = f q s split into (hi, lo)
+// fp16 rows and B = the codes' operand values; the second ("bias") is one
+// product per k-step with A = f q (exact in fp16) and B columns z / f and -s.
+//   out_h = sum_t p_t (sv_t code_tc + zv_t)
+//         = sum_t (f_t p_t sv_t)(1 + code_tc / f_t) + sum_t (f_t p_t)(zv_t / f_t - sv_t)
+// likewise with one A per channel group (sv depends on the group) and one
+// correction product whose columns are (zv / f, -sv) per channel group.
 template <int D, int BITS>
-__device__ __forceinline__ void dequant_v_row(const uint32_t* vc_g, const uint32_t* vm, int ch, uint32_t ta) {
-  constexpr int PH = 16 / BITS;
-  uint32_t wv[BITS];
-  if (BITS == 2) {
-    const uint2 v = *reinterpret_cast<const uint2*>(vc_g + ch * 2);
-    wv[0] = v.x;
-    wv[1] = v.y;
-  } else {
+__device__ __forceinline__ void group_mma(const uint32_t* kc_g, const uint16_t* ksz_g, const uint32_t* vc_g,
+                                          const uint16_t* vsz_g, const uint32_t (&qf)[D / 16][2],
+                                          uint32_t bias_mul0, uint32_t bias_mul1,
+                                          uint32_t zcol_mul0, uint32_t zcol_mul1, int zcol_off, float cs,
+                                          WarpState<D>& st, int lane) {
+  constexpr int KS = D / 16, NT = D / 8, NCG = D / 32, WPL = D * BITS / 32;
+  const int gid = lane >> 2, tig = lane & 3;
+  // ---------------- QK
+  uint32_t kw[WPL];
+  load_lane_words<WPL>(kc_g, lane, kw);
+  // scales of the lane's channels (D/4) tig + 4ks + 2r + {0, 1}: one half2 per (ks, r)
+  const uint32_t* srow = reinterpret_cast<const uint32_t*>(ksz_g) + (D / 8) * tig;
+  const uint32_t* zrow = reinterpret_cast<const uint32_t*>(ksz_g) + (gid == 0 ? D / 2 : 0) + (D / 8) * tig;
+  float c[4][4];
 #pragma unroll
-    for (int c4 = 0; c4 < BITS / 4; ++c4) {
-      const uint4 v = *reinterpret_cast<const uint4*>(vc_g + (c4 * D + ch) * 4);
-      wv[4 * c4] = v.x; wv[4 * c4 + 1] = v.y; wv[4 * c4 + 2] = v.z; wv[4 * c4 + 3] = v.w;
+  for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
+  float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int kq = 0; kq < KS / 2; ++kq) {
+    const uint4 s4 = *reinterpret_cast<const uint4*>(srow + 4 * kq);     // (ks, r) = (2kq, 0), (2kq, 1), (2kq+1, 0), (2kq+1, 1)
+    const uint4 z4 = *reinterpret_cast<const uint4*>(zrow + 4 * kq);
+    const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
+    const uint32_t zv[4] = {z4.x, z4.y, z4.z, z4.w};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int ks = 2 * kq + h;
+      uint32_t a0, a1, a2, a3;
+      split_mul(u2h(qf[ks][0]), u2h(sv[2 * h]), a0, a1);
+      split_mul(u2h(qf[ks][1]), u2h(sv[2 * h + 1]), a2, a3);
+      mma16816(cb, qf[ks][0], 0u, qf[ks][1], 0u, h2u(__hmul2(u2h(zv[2 * h]), u2h(bias_mul0))),
+               h2u(__hmul2(u2h(zv[2 * h + 1]), u2h(bias_mul1))));
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t b0, b1;
+        fragment<BITS, WPL>(kw, j * KS + ks, b0, b1);
+        mma16816(c[j], a0, a1, a2, a3, b0, b1);
+      }
     }
   }
-  uint32_t r[16];
+  // bias of row gid: columns 0 (q.z) and 1 (-q.f s) live in the quad's tig 0 lane
+  const float bias = __shfl_sync(0xffffffffu, cb[0] + cb[1], lane & ~3);
+  // ---------------- online softmax (row gid; tokens 8 tig + 4e + j)
+  float y[4][2];
+  float my = -INFINITY;
 #pragma unroll
-  for (int m0 = 0; m0 < 16; m0 += 4) {
-    const uint4 s4 = *reinterpret_cast<const uint4*>(vm + m0);
-    const uint4 z4 = *reinterpret_cast<const uint4*>(vm + 16 + m0);
-    const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w}, zv[4] = {z4.x, z4.y, z4.z, z4.w};
+  for (int j = 0; j < 4; ++j)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int m = m0 + i, k = m % PH;
-      r[m] = dequant2<BITS>(pair_operand<BITS>(wv[m / PH], k), k, sv[i], zv[i]);
+    for (int e = 0; e < 2; ++e) {
+      y[j][e] = c[j][e] + c[j][2 + e];
+      my = fmaxf(my, y[j][e]);
+    }
+  my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 1));
+  my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 2));
+  const float mx = (my + bias) * cs;
+  const bool need = !(mx <= st.m + kLazy);
+  if (__any_sync(0xffffffffu, need)) {
+    const float mn = need ? mx : st.m;
+    const float alpha = fast_exp2(st.m - mn);          // m = -inf at the start: alpha = 0
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) st.o[nt][k] *= alpha;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) st.oz[k] *= alpha;
+    st.l0 *= alpha;
+    st.l1 *= alpha;
+    st.m = mn;
+  }
+  const float k0 = fmaf(bias, cs, -st.m);
+  // weights times f_r (r = j % 2), split into fp16 (hi, lo)
+  uint32_t ph[4], pl[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float kk = k0 + field_log2<BITS>(j & 1);
+    const float p0 = fast_exp2(fmaf(y[j][0], cs, kk));
+    const float p1 = fast_exp2(fmaf(y[j][1], cs, kk));
+    if (j & 1) st.l1 += p0 + p1; else st.l0 += p0 + p1;
+    const __half2 h = __floats2half2_rn(p0, p1);
+    const float2 hf = __half22float2(h);
+    ph[j] = h2u(h);
+    pl[j] = h2u(__floats2half2_rn(p0 - hf.x, p1 - hf.y));
+  }
+  // ---------------- PV
+  uint32_t vw[WPL];
+  load_lane_words<WPL>(vc_g, lane, vw);
+  // correction columns: lane gid feeds column gid = (group gid/2, zeros | scales)
+  {
+    const uint4 r4 = *reinterpret_cast<const uint4*>(vsz_g + zcol_off + 8 * tig);
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const uint32_t b0 = h2u(__hmul2(u2h(s ? r4.z : r4.x), u2h(zcol_mul0)));
+      const uint32_t b1 = h2u(__hmul2(u2h(s ? r4.w : r4.y), u2h(zcol_mul1)));
+      mma16816(st.oz, ph[2 * s], pl[2 * s], ph[2 * s + 1], pl[2 * s + 1], b0, b1);
     }
   }
-  vc_tc_st16(ta, r);
+#pragma unroll
+  for (int g = 0; g < NCG; ++g) {
+    const uint4 s4 = *reinterpret_cast<const uint4*>(vsz_g + g * 64 + 8 * tig);   // (s, r) = (0,0), (0,1), (1,0), (1,1)
+    const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      uint32_t a[4];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const __half2 x = u2h(ph[2 * s + r]), sc = u2h(sv[2 * s + r]);
+        const __half2 h = __hmul2(x, sc);
+        a[2 * r] = h2u(h);
+        a[2 * r + 1] = h2u(__hfma2(u2h(pl[2 * s + r]), sc, __hfma2(x, sc, __hneg2(h))));
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int nt = 4 * g + u;
+        uint32_t b0, b1;
+        fragment<BITS, WPL>(vw, s * NT + nt, b0, b1);
+        mma16816(st.o[nt], a[0], a[1], a[2], a[3], b0, b1);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ transposed group product (G = 4)
+// With G = 4 the 16 rows of a product above carry only 8 of 16 (hi, lo) query
+// rows.  Here the roles swap: S^T = codes . Q'^T and O^T = V^T . P'^T, with
+// the codes as the A operand (16 tokens or 16 channels per tile) and the
+// 4 heads' hi and lo parts as the 8 columns: 16 QK + 16 PV products per group
+// instead of 32 + 32.  The packed words need no change: the B fragment of
+// n-tile j is the top (b0) / bottom (b1) register pair of an A fragment whose
+// rows are the tokens of n-tiles j and j' (a0 = b0 of j, a1 = b0 of j',
+// a2 = b1 of j, a3 = b1 of j').  The QK accumulator block of tokens 4 gid + j
+// (j = 2 mt + half), transposed in registers (movmatrix), is the PV B fragment
+// of k-step s = j / 2, register r = j % 2.
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Per-warp running state of one segment, transposed: the lane's heads are
+// h0 = 2 (tig & 1) and h0 + 1.
+template <int D>
+struct WarpStateT {
+  static constexpr int MT = D / 16;
+  float o[MT][4];       // O^T: rows = channels 16 mt + gid (+ 8), cols 2 tig (+1) = (lo if tig >= 2) of heads h0 (+1)
+  float oz[4];          // correction: rows = P' columns (gid: lo if >= 4, head gid & 3), cols = (channel group tig, zeros | scales)
+  float l0[2], l1[2];   // per head: sums of the weights of r = 0 / r = 1 tokens (times f_r)
+  float m[2];           // per head: running max (log2 units)
+};
+
+template <int D, int G>
+struct StateOf {
+  using type = WarpState<D>;
+};
+template <int D>
+struct StateOf<D, 4> {
+  using type = WarpStateT<D>;
+};
+
+template <int D>
+__device__ __forceinline__ void init_state(WarpState<D>& st) {
+#pragma unroll
+  for (int nt = 0; nt < D / 8; ++nt) st.o[nt][0] = st.o[nt][1] = st.o[nt][2] = st.o[nt][3] = 0.0f;
+  st.oz[0] = st.oz[1] = st.oz[2] = st.oz[3] = 0.0f;
+  st.l0 = st.l1 = 0.0f;
+  st.m = -INFINITY;
+}
+template <int D>
+__device__ __forceinline__ void init_state(WarpStateT<D>& st) {
+#pragma unroll
+  for (int m = 0; m < D / 16; ++m) st.o[m][0] = st.o[m][1] = st.o[m][2] = st.o[m][3] = 0.0f;
+  st.oz[0] = st.oz[1] = st.oz[2] = st.oz[3] = 0.0f;
+  st.l0[0] = st.l0[1] = st.l1[0] = st.l1[1] = 0.0f;
+  st.m[0] = st.m[1] = -INFINITY;
+}
+
+template <int D, int BITS>
+__device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t* ksz_g, const uint32_t* vc_g,
+                                            const uint16_t* vsz_g, const uint32_t (&qf)[D / 16][2],
+                                            uint32_t bias_mul0, uint32_t bias_mul1,
+                                            uint32_t zcol_mul0, uint32_t zcol_mul1, int zcol_off, float cs,
+                                            WarpStateT<D>& st, int lane) {
+  constexpr int KS = D / 16, NT = D / 8, NCG = D / 32, WPL = D * BITS / 32;
+  const int gid = lane >> 2, tig = lane & 3;
+  const bool lo_p = tig >= 2;                   // P block columns 2 tig (+1): remainder parts
+  const int h0 = 2 * (tig & 1);
+  // ---------------- S^T = codes . Q'^T
+  uint32_t kw[WPL];
+  load_lane_words<WPL>(kc_g, lane, kw);
+  const uint32_t* srow = reinterpret_cast<const uint32_t*>(ksz_g) + (D / 8) * tig;
+  const uint32_t* zrow = reinterpret_cast<const uint32_t*>(ksz_g) + (gid == 0 ? D / 2 : 0) + (D / 8) * tig;
+  float c[2][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) c[mt][0] = c[mt][1] = c[mt][2] = c[mt][3] = 0.0f;
+  float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int kq = 0; kq < KS / 2; ++kq) {
+    const uint4 s4 = *reinterpret_cast<const uint4*>(srow + 4 * kq);
+    const uint4 z4 = *reinterpret_cast<const uint4*>(zrow + 4 * kq);
+    const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
+    const uint32_t zv[4] = {z4.x, z4.y, z4.z, z4.w};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int ks = 2 * kq + h;
+      // Q'^T columns gid and gid + 4 both carry head gid & 3 (fp16 f q s)
+      const uint32_t qb0 = h2u(__hmul2(u2h(qf[ks][0]), u2h(sv[2 * h])));
+      const uint32_t qb1 = h2u(__hmul2(u2h(qf[ks][1]), u2h(sv[2 * h + 1])));
+      mma16816(cb, qf[ks][0], 0u, qf[ks][1], 0u, h2u(__hmul2(u2h(zv[2 * h]), u2h(bias_mul0))),
+               h2u(__hmul2(u2h(zv[2 * h + 1]), u2h(bias_mul1))));
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        fragment<BITS, WPL>(kw, (2 * mt) * KS + ks, a0, a2);
+        fragment<BITS, WPL>(kw, (2 * mt + 1) * KS + ks, a1, a3);
+        mma16816(c[mt], a0, a1, a2, a3, qb0, qb1);
+      }
+    }
+  }
+  // bias of head h: row h of the bias product, columns 0 (q.z) and 1 (-q.f s) in lane 4 h
+  const float cbs = cb[0] + cb[1];
+  const float bias[2] = {__shfl_sync(0xffffffffu, cbs, 4 * h0), __shfl_sync(0xffffffffu, cbs, 4 * h0 + 4)};
+  // y[mt][2 half + hh] = score of token 4 gid + 2 mt + half, head h0 + hh (columns
+  // 2 tig, 2 tig + 1 hold heads h0, h0 + 1 in both column halves)
+  float (&y)[2][4] = c;
+  // ---------------- online softmax, one state per head
+  float mx[2];
+  bool need[2];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    float my = fmaxf(fmaxf(y[0][hh], y[0][2 + hh]), fmaxf(y[1][hh], y[1][2 + hh]));
+    my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 4));
+    my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 8));
+    my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 16));
+    mx[hh] = (my + bias[hh]) * cs;
+    need[hh] = !(mx[hh] <= st.m[hh] + kLazy);
+  }
+  if (__any_sync(0xffffffffu, need[0] || need[1])) {
+    float alpha[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float mn = need[hh] ? mx[hh] : st.m[hh];
+      alpha[hh] = fast_exp2(st.m[hh] - mn);     // m = -inf at the start: alpha = 0
+      st.l0[hh] *= alpha[hh];
+      st.l1[hh] *= alpha[hh];
+      st.m[hh] = mn;
+    }
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      st.o[mt][0] *= alpha[0];
+      st.o[mt][1] *= alpha[1];
+      st.o[mt][2] *= alpha[0];
+      st.o[mt][3] *= alpha[1];
+    }
+    // correction rows belong to head gid & 3: its factor sits in lane (gid, (gid & 3) >> 1)
+    const float a_g = (gid & 1) ? alpha[1] : alpha[0];
+    const float a_oz = __shfl_sync(0xffffffffu, a_g, 4 * gid + ((gid & 3) >> 1));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) st.oz[k] *= a_oz;
+  }
+  const float kk[2] = {fmaf(bias[0], cs, -st.m[0]), fmaf(bias[1], cs, -st.m[1])};
+  // weights times f_r (r = token parity = half) in fp16; block j = 2 mt + half
+  uint32_t ph[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int mt = j >> 1, half = j & 1;
+    const float lf = field_log2<BITS>(half);
+    const float p0 = fast_exp2(fmaf(y[mt][2 * half], cs, kk[0] + lf));
+    const float p1 = fast_exp2(fmaf(y[mt][2 * half + 1], cs, kk[1] + lf));
+    if (half) {
+      st.l1[0] += p0;
+      st.l1[1] += p1;
+    } else {
+      st.l0[0] += p0;
+      st.l0[1] += p1;
+    }
+    ph[j] = h2u(__floats2half2_rn(p0, p1));
+  }
+  // ---------------- correction: A = P' blocks transposed (rows = P' columns; rows 4-7 zero), B = meta columns
+  {
+    uint32_t pu[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) pu[j] = movmatrix_t(lo_p ? 0u : ph[j]);
+    const uint4 r4 = *reinterpret_cast<const uint4*>(vsz_g + zcol_off + 8 * tig);
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const uint32_t b0 = h2u(__hmul2(u2h(s ? r4.z : r4.x), u2h(zcol_mul0)));
+      const uint32_t b1 = h2u(__hmul2(u2h(s ? r4.w : r4.y), u2h(zcol_mul1)));
+      mma16816(st.oz, pu[2 * s], 0u, pu[2 * s + 1], 0u, b0, b1);
+    }
+  }
+  // ---------------- O^T += V^T . P'^T, one P'^T per channel group (the value scales of its tokens)
+  uint32_t vw[WPL];
+  load_lane_words<WPL>(vc_g, lane, vw);
+#pragma unroll
+  for (int g = 0; g < NCG; ++g) {
+    // scales of tokens 4 gid + j: entry 8 (gid >> 1) + 2 j + (gid & 1) of the group's scale row
+    const uint4 s4 = *reinterpret_cast<const uint4*>(vsz_g + g * 64 + 8 * (gid >> 1));
+    const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w};
+    const uint32_t sel = (gid & 1) ? 0x3232u : 0x1010u;
+    uint32_t pb[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t sv2;
+      asm("prmt.b32 %0, %1, %1, %2;" : "=r"(sv2) : "r"(sw[j]), "r"(sel));   // (sv, sv) of token 4 gid + j
+      pb[j] = movmatrix_t(lo_p ? 0u : h2u(__hmul2(u2h(ph[j]), u2h(sv2))));   // every lane transposes
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int m = 2 * g + u;                  // channels 16 m .. 16 m + 15 = n-tiles 2 m, 2 m + 1
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        uint32_t a0, a1, a2, a3;
+        fragment<BITS, WPL>(vw, s * NT + 2 * m, a0, a2);
+        fragment<BITS, WPL>(vw, s * NT + 2 * m + 1, a1, a3);
+        mma16816(st.o[m], a0, a1, a2, a3, pb[2 * s], pb[2 * s + 1]);
+      }
+    }
+  }
 }
 
 // ------------------------------------------------------------------ merge / arrive / combine
-// Barrier over `nthr` threads: the whole tail CTA, or the compute warps of a
-// stream CTA (named barrier 2).
-__device__ __forceinline__ void sync_part(int nthr) {
-  if (nthr == static_cast<int>(blockDim.x)) __syncthreads(); else vc_bar_sync(2, nthr);
+template <int D, int BITS, int G>
+__device__ void merge_partials(const DraftArgs& a, uint8_t* smem, int bh, int slot);
+
+// Partial of this CTA for slice bh: merge the warps' (max, sum, output) in
+// shared memory and write one normalised partial + log2-sum-exp per head.
+template <int D, int BITS, int G>
+__device__ void write_partial(const DraftArgs& a, uint8_t* smem, int bh, int slot, WarpState<D>& st) {
+  using P = Plan<D, BITS, G>;
+  constexpr int NT = D / 8, NCG = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  float* red = reinterpret_cast<float*>(smem + P::off_red);             // [warp][G][D]
+  float* wstat = reinterpret_cast<float*>(smem + P::off_wstat);         // [warp][8][2]
+  // correction of channel group g for row gid sits in lane (gid, g)
+  const float ozl = st.oz[0] + st.oz[1] + st.oz[2] + st.oz[3];
+  float ozg[NCG];
+#pragma unroll
+  for (int g = 0; g < NCG; ++g) ozg[g] = __shfl_sync(0xffffffffu, ozl, (lane & ~3) | g);
+  float l = st.l0 * (1.0f / field_scale<BITS>(0)) + st.l1 * (1.0f / field_scale<BITS>(1));
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  if (gid < G) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float2 v;
+      v.x = st.o[nt][0] + st.o[nt][2] + ozg[nt / 4];
+      v.y = st.o[nt][1] + st.o[nt][3] + ozg[nt / 4];
+      *reinterpret_cast<float2*>(red + (warp * G + gid) * D + 8 * nt + 2 * tig) = v;
+    }
+    if (tig == 0) {
+      wstat[(warp * 8 + gid) * 2] = st.m;
+      wstat[(warp * 8 + gid) * 2 + 1] = l;
+    }
+  }
+  vc_bar_sync(1, kConsumers);
+  merge_partials<D, BITS, G>(a, smem, bh, slot);
+}
+
+// The warps' (max, sum, output) of slice bh, left in `red` / `wstat` by the
+// consumer warps (after a consumer barrier), merged into one normalised
+// partial + log2-sum-exp per head.
+template <int D, int BITS, int G>
+__device__ void merge_partials(const DraftArgs& a, uint8_t* smem, int bh, int slot) {
+  using P = Plan<D, BITS, G>;
+  const float* red = reinterpret_cast<const float*>(smem + P::off_red);
+  const float* wstat = reinterpret_cast<const float*>(smem + P::off_wstat);
+  const int b = bh / a.Hkv, kvh = bh % a.Hkv;
+  for (int i = threadIdx.x; i < G * D; i += kConsumers) {
+    const int h = i / D, c = i % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int x = 0; x < kWarps; ++x) M = fmaxf(M, wstat[(x * 8 + h) * 2]);
+    const size_t row = static_cast<size_t>(b * a.Hq + kvh * G + h) * a.max_parts + slot;
+    if (M == -INFINITY) {
+      if (c == 0) a.part_lse[row] = -INFINITY;
+      continue;
+    }
+    float o = 0.0f, Ls = 0.0f;
+#pragma unroll
+    for (int x = 0; x < kWarps; ++x) {
+      const float mx = wstat[(x * 8 + h) * 2];
+      if (mx == -INFINITY) continue;
+      const float wgt = exp2f(mx - M);
+      o = fmaf(wgt, red[(x * G + h) * D + c], o);
+      Ls = fmaf(wgt, wstat[(x * 8 + h) * 2 + 1], Ls);
+    }
+    a.part_o[row * D + c] = o / Ls;
+    if (c == 0) a.part_lse[row] = M + log2f(Ls);
+  }
+}
+
+// write_partial for the transposed state: per head the hi + lo columns, the
+// correction of each channel group, the softmax sum over the warp's tokens.
+template <int D, int BITS, int G>
+__device__ void write_partial_t(const DraftArgs& a, uint8_t* smem, int bh, int slot, WarpStateT<D>& st) {
+  using P = Plan<D, BITS, G>;
+  static_assert(G == 4, "the transposed product carries 4 heads");
+  constexpr int MT = D / 16, NCG = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int h0 = 2 * (tig & 1);
+  float* red = reinterpret_cast<float*>(smem + P::off_red);             // [warp][G][D]
+  float* wstat = reinterpret_cast<float*>(smem + P::off_wstat);         // [warp][8][2]
+  // correction of (head gid & 3, channel group tig): hi row gid + lo row gid ^ 4
+  float cz = st.oz[0] + st.oz[1] + st.oz[2] + st.oz[3];
+  cz += __shfl_xor_sync(0xffffffffu, cz, 16);
+  float corr[2][NCG];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+    for (int g = 0; g < NCG; ++g) corr[hh][g] = __shfl_sync(0xffffffffu, cz, 4 * (h0 + hh) + g);
+  float l[2];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    float x = st.l0[hh] * (1.0f / field_scale<BITS>(0)) + st.l1[hh] * (1.0f / field_scale<BITS>(1));
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    x += __shfl_xor_sync(0xffffffffu, x, 8);
+    x += __shfl_xor_sync(0xffffffffu, x, 16);
+    l[hh] = x;
+  }
+  float v[MT][4];
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[m][e] = st.o[m][e] + __shfl_xor_sync(0xffffffffu, st.o[m][e], 2);
+  if (tig < 2) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      const int c0 = 16 * m + gid, g = m / 2;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        red[(warp * G + h0 + hh) * D + c0] = v[m][hh] + corr[hh][g];
+        red[(warp * G + h0 + hh) * D + c0 + 8] = v[m][2 + hh] + corr[hh][g];
+      }
+    }
+    if (gid == 0) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        wstat[(warp * 8 + h0 + hh) * 2] = st.m[hh];
+        wstat[(warp * 8 + h0 + hh) * 2 + 1] = l[hh];
+      }
+    }
+  }
+  vc_bar_sync(1, kConsumers);
+  merge_partials<D, BITS, G>(a, smem, bh, slot);
 }
 
 // Count this CTA's partial for slice bh; the last of the n_parts arrivals
 // merges all partials of the slice and writes its bf16 output.
+// `nthr` threads take part: the consumer warps of a stream CTA (named barrier
+// 1) or the whole tail CTA.
+__device__ __forceinline__ void sync_part(int nthr) {
+  if (nthr == kConsumers) vc_bar_sync(1, kConsumers); else __syncthreads();
+}
+
 template <int G, int D>
 __device__ void arrive_and_combine(const DraftArgs& a, unsigned int* flag, int bh, int n_parts, int nthr) {
   __threadfence();
@@ -333,452 +755,160 @@ __device__ void arrive_and_combine(const DraftArgs& a, unsigned int* flag, int b
 }
 
 // ------------------------------------------------------------------ stream CTA
-template <int D, int BITS, int G>
-struct Stream {
-  using P = Plan<D, BITS>;
-  using R = Roles<D>;
-  using C = Cols<D>;
-  static constexpr int NL = G <= 8 ? 8 : 16;       // TMEM columns a thread reads per row
-
-  uint8_t* smem;
-  uint64_t* full;
-  uint64_t* empty;
-  uint64_t *ak, *sf, *av, *pr, *of, *ofree, *mr, *done;
-  uint32_t tmem;
-  unsigned int* flag;
-  volatile uint32_t* abort;
-
-  __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity) {
-    return vc_mbar_wait_or_abort(bar, parity, abort, kWaitCycles);
-  }
+// Segments of stream CTA c: consecutive calls walk [range_lo(c), range_lo(c+1)).
+struct Segment {
+  int bh, gs, n_valid, n_st;
 };
-
-// Producer (one thread): the tile stages of every segment, in order.
-template <int D, int BITS, int G>
-__device__ void produce(const DraftArgs& a, Stream<D, BITS, G>& S, int c) {
-  using P = Plan<D, BITS>;
-  const long long hi = range_lo(c + 1, a.total, a.n_stream);
-  long long pos = range_lo(c, a.total, a.n_stream);
-  Segment sg{};
-  bool over, ok = true;
-  long long gt = 0;                           // global tile index (tiles issued so far)
-  while (ok && next_segment(a, pos, hi, sg, over)) {
-    for (int j = 0; j < sg.n_tiles; ++j, ++gt) {
-      const int s = static_cast<int>(gt % P::NS);
-      if (gt >= P::NS && !S.wait(S.empty + s, static_cast<uint32_t>((gt / P::NS - 1) & 1))) {
-        ok = false;
-        break;
-      }
-      const int n = min(kTileGroups, sg.n_valid - j * kTileGroups);
-      const size_t g0 = static_cast<size_t>(sg.bh) * a.NG + sg.gs + j * kTileGroups;
-      uint8_t* st = S.smem + s * P::stage;
-      vc_mbar_arrive_expect_tx(S.full + s, n * (P::kcb + P::kmb + P::vcb + P::vmb));
-      vc_bulk_g2s(st + P::off_kc, a.kc + g0 * (P::kcb / 4), n * P::kcb, S.full + s);
-      vc_bulk_g2s(st + P::off_km, a.ksz + g0 * (P::kmb / 2), n * P::kmb, S.full + s);
-      vc_bulk_g2s(st + P::off_vc, a.vc + g0 * (P::vcb / 4), n * P::vcb, S.full + s);
-      vc_bulk_g2s(st + P::off_vm, a.vsz + g0 * (P::vmb / 2), n * P::vmb, S.full + s);
-    }
-  }
-  // drain: every stage issued has landed before the CTA may exit
-  for (long long x = gt - P::NS < 0 ? 0 : gt - P::NS; x < gt; ++x)
-    vc_mbar_wait_bounded(S.full + x % P::NS, static_cast<uint32_t>((x / P::NS) & 1), kWaitCycles);
+__device__ __forceinline__ bool next_segment(const DraftArgs& a, long long& pos, long long hi, Segment& sg,
+                                             bool& over_capacity) {
+  if (pos >= hi) return false;
+  sg.bh = static_cast<int>(pos / a.NGmax);
+  sg.gs = static_cast<int>(pos % a.NGmax);
+  const int ge = static_cast<int>(min(static_cast<long long>(a.NGmax), sg.gs + (hi - pos)));
+  pos += ge - sg.gs;
+  int ng_req = a.packed_len[sg.bh / a.Hkv] / kGroup;
+  over_capacity = ng_req > a.NGmax;
+  if (over_capacity) ng_req = a.NGmax;
+  sg.n_valid = max(0, min(ge, ng_req) - sg.gs);
+  sg.n_st = (sg.n_valid + kWarps - 1) / kWarps;
+  return true;
 }
 
-// Products (one thread): per tile S = K^ . Q^T, then O^T = V^T . P^T.
+// Producer warp (lane 0): fills the ring stage by stage, across segments,
+// each stage once all consumer warps released its previous use.
 template <int D, int BITS, int G>
-__device__ void issue(const DraftArgs& a, Stream<D, BITS, G>& S, int c) {
-  using P = Plan<D, BITS>;
-  using C = Cols<D>;
-  constexpr uint32_t id_qk = vc_tc_idesc_f16(128, kN, false), id_pv = vc_tc_idesc_f16(128, kN, true);
-  const uint32_t q0 = vc_smem_addr(S.smem + P::off_q), p0 = vc_smem_addr(S.smem + P::off_p);
+__device__ void produce(const DraftArgs& a, uint8_t* smem, int c, uint64_t* full, uint64_t* empty,
+                        volatile uint32_t* abort) {
+  using P = Plan<D, BITS, G>;
+  int buf = 0;                                  // ring position of the next stage use
+  uint32_t phase = 0;                           // completed wraps of the ring, mod 2
+  bool wrapped = false;                         // every buffer used at least once
   const long long hi = range_lo(c + 1, a.total, a.n_stream);
   long long pos = range_lo(c, a.total, a.n_stream);
-  Segment sg{};
-  bool over, ok = true, any = false;
-  long long gt = 0;
-  int seg = 0;
-  auto qk = [&](long long t, int sb) {
-    const int b = static_cast<int>(t & 1);
-    if (!S.wait(S.ak + b, static_cast<uint32_t>((t >> 1) & 1))) return false;
-    vc_tc_fence_after();
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks)
-      vc_tc_mma_ta(S.tmem + C::s + b * kN, S.tmem + C::ak + b * (D / 2) + ks * 8,
-                   vc_tc_desc(q0 + sb * P::q_bytes + ks * 256, 128, 16 * D), id_qk, ks > 0);
-    vc_tc_commit(S.sf + b);
-    return true;
-  };
-  auto pv = [&](long long t) {
-    const int b = static_cast<int>(t & 1);
-    if (!S.wait(S.pr + b, static_cast<uint32_t>((t >> 1) & 1))) return false;
-    if (!S.wait(S.av + b, static_cast<uint32_t>((t >> 1) & 1))) return false;
-    if (t >= 2 && !S.wait(S.ofree + b, static_cast<uint32_t>(((t >> 1) + 1) & 1))) return false;
-    vc_tc_fence_after();
-#pragma unroll
-    for (int ks = 0; ks < kTile / 16; ++ks)
-      vc_tc_mma_ta(S.tmem + C::o + b * kN, S.tmem + C::av + b * (kTile / 2) + ks * 8,
-                   vc_tc_desc(p0 + b * P::p_bytes + ks * 512, 256, 128), id_pv, ks > 0);
-    vc_tc_commit(S.of + b);
-    return true;
-  };
-  while (ok && next_segment(a, pos, hi, sg, over)) {
-    const int sb = seg & 1;
-    if (sg.n_tiles > 0) {
-      any = true;
-      ok = qk(gt, sb);
-      for (int j = 0; ok && j < sg.n_tiles; ++j) {
-        if (j + 1 < sg.n_tiles) ok = qk(gt + j + 1, sb);
-        if (ok) ok = pv(gt + j);
-      }
-      gt += sg.n_tiles;
-    }
-    ++seg;
-  }
-  // every product issued has completed before TMEM is freed
-  if (any) {
-    vc_tc_commit(S.done);
-    vc_mbar_wait_bounded(S.done, 0, kWaitCycles);
-  }
-}
-
-// Q of slice bh (G heads) into the K-major operand buffer sb: fp16 q * scale * log2(e).
-template <int D, int BITS, int G>
-__device__ __forceinline__ void write_q(const DraftArgs& a, Stream<D, BITS, G>& S, int bh, int sb) {
-  using P = Plan<D, BITS>;
-  const int b = bh / a.Hkv, kvh = bh % a.Hkv;
-  uint8_t* qs = S.smem + P::off_q + sb * P::q_bytes;
-  for (int i = threadIdx.x; i < G * D / 8; i += 32 * kTokWarps) {
-    const int h = i / (D / 8), kc = i % (D / 8);
-    const uint4 raw = *reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * a.Hq + kvh * G + h) * D + 8 * kc);
-    const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      o[j] = h2u(__floats2half2_rn(vc_bf16_to_f32(static_cast<uint16_t>(rw[j])) * a.scale_log2,
-                                   vc_bf16_to_f32(static_cast<uint16_t>(rw[j] >> 16)) * a.scale_log2));
-    *reinterpret_cast<uint4*>(qs + (h / 8) * (16 * D) + kc * 128 + (h % 8) * 16) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-  vc_fence_proxy_async_smem();
-}
-
-// Token warp q.
-template <int D, int BITS, int G>
-__device__ void token_warp(const DraftArgs& a, Stream<D, BITS, G>& S, int c) {
-  using P = Plan<D, BITS>;
-  using R = Roles<D>;
-  using C = Cols<D>;
-  constexpr int NL = Stream<D, BITS, G>::NL;
-  const int q = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t t_lane = S.tmem + (static_cast<uint32_t>(q * 32) << 16);
-  float* red = reinterpret_cast<float*>(S.smem + P::off_red);
-  float* mt = reinterpret_cast<float*>(S.smem + P::off_mt);
-  const long long hi = range_lo(c + 1, a.total, a.n_stream);
-  long long pos = range_lo(c, a.total, a.n_stream);
-  Segment sg{};
+  Segment sg;
   bool over;
-  long long gt = 0;
-  int seg = 0;
-  float m[G], l[G];
-
-  // tile t of the CTA (j-th of the segment): K rows of group q into A_K[t & 1]
-  auto extract = [&](long long t, int j, int sb) {
-    const int s = static_cast<int>(t % P::NS);
-    bool ok = S.wait(S.full + s, static_cast<uint32_t>((t / P::NS) & 1));
-    ok = __all_sync(0xffffffffu, ok);
-    if (j == 0) write_q(a, S, sg.bh, sb);        // this segment's queries (first tile)
-    const int n = min(kTileGroups, sg.n_valid - j * kTileGroups);
-    if (ok && q < n) {
-      const uint8_t* st = S.smem + s * P::stage;
-      dequant_k_row<D, BITS>(reinterpret_cast<const uint32_t*>(st + P::off_kc + q * P::kcb),
-                             reinterpret_cast<const uint32_t*>(st + P::off_km + q * P::kmb), lane,
-                             t_lane + C::ak + static_cast<uint32_t>(t & 1) * (D / 2));
-      vc_tc_wait_st();
-    }
-    vc_tc_fence_before();
-    __syncwarp();
-    if (lane == 0) {
-      vc_mbar_arrive(S.ak + (t & 1));
-      vc_mbar_arrive(S.empty + s);
-    }
-  };
-
-  // softmax of tile t: weights of group q's tokens into P[t & 1]
-  auto softmax = [&](long long t, int j) {
-    const int b = static_cast<int>(t & 1);
-    const int n = min(kTileGroups, sg.n_valid - j * kTileGroups);
-    const bool valid = q < n;
-    bool ok = S.wait(S.sf + b, static_cast<uint32_t>((t >> 1) & 1));
-    ok = __all_sync(0xffffffffu, ok);
-    vc_tc_fence_after();
-    float sc[NL];
-    if constexpr (NL == 8) vc_tc_ld8(t_lane + C::s + b * kN, sc);
-    else vc_tc_ld16(t_lane + C::s + b * kN, sc);
-    const bool live = ok && valid;
-    bool need = false;
-#pragma unroll
-    for (int h = 0; h < G; ++h) need |= live && !(sc[h] <= m[h] + kLazy);
-    if (vc_bar_red_or(1, 32 * kTokWarps, need)) {            // raise the running max (same in every token warp)
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float x = live ? sc[h] : -INFINITY;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-        if (lane == 0) red[q * kN + h] = x;
-      }
-      vc_bar_sync(1, 32 * kTokWarps);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float mx = fmaxf(fmaxf(red[h], red[kN + h]), fmaxf(red[2 * kN + h], red[3 * kN + h]));
-        const float mn = fmaxf(m[h], mx);
-        if (mn != -INFINITY) {
-          l[h] *= fast_exp2(m[h] - mn);                       // m = -inf at the start: 0
-          m[h] = mn;
-        }
-      }
-      vc_bar_sync(1, 32 * kTokWarps);
-    }
-    float p[kN];
-#pragma unroll
-    for (int h = 0; h < kN; ++h) {
-      p[h] = 0.0f;
-      if (h < G && live) {
-        p[h] = fast_exp2(sc[h] - m[h]);
-        l[h] += p[h];
-      }
-    }
-    vc_tc_fence_before();                                     // S read out before the buffer is refilled
-    // P[b] and the tile max: their previous readers (tile t - 2) are done
-    if (t >= 2) {
-      ok = S.wait(S.ofree + b, static_cast<uint32_t>(((t >> 1) + 1) & 1));
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    uint8_t* pb = S.smem + P::off_p + b * P::p_bytes;
-    const int pt = q * 32 + lane;                              // the token's position in the tile
-    uint32_t w[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = h2u(__floats2half2_rn(p[2 * i], p[2 * i + 1]));
-    *reinterpret_cast<uint4*>(pb + (pt / 8) * 256 + (pt % 8) * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-    if (G > 8) *reinterpret_cast<uint4*>(pb + (pt / 8) * 256 + 128 + (pt % 8) * 16) = make_uint4(w[4], w[5], w[6], w[7]);
-    vc_fence_proxy_async_smem();
-    if (q == 0 && lane == 0) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) mt[b * kN + h] = m[h];
-    }
-    __syncwarp();
-    if (lane == 0) {
-      vc_mbar_arrive(S.pr + b);
-      if (q == 0) vc_mbar_arrive(S.mr + b);
-    }
-  };
-
   while (next_segment(a, pos, hi, sg, over)) {
-    if (over && threadIdx.x == 0) atomicOr(&g_draft_status, VC_DEV_CAPACITY);
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.0f;
-    }
-    const int sb = seg & 1;
-    if (sg.n_tiles > 0) extract(gt, 0, sb);
-    for (int j = 0; j < sg.n_tiles; ++j) {
-      if (j + 1 < sg.n_tiles) extract(gt + j + 1, j + 1, sb);
-      softmax(gt + j, j);
-    }
-    gt += sg.n_tiles;
-    ++seg;
-    // segment end: the weight sums of the 128 token rows, per head, for the channel warps
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float x = l[h];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-      if (lane == 0) red[q * kN + h] = x;
-    }
-    vc_bar_sync(2, R::compute_threads);                        // sums in red; channel warps write the partial
-    int first, last;
-    ctas_of(sg.bh, a, first, last);
-    arrive_and_combine<G, D>(a, S.flag, sg.bh, last - first + 2, R::compute_threads);
-    vc_bar_sync(2, R::compute_threads);                        // red / flag reused by the next segment
-  }
-}
-
-// Channel warp cw (warp kTokWarps + cw): channels 32 cw .. 32 cw + 31.
-template <int D, int BITS, int G>
-__device__ void channel_warp(const DraftArgs& a, Stream<D, BITS, G>& S, int c) {
-  using P = Plan<D, BITS>;
-  using R = Roles<D>;
-  using C = Cols<D>;
-  constexpr int NL = Stream<D, BITS, G>::NL;
-  const int cw = (threadIdx.x >> 5) - kTokWarps, lane = threadIdx.x & 31;
-  const int ch = 32 * cw + lane;
-  const uint32_t t_lane = S.tmem + (static_cast<uint32_t>(cw * 32) << 16);   // warp % 4 == cw
-  const float* red = reinterpret_cast<const float*>(S.smem + P::off_red);
-  const float* mt = reinterpret_cast<const float*>(S.smem + P::off_mt);
-  const long long hi = range_lo(c + 1, a.total, a.n_stream);
-  long long pos = range_lo(c, a.total, a.n_stream);
-  Segment sg{};
-  bool over;
-  long long gt = 0;
-  float o[G], mc[G];
-
-  // tile t: V rows of this warp's channels into A_V[t & 1] (zeros past the valid groups)
-  auto extract = [&](long long t, int j) {
-    const int s = static_cast<int>(t % P::NS);
-    bool ok = S.wait(S.full + s, static_cast<uint32_t>((t / P::NS) & 1));
-    ok = __all_sync(0xffffffffu, ok);
-    const int n = min(kTileGroups, sg.n_valid - j * kTileGroups);
-    const uint8_t* st = S.smem + s * P::stage;
-    const uint32_t ta = t_lane + C::av + static_cast<uint32_t>(t & 1) * (kTile / 2);
-#pragma unroll
-    for (int g = 0; g < kTileGroups; ++g) {
-      if (ok && g < n) {
-        dequant_v_row<D, BITS>(reinterpret_cast<const uint32_t*>(st + P::off_vc + g * P::vcb),
-                               reinterpret_cast<const uint32_t*>(st + P::off_vm + g * P::vmb) + cw * 32, ch,
-                               ta + g * 16);
-      } else {
-        const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-        vc_tc_st16(ta + g * 16, z);
+    for (int s = 0; s < sg.n_st; ++s) {
+      // the previous use of `buf` (one wrap earlier) must have been released
+      if (wrapped && !vc_mbar_wait_or_abort(empty + buf, phase ^ 1u, abort, kWaitCycles)) return;
+      issue_stage<D, BITS, G>(a, smem + buf * P::stage, full + buf, sg.bh, sg.gs + s * kWarps,
+                              min(kWarps, sg.n_valid - s * kWarps));
+      if (++buf == P::NS) {
+        buf = 0;
+        phase ^= 1u;
+        wrapped = true;
       }
     }
-    vc_tc_wait_st();
-    vc_tc_fence_before();
-    __syncwarp();
-    if (lane == 0) {
-      vc_mbar_arrive(S.av + (t & 1));
-      vc_mbar_arrive(S.empty + s);
-    }
-  };
-
-  // tile t's O^T rows of this warp's channels into the running outputs
-  auto merge = [&](long long t) {
-    const int b = static_cast<int>(t & 1);
-    bool ok = S.wait(S.of + b, static_cast<uint32_t>((t >> 1) & 1));
-    ok = ok && S.wait(S.mr + b, static_cast<uint32_t>((t >> 1) & 1));
-    ok = __all_sync(0xffffffffu, ok);
-    vc_tc_fence_after();
-    float ot[NL];
-    if constexpr (NL == 8) vc_tc_ld8(t_lane + C::o + b * kN, ot);
-    else vc_tc_ld16(t_lane + C::o + b * kN, ot);
-    if (ok) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float mtile = mt[b * kN + h];
-        if (mtile > mc[h]) {
-          o[h] *= fast_exp2(mc[h] - mtile);                   // mc = -inf at the start: 0
-          mc[h] = mtile;
-        }
-        o[h] += ot[h];
-      }
-    }
-    vc_tc_fence_before();
-    __syncwarp();
-    if (lane == 0) vc_mbar_arrive(S.ofree + b);
-  };
-
-  while (next_segment(a, pos, hi, sg, over)) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      o[h] = 0.0f;
-      mc[h] = -INFINITY;
-    }
-    if (sg.n_tiles > 0) extract(gt, 0);
-    for (int j = 0; j < sg.n_tiles; ++j) {
-      if (j + 1 < sg.n_tiles) extract(gt + j + 1, j + 1);
-      merge(gt + j);
-    }
-    gt += sg.n_tiles;
-    vc_bar_sync(2, R::compute_threads);                        // the token warps' sums are in red
-    int first, last;
-    ctas_of(sg.bh, a, first, last);
-    const int b = sg.bh / a.Hkv, kvh = sg.bh % a.Hkv;
-    const int slot = c - first;
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float lh = red[h] + red[kN + h] + red[2 * kN + h] + red[3 * kN + h];
-      const size_t row = static_cast<size_t>(b * a.Hq + kvh * G + h) * a.max_parts + slot;
-      a.part_o[row * D + ch] = lh > 0.0f ? o[h] / lh : 0.0f;
-      if (ch == 0) a.part_lse[row] = lh > 0.0f ? mc[h] + log2f(lh) : -INFINITY;
-    }
-    arrive_and_combine<G, D>(a, S.flag, sg.bh, last - first + 2, R::compute_threads);
-    vc_bar_sync(2, R::compute_threads);
   }
 }
 
 template <int D, int BITS, int G>
 __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
-  using P = Plan<D, BITS>;
-  using R = Roles<D>;
-  using C = Cols<D>;
+  using P = Plan<D, BITS, G>;
+  constexpr int NS = P::NS, KS = D / 16, NCG = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  Stream<D, BITS, G> S;
-  S.smem = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P::off_bar);
-  S.full = bars;
-  S.empty = bars + P::NS;
-  S.ak = bars + 2 * P::NS;
-  S.sf = S.ak + 2;
-  S.av = S.sf + 2;
-  S.pr = S.av + 2;
-  S.of = S.pr + 2;
-  S.ofree = S.of + 2;
-  S.mr = S.ofree + 2;
-  S.done = S.mr + 2;
-  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + P::off_misc);
-  S.flag = misc + 1;
-  S.abort = misc + 2;
-  if (warp == 0) vc_tc_alloc(misc, C::alloc);
-  if (threadIdx.x == 32) {
-    for (int i = 0; i < P::NS; ++i) {
-      vc_mbar_init(S.full + i, 1);
-      vc_mbar_init(S.empty + i, R::compute_warps);
+  const int gid = lane >> 2, tig = lane & 3;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + P::off_bar);
+  uint64_t* empty = full + NS;
+  unsigned int* flag = reinterpret_cast<unsigned int*>(smem + P::off_flag);
+  volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(flag + 1);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      vc_mbar_init(full + i, 1);
+      vc_mbar_init(empty + i, kWarps);
     }
-    for (int b = 0; b < 2; ++b) {
-      vc_mbar_init(S.ak + b, kTokWarps);
-      vc_mbar_init(S.sf + b, 1);
-      vc_mbar_init(S.av + b, R::chan_warps);
-      vc_mbar_init(S.pr + b, kTokWarps);
-      vc_mbar_init(S.of + b, 1);
-      vc_mbar_init(S.ofree + b, R::chan_warps);
-      vc_mbar_init(S.mr + b, 1);
-    }
-    vc_mbar_init(S.done, 1);
-    *S.abort = 0u;
+    *abort = 0u;
     vc_fence_mbar_init();
   }
-  // zero the operand buffers once: the padded heads of Q and P stay zero
-  for (int i = threadIdx.x; i < static_cast<int>(2 * (P::q_bytes + P::p_bytes) / 16); i += blockDim.x)
-    reinterpret_cast<uint4*>(smem + P::off_q)[i] = make_uint4(0u, 0u, 0u, 0u);
-  vc_fence_proxy_async_smem();
-  vc_tc_fence_before();
   __syncthreads();
-  vc_tc_fence_after();
-  S.tmem = misc[0];
-
-  if (warp < kTokWarps) {
-    token_warp<D, BITS, G>(a, S, c);
-  } else if (warp < R::compute_warps) {
-    channel_warp<D, BITS, G>(a, S, c);
-  } else if (warp == R::producer_warp) {
-    if (lane == 0) produce<D, BITS, G>(a, S, c);
-  } else if (lane == 0) {
-    issue<D, BITS, G>(a, S, c);
+  if (warp == kWarps) {                         // producer warp
+    if (lane == 0) produce<D, BITS, G>(a, smem, c, full, empty, abort);
+    return;
   }
-  vc_tc_fence_before();
-  __syncthreads();
-  vc_tc_fence_after();
-  if (threadIdx.x == 0 && *S.abort != 0u) atomicOr(&g_draft_status, VC_DEV_BARRIER_TIMEOUT);
-  if (warp == 0) vc_tc_dealloc(S.tmem, C::alloc);
+  // lane constants: bias columns (gid 0: zeros / f, gid 1: -scales) and
+  // correction columns (gid = 2g: zeros / f, gid = 2g + 1: -scales of channel
+  // group g; a V meta row pair holds the scales first, then the zeros)
+  const float f0 = field_scale<BITS>(0), f1 = field_scale<BITS>(1);
+  const uint32_t bias_mul0 = h2u(__float2half2_rn(gid == 0 ? 1.0f / f0 : (gid == 1 ? -1.0f : 0.0f)));
+  const uint32_t bias_mul1 = h2u(__float2half2_rn(gid == 0 ? 1.0f / f1 : (gid == 1 ? -1.0f : 0.0f)));
+  const bool zc = gid < 2 * NCG;
+  const uint32_t zcol_mul0 = h2u(__float2half2_rn(!zc ? 0.0f : ((gid & 1) ? -1.0f : 1.0f / f0)));
+  const uint32_t zcol_mul1 = h2u(__float2half2_rn(!zc ? 0.0f : ((gid & 1) ? -1.0f : 1.0f / f1)));
+  const int zcol_off = zc ? 32 * (gid ^ 1) : 0;
+  int buf = 0;                                  // ring position and phase of the next stage use
+  uint32_t phase = 0;
+  const long long hi = range_lo(c + 1, a.total, a.n_stream);
+  long long pos = range_lo(c, a.total, a.n_stream);
+  Segment sg;
+  bool over;
+  while (next_segment(a, pos, hi, sg, over)) {
+    if (over && threadIdx.x == 0) atomicOr(&g_draft_status, VC_DEV_CAPACITY);
+    const int b = sg.bh / a.Hkv, kvh = sg.bh % a.Hkv;
+    int first, last;
+    ctas_of(sg.bh, a, first, last);
+    // query fragments of head gid, times f_r: channels (D/4) tig + 4ks + 2r + {0, 1}
+    // (the transposed product, G = 4: lanes gid and gid + 4 both hold head gid & 3)
+    uint32_t qf[KS][2];
+    {
+      constexpr bool kT = G == 4;
+      const int head = kT ? (gid & 3) : (gid < G ? gid : 0);
+      const uint16_t* qrow = a.q + (static_cast<size_t>(b) * a.Hq + kvh * G + head) * D + (D / 4) * tig;
+      const float on = (kT || gid < G) ? 1.0f : 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(qrow + 4 * ks);
+        const float q0 = vc_bf16_to_f32(static_cast<uint16_t>(raw.x)), q1 = vc_bf16_to_f32(static_cast<uint16_t>(raw.x >> 16));
+        const float q2 = vc_bf16_to_f32(static_cast<uint16_t>(raw.y)), q3 = vc_bf16_to_f32(static_cast<uint16_t>(raw.y >> 16));
+        qf[ks][0] = h2u(__floats2half2_rn(q0 * on * f0, q1 * on * f0));
+        qf[ks][1] = h2u(__floats2half2_rn(q2 * on * f1, q3 * on * f1));
+      }
+    }
+    typename StateOf<D, G>::type st;
+    init_state(st);
+    for (int s = 0; s < sg.n_st; ++s) {
+      const bool ok = __all_sync(0xffffffffu, vc_mbar_wait_or_abort(full + buf, phase, abort, kWaitCycles));
+      if (ok && s * kWarps + warp < sg.n_valid) {
+        const uint8_t* base = smem + buf * P::stage;
+        const uint32_t* kc_g = reinterpret_cast<const uint32_t*>(base + warp * P::codes);
+        const uint16_t* ksz_g = reinterpret_cast<const uint16_t*>(base + P::kc + warp * P::meta);
+        const uint32_t* vc_g = reinterpret_cast<const uint32_t*>(base + P::kc + P::mt + warp * P::codes);
+        const uint16_t* vsz_g = reinterpret_cast<const uint16_t*>(base + 2 * P::kc + P::mt + warp * P::meta);
+        if constexpr (G == 4)
+          group_mma_t<D, BITS>(kc_g, ksz_g, vc_g, vsz_g, qf, bias_mul0, bias_mul1, zcol_mul0, zcol_mul1, zcol_off,
+                               a.scale_log2, st, lane);
+        else
+          group_mma<D, BITS>(kc_g, ksz_g, vc_g, vsz_g, qf, bias_mul0, bias_mul1, zcol_mul0, zcol_mul1, zcol_off,
+                             a.scale_log2, st, lane);
+      }
+      __syncwarp();
+      if (lane == 0) vc_mbar_arrive(empty + buf);          // this warp is done with the stage
+      if (++buf == NS) {
+        buf = 0;
+        phase ^= 1u;
+      }
+    }
+    // every consumer thread takes the same branch: the OR of the abort flag
+    if (vc_bar_red_or(1, kConsumers, *abort != 0u)) {
+      if (threadIdx.x == 0) atomicOr(&g_draft_status, VC_DEV_BARRIER_TIMEOUT);
+      return;                                               // outputs of this call are invalid
+    }
+    if constexpr (G == 4)
+      write_partial_t<D, BITS, G>(a, smem, sg.bh, c - first, st);
+    else
+      write_partial<D, BITS, G>(a, smem, sg.bh, c - first, st);
+    arrive_and_combine<G, D>(a, flag, sg.bh, last - first + 2, kConsumers);
+    vc_bar_sync(1, kConsumers);                             // red / flag reused by the next segment
+  }
 }
 
 // ------------------------------------------------------------------ tail CTA
 // bf16 tail tokens 0 .. tail_len + step - 1 and the current token of slice bh.
 template <int D, int BITS, int G>
 __device__ void tail_cta(const DraftArgs& a, uint8_t* smem, int bh) {
-  using T = TailPlan<D, G>;
+  using P = Plan<D, BITS, G>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cap = a.tail_cap;
-  float* q_s = reinterpret_cast<float*>(smem + T::off_q(cap));
-  unsigned int* flag = reinterpret_cast<unsigned int*>(smem + T::off_flag(cap));
+  float* q_s = reinterpret_cast<float*>(smem + P::off_q);
+  unsigned int* flag = reinterpret_cast<unsigned int*>(smem + P::off_flag);
   const int b = bh / a.Hkv, kvh = bh % a.Hkv;
   int first, last;
   ctas_of(bh, a, first, last);
@@ -797,9 +927,9 @@ __device__ void tail_cta(const DraftArgs& a, uint8_t* smem, int bh) {
     return;
   }
   uint16_t* krow = reinterpret_cast<uint16_t*>(smem);                      // [n_tok][D]
-  uint16_t* vrow = krow + static_cast<size_t>(cap + 1) * D;
-  float* sc = reinterpret_cast<float*>(smem + T::off_sc(cap));             // [G][n_tok]
-  float* ml = reinterpret_cast<float*>(smem + T::off_ml(cap));             // [G][2]
+  uint16_t* vrow = krow + static_cast<size_t>(a.tail_cap + 1) * D;
+  float* sc = reinterpret_cast<float*>(vrow + static_cast<size_t>(a.tail_cap + 1) * D);   // [G][n_tok]
+  float* ml = reinterpret_cast<float*>(smem + P::off_wstat);               // [G][2]
   constexpr int VEC = D / 8;
   for (int i = threadIdx.x; i < n_tok * VEC; i += blockDim.x) {
     const int t = i / VEC, v = i % VEC;
@@ -808,10 +938,7 @@ __device__ void tail_cta(const DraftArgs& a, uint8_t* smem, int bh) {
     *reinterpret_cast<uint4*>(krow + t * D + v * 8) = *reinterpret_cast<const uint4*>(ks + v * 8);
     *reinterpret_cast<uint4*>(vrow + t * D + v * 8) = *reinterpret_cast<const uint4*>(vs + v * 8);
   }
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const int h = i / D, c = i % D;
-    q_s[i] = vc_bf16_to_f32(a.q[(static_cast<size_t>(b) * a.Hq + kvh * G + h) * D + c]) * a.scale_log2;
-  }
+  load_q<D, G>(a, b, kvh, q_s);
   __syncthreads();
   // scores: warp per token, lanes over channel pairs
   const int nw = blockDim.x / 32;
@@ -874,9 +1001,9 @@ __device__ void tail_cta(const DraftArgs& a, uint8_t* smem, int bh) {
   arrive_and_combine<G, D>(a, flag, bh, n_c + 1, blockDim.x);
 }
 
-template <int D, int BITS, int G>
-__global__ void __launch_bounds__(Roles<D>::threads, 1) draft_kernel(DraftArgs a) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+template <int D, int BITS, int G, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) draft_kernel(DraftArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
   const int nbh = a.B * a.Hkv;
   if (static_cast<int>(blockIdx.x) < nbh)
     tail_cta<D, BITS, G>(a, smem, blockIdx.x);
@@ -896,26 +1023,33 @@ vc_status_t check(const vc_shape_t* s) {
   return VC_OK;
 }
 
+// One CTA of kThreads (11 consumer warps + the producer) per SM: the warps keep
+// the output accumulators and the query fragments in registers.
+template <int G>
+struct MinBlocks {
+  static constexpr int value = 1;
+};
+
 struct LaunchPlan {
-  int n_stream = 0, max_parts = 1, threads = 0;
+  int n_stream = 0, max_parts = 1;
   long long total = 0;
   size_t smem = 0;
 };
 
 template <int D, int BITS, int G>
 vc_status_t plan_t(const vc_shape_t* s, int max_packed, LaunchPlan* lp) {
-  using P = Plan<D, BITS>;
-  auto fn = draft_kernel<D, BITS, G>;
+  using P = Plan<D, BITS, G>;
+  auto fn = draft_kernel<D, BITS, G, MinBlocks<G>::value>;
   VC_CUDA_CHECK(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P::total)));
   int dev = 0, sms = 0, occ = 0;
   VC_CUDA_CHECK(cudaGetDevice(&dev));
   VC_CUDA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  VC_CUDA_CHECK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, Roles<D>::threads, P::total));
+  VC_CUDA_CHECK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kThreads, P::total));
   if (occ < 1) VC_FAIL(VC_ERR_UNSUPPORTED, "draft kernel does not fit on an SM");
   const long long NGmax = max_packed / kGroup;
   lp->total = static_cast<long long>(s->B) * s->Hkv * NGmax;
-  long long n = sms;                                            // one CTA per SM (TMEM and shared memory)
-  const long long by_work = lp->total / kTileGroups;            // at least one tile per CTA
+  long long n = static_cast<long long>(occ) * sms;
+  const long long by_work = lp->total / kWarps;                 // at least one stage per CTA
   if (n > by_work) n = by_work;
   if (n < 1 && lp->total > 0) n = 1;
   lp->n_stream = static_cast<int>(lp->total > 0 ? n : 0);
@@ -926,7 +1060,6 @@ vc_status_t plan_t(const vc_shape_t* s, int max_packed, LaunchPlan* lp) {
     lp->max_parts = 1;
   }
   lp->smem = P::total;
-  lp->threads = Roles<D>::threads;
   return VC_OK;
 }
 
@@ -950,10 +1083,10 @@ size_t ws_bytes(const vc_shape_t* s, const LaunchPlan& lp) {
 
 template <int D, int BITS, int G>
 vc_status_t launch_t(const DraftArgs& a, const LaunchPlan& lp, cudaStream_t cs) {
-  if (TailPlan<D, G>::total(a.tail_cap) > Plan<D, BITS>::total)
+  if (tail_smem<D, G>(a.tail_cap) > Plan<D, BITS, G>::off_q)
     VC_FAIL(VC_ERR_UNSUPPORTED, "tail_cap %d too large for the shared-memory plan", a.tail_cap);
   const int grid = a.B * a.Hkv + lp.n_stream;
-  draft_kernel<D, BITS, G><<<grid, lp.threads, lp.smem, cs>>>(a);
+  draft_kernel<D, BITS, G, MinBlocks<G>::value><<<grid, kThreads, lp.smem, cs>>>(a);
   VC_LAUNCH_CHECK("draft_kernel");
   return VC_OK;
 }

@@ -117,6 +117,33 @@ __device__ __forceinline__ bool vc_mbar_wait_or_abort(uint64_t* bar, uint32_t pa
   }
   return true;
 }
+// As vc_mbar_wait_or_abort, but each probe lets the thread sleep up to
+// `sleep_ns` nanoseconds for the phase (mbarrier.try_wait with a suspend-time
+// hint) instead of spinning: a waiting warp takes no issue slots.
+__device__ __forceinline__ bool vc_mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t sleep_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(vc_smem_addr(bar)), "r"(parity), "r"(sleep_ns)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool vc_mbar_wait_sleep_or_abort(uint64_t* bar, uint32_t parity, volatile uint32_t* abort,
+                                                            long long limit_cycles, uint32_t sleep_ns = 20000u) {
+  if (vc_mbar_try_wait_sleep(bar, parity, sleep_ns)) return true;
+  const long long t0 = clock64();
+  while (!vc_mbar_try_wait_sleep(bar, parity, sleep_ns)) {
+    if (*abort != 0u) return false;
+    if (clock64() - t0 > limit_cycles) {
+      *abort = 1u;
+      return false;
+    }
+  }
+  return true;
+}
 // Barrier over the first `count` threads of the CTA (named barrier `id`, 1..15).
 __device__ __forceinline__ void vc_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -30,38 +30,60 @@ constexpr int kGroup = 32;
 // ------------------------------------------------------------------ quantiser
 
 // ------------------------------------------------------------------ packed layout
-// Field rules of the packed words (the library's format; include/vc.h).  Per
-// group, K codes are 32 token rows of d*b/32 words and V codes d channel rows
-// of b words, stored in chunks of CW = min(words per row, 4): word w of row r
-// at ((w / CW) * rows + r) * CW + w % CW.  Word w of a row holds row elements
-// 2((16/b)w + k) + e (channels of a K row, tokens of a V row) in the b-bit
-// field at bit 16e + b*k (k < 16/b).  Elements 2m and 2m + 1 thus share a
-// field position in the two half-words of one word.  No field crosses bit 31.
+// Field rules of the packed words (the library's format; include/vc.h): per
+// group, 32 lanes x d*b/32 words; word w of lane L at (w/4)*128 + 4L + w%4.
+// b = 2: slot (u, r, e) starts at bit 16e + 4u + 2(1 - r);
+// b = 4: slot (u, e) starts at 16e + 4u; b = 8: at 16e + 8u.  No field crosses bit 31.
+__device__ __forceinline__ int field_pos(int bits, int u, int r, int e) {
+  return bits == 2 ? (16 * e + 4 * u + 2 * (1 - r)) : (16 * e + bits * u);
+}
 
 // Word `idx` of a group's K codes (V codes when IS_V) from a code tile
-// codes[t * ld + c].
+// codes[t * ld + c].  K: lane L = 4a + c holds tokens 4a + j, channels
+// (d/4) c + 4k + 2r + e, fragment i = j*(d/16) + k.  V: tokens 8c + 4e + 2s + r,
+// channels 8n + a, fragment i = s*(d/8) + n.  b = 2: word i/4, u = i%4;
+// b = 4, 8: i2 = 2i + r, SPW = 16/b slots per word, word i2/SPW, u = i2%SPW.
 template <int BITS, bool IS_V, int D>
 __device__ __forceinline__ uint32_t build_word(const uint8_t* codes, int ld, int idx) {
-  constexpr int PH = 16 / BITS;                      // fields per half-word
-  constexpr int W = (IS_V ? kGroup : D) * BITS / 32; // words per row
-  constexpr int CW = W < 4 ? W : 4;                  // words per chunk
-  constexpr int NR = IS_V ? D : kGroup;              // rows
-  const int chunk = idx / (NR * CW), rem = idx % (NR * CW);
-  const int row = rem / CW, w = chunk * CW + rem % CW;
+  const int L = (idx % 128) / 4, w = (idx / 128) * 4 + idx % 4;
+  const int a = L / 4, c = L % 4;
+  constexpr int per = IS_V ? D / 8 : D / 16;      // fragments per j (K) or per s (V)
+  constexpr int SPW = BITS == 2 ? 4 : 16 / BITS;   // slots per word
   uint32_t word = 0;
 #pragma unroll
-  for (int k = 0; k < PH; ++k)
+  for (int u = 0; u < SPW; ++u)
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int x = 2 * (PH * w + k) + e;
-      const uint32_t code = IS_V ? codes[x * ld + row] : codes[row * ld + x];
-      word += code << (16 * e + BITS * k);           // disjoint fields: + == |
+    for (int r = 0; r < 2; ++r) {
+      int i;
+      if (BITS == 2) {
+        i = 4 * w + u;
+      } else {
+        if ((u & 1) != r) continue;               // b = 4, 8: slot u carries r = u % 2 (SPW even)
+        i = (SPW * w + u) >> 1;
+      }
+      const int hi = i / per, lo = i % per;         // (j, k) for K, (s, n) for V
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        int t, ch;
+        if (IS_V) {
+          t = 8 * c + 4 * e + 2 * hi + r;
+          ch = 8 * lo + a;
+        } else {
+          t = 4 * a + hi;
+          ch = (D / 4) * c + 4 * lo + 2 * r + e;
+        }
+        const uint32_t code = codes[t * ld + ch];
+        word += code << field_pos(BITS, u, r, e);      // disjoint fields: + == |
+      }
     }
   return word;
 }
 
-// Entry of a V meta row (32 entries, one per token) that holds token t: token order.
-__device__ __forceinline__ int vmeta_entry(int t) { return t; }
+// Entry of a V meta row (32 entries, one per token) that holds token t:
+// entry 8c + 4s + 2r + e holds token 8c + 4e + 2s + r.
+__device__ __forceinline__ int vmeta_entry(int t) {
+  return (t & ~7) | (((t >> 1) & 1) << 2) | ((t & 1) << 1) | ((t >> 2) & 1);
+}
 
 // Quantisation parameters of one group (KIVI recipe): scale s = fp16((max - min) / qmax),
 // zero z = fp16(min), both applied in fp32.
@@ -478,12 +500,35 @@ __global__ void append_lengths_kernel(const int32_t* __restrict__ n_acc, int B, 
 // Position of code (t, ch) of a group: word index and field start.
 template <int BITS, bool IS_V>
 __device__ __forceinline__ void locate(int t, int ch, int d, int& idx, int& pos) {
-  constexpr int PH = 16 / BITS;
-  const int row = IS_V ? ch : t, x = IS_V ? t : ch;
-  const int W = (IS_V ? kGroup : d) * BITS / 32, CW = W < 4 ? W : 4, NR = IS_V ? d : kGroup;
-  const int m = x >> 1, e = x & 1, w = m / PH;
-  idx = ((w / CW) * NR + row) * CW + w % CW;
-  pos = 16 * e + BITS * (m % PH);
+  int L, i, r, e;
+  if (IS_V) {
+    const int c = t / 8, s = (t >> 1) & 1;
+    e = (t >> 2) & 1;
+    r = t & 1;
+    const int a = ch % 8, n = ch / 8;
+    L = 4 * a + c;
+    i = s * (d / 8) + n;
+  } else {
+    const int a = t / 4, j = t % 4;
+    const int c = ch / (d / 4), rem = ch % (d / 4);
+    const int k = rem / 4;
+    r = (rem >> 1) & 1;
+    e = rem & 1;
+    L = 4 * a + c;
+    i = j * (d / 16) + k;
+  }
+  int w, u;
+  if (BITS == 2) {
+    w = i / 4;
+    u = i % 4;
+  } else {
+    constexpr int SPW = 16 / BITS;
+    const int i2 = 2 * i + r;
+    w = i2 / SPW;
+    u = i2 % SPW;
+  }
+  idx = (w / 4) * 128 + 4 * L + w % 4;
+  pos = field_pos(BITS, u, r, e);
 }
 
 // grid (T/32, B*Hkv), thread per (token, channel) pairs.
