@@ -416,12 +416,17 @@ struct WarpStateT {
   float m[2];           // per head: running max (log2 units)
 };
 
-template <int D, int G>
+// Every head count up to 8 takes the transposed product (heads as the 8 columns).
+template <int G>
+struct Transposed {
+  static constexpr bool value = G <= 8;
+};
+template <int D, int G, bool T = Transposed<G>::value>
 struct StateOf {
   using type = WarpState<D>;
 };
-template <int D>
-struct StateOf<D, 4> {
+template <int D, int G>
+struct StateOf<D, G, true> {
   using type = WarpStateT<D>;
 };
 
@@ -442,7 +447,7 @@ __device__ __forceinline__ void init_state(WarpStateT<D>& st) {
   st.m[0] = st.m[1] = -INFINITY;
 }
 
-template <int D, int BITS>
+template <int D, int BITS, int G>
 __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t* ksz_g, const uint32_t* vc_g,
                                             const uint16_t* vsz_g, const uint32_t (&qf)[D / 16][2],
                                             uint32_t bias_mul0, uint32_t bias_mul1,
@@ -450,8 +455,11 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
                                             WarpStateT<D>& st, int lane) {
   constexpr int KS = D / 16, NT = D / 8, NCG = D / 32, WPL = D * BITS / 32;
   const int gid = lane >> 2, tig = lane & 3;
-  const bool lo_p = tig >= 2;                   // P block columns 2 tig (+1): remainder parts
-  const int h0 = 2 * (tig & 1);
+  // G = 4: columns 4-7 repeat heads 0-3 (each lane then holds its heads' whole
+  // scores) and their weights are zero; otherwise column n is head n (zero
+  // query past G).  The lane's heads are columns 2 tig, 2 tig + 1.
+  const bool lo_p = G == 4 && tig >= 2;
+  const int h0 = G == 4 ? 2 * (tig & 1) : 2 * tig;
   // ---------------- S^T = codes . Q'^T
   uint32_t kw[WPL];
   load_lane_words<WPL>(kc_g, lane, kw);
@@ -461,6 +469,10 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) c[mt][0] = c[mt][1] = c[mt][2] = c[mt][3] = 0.0f;
   float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  // cone: the sum over channels of the fp16 Q' values themselves (an all-ones A),
+  // so the "1 +" part of the code operands cancels exactly whatever Q' rounded to
+  float cone[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  constexpr uint32_t kOnes = 0x3C003C00u;
 #pragma unroll
   for (int kq = 0; kq < KS / 2; ++kq) {
     const uint4 s4 = *reinterpret_cast<const uint4*>(srow + 4 * kq);
@@ -470,11 +482,12 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int ks = 2 * kq + h;
-      // Q'^T columns gid and gid + 4 both carry head gid & 3 (fp16 f q s)
+      // Q'^T column n carries head n (G = 4: head n & 3), fp16 f q s
       const uint32_t qb0 = h2u(__hmul2(u2h(qf[ks][0]), u2h(sv[2 * h])));
       const uint32_t qb1 = h2u(__hmul2(u2h(qf[ks][1]), u2h(sv[2 * h + 1])));
       mma16816(cb, qf[ks][0], 0u, qf[ks][1], 0u, h2u(__hmul2(u2h(zv[2 * h]), u2h(bias_mul0))),
                h2u(__hmul2(u2h(zv[2 * h + 1]), u2h(bias_mul1))));
+      mma16816(cone, kOnes, kOnes, kOnes, kOnes, qb0, qb1);
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         uint32_t a0, a1, a2, a3;
@@ -484,9 +497,10 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
       }
     }
   }
-  // bias of head h: row h of the bias product, columns 0 (q.z) and 1 (-q.f s) in lane 4 h
-  const float cbs = cb[0] + cb[1];
-  const float bias[2] = {__shfl_sync(0xffffffffu, cbs, 4 * h0), __shfl_sync(0xffffffffu, cbs, 4 * h0 + 4)};
+  // bias of head h: q.z (row h, column 0 of the bias product, in lane 4 h) minus
+  // the sum of its Q' column (every row of cone: this lane's own columns)
+  const float bias[2] = {__shfl_sync(0xffffffffu, cb[0], 4 * h0) - cone[0],
+                         __shfl_sync(0xffffffffu, cb[0], 4 * h0 + 4) - cone[1]};
   // y[mt][2 half + hh] = score of token 4 gid + 2 mt + half, head h0 + hh (columns
   // 2 tig, 2 tig + 1 hold heads h0, h0 + 1 in both column halves)
   float (&y)[2][4] = c;
@@ -519,9 +533,10 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
       st.o[mt][2] *= alpha[0];
       st.o[mt][3] *= alpha[1];
     }
-    // correction rows belong to head gid & 3: its factor sits in lane (gid, (gid & 3) >> 1)
+    // correction row gid belongs to head gid (gid & 3 for G = 4): its factor sits in
+    // the lane of that row whose columns hold the head
     const float a_g = (gid & 1) ? alpha[1] : alpha[0];
-    const float a_oz = __shfl_sync(0xffffffffu, a_g, 4 * gid + ((gid & 3) >> 1));
+    const float a_oz = __shfl_sync(0xffffffffu, a_g, 4 * gid + (G == 4 ? ((gid & 3) >> 1) : (gid >> 1)));
 #pragma unroll
     for (int k = 0; k < 4; ++k) st.oz[k] *= a_oz;
   }
@@ -658,21 +673,22 @@ __device__ void merge_partials(const DraftArgs& a, uint8_t* smem, int bh, int sl
   }
 }
 
-// write_partial for the transposed state: per head the hi + lo columns, the
-// correction of each channel group, the softmax sum over the warp's tokens.
+// write_partial for the transposed state: per head its columns (G = 4: the
+// column and its zero-weight repeat), the correction of each channel group,
+// the softmax sum over the warp's tokens.
 template <int D, int BITS, int G>
 __device__ void write_partial_t(const DraftArgs& a, uint8_t* smem, int bh, int slot, WarpStateT<D>& st) {
   using P = Plan<D, BITS, G>;
-  static_assert(G == 4, "the transposed product carries 4 heads");
+  static_assert(G <= 8, "the transposed product carries at most 8 heads");
   constexpr int MT = D / 16, NCG = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const int h0 = 2 * (tig & 1);
+  const int h0 = G == 4 ? 2 * (tig & 1) : 2 * tig;
   float* red = reinterpret_cast<float*>(smem + P::off_red);             // [warp][G][D]
   float* wstat = reinterpret_cast<float*>(smem + P::off_wstat);         // [warp][8][2]
-  // correction of (head gid & 3, channel group tig): hi row gid + lo row gid ^ 4
+  // correction of (head of row gid, channel group tig); G = 4: rows gid and gid ^ 4 hold the same head
   float cz = st.oz[0] + st.oz[1] + st.oz[2] + st.oz[3];
-  cz += __shfl_xor_sync(0xffffffffu, cz, 16);
+  if (G == 4) cz += __shfl_xor_sync(0xffffffffu, cz, 16);
   float corr[2][NCG];
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh)
@@ -691,13 +707,15 @@ __device__ void write_partial_t(const DraftArgs& a, uint8_t* smem, int bh, int s
 #pragma unroll
   for (int m = 0; m < MT; ++m)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) v[m][e] = st.o[m][e] + __shfl_xor_sync(0xffffffffu, st.o[m][e], 2);
-  if (tig < 2) {
+    for (int e = 0; e < 4; ++e)
+      v[m][e] = G == 4 ? st.o[m][e] + __shfl_xor_sync(0xffffffffu, st.o[m][e], 2) : st.o[m][e];
+  if (G != 4 || tig < 2) {
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       const int c0 = 16 * m + gid, g = m / 2;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
+        if (h0 + hh >= G) continue;
         red[(warp * G + h0 + hh) * D + c0] = v[m][hh] + corr[hh][g];
         red[(warp * G + h0 + hh) * D + c0 + 8] = v[m][2 + hh] + corr[hh][g];
       }
@@ -705,6 +723,7 @@ __device__ void write_partial_t(const DraftArgs& a, uint8_t* smem, int bh, int s
     if (gid == 0) {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
+        if (h0 + hh >= G) continue;
         wstat[(warp * 8 + h0 + hh) * 2] = st.m[hh];
         wstat[(warp * 8 + h0 + hh) * 2 + 1] = l[hh];
       }
@@ -850,7 +869,7 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
     // (the transposed product, G = 4: lanes gid and gid + 4 both hold head gid & 3)
     uint32_t qf[KS][2];
     {
-      constexpr bool kT = G == 4;
+      constexpr bool kT = G == 4;                // heads repeated in columns 4-7
       const int head = kT ? (gid & 3) : (gid < G ? gid : 0);
       const uint16_t* qrow = a.q + (static_cast<size_t>(b) * a.Hq + kvh * G + head) * D + (D / 4) * tig;
       const float on = (kT || gid < G) ? 1.0f : 0.0f;
@@ -873,9 +892,9 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
         const uint16_t* ksz_g = reinterpret_cast<const uint16_t*>(base + P::kc + warp * P::meta);
         const uint32_t* vc_g = reinterpret_cast<const uint32_t*>(base + P::kc + P::mt + warp * P::codes);
         const uint16_t* vsz_g = reinterpret_cast<const uint16_t*>(base + 2 * P::kc + P::mt + warp * P::meta);
-        if constexpr (G == 4)
-          group_mma_t<D, BITS>(kc_g, ksz_g, vc_g, vsz_g, qf, bias_mul0, bias_mul1, zcol_mul0, zcol_mul1, zcol_off,
-                               a.scale_log2, st, lane);
+        if constexpr (Transposed<G>::value)
+          group_mma_t<D, BITS, G>(kc_g, ksz_g, vc_g, vsz_g, qf, bias_mul0, bias_mul1, zcol_mul0, zcol_mul1,
+                                  zcol_off, a.scale_log2, st, lane);
         else
           group_mma<D, BITS>(kc_g, ksz_g, vc_g, vsz_g, qf, bias_mul0, bias_mul1, zcol_mul0, zcol_mul1, zcol_off,
                              a.scale_log2, st, lane);
@@ -892,7 +911,7 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
       if (threadIdx.x == 0) atomicOr(&g_draft_status, VC_DEV_BARRIER_TIMEOUT);
       return;                                               // outputs of this call are invalid
     }
-    if constexpr (G == 4)
+    if constexpr (Transposed<G>::value)
       write_partial_t<D, BITS, G>(a, smem, sg.bh, c - first, st);
     else
       write_partial<D, BITS, G>(a, smem, sg.bh, c - first, st);
