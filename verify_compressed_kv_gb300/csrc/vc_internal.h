@@ -20,6 +20,8 @@ void vc_internal_clear(void);
 #endif
 
 #ifdef __CUDACC__
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -174,6 +176,29 @@ __device__ __forceinline__ void vc_bulk_g2s(void* dst, const void* src, uint32_t
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(vc_smem_addr(dst)), "l"(src), "r"(bytes), "r"(vc_smem_addr(bar))
       : "memory");
+}
+
+// TMA tensor copy (2-D tile at coordinates x (innermost), y) into this CTA's
+// shared memory, completion as transaction bytes on `bar`.  x times the element
+// size must be a multiple of 16 bytes.
+__device__ __forceinline__ void vc_tma2(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(vc_smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(vc_smem_addr(bar))
+      : "memory");
+}
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link to
+// the driver library); null when the driver does not provide it.
+static inline PFN_cuTensorMapEncodeTiled_v12000 vc_tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
 }
 
 // ---------------------------------------------------------------- PTX: tcgen05 (tensor cores with TMEM accumulators)

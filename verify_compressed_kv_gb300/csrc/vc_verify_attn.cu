@@ -18,12 +18,13 @@
 // Chunk kernel: grid (parts, row blocks, B*Hkv).  Each CTA owns up to 128
 // query rows of one KV head ((k+1)*G rows: all verify positions x the G
 // query heads sharing that KV head) and 1/parts of the chunk's tokens.  QK^T
-// and PV run on the tensor cores (mma.sync m16n8k16 bf16 -> fp32), K/V tiles
-// of 64 tokens double-buffered in shared memory with cp.async, online softmax
-// in registers.  The part's (max, sum, unnormalised output) is merged into a
-// per-part running state in the workspace with the log-sum-exp rule, so any
-// number of chunks needs only `parts` states.  The finish kernel adds the
-// causal block of the k+1 new tokens and merges everything into bf16 output.
+// and PV run on the tcgen05 tensor cores with fp32 accumulators in TMEM, K/V
+// tiles of 64 tokens arrive by TMA (two stages), the online softmax runs one
+// row per thread out of TMEM.  The part's (max, sum, unnormalised output) is
+// merged into a per-part running state in the workspace with the log-sum-exp
+// rule, so any number of chunks needs only `parts` states.  The finish kernel
+// (mma.sync m16n8k16: a few rows of new tokens) adds the causal block of the
+// k+1 new tokens and merges everything into bf16 output.
 #include <cfloat>
 #include <cstdlib>
 #include <string>
@@ -263,80 +264,6 @@ __device__ __forceinline__ void finish_l(float (&l)[2]) {
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kBoundThreads) verify_chunk_kernel(VerifyArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  constexpr int LD = Cfg<D>::LD;
-  const int nw = blockDim.x >> 5;
-  uint16_t* q_s = reinterpret_cast<uint16_t*>(smem);
-  uint16_t* k_s = q_s + nw * 16 * LD;
-  uint16_t* v_s = k_s + 2 * kTile * LD;
-  const int part = blockIdx.x, rb = blockIdx.y, bh = blockIdx.z;
-  const int b = bh / a.Hkv, kvh = bh % a.Hkv;
-  const int row0 = rb * nw * 16;
-  const int n_valid = min(max(a.prefix_len[b] - a.chunk_start, 0), a.C);
-  const int t_lo = part * a.part_tokens;
-  const int t_hi = min(n_valid, t_lo + a.part_tokens);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float acc[Cfg<D>::NT_O][4];
-#pragma unroll
-  for (int nt = 0; nt < Cfg<D>::NT_O; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
-  if (t_hi > t_lo) {
-    load_q_rows<D>(q_s, a, b, kvh, row0, nw);
-    const size_t slice = static_cast<size_t>(bh) * a.C * D;
-    attend_range<D>(q_s, k_s, v_s, a.k_src + slice, a.v_src + slice, D, t_lo, t_hi, false, a.G, row0,
-                    a.scale_log2, acc, m, l);
-  } else if (!a.first) {
-    return;                                     // nothing to merge
-  }
-  finish_l(l);
-  // merge into the running state of this part; every lane of a row's quad
-  // reads the old (max, sum) before any lane writes the new one
-  const int r_a = row0 + warp * 16 + (lane >> 2);
-  float2 old_ml[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int r = r_a + h * 8;
-    const size_t row = (static_cast<size_t>(part) * a.B * a.Hkv + bh) * a.M + r;
-    old_ml[h] = (r < a.M && !a.first) ? reinterpret_cast<const float2*>(a.st_ml)[row] : make_float2(-INFINITY, 0.0f);
-  }
-  __syncwarp();
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int r = r_a + h * 8;
-    if (r >= a.M) continue;
-    const size_t row = (static_cast<size_t>(part) * a.B * a.Hkv + bh) * a.M + r;
-    float* so = a.st_o + row * D;
-    float2* sml = reinterpret_cast<float2*>(a.st_ml) + row;
-    float sa = 1.0f, sb = 0.0f, mo = m[h], lo = l[h];
-    if (!a.first) {
-      const float2 old = old_ml[h];
-      const float mn = fmaxf(old.x, m[h]);
-      if (mn != -INFINITY) {
-        sb = exp2f(old.x - mn);
-        sa = exp2f(m[h] - mn);
-      }
-      mo = mn;
-      lo = old.y * sb + l[h] * sa;
-    }
-#pragma unroll
-    for (int nt = 0; nt < Cfg<D>::NT_O; ++nt) {
-      const int c = nt * 8 + (lane & 3) * 2;
-      float2 v = make_float2(acc[nt][h * 2] * sa, acc[nt][h * 2 + 1] * sa);
-      if (!a.first) {
-        const float2 old = *reinterpret_cast<const float2*>(so + c);
-        v.x = fmaf(old.x, sb, v.x);
-        v.y = fmaf(old.y, sb, v.y);
-      }
-      *reinterpret_cast<float2*>(so + c) = v;
-    }
-    if ((lane & 3) == 0) *sml = make_float2(mo, lo);
-  }
-}
-
 // New-token causal block + merge of every part state -> bf16 output.
 // grid (row blocks, B*Hkv).
 template <int D>
@@ -407,6 +334,293 @@ __global__ void __launch_bounds__(kBoundThreads) verify_finish_kernel(VerifyArgs
       *reinterpret_cast<uint32_t*>(dst + nt * 8 + (lane & 3) * 2) = pk;
     }
   }
+}
+
+// ------------------------------------------------------------------ chunk kernel on tcgen05
+// grid (parts, ceil(M / 128), B*Hkv); 6 warps:
+//   * warps 0-3: one query row per thread (row = TMEM lane): load the CTA's
+//     128 rows of Q into shared memory, then per tile read the row's scores S
+//     from TMEM, keep the online softmax (max raised only past max + 2^8, the
+//     row's O in TMEM rescaled when it is), write P as bf16 over the row's
+//     scores, and at the end merge the row's (max, sum, O) into the part's
+//     running state;
+//   * warp 4, one thread: K and V tiles of 64 tokens by TMA (128-byte swizzle,
+//     two stages);
+//   * warp 5, one thread: S = Q . K^T (M = 128 rows, N = 64 tokens, K = d;
+//     Q and K K-major in shared memory) and O += P . V (M = 128 rows, N = d,
+//     K = 64 tokens; P from TMEM, V MN-major in shared memory), bf16 operands,
+//     fp32 accumulators in TMEM.  Products of one thread run in issue order,
+//     so S of tile i + 2 is written only after P of tile i has been read.
+constexpr int kTcRows = 128;
+constexpr int kTcTok = 64;
+constexpr int kTcStages = 2;
+constexpr int kTcThreads = 192;
+constexpr long long kTcWait = 4000000000LL;   // ~2 s
+constexpr float kTcLazy = 8.0f;
+
+template <int D>
+struct TcPlan {
+  static constexpr int H = D / 64;                           // 64-channel (128-byte) column halves
+  static constexpr uint32_t q_bytes = H * kTcRows * 128;
+  static constexpr uint32_t kv_bytes = H * kTcTok * 128;     // one K or V tile
+  static constexpr uint32_t stage = 2 * kv_bytes;
+  static constexpr uint32_t off_st = q_bytes;
+  static constexpr uint32_t off_bar = off_st + kTcStages * stage;
+  // full[S], empty[S], q_ready, s_full[2], p_ready[2], o_done[2], done
+  static constexpr int n_bars = 2 * kTcStages + 8;
+  static constexpr uint32_t off_misc = off_bar + n_bars * 8;   // TMEM base, abort flag
+  static constexpr uint32_t total = off_misc + 16 + 1024;      // + room to align the base to 1024
+  static constexpr uint32_t col_s = 0, col_o = 2 * kTcTok;    // TMEM: S[2] (P written over S), O
+  static constexpr uint32_t alloc = col_o + D <= 256 ? 256 : 512;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads) verify_chunk_tc(VerifyArgs a, const __grid_constant__ CUtensorMap tkv) {
+  using P = TcPlan<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (vc_smem_addr(smem_raw) & 1023u)) & 1023u);   // swizzle atoms: 1024-aligned
+  const int part = blockIdx.x, rb = blockIdx.y, bh = blockIdx.z;
+  const int b = bh / a.Hkv, kvh = bh % a.Hkv;
+  const int n_valid = min(max(a.prefix_len[b] - a.chunk_start, 0), a.C);
+  const int t_lo = part * a.part_tokens;
+  const int t_hi = min(n_valid, t_lo + a.part_tokens);
+  const int n_tiles = t_hi > t_lo ? (t_hi - t_lo + kTcTok - 1) / kTcTok : 0;
+  if (n_tiles == 0 && !a.first) return;                      // nothing to merge (uniform over the CTA)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P::off_bar);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kTcStages;
+  uint64_t* q_ready = bars + 2 * kTcStages;
+  uint64_t* s_full = q_ready + 1;
+  uint64_t* p_ready = s_full + 2;
+  uint64_t* o_done = p_ready + 2;
+  uint64_t* done = o_done + 2;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + P::off_misc);
+  volatile uint32_t* abort = misc + 1;
+  if (warp == 0) vc_tc_alloc(misc, P::alloc);
+  if (threadIdx.x == 32) {
+    for (int i = 0; i < kTcStages; ++i) {
+      vc_mbar_init(full + i, 1);
+      vc_mbar_init(empty + i, 1);
+    }
+    vc_mbar_init(q_ready, 4);
+    for (int i = 0; i < 2; ++i) {
+      vc_mbar_init(s_full + i, 1);
+      vc_mbar_init(p_ready + i, 4);
+      vc_mbar_init(o_done + i, 1);
+    }
+    vc_mbar_init(done, 1);
+    *abort = 0u;
+    vc_fence_mbar_init();
+  }
+  vc_tc_fence_before();
+  __syncthreads();
+  vc_tc_fence_after();
+  const uint32_t tmem = misc[0];
+  auto wait = [&](uint64_t* bar, uint32_t parity) { return vc_mbar_wait_sleep_or_abort(bar, parity, abort, kTcWait); };
+
+  if (warp < 4) {
+    // ---------------- one query row per thread
+    const int rl = warp * 32 + lane, r = rb * kTcRows + rl;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    bool ok = true;
+    if (n_tiles > 0) {
+      const bool rv = r < a.M;
+      const int j = rv ? r / a.G : 0, g = rv ? r % a.G : 0;
+      const uint16_t* src = a.q + ((static_cast<size_t>(b) * a.R + j) * a.Hq + kvh * a.G + g) * D;
+#pragma unroll
+      for (int c8 = 0; c8 < D / 8; ++c8) {                   // 128-byte swizzle: chunk c of row rl at c ^ (rl % 8)
+        const uint4 v = rv ? *reinterpret_cast<const uint4*>(src + 8 * c8) : make_uint4(0u, 0u, 0u, 0u);
+        const int h = c8 / 8, c = c8 % 8;
+        *reinterpret_cast<uint4*>(smem + h * (kTcRows * 128) + (rl / 8) * 1024 + (rl % 8) * 128 + ((c ^ (rl % 8)) * 16)) = v;
+      }
+      vc_fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) vc_mbar_arrive(q_ready);
+    }
+    float m = -INFINITY, l = 0.0f;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int bb = i & 1;
+      ok = __all_sync(0xffffffffu, ok && wait(s_full + bb, static_cast<uint32_t>((i >> 1) & 1)));
+      vc_tc_fence_after();
+      float sv[kTcTok];
+      __syncwarp();
+      vc_tc_ld64(t_lane + P::col_s + bb * kTcTok, sv);
+      const int t0 = t_lo + i * kTcTok;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int x = 0; x < kTcTok; ++x) {
+        sv[x] = (t0 + x < t_hi) ? sv[x] * a.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, sv[x]);
+      }
+      // Raise the running max of the rows that outgrew it by more than kTcLazy
+      // (log2 units; rare after the first tile).  The decision is per warp:
+      // TMEM loads and stores are warp-collective, so every lane takes part and
+      // the lanes that keep their max rescale by 1.
+      const bool raise = mx > m + kTcLazy;
+      if (__any_sync(0xffffffffu, raise)) {
+        const float mn = raise ? mx : m;                     // finite: every tile holds a valid token
+        const float alpha = exp2f(m - mn);                   // m = -inf: 0
+        if (i > 0 && ok) {                                   // O holds tiles 0 .. i-1: rescale it in TMEM
+          ok = __all_sync(0xffffffffu, wait(o_done + ((i - 1) & 1), static_cast<uint32_t>(((i - 1) >> 1) & 1)));
+          vc_tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            float ov[32];
+            vc_tc_ld32(t_lane + P::col_o + c0, ov);
+            uint32_t w0[16], w1[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+              w0[x] = __float_as_uint(ov[x] * alpha);
+              w1[x] = __float_as_uint(ov[16 + x] * alpha);
+            }
+            vc_tc_st16(t_lane + P::col_o + c0, w0);
+            vc_tc_st16(t_lane + P::col_o + c0 + 16, w1);
+          }
+          vc_tc_wait_st();
+        }
+        l *= alpha;
+        m = mn;
+      }
+      uint32_t pk[kTcTok / 2];
+      float ps = 0.0f;
+#pragma unroll
+      for (int x = 0; x < kTcTok / 2; ++x) {
+        const float p0 = exp2f(sv[2 * x] - m), p1 = exp2f(sv[2 * x + 1] - m);
+        ps += p0 + p1;
+        pk[x] = pack_bf16(p0, p1);
+      }
+      l += ps;
+      // P (bf16 pairs) over the first kTcTok / 2 columns of this tile's S
+      __syncwarp();
+      vc_tc_st16(t_lane + P::col_s + bb * kTcTok, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+      vc_tc_st16(t_lane + P::col_s + bb * kTcTok + 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+      vc_tc_wait_st();
+      vc_tc_fence_before();
+      __syncwarp();
+      if (lane == 0) vc_mbar_arrive(p_ready + bb);
+    }
+    // ---------------- merge the row into the part's running state
+    if (n_tiles > 0) {
+      ok = ok && wait(o_done + ((n_tiles - 1) & 1), static_cast<uint32_t>(((n_tiles - 1) >> 1) & 1));
+      vc_tc_fence_after();
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    const bool rv = r < a.M;
+    // warp-uniform: the TMEM loads below are warp-collective, rows past M only skip the stores
+    if (ok && __any_sync(0xffffffffu, rv)) {
+      const size_t row = (static_cast<size_t>(part) * a.B * a.Hkv + bh) * a.M + (rv ? r : 0);
+      float* so = a.st_o + row * D;
+      float2* sml = reinterpret_cast<float2*>(a.st_ml) + row;
+      float sa = 1.0f, sb = 0.0f, mo = m, lo = l;
+      if (!a.first && rv) {
+        const float2 old = *sml;
+        const float mn = fmaxf(old.x, m);
+        if (mn != -INFINITY) {
+          sb = exp2f(old.x - mn);
+          sa = exp2f(m - mn);
+        }
+        mo = mn;
+        lo = old.y * sb + l * sa;
+      }
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float ov[32];
+        __syncwarp();
+        if (n_tiles > 0) {
+          vc_tc_ld32(t_lane + P::col_o + c0, ov);
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) ov[x] = 0.0f;
+        }
+        if (rv) {
+#pragma unroll
+          for (int x = 0; x < 32; x += 4) {
+            float4 v = make_float4(ov[x] * sa, ov[x + 1] * sa, ov[x + 2] * sa, ov[x + 3] * sa);
+            if (!a.first) {
+              const float4 o4 = *reinterpret_cast<const float4*>(so + c0 + x);
+              v.x = fmaf(o4.x, sb, v.x);
+              v.y = fmaf(o4.y, sb, v.y);
+              v.z = fmaf(o4.z, sb, v.z);
+              v.w = fmaf(o4.w, sb, v.w);
+            }
+            *reinterpret_cast<float4*>(so + c0 + x) = v;
+          }
+        }
+      }
+      if (rv) *sml = make_float2(mo, lo);
+    }
+  } else if (warp == 4) {
+    // ---------------- K / V tiles by TMA
+    if (lane == 0 && n_tiles > 0) {
+      const int krow0 = (b * a.Hkv + kvh) * a.C;
+      const int vrow0 = a.B * a.Hkv * a.C + krow0;
+      int issued = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int s = i % kTcStages;
+        if (i >= kTcStages && !wait(empty + s, static_cast<uint32_t>(((i / kTcStages) - 1) & 1))) break;
+        uint8_t* st = smem + P::off_st + s * P::stage;
+        const int t0 = t_lo + i * kTcTok;
+        vc_mbar_arrive_expect_tx(full + s, P::stage);
+#pragma unroll
+        for (int h = 0; h < P::H; ++h) {
+          vc_tma2(st + h * (kTcTok * 128), &tkv, 64 * h, krow0 + t0, full + s);
+          vc_tma2(st + P::kv_bytes + h * (kTcTok * 128), &tkv, 64 * h, vrow0 + t0, full + s);
+        }
+        ++issued;
+      }
+      // every tile issued has landed before the CTA may exit
+      for (int i = issued - kTcStages < 0 ? 0 : issued - kTcStages; i < issued; ++i)
+        vc_mbar_wait_bounded(full + i % kTcStages, static_cast<uint32_t>((i / kTcStages) & 1), kTcWait);
+    }
+  } else {
+    // ---------------- products (one thread)
+    if (lane == 0 && n_tiles > 0) {
+      constexpr uint32_t id_qk = vc_tc_idesc_bf16(128, kTcTok);
+      constexpr uint32_t id_pv = vc_tc_idesc_bf16(128, D) | (1u << 16);    // V: MN-major B
+      const uint32_t q_addr = vc_smem_addr(smem), st_addr = vc_smem_addr(smem + P::off_st);
+      bool ok = wait(q_ready, 0);
+      auto pv = [&](int t) {
+        const int s = t % kTcStages, bb = t & 1;
+        if (!wait(p_ready + bb, static_cast<uint32_t>((t >> 1) & 1))) return false;
+        vc_tc_fence_after();
+        const uint32_t v_addr = st_addr + s * P::stage + P::kv_bytes;
+#pragma unroll
+        for (int ks = 0; ks < kTcTok / 16; ++ks)
+          vc_tc_mma_ta(tmem + P::col_o, tmem + P::col_s + bb * kTcTok + ks * 8,
+                       vc_tc_desc(v_addr + ks * 2048, kTcTok * 128, 1024) | (2ull << 61), id_pv, t > 0 || ks > 0);
+        vc_tc_commit(o_done + bb);
+        vc_tc_commit(empty + s);
+        return true;
+      };
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        const int s = i % kTcStages, bb = i & 1;
+        if (!wait(full + s, static_cast<uint32_t>((i / kTcStages) & 1))) {
+          ok = false;
+          break;
+        }
+        vc_tc_fence_after();
+        const uint32_t k_addr = st_addr + s * P::stage;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          vc_tc_mma(tmem + P::col_s + bb * kTcTok,
+                    vc_tc_desc_sw128(q_addr + (ks / 4) * (kTcRows * 128) + (ks % 4) * 32),
+                    vc_tc_desc_sw128(k_addr + (ks / 4) * (kTcTok * 128) + (ks % 4) * 32), id_qk, ks > 0);
+        vc_tc_commit(s_full + bb);
+        if (i > 0) ok = pv(i - 1);
+      }
+      if (ok) ok = pv(n_tiles - 1);
+      // every product issued has completed before TMEM is freed
+      vc_tc_commit(done);
+      vc_mbar_wait_bounded(done, 0, kTcWait);
+      if (!ok) *abort = 1u;
+    }
+  }
+  vc_tc_fence_before();
+  __syncthreads();
+  vc_tc_fence_after();
+  if (threadIdx.x == 0 && *abort != 0u) atomicOr(&g_verify_status, VC_DEV_BARRIER_TIMEOUT);
+  if (warp == 0) vc_tc_dealloc(tmem, P::alloc);
 }
 
 // Commit: grid (2 * Hkv, B), one CTA per (K|V, KV head, request).  Writes rows
@@ -484,14 +698,36 @@ void fill_args(VerifyArgs& a, const vc_shape_t* s, int parts, void* ws) {
   a.st_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + ((rows * s->d * sizeof(float) + 255) & ~size_t(255)));
 }
 
+// Row blocks of the tcgen05 chunk kernel: 128 rows each.
+int tc_row_blocks(const vc_shape_t* s) { return ((s->k + 1) * (s->Hq / s->Hkv) + kTcRows - 1) / kTcRows; }
+
 template <int D>
-vc_status_t launch_chunk(const VerifyArgs& a, const Geometry& g, cudaStream_t cs) {
-  const size_t sm = smem_bytes<D>(g.nw);
-  VC_CUDA_CHECK(cudaFuncSetAttribute(verify_chunk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
-  VC_CUDA_CHECK(cudaFuncSetAttribute(verify_chunk_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+vc_status_t tc_setup() {
+  VC_CUDA_CHECK(cudaFuncSetAttribute(verify_chunk_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(TcPlan<D>::total)));
+  VC_CUDA_CHECK(cudaFuncSetAttribute(verify_chunk_tc<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared));   // two CTAs per SM
-  verify_chunk_kernel<D><<<dim3(a.parts, g.row_blocks, a.B * a.Hkv), g.nw * 32, sm, cs>>>(a);
-  VC_LAUNCH_CHECK("verify_chunk_kernel");
+  return VC_OK;
+}
+
+// A chunk slot [K|V][B][Hkv][C][d] as one 2-D tensor of 2*B*Hkv*C rows of d
+// bf16, in boxes of 64 channels x 64 tokens with the 128-byte swizzle (zero past the end).
+template <int D>
+vc_status_t launch_chunk(const VerifyArgs& a, const vc_shape_t* s, cudaStream_t cs) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = vc_tensor_map_encoder();
+  if (!encode) VC_FAIL(VC_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  CUtensorMap tkv;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), 2ull * a.B * a.Hkv * a.C};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTcTok)}, es[2] = {1, 1};
+  const CUresult r = encode(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.k_src), dims, strides,
+                            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) VC_FAIL(VC_ERR_CUDA, "chunk tensor map: error %d", static_cast<int>(r));
+  vc_status_t st = tc_setup<D>();
+  if (st != VC_OK) return st;
+  verify_chunk_tc<D><<<dim3(a.parts, tc_row_blocks(s), a.B * a.Hkv), kTcThreads, TcPlan<D>::total, cs>>>(a, tkv);
+  VC_LAUNCH_CHECK("verify_chunk_tc");
   return VC_OK;
 }
 
@@ -514,10 +750,9 @@ vc_status_t chunk_impl(const vc_shape_t* s, const uint16_t* q, const uint16_t* k
   a.C = C;
   a.chunk_start = chunk_start;
   a.prefix_len = prefix_len;
-  a.part_tokens = ((C + parts - 1) / parts + kTile - 1) / kTile * kTile;
+  a.part_tokens = ((C + parts - 1) / parts + kTcTok - 1) / kTcTok * kTcTok;
   a.first = first;
-  const Geometry g = geometry(s);
-  return s->d == 128 ? launch_chunk<128>(a, g, cs) : launch_chunk<64>(a, g, cs);
+  return s->d == 128 ? launch_chunk<128>(a, s, cs) : launch_chunk<64>(a, s, cs);
 }
 
 vc_status_t finish_impl(const vc_shape_t* s, const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
@@ -598,18 +833,16 @@ extern "C" vc_status_t vc_verify_attn_workspace_size(const vc_shape_t* s, int32_
 namespace {
 template <int D>
 vc_status_t plan_parts(const vc_shape_t* s, int C, int* parts) {
-  const Geometry g = geometry(s);
-  const size_t sm = smem_bytes<D>(g.nw);
-  VC_CUDA_CHECK(cudaFuncSetAttribute(verify_chunk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
-  VC_CUDA_CHECK(cudaFuncSetAttribute(verify_chunk_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared));   // two CTAs per SM
+  vc_status_t st = tc_setup<D>();
+  if (st != VC_OK) return st;
   int per_sm = 0, dev = 0, sms = 0;
-  VC_CUDA_CHECK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_chunk_kernel<D>, g.nw * 32, sm));
+  VC_CUDA_CHECK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_chunk_tc<D>, kTcThreads,
+                                                              TcPlan<D>::total));
   VC_CUDA_CHECK(cudaGetDevice(&dev));
   VC_CUDA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   const int64_t slots = static_cast<int64_t>(per_sm > 0 ? per_sm : 1) * sms;
-  const int64_t units = static_cast<int64_t>(s->B) * s->Hkv * g.row_blocks;
-  const int tiles = (C + kTile - 1) / kTile;
+  const int64_t units = static_cast<int64_t>(s->B) * s->Hkv * tc_row_blocks(s);
+  const int tiles = (C + kTcTok - 1) / kTcTok;
   int best = 1;
   int64_t best_cost = INT64_MAX;
   for (int p = 1; p <= kMaxPlannedParts && p <= tiles; ++p) {
