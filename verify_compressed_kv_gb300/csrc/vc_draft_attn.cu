@@ -17,17 +17,16 @@
 //     by bulk async copies (cp.async.bulk + mbarrier transaction counts, bounded
 //     waits) while the 11 consumer warps compute on earlier stages;
 //   * each warp owns one group per stage and keeps its own online-softmax
-//     state (max, sums) and output accumulators, all G heads of the KV head as
-//     rows of 16x8x16 tensor-core products: the packed codes become operand
-//     registers with one shift and one logic op per pair (1 + code/f is exact
-//     in fp16), the key scales fold into the query and the value scales into
-//     the softmax weights, each fold carried as an fp16 (hi, lo) pair so the
-//     products keep ~22 bits, and the zero points enter through two narrow
-//     correction products (group_mma below); with G = 4 the roles swap
-//     (codes as the A operand, the 4 heads as the 8 columns, group_mma_t),
-//     which halves the QK and PV products, and the folds are single fp16
-//     values (the draft is lossy by design: fp16 rounding of the folded
-//     operands sits far below the codes' own error);
+//     state (max, sums) and output accumulators for all G heads of the KV
+//     head, on 16x8x16 fp16 tensor-core products with the codes as the A
+//     operand and the heads as the 8 columns (group_mma): a packed code field,
+//     masked in place, is itself an fp16 subnormal, code * 2^(p - 24), so an
+//     operand register of two codes costs one AND; the key scales and the
+//     codes' powers of two fold into the query, the value scales into the
+//     softmax weights, and the zero points enter through two narrow products
+//     (q . z per head; weights . z per channel group).  The folded operands
+//     are single fp16 values: the draft is lossy by design, and their
+//     rounding sits far below the codes' own error;
 //   * at the end of a segment the warps are merged (log-sum-exp) into one
 //     partial per query head; the last CTA to finish a (request, KV head)
 //     (arrival counter in the workspace, reset by that CTA) merges all its
@@ -173,61 +172,61 @@ __device__ __forceinline__ float fast_exp2(float x) {
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
-// (hi, lo) of x*y: hi = fp16(x*y), lo = fp16(x*y - hi) (the residual of the
-// exact product; exact itself when x and y carry <= 22 significant bits).
-__device__ __forceinline__ void split_mul(__half2 x, __half2 y, uint32_t& hi, uint32_t& lo) {
-  const __half2 h = __hmul2(x, y);
-  hi = h2u(h);
-  lo = h2u(__hfma2(x, y, __hneg2(h)));
-}
-
-// Operand value of a packed code field: OR the field (moved to the top
-// mantissa bits by slot_shift) into the bit pattern of 1.0: 1 + code/f exactly.
-//   b = 2, r = 0: bits 8-9 of each half -> 1 + code/4   (f = 4)
-//   b = 2, r = 1: bits 6-7              -> 1 + code/16  (f = 16)
-//   b = 4:        bits 6-9              -> 1 + code/16  (f = 16)
-//   b = 8:        bits 2-9              -> 1 + code/256 (f = 256)
+// Code operands.  A packed code field becomes a tensor-core operand with no
+// arithmetic: masked in place inside the mantissa of an fp16 whose exponent
+// bits are zero, the field IS the subnormal number code * 2^(p - 24), p its
+// lowest bit.  One AND (one immediate) per operand register, two codes, one
+// per 16-bit half; the fields that lie above bit 9 are first brought down by
+// one shift of the whole word, shared by every field of that word.  The power
+// 2^(p - 24) is folded into the other operand (the query, per k-step and
+// register, for keys; the weights per register and a per-channel output factor
+// for values) and into the softmax scale.  Field positions (include/vc.h):
+//   b = 2: slot (u, r) at 16e + 4u + 2(1 - r); u = 2, 3 from the word shifted
+//          right by 6, so p = R(u) + C(r), R = {0, 4, 2, 6}, C(r) = 2(1 - r);
+//   b = 4: slot u at 16e + 4u; u = 2, 3 from the word shifted right by 8, so
+//          p = 4 (u & 1), which is 4r for keys and values alike;
+//   b = 8: slot u at 16e + 8u; u = 1 from the word shifted right by 8; p = 0.
 template <int BITS>
-__device__ __forceinline__ uint32_t field_value(uint32_t x, int r) {
-  if (BITS == 2) return r == 0 ? ((x & 0x03000300u) | 0x3C003C00u) : ((x & 0x00C000C0u) | 0x3C003C00u);
-  if (BITS == 8) return (x & 0x03FC03FCu) | 0x3C003C00u;
-  return (x & 0x03C003C0u) | 0x3C003C00u;
+__host__ __device__ constexpr int pos_row(int u) {
+  return BITS == 2 ? 4 * (u & 1) + 2 * (u >> 1) : 0;
 }
 template <int BITS>
-__host__ __device__ constexpr float field_scale(int r) {
-  return BITS == 8 ? 256.0f : ((BITS == 2 && r == 0) ? 4.0f : 16.0f);
+__host__ __device__ constexpr int pos_col(int r) {
+  return BITS == 2 ? 2 * (1 - r) : (BITS == 4 ? 4 * r : 0);
 }
+// Key operands carry slot u = ks % 4 in k-step ks (b = 2), so the field
+// position of register r of k-step ks is:
 template <int BITS>
-__host__ __device__ constexpr float field_log2(int r) {
-  return BITS == 8 ? 8.0f : ((BITS == 2 && r == 0) ? 2.0f : 4.0f);
+__host__ __device__ constexpr int pos_key(int ks, int r) {
+  return pos_row<BITS>(ks % 4) + pos_col<BITS>(r);
 }
-
-// Word w moved so that slot u's fields land in the operand windows: the e = 0
-// field of slot u starts at 4u + 2(1 - r) (b = 2) or 4u (b = 4), so a shift by
-// 4u - 6 brings it to bit 8 (r = 0) / bit 6 (r = 1, b = 4); the e = 1 field,
-// 16 bits higher, lands 16 bits higher too.  One plain shift, nothing wraps.
-__device__ __forceinline__ uint32_t slot_shift(uint32_t w, int u) {
-  return u == 0 ? (w << 6) : u == 1 ? (w << 2) : u == 2 ? (w >> 2) : (w >> 6);
+// The folded operands keep the codes' powers of two at most 2^kFold, as the
+// weights (<= 2^kLazy) and the folded query must stay inside the fp16 range:
+// keys Q' = q s 2^(kFold - p) (scores come out times 2^(kFold - 24)), values
+// P' = p s 2^(kFold - C(r)) (outputs times 2^(kFold - 24 + R(u))).
+constexpr int kFold = 4;
+// fp16 2^k in both halves of a register (|k| <= 14).
+__host__ __device__ constexpr uint32_t pow2_h2(int k) {
+  return (static_cast<uint32_t>(k + 15) << 10) * 0x10001u;
 }
-// b = 8: the e = 0 field of slot u starts at 8u; a shift by 8u - 2 brings it to bit 2.
-__device__ __forceinline__ uint32_t slot_shift8(uint32_t w, int u) { return u == 0 ? (w << 2) : (w >> 6); }
 
 // Operand registers (r = 0, 1) of fragment index i — the field rules of the
 // packed words (include/vc.h): b = 2: word i/4, slot u = i%4; b = 4: i2 = 2i + r,
 // word i2/4, slot u = i2%4; b = 8: word (2i + r)/2 = i, slot u = r.
 template <int BITS, int WPL>
-__device__ __forceinline__ void fragment(const uint32_t (&w)[WPL], int i, uint32_t& b0, uint32_t& b1) {
+__device__ __forceinline__ void code_operands(const uint32_t (&w)[WPL], int i, uint32_t& b0, uint32_t& b1) {
   if (BITS == 2) {
-    const uint32_t x = slot_shift(w[i / 4], i % 4);
-    b0 = field_value<2>(x, 0);
-    b1 = field_value<2>(x, 1);
+    const int u = i % 4;
+    const uint32_t x = u < 2 ? w[i / 4] : (w[i / 4] >> 6);
+    b0 = x & (0x00030003u << (pos_row<2>(u) + pos_col<2>(0)));
+    b1 = x & (0x00030003u << (pos_row<2>(u) + pos_col<2>(1)));
   } else if (BITS == 4) {
     const int i0 = 2 * i, i1 = 2 * i + 1;
-    b0 = field_value<4>(slot_shift(w[i0 / 4], i0 % 4), 0);
-    b1 = field_value<4>(slot_shift(w[i1 / 4], i1 % 4), 1);
-  } else {                                   // b = 8: word i holds slots u = 0 (r = 0) and 1 (r = 1)
-    b0 = field_value<8>(slot_shift8(w[i], 0), 0);
-    b1 = field_value<8>(slot_shift8(w[i], 1), 1);
+    b0 = ((i0 % 4) < 2 ? w[i0 / 4] : (w[i0 / 4] >> 8)) & 0x000F000Fu;
+    b1 = ((i1 % 4) < 2 ? w[i1 / 4] : (w[i1 / 4] >> 8)) & 0x00F000F0u;
+  } else {
+    b0 = w[i] & 0x00FF00FFu;
+    b1 = (w[i] >> 8) & 0x00FF00FFu;
   }
 }
 
@@ -241,163 +240,30 @@ __device__ __forceinline__ void load_lane_words(const uint32_t* g, int lane, uin
   }
 }
 
-// Per-warp running state of one segment: rows = the lane's head gid.
-template <int D>
-struct WarpState {
-  static constexpr int NT = D / 8;
-  float o[NT][4];       // PV accumulators: cols 8nt + 2tig (+1), rows gid / gid+8
-  float oz[4];          // correction columns (2g: zeros, 2g+1: scales) of group g = tig
-  float l0, l1;         // sums of the softmax weights of r = 0 / r = 1 tokens (times f_r)
-  float m;              // running max (log2 units) the weights are relative to
-};
-
 // Rescale threshold (log2 units): the running max is raised only when a group's
 // max exceeds it by more than this, so weights stay <= 2^kLazy * 16.
 constexpr float kLazy = 3.0f;
 
-// One group of 32 tokens for the lane's head (row gid), all on tensor cores.
-//
-//   score(t) = sum_c q_c (s_c code_tc + z_c)
-//            = sum_c (f_c q_c s_c)(1 + code_tc / f_c) + sum_c q_c (z_c - f_c s_c)
-// The first sum is one product per n-tile with A = f q s split into (hi, lo)
-// fp16 rows and B = the codes' operand values; the second ("bias") is one
-// product per k-step with A = f q (exact in fp16) and B columns z / f and -s.
-//   out_h = sum_t p_t (sv_t code_tc + zv_t)
-//         = sum_t (f_t p_t sv_t)(1 + code_tc / f_t) + sum_t (f_t p_t)(zv_t / f_t - sv_t)
-// likewise with one A per channel group (sv depends on the group) and one
-// correction product whose columns are (zv / f, -sv) per channel group.
-template <int D, int BITS>
-__device__ __forceinline__ void group_mma(const uint32_t* kc_g, const uint16_t* ksz_g, const uint32_t* vc_g,
-                                          const uint16_t* vsz_g, const uint32_t (&qf)[D / 16][2],
-                                          uint32_t bias_mul0, uint32_t bias_mul1,
-                                          uint32_t zcol_mul0, uint32_t zcol_mul1, int zcol_off, float cs,
-                                          WarpState<D>& st, int lane) {
-  constexpr int KS = D / 16, NT = D / 8, NCG = D / 32, WPL = D * BITS / 32;
-  const int gid = lane >> 2, tig = lane & 3;
-  // ---------------- QK
-  uint32_t kw[WPL];
-  load_lane_words<WPL>(kc_g, lane, kw);
-  // scales of the lane's channels (D/4) tig + 4ks + 2r + {0, 1}: one half2 per (ks, r)
-  const uint32_t* srow = reinterpret_cast<const uint32_t*>(ksz_g) + (D / 8) * tig;
-  const uint32_t* zrow = reinterpret_cast<const uint32_t*>(ksz_g) + (gid == 0 ? D / 2 : 0) + (D / 8) * tig;
-  float c[4][4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
-  float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-  for (int kq = 0; kq < KS / 2; ++kq) {
-    const uint4 s4 = *reinterpret_cast<const uint4*>(srow + 4 * kq);     // (ks, r) = (2kq, 0), (2kq, 1), (2kq+1, 0), (2kq+1, 1)
-    const uint4 z4 = *reinterpret_cast<const uint4*>(zrow + 4 * kq);
-    const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
-    const uint32_t zv[4] = {z4.x, z4.y, z4.z, z4.w};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int ks = 2 * kq + h;
-      uint32_t a0, a1, a2, a3;
-      split_mul(u2h(qf[ks][0]), u2h(sv[2 * h]), a0, a1);
-      split_mul(u2h(qf[ks][1]), u2h(sv[2 * h + 1]), a2, a3);
-      mma16816(cb, qf[ks][0], 0u, qf[ks][1], 0u, h2u(__hmul2(u2h(zv[2 * h]), u2h(bias_mul0))),
-               h2u(__hmul2(u2h(zv[2 * h + 1]), u2h(bias_mul1))));
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t b0, b1;
-        fragment<BITS, WPL>(kw, j * KS + ks, b0, b1);
-        mma16816(c[j], a0, a1, a2, a3, b0, b1);
-      }
-    }
-  }
-  // bias of row gid: columns 0 (q.z) and 1 (-q.f s) live in the quad's tig 0 lane
-  const float bias = __shfl_sync(0xffffffffu, cb[0] + cb[1], lane & ~3);
-  // ---------------- online softmax (row gid; tokens 8 tig + 4e + j)
-  float y[4][2];
-  float my = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      y[j][e] = c[j][e] + c[j][2 + e];
-      my = fmaxf(my, y[j][e]);
-    }
-  my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 1));
-  my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 2));
-  const float mx = (my + bias) * cs;
-  const bool need = !(mx <= st.m + kLazy);
-  if (__any_sync(0xffffffffu, need)) {
-    const float mn = need ? mx : st.m;
-    const float alpha = fast_exp2(st.m - mn);          // m = -inf at the start: alpha = 0
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) st.o[nt][k] *= alpha;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) st.oz[k] *= alpha;
-    st.l0 *= alpha;
-    st.l1 *= alpha;
-    st.m = mn;
-  }
-  const float k0 = fmaf(bias, cs, -st.m);
-  // weights times f_r (r = j % 2), split into fp16 (hi, lo)
-  uint32_t ph[4], pl[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float kk = k0 + field_log2<BITS>(j & 1);
-    const float p0 = fast_exp2(fmaf(y[j][0], cs, kk));
-    const float p1 = fast_exp2(fmaf(y[j][1], cs, kk));
-    if (j & 1) st.l1 += p0 + p1; else st.l0 += p0 + p1;
-    const __half2 h = __floats2half2_rn(p0, p1);
-    const float2 hf = __half22float2(h);
-    ph[j] = h2u(h);
-    pl[j] = h2u(__floats2half2_rn(p0 - hf.x, p1 - hf.y));
-  }
-  // ---------------- PV
-  uint32_t vw[WPL];
-  load_lane_words<WPL>(vc_g, lane, vw);
-  // correction columns: lane gid feeds column gid = (group gid/2, zeros | scales)
-  {
-    const uint4 r4 = *reinterpret_cast<const uint4*>(vsz_g + zcol_off + 8 * tig);
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      const uint32_t b0 = h2u(__hmul2(u2h(s ? r4.z : r4.x), u2h(zcol_mul0)));
-      const uint32_t b1 = h2u(__hmul2(u2h(s ? r4.w : r4.y), u2h(zcol_mul1)));
-      mma16816(st.oz, ph[2 * s], pl[2 * s], ph[2 * s + 1], pl[2 * s + 1], b0, b1);
-    }
-  }
-#pragma unroll
-  for (int g = 0; g < NCG; ++g) {
-    const uint4 s4 = *reinterpret_cast<const uint4*>(vsz_g + g * 64 + 8 * tig);   // (s, r) = (0,0), (0,1), (1,0), (1,1)
-    const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      uint32_t a[4];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const __half2 x = u2h(ph[2 * s + r]), sc = u2h(sv[2 * s + r]);
-        const __half2 h = __hmul2(x, sc);
-        a[2 * r] = h2u(h);
-        a[2 * r + 1] = h2u(__hfma2(u2h(pl[2 * s + r]), sc, __hfma2(x, sc, __hneg2(h))));
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int nt = 4 * g + u;
-        uint32_t b0, b1;
-        fragment<BITS, WPL>(vw, s * NT + nt, b0, b1);
-        mma16816(st.o[nt], a[0], a[1], a[2], a[3], b0, b1);
-      }
-    }
-  }
-}
-
-// ------------------------------------------------------------------ transposed group product (G = 4)
-// With G = 4 the 16 rows of a product above carry only 8 of 16 (hi, lo) query
-// rows.  Here the roles swap: S^T = codes . Q'^T and O^T = V^T . P'^T, with
-// the codes as the A operand (16 tokens or 16 channels per tile) and the
-// 4 heads' hi and lo parts as the 8 columns: 16 QK + 16 PV products per group
-// instead of 32 + 32.  The packed words need no change: the B fragment of
-// n-tile j is the top (b0) / bottom (b1) register pair of an A fragment whose
-// rows are the tokens of n-tiles j and j' (a0 = b0 of j, a1 = b0 of j',
-// a2 = b1 of j, a3 = b1 of j').  The QK accumulator block of tokens 4 gid + j
-// (j = 2 mt + half), transposed in registers (movmatrix), is the PV B fragment
-// of k-step s = j / 2, register r = j % 2.
+// ------------------------------------------------------------------ group product
+// One group of 32 tokens for all G heads of the warp's KV head, on tensor
+// cores with the codes as the A operand and the heads as the 8 columns:
+//   S^T = codes . Q'^T (16 tokens per m-tile, k = channels), and
+//   O^T += V^T . P'^T  (16 channels per m-tile, k = tokens),
+// 16 QK + 16 PV products per group (d = 128).  With
+//   score(t) = sum_c q_c (s_c code_tc + z_c) = sum_c Q'_c code_tc 2^(p_c - 24) 2^(24 - kFold) + sum_c q_c z_c
+// the first sum is the QK product (code operands as above, Q' = q s 2^(kFold - p)
+// per k-step and register) and the second, the bias, one narrow product per
+// k-step with A = q and B = the zeros.  Likewise
+//   out_h(c) = sum_t p_t (sv_t code_tc + zv_t)
+// is the PV product (P' = p sv 2^(kFold - C(r))) times the channel's output
+// factor, plus one correction product per k-step with A = the weights and B =
+// the zeros of each channel group.  The packed words need no change: the B
+// fragment of n-tile j is the top (b0) / bottom (b1) register pair of an A
+// fragment whose rows are the tokens of n-tiles j and j' (a0 = b0 of j, a1 =
+// b0 of j', a2 = b1 of j, a3 = b1 of j').  The QK accumulator block of tokens
+// 4 gid + j (j = 2 mt + half), transposed in registers (movmatrix), is the PV
+// B fragment of k-step s = j / 2, register r = j % 2.  G = 4 fills columns
+// 4-7 with the same 4 heads at zero weight (each lane then holds whole heads).
 
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   uint32_t y;
@@ -405,41 +271,19 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   return y;
 }
 
-// Per-warp running state of one segment, transposed: the lane's heads are
-// h0 = 2 (tig & 1) and h0 + 1.
+// Per-warp running state of one segment: the lane's heads are h0 = 2 (tig & 1)
+// (G = 4) or 2 tig, and h0 + 1.
 template <int D>
-struct WarpStateT {
+struct WarpState {
   static constexpr int MT = D / 16;
-  float o[MT][4];       // O^T: rows = channels 16 mt + gid (+ 8), cols 2 tig (+1) = (lo if tig >= 2) of heads h0 (+1)
-  float oz[4];          // correction: rows = P' columns (gid: lo if >= 4, head gid & 3), cols = (channel group tig, zeros | scales)
-  float l0[2], l1[2];   // per head: sums of the weights of r = 0 / r = 1 tokens (times f_r)
+  float o[MT][4];       // O^T: rows = channels 16 mt + gid (+ 8), cols 2 tig (+1) = heads h0 (+1)
+  float oz[4];          // correction: rows = P' columns (head gid; G = 4: gid & 3), cols = channel group tig (zeros)
+  float l0[2], l1[2];   // per head: sums of the weights of r = 0 / r = 1 tokens (times 2^(kFold - C(r)))
   float m[2];           // per head: running max (log2 units)
-};
-
-// Every head count up to 8 takes the transposed product (heads as the 8 columns).
-template <int G>
-struct Transposed {
-  static constexpr bool value = G <= 8;
-};
-template <int D, int G, bool T = Transposed<G>::value>
-struct StateOf {
-  using type = WarpState<D>;
-};
-template <int D, int G>
-struct StateOf<D, G, true> {
-  using type = WarpStateT<D>;
 };
 
 template <int D>
 __device__ __forceinline__ void init_state(WarpState<D>& st) {
-#pragma unroll
-  for (int nt = 0; nt < D / 8; ++nt) st.o[nt][0] = st.o[nt][1] = st.o[nt][2] = st.o[nt][3] = 0.0f;
-  st.oz[0] = st.oz[1] = st.oz[2] = st.oz[3] = 0.0f;
-  st.l0 = st.l1 = 0.0f;
-  st.m = -INFINITY;
-}
-template <int D>
-__device__ __forceinline__ void init_state(WarpStateT<D>& st) {
 #pragma unroll
   for (int m = 0; m < D / 16; ++m) st.o[m][0] = st.o[m][1] = st.o[m][2] = st.o[m][3] = 0.0f;
   st.oz[0] = st.oz[1] = st.oz[2] = st.oz[3] = 0.0f;
@@ -447,18 +291,16 @@ __device__ __forceinline__ void init_state(WarpStateT<D>& st) {
   st.m[0] = st.m[1] = -INFINITY;
 }
 
+// cs = softmax scale in log2 units; cs_code = cs * 2^(24 - kFold) for the
+// code products.
 template <int D, int BITS, int G>
-__device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t* ksz_g, const uint32_t* vc_g,
-                                            const uint16_t* vsz_g, const uint32_t (&qf)[D / 16][2],
-                                            uint32_t bias_mul0, uint32_t bias_mul1,
-                                            uint32_t zcol_mul0, uint32_t zcol_mul1, int zcol_off, float cs,
-                                            WarpStateT<D>& st, int lane) {
+__device__ __forceinline__ void group_mma(const uint32_t* kc_g, const uint16_t* ksz_g, const uint32_t* vc_g,
+                                          const uint16_t* vsz_g, const uint32_t (&qf)[D / 16][2],
+                                          uint32_t zcol_mul0, uint32_t zcol_mul1, int zcol_off, float cs,
+                                          float cs_code, WarpState<D>& st, int lane) {
   constexpr int KS = D / 16, NT = D / 8, NCG = D / 32, WPL = D * BITS / 32;
   const int gid = lane >> 2, tig = lane & 3;
-  // G = 4: columns 4-7 repeat heads 0-3 (each lane then holds its heads' whole
-  // scores) and their weights are zero; otherwise column n is head n (zero
-  // query past G).  The lane's heads are columns 2 tig, 2 tig + 1.
-  const bool lo_p = G == 4 && tig >= 2;
+  const bool lo_p = G == 4 && tig >= 2;         // G = 4: columns 4-7 (zero weight)
   const int h0 = G == 4 ? 2 * (tig & 1) : 2 * tig;
   // ---------------- S^T = codes . Q'^T
   uint32_t kw[WPL];
@@ -469,10 +311,6 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) c[mt][0] = c[mt][1] = c[mt][2] = c[mt][3] = 0.0f;
   float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  // cone: the sum over channels of the fp16 Q' values themselves (an all-ones A),
-  // so the "1 +" part of the code operands cancels exactly whatever Q' rounded to
-  float cone[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  constexpr uint32_t kOnes = 0x3C003C00u;
 #pragma unroll
   for (int kq = 0; kq < KS / 2; ++kq) {
     const uint4 s4 = *reinterpret_cast<const uint4*>(srow + 4 * kq);
@@ -482,27 +320,27 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int ks = 2 * kq + h;
-      // Q'^T column n carries head n (G = 4: head n & 3), fp16 f q s
+      // Q'^T column n carries head n (G = 4: head n & 3): fp16 q s 2^(kFold - p)
       const uint32_t qb0 = h2u(__hmul2(u2h(qf[ks][0]), u2h(sv[2 * h])));
       const uint32_t qb1 = h2u(__hmul2(u2h(qf[ks][1]), u2h(sv[2 * h + 1])));
-      mma16816(cb, qf[ks][0], 0u, qf[ks][1], 0u, h2u(__hmul2(u2h(zv[2 * h]), u2h(bias_mul0))),
-               h2u(__hmul2(u2h(zv[2 * h + 1]), u2h(bias_mul1))));
-      mma16816(cone, kOnes, kOnes, kOnes, kOnes, qb0, qb1);
+      // bias q . z (column 0; gid 0 lanes feed the zeros): q itself, the power of two undone exactly
+      const int e0 = pos_key<BITS>(ks, 0) - kFold, e1 = pos_key<BITS>(ks, 1) - kFold;
+      const uint32_t qz0 = e0 == 0 ? qf[ks][0] : h2u(__hmul2(u2h(qf[ks][0]), u2h(pow2_h2(e0))));
+      const uint32_t qz1 = e1 == 0 ? qf[ks][1] : h2u(__hmul2(u2h(qf[ks][1]), u2h(pow2_h2(e1))));
+      mma16816(cb, qz0, 0u, qz1, 0u, zv[2 * h], zv[2 * h + 1]);
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         uint32_t a0, a1, a2, a3;
-        fragment<BITS, WPL>(kw, (2 * mt) * KS + ks, a0, a2);
-        fragment<BITS, WPL>(kw, (2 * mt + 1) * KS + ks, a1, a3);
+        code_operands<BITS, WPL>(kw, (2 * mt) * KS + ks, a0, a2);
+        code_operands<BITS, WPL>(kw, (2 * mt + 1) * KS + ks, a1, a3);
         mma16816(c[mt], a0, a1, a2, a3, qb0, qb1);
       }
     }
   }
-  // bias of head h: q.z (row h, column 0 of the bias product, in lane 4 h) minus
-  // the sum of its Q' column (every row of cone: this lane's own columns)
-  const float bias[2] = {__shfl_sync(0xffffffffu, cb[0], 4 * h0) - cone[0],
-                         __shfl_sync(0xffffffffu, cb[0], 4 * h0 + 4) - cone[1]};
-  // y[mt][2 half + hh] = score of token 4 gid + 2 mt + half, head h0 + hh (columns
-  // 2 tig, 2 tig + 1 hold heads h0, h0 + 1 in both column halves)
+  // bias of head h: row h, column 0 of the bias product (lane 4 h)
+  const float bias[2] = {__shfl_sync(0xffffffffu, cb[0], 4 * h0), __shfl_sync(0xffffffffu, cb[0], 4 * h0 + 4)};
+  // y[mt][2 half + hh] = code part of the score of token 4 gid + 2 mt + half, head
+  // h0 + hh, times 2^(kFold - 24) (columns 2 tig, 2 tig + 1 hold heads h0, h0 + 1)
   float (&y)[2][4] = c;
   // ---------------- online softmax, one state per head
   float mx[2];
@@ -513,7 +351,7 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
     my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 4));
     my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 8));
     my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 16));
-    mx[hh] = (my + bias[hh]) * cs;
+    mx[hh] = fmaf(my, cs_code, bias[hh] * cs);
     need[hh] = !(mx[hh] <= st.m[hh] + kLazy);
   }
   if (__any_sync(0xffffffffu, need[0] || need[1])) {
@@ -541,14 +379,14 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
     for (int k = 0; k < 4; ++k) st.oz[k] *= a_oz;
   }
   const float kk[2] = {fmaf(bias[0], cs, -st.m[0]), fmaf(bias[1], cs, -st.m[1])};
-  // weights times f_r (r = token parity = half) in fp16; block j = 2 mt + half
+  // weights times 2^(kFold - C(r)) (r = token parity = half) in fp16; block j = 2 mt + half
   uint32_t ph[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int mt = j >> 1, half = j & 1;
-    const float lf = field_log2<BITS>(half);
-    const float p0 = fast_exp2(fmaf(y[mt][2 * half], cs, kk[0] + lf));
-    const float p1 = fast_exp2(fmaf(y[mt][2 * half + 1], cs, kk[1] + lf));
+    const float lf = static_cast<float>(kFold - pos_col<BITS>(half));
+    const float p0 = fast_exp2(fmaf(y[mt][2 * half], cs_code, kk[0] + lf));
+    const float p1 = fast_exp2(fmaf(y[mt][2 * half + 1], cs_code, kk[1] + lf));
     if (half) {
       st.l1[0] += p0;
       st.l1[1] += p1;
@@ -558,7 +396,7 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
     }
     ph[j] = h2u(__floats2half2_rn(p0, p1));
   }
-  // ---------------- correction: A = P' blocks transposed (rows = P' columns; rows 4-7 zero), B = meta columns
+  // ---------------- correction: A = P' blocks transposed (rows = P' columns; rows 8-15 zero), B = zero columns
   {
     uint32_t pu[4];
 #pragma unroll
@@ -593,8 +431,8 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
         uint32_t a0, a1, a2, a3;
-        fragment<BITS, WPL>(vw, s * NT + 2 * m, a0, a2);
-        fragment<BITS, WPL>(vw, s * NT + 2 * m + 1, a1, a3);
+        code_operands<BITS, WPL>(vw, s * NT + 2 * m, a0, a2);
+        code_operands<BITS, WPL>(vw, s * NT + 2 * m + 1, a1, a3);
         mma16816(st.o[m], a0, a1, a2, a3, pb[2 * s], pb[2 * s + 1]);
       }
     }
@@ -604,41 +442,6 @@ __device__ __forceinline__ void group_mma_t(const uint32_t* kc_g, const uint16_t
 // ------------------------------------------------------------------ merge / arrive / combine
 template <int D, int BITS, int G>
 __device__ void merge_partials(const DraftArgs& a, uint8_t* smem, int bh, int slot);
-
-// Partial of this CTA for slice bh: merge the warps' (max, sum, output) in
-// shared memory and write one normalised partial + log2-sum-exp per head.
-template <int D, int BITS, int G>
-__device__ void write_partial(const DraftArgs& a, uint8_t* smem, int bh, int slot, WarpState<D>& st) {
-  using P = Plan<D, BITS, G>;
-  constexpr int NT = D / 8, NCG = D / 32;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = lane >> 2, tig = lane & 3;
-  float* red = reinterpret_cast<float*>(smem + P::off_red);             // [warp][G][D]
-  float* wstat = reinterpret_cast<float*>(smem + P::off_wstat);         // [warp][8][2]
-  // correction of channel group g for row gid sits in lane (gid, g)
-  const float ozl = st.oz[0] + st.oz[1] + st.oz[2] + st.oz[3];
-  float ozg[NCG];
-#pragma unroll
-  for (int g = 0; g < NCG; ++g) ozg[g] = __shfl_sync(0xffffffffu, ozl, (lane & ~3) | g);
-  float l = st.l0 * (1.0f / field_scale<BITS>(0)) + st.l1 * (1.0f / field_scale<BITS>(1));
-  l += __shfl_xor_sync(0xffffffffu, l, 1);
-  l += __shfl_xor_sync(0xffffffffu, l, 2);
-  if (gid < G) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float2 v;
-      v.x = st.o[nt][0] + st.o[nt][2] + ozg[nt / 4];
-      v.y = st.o[nt][1] + st.o[nt][3] + ozg[nt / 4];
-      *reinterpret_cast<float2*>(red + (warp * G + gid) * D + 8 * nt + 2 * tig) = v;
-    }
-    if (tig == 0) {
-      wstat[(warp * 8 + gid) * 2] = st.m;
-      wstat[(warp * 8 + gid) * 2 + 1] = l;
-    }
-  }
-  vc_bar_sync(1, kConsumers);
-  merge_partials<D, BITS, G>(a, smem, bh, slot);
-}
 
 // The warps' (max, sum, output) of slice bh, left in `red` / `wstat` by the
 // consumer warps (after a consumer barrier), merged into one normalised
@@ -673,13 +476,15 @@ __device__ void merge_partials(const DraftArgs& a, uint8_t* smem, int bh, int sl
   }
 }
 
-// write_partial for the transposed state: per head its columns (G = 4: the
-// column and its zero-weight repeat), the correction of each channel group,
-// the softmax sum over the warp's tokens.
+// Partial of this CTA for slice bh: each warp leaves per head its output
+// (G = 4: the column and its zero-weight repeat added; the code part times the
+// channel's output factor 2^(24 - kFold - R(u)), plus the correction of the
+// channel group) and its (max, softmax sum) in shared memory; then the warps
+// are merged into one normalised partial + log2-sum-exp per head.
 template <int D, int BITS, int G>
-__device__ void write_partial_t(const DraftArgs& a, uint8_t* smem, int bh, int slot, WarpStateT<D>& st) {
+__device__ void write_partial(const DraftArgs& a, uint8_t* smem, int bh, int slot, WarpState<D>& st) {
   using P = Plan<D, BITS, G>;
-  static_assert(G <= 8, "the transposed product carries at most 8 heads");
+  static_assert(G <= 8, "the group product carries at most 8 heads");
   constexpr int MT = D / 16, NCG = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -697,7 +502,8 @@ __device__ void write_partial_t(const DraftArgs& a, uint8_t* smem, int bh, int s
   float l[2];
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
-    float x = st.l0[hh] * (1.0f / field_scale<BITS>(0)) + st.l1[hh] * (1.0f / field_scale<BITS>(1));
+    float x = st.l0[hh] * exp2f(static_cast<float>(pos_col<BITS>(0) - kFold)) +
+              st.l1[hh] * exp2f(static_cast<float>(pos_col<BITS>(1) - kFold));
     x += __shfl_xor_sync(0xffffffffu, x, 4);
     x += __shfl_xor_sync(0xffffffffu, x, 8);
     x += __shfl_xor_sync(0xffffffffu, x, 16);
@@ -713,11 +519,14 @@ __device__ void write_partial_t(const DraftArgs& a, uint8_t* smem, int bh, int s
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       const int c0 = 16 * m + gid, g = m / 2;
+      // rows gid / gid + 8 of m-tile m: n-tiles 2 m / 2 m + 1, slots (2 m) % 4 / (2 m + 1) % 4
+      const float f_lo = exp2f(static_cast<float>(24 - kFold - pos_row<BITS>((2 * m) % 4)));
+      const float f_hi = exp2f(static_cast<float>(24 - kFold - pos_row<BITS>((2 * m + 1) % 4)));
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         if (h0 + hh >= G) continue;
-        red[(warp * G + h0 + hh) * D + c0] = v[m][hh] + corr[hh][g];
-        red[(warp * G + h0 + hh) * D + c0 + 8] = v[m][2 + hh] + corr[hh][g];
+        red[(warp * G + h0 + hh) * D + c0] = fmaf(v[m][hh], f_lo, corr[hh][g]);
+        red[(warp * G + h0 + hh) * D + c0 + 8] = fmaf(v[m][2 + hh], f_hi, corr[hh][g]);
       }
     }
     if (gid == 0) {
@@ -844,16 +653,14 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
     if (lane == 0) produce<D, BITS, G>(a, smem, c, full, empty, abort);
     return;
   }
-  // lane constants: bias columns (gid 0: zeros / f, gid 1: -scales) and
-  // correction columns (gid = 2g: zeros / f, gid = 2g + 1: -scales of channel
-  // group g; a V meta row pair holds the scales first, then the zeros)
-  const float f0 = field_scale<BITS>(0), f1 = field_scale<BITS>(1);
-  const uint32_t bias_mul0 = h2u(__float2half2_rn(gid == 0 ? 1.0f / f0 : (gid == 1 ? -1.0f : 0.0f)));
-  const uint32_t bias_mul1 = h2u(__float2half2_rn(gid == 0 ? 1.0f / f1 : (gid == 1 ? -1.0f : 0.0f)));
-  const bool zc = gid < 2 * NCG;
-  const uint32_t zcol_mul0 = h2u(__float2half2_rn(!zc ? 0.0f : ((gid & 1) ? -1.0f : 1.0f / f0)));
-  const uint32_t zcol_mul1 = h2u(__float2half2_rn(!zc ? 0.0f : ((gid & 1) ? -1.0f : 1.0f / f1)));
-  const int zcol_off = zc ? 32 * (gid ^ 1) : 0;
+  // lane constants: correction columns (gid = 2g: the zeros of channel group
+  // g, over the weights' factor 2^(kFold - C(r)); odd gid: zero columns; a V
+  // meta row pair holds the scales first, then the zeros)
+  const bool zc = gid < 2 * NCG && (gid & 1) == 0;
+  const uint32_t zcol_mul0 = zc ? pow2_h2(pos_col<BITS>(0) - kFold) : 0u;
+  const uint32_t zcol_mul1 = zc ? pow2_h2(pos_col<BITS>(1) - kFold) : 0u;
+  const int zcol_off = zc ? 32 * (gid + 1) : 0;
+  const float cs_code = a.scale_log2 * exp2f(static_cast<float>(24 - kFold));
   int buf = 0;                                  // ring position and phase of the next stage use
   uint32_t phase = 0;
   const long long hi = range_lo(c + 1, a.total, a.n_stream);
@@ -865,8 +672,8 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
     const int b = sg.bh / a.Hkv, kvh = sg.bh % a.Hkv;
     int first, last;
     ctas_of(sg.bh, a, first, last);
-    // query fragments of head gid, times f_r: channels (D/4) tig + 4ks + 2r + {0, 1}
-    // (the transposed product, G = 4: lanes gid and gid + 4 both hold head gid & 3)
+    // query fragments of head gid times 2^(kFold - p) of their k-step and register:
+    // channels (D/4) tig + 4ks + 2r + {0, 1} (G = 4: lanes gid and gid + 4 both hold head gid & 3)
     uint32_t qf[KS][2];
     {
       constexpr bool kT = G == 4;                // heads repeated in columns 4-7
@@ -878,11 +685,13 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
         const uint2 raw = *reinterpret_cast<const uint2*>(qrow + 4 * ks);
         const float q0 = vc_bf16_to_f32(static_cast<uint16_t>(raw.x)), q1 = vc_bf16_to_f32(static_cast<uint16_t>(raw.x >> 16));
         const float q2 = vc_bf16_to_f32(static_cast<uint16_t>(raw.y)), q3 = vc_bf16_to_f32(static_cast<uint16_t>(raw.y >> 16));
-        qf[ks][0] = h2u(__floats2half2_rn(q0 * on * f0, q1 * on * f0));
-        qf[ks][1] = h2u(__floats2half2_rn(q2 * on * f1, q3 * on * f1));
+        const float f0 = on * exp2f(static_cast<float>(kFold - pos_key<BITS>(ks, 0)));
+        const float f1 = on * exp2f(static_cast<float>(kFold - pos_key<BITS>(ks, 1)));
+        qf[ks][0] = h2u(__floats2half2_rn(q0 * f0, q1 * f0));
+        qf[ks][1] = h2u(__floats2half2_rn(q2 * f1, q3 * f1));
       }
     }
-    typename StateOf<D, G>::type st;
+    WarpState<D> st;
     init_state(st);
     for (int s = 0; s < sg.n_st; ++s) {
       const bool ok = __all_sync(0xffffffffu, vc_mbar_wait_or_abort(full + buf, phase, abort, kWaitCycles));
@@ -892,12 +701,8 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
         const uint16_t* ksz_g = reinterpret_cast<const uint16_t*>(base + P::kc + warp * P::meta);
         const uint32_t* vc_g = reinterpret_cast<const uint32_t*>(base + P::kc + P::mt + warp * P::codes);
         const uint16_t* vsz_g = reinterpret_cast<const uint16_t*>(base + 2 * P::kc + P::mt + warp * P::meta);
-        if constexpr (Transposed<G>::value)
-          group_mma_t<D, BITS, G>(kc_g, ksz_g, vc_g, vsz_g, qf, bias_mul0, bias_mul1, zcol_mul0, zcol_mul1,
-                                  zcol_off, a.scale_log2, st, lane);
-        else
-          group_mma<D, BITS>(kc_g, ksz_g, vc_g, vsz_g, qf, bias_mul0, bias_mul1, zcol_mul0, zcol_mul1, zcol_off,
-                             a.scale_log2, st, lane);
+        group_mma<D, BITS, G>(kc_g, ksz_g, vc_g, vsz_g, qf, zcol_mul0, zcol_mul1, zcol_off, a.scale_log2, cs_code,
+                              st, lane);
       }
       __syncwarp();
       if (lane == 0) vc_mbar_arrive(empty + buf);          // this warp is done with the stage
@@ -911,10 +716,7 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
       if (threadIdx.x == 0) atomicOr(&g_draft_status, VC_DEV_BARRIER_TIMEOUT);
       return;                                               // outputs of this call are invalid
     }
-    if constexpr (Transposed<G>::value)
-      write_partial_t<D, BITS, G>(a, smem, sg.bh, c - first, st);
-    else
-      write_partial<D, BITS, G>(a, smem, sg.bh, c - first, st);
+    write_partial<D, BITS, G>(a, smem, sg.bh, c - first, st);
     arrive_and_combine<G, D>(a, flag, sg.bh, last - first + 2, kConsumers);
     vc_bar_sync(1, kConsumers);                             // red / flag reused by the next segment
   }
