@@ -306,10 +306,13 @@ __device__ __forceinline__ void group_mma(const uint32_t* kc_g, const uint16_t* 
   uint32_t kw[WPL];
   load_lane_words<WPL>(kc_g, lane, kw);
   const uint32_t* srow = reinterpret_cast<const uint32_t*>(ksz_g) + (D / 8) * tig;
-  const uint32_t* zrow = reinterpret_cast<const uint32_t*>(ksz_g) + (gid == 0 ? D / 2 : 0) + (D / 8) * tig;
-  float c[2][4];
+  // bias columns: gid 0 and 1 feed the zeros (of the even / odd k-step of a pair)
+  const uint32_t* zrow = reinterpret_cast<const uint32_t*>(ksz_g) + (gid <= 1 ? D / 2 : 0) + (D / 8) * tig;
+  float c[2][2][4];                              // [m-tile][k-step parity]: two short chains each
 #pragma unroll
-  for (int mt = 0; mt < 2; ++mt) c[mt][0] = c[mt][1] = c[mt][2] = c[mt][3] = 0.0f;
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) c[mt][h][0] = c[mt][h][1] = c[mt][h][2] = c[mt][h][3] = 0.0f;
   float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
   for (int kq = 0; kq < KS / 2; ++kq) {
@@ -317,48 +320,63 @@ __device__ __forceinline__ void group_mma(const uint32_t* kc_g, const uint16_t* 
     const uint4 z4 = *reinterpret_cast<const uint4*>(zrow + 4 * kq);
     const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
     const uint32_t zv[4] = {z4.x, z4.y, z4.z, z4.w};
+    // bias q . z of k-steps 2 kq and 2 kq + 1 in one product: A rows 0-7 = q of the
+    // even k-step, rows 8-15 = q of the odd one; B column 0 = zeros of the even,
+    // column 1 = zeros of the odd k-step (q itself: the power of two undone exactly)
+    uint32_t qz[2][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int e = pos_key<BITS>(2 * kq + h, r) - kFold;
+        qz[h][r] = e == 0 ? qf[2 * kq + h][r] : h2u(__hmul2(u2h(qf[2 * kq + h][r]), u2h(pow2_h2(e))));
+      }
+    mma16816(cb, qz[0][0], qz[1][0], qz[0][1], qz[1][1], gid == 1 ? zv[2] : zv[0], gid == 1 ? zv[3] : zv[1]);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int ks = 2 * kq + h;
       // Q'^T column n carries head n (G = 4: head n & 3): fp16 q s 2^(kFold - p)
       const uint32_t qb0 = h2u(__hmul2(u2h(qf[ks][0]), u2h(sv[2 * h])));
       const uint32_t qb1 = h2u(__hmul2(u2h(qf[ks][1]), u2h(sv[2 * h + 1])));
-      // bias q . z (column 0; gid 0 lanes feed the zeros): q itself, the power of two undone exactly
-      const int e0 = pos_key<BITS>(ks, 0) - kFold, e1 = pos_key<BITS>(ks, 1) - kFold;
-      const uint32_t qz0 = e0 == 0 ? qf[ks][0] : h2u(__hmul2(u2h(qf[ks][0]), u2h(pow2_h2(e0))));
-      const uint32_t qz1 = e1 == 0 ? qf[ks][1] : h2u(__hmul2(u2h(qf[ks][1]), u2h(pow2_h2(e1))));
-      mma16816(cb, qz0, 0u, qz1, 0u, zv[2 * h], zv[2 * h + 1]);
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         uint32_t a0, a1, a2, a3;
         code_operands<BITS, WPL>(kw, (2 * mt) * KS + ks, a0, a2);
         code_operands<BITS, WPL>(kw, (2 * mt + 1) * KS + ks, a1, a3);
-        mma16816(c[mt], a0, a1, a2, a3, qb0, qb1);
+        mma16816(c[mt][h], a0, a1, a2, a3, qb0, qb1);
       }
     }
   }
-  // bias of head h: row h, column 0 of the bias product (lane 4 h)
-  const float bias[2] = {__shfl_sync(0xffffffffu, cb[0], 4 * h0), __shfl_sync(0xffffffffu, cb[0], 4 * h0 + 4)};
+  // bias of head h: row h, column 0 plus row h + 8, column 1 (lane 4 h)
+  const float cbs = cb[0] + cb[3];
+  const float bias[2] = {__shfl_sync(0xffffffffu, cbs, 4 * h0), __shfl_sync(0xffffffffu, cbs, 4 * h0 + 4)};
   // y[mt][2 half + hh] = code part of the score of token 4 gid + 2 mt + half, head
   // h0 + hh, times 2^(kFold - 24) (columns 2 tig, 2 tig + 1 hold heads h0, h0 + 1)
-  float (&y)[2][4] = c;
+  float y[2][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) y[mt][k] = c[mt][0][k] + c[mt][1][k];
   // ---------------- online softmax, one state per head
-  float mx[2];
-  bool need[2];
+  // The running max is raised only past max + kLazy: a lane-local check of its own
+  // 4 tokens per head, and the exact group max (8 lanes) only when some lane needs it.
+  float my[2];
+  bool need_l = false;
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
-    float my = fmaxf(fmaxf(y[0][hh], y[0][2 + hh]), fmaxf(y[1][hh], y[1][2 + hh]));
-    my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 4));
-    my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 8));
-    my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 16));
-    mx[hh] = fmaf(my, cs_code, bias[hh] * cs);
-    need[hh] = !(mx[hh] <= st.m[hh] + kLazy);
+    my[hh] = fmaxf(fmaxf(y[0][hh], y[0][2 + hh]), fmaxf(y[1][hh], y[1][2 + hh]));
+    need_l = need_l || !(fmaf(my[hh], cs_code, bias[hh] * cs) <= st.m[hh] + kLazy);
   }
-  if (__any_sync(0xffffffffu, need[0] || need[1])) {
+  if (__any_sync(0xffffffffu, need_l)) {
     float alpha[2];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      const float mn = need[hh] ? mx[hh] : st.m[hh];
+      float g = my[hh];
+      g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, 4));
+      g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, 8));
+      g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, 16));
+      const float mx = fmaf(g, cs_code, bias[hh] * cs);
+      const float mn = mx <= st.m[hh] + kLazy ? st.m[hh] : mx;
       alpha[hh] = fast_exp2(st.m[hh] - mn);     // m = -inf at the start: alpha = 0
       st.l0[hh] *= alpha[hh];
       st.l1[hh] *= alpha[hh];
@@ -397,10 +415,11 @@ __device__ __forceinline__ void group_mma(const uint32_t* kc_g, const uint16_t* 
     ph[j] = h2u(__floats2half2_rn(p0, p1));
   }
   // ---------------- correction: A = P' blocks transposed (rows = P' columns; rows 8-15 zero), B = zero columns
-  {
-    uint32_t pu[4];
+  // pu[j], lane (gid, tig): head gid (G = 4: gid & 3), tokens 8 tig + j and 8 tig + 4 + j
+  uint32_t pu[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) pu[j] = movmatrix_t(lo_p ? 0u : ph[j]);
+  for (int j = 0; j < 4; ++j) pu[j] = movmatrix_t(lo_p ? 0u : ph[j]);
+  {
     const uint4 r4 = *reinterpret_cast<const uint4*>(vsz_g + zcol_off + 8 * tig);
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
@@ -414,17 +433,13 @@ __device__ __forceinline__ void group_mma(const uint32_t* kc_g, const uint16_t* 
   load_lane_words<WPL>(vc_g, lane, vw);
 #pragma unroll
   for (int g = 0; g < NCG; ++g) {
-    // scales of tokens 4 gid + j: entry 8 (gid >> 1) + 2 j + (gid & 1) of the group's scale row
-    const uint4 s4 = *reinterpret_cast<const uint4*>(vsz_g + g * 64 + 8 * (gid >> 1));
+    // scales of tokens 8 tig + j, 8 tig + 4 + j: word 4 tig + j of the group's
+    // scale row (the value meta layout pairs exactly these tokens)
+    const uint4 s4 = *reinterpret_cast<const uint4*>(vsz_g + g * 64 + 8 * tig);
     const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w};
-    const uint32_t sel = (gid & 1) ? 0x3232u : 0x1010u;
     uint32_t pb[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint32_t sv2;
-      asm("prmt.b32 %0, %1, %1, %2;" : "=r"(sv2) : "r"(sw[j]), "r"(sel));   // (sv, sv) of token 4 gid + j
-      pb[j] = movmatrix_t(lo_p ? 0u : h2u(__hmul2(u2h(ph[j]), u2h(sv2))));   // every lane transposes
-    }
+    for (int j = 0; j < 4; ++j) pb[j] = h2u(__hmul2(u2h(pu[j]), u2h(sw[j])));
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int m = 2 * g + u;                  // channels 16 m .. 16 m + 15 = n-tiles 2 m, 2 m + 1
