@@ -6,8 +6,8 @@
 // compressed KV).  One query token per request per step; all G query heads
 // of a KV head share every byte read.
 //
-// One launch per draft step.  Grid = B*Hkv tail CTAs followed by a persistent
-// set of stream CTAs (occupancy x SM count):
+// One launch per draft step: one wave of persistent stream CTAs (occupancy x
+// SM count), then up to as many tail CTAs:
 //   * stream-K partition: the packed groups of every (request, KV head) are
 //     laid end to end and each stream CTA takes an equal contiguous range, so
 //     the work is balanced whatever B*Hkv is; a range may span two heads
@@ -31,9 +31,12 @@
 //     partial per query head; the last CTA to finish a (request, KV head)
 //     (arrival counter in the workspace, reset by that CTA) merges all its
 //     partials and writes the bf16 output.
-// The tail CTAs handle the bf16 tail (tokens committed since the last full
-// group plus earlier draft steps) and the current token, and store the
-// current token's K/V into the tail for the following steps.
+// Tail CTAs, launched after the stream CTAs (they start as the first stream
+// CTAs finish, in the shadow of the slowest), take the bf16 tails (tokens
+// committed since the last full group, earlier draft steps, the current
+// token) and store the current token's K/V into the tail for the following
+// steps.
+#include <algorithm>
 #include <cfloat>
 
 #include "vc_internal.h"
@@ -66,7 +69,8 @@ struct DraftArgs {
   int B, Hq, Hkv;
   int NG;                   // layout stride: T_cap / 32 groups per (b, h)
   int NGmax;                // groups per (b, h) covered by the partition
-  int n_stream;             // stream CTAs
+  int n_stream;             // stream CTAs with packed groups
+  int n_cta;                // CTAs launched: n_stream stream CTAs, then the tail CTAs
   long long total;          // B * Hkv * NGmax
   int max_parts;            // partial slots per (b, h): stream CTAs + the tail
   float scale_log2;
@@ -77,7 +81,10 @@ struct DraftArgs {
 };
 
 // ------------------------------------------------------------------ partition
-__host__ __device__ inline long long range_lo(long long c, long long total, long long n) { return c * total / n; }
+// Start of stream CTA c's groups in the stream-K order (equal shares).
+__host__ __device__ inline long long range_lo(long long c, const DraftArgs& a) {
+  return c >= a.n_stream ? a.total : c * a.total / a.n_stream;
+}
 
 // Stream CTAs overlapping the groups of (b, h) index bh: [first, last].
 __host__ __device__ inline void ctas_of(int bh, const DraftArgs& a, int& first, int& last) {
@@ -88,13 +95,13 @@ __host__ __device__ inline void ctas_of(int bh, const DraftArgs& a, int& first, 
   }
   const long long s = static_cast<long long>(bh) * a.NGmax, e = s + a.NGmax;
   long long c = s * a.n_stream / a.total;
-  while (c + 1 < a.n_stream && range_lo(c + 1, a.total, a.n_stream) <= s) ++c;
-  while (c > 0 && range_lo(c, a.total, a.n_stream) > s) --c;
+  while (c + 1 < a.n_stream && range_lo(c + 1, a) <= s) ++c;
+  while (c > 0 && range_lo(c, a) > s) --c;
   first = static_cast<int>(c);
   long long d = (e * a.n_stream + a.total - 1) / a.total;
   if (d > a.n_stream - 1) d = a.n_stream - 1;
-  while (d > 0 && range_lo(d, a.total, a.n_stream) >= e) --d;
-  while (d + 1 < a.n_stream && range_lo(d + 1, a.total, a.n_stream) < e) ++d;
+  while (d > 0 && range_lo(d, a) >= e) --d;
+  while (d + 1 < a.n_stream && range_lo(d + 1, a) < e) ++d;
   last = static_cast<int>(d);
 }
 
@@ -112,29 +119,12 @@ struct Plan {
   static constexpr size_t red = static_cast<size_t>(kWarps) * G * D * 4;   // warp merge
   static constexpr size_t off_red = ring;
   static constexpr size_t body = ring + red;
-  static constexpr size_t q = static_cast<size_t>(G) * D * 4;             // tail CTA: fp32 queries
   static constexpr size_t wstat = static_cast<size_t>(kWarps) * 8 * 2 * 4;  // per-warp (max, sum) per head
-  static constexpr size_t off_q = body;
-  static constexpr size_t off_wstat = off_q + q;
+  static constexpr size_t off_wstat = body;
   static constexpr size_t off_bar = (off_wstat + wstat + 15) & ~size_t(15);   // full[NS], empty[NS]
   static constexpr size_t off_flag = off_bar + 16 * NS;                      // combine flag, abort flag
   static constexpr size_t total = off_flag + 16;
 };
-
-// Shared memory the tail CTA needs inside the same allocation (rows of the tail
-// K/V plus its scores); checked on the host against Plan::off_q.
-template <int D, int G>
-__host__ __device__ inline size_t tail_smem(int tail_cap) {
-  return 2 * static_cast<size_t>(tail_cap + 1) * D * 2 + static_cast<size_t>(G) * (tail_cap + 1) * 4 + 64;
-}
-
-template <int D, int G>
-__device__ __forceinline__ void load_q(const DraftArgs& a, int b, int kvh, float* q_s) {
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const int h = i / D, c = i % D;
-    q_s[i] = vc_bf16_to_f32(a.q[(static_cast<size_t>(b) * a.Hq + kvh * G + h) * D + c]) * a.scale_log2;
-  }
-}
 
 // Issue the bulk copies of one stage (groups [g, g + n) of slice bh) into `buf`.
 template <int D, int BITS, int G>
@@ -558,12 +548,9 @@ __device__ void write_partial(const DraftArgs& a, uint8_t* smem, int bh, int slo
 }
 
 // Count this CTA's partial for slice bh; the last of the n_parts arrivals
-// merges all partials of the slice and writes its bf16 output.
-// `nthr` threads take part: the consumer warps of a stream CTA (named barrier
-// 1) or the whole tail CTA.
-__device__ __forceinline__ void sync_part(int nthr) {
-  if (nthr == kConsumers) vc_bar_sync(1, kConsumers); else __syncthreads();
-}
+// merges all partials of the slice and writes its bf16 output.  The consumer
+// warps of the CTA take part (named barrier 1; the producer warp does not).
+__device__ __forceinline__ void sync_part(int nthr) { vc_bar_sync(1, nthr); }
 
 template <int G, int D>
 __device__ void arrive_and_combine(const DraftArgs& a, unsigned int* flag, int bh, int n_parts, int nthr) {
@@ -580,21 +567,156 @@ __device__ void arrive_and_combine(const DraftArgs& a, unsigned int* flag, int b
   for (int i = threadIdx.x; i < G * D; i += nthr) {
     const int h = i / D, c = i % D;
     const size_t row = static_cast<size_t>(b * a.Hq + kvh * G + h) * a.max_parts;
-    float M = -INFINITY;
-    for (int x = 0; x < n_parts; ++x) M = fmaxf(M, __ldcg(a.part_lse + row + x));
-    float num = 0.0f, den = 0.0f;
-    if (M != -INFINITY) {
-      for (int x = 0; x < n_parts; ++x) {
-        const float lse = __ldcg(a.part_lse + row + x);
-        if (lse == -INFINITY) continue;
-        const float wgt = exp2f(lse - M);
-        num = fmaf(wgt, __ldcg(a.part_o + (row + x) * D + c), num);
+    // parts 8 at a time, all loads of a chunk in flight together; the running
+    // (max, numerator, denominator) is rescaled when a chunk raises the max
+    float M = -INFINITY, num = 0.0f, den = 0.0f;
+    for (int x0 = 0; x0 < n_parts; x0 += 8) {
+      float lse[8], ov[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const bool in = x0 + u < n_parts;
+        lse[u] = in ? __ldcg(a.part_lse + row + x0 + u) : -INFINITY;
+        ov[u] = in ? __ldcg(a.part_o + (row + x0 + u) * D + c) : 0.0f;
+      }
+      float cm = M;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) cm = fmaxf(cm, lse[u]);
+      if (cm == -INFINITY) continue;
+      const float r = exp2f(M - cm);             // M = -inf: 0
+      num *= r;
+      den *= r;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (lse[u] == -INFINITY) continue;         // an empty part: its output is not read
+        const float wgt = exp2f(lse[u] - cm);
+        num = fmaf(wgt, ov[u], num);
         den += wgt;
       }
+      M = cm;
     }
     a.out[(static_cast<size_t>(b) * a.Hq + kvh * G + h) * D + c] = vc_f32_to_bf16_rn(den > 0.0f ? num / den : 0.0f);
   }
   if (threadIdx.x == 0) a.counter[bh] = 0u;          // zero again for the next call
+}
+
+// ------------------------------------------------------------------ bf16 tail
+// The bf16 tail tokens 0 .. tail_len + step - 1 and the current token of slice
+// bh, taken by the consumer warps of a tail CTA.  Warp w takes the tokens t = w
+// (mod kWarps), 8 in flight, K and V rows straight from global memory (each
+// lane D/32 channels), with an online-softmax state per head in registers;
+// the warps' (max, sum, output) go to the warp-merge region and
+// merge_partials writes the tail's partial (the slot after the stream CTAs'
+// of the slice).  The current token's K/V are kept in the tail for the
+// following steps.
+template <int D, int BITS, int G>
+__device__ void tail_part(const DraftArgs& a, uint8_t* smem, int bh) {
+  using P = Plan<D, BITS, G>;
+  constexpr int CPL = D / 32;                  // channels per lane
+  constexpr int U = 8;                         // tokens per warp in flight
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* red = reinterpret_cast<float*>(smem + P::off_red);
+  float* wstat = reinterpret_cast<float*>(smem + P::off_wstat);
+  unsigned int* flag = reinterpret_cast<unsigned int*>(smem + P::off_flag);
+  const int b = bh / a.Hkv, kvh = bh % a.Hkv;
+  int first, last;
+  ctas_of(bh, a, first, last);
+  const int n_c = last - first + 1;
+  const int slot = n_c;                        // the tail's partial follows the stream CTAs'
+  const int n_tail = a.tail_len[b] + a.step;
+  const bool has_cur = a.k_cur != nullptr;
+  const int n_tok = n_tail + (has_cur ? 1 : 0);
+  const size_t tbase = static_cast<size_t>(bh) * a.tail_cap * D;
+  const bool bad = n_tail < 0 || n_tail > a.tail_cap || (has_cur && n_tail >= a.tail_cap);
+  if (bad && threadIdx.x == 0) atomicOr(&g_draft_status, VC_DEV_CAPACITY);
+  if (bad || n_tok == 0) {
+    for (int h = threadIdx.x; h < G; h += kConsumers)
+      a.part_lse[static_cast<size_t>(b * a.Hq + kvh * G + h) * a.max_parts + slot] = -INFINITY;
+    arrive_and_combine<G, D>(a, flag, bh, n_c + 1, kConsumers);
+    return;
+  }
+  float m[G], l[G], o[G][CPL];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) o[h][j] = 0.0f;
+  }
+  float qv[G][CPL];
+  for (int t0 = warp; t0 < n_tok; t0 += kWarps * U) {
+    uint32_t kr[U][CPL / 2], vr[U][CPL / 2];   // bf16 pairs of the lane's channels
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int t = t0 + u * kWarps;
+      const uint16_t* kp = t < n_tail ? a.tail_k + tbase + static_cast<size_t>(t) * D : a.k_cur + static_cast<size_t>(bh) * D;
+      const uint16_t* vp = t < n_tail ? a.tail_v + tbase + static_cast<size_t>(t) * D : a.v_cur + static_cast<size_t>(bh) * D;
+#pragma unroll
+      for (int j = 0; j < CPL / 2; ++j) {
+        kr[u][j] = t < n_tok ? reinterpret_cast<const uint32_t*>(kp + CPL * lane)[j] : 0u;
+        vr[u][j] = t < n_tok ? reinterpret_cast<const uint32_t*>(vp + CPL * lane)[j] : 0u;
+      }
+    }
+    if (t0 == warp) {                          // the queries, once the first rows are in flight
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const uint32_t* qp = reinterpret_cast<const uint32_t*>(a.q + (static_cast<size_t>(b) * a.Hq + kvh * G + h) * D + CPL * lane);
+#pragma unroll
+        for (int j = 0; j < CPL / 2; ++j) {
+          const uint32_t x = qp[j];
+          qv[h][2 * j] = __uint_as_float(x << 16) * a.scale_log2;
+          qv[h][2 * j + 1] = __uint_as_float(x & 0xFFFF0000u) * a.scale_log2;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (t0 + u * kWarps >= n_tok) break;     // uniform over the warp
+      float kf[CPL], vf[CPL];
+#pragma unroll
+      for (int j = 0; j < CPL / 2; ++j) {
+        kf[2 * j] = __uint_as_float(kr[u][j] << 16);
+        kf[2 * j + 1] = __uint_as_float(kr[u][j] & 0xFFFF0000u);
+        vf[2 * j] = __uint_as_float(vr[u][j] << 16);
+        vf[2 * j + 1] = __uint_as_float(vr[u][j] & 0xFFFF0000u);
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) s = fmaf(qv[h][j], kf[j], s);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        const float mn = fmaxf(m[h], s);
+        const float alpha = exp2f(m[h] - mn);  // m = -inf at the first token: 0
+        const float p = exp2f(s - mn);
+        l[h] = fmaf(l[h], alpha, p);
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) o[h][j] = fmaf(o[h][j], alpha, p * vf[j]);
+        m[h] = mn;
+      }
+    }
+  }
+  // the warp's (max, sum, output) per head (a warp without tokens leaves max = -inf)
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) red[(warp * G + h) * D + CPL * lane + j] = o[h][j];
+    if (lane == 0) {
+      wstat[(warp * 8 + h) * 2] = m[h];
+      wstat[(warp * 8 + h) * 2 + 1] = l[h];
+    }
+  }
+  vc_bar_sync(1, kConsumers);
+  merge_partials<D, BITS, G>(a, smem, bh, slot);
+  if (has_cur) {                               // keep the current token for the next steps
+    for (int i = threadIdx.x; i < D / 8; i += kConsumers) {
+      reinterpret_cast<uint4*>(a.tail_k + tbase + static_cast<size_t>(n_tail) * D)[i] =
+          reinterpret_cast<const uint4*>(a.k_cur + static_cast<size_t>(bh) * D)[i];
+      reinterpret_cast<uint4*>(a.tail_v + tbase + static_cast<size_t>(n_tail) * D)[i] =
+          reinterpret_cast<const uint4*>(a.v_cur + static_cast<size_t>(bh) * D)[i];
+    }
+  }
+  arrive_and_combine<G, D>(a, flag, bh, n_c + 1, kConsumers);
 }
 
 // ------------------------------------------------------------------ stream CTA
@@ -626,8 +748,8 @@ __device__ void produce(const DraftArgs& a, uint8_t* smem, int c, uint64_t* full
   int buf = 0;                                  // ring position of the next stage use
   uint32_t phase = 0;                           // completed wraps of the ring, mod 2
   bool wrapped = false;                         // every buffer used at least once
-  const long long hi = range_lo(c + 1, a.total, a.n_stream);
-  long long pos = range_lo(c, a.total, a.n_stream);
+  const long long hi = range_lo(c + 1, a);
+  long long pos = range_lo(c, a);
   Segment sg;
   bool over;
   while (next_segment(a, pos, hi, sg, over)) {
@@ -678,8 +800,8 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
   const float cs_code = a.scale_log2 * exp2f(static_cast<float>(24 - kFold));
   int buf = 0;                                  // ring position and phase of the next stage use
   uint32_t phase = 0;
-  const long long hi = range_lo(c + 1, a.total, a.n_stream);
-  long long pos = range_lo(c, a.total, a.n_stream);
+  const long long hi = range_lo(c + 1, a);
+  long long pos = range_lo(c, a);
   Segment sg;
   bool over;
   while (next_segment(a, pos, hi, sg, over)) {
@@ -737,114 +859,15 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
   }
 }
 
-// ------------------------------------------------------------------ tail CTA
-// bf16 tail tokens 0 .. tail_len + step - 1 and the current token of slice bh.
-template <int D, int BITS, int G>
-__device__ void tail_cta(const DraftArgs& a, uint8_t* smem, int bh) {
-  using P = Plan<D, BITS, G>;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* q_s = reinterpret_cast<float*>(smem + P::off_q);
-  unsigned int* flag = reinterpret_cast<unsigned int*>(smem + P::off_flag);
-  const int b = bh / a.Hkv, kvh = bh % a.Hkv;
-  int first, last;
-  ctas_of(bh, a, first, last);
-  const int n_c = last - first + 1;
-  const int slot = n_c;                                  // the tail's partial follows the stream CTAs'
-  const int n_tail = a.tail_len[b] + a.step;
-  const bool has_cur = a.k_cur != nullptr;
-  const int n_tok = n_tail + (has_cur ? 1 : 0);
-  const size_t tbase = static_cast<size_t>(bh) * a.tail_cap * D;
-  const bool bad = n_tail < 0 || n_tail > a.tail_cap || (has_cur && n_tail >= a.tail_cap);
-  if (bad && threadIdx.x == 0) atomicOr(&g_draft_status, VC_DEV_CAPACITY);
-  if (bad || n_tok == 0) {
-    for (int h = threadIdx.x; h < G; h += blockDim.x)
-      a.part_lse[static_cast<size_t>(b * a.Hq + kvh * G + h) * a.max_parts + slot] = -INFINITY;
-    arrive_and_combine<G, D>(a, flag, bh, n_c + 1, blockDim.x);
-    return;
-  }
-  uint16_t* krow = reinterpret_cast<uint16_t*>(smem);                      // [n_tok][D]
-  uint16_t* vrow = krow + static_cast<size_t>(a.tail_cap + 1) * D;
-  float* sc = reinterpret_cast<float*>(vrow + static_cast<size_t>(a.tail_cap + 1) * D);   // [G][n_tok]
-  float* ml = reinterpret_cast<float*>(smem + P::off_wstat);               // [G][2]
-  constexpr int VEC = D / 8;
-  for (int i = threadIdx.x; i < n_tok * VEC; i += blockDim.x) {
-    const int t = i / VEC, v = i % VEC;
-    const uint16_t* ks = (t < n_tail) ? a.tail_k + tbase + static_cast<size_t>(t) * D : a.k_cur + static_cast<size_t>(bh) * D;
-    const uint16_t* vs = (t < n_tail) ? a.tail_v + tbase + static_cast<size_t>(t) * D : a.v_cur + static_cast<size_t>(bh) * D;
-    *reinterpret_cast<uint4*>(krow + t * D + v * 8) = *reinterpret_cast<const uint4*>(ks + v * 8);
-    *reinterpret_cast<uint4*>(vrow + t * D + v * 8) = *reinterpret_cast<const uint4*>(vs + v * 8);
-  }
-  load_q<D, G>(a, b, kvh, q_s);
-  __syncthreads();
-  // scores: warp per token, lanes over channel pairs
-  const int nw = blockDim.x / 32;
-  for (int t = warp; t < n_tok; t += nw) {
-    float part[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) part[h] = 0.0f;
-    for (int c = 2 * lane; c < D; c += 64) {
-      const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(krow + t * D + c));
-#pragma unroll
-      for (int h = 0; h < G; ++h) part[h] = fmaf(q_s[h * D + c], kv.x, fmaf(q_s[h * D + c + 1], kv.y, part[h]));
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) part[h] += __shfl_xor_sync(0xffffffffu, part[h], off);
-      if (lane == 0) sc[h * n_tok + t] = part[h];
-    }
-  }
-  __syncthreads();
-  for (int h = warp; h < G; h += nw) {
-    float mx = -INFINITY;
-    for (int t = lane; t < n_tok; t += 32) mx = fmaxf(mx, sc[h * n_tok + t]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float sum = 0.0f;
-    for (int t = lane; t < n_tok; t += 32) {
-      const float p = exp2f(sc[h * n_tok + t] - mx);
-      sc[h * n_tok + t] = p;
-      sum += p;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    if (lane == 0) { ml[2 * h] = mx; ml[2 * h + 1] = sum; }
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < G * D / 2; i += blockDim.x) {
-    const int h = i / (D / 2), c = 2 * (i % (D / 2));
-    float ox = 0.0f, oy = 0.0f;
-    for (int t = 0; t < n_tok; ++t) {
-      const float p = sc[h * n_tok + t];
-      const float2 vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vrow + t * D + c));
-      ox = fmaf(p, vv.x, ox);
-      oy = fmaf(p, vv.y, oy);
-    }
-    const size_t row = static_cast<size_t>(b * a.Hq + kvh * G + h) * a.max_parts + slot;
-    const float inv = 1.0f / ml[2 * h + 1];
-    a.part_o[row * D + c] = ox * inv;
-    a.part_o[row * D + c + 1] = oy * inv;
-    if (c == 0) a.part_lse[row] = ml[2 * h] + log2f(ml[2 * h + 1]);
-  }
-  if (has_cur) {                                   // keep the current token for the next steps
-    for (int i = threadIdx.x; i < VEC; i += blockDim.x) {
-      *reinterpret_cast<uint4*>(a.tail_k + tbase + static_cast<size_t>(n_tail) * D + i * 8) =
-          *reinterpret_cast<const uint4*>(krow + n_tail * D + i * 8);
-      *reinterpret_cast<uint4*>(a.tail_v + tbase + static_cast<size_t>(n_tail) * D + i * 8) =
-          *reinterpret_cast<const uint4*>(vrow + n_tail * D + i * 8);
-    }
-  }
-  arrive_and_combine<G, D>(a, flag, bh, n_c + 1, blockDim.x);
-}
-
 template <int D, int BITS, int G, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB) draft_kernel(DraftArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
-  const int nbh = a.B * a.Hkv;
-  if (static_cast<int>(blockIdx.x) < nbh)
-    tail_cta<D, BITS, G>(a, smem, blockIdx.x);
-  else
-    stream_cta<D, BITS, G>(a, smem, blockIdx.x - nbh);
+  const int c = blockIdx.x;
+  if (c < a.n_stream) {
+    stream_cta<D, BITS, G>(a, smem, c);
+  } else if ((threadIdx.x >> 5) < kWarps) {     // tail CTA: its consumer warps take slices t, t + n_tail_cta, ...
+    for (int bh = c - a.n_stream; bh < a.B * a.Hkv; bh += a.n_cta - a.n_stream) tail_part<D, BITS, G>(a, smem, bh);
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -867,7 +890,7 @@ struct MinBlocks {
 };
 
 struct LaunchPlan {
-  int n_stream = 0, max_parts = 1;
+  int n_stream = 0, n_cta = 0, max_parts = 1;
   long long total = 0;
   size_t smem = 0;
 };
@@ -889,8 +912,11 @@ vc_status_t plan_t(const vc_shape_t* s, int max_packed, LaunchPlan* lp) {
   if (n > by_work) n = by_work;
   if (n < 1 && lp->total > 0) n = 1;
   lp->n_stream = static_cast<int>(lp->total > 0 ? n : 0);
+  // tail CTAs follow the stream CTAs: they start as the first stream CTAs finish
+  const long long slices = static_cast<long long>(s->B) * s->Hkv;
+  lp->n_cta = lp->n_stream + static_cast<int>(std::min<long long>(slices, static_cast<long long>(occ) * sms));
   if (lp->n_stream > 0) {
-    const long long per = lp->total / lp->n_stream;               // >= 1 group per CTA
+    const long long per = lp->total / lp->n_stream;               // >= kWarps groups per CTA
     lp->max_parts = static_cast<int>((NGmax + per - 1) / per + 1) + 1;
   } else {
     lp->max_parts = 1;
@@ -919,9 +945,7 @@ size_t ws_bytes(const vc_shape_t* s, const LaunchPlan& lp) {
 
 template <int D, int BITS, int G>
 vc_status_t launch_t(const DraftArgs& a, const LaunchPlan& lp, cudaStream_t cs) {
-  if (tail_smem<D, G>(a.tail_cap) > Plan<D, BITS, G>::off_q)
-    VC_FAIL(VC_ERR_UNSUPPORTED, "tail_cap %d too large for the shared-memory plan", a.tail_cap);
-  const int grid = a.B * a.Hkv + lp.n_stream;
+  const int grid = lp.n_cta;
   draft_kernel<D, BITS, G, MinBlocks<G>::value><<<grid, kThreads, lp.smem, cs>>>(a);
   VC_LAUNCH_CHECK("draft_kernel");
   return VC_OK;
@@ -983,6 +1007,7 @@ extern "C" vc_status_t vc_draft_attn(const vc_shape_t* s, const uint16_t* q, con
   a.NG = T_cap / kGroup;
   a.NGmax = max_packed / kGroup;
   a.n_stream = lp.n_stream;
+  a.n_cta = lp.n_cta;
   a.total = lp.total;
   a.max_parts = lp.max_parts;
   a.scale_log2 = s->softmax_scale * kLog2e;
