@@ -718,10 +718,13 @@ def run_ours(args, rank, world, local_rank):
         dict(full_kv_resident, speedup_of_value=value_local / full_kv_resident["value"]),
         "clocks": clk,
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(args.workload, w)
     for gg in groups:
         gg.close()
+    if rank == 0 and world == 1 and not args.no_adaptive:
+        why = adaptive_skip_reason(w)
+        out["adaptive"] = {"skipped": why} if why else adaptive_compare(args, device, w, 4)
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.workload, w)
     return out
 
 
@@ -977,27 +980,35 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------- distributed plumbing
-def run_adaptive(args, local_rank):
+ADAPTIVE_BLOCK = 10          # rounds per block; the fixed and the controller arm alternate blocks
+STALL_FRAC = 0.8             # a round whose copy ran below this share of the measured link stalled
+
+
+def adaptive_skip_reason(w):
+    if w.groups != 1:
+        return "two request groups (staggered): the controller plans one group's rounds"
+    if w.keep_frac < 1.0:
+        return "token dropping: the packed prefix is not the full prefix the controller's cost model assumes"
+    return None
+
+
+def adaptive_compare(args, device, w, n_blocks):
     """Fixed draft length (the workload's k) against a per-round draft length
     chosen by the controller from the previous rounds' measured spans, on one
     group whose buffers hold up to --k-max draft tokens.  Same process, same
-    prefix, alternating blocks of rounds."""
+    prefix and seeds, alternating blocks of ADAPTIVE_BLOCK rounds (n_blocks,
+    even, fixed first)."""
     import dataclasses
+    import statistics
 
     import torch
 
-    import synth
     from verify_compressed_kv_gb300 import runtime as rt
     from verify_compressed_kv_gb300.schedule import DraftLengthController
 
-    torch.cuda.set_device(local_rank)
-    device = torch.device("cuda", local_rank)
-    w = workload_of(args)
-    if w.groups != 1 or w.keep_frac < 1.0:
-        raise SystemExit("--adaptive runs the single-group workloads without token dropping")
     k_max = max(args.k_max, w.k)
     choices = sorted({w.k, k_max} | {c for c in range(4, k_max + 1, 4)})
-    rounds_total = args.warmup + 2 * args.steps + 4
+    rounds_total = args.warmup + n_blocks * ADAPTIVE_BLOCK + 4
     g = build_group(dataclasses.replace(w, k=k_max), w.layers, device, rounds_total, args.slots or None)
     n_inp = 3
     host_in = {k: [make_round_inputs(dataclasses.replace(w, k=k), r, 0, device, w.layers) for r in range(n_inp)]
@@ -1059,45 +1070,65 @@ def run_adaptive(args, local_rank):
         t_verify = (k + 1) * row_chunk_ms * g.chunks() * g.L
         ctl.observe(g.n_acc_host.numpy(), k, t_step=d_ms / k, t_copy=t_copy, t_tail=t_tail, t_verify=t_verify)
         ctl.t_verify = {kk: v * g.chunks() * g.L for kk, v in chunk_of_k.items()}
-        return toks, r_ms
+        c_ms = tl.ms("copy_start", "copy_end")
+        return toks, r_ms, (h2d_bytes / c_ms / 1e6 if c_ms > 0 else None)
 
     for r in range(args.warmup):
         one(w.k, r)
     res = {"fixed": [0, 0.0], "adaptive": [0, 0.0]}
     per_round = {"fixed": [], "adaptive": []}            # (tokens, ms) of every round
+    stalled = {"fixed": 0, "adaptive": 0}
     chosen = {}
     r = args.warmup
-    for blk in range(2 * args.steps // 10):                 # blocks of 10 rounds, alternating
+    for blk in range(n_blocks):
         mode = "fixed" if blk % 2 == 0 else "adaptive"
-        for _ in range(10):
+        for _ in range(ADAPTIVE_BLOCK):
             k = w.k if mode == "fixed" else ctl.next_k()
             if mode == "adaptive":
                 chosen[k] = chosen.get(k, 0) + 1
-            toks, ms = one(k, r)
+            toks, ms, copy_gbs = one(k, r)
             res[mode][0] += toks * w.layers
             res[mode][1] += ms
             per_round[mode].append((toks * w.layers, ms))
+            stalled[mode] += int(copy_gbs is not None and copy_gbs < STALL_FRAC * link_gbs)
             r += 1
     g.close()
     val = {m: v[0] / (v[1] / 1e3) for m, v in res.items()}
     # the same with each mode's median round time (insensitive to the host link's
     # occasional stalls, which land in either mode's blocks at random)
-    import statistics
     val_med = {m: statistics.mean(t for t, _ in v) / (statistics.median(ms for _, ms in v) / 1e3)
                for m, v in per_round.items() if v}
-    return {"metric": "verified tokens/s/layer", "value": val["adaptive"], "unit": "tokens/s/layer",
-            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
-            "dtype": "bf16/int%d->f32" % w.bits, "data": "synthetic (seeded)",
-            "config": {"workload": workload_name(w), "schedule": "adaptive draft length", "k_fixed": w.k,
-                       "k_max": k_max, "choices": choices},
-            "fixed_k_value": val["fixed"], "adaptive_over_fixed": val["adaptive"] / val["fixed"],
+    return {"fixed_k": w.k, "k_max": k_max, "choices": choices,
+            "rounds_per_arm": {m: len(v) for m, v in per_round.items()}, "block_rounds": ADAPTIVE_BLOCK,
+            "fixed_value": val["fixed"], "adaptive_value": val["adaptive"],
+            "adaptive_over_fixed": val["adaptive"] / val["fixed"],
             "at_median_round": {"fixed": val_med.get("fixed"), "adaptive": val_med.get("adaptive"),
                                 "adaptive_over_fixed": (val_med["adaptive"] / val_med["fixed"])
                                 if "fixed" in val_med and "adaptive" in val_med else None},
+            "stalled_rounds": stalled, "stall_rule": "copy below %.0f%% of the measured link" % (100 * STALL_FRAC),
             "k_chosen": chosen, "acceptance_estimate": ctl.acceptance(),
             "measured": {"t_step_ms": ctl.t_step, "t_copy_ms": ctl.t_copy, "t_tail_ms": ctl.t_tail,
                          "t_verify_row_ms": ctl.t_row, "link_peak_gbs": link_gbs,
                          "copy_gbs": rate["bytes_per_ms"] / 1e6, "verify_row_chunk_ms": row_chunk_ms}}
+
+
+def run_adaptive(args, local_rank):
+    """--adaptive: the fixed and the controller arm as the headline of the line."""
+    import torch
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    w = workload_of(args)
+    why = adaptive_skip_reason(w)
+    if why:
+        raise SystemExit("--adaptive: " + why)
+    cmp_ = adaptive_compare(args, device, w, max(2, 2 * args.steps // ADAPTIVE_BLOCK))
+    return {"metric": "verified tokens/s/layer", "value": cmp_["adaptive_value"], "unit": "tokens/s/layer",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "bf16/int%d->f32" % w.bits, "data": "synthetic (seeded)",
+            "config": {"workload": workload_name(w), "schedule": "adaptive draft length", "k_fixed": w.k,
+                       "k_max": cmp_["k_max"], "choices": cmp_["choices"]},
+            "adaptive": cmp_}
 
 
 def run_remote(args, local_rank):
@@ -1217,6 +1248,8 @@ def main(argv=None):
     ap.add_argument("--link-peak-gbs", type=float, default=0.0,
                     help="pinned host->device peak in GB/s (default 0: measure it at start-up)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-adaptive", action="store_true",
+                    help="leave out the fixed-k vs controller comparison of the default line")
     ap.add_argument("--adaptive", action="store_true",
                     help="compare the fixed draft length with a per-round length chosen by the controller")
     ap.add_argument("--bits", type=int, default=0, choices=[0, 2, 4, 8],
