@@ -25,6 +25,7 @@
 // rule, so any number of chunks needs only `parts` states.  The finish kernel
 // (mma.sync m16n8k16: a few rows of new tokens) adds the causal block of the
 // k+1 new tokens and merges everything into bf16 output.
+#include <algorithm>
 #include <cfloat>
 #include <cstdlib>
 #include <string>
@@ -366,8 +367,8 @@ struct TcPlan {
   static constexpr uint32_t stage = 2 * kv_bytes;
   static constexpr uint32_t off_st = q_bytes;
   static constexpr uint32_t off_bar = off_st + kTcStages * stage;
-  // full[S], empty[S], q_ready, s_full[2], p_ready[2], o_done[2], done
-  static constexpr int n_bars = 2 * kTcStages + 8;
+  // full_k[S], full_v[S], empty_k[S], empty_v[S], q_ready, s_full[2], p_ready[2], o_done[2], done
+  static constexpr int n_bars = 4 * kTcStages + 8;
   static constexpr uint32_t off_misc = off_bar + n_bars * 8;   // TMEM base, abort flag
   static constexpr uint32_t total = off_misc + 16 + 1024;      // + room to align the base to 1024
   static constexpr uint32_t col_s = 0, col_o = 2 * kTcTok;    // TMEM: S[2] (P written over S), O
@@ -388,9 +389,11 @@ __global__ void __launch_bounds__(kTcThreads) verify_chunk_tc(VerifyArgs a, cons
   if (n_tiles == 0 && !a.first) return;                      // nothing to merge (uniform over the CTA)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P::off_bar);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + kTcStages;
-  uint64_t* q_ready = bars + 2 * kTcStages;
+  uint64_t* full_k = bars;
+  uint64_t* full_v = bars + kTcStages;
+  uint64_t* empty_k = bars + 2 * kTcStages;
+  uint64_t* empty_v = bars + 3 * kTcStages;
+  uint64_t* q_ready = bars + 4 * kTcStages;
   uint64_t* s_full = q_ready + 1;
   uint64_t* p_ready = s_full + 2;
   uint64_t* o_done = p_ready + 2;
@@ -399,10 +402,7 @@ __global__ void __launch_bounds__(kTcThreads) verify_chunk_tc(VerifyArgs a, cons
   volatile uint32_t* abort = misc + 1;
   if (warp == 0) vc_tc_alloc(misc, P::alloc);
   if (threadIdx.x == 32) {
-    for (int i = 0; i < kTcStages; ++i) {
-      vc_mbar_init(full + i, 1);
-      vc_mbar_init(empty + i, 1);
-    }
+    for (int i = 0; i < 4 * kTcStages; ++i) vc_mbar_init(bars + i, 1);
     vc_mbar_init(q_ready, 4);
     for (int i = 0; i < 2; ++i) {
       vc_mbar_init(s_full + i, 1);
@@ -551,27 +551,51 @@ __global__ void __launch_bounds__(kTcThreads) verify_chunk_tc(VerifyArgs a, cons
       if (rv) *sml = make_float2(mo, lo);
     }
   } else if (warp == 4) {
-    // ---------------- K / V tiles by TMA
+    // ---------------- K / V tiles by TMA, each ring refilled as soon as its own
+    // consumer (S = Q.K^T for K, O += P.V for V) has completed on that stage
     if (lane == 0 && n_tiles > 0) {
       const int krow0 = (b * a.Hkv + kvh) * a.C;
       const int vrow0 = a.B * a.Hkv * a.C + krow0;
-      int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int s = i % kTcStages;
-        if (i >= kTcStages && !wait(empty + s, static_cast<uint32_t>(((i / kTcStages) - 1) & 1))) break;
-        uint8_t* st = smem + P::off_st + s * P::stage;
-        const int t0 = t_lo + i * kTcTok;
-        vc_mbar_arrive_expect_tx(full + s, P::stage);
+      int ik = 0, iv = 0;                                    // next K / V tile to issue
+      long long t_last = clock64();
+      while (ik < n_tiles || iv < n_tiles) {
+        bool moved = false;
+        if (ik < n_tiles && (ik < kTcStages ||
+                             vc_mbar_try_wait(empty_k + ik % kTcStages, static_cast<uint32_t>(((ik / kTcStages) - 1) & 1)))) {
+          uint8_t* st = smem + P::off_st + (ik % kTcStages) * P::stage;
+          vc_mbar_arrive_expect_tx(full_k + ik % kTcStages, P::kv_bytes);
 #pragma unroll
-        for (int h = 0; h < P::H; ++h) {
-          vc_tma2(st + h * (kTcTok * 128), &tkv, 64 * h, krow0 + t0, full + s);
-          vc_tma2(st + P::kv_bytes + h * (kTcTok * 128), &tkv, 64 * h, vrow0 + t0, full + s);
+          for (int h = 0; h < P::H; ++h)
+            vc_tma2(st + h * (kTcTok * 128), &tkv, 64 * h, krow0 + t_lo + ik * kTcTok, full_k + ik % kTcStages);
+          ++ik;
+          moved = true;
         }
-        ++issued;
+        if (iv < n_tiles && (iv < kTcStages ||
+                             vc_mbar_try_wait(empty_v + iv % kTcStages, static_cast<uint32_t>(((iv / kTcStages) - 1) & 1)))) {
+          uint8_t* st = smem + P::off_st + (iv % kTcStages) * P::stage + P::kv_bytes;
+          vc_mbar_arrive_expect_tx(full_v + iv % kTcStages, P::kv_bytes);
+#pragma unroll
+          for (int h = 0; h < P::H; ++h)
+            vc_tma2(st + h * (kTcTok * 128), &tkv, 64 * h, vrow0 + t_lo + iv * kTcTok, full_v + iv % kTcStages);
+          ++iv;
+          moved = true;
+        }
+        if (moved) {
+          t_last = clock64();
+        } else {
+          if (*abort != 0u) break;
+          if (clock64() - t_last > kTcWait) {
+            *abort = 1u;
+            break;
+          }
+          __nanosleep(64);
+        }
       }
       // every tile issued has landed before the CTA may exit
-      for (int i = issued - kTcStages < 0 ? 0 : issued - kTcStages; i < issued; ++i)
-        vc_mbar_wait_bounded(full + i % kTcStages, static_cast<uint32_t>((i / kTcStages) & 1), kTcWait);
+      for (int i = ik - kTcStages < 0 ? 0 : ik - kTcStages; i < ik; ++i)
+        vc_mbar_wait_bounded(full_k + i % kTcStages, static_cast<uint32_t>((i / kTcStages) & 1), kTcWait);
+      for (int i = iv - kTcStages < 0 ? 0 : iv - kTcStages; i < iv; ++i)
+        vc_mbar_wait_bounded(full_v + i % kTcStages, static_cast<uint32_t>((i / kTcStages) & 1), kTcWait);
     }
   } else {
     // ---------------- products (one thread)
@@ -583,6 +607,7 @@ __global__ void __launch_bounds__(kTcThreads) verify_chunk_tc(VerifyArgs a, cons
       auto pv = [&](int t) {
         const int s = t % kTcStages, bb = t & 1;
         if (!wait(p_ready + bb, static_cast<uint32_t>((t >> 1) & 1))) return false;
+        if (!wait(full_v + s, static_cast<uint32_t>((t / kTcStages) & 1))) return false;
         vc_tc_fence_after();
         const uint32_t v_addr = st_addr + s * P::stage + P::kv_bytes;
 #pragma unroll
@@ -590,12 +615,12 @@ __global__ void __launch_bounds__(kTcThreads) verify_chunk_tc(VerifyArgs a, cons
           vc_tc_mma_ta(tmem + P::col_o, tmem + P::col_s + bb * kTcTok + ks * 8,
                        vc_tc_desc(v_addr + ks * 2048, kTcTok * 128, 1024) | (2ull << 61), id_pv, t > 0 || ks > 0);
         vc_tc_commit(o_done + bb);
-        vc_tc_commit(empty + s);
+        vc_tc_commit(empty_v + s);
         return true;
       };
       for (int i = 0; ok && i < n_tiles; ++i) {
         const int s = i % kTcStages, bb = i & 1;
-        if (!wait(full + s, static_cast<uint32_t>((i / kTcStages) & 1))) {
+        if (!wait(full_k + s, static_cast<uint32_t>((i / kTcStages) & 1))) {
           ok = false;
           break;
         }
@@ -607,6 +632,7 @@ __global__ void __launch_bounds__(kTcThreads) verify_chunk_tc(VerifyArgs a, cons
                     vc_tc_desc_sw128(q_addr + (ks / 4) * (kTcRows * 128) + (ks % 4) * 32),
                     vc_tc_desc_sw128(k_addr + (ks / 4) * (kTcTok * 128) + (ks % 4) * 32), id_qk, ks > 0);
         vc_tc_commit(s_full + bb);
+        vc_tc_commit(empty_k + s);                            // the K stage is free once S is computed
         if (i > 0) ok = pv(i - 1);
       }
       if (ok) ok = pv(n_tiles - 1);
@@ -826,34 +852,36 @@ extern "C" vc_status_t vc_verify_attn_workspace_size(const vc_shape_t* s, int32_
   return VC_OK;
 }
 
-// Parts per chunk for a chunk launch: the CTAs that fit at once (occupancy of
-// the chunk kernel x SMs) run in waves, and each CTA walks ceil(tiles / parts)
-// 64-token tiles and then merges its state (about one tile's worth of traffic);
-// pick the parts with the least waves x (tiles per part + 1), fewest on ties.
+// Parts per chunk for a chunk launch: the most that keep all B * Hkv * row
+// blocks * parts CTAs in one wave of the CTAs that fit at once (per SM from
+// the kernel's registers, shared memory and TMEM columns, x SMs).  Each CTA
+// walks ceil(tiles / parts) 64-token tiles and then merges its state.
 namespace {
 template <int D>
 vc_status_t plan_parts(const vc_shape_t* s, int C, int* parts) {
   vc_status_t st = tc_setup<D>();
   if (st != VC_OK) return st;
-  int per_sm = 0, dev = 0, sms = 0;
-  VC_CUDA_CHECK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_chunk_tc<D>, kTcThreads,
-                                                              TcPlan<D>::total));
+  // CTAs resident per SM from the kernel's own limits: registers, shared memory
+  // and TMEM columns (512 per SM)
+  int dev = 0, sms = 0, smem_sm = 0, smem_rsv = 0;
   VC_CUDA_CHECK(cudaGetDevice(&dev));
   VC_CUDA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  const int64_t slots = static_cast<int64_t>(per_sm > 0 ? per_sm : 1) * sms;
+  VC_CUDA_CHECK(cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev));
+  VC_CUDA_CHECK(cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev));
+  cudaFuncAttributes fa{};
+  VC_CUDA_CHECK(cudaFuncGetAttributes(&fa, verify_chunk_tc<D>));
+  const int by_regs = 65536 / (((fa.numRegs + 7) / 8) * 8 * kTcThreads);
+  const int by_smem = smem_sm / (static_cast<int>(TcPlan<D>::total) + smem_rsv);
+  const int by_tmem = 512 / static_cast<int>(TcPlan<D>::alloc);
+  const int per_sm = std::max(1, std::min(by_regs, std::min(by_smem, by_tmem)));
+  const int64_t slots = static_cast<int64_t>(per_sm) * sms;
   const int64_t units = static_cast<int64_t>(s->B) * s->Hkv * tc_row_blocks(s);
   const int tiles = (C + kTcTok - 1) / kTcTok;
-  int best = 1;
-  int64_t best_cost = INT64_MAX;
-  for (int p = 1; p <= kMaxPlannedParts && p <= tiles; ++p) {
-    const int64_t waves = (units * p + slots - 1) / slots;
-    const int64_t cost = waves * ((tiles + p - 1) / p + 1);
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = p;
-    }
-  }
-  *parts = best;
+  // as many parts as keep every CTA in one wave: a second wave (or a CTA that
+  // waits for a slot) costs more than the longer tile loop of fewer parts
+  int64_t best = slots / std::max<int64_t>(1, units);
+  best = std::max<int64_t>(1, std::min<int64_t>(best, std::min(tiles, kMaxPlannedParts)));
+  *parts = static_cast<int>(best);
   return VC_OK;
 }
 }  // namespace
