@@ -243,6 +243,19 @@ vc_status_t vc_draft_attn(const vc_shape_t* s, const uint16_t* q, const uint16_t
                           void* workspace, size_t workspace_bytes, vc_stream_t stream);
 /* Device status (barrier time-outs) since the last call; synchronises. */
 vc_status_t vc_draft_attn_device_status(uint32_t* status);
+/* Test hooks, for the failure-detection test only (host-side settings of this
+ * library, not thread-safe, apply to later vc_draft_attn calls):
+ *   wait_cycles           bound of every mbarrier wait of the draft kernel in
+ *                         SM clock cycles; 0 restores the default (about 2 s),
+ *                         otherwise >= 1000;
+ *   withhold_first_stage  1: each stream CTA's producer issues no copy for its
+ *                         first ring stage, so that stage's consumers' waits
+ *                         run out; 0: normal.
+ * A call that ran out raises the barrier time-out bit of
+ * vc_draft_attn_device_status, leaves its output undefined and its workspace
+ * dirty: zero the workspace before reusing it.  No wait is unbounded and no
+ * fault is raised. */
+vc_status_t vc_draft_attn_test_hooks(int64_t wait_cycles, int32_t withhold_first_stage);
 
 /* ----------------------------------------------------- libvc_verify_attn
  * Verify attention (VeriCache, Core Algorithm, Verification: one forward

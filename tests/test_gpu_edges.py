@@ -71,6 +71,55 @@ def test_draft_with_an_empty_request_and_repeat_calls(vc):
     assert vc.vc_draft_attn_device_status() == 0
 
 
+def test_draft_wait_bound_runs_out_and_is_reported(vc):
+    """Failure detection without a fault: with a short wait bound and the first
+    ring stage withheld, the consumers' bounded waits run out, the call returns,
+    the device status reports the barrier time-out, and the context stays usable
+    (the next call, on a zeroed workspace, matches the oracle)."""
+    w = synth.get("mistral", B=3, T=1024)
+    K, V = synth.kv(w)
+    s = vc.shape(w.B, w.Hq, w.Hkv, w.d, bits=w.bits, softmax_scale=1 / math.sqrt(w.d))
+    arrs = _pack(vc, s, K, V, 1024)
+    tail_cap = 32 + w.k + 1
+    tk = np.zeros((w.B, w.Hkv, tail_cap, w.d), np.uint16)
+    plen, tlen = [1024, 1024, 1024], [0, 0, 0]
+    wsb = vc.vc_draft_attn_workspace_size(s, 1024)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    q = synth.draft_q(w, 0, 0)
+    kc_, vc_ = synth.draft_kv_cur(w, 0, 0)
+    assert vc.vc_draft_attn_device_status() == 0
+
+    def call():
+        out = torch.empty((w.B, w.Hq, w.d), dtype=torch.int16, device="cuda")
+        vc.vc_draft_attn(s, _t(q), _t(kc_), _t(vc_), *arrs, _t(np.array(plen, np.int32)), 1024, 1024, _t(tk), _t(tk),
+                         _t(np.array(tlen, np.int32)), tail_cap, 0, out, ws, wsb)
+        torch.cuda.synchronize()
+        return out
+
+    try:
+        vc.vc_draft_attn_test_hooks(2_000_000, 1)          # ~1 ms per wait, first stage withheld
+        call()
+        status = vc.vc_draft_attn_device_status()
+    finally:
+        vc.vc_draft_attn_test_hooks(0, 0)
+    assert status & 1, f"barrier time-out not reported (status {status})"
+    ws.zero_()                                               # the timed-out call left its counters
+    out = call()
+    want = oatt.draft_attention(q, *kivi.quant_pack(K, V, w.bits), plen, tk, tk, tlen, w.bits, 1 / math.sqrt(w.d),
+                                k_cur=kc_, v_cur=vc_)
+    err = np.abs(_f64(out) - want)
+    assert err.max() <= 2e-2 and err.mean() <= 2e-3
+    assert vc.vc_draft_attn_device_status() == 0
+
+
+def test_draft_test_hooks_reject_bad_arguments(vc):
+    with pytest.raises(vc.VcError):
+        vc.vc_draft_attn_test_hooks(10, 0)
+    with pytest.raises(vc.VcError):
+        vc.vc_draft_attn_test_hooks(0, 2)
+    vc.vc_draft_attn_test_hooks(0, 0)
+
+
 def test_draft_single_group_and_no_current_token(vc):
     w = synth.get("qwen", B=1, T=32, keep_frac=1.0)
     K, V = synth.kv(w)

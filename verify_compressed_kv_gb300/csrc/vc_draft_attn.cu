@@ -52,7 +52,11 @@ constexpr int kConsumers = kWarps * 32;
 constexpr int kThreads = kConsumers + 32;        // + one producer warp
 constexpr int kGroup = 32;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz
+constexpr long long kWaitCycles = 4000000000LL;   // default wait bound: ~2 s at 2 GHz
+// Test hooks (vc_draft_attn_test_hooks): the wait bound and a withheld first
+// stage, so that a test can make the bounded waits run out.  Host side only.
+long long g_wait_cycles = kWaitCycles;
+int g_withhold_first = 0;
 struct DraftArgs {
   const uint16_t* q;        // [B, Hq, D]
   const uint16_t* k_cur;    // [B, Hkv, D] or null
@@ -74,6 +78,8 @@ struct DraftArgs {
   long long total;          // B * Hkv * NGmax
   int max_parts;            // partial slots per (b, h): stream CTAs + the tail
   float scale_log2;
+  long long wait_cycles;    // bound of every mbarrier wait (clock64 cycles)
+  int withhold_first;       // test only: the producers issue nothing for their first stage
   float* part_o;            // [B*Hq, max_parts, D]   normalised partial outputs
   float* part_lse;          // [B*Hq, max_parts]      log2-sum-exp of each partial
   unsigned int* counter;    // [B*Hkv] arrivals (zero between calls)
@@ -740,7 +746,9 @@ __device__ __forceinline__ bool next_segment(const DraftArgs& a, long long& pos,
 }
 
 // Producer warp (lane 0): fills the ring stage by stage, across segments,
-// each stage once all consumer warps released its previous use.
+// each stage once all consumer warps released its previous use.  It stops
+// issuing once the CTA's abort flag is up, and before returning waits (bounded)
+// for the copies of its last stages, so that no copy lands after the CTA ends.
 template <int D, int BITS, int G>
 __device__ void produce(const DraftArgs& a, uint8_t* smem, int c, uint64_t* full, uint64_t* empty,
                         volatile uint32_t* abort) {
@@ -748,16 +756,29 @@ __device__ void produce(const DraftArgs& a, uint8_t* smem, int c, uint64_t* full
   int buf = 0;                                  // ring position of the next stage use
   uint32_t phase = 0;                           // completed wraps of the ring, mod 2
   bool wrapped = false;                         // every buffer used at least once
+  uint32_t in_flight = 0;                       // bit i: buffer i holds an issued copy not yet drained
+  uint32_t in_phase = 0;                        // bit i: its phase
   const long long hi = range_lo(c + 1, a);
   long long pos = range_lo(c, a);
   Segment sg;
   bool over;
-  while (next_segment(a, pos, hi, sg, over)) {
+  bool stop = false;
+  while (!stop && next_segment(a, pos, hi, sg, over)) {
     for (int s = 0; s < sg.n_st; ++s) {
       // the previous use of `buf` (one wrap earlier) must have been released
-      if (wrapped && !vc_mbar_wait_or_abort(empty + buf, phase ^ 1u, abort, kWaitCycles)) return;
-      issue_stage<D, BITS, G>(a, smem + buf * P::stage, full + buf, sg.bh, sg.gs + s * kWarps,
-                              min(kWarps, sg.n_valid - s * kWarps));
+      if ((wrapped && !vc_mbar_wait_or_abort(empty + buf, phase ^ 1u, abort, a.wait_cycles)) || *abort != 0u) {
+        stop = true;
+        break;
+      }
+      // (test only) the first stage withheld: its consumers' waits run out
+      if (!(a.withhold_first && !wrapped && buf == 0)) {
+        issue_stage<D, BITS, G>(a, smem + buf * P::stage, full + buf, sg.bh, sg.gs + s * kWarps,
+                                min(kWarps, sg.n_valid - s * kWarps));
+        in_flight |= 1u << buf;
+        in_phase = (in_phase & ~(1u << buf)) | (phase << buf);
+      } else {
+        in_flight &= ~(1u << buf);
+      }
       if (++buf == P::NS) {
         buf = 0;
         phase ^= 1u;
@@ -765,6 +786,9 @@ __device__ void produce(const DraftArgs& a, uint8_t* smem, int c, uint64_t* full
       }
     }
   }
+  // the copies of the last use of every buffer have landed (consumed ones return at once)
+  for (int i = 0; i < P::NS; ++i)
+    if (in_flight & (1u << i)) vc_mbar_wait_bounded(full + i, (in_phase >> i) & 1u, a.wait_cycles);
 }
 
 template <int D, int BITS, int G>
@@ -831,7 +855,7 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
     WarpState<D> st;
     init_state(st);
     for (int s = 0; s < sg.n_st; ++s) {
-      const bool ok = __all_sync(0xffffffffu, vc_mbar_wait_or_abort(full + buf, phase, abort, kWaitCycles));
+      const bool ok = __all_sync(0xffffffffu, vc_mbar_wait_or_abort(full + buf, phase, abort, a.wait_cycles));
       if (ok && s * kWarps + warp < sg.n_valid) {
         const uint8_t* base = smem + buf * P::stage;
         const uint32_t* kc_g = reinterpret_cast<const uint32_t*>(base + warp * P::codes);
@@ -1011,6 +1035,8 @@ extern "C" vc_status_t vc_draft_attn(const vc_shape_t* s, const uint16_t* q, con
   a.total = lp.total;
   a.max_parts = lp.max_parts;
   a.scale_log2 = s->softmax_scale * kLog2e;
+  a.wait_cycles = g_wait_cycles;
+  a.withhold_first = g_withhold_first;
   const size_t rows = static_cast<size_t>(s->B) * s->Hq * lp.max_parts;
   char* ws = static_cast<char*>(workspace);
   a.part_o = reinterpret_cast<float*>(ws);
@@ -1020,6 +1046,14 @@ extern "C" vc_status_t vc_draft_attn(const vc_shape_t* s, const uint16_t* q, con
   a.counter = reinterpret_cast<unsigned int*>(ws + off);
   a.out = out;
   return launch(s, a, lp, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" vc_status_t vc_draft_attn_test_hooks(int64_t wait_cycles, int32_t withhold_first_stage) {
+  VC_REQUIRE(wait_cycles == 0 || wait_cycles >= 1000, "wait_cycles must be 0 (default) or >= 1000");
+  VC_REQUIRE(withhold_first_stage == 0 || withhold_first_stage == 1, "withhold_first_stage must be 0 or 1");
+  g_wait_cycles = wait_cycles == 0 ? kWaitCycles : wait_cycles;
+  g_withhold_first = withhold_first_stage;
+  return VC_OK;
 }
 
 extern "C" vc_status_t vc_draft_attn_device_status(uint32_t* status) {
