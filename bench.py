@@ -453,12 +453,13 @@ def run_ours(args, rank, world, local_rank):
     w = workload_of(args)
     layers = w.layers
     n_groups = w.groups
-    rounds_total = args.warmup + args.steps + 1
+    # capacity (full-KV store, rings, draft cache) for every round the run makes: the
+    # warm-up, the timed rounds and the e2e leg's rounds
+    rounds_total = args.warmup + 2 * args.steps + 1
     n_inp = min(3, rounds_total)
     n_slots = args.slots or None
     cs = torch.cuda.Stream(device)
     xs = torch.cuda.Stream(device)
-    ins = torch.cuda.Stream(device)           # the e2e leg's per-round input copies
     groups = [build_group(w, layers, device, rounds_total, n_slots, gi) for gi in range(n_groups)]
     host_inputs = [[make_round_inputs(w, r, gi, device, layers) for r in range(n_inp)] for gi in range(n_groups)]
     dev_inputs = [[to_device(x, device) for x in hi] for hi in host_inputs]
@@ -486,16 +487,14 @@ def run_ours(args, rank, world, local_rank):
         if n_groups == 1:
             g = groups[0]
             inp = with_drafts(dev_inputs[0][r % n_inp], dev_drafts[0][r])
-            ready = None
+            copy_in = None
             if e2e:
-                # the round's inputs come over the link on their own stream; only the
-                # drafting waits for them, not the round's full-KV transfer
-                ins.wait_stream(cs)
-                copy_inputs(e2e_bufs[0], with_drafts(pin_inputs[0][r % n_inp], pin_drafts[0][r]), ins)
-                ready = torch.cuda.Event()
-                ready.record(ins)
+                # the round's inputs come over the link ahead of its full KV (on the copy
+                # stream); only the drafting waits for them
+                src = with_drafts(pin_inputs[0][r % n_inp], pin_drafts[0][r])
+                copy_in = lambda st, src=src: copy_inputs(e2e_bufs[0], src, st)
                 inp = e2e_bufs[0]
-            tl = rt.round_single(g, inp, cs, xs, timeline, ready=ready)
+            tl = rt.round_single(g, inp, cs, xs, timeline, copy_in=copy_in)
             return tl, [g]
         if args.schedule == "lockstep":
             # every group drafts cycle r, then every group verifies it
@@ -521,17 +520,17 @@ def run_ours(args, rank, world, local_rank):
             tl.mark("end", cs)
             return tl, []
         inp_y = with_drafts(dev_inputs[iy][vcyc % n_inp], dev_drafts[iy][vcyc])
-        ready = None
+        copy_in = None
         if e2e:
-            ins.wait_stream(cs)
-            # each group copies what its role in this round reads
-            copy_inputs(e2e_bufs[ix], with_drafts(pin_inputs[ix][dc % n_inp], pin_drafts[ix][dc]), ins, DRAFT_FIELDS)
-            copy_inputs(e2e_bufs[iy], with_drafts(pin_inputs[iy][vcyc % n_inp], pin_drafts[iy][vcyc]), ins,
-                        VERIFY_FIELDS)
-            ready = torch.cuda.Event()
-            ready.record(ins)
+            # each group copies what its role in this round reads, ahead of the full KV
+            sx = with_drafts(pin_inputs[ix][dc % n_inp], pin_drafts[ix][dc])
+            sy = with_drafts(pin_inputs[iy][vcyc % n_inp], pin_drafts[iy][vcyc])
+
+            def copy_in(st, sx=sx, sy=sy, ix=ix, iy=iy):
+                copy_inputs(e2e_bufs[ix], sx, st, DRAFT_FIELDS)
+                copy_inputs(e2e_bufs[iy], sy, st, VERIFY_FIELDS)
             inp_x, inp_y = e2e_bufs[ix], e2e_bufs[iy]
-        tl = rt.round_staggered(X, Y, inp_x, inp_y, cs, xs, timeline, ready=ready)
+        tl = rt.round_staggered(X, Y, inp_x, inp_y, cs, xs, timeline, copy_in=copy_in)
         return tl, [Y]
 
     def finish(tl, done):
@@ -575,6 +574,28 @@ def run_ours(args, rank, world, local_rank):
     total_ms = t_start.elapsed_time(t_end)
     layer_tokens = tokens * layers
     value_local = layer_tokens / (total_ms / 1e3)
+
+    # ---- e2e: the same rounds right after the device-resident ones (same state of the
+    # group and its rings), inputs copied from pinned host memory every round, result read back
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    e2e_tokens = 0
+    e2e_tls = []
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(cs)
+    for _ in range(args.steps):
+        tl, done = one_round(e2e=True)
+        e2e_tokens += finish(tl, done)
+        e2e_tls.append(tl)
+    s1.record(cs)
+    torch.cuda.synchronize()
+    e2e_ms = s0.elapsed_time(s1)
+    e2e_local = e2e_tokens * layers / (e2e_ms / 1e3)
+    if n_groups == 1 or args.schedule == "lockstep":
+        per_round_in = input_bytes(pin_inputs[0][0]) * n_groups
+    else:                                       # staggered: one group's draft inputs, the other's verify inputs
+        per_round_in = input_bytes(pin_inputs[0][0], DRAFT_FIELDS) + input_bytes(pin_inputs[0][0], VERIFY_FIELDS)
+    per_round_out = 4 * w.B
 
     # per-round breakdown from the timelines
     def med(xs_):
@@ -654,25 +675,6 @@ def run_ours(args, rank, world, local_rank):
                "what": "greedy decoding with the full KV streamed host->device every step (same kernels, k = 0)"}
     full_kv_resident = time_full_kv_resident(g, q1, kv1, out1, layers, cs)
 
-    # ---- e2e: same rounds, inputs copied from pinned host memory every round, result read back
-    dist_barrier(world)
-    torch.cuda.synchronize()
-    e2e_tokens = 0
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s0.record(cs)
-    for _ in range(args.steps):
-        tl, done = one_round(e2e=True)
-        e2e_tokens += finish(tl, done)
-    s1.record(cs)
-    torch.cuda.synchronize()
-    e2e_ms = s0.elapsed_time(s1)
-    e2e_local = e2e_tokens * layers / (e2e_ms / 1e3)
-    if n_groups == 1 or args.schedule == "lockstep":
-        per_round_in = input_bytes(pin_inputs[0][0]) * n_groups
-    else:                                       # staggered: one group's draft inputs, the other's verify inputs
-        per_round_in = input_bytes(pin_inputs[0][0], DRAFT_FIELDS) + input_bytes(pin_inputs[0][0], VERIFY_FIELDS)
-    per_round_out = 4 * w.B
-
     # ---- reduce over ranks (replicas): value = sum, time = max
     value, e2e_value, t_max = reduce_over_ranks(value_local, e2e_local, total_ms, world)
 
@@ -695,6 +697,9 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded; shapes and distributions of the workload; no weights)",
         "config": bench_config(w, args, world),
         "e2e": {"value": e2e_value, "unit": "tokens/s/layer", "h2d_bytes_per_step": per_round_in,
+                "round_ms_median": med([tl.ms("start", "end") for tl in e2e_tls]),
+                "copy_ms_median": med([tl.ms("copy_start", "copy_end") for tl in e2e_tls]),
+                "tokens_per_round": e2e_tokens / max(1, args.steps), "tokens_per_round_value": tokens / max(1, args.steps),
                 "d2h_bytes_per_step": per_round_out},
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",

@@ -305,19 +305,23 @@ vc_status_t vc_verify_pipeline_destroy(vc_verify_pipeline_t p);
 /* Host-side prefetch of chunks [0, n_chunks) on the copy stream into ring
  * slots, as far as free slots allow, without the compute side.  Lets a
  * caller start the transfer before the verify queries exist (e.g. while
- * drafting).  Tokens at or beyond max_prefix are not copied. */
+ * drafting).  Tokens at or beyond max_prefix are not copied.  T_cap is the
+ * pinned store's capacity in tokens per request (a multiple of C, the same
+ * value vc_verify_commit takes); max_prefix > T_cap is an argument error, so
+ * no copy reads past the store. */
 vc_status_t vc_verify_prefetch(vc_verify_pipeline_t p, const vc_shape_t* s,
                                const uint16_t* host_kv, int32_t C, int32_t max_prefix,
-                               uint16_t* dev_slots, vc_stream_t copy_stream);
+                               int32_t T_cap, uint16_t* dev_slots, vc_stream_t copy_stream);
 
 /* Whole verify for one layer: streams chunks 0 .. ceil(max_prefix / C) - 1
- * of host_kv (pinned) through the ring dev_slots (device, n_slots slots of
- * 2*B*Hkv*C*d bf16 each) on copy_stream, runs the chunk kernels on
- * compute_stream as chunks land (CUDA events, no host waits), then the new
- * tokens and the combine.  max_prefix (host) bounds prefix_len[b] (device). */
+ * of host_kv (pinned, T_cap / C chunks) through the ring dev_slots (device,
+ * n_slots slots of 2*B*Hkv*C*d bf16 each) on copy_stream, runs the chunk
+ * kernels on compute_stream as chunks land (CUDA events, no host waits), then
+ * the new tokens and the combine.  max_prefix (host) bounds prefix_len[b]
+ * (device) and must not exceed T_cap. */
 vc_status_t vc_verify_attn_streamed(vc_verify_pipeline_t p, const vc_shape_t* s,
                                     const uint16_t* q, const uint16_t* host_kv, int32_t C,
-                                    int32_t max_prefix, const int32_t* prefix_len,
+                                    int32_t max_prefix, int32_t T_cap, const int32_t* prefix_len,
                                     uint16_t* dev_slots, const uint16_t* k_new,
                                     const uint16_t* v_new, uint16_t* out, int32_t parts_per_chunk,
                                     void* workspace, size_t workspace_bytes,

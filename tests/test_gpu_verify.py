@@ -132,8 +132,8 @@ def test_streamed_pipeline_and_commit(vc):
             qd, knd, vnd = dev(q), dev(kn), dev(vn)
             torch.cuda.synchronize()
             max_prefix = int(plen.max())
-            vc.vc_verify_prefetch(pipe, s, st, C, max_prefix, slots, xs)
-            vc.vc_verify_attn_streamed(pipe, s, qd, st, C, max_prefix, pl, slots, knd, vnd, out, parts, ws, wsb,
+            vc.vc_verify_prefetch(pipe, s, st, C, max_prefix, T_cap, slots, xs)
+            vc.vc_verify_attn_streamed(pipe, s, qd, st, C, max_prefix, T_cap, pl, slots, knd, vnd, out, parts, ws, wsb,
                                        cs, xs)
             cs.synchronize()
             Kcur = np.zeros((w.B, w.Hkv, T_cap, w.d), np.uint16)
@@ -169,7 +169,7 @@ def test_streamed_rejects_pageable_host_memory(vc):
     try:
         host = torch.zeros(2 * 64 * 64, dtype=torch.int16)      # not pinned
         with pytest.raises(vc.VcError) as e:
-            vc.vc_verify_prefetch(pipe, s, host, 64, 64, torch.empty(8192, dtype=torch.int16, device=DEV), None)
+            vc.vc_verify_prefetch(pipe, s, host, 64, 64, 64, torch.empty(8192, dtype=torch.int16, device=DEV), None)
         assert e.value.status == 1
     finally:
         vc.vc_verify_pipeline_destroy(pipe)
@@ -201,7 +201,7 @@ def test_verify_full_size_sampled(vc, name):
         qd, knd, vnd = dev(q), dev(kn), dev(vn)
         pl = dev(np.full(w.B, w.T, np.int32))
         torch.cuda.synchronize()
-        vc.vc_verify_attn_streamed(pipe, s, qd, st, C, w.T, pl, slots, knd, vnd, out, parts, ws, wsb, cs, xs)
+        vc.vc_verify_attn_streamed(pipe, s, qd, st, C, w.T, n_chunks * C, pl, slots, knd, vnd, out, parts, ws, wsb, cs, xs)
         cs.synchronize()
     finally:
         vc.vc_verify_pipeline_destroy(pipe)

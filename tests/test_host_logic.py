@@ -64,9 +64,26 @@ def test_injected_h2d_failure_returns_status_without_a_gpu(monkeypatch):
     s = vc.shape(1, 4, 1, 64, k=1)
     # all pointers non-NULL (plain integers): the call must fail on the injected fault
     with pytest.raises(vc.VcError) as e:
-        vc.vc_verify_attn_streamed(0x1000, s, 0x2000, 0x3000, 64, 64, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000, 1,
+        vc.vc_verify_attn_streamed(0x1000, s, 0x2000, 0x3000, 64, 64, 64, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000, 1,
                                    0x9000, 1 << 30, 0, 0)
     assert e.value.status == 3 and "injected" in str(e.value)
+
+
+def test_streamed_rejects_a_prefix_past_the_store():
+    """max_prefix beyond the pinned store's capacity is an argument error (checked
+    on the host, before any copy could read past the store)."""
+    from verify_compressed_kv_gb300 import _lib as vc
+    s = vc.shape(1, 4, 1, 64, k=1)
+    with pytest.raises(vc.VcError) as e:
+        vc.vc_verify_attn_streamed(0x1000, s, 0x2000, 0x3000, 64, 128 + 1, 128, 0x4000, 0x5000, 0x6000, 0x7000,
+                                   0x8000, 1, 0x9000, 1 << 30, 0, 0)
+    assert e.value.status == 1 and "outside the store" in str(e.value)
+    with pytest.raises(vc.VcError) as e:
+        vc.vc_verify_prefetch(0x1000, s, 0x3000, 64, 65, 64, 0x5000, 0)
+    assert e.value.status == 1
+    with pytest.raises(vc.VcError) as e:
+        vc.vc_verify_prefetch(0x1000, s, 0x3000, 64, 10, 100, 0x5000, 0)      # capacity not a multiple of C
+    assert e.value.status == 1
 
 
 def test_workload_table_matches_the_shapes():

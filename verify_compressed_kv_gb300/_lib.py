@@ -87,8 +87,8 @@ _SIGS = {
         "vc_verify_attn_finish": [S, P, P, P, I32, I32, P, P, SZ, P],
         "vc_verify_pipeline_create": [I32, POINTER(c_void_p)],
         "vc_verify_pipeline_destroy": [P],
-        "vc_verify_prefetch": [P, S, P, I32, I32, P, P],
-        "vc_verify_attn_streamed": [P, S, P, P, I32, I32, P, P, P, P, P, I32, P, SZ, P, P],
+        "vc_verify_prefetch": [P, S, P, I32, I32, I32, P, P],
+        "vc_verify_attn_streamed": [P, S, P, P, I32, I32, I32, P, P, P, P, P, I32, P, SZ, P, P],
         "vc_verify_commit": [S, P, P, P, P, P, I32, I32, P],
         "vc_verify_attn_device_status": [POINTER(c_uint32)],
     },
@@ -273,14 +273,14 @@ def vc_verify_pipeline_destroy(h: int):
     _call("vc_verify_pipeline_destroy", h)
 
 
-def vc_verify_prefetch(h, s, host_kv, C, max_prefix, dev_slots, copy_stream):
-    _call("vc_verify_prefetch", h, ctypes.byref(s), _ptr(host_kv), C, max_prefix, _ptr(dev_slots),
+def vc_verify_prefetch(h, s, host_kv, C, max_prefix, T_cap, dev_slots, copy_stream):
+    _call("vc_verify_prefetch", h, ctypes.byref(s), _ptr(host_kv), C, max_prefix, T_cap, _ptr(dev_slots),
           _stream(copy_stream))
 
 
-def vc_verify_attn_streamed(h, s, q, host_kv, C, max_prefix, prefix_len, dev_slots, k_new, v_new, out,
+def vc_verify_attn_streamed(h, s, q, host_kv, C, max_prefix, T_cap, prefix_len, dev_slots, k_new, v_new, out,
                             parts, ws, ws_bytes, compute_stream, copy_stream):
-    _call("vc_verify_attn_streamed", h, ctypes.byref(s), _ptr(q), _ptr(host_kv), C, max_prefix,
+    _call("vc_verify_attn_streamed", h, ctypes.byref(s), _ptr(q), _ptr(host_kv), C, max_prefix, T_cap,
           _ptr(prefix_len), _ptr(dev_slots), _ptr(k_new), _ptr(v_new), _ptr(out), parts, _ptr(ws),
           ws_bytes, _stream(compute_stream), _stream(copy_stream))
 

@@ -967,12 +967,14 @@ extern "C" vc_status_t vc_verify_pipeline_destroy(vc_verify_pipeline_t p) {
 }
 
 extern "C" vc_status_t vc_verify_prefetch(vc_verify_pipeline_t p, const vc_shape_t* s, const uint16_t* host_kv,
-                                          int32_t C, int32_t max_prefix, uint16_t* dev_slots,
+                                          int32_t C, int32_t max_prefix, int32_t T_cap, uint16_t* dev_slots,
                                           vc_stream_t copy_stream) {
   vc_status_t st = check(s);
   if (st != VC_OK) return st;
   VC_REQUIRE(p && host_kv && dev_slots, "NULL pointer");
-  VC_REQUIRE(C >= 1 && max_prefix >= 0, "need C >= 1 and max_prefix >= 0");
+  VC_REQUIRE(C >= 1 && T_cap >= 0 && T_cap % C == 0, "need C >= 1 and T_cap a multiple of C");
+  VC_REQUIRE(max_prefix >= 0 && max_prefix <= T_cap, "max_prefix %d outside the store's 0 .. %d tokens", max_prefix,
+             T_cap);
   if ((st = check_pinned(host_kv)) != VC_OK) return st;
   const int n_chunks = (max_prefix + C - 1) / C;
   const int upto = n_chunks < p->n_slots ? n_chunks : p->n_slots;
@@ -981,14 +983,16 @@ extern "C" vc_status_t vc_verify_prefetch(vc_verify_pipeline_t p, const vc_shape
 
 extern "C" vc_status_t vc_verify_attn_streamed(vc_verify_pipeline_t p, const vc_shape_t* s, const uint16_t* q,
                                                const uint16_t* host_kv, int32_t C, int32_t max_prefix,
-                                               const int32_t* prefix_len, uint16_t* dev_slots,
+                                               int32_t T_cap, const int32_t* prefix_len, uint16_t* dev_slots,
                                                const uint16_t* k_new, const uint16_t* v_new, uint16_t* out,
                                                int32_t parts_per_chunk, void* workspace, size_t workspace_bytes,
                                                vc_stream_t compute_stream, vc_stream_t copy_stream) {
   vc_status_t st = check(s);
   if (st != VC_OK) return st;
   VC_REQUIRE(p && q && host_kv && prefix_len && dev_slots && k_new && v_new && out, "NULL pointer");
-  VC_REQUIRE(C >= 1 && max_prefix >= 0, "need C >= 1 and max_prefix >= 0");
+  VC_REQUIRE(C >= 1 && T_cap >= 0 && T_cap % C == 0, "need C >= 1 and T_cap a multiple of C");
+  VC_REQUIRE(max_prefix >= 0 && max_prefix <= T_cap, "max_prefix %d outside the store's 0 .. %d tokens", max_prefix,
+             T_cap);
   VC_REQUIRE(parts_per_chunk >= 1 && parts_per_chunk <= 64, "1 <= parts_per_chunk <= 64");
   const size_t need = ws_bytes(s, parts_per_chunk);
   if (!workspace || workspace_bytes < need)

@@ -156,7 +156,8 @@ class GpuSpeculativeDecoder:
         ws = self.ws_v if ws_bytes <= self.ws_v_bytes else torch.zeros(ws_bytes, dtype=torch.uint8,
                                                                         device=self.device)
         vc.vc_verify_attn_streamed(self.pipe, sh, _dev(q[None], self.device), lay.host, lay.C, self.max_prefix,
-                                   lay.prefix_len, lay.slots, kn, vn, out, 1, ws, ws.numel(), self.cs, self.xs)
+                                   lay.T_cap, lay.prefix_len, lay.slots, kn, vn, out, 1, ws, ws.numel(), self.cs,
+                                   self.xs)
         self.cs.synchronize()
         return _bf16_out(out)[0]
 

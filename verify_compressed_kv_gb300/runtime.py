@@ -216,7 +216,7 @@ class Group:
 
     # ---------------------------------------------------------------- the round's steps
     def prefetch(self, layer, copy_stream):
-        vc.vc_verify_prefetch(self.pipes[layer], self.shape, self.host_kv[layer], self.C, self.max_prefix,
+        vc.vc_verify_prefetch(self.pipes[layer], self.shape, self.host_kv[layer], self.C, self.max_prefix, self.T_cap,
                               self.ring[layer], copy_stream)
 
     def prefetch_all(self, copy_stream):
@@ -233,7 +233,8 @@ class Group:
 
     def verify(self, inp: RoundInputs, layer: int, compute_stream, copy_stream):
         vc.vc_verify_attn_streamed(self.pipes[layer], self.shape_k(inp.k), inp.q_verify[layer], self.host_kv[layer],
-                                   self.C, self.max_prefix, self.prefix_len[layer], self.ring[layer], inp.kv_new[0, layer],
+                                   self.C, self.max_prefix, self.T_cap, self.prefix_len[layer], self.ring[layer],
+                                   inp.kv_new[0, layer],
                                    inp.kv_new[1, layer], self.verify_out_k(inp.k), self.parts, self.ws_verify,
                                    self.ws_verify_bytes, compute_stream, copy_stream)
         self.launches += self.chunks() + 1     # one kernel per chunk, then the new-token block + merge
@@ -248,7 +249,7 @@ class Group:
             self._ws0_bytes = vc.vc_verify_attn_workspace_size(self._shape0, self.parts)
             self._ws0 = torch.zeros(self._ws0_bytes, dtype=torch.uint8, device=self.device)
         vc.vc_verify_attn_streamed(self.pipes[layer], self._shape0, q1, self.host_kv[layer], self.C, self.max_prefix,
-                                   self.prefix_len[layer], self.ring[layer], kv1[0], kv1[1], out1, self.parts, self._ws0,
+                                   self.T_cap, self.prefix_len[layer], self.ring[layer], kv1[0], kv1[1], out1, self.parts, self._ws0,
                                    self._ws0_bytes, compute_stream, copy_stream)
         self.launches += self.chunks() + 1
 
@@ -290,6 +291,9 @@ class Group:
         """Host bookkeeping once the read-back has landed."""
         n = self.n_acc_host
         self.max_prefix += int(n.max()) + 1
+        if self.max_prefix > self.T_cap:
+            raise RuntimeError(f"the group's full-KV store holds {self.T_cap} tokens a request, the prefix reached "
+                               f"{self.max_prefix}: size extra_tokens for every round the group makes")
         return int(n.sum()) + self.B          # tokens produced this round
 
 
@@ -309,17 +313,32 @@ class Timeline:
         return self.ev[a].elapsed_time(self.ev[b])
 
 
-def round_single(g: Group, inp: RoundInputs, cs, xs, tl: Timeline | None = None, ready=None):
+def _inputs_first(copy_in, xs, cs):
+    """The round's host inputs over the link ahead of its bulk full-KV stream:
+    copy_in(stream) enqueues their copies on the copy stream, the drafting
+    waits for them."""
+    if copy_in is None:
+        return
+    copy_in(xs)
+    ev = torch.cuda.Event()
+    ev.record(xs)
+    cs.wait_event(ev)
+
+
+def round_single(g: Group, inp: RoundInputs, cs, xs, tl: Timeline | None = None, ready=None, copy_in=None):
     """One round of one group: the first chunks of every layer's full KV start
     streaming while the group drafts (prefix chunks do not depend on the
     drafts), then verify, accept, commit.  `ready`: an event the round's inputs
     wait for (e.g. their copy from host memory on another stream); the full-KV
-    stream does not.  Returns the round's timeline; call g.after_round() after
-    syncing."""
+    stream does not.  `copy_in(stream)`: enqueue the copies of the round's inputs
+    from host memory; they go on the copy stream ahead of the full KV, and the
+    drafting waits for them.  Returns the round's timeline; call
+    g.after_round() after syncing."""
     tl = tl or Timeline()
     tl.mark("start", cs)
     xs.wait_event(tl.ev["start"])
     tl.mark("copy_start", xs)
+    _inputs_first(copy_in, xs, cs)
     g.prefetch_all(xs)
     tl.mark("prefetch_end", xs)            # the first slots' copies: they never wait for a slot
     if ready is not None:
@@ -344,14 +363,15 @@ def round_single(g: Group, inp: RoundInputs, cs, xs, tl: Timeline | None = None,
 
 
 def round_staggered(X: Group, Y: Group, inp_x: RoundInputs, inp_y: RoundInputs, cs, xs, tl: Timeline | None = None,
-                    ready=None):
+                    ready=None, copy_in=None):
     """Cross-resource staggering: X drafts (HBM) while Y's full KV streams over
     the link and Y verifies, accepts and commits.  Roles swap every round.
-    `ready` as in round_single."""
+    `ready` and `copy_in` as in round_single."""
     tl = tl or Timeline()
     tl.mark("start", cs)
     xs.wait_event(tl.ev["start"])
     tl.mark("copy_start", xs)
+    _inputs_first(copy_in, xs, cs)
     Y.prefetch_all(xs)
     if ready is not None:
         cs.wait_event(ready)
