@@ -223,10 +223,11 @@ vc_status_t vc_quant_kv_device_status(uint32_t* status);
  * evenly over a persistent grid sized to the current device (stream-K), the
  * partials are merged with a log-sum-exp rule by the last CTA of each slice.
  * The packed tokens go through fp16 tensor-core products with fp32
- * accumulation: key scales fold into the query and value scales into the
- * softmax weights, each fold kept as an fp16 (hi, lo) pair (~22 bits).  Range
- * limits of those fp16 operands, with f = 16 (bits 2, 4) or 256 (bits 8):
- * |q| * key scale * f and 8 * f * value scale must stay below 65504.
+ * accumulation: each code field, masked in place, is the fp16 subnormal
+ * code * 2^(p - 24); key scales (and the fields' powers of two) fold into the
+ * query and value scales into the softmax weights, as single fp16 values.
+ * Range limits of those fp16 operands (every code width): |q| * key scale * 16
+ * and 8 * 16 * value scale must stay below 65504.
  * G = Hq / Hkv in {1, 2, 4, 5, 8}; softmax_scale > 0.
  * The workspace holds the partials and one arrival
  * counter per slice: it must be zero-filled before its first use, and every
