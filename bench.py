@@ -516,7 +516,7 @@ def run_ours(args, rank, world, local_rank):
             tl.mark("start", cs)
             for i in range(X.k):
                 for l in range(X.L):
-                    X.draft_step(inp_x, l, i, cs)
+                    X.draft_step(inp_x, l, i, cs, chained=i + l > 0)
             tl.mark("end", cs)
             return tl, []
         inp_y = with_drafts(dev_inputs[iy][vcyc % n_inp], dev_drafts[iy][vcyc])
@@ -611,19 +611,25 @@ def run_ours(args, rank, world, local_rank):
     round_ms = [tl.ms("start", "end") for tl in tls]
     commit_span = [tl.ms("commit_start", "commit_end") for tl in tls if "commit_start" in tl.ev]
 
-    # ---- the draft call alone, timed on its stream (CUDA events, L2 > inputs)
+    # ---- the draft call alone, timed on its stream (CUDA events, L2 > inputs):
+    # back-to-back calls chained as in a round (each may start while the
+    # previous one finishes), and the same calls each waiting for the previous
     g = groups[0]
     inp = dev_inputs[0][0]
     n_draft = 20
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    for i in range(3):
-        g.draft_step(inp, 0, 0, cs)
-    ev[0].record(cs)
-    for i in range(n_draft):
-        g.draft_step(inp, 0, 0, cs)
-    ev[1].record(cs)
-    ev[1].synchronize()
-    draft_call_ms = ev[0].elapsed_time(ev[1]) / n_draft
+
+    def draft_calls_ms(chained):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        for i in range(3):
+            g.draft_step(inp, 0, 0, cs, chained=chained and i > 0)
+        ev[0].record(cs)
+        for i in range(n_draft):
+            g.draft_step(inp, 0, 0, cs, chained=chained)
+        ev[1].record(cs)
+        ev[1].synchronize()
+        return ev[0].elapsed_time(ev[1]) / n_draft
+    draft_unchained_ms = draft_calls_ms(False)
+    draft_call_ms = draft_calls_ms(True)
     P = int(g.packed_len[0].max().item())
     alg_bytes = algorithmic_draft_bytes(w, P)
     peaks = load_peaks()
@@ -704,8 +710,10 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
-                     "kernel": "vc_draft_attn (split-KV + tail + combine), alone on its stream",
+                     "kernel": "vc_draft_attn (stream-K split, bf16 tail and combine in one grid), "
+                               "back-to-back chained calls alone on its stream",
                      "bytes_per_launch": alg_bytes, "ms_per_launch": draft_call_ms,
+                     "ms_per_launch_unchained": draft_unchained_ms,
                      "ms_per_launch_in_round": draft_in_round_ms, "peak_source": peaks["source"]},
         "h2d": {"gbs": h2d_rate, "bytes_per_round": h2d_bytes / args.steps, "copy_ms": med(copy_span),
                 "slots_per_layer": groups[0].n_slots,

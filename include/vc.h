@@ -233,15 +233,26 @@ vc_status_t vc_quant_kv_device_status(uint32_t* status);
  * counter per slice: it must be zero-filled before its first use, and every
  * call leaves the counters at zero again.  Its size depends on the device
  * (SM count, occupancy): query it with the same device current.  Calls that
- * share a workspace must not overlap on the GPU.
+ * share a workspace must not overlap on the GPU, other than as chained calls
+ * (below), which order their workspace accesses themselves.
+ * flags: 0, or VC_DRAFT_CHAINED for a call enqueued directly after another
+ * vc_draft_attn call on the same stream (the draft steps of a round, layer
+ * after layer).  Such a call is launched with programmatic dependent launch:
+ * its CTAs may start while the previous call's last CTAs run, and before
+ * that call has finished they read only this call's packed cache (kc, ksz,
+ * vc, vsz, packed_len); queries, k_cur/v_cur, the tail, the workspace and
+ * out are touched only after it.  The caller guarantees that the packed
+ * cache was complete before the previous call was enqueued (no draft call
+ * writes one).  Other bits: VC_ERR_INVALID_ARG.
  * Reads B, Hq, Hkv, d, bits, softmax_scale. */
+#define VC_DRAFT_CHAINED 1u
 vc_status_t vc_draft_attn_workspace_size(const vc_shape_t* s, int32_t max_packed, size_t* bytes);
 vc_status_t vc_draft_attn(const vc_shape_t* s, const uint16_t* q, const uint16_t* k_cur,
                           const uint16_t* v_cur, const uint32_t* kc, const uint16_t* ksz,
                           const uint32_t* vc, const uint16_t* vsz, const int32_t* packed_len,
                           int32_t max_packed, int32_t T_cap, uint16_t* tail_k, uint16_t* tail_v,
                           const int32_t* tail_len, int32_t tail_cap, int32_t step, uint16_t* out,
-                          void* workspace, size_t workspace_bytes, vc_stream_t stream);
+                          void* workspace, size_t workspace_bytes, uint32_t flags, vc_stream_t stream);
 /* Device status (barrier time-outs) since the last call; synchronises. */
 vc_status_t vc_draft_attn_device_status(uint32_t* status);
 /* Test hooks, for the failure-detection test only (host-side settings of this

@@ -44,6 +44,20 @@ def test_every_declared_symbol_is_exported(vc):
         assert hasattr(lib, fn), f"{fn} not exported by lib{exported[fn]}.so"
 
 
+def test_binding_arity_matches_the_header(vc):
+    """Every bound call passes as many arguments as vc.h declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    decl = {m.group(1): m.group(2) for m in re.finditer(r"\b(vc_[a-z0-9_]+)\s*\(([^()]*)\)\s*;", text)}
+    n = 0
+    for lib, fns in vc._SIGS.items():
+        for fn, argtypes in fns.items():
+            params = decl[fn].strip()
+            count = 0 if params in ("", "void") else params.count(",") + 1
+            assert count == len(argtypes), f"{fn}: vc.h declares {count} parameters, the binding passes {len(argtypes)}"
+            n += 1
+    assert n >= 20
+
+
 def test_status_strings(vc):
     assert vc.status_str(0) == "ok"
     assert "workspace" in vc.status_str(5)
@@ -107,6 +121,10 @@ def test_misaligned_and_null_pointers_are_rejected_before_launch(vc):
         vc.vc_draft_attn(s, 0x1000, 0x2000, None, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 64, 64, 0x8000, 0x9000,
                          0xa000, 8, 0, 0xb000, 0xc000, 1 << 20, stream=0)
     assert e.value.status == 1
+    with pytest.raises(vc.VcError) as e:                      # a flag bit the call does not know
+        vc.vc_draft_attn(s, 0x1000, 0x2000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 64, 64, 0x8000, 0x9000,
+                         0xa000, 8, 0, 0xb000, 0xc000, 1 << 20, stream=0, flags=2)
+    assert e.value.status == 1 and "flags" in str(e.value)
 
 
 def test_stage_groups_checks_ranges_before_any_copy(vc):

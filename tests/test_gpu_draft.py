@@ -137,6 +137,78 @@ def test_draft_full_size_sampled(vc, name):
         assert_attn_close(got[b, h * G:(h + 1) * G], want[0], what=f"{name} b{b} h{h}")
 
 
+def test_draft_chained_calls_equal_unchained_and_the_oracle(vc):
+    """The draft steps of a round, layer after layer, as chained calls (each may
+    start while the previous one finishes; one workspace shared by all): every
+    output bit for bit that of the same calls each waiting for the previous, the
+    tail rows each step stores, and sampled slices against the oracle with the
+    tail the earlier steps wrote.  A full grid of stream CTAs (Llama-shaped
+    layer, 4096 packed tokens)."""
+    from gpu_util import dev, zeros_bytes, bf16_to_f64, DEV, assert_attn_close
+    w = synth.get("llama", T=4096)
+    L, k = 2, 3
+    scale = 1.0 / math.sqrt(w.d)
+    s = vc.shape(w.B, w.Hq, w.Hkv, w.d, bits=w.bits, softmax_scale=scale)
+    rng = np.random.default_rng(11)
+    tlen = rng.integers(0, 16, size=w.B).astype(np.int32)
+    tail_cap = 32 + k + 1
+    kcb, kszb, vcb, vszb = vc.vc_quant_packed_bytes(s, w.T)
+    lay = []
+    for l in range(L):
+        K, V = synth.kv(w, layer=l)
+        packed = [torch.zeros(n // e, dtype=dt, device=DEV)
+                  for n, e, dt in ((kcb, 4, torch.int32), (kszb, 2, torch.int16), (vcb, 4, torch.int32), (vszb, 2, torch.int16))]
+        vc.vc_quant_kv_pack(s, w.T, w.T, dev(K), dev(V), *packed)
+        tk0 = synth.bf16_bits(rng.standard_normal((w.B, w.Hkv, tail_cap, w.d)).astype(np.float32))
+        tv0 = synth.bf16_bits(rng.standard_normal((w.B, w.Hkv, tail_cap, w.d)).astype(np.float32))
+        lay.append(dict(K=K, V=V, packed=packed, tk0=tk0, tv0=tv0))
+    q = {(l, i): synth.draft_q(w, 0, i, layer=l) for l in range(L) for i in range(k)}
+    cur = {(l, i): synth.draft_kv_cur(w, 0, i, layer=l) for l in range(L) for i in range(k)}
+    q_d = {key: dev(v) for key, v in q.items()}
+    cur_d = {key: (dev(v[0]), dev(v[1])) for key, v in cur.items()}
+    plen_d, tlen_d = dev(np.full(w.B, w.T, np.int32)), dev(tlen)
+    wsb = vc.vc_draft_attn_workspace_size(s, w.T)
+
+    def run(chained):
+        ws = zeros_bytes(wsb)
+        tails = [(dev(x["tk0"]), dev(x["tv0"])) for x in lay]
+        outs = {key: torch.empty((w.B, w.Hq, w.d), dtype=torch.int16, device=DEV) for key in q}
+        torch.cuda.synchronize()
+        for i in range(k):                     # nothing else on the stream between the calls
+            for l in range(L):
+                vc.vc_draft_attn(s, q_d[l, i], *cur_d[l, i], *lay[l]["packed"], plen_d, w.T, w.T, *tails[l], tlen_d,
+                                 tail_cap, i, outs[l, i], ws, wsb,
+                                 flags=vc.VC_DRAFT_CHAINED if chained and i + l > 0 else 0)
+        torch.cuda.synchronize()
+        assert vc.vc_draft_attn_device_status() == 0
+        return ({key: o.cpu().numpy() for key, o in outs.items()},
+                [(a.cpu().numpy().view(np.uint16), b.cpu().numpy().view(np.uint16)) for a, b in tails])
+
+    plain, plain_tails = run(False)
+    chained, chained_tails = run(True)
+    for key in q:
+        assert np.array_equal(chained[key], plain[key]), f"layer {key[0]} step {key[1]}"
+    for l in range(L):
+        for x, y in zip(chained_tails[l], plain_tails[l]):
+            assert np.array_equal(x, y)
+        for i in range(k):
+            for b in range(w.B):
+                assert np.array_equal(chained_tails[l][0][b, :, tlen[b] + i], cur[l, i][0][b])
+                assert np.array_equal(chained_tails[l][1][b, :, tlen[b] + i], cur[l, i][1][b])
+    G = w.G
+    for l in range(L):
+        for (b, h) in [(0, 0), (w.B - 1, w.Hkv - 1)]:
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            pk = kivi.quant_pack(lay[l]["K"][sl], lay[l]["V"][sl], w.bits)
+            tk, tv = lay[l]["tk0"][sl].copy(), lay[l]["tv0"][sl].copy()
+            for i in range(k):
+                want = oatt.draft_attention(q[l, i][b:b + 1, h * G:(h + 1) * G], *pk, [w.T], tk, tv, tlen[b:b + 1],
+                                            w.bits, scale, k_cur=cur[l, i][0][sl], v_cur=cur[l, i][1][sl], step=i)
+                got = (chained[l, i][b, h * G:(h + 1) * G].view(np.uint16).astype(np.uint32) << 16).view(np.float32)
+                assert_attn_close(got.astype(np.float64), want[0], what=f"layer {l} step {i} b{b} h{h}")
+                tk[0, 0, tlen[b] + i], tv[0, 0, tlen[b] + i] = cur[l, i][0][b, h], cur[l, i][1][b, h]
+
+
 def test_draft_argument_errors(vc):
     from gpu_util import DEV
     s = vc.shape(1, 4, 1, 96, bits=2)

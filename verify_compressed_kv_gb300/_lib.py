@@ -76,7 +76,7 @@ _SIGS = {
     },
     "vc_draft_attn": {
         "vc_draft_attn_workspace_size": [S, I32, POINTER(c_size_t)],
-        "vc_draft_attn": [S, P, P, P, P, P, P, P, P, I32, I32, P, P, P, I32, I32, P, P, SZ, P],
+        "vc_draft_attn": [S, P, P, P, P, P, P, P, P, I32, I32, P, P, P, I32, I32, P, P, SZ, c_uint32, P],
         "vc_draft_attn_device_status": [POINTER(c_uint32)],
         "vc_draft_attn_test_hooks": [ctypes.c_int64, I32],
     },
@@ -222,11 +222,15 @@ def vc_draft_attn_workspace_size(s, max_packed):
     return n.value
 
 
+VC_DRAFT_CHAINED = 1
+
+
 def vc_draft_attn(s, q, k_cur, v_cur, kc, ksz, vc, vsz, packed_len, max_packed, T_cap, tail_k, tail_v,
-                  tail_len, tail_cap, step, out, ws, ws_bytes, stream=None):
+                  tail_len, tail_cap, step, out, ws, ws_bytes, stream=None, flags=0):
+    """`flags` is the C call's argument before the stream (0 or VC_DRAFT_CHAINED)."""
     _call("vc_draft_attn", ctypes.byref(s), _ptr(q), _ptr(k_cur), _ptr(v_cur), _ptr(kc), _ptr(ksz),
           _ptr(vc), _ptr(vsz), _ptr(packed_len), max_packed, T_cap, _ptr(tail_k), _ptr(tail_v),
-          _ptr(tail_len), tail_cap, step, _ptr(out), _ptr(ws), ws_bytes, _stream(stream))
+          _ptr(tail_len), tail_cap, step, _ptr(out), _ptr(ws), ws_bytes, int(flags), _stream(stream))
 
 
 def vc_draft_attn_test_hooks(wait_cycles: int, withhold_first_stage: int) -> None:

@@ -86,6 +86,16 @@ struct DraftArgs {
   uint16_t* out;            // [B, Hq, D]
 };
 
+// Programmatic dependent launch.  Every CTA lets the next grid on the stream
+// launch as soon as it starts; that grid's CTAs then take SMs as this one's
+// finish.  Every CTA's consumer threads wait for the previous grid before
+// their first read of anything but the packed cache, so a grid completes only
+// after its predecessor did, and each grid sees all earlier grids' writes.
+// Both instructions are no-ops for a launch without the programmatic
+// serialisation attribute.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ partition
 // Start of stream CTA c's groups in the stream-K order (equal shares).
 __host__ __device__ inline long long range_lo(long long c, const DraftArgs& a) {
@@ -814,6 +824,10 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
     if (lane == 0) produce<D, BITS, G>(a, smem, c, full, empty, abort);
     return;
   }
+  // a chained call: everything past this point (queries, partials, counters,
+  // output) waits for the previous grid on the stream; only the producer's
+  // packed-cache copies run ahead of it
+  grid_dependency_wait();
   // lane constants: correction columns (gid = 2g: the zeros of channel group
   // g, over the weights' factor 2^(kFold - C(r)); odd gid: zero columns; a V
   // meta row pair holds the scales first, then the zeros)
@@ -887,9 +901,11 @@ template <int D, int BITS, int G, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB) draft_kernel(DraftArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int c = blockIdx.x;
+  grid_launch_dependents();
   if (c < a.n_stream) {
     stream_cta<D, BITS, G>(a, smem, c);
   } else if ((threadIdx.x >> 5) < kWarps) {     // tail CTA: its consumer warps take slices t, t + n_tail_cta, ...
+    grid_dependency_wait();                     // the tail rows come from earlier calls
     for (int bh = c - a.n_stream; bh < a.B * a.Hkv; bh += a.n_cta - a.n_stream) tail_part<D, BITS, G>(a, smem, bh);
   }
 }
@@ -967,18 +983,29 @@ size_t ws_bytes(const vc_shape_t* s, const LaunchPlan& lp) {
   return o + static_cast<size_t>(s->B) * s->Hkv * sizeof(unsigned int);
 }
 
+// chained: launched with programmatic stream serialisation, so that it may
+// start while the previous kernel on the stream (a draft call) finishes.
 template <int D, int BITS, int G>
-vc_status_t launch_t(const DraftArgs& a, const LaunchPlan& lp, cudaStream_t cs) {
-  const int grid = lp.n_cta;
-  draft_kernel<D, BITS, G, MinBlocks<G>::value><<<grid, kThreads, lp.smem, cs>>>(a);
+vc_status_t launch_t(const DraftArgs& a, const LaunchPlan& lp, cudaStream_t cs, bool chained) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(lp.n_cta));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = lp.smem;
+  cfg.stream = cs;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = chained ? 1 : 0;
+  VC_CUDA_CHECK(cudaLaunchKernelEx(&cfg, draft_kernel<D, BITS, G, MinBlocks<G>::value>, a));
   VC_LAUNCH_CHECK("draft_kernel");
   return VC_OK;
 }
 
-vc_status_t launch(const vc_shape_t* s, const DraftArgs& a, const LaunchPlan& lp, cudaStream_t cs) {
+vc_status_t launch(const vc_shape_t* s, const DraftArgs& a, const LaunchPlan& lp, cudaStream_t cs, bool chained) {
   const int G = s->Hq / s->Hkv;
 #define VC_L(D_, B_, G_) \
-  if (s->d == D_ && s->bits == B_ && G == G_) return launch_t<D_, B_, G_>(a, lp, cs);
+  if (s->d == D_ && s->bits == B_ && G == G_) return launch_t<D_, B_, G_>(a, lp, cs, chained);
 #define VC_L_G(D_, B_) VC_L(D_, B_, 1) VC_L(D_, B_, 2) VC_L(D_, B_, 4) VC_L(D_, B_, 5) VC_L(D_, B_, 8)
   VC_L_G(128, 2) VC_L_G(128, 4) VC_L_G(128, 8) VC_L_G(64, 2) VC_L_G(64, 4) VC_L_G(64, 8)
 #undef VC_L_G
@@ -1004,9 +1031,10 @@ extern "C" vc_status_t vc_draft_attn(const vc_shape_t* s, const uint16_t* q, con
                                      const uint32_t* vc, const uint16_t* vsz, const int32_t* packed_len,
                                      int32_t max_packed, int32_t T_cap, uint16_t* tail_k, uint16_t* tail_v,
                                      const int32_t* tail_len, int32_t tail_cap, int32_t step, uint16_t* out,
-                                     void* workspace, size_t workspace_bytes, vc_stream_t stream) {
+                                     void* workspace, size_t workspace_bytes, uint32_t flags, vc_stream_t stream) {
   vc_status_t st = check(s);
   if (st != VC_OK) return st;
+  VC_REQUIRE((flags & ~VC_DRAFT_CHAINED) == 0u, "unknown flags 0x%x", flags);
   VC_REQUIRE(max_packed >= 0 && max_packed % kGroup == 0 && max_packed <= T_cap && T_cap % kGroup == 0,
              "need 0 <= max_packed <= T_cap, multiples of 32 (max_packed=%d, T_cap=%d)", max_packed, T_cap);
   VC_REQUIRE(q && out && packed_len && tail_len && tail_k && tail_v, "NULL pointer");
@@ -1045,7 +1073,7 @@ extern "C" vc_status_t vc_draft_attn(const vc_shape_t* s, const uint16_t* q, con
   off += (rows * sizeof(float) + 255) & ~size_t(255);
   a.counter = reinterpret_cast<unsigned int*>(ws + off);
   a.out = out;
-  return launch(s, a, lp, reinterpret_cast<cudaStream_t>(stream));
+  return launch(s, a, lp, reinterpret_cast<cudaStream_t>(stream), (flags & VC_DRAFT_CHAINED) != 0u);
 }
 
 extern "C" vc_status_t vc_draft_attn_test_hooks(int64_t wait_cycles, int32_t withhold_first_stage) {

@@ -224,12 +224,15 @@ class Group:
         for layer in range(self.L):
             self.prefetch(layer, copy_stream)
 
-    def draft_step(self, inp: RoundInputs, layer: int, step: int, stream):
+    def draft_step(self, inp: RoundInputs, layer: int, step: int, stream, chained=False):
+        """chained: the previous work on `stream` is another draft call, so
+        this one may start while that one finishes (VC_DRAFT_CHAINED)."""
         vc.vc_draft_attn(self.shape, inp.q_draft[layer, step], inp.kv_cur[0, layer, step], inp.kv_cur[1, layer, step],
                          self.kc[layer], self.ksz[layer], self.vc[layer], self.vsz[layer], self.packed_len[layer],
                          self.P_cap, self.P_cap, self.tail_k[layer], self.tail_v[layer], self.tail_len[layer],
-                         self.tail_cap, step, self.draft_out, self.ws_draft, self.ws_draft_bytes, stream)
-        self.launches += 3                     # split-KV, tail, combine
+                         self.tail_cap, step, self.draft_out, self.ws_draft, self.ws_draft_bytes, stream,
+                         flags=vc.VC_DRAFT_CHAINED if chained else 0)
+        self.launches += 1                     # stream CTAs, tail CTAs and the combine: one grid
 
     def verify(self, inp: RoundInputs, layer: int, compute_stream, copy_stream):
         vc.vc_verify_attn_streamed(self.pipes[layer], self.shape_k(inp.k), inp.q_verify[layer], self.host_kv[layer],
@@ -346,7 +349,7 @@ def round_single(g: Group, inp: RoundInputs, cs, xs, tl: Timeline | None = None,
     tl.mark("draft_start", cs)
     for i in range(inp.k):
         for l in range(g.L):
-            g.draft_step(inp, l, i, cs)
+            g.draft_step(inp, l, i, cs, chained=i + l > 0)
     tl.mark("draft_end", cs)
     for l in range(g.L):
         g.verify(inp, l, cs, xs)
@@ -378,7 +381,7 @@ def round_staggered(X: Group, Y: Group, inp_x: RoundInputs, inp_y: RoundInputs, 
     tl.mark("draft_start", cs)
     for i in range(inp_x.k):
         for l in range(X.L):
-            X.draft_step(inp_x, l, i, cs)
+            X.draft_step(inp_x, l, i, cs, chained=i + l > 0)
     tl.mark("draft_end", cs)
     for l in range(Y.L):
         Y.verify(inp_y, l, cs, xs)
@@ -400,10 +403,12 @@ def round_lockstep(groups, inps, cs, xs, tl: Timeline | None = None):
     tl = tl or Timeline()
     tl.mark("start", cs)
     tl.mark("draft_start", cs)
+    first = True
     for g, inp in zip(groups, inps):
         for i in range(inp.k):
             for l in range(g.L):
-                g.draft_step(inp, l, i, cs)
+                g.draft_step(inp, l, i, cs, chained=not first)
+                first = False
     tl.mark("draft_end", cs)
     xs.wait_event(tl.ev["draft_end"])
     tl.mark("copy_start", xs)
