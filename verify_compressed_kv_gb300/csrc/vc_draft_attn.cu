@@ -7,11 +7,13 @@
 // of a KV head share every byte read.
 //
 // One launch per draft step: one wave of persistent stream CTAs (occupancy x
-// SM count), then up to as many tail CTAs:
+// SM count):
 //   * stream-K partition: the packed groups of every (request, KV head) are
-//     laid end to end and each stream CTA takes an equal contiguous range, so
-//     the work is balanced whatever B*Hkv is; a range may span two heads
-//     (segments);
+//     laid end to end and each stream CTA takes a contiguous range, so the
+//     work is balanced whatever B*Hkv is; a range may span several heads
+//     (segments).  The ranges are balanced by cost, not by groups: a head
+//     switch inside a range and a bf16 tail pass (below) are each charged as
+//     a number of groups, measured on per-CTA timestamps;
 //   * a segment is streamed through a ring of shared-memory stages (11 groups
 //     of 32 tokens each: K codes, K scale/zero, V codes, V scale/zero), filled
 //     by bulk async copies (cp.async.bulk + mbarrier transaction counts, bounded
@@ -31,13 +33,16 @@
 //     partial per query head; the last CTA to finish a (request, KV head)
 //     (arrival counter in the workspace, reset by that CTA) merges all its
 //     partials and writes the bf16 output.
-// Tail CTAs, launched after the stream CTAs (they start as the first stream
-// CTAs finish, in the shadow of the slowest), take the bf16 tails (tokens
-// committed since the last full group, earlier draft steps, the current
-// token) and store the current token's K/V into the tail for the following
-// steps.
+// The bf16 tails (tokens committed since the last full group, earlier draft
+// steps, the current token) are taken by the stream CTAs before their ranges
+// (the ring fills meanwhile), each slice's by a fixed CTA, which also stores
+// the current token's K/V into the tail for the following steps.  Without packed groups, tail CTAs alone
+// take them.
 #include <algorithm>
 #include <cfloat>
+#include <climits>
+#include <mutex>
+#include <vector>
 
 #include "vc_internal.h"
 
@@ -52,6 +57,15 @@ constexpr int kConsumers = kWarps * 32;
 constexpr int kThreads = kConsumers + 32;        // + one producer warp
 constexpr int kGroup = 32;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxStream = 512;                 // stream CTAs one launch can describe (partition table)
+// Costs charged in the partition, in 32-token groups of 3072 bytes (d = 128,
+// int2), scaled by 3072 / (bytes of a group) for other shapes.  Per-CTA
+// timestamps: such a group streams in ~0.1 us; a head switch inside a range
+// costs 6-8 us (flush, the next head's queries, ring refill); a tail pass
+// ~5 us (a chain of dependent global round trips under full HBM load).
+constexpr long long kSwitchGroups = 72;
+constexpr long long kTailGroups = 50;
+constexpr long long kRefGroupBytes = 3072;
 constexpr long long kWaitCycles = 4000000000LL;   // default wait bound: ~2 s at 2 GHz
 // Test hooks (vc_draft_attn_test_hooks): the wait bound and a withheld first
 // stage, so that a test can make the bounded waits run out.  Host side only.
@@ -73,8 +87,8 @@ struct DraftArgs {
   int B, Hq, Hkv;
   int NG;                   // layout stride: T_cap / 32 groups per (b, h)
   int NGmax;                // groups per (b, h) covered by the partition
-  int n_stream;             // stream CTAs with packed groups
-  int n_cta;                // CTAs launched: n_stream stream CTAs, then the tail CTAs
+  int n_stream;             // stream CTAs (0: no packed groups)
+  int n_cta;                // CTAs launched: n_stream stream CTAs, or tail CTAs alone
   long long total;          // B * Hkv * NGmax
   int max_parts;            // partial slots per (b, h): stream CTAs + the tail
   float scale_log2;
@@ -84,6 +98,7 @@ struct DraftArgs {
   float* part_lse;          // [B*Hq, max_parts]      log2-sum-exp of each partial
   unsigned int* counter;    // [B*Hkv] arrivals (zero between calls)
   uint16_t* out;            // [B, Hq, D]
+  int lo_tab[kMaxStream + 1];  // stream CTA c takes groups [lo_tab[c], lo_tab[c + 1]) (slice-major)
 };
 
 // Programmatic dependent launch.  Every CTA lets the next grid on the stream
@@ -97,9 +112,20 @@ __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepco
 __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ------------------------------------------------------------------ partition
-// Start of stream CTA c's groups in the stream-K order (equal shares).
+// Start of stream CTA c's groups in the stream-K order.
 __host__ __device__ inline long long range_lo(long long c, const DraftArgs& a) {
-  return c >= a.n_stream ? a.total : c * a.total / a.n_stream;
+  return c >= a.n_stream ? a.total : a.lo_tab[c];
+}
+
+// The stream CTA whose range holds position x: the largest c < n with
+// lo[c] <= x (lo[0] = 0 and the ranges are non-empty up to the last group).
+__host__ __device__ inline int cta_at(long long x, const int* lo, int n) {
+  int l = 0, h = n - 1;
+  while (l < h) {
+    const int m = (l + h + 1) >> 1;
+    if (lo[m] <= x) l = m; else h = m - 1;
+  }
+  return l;
 }
 
 // Stream CTAs overlapping the groups of (b, h) index bh: [first, last].
@@ -109,16 +135,15 @@ __host__ __device__ inline void ctas_of(int bh, const DraftArgs& a, int& first, 
     last = -1;
     return;
   }
-  const long long s = static_cast<long long>(bh) * a.NGmax, e = s + a.NGmax;
-  long long c = s * a.n_stream / a.total;
-  while (c + 1 < a.n_stream && range_lo(c + 1, a) <= s) ++c;
-  while (c > 0 && range_lo(c, a) > s) --c;
-  first = static_cast<int>(c);
-  long long d = (e * a.n_stream + a.total - 1) / a.total;
-  if (d > a.n_stream - 1) d = a.n_stream - 1;
-  while (d > 0 && range_lo(d, a) >= e) --d;
-  while (d + 1 < a.n_stream && range_lo(d + 1, a) < e) ++d;
-  last = static_cast<int>(d);
+  const long long s = static_cast<long long>(bh) * a.NGmax;
+  first = cta_at(s, a.lo_tab, a.n_stream);
+  last = cta_at(s + a.NGmax - 1, a.lo_tab, a.n_stream);
+}
+
+// Slices whose bf16 tail stream CTA c runs after its range: bh with
+// floor(bh * n / nbh) = c, i.e. [tail_lo(c), tail_lo(c + 1)).
+__host__ __device__ inline long long tail_lo(long long c, long long n, long long nbh) {
+  return (c * nbh + n - 1) / n;
 }
 
 // ------------------------------------------------------------------ shared memory plan
@@ -824,10 +849,25 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
     if (lane == 0) produce<D, BITS, G>(a, smem, c, full, empty, abort);
     return;
   }
-  // a chained call: everything past this point (queries, partials, counters,
-  // output) waits for the previous grid on the stream; only the producer's
-  // packed-cache copies run ahead of it
+  // the first segment from packed_len (packed-cache data); a chained call:
+  // everything past the wait (queries, tails, partials, counters, output)
+  // waits for the previous grid on the stream; only packed-cache reads run
+  // ahead of it
+  const long long hi = range_lo(c + 1, a);
+  long long pos = range_lo(c, a);
+  Segment sg;
+  bool over;
+  bool more = next_segment(a, pos, hi, sg, over);
   grid_dependency_wait();
+  // the bf16 tails of the slices assigned to this CTA, first: the ring is
+  // already filled, and a tail partial arrives long before the stream
+  // partials of its slice and leaves the merge to the last of them
+  {
+    const long long nbh = static_cast<long long>(a.B) * a.Hkv;
+    for (long long bh = tail_lo(c, a.n_stream, nbh); bh < tail_lo(c + 1, a.n_stream, nbh); ++bh)
+      tail_part<D, BITS, G>(a, smem, static_cast<int>(bh));
+    vc_bar_sync(1, kConsumers);                             // red / flag reused by the segments
+  }
   // lane constants: correction columns (gid = 2g: the zeros of channel group
   // g, over the weights' factor 2^(kFold - C(r)); odd gid: zero columns; a V
   // meta row pair holds the scales first, then the zeros)
@@ -838,11 +878,7 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
   const float cs_code = a.scale_log2 * exp2f(static_cast<float>(24 - kFold));
   int buf = 0;                                  // ring position and phase of the next stage use
   uint32_t phase = 0;
-  const long long hi = range_lo(c + 1, a);
-  long long pos = range_lo(c, a);
-  Segment sg;
-  bool over;
-  while (next_segment(a, pos, hi, sg, over)) {
+  for (; more; more = next_segment(a, pos, hi, sg, over)) {
     if (over && threadIdx.x == 0) atomicOr(&g_draft_status, VC_DEV_CAPACITY);
     const int b = sg.bh / a.Hkv, kvh = sg.bh % a.Hkv;
     int first, last;
@@ -898,15 +934,15 @@ __device__ void stream_cta(const DraftArgs& a, uint8_t* smem, int c) {
 }
 
 template <int D, int BITS, int G, int MINB>
-__global__ void __launch_bounds__(kThreads, MINB) draft_kernel(DraftArgs a) {
+__global__ void __launch_bounds__(kThreads, MINB) draft_kernel(const __grid_constant__ DraftArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int c = blockIdx.x;
   grid_launch_dependents();
-  if (c < a.n_stream) {
+  if (a.n_stream > 0) {
     stream_cta<D, BITS, G>(a, smem, c);
-  } else if ((threadIdx.x >> 5) < kWarps) {     // tail CTA: its consumer warps take slices t, t + n_tail_cta, ...
+  } else if ((threadIdx.x >> 5) < kWarps) {     // no packed groups: tail CTA c takes slices c, c + n_cta, ...
     grid_dependency_wait();                     // the tail rows come from earlier calls
-    for (int bh = c - a.n_stream; bh < a.B * a.Hkv; bh += a.n_cta - a.n_stream) tail_part<D, BITS, G>(a, smem, bh);
+    for (int bh = c; bh < a.B * a.Hkv; bh += a.n_cta) tail_part<D, BITS, G>(a, smem, bh);
   }
 }
 
@@ -933,6 +969,59 @@ struct LaunchPlan {
   int n_stream = 0, n_cta = 0, max_parts = 1;
   long long total = 0;
   size_t smem = 0;
+  std::vector<int> lo;                          // n_stream + 1 range starts
+};
+
+// Cost-balanced stream-K partition of the slice-major groups [0, total)
+// (slice boundaries every NG groups) over n CTAs.  A CTA's cost is its
+// groups, plus `sw` per slice boundary strictly inside its range, plus `tl`
+// per bf16 tail it runs.  Each CTA in turn takes the longest range whose
+// cost stays within T; T is the smallest budget that covers every group, by
+// bisection.  Every range holds at least one group until the groups run out.
+struct Partition {
+  long long total, NG, sw, tl;
+  int n;
+  long long nbh;
+  long long crossings(long long p, long long e) const { return e > p + 1 ? (e - 1) / NG - p / NG : 0; }
+  long long end_of(int c, long long p, long long T) const {
+    long long budget = T - tl * (tail_lo(c + 1, n, nbh) - tail_lo(c, n, nbh));
+    if (budget < 1) budget = 1;
+    long long best = std::min(total, p + 1);
+    for (long long k = 0;; ++k) {               // ends between boundaries, crossing at most k
+      const long long e = std::min(total, p + budget - sw * k);
+      if (e <= p) break;
+      if (crossings(p, e) <= k) {
+        best = std::max(best, e);
+        break;
+      }
+    }
+    for (long long j = 1;; ++j) {               // ends on the j-th boundary after p
+      const long long b = (p / NG + j) * NG;
+      if (b > total || b - p + sw * (j - 1) > budget) break;
+      best = std::max(best, b);
+    }
+    return best;
+  }
+  bool covers(long long T) const {
+    long long p = 0;
+    for (int c = 0; c < n && p < total; ++c) p = end_of(c, p, T);
+    return p >= total;
+  }
+  void fill(std::vector<int>& lo) const {
+    long long T_hi = std::max<long long>(1, (total + n - 1) / n);
+    while (!covers(T_hi)) T_hi *= 2;
+    long long T_lo = 0;                         // not covering
+    while (T_hi - T_lo > 1) {
+      const long long m = T_lo + (T_hi - T_lo) / 2;
+      if (covers(m)) T_hi = m; else T_lo = m;
+    }
+    lo.assign(static_cast<size_t>(n) + 1, static_cast<int>(total));
+    long long p = 0;
+    for (int c = 0; c < n; ++c) {
+      lo[c] = static_cast<int>(p);
+      if (p < total) p = end_of(c, p, T_hi);
+    }
+  }
 };
 
 template <int D, int BITS, int G>
@@ -946,26 +1035,76 @@ vc_status_t plan_t(const vc_shape_t* s, int max_packed, LaunchPlan* lp) {
   VC_CUDA_CHECK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kThreads, P::total));
   if (occ < 1) VC_FAIL(VC_ERR_UNSUPPORTED, "draft kernel does not fit on an SM");
   const long long NGmax = max_packed / kGroup;
-  lp->total = static_cast<long long>(s->B) * s->Hkv * NGmax;
-  long long n = static_cast<long long>(occ) * sms;
+  const long long slices = static_cast<long long>(s->B) * s->Hkv;
+  lp->total = slices * NGmax;
+  if (lp->total > INT_MAX) VC_FAIL(VC_ERR_UNSUPPORTED, "B * Hkv * max_packed / 32 = %lld groups exceeds 2^31 - 1", lp->total);
+  long long n = std::min<long long>(static_cast<long long>(occ) * sms, kMaxStream);
   const long long by_work = lp->total / kWarps;                 // at least one stage per CTA
   if (n > by_work) n = by_work;
   if (n < 1 && lp->total > 0) n = 1;
   lp->n_stream = static_cast<int>(lp->total > 0 ? n : 0);
-  // tail CTAs follow the stream CTAs: they start as the first stream CTAs finish
-  const long long slices = static_cast<long long>(s->B) * s->Hkv;
-  lp->n_cta = lp->n_stream + static_cast<int>(std::min<long long>(slices, static_cast<long long>(occ) * sms));
-  if (lp->n_stream > 0) {
-    const long long per = lp->total / lp->n_stream;               // >= kWarps groups per CTA
-    lp->max_parts = static_cast<int>((NGmax + per - 1) / per + 1) + 1;
-  } else {
-    lp->max_parts = 1;
-  }
   lp->smem = P::total;
+  if (lp->n_stream == 0) {                                      // tail CTAs alone
+    lp->n_cta = static_cast<int>(std::min<long long>(slices, static_cast<long long>(occ) * sms));
+    lp->max_parts = 1;
+    lp->lo.assign(1, 0);
+    return VC_OK;
+  }
+  lp->n_cta = lp->n_stream;
+  constexpr long long group_bytes = 2 * static_cast<long long>(P::codes + P::meta);
+  const Partition part{lp->total, NGmax, kSwitchGroups * kRefGroupBytes / group_bytes,
+                       kTailGroups * kRefGroupBytes / group_bytes, lp->n_stream, slices};
+  part.fill(lp->lo);
+  // partial slots of a slice: its stream CTAs, then the tail
+  int mp = 1;
+  for (long long bh = 0; bh < slices; ++bh) {
+    const int first = cta_at(bh * NGmax, lp->lo.data(), lp->n_stream);
+    const int last = cta_at(bh * NGmax + NGmax - 1, lp->lo.data(), lp->n_stream);
+    mp = std::max(mp, last - first + 2);
+  }
+  lp->max_parts = mp;
   return VC_OK;
 }
 
+// Plans by (device, shape, max_packed): the partition costs a bisection, and
+// the draft steps of a decode loop repeat a handful of shapes.
+struct PlanKey {
+  int dev, d, bits, G, B, Hkv, max_packed;
+  bool operator==(const PlanKey& o) const {
+    return dev == o.dev && d == o.d && bits == o.bits && G == o.G && B == o.B && Hkv == o.Hkv && max_packed == o.max_packed;
+  }
+};
+constexpr int kPlanCache = 16;
+std::mutex g_plan_mu;
+PlanKey g_plan_key[kPlanCache];
+LaunchPlan g_plan_val[kPlanCache];
+int g_plan_n = 0, g_plan_next = 0;
+
+vc_status_t plan_uncached(const vc_shape_t* s, int max_packed, LaunchPlan* lp);
+
 vc_status_t plan(const vc_shape_t* s, int max_packed, LaunchPlan* lp) {
+  int dev = 0;
+  VC_CUDA_CHECK(cudaGetDevice(&dev));
+  const PlanKey key{dev, s->d, s->bits, s->Hq / s->Hkv, s->B, s->Hkv, max_packed};
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    for (int i = 0; i < g_plan_n; ++i)
+      if (g_plan_key[i] == key) {
+        *lp = g_plan_val[i];
+        return VC_OK;
+      }
+  }
+  const vc_status_t st = plan_uncached(s, max_packed, lp);
+  if (st != VC_OK) return st;
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  g_plan_key[g_plan_next] = key;
+  g_plan_val[g_plan_next] = *lp;
+  g_plan_next = (g_plan_next + 1) % kPlanCache;
+  g_plan_n = std::min(g_plan_n + 1, kPlanCache);
+  return VC_OK;
+}
+
+vc_status_t plan_uncached(const vc_shape_t* s, int max_packed, LaunchPlan* lp) {
   const int G = s->Hq / s->Hkv;
 #define VC_PLAN(D_, B_, G_) \
   if (s->d == D_ && s->bits == B_ && G == G_) return plan_t<D_, B_, G_>(s, max_packed, lp);
@@ -1065,6 +1204,7 @@ extern "C" vc_status_t vc_draft_attn(const vc_shape_t* s, const uint16_t* q, con
   a.scale_log2 = s->softmax_scale * kLog2e;
   a.wait_cycles = g_wait_cycles;
   a.withhold_first = g_withhold_first;
+  for (int c = 0; c <= lp.n_stream; ++c) a.lo_tab[c] = lp.lo[c];
   const size_t rows = static_cast<size_t>(s->B) * s->Hq * lp.max_parts;
   char* ws = static_cast<char*>(workspace);
   a.part_o = reinterpret_cast<float*>(ws);
