@@ -424,6 +424,83 @@ def time_prefill_rows(w, shape, device, cs):
     return rows
 
 
+def run_kernel(args, local_rank):
+    """--kernel draft|verify: one kernel alone on one layer of the workload,
+    `--calls` back-to-back launches timed with CUDA events (a small device
+    footprint and few launches, e.g. for ncu captures of that kernel).
+    draft: vc_draft_attn over the layer's packed prefix (Qwen: the kept
+    tokens), the current token only in the tail, calls chained as in a round.
+    verify: vc_verify_attn_chunk on one resident chunk of the exact K/V."""
+    import numpy as np
+    import torch
+
+    import synth
+    from verify_compressed_kv_gb300 import _lib as vc
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    w = workload_of(args)
+    peaks = load_peaks()
+    cs = torch.cuda.Stream(device)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device)
+    calls = max(1, args.calls)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    if args.kernel == "draft":
+        T = w.T_keep if w.keep_frac < 1.0 else w.T
+        shape = vc.shape(w.B, w.Hq, w.Hkv, w.d, w.k, w.bits, 1.0 / math.sqrt(w.d))
+        K, V = synth.kv(w, layer=0, group=0, T=T, threads=16)
+        packed = [torch.zeros(n, dtype=torch.uint8, device=device) for n in vc.vc_quant_packed_bytes(shape, T)]
+        vc.vc_quant_kv_pack(shape, T, T, dev(K), dev(V), *packed, cs)
+        del K, V
+        tail_cap = 32 + w.k + 1
+        tk = torch.zeros((w.B, w.Hkv, tail_cap, w.d), dtype=torch.int16, device=device)
+        tv = torch.zeros_like(tk)
+        plen = torch.full((w.B,), T, dtype=torch.int32, device=device)
+        tlen = torch.zeros(w.B, dtype=torch.int32, device=device)
+        q = dev(synth.draft_q(w, 0, 0))
+        kcur, vcur = (dev(x) for x in synth.draft_kv_cur(w, 0, 0))
+        out = torch.empty((w.B, w.Hq, w.d), dtype=torch.int16, device=device)
+        wsb = vc.vc_draft_attn_workspace_size(shape, T)
+        ws = torch.zeros(wsb, dtype=torch.uint8, device=device)
+
+        def call(i):
+            vc.vc_draft_attn(shape, q, kcur, vcur, *packed, plen, T, T, tk, tv, tlen, tail_cap, 0, out, ws, wsb, cs,
+                             flags=vc.VC_DRAFT_CHAINED if i > 0 else 0)
+        nbytes = algorithmic_draft_bytes(w, T)
+        status = vc.vc_draft_attn_device_status
+    else:
+        C = w.C
+        shape = vc.shape(w.B, w.Hq, w.Hkv, w.d, w.k, w.bits, 1.0 / math.sqrt(w.d))
+        parts = vc.vc_verify_attn_parts(shape, C)
+        wsb = vc.vc_verify_attn_workspace_size(shape, parts)
+        ws = torch.zeros(wsb, dtype=torch.uint8, device=device)
+        K, V = synth.kv(w, layer=0, group=0, T=C, threads=16)
+        slot = torch.stack([dev(K), dev(V)])
+        del K, V
+        q = dev(synth.verify_q(w, 0))
+        plen = torch.full((w.B,), 4 * C, dtype=torch.int32, device=device)
+
+        def call(i):
+            vc.vc_verify_attn_chunk(shape, q, slot, C, 0, plen, parts, True, ws, wsb, cs)
+        nbytes = 2 * w.B * w.Hkv * C * w.d * 2
+        status = vc.vc_verify_attn_device_status
+    torch.cuda.synchronize()
+    for i in range(3):
+        call(i)
+    ev[0].record(cs)
+    for i in range(calls):
+        call(3 + i)
+    ev[1].record(cs)
+    ev[1].synchronize()
+    ms = ev[0].elapsed_time(ev[1]) / calls
+    st = status()
+    if st != 0:
+        raise RuntimeError(f"device status {st:#x}")
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"workload": workload_name(w), "mode": "kernel", "kernel": args.kernel, "calls": calls, "ms_per_call": ms,
+            "bytes_per_call": nbytes, "gbs": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
+            "data": "synthetic"}
+
+
 def run_rows(args, local_rank):
     """--rows-only: the prefill rows of one layer, without the decode loop (a small
     device footprint, e.g. for kernel captures)."""
@@ -1273,6 +1350,9 @@ def main(argv=None):
     ap.add_argument("--k", type=int, default=0, help="draft length instead of the workload's own (0: keep it)")
     ap.add_argument("--rows-only", action="store_true",
                     help="time only the prefill rows (pack, token score / select / gather) of one layer")
+    ap.add_argument("--kernel", default="", choices=["", "draft", "verify"],
+                    help="time one kernel alone on one layer (3 warm-up + --calls launches)")
+    ap.add_argument("--calls", type=int, default=8, help="timed launches of --kernel")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1281,6 +1361,8 @@ def main(argv=None):
         out = run_reference(args, rank, world)
     elif args.rows_only:
         out = run_rows(args, local) if rank == 0 else None
+    elif args.kernel:
+        out = run_kernel(args, local) if rank == 0 else None
     elif args.adaptive:
         out = run_adaptive(args, local) if rank == 0 else None
     elif args.remote_prefix > 0:

@@ -218,7 +218,9 @@ vc_status_t vc_quant_kv_device_status(uint32_t* status);
  * position tail_len[b] + step (for the following draft steps); if NULL, the
  * current token is not added and the tail is not written.
  * q bf16 [B, Hq, d] -> out bf16 [B, Hq, d].  packed_len, tail_len: int32 [B]
- * device.  max_packed: an upper bound of packed_len over the batch (host).
+ * device.  max_packed: an upper bound of packed_len over the batch (host);
+ * the launch's partition spreads max_packed / 32 groups a slice over the
+ * SMs, so the tightest bound balances best.
  * One launch: the packed groups of all (request, KV head) slices are split
  * evenly over a persistent grid sized to the current device (stream-K), the
  * partials are merged with a log-sum-exp rule by the last CTA of each slice.
@@ -232,7 +234,9 @@ vc_status_t vc_quant_kv_device_status(uint32_t* status);
  * The workspace holds the partials and one arrival
  * counter per slice: it must be zero-filled before its first use, and every
  * call leaves the counters at zero again.  Its size depends on the device
- * (SM count, occupancy): query it with the same device current.  Calls that
+ * (SM count, occupancy) and the shape: query it with the same device
+ * current.  A size queried with some max_packed > 0 serves calls of the same
+ * shape with every max_packed.  Calls that
  * share a workspace must not overlap on the GPU, other than as chained calls
  * (below), which order their workspace accesses themselves.
  * flags: 0, or VC_DRAFT_CHAINED for a call enqueued directly after another

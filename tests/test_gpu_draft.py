@@ -209,6 +209,44 @@ def test_draft_chained_calls_equal_unchained_and_the_oracle(vc):
                 tk[0, 0, tlen[b] + i], tv[0, 0, tlen[b] + i] = cur[l, i][0][b, h], cur[l, i][1][b, h]
 
 
+def test_draft_max_packed_below_capacity(vc):
+    """A cache laid out for T_cap tokens holding fewer packed ones: calls with
+    max_packed at the capacity and at the packed length (a different partition)
+    both match the oracle, and the workspace sized for the capacity serves
+    both (its size does not depend on max_packed)."""
+    from gpu_util import dev, zeros_bytes, bf16_to_f64, DEV, assert_attn_close
+    w = synth.get("llama", B=2, T=2048)
+    T_cap, P = 4096, 2048
+    scale = 1.0 / math.sqrt(w.d)
+    s = vc.shape(w.B, w.Hq, w.Hkv, w.d, bits=w.bits, softmax_scale=scale)
+    sizes = {mp: vc.vc_draft_attn_workspace_size(s, mp) for mp in (32, 1024, P, T_cap)}
+    assert len(set(sizes.values())) == 1, sizes
+    K, V = synth.kv(w)
+    kcb, kszb, vcb, vszb = vc.vc_quant_packed_bytes(s, T_cap)
+    packed = [torch.zeros(n // e, dtype=dt, device=DEV)
+              for n, e, dt in ((kcb, 4, torch.int32), (kszb, 2, torch.int16), (vcb, 4, torch.int32), (vszb, 2, torch.int16))]
+    vc.vc_quant_kv_pack(s, P, T_cap, dev(K), dev(V), *packed)
+    rng = np.random.default_rng(5)
+    tail_cap = 32 + w.k + 1
+    tlen = np.array([3, 0], np.int32)
+    tk0 = synth.bf16_bits(rng.standard_normal((w.B, w.Hkv, tail_cap, w.d)).astype(np.float32))
+    tv0 = synth.bf16_bits(rng.standard_normal((w.B, w.Hkv, tail_cap, w.d)).astype(np.float32))
+    q = synth.draft_q(w, 0, 0)
+    k_cur, v_cur = synth.draft_kv_cur(w, 0, 0)
+    plen = np.full(w.B, P, np.int32)
+    want = oatt.draft_attention(q, *kivi.quant_pack(K, V, w.bits), plen, tk0, tv0, tlen, w.bits, scale,
+                                k_cur=k_cur, v_cur=v_cur, step=0)
+    wsb = sizes[T_cap]
+    for mp in (T_cap, P):
+        ws = zeros_bytes(wsb)
+        out = torch.empty((w.B, w.Hq, w.d), dtype=torch.int16, device=DEV)
+        vc.vc_draft_attn(s, dev(q), dev(k_cur), dev(v_cur), *packed, dev(plen), mp, T_cap, dev(tk0), dev(tv0),
+                         dev(tlen), tail_cap, 0, out, ws, wsb)
+        torch.cuda.synchronize()
+        assert vc.vc_draft_attn_device_status() == 0
+        assert_attn_close(bf16_to_f64(out), want, what=f"max_packed {mp}")
+
+
 def test_draft_argument_errors(vc):
     from gpu_util import DEV
     s = vc.shape(1, 4, 1, 96, bits=2)

@@ -96,3 +96,26 @@ def test_workload_table_matches_the_shapes():
     assert ll.layers == 8 and ll.G == 8 and ll.T == 131072
     st = synth.get("stagger")
     assert st.groups == 2 and st.B == 32 and st.k == 24
+
+
+def test_length_bounds_are_the_longest_request_not_a_sum_of_maxima():
+    """The host bounds the drafting and the full-KV transfer use: max_prefix is
+    the longest request's prefix (prefix at load + its own committed tokens,
+    n_acc + 1 a round), not the sum of each round's largest commit;
+    max_packed follows the same tokens from the packed length at load."""
+    from verify_compressed_kv_gb300.runtime import LengthBounds
+    b = LengthBounds(3)
+    b.prefix_from(1000)
+    b.packed_from(992)
+    assert (b.max_prefix, b.max_packed) == (1000, 992)
+    b.commit([5, 0, 2])                      # commits 6, 1, 3
+    assert (b.max_prefix, b.max_packed) == (1006, 998)
+    b.commit([0, 9, 2])                      # totals 7, 11, 6: the sum of maxima would say 16
+    assert (b.max_prefix, b.max_packed) == (1011, 1003)
+    b.commit([0, 0, 0])
+    assert b.max_prefix == 1012
+    b.prefix_from(2048)                      # a new prefix: commits counted from there
+    b.packed_from(512)                       # e.g. the kept tokens of a token-dropped prefix
+    assert (b.max_prefix, b.max_packed) == (2048, 512)
+    b.commit([31, 3, 0])
+    assert (b.max_prefix, b.max_packed) == (2080, 544)

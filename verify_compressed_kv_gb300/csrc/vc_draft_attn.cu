@@ -976,17 +976,18 @@ struct LaunchPlan {
 // (slice boundaries every NG groups) over n CTAs.  A CTA's cost is its
 // groups, plus `sw` per slice boundary strictly inside its range, plus `tl`
 // per bf16 tail it runs.  Each CTA in turn takes the longest range whose
-// cost stays within T; T is the smallest budget that covers every group, by
-// bisection.  Every range holds at least one group until the groups run out.
+// cost stays within T, but at least `min_range` groups (so that a slice
+// meets a bounded number of CTAs); T is the smallest budget that covers
+// every group, by bisection.
 struct Partition {
   long long total, NG, sw, tl;
   int n;
-  long long nbh;
+  long long nbh, min_range;
   long long crossings(long long p, long long e) const { return e > p + 1 ? (e - 1) / NG - p / NG : 0; }
   long long end_of(int c, long long p, long long T) const {
     long long budget = T - tl * (tail_lo(c + 1, n, nbh) - tail_lo(c, n, nbh));
     if (budget < 1) budget = 1;
-    long long best = std::min(total, p + 1);
+    long long best = std::min(total, p + min_range);
     for (long long k = 0;; ++k) {               // ends between boundaries, crossing at most k
       const long long e = std::min(total, p + budget - sw * k);
       if (e <= p) break;
@@ -1038,7 +1039,8 @@ vc_status_t plan_t(const vc_shape_t* s, int max_packed, LaunchPlan* lp) {
   const long long slices = static_cast<long long>(s->B) * s->Hkv;
   lp->total = slices * NGmax;
   if (lp->total > INT_MAX) VC_FAIL(VC_ERR_UNSUPPORTED, "B * Hkv * max_packed / 32 = %lld groups exceeds 2^31 - 1", lp->total);
-  long long n = std::min<long long>(static_cast<long long>(occ) * sms, kMaxStream);
+  const long long n_max = std::min<long long>(static_cast<long long>(occ) * sms, kMaxStream);
+  long long n = n_max;
   const long long by_work = lp->total / kWarps;                 // at least one stage per CTA
   if (n > by_work) n = by_work;
   if (n < 1 && lp->total > 0) n = 1;
@@ -1051,18 +1053,24 @@ vc_status_t plan_t(const vc_shape_t* s, int max_packed, LaunchPlan* lp) {
     return VC_OK;
   }
   lp->n_cta = lp->n_stream;
+  // partial slots of a slice: at most `stream_parts` stream CTAs, a bound set
+  // by the device and B * Hkv alone (so that a workspace sized for one
+  // max_packed serves every max_packed), then the tail.  Each range inside a
+  // slice holds >= min_range groups, so at most stream_parts - 2 of them fit.
+  const long long stream_parts = std::min(n_max, 2 * ((n_max + slices - 1) / slices) + 2);
+  const long long min_range = stream_parts >= n ? 1 : (NGmax + stream_parts - 3) / (stream_parts - 2);
+  lp->max_parts = static_cast<int>(stream_parts) + 1;
   constexpr long long group_bytes = 2 * static_cast<long long>(P::codes + P::meta);
   const Partition part{lp->total, NGmax, kSwitchGroups * kRefGroupBytes / group_bytes,
-                       kTailGroups * kRefGroupBytes / group_bytes, lp->n_stream, slices};
+                       kTailGroups * kRefGroupBytes / group_bytes, lp->n_stream, slices, min_range};
   part.fill(lp->lo);
-  // partial slots of a slice: its stream CTAs, then the tail
-  int mp = 1;
   for (long long bh = 0; bh < slices; ++bh) {
     const int first = cta_at(bh * NGmax, lp->lo.data(), lp->n_stream);
     const int last = cta_at(bh * NGmax + NGmax - 1, lp->lo.data(), lp->n_stream);
-    mp = std::max(mp, last - first + 2);
+    if (last - first + 2 > lp->max_parts)
+      VC_FAIL(VC_ERR_UNSUPPORTED, "partition: slice %lld meets %d CTAs (bound %d)", bh, last - first + 1,
+              lp->max_parts - 1);
   }
-  lp->max_parts = mp;
   return VC_OK;
 }
 

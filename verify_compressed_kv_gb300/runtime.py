@@ -56,6 +56,38 @@ class RoundInputs:
         return int(self.drafts.shape[1])
 
 
+class LengthBounds:
+    """Host-side bounds of a group's lengths, kept from the accepted lengths
+    read back every round (each request commits n_acc + 1 tokens a round):
+    max_prefix is the longest request's prefix, exactly; max_packed bounds
+    packed_len (the tokens packed at load plus every token committed since;
+    packed_len is a multiple of 32 at most that)."""
+
+    def __init__(self, B):
+        self.committed = torch.zeros(B, dtype=torch.int64)
+        self.prefix0 = self.packed0 = 0
+
+    def prefix_from(self, T):
+        """The full prefix was (re)written with T tokens a request."""
+        self.prefix0 = T
+        self.committed.zero_()
+
+    def packed_from(self, T):
+        """The draft cache was (re)loaded with T packed tokens a request."""
+        self.packed0 = T
+
+    def commit(self, n_acc):
+        self.committed += torch.as_tensor(n_acc).to(torch.int64) + 1
+
+    @property
+    def max_prefix(self):
+        return self.prefix0 + int(self.committed.max())
+
+    @property
+    def max_packed(self):
+        return self.packed0 + int(self.committed.max())
+
+
 class Group:
     def __init__(self, B, Hq, Hkv, d, k, bits, V, C, T0, layers=1, extra_tokens=None, n_slots=None,
                  parts_per_chunk=None, softmax_scale=1.0, device="cuda", packed_T0=None,
@@ -90,7 +122,7 @@ class Group:
         self.host_kv = [torch.empty(self.n_chunks_cap * self.chunk_elems, dtype=torch.int16, pin_memory=True)
                         for _ in range(layers)]
         self.prefix_len = [torch.zeros(B, dtype=torch.int32, device=dev) for _ in range(layers)]
-        self.max_prefix = 0          # host-side bound of prefix_len (exact: read back every round)
+        self.bounds = LengthBounds(B)
         # ---- verify rings (one per layer) + workspaces.  A round prefetches every
         # layer's first chunks while the group drafts, so the link is busy from the
         # start of the round; by default each ring holds all of its layer's chunks
@@ -117,6 +149,10 @@ class Group:
         self.next_tok = torch.zeros(B, dtype=torch.int32, device=dev)
         self.n_acc_host = torch.zeros(B, dtype=torch.int32, pin_memory=True)
         self._shapes = {}
+
+    @property
+    def max_prefix(self):
+        return self.bounds.max_prefix
 
     def shape_k(self, k):
         """Shape struct of a round drafting k <= self.k tokens (buffers and
@@ -152,8 +188,7 @@ class Group:
         self.packed_len[layer].fill_(T0)
         self.tail_len[layer].zero_()
         self.write_store(layer, K, V)
-        self.prefix_len[layer].fill_(T0)
-        self.max_prefix = T0
+        self.bounds.packed_from(T0)
 
     def load_packed_only(self, layer, K, V, stream=None):
         """Draft cache from an already-compressed (e.g. token-dropped) prefix."""
@@ -162,6 +197,7 @@ class Group:
                             self.vsz[layer], stream)
         self.packed_len[layer].fill_(T)
         self.tail_len[layer].zero_()
+        self.bounds.packed_from(T)
 
     # ---------------------------------------------------------------- remote prefix (emulated)
     def export_packed(self, layer, T):
@@ -201,6 +237,7 @@ class Group:
         with torch.cuda.stream(stream):
             self.packed_len[layer].fill_(T)
             self.tail_len[layer].zero_()
+        self.bounds.packed_from(T)
         return time.perf_counter() - t0
 
     def write_store(self, layer, K, V):
@@ -212,7 +249,7 @@ class Group:
             st[c, 0, :, :, :n].copy_(K[:, :, c * self.C:c * self.C + n])
             st[c, 1, :, :, :n].copy_(V[:, :, c * self.C:c * self.C + n])
         self.prefix_len[layer].fill_(T)
-        self.max_prefix = T
+        self.bounds.prefix_from(T)
 
     # ---------------------------------------------------------------- the round's steps
     def prefetch(self, layer, copy_stream):
@@ -227,9 +264,12 @@ class Group:
     def draft_step(self, inp: RoundInputs, layer: int, step: int, stream, chained=False):
         """chained: the previous work on `stream` is another draft call, so
         this one may start while that one finishes (VC_DRAFT_CHAINED)."""
+        # packed_len is a multiple of 32 no larger than the host bound: the
+        # partition then covers the packed groups, not the cache's capacity
+        max_packed = min(self.P_cap, self.bounds.max_packed // GROUP * GROUP)
         vc.vc_draft_attn(self.shape, inp.q_draft[layer, step], inp.kv_cur[0, layer, step], inp.kv_cur[1, layer, step],
                          self.kc[layer], self.ksz[layer], self.vc[layer], self.vsz[layer], self.packed_len[layer],
-                         self.P_cap, self.P_cap, self.tail_k[layer], self.tail_v[layer], self.tail_len[layer],
+                         max_packed, self.P_cap, self.tail_k[layer], self.tail_v[layer], self.tail_len[layer],
                          self.tail_cap, step, self.draft_out, self.ws_draft, self.ws_draft_bytes, stream,
                          flags=vc.VC_DRAFT_CHAINED if chained else 0)
         self.launches += 1                     # stream CTAs, tail CTAs and the combine: one grid
@@ -293,7 +333,7 @@ class Group:
     def after_round(self):
         """Host bookkeeping once the read-back has landed."""
         n = self.n_acc_host
-        self.max_prefix += int(n.max()) + 1
+        self.bounds.commit(n)
         if self.max_prefix > self.T_cap:
             raise RuntimeError(f"the group's full-KV store holds {self.T_cap} tokens a request, the prefix reached "
                                f"{self.max_prefix}: size extra_tokens for every round the group makes")
