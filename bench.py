@@ -259,9 +259,14 @@ def source_hash(path):
     return hashlib.sha256("".join(text.split()).encode()).hexdigest()[:16]
 
 
-def ncu_traffic(kernel_file, workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current source of the kernel (else None)."""
+def ncu_traffic(kernel_file, workload, alg_bytes):
+    """DRAM bytes of one draft launch moving `alg_bytes` algorithmic bytes, from
+    the committed ncu summary if it was taken on the current source of the
+    kernel (else None).  The capture's launch (one layer of the workload at
+    its prefix length) moves the summary's algorithmic bytes; the launches a
+    bench times carry the tokens the rounds appended, and the DRAM bytes are
+    scaled by the ratio of algorithmic bytes (the kernel reads every packed
+    byte once, so its traffic grows in proportion)."""
     prof = os.path.join(ROOT, "profiles", f"draft_attn_{workload}.md")
     if not os.path.exists(prof):
         return None
@@ -273,8 +278,8 @@ def ncu_traffic(kernel_file, workload):
     if kv.get("source_sha256_16") != source_hash(kernel_file):
         return None
     try:
-        return float(kv["dram_bytes_per_launch_full_size"])
-    except (KeyError, ValueError):
+        return float(kv["dram_bytes_per_launch"]) * alg_bytes / float(kv["algorithmic_bytes_per_launch"])
+    except (KeyError, ValueError, ZeroDivisionError):
         return None
 
 
@@ -425,12 +430,13 @@ def time_prefill_rows(w, shape, device, cs):
 
 
 def run_kernel(args, local_rank):
-    """--kernel draft|verify: one kernel alone on one layer of the workload,
-    `--calls` back-to-back launches timed with CUDA events (a small device
-    footprint and few launches, e.g. for ncu captures of that kernel).
+    """--kernel draft|verify|accept: one kernel alone on one layer of the
+    workload, `--calls` back-to-back launches timed with CUDA events (a small
+    device footprint and few launches, e.g. for ncu captures of that kernel).
     draft: vc_draft_attn over the layer's packed prefix (Qwen: the kept
     tokens), the current token only in the tail, calls chained as in a round.
-    verify: vc_verify_attn_chunk on one resident chunk of the exact K/V."""
+    verify: vc_verify_attn_chunk on one resident chunk of the exact K/V.
+    accept: vc_accept on the round's logits and drafts."""
     import numpy as np
     import torch
 
@@ -467,7 +473,7 @@ def run_kernel(args, local_rank):
                              flags=vc.VC_DRAFT_CHAINED if i > 0 else 0)
         nbytes = algorithmic_draft_bytes(w, T)
         status = vc.vc_draft_attn_device_status
-    else:
+    elif args.kernel == "verify":
         C = w.C
         shape = vc.shape(w.B, w.Hq, w.Hkv, w.d, w.k, w.bits, 1.0 / math.sqrt(w.d))
         parts = vc.vc_verify_attn_parts(shape, C)
@@ -483,6 +489,19 @@ def run_kernel(args, local_rank):
             vc.vc_verify_attn_chunk(shape, q, slot, C, 0, plen, parts, True, ws, wsb, cs)
         nbytes = 2 * w.B * w.Hkv * C * w.d * 2
         status = vc.vc_verify_attn_device_status
+    else:
+        logits, drafts, _ = synth.logits_and_drafts(w, 0)
+        lg = torch.from_numpy(np.ascontiguousarray(logits, np.float32)).to(device)
+        dr = torch.from_numpy(np.ascontiguousarray(drafts, np.int32)).to(device)
+        n_acc = torch.zeros(w.B, dtype=torch.int32, device=device)
+        nxt = torch.zeros_like(n_acc)
+        wsb = vc.vc_accept_workspace_size(w.B, w.k, w.V)
+        ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=device)
+
+        def call(i):
+            vc.vc_accept(w.B, w.k, w.V, lg, dr, n_acc, nxt, None, ws, wsb, cs)
+        nbytes = lg.numel() * 4
+        status = lambda: 0
     torch.cuda.synchronize()
     for i in range(3):
         call(i)
@@ -762,7 +781,7 @@ def run_ours(args, rank, world, local_rank):
     value, e2e_value, t_max = reduce_over_ranks(value_local, e2e_local, total_ms, world)
 
     draft_src = os.path.join(ROOT, "verify_compressed_kv_gb300", "csrc", "vc_draft_attn.cu")
-    traffic = ncu_traffic(draft_src, args.workload)
+    traffic = ncu_traffic(draft_src, args.workload, alg_bytes)
     link_peak = measured_link
     h2d_rate = (h2d_bytes / args.steps) / (med(copy_span) / 1e3) / 1e9 if copy_span else None
     out = {
@@ -1350,7 +1369,7 @@ def main(argv=None):
     ap.add_argument("--k", type=int, default=0, help="draft length instead of the workload's own (0: keep it)")
     ap.add_argument("--rows-only", action="store_true",
                     help="time only the prefill rows (pack, token score / select / gather) of one layer")
-    ap.add_argument("--kernel", default="", choices=["", "draft", "verify"],
+    ap.add_argument("--kernel", default="", choices=["", "draft", "verify", "accept"],
                     help="time one kernel alone on one layer (3 warm-up + --calls launches)")
     ap.add_argument("--calls", type=int, default=8, help="timed launches of --kernel")
     args = ap.parse_args(argv)
