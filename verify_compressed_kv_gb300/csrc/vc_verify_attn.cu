@@ -74,6 +74,41 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// 2^x (ex2.approx.ftz: relative error ~2^-22; results below 2^-126 flush to
+// 0, far below what a bf16 softmax weight next to the row's max can hold)
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Two fp32 lanes in one 64-bit register pair (fma/add .f32x2, sm_100 and later).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -446,13 +481,17 @@ __global__ void __launch_bounds__(kTcThreads) verify_chunk_tc(VerifyArgs a, cons
       float sv[kTcTok];
       __syncwarp();
       vc_tc_ld64(t_lane + P::col_s + bb * kTcTok, sv);
+      // raw scores: the max commutes with the (positive) scale, which enters
+      // once per tile here and once per score inside the exponent below
       const int t0 = t_lo + i * kTcTok;
-      float mx = -INFINITY;
+      if (t0 + kTcTok > t_hi) {                              // a part's last tile: mask past t_hi
 #pragma unroll
-      for (int x = 0; x < kTcTok; ++x) {
-        sv[x] = (t0 + x < t_hi) ? sv[x] * a.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, sv[x]);
+        for (int x = 0; x < kTcTok; ++x) sv[x] = (t0 + x < t_hi) ? sv[x] : -INFINITY;
       }
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int x = 0; x < kTcTok; x += 2) mq[(x >> 1) & 3] = fmax3(mq[(x >> 1) & 3], sv[x], sv[x + 1]);
+      const float mx = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]) * a.scale_log2;
       // Raise the running max of the rows that outgrew it by more than kTcLazy
       // (log2 units; rare after the first tile).  The decision is per warp:
       // TMEM loads and stores are warp-collective, so every lane takes part and
@@ -460,7 +499,7 @@ __global__ void __launch_bounds__(kTcThreads) verify_chunk_tc(VerifyArgs a, cons
       const bool raise = mx > m + kTcLazy;
       if (__any_sync(0xffffffffu, raise)) {
         const float mn = raise ? mx : m;                     // finite: every tile holds a valid token
-        const float alpha = exp2f(m - mn);                   // m = -inf: 0
+        const float alpha = fast_exp2(m - mn);               // m = -inf: 0
         if (i > 0 && ok) {                                   // O holds tiles 0 .. i-1: rescale it in TMEM
           ok = __all_sync(0xffffffffu, wait(o_done + ((i - 1) & 1), static_cast<uint32_t>(((i - 1) >> 1) & 1)));
           vc_tc_fence_after();
@@ -482,15 +521,23 @@ __global__ void __launch_bounds__(kTcThreads) verify_chunk_tc(VerifyArgs a, cons
         l *= alpha;
         m = mn;
       }
+      // weights 2^(s * scale - m) two lanes per instruction; the sum in two
+      // lane pairs
       uint32_t pk[kTcTok / 2];
-      float ps = 0.0f;
+      const uint64_t c2 = f2_pack(a.scale_log2, a.scale_log2), nm2 = f2_pack(-m, -m);
+      uint64_t ps2[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};
 #pragma unroll
       for (int x = 0; x < kTcTok / 2; ++x) {
-        const float p0 = exp2f(sv[2 * x] - m), p1 = exp2f(sv[2 * x + 1] - m);
-        ps += p0 + p1;
+        float e0, e1;
+        f2_unpack(f2_fma(f2_pack(sv[2 * x], sv[2 * x + 1]), c2, nm2), e0, e1);
+        const float p0 = fast_exp2(e0), p1 = fast_exp2(e1);
+        ps2[x & 1] = f2_add(ps2[x & 1], f2_pack(p0, p1));
         pk[x] = pack_bf16(p0, p1);
       }
-      l += ps;
+      float q0, q1, q2, q3;
+      f2_unpack(ps2[0], q0, q1);
+      f2_unpack(ps2[1], q2, q3);
+      l += (q0 + q1) + (q2 + q3);
       // P (bf16 pairs) over the first kTcTok / 2 columns of this tile's S
       __syncwarp();
       vc_tc_st16(t_lane + P::col_s + bb * kTcTok, *reinterpret_cast<const uint32_t(*)[16]>(pk));
