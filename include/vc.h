@@ -259,6 +259,22 @@ vc_status_t vc_draft_attn(const vc_shape_t* s, const uint16_t* q, const uint16_t
                           void* workspace, size_t workspace_bytes, uint32_t flags, vc_stream_t stream);
 /* Device status (barrier time-outs) since the last call; synchronises. */
 vc_status_t vc_draft_attn_device_status(uint32_t* status);
+/* The stream-K partition a vc_draft_attn launch uses, computed on the host
+ * (no device access), for inspection and tests.  The packed groups of the
+ * B * Hkv slices (max_packed / 32 each) are laid end to end, slice-major.
+ * slots is the launch's CTA slots: occupancy x SM count, one CTA per SM for
+ * this kernel.  Outputs:
+ *   n_stream   the stream CTAs: at most slots (and 512), at most one per 11
+ *              groups, 0 when max_packed is 0;
+ *   lo         lo[0 .. n_stream]: CTA c takes groups [lo[c], lo[c + 1]);
+ *              lo[0] = 0 and lo[n_stream] = the groups in all;
+ *   max_parts  partial slots of a slice: the bound of stream CTAs that meet
+ *              one slice, plus the tail's slot.
+ * A CTA's range is balanced by cost: its groups, plus a charge per slice
+ * boundary inside it and per bf16 tail pass it runs, scaled by the bytes of
+ * a group.  lo_len < n_stream + 1: VC_ERR_INVALID_ARG. */
+vc_status_t vc_draft_attn_partition(const vc_shape_t* s, int32_t max_packed, int32_t slots, int32_t* n_stream,
+                                    int32_t* lo, int32_t lo_len, int32_t* max_parts);
 /* Test hooks, for the failure-detection test only (host-side settings of this
  * library, not thread-safe, apply to later vc_draft_attn calls):
  *   wait_cycles           bound of every mbarrier wait of the draft kernel in

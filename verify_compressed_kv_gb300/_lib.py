@@ -79,6 +79,7 @@ _SIGS = {
         "vc_draft_attn": [S, P, P, P, P, P, P, P, P, I32, I32, P, P, P, I32, I32, P, P, SZ, c_uint32, P],
         "vc_draft_attn_device_status": [POINTER(c_uint32)],
         "vc_draft_attn_test_hooks": [ctypes.c_int64, I32],
+        "vc_draft_attn_partition": [S, I32, I32, POINTER(c_int32), P, I32, POINTER(c_int32)],
     },
     "vc_verify_attn": {
         "vc_verify_attn_workspace_size": [S, I32, POINTER(c_size_t)],
@@ -231,6 +232,16 @@ def vc_draft_attn(s, q, k_cur, v_cur, kc, ksz, vc, vsz, packed_len, max_packed, 
     _call("vc_draft_attn", ctypes.byref(s), _ptr(q), _ptr(k_cur), _ptr(v_cur), _ptr(kc), _ptr(ksz),
           _ptr(vc), _ptr(vsz), _ptr(packed_len), max_packed, T_cap, _ptr(tail_k), _ptr(tail_v),
           _ptr(tail_len), tail_cap, step, _ptr(out), _ptr(ws), ws_bytes, int(flags), _stream(stream))
+
+
+def vc_draft_attn_partition(s, max_packed, slots):
+    """(n_stream, lo [n_stream + 1] int list, max_parts) of the launch's stream-K partition."""
+    n, mp = c_int32(), c_int32()
+    cap = 513
+    buf = (c_int32 * cap)()
+    _call("vc_draft_attn_partition", ctypes.byref(s), max_packed, slots, ctypes.byref(n), ctypes.cast(buf, c_void_p),
+          cap, ctypes.byref(mp))
+    return n.value, list(buf[:n.value + 1]), mp.value
 
 
 def vc_draft_attn_test_hooks(wait_cycles: int, withhold_first_stage: int) -> None:

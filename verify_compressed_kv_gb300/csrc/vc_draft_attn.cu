@@ -1025,29 +1025,21 @@ struct Partition {
   }
 };
 
-template <int D, int BITS, int G>
-vc_status_t plan_t(const vc_shape_t* s, int max_packed, LaunchPlan* lp) {
-  using P = Plan<D, BITS, G>;
-  auto fn = draft_kernel<D, BITS, G, MinBlocks<G>::value>;
-  VC_CUDA_CHECK(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P::total)));
-  int dev = 0, sms = 0, occ = 0;
-  VC_CUDA_CHECK(cudaGetDevice(&dev));
-  VC_CUDA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  VC_CUDA_CHECK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kThreads, P::total));
-  if (occ < 1) VC_FAIL(VC_ERR_UNSUPPORTED, "draft kernel does not fit on an SM");
-  const long long NGmax = max_packed / kGroup;
-  const long long slices = static_cast<long long>(s->B) * s->Hkv;
+// The stream CTAs, partition table and partial slots of a launch over
+// `slices` slices of NGmax groups, with `slots` launch slots (occupancy x
+// SMs); host only.  group_bytes: the packed bytes of one group (K and V
+// codes, K and V scale/zero), which scale the partition's charges.
+vc_status_t partition_plan(long long slices, long long NGmax, long long slots, long long group_bytes, LaunchPlan* lp) {
   lp->total = slices * NGmax;
   if (lp->total > INT_MAX) VC_FAIL(VC_ERR_UNSUPPORTED, "B * Hkv * max_packed / 32 = %lld groups exceeds 2^31 - 1", lp->total);
-  const long long n_max = std::min<long long>(static_cast<long long>(occ) * sms, kMaxStream);
+  const long long n_max = std::min<long long>(slots, kMaxStream);
   long long n = n_max;
   const long long by_work = lp->total / kWarps;                 // at least one stage per CTA
   if (n > by_work) n = by_work;
   if (n < 1 && lp->total > 0) n = 1;
   lp->n_stream = static_cast<int>(lp->total > 0 ? n : 0);
-  lp->smem = P::total;
   if (lp->n_stream == 0) {                                      // tail CTAs alone
-    lp->n_cta = static_cast<int>(std::min<long long>(slices, static_cast<long long>(occ) * sms));
+    lp->n_cta = static_cast<int>(std::min(slices, slots));
     lp->max_parts = 1;
     lp->lo.assign(1, 0);
     return VC_OK;
@@ -1060,7 +1052,6 @@ vc_status_t plan_t(const vc_shape_t* s, int max_packed, LaunchPlan* lp) {
   const long long stream_parts = std::min(n_max, 2 * ((n_max + slices - 1) / slices) + 2);
   const long long min_range = stream_parts >= n ? 1 : (NGmax + stream_parts - 3) / (stream_parts - 2);
   lp->max_parts = static_cast<int>(stream_parts) + 1;
-  constexpr long long group_bytes = 2 * static_cast<long long>(P::codes + P::meta);
   const Partition part{lp->total, NGmax, kSwitchGroups * kRefGroupBytes / group_bytes,
                        kTailGroups * kRefGroupBytes / group_bytes, lp->n_stream, slices, min_range};
   part.fill(lp->lo);
@@ -1072,6 +1063,21 @@ vc_status_t plan_t(const vc_shape_t* s, int max_packed, LaunchPlan* lp) {
               lp->max_parts - 1);
   }
   return VC_OK;
+}
+
+template <int D, int BITS, int G>
+vc_status_t plan_t(const vc_shape_t* s, int max_packed, LaunchPlan* lp) {
+  using P = Plan<D, BITS, G>;
+  auto fn = draft_kernel<D, BITS, G, MinBlocks<G>::value>;
+  VC_CUDA_CHECK(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P::total)));
+  int dev = 0, sms = 0, occ = 0;
+  VC_CUDA_CHECK(cudaGetDevice(&dev));
+  VC_CUDA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  VC_CUDA_CHECK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kThreads, P::total));
+  if (occ < 1) VC_FAIL(VC_ERR_UNSUPPORTED, "draft kernel does not fit on an SM");
+  lp->smem = P::total;
+  return partition_plan(static_cast<long long>(s->B) * s->Hkv, max_packed / kGroup, static_cast<long long>(occ) * sms,
+                        2 * static_cast<long long>(P::codes + P::meta), lp);
 }
 
 // Plans by (device, shape, max_packed): the partition costs a bisection, and
@@ -1222,6 +1228,24 @@ extern "C" vc_status_t vc_draft_attn(const vc_shape_t* s, const uint16_t* q, con
   a.counter = reinterpret_cast<unsigned int*>(ws + off);
   a.out = out;
   return launch(s, a, lp, reinterpret_cast<cudaStream_t>(stream), (flags & VC_DRAFT_CHAINED) != 0u);
+}
+
+extern "C" vc_status_t vc_draft_attn_partition(const vc_shape_t* s, int32_t max_packed, int32_t slots,
+                                               int32_t* n_stream, int32_t* lo, int32_t lo_len, int32_t* max_parts) {
+  vc_status_t st = check(s);
+  if (st != VC_OK) return st;
+  VC_REQUIRE(n_stream && lo && max_parts, "NULL pointer");
+  VC_REQUIRE(max_packed >= 0 && max_packed % kGroup == 0, "max_packed must be a non-negative multiple of 32");
+  VC_REQUIRE(slots >= 1, "slots must be >= 1");
+  LaunchPlan lp;
+  const long long group_bytes = 8LL * s->d * (s->bits + 1);    // K and V codes, K and V scale/zero
+  if ((st = partition_plan(static_cast<long long>(s->B) * s->Hkv, max_packed / kGroup, slots, group_bytes, &lp)) != VC_OK)
+    return st;
+  VC_REQUIRE(lo_len >= lp.n_stream + 1, "lo holds %d entries, the partition needs %d", lo_len, lp.n_stream + 1);
+  for (int c = 0; c <= lp.n_stream; ++c) lo[c] = lp.lo[c];
+  *n_stream = lp.n_stream;
+  *max_parts = lp.max_parts;
+  return VC_OK;
 }
 
 extern "C" vc_status_t vc_draft_attn_test_hooks(int64_t wait_cycles, int32_t withhold_first_stage) {
