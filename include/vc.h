@@ -400,11 +400,11 @@ vc_status_t vc_accept(int32_t B, int32_t k, int32_t V, const float* logits, cons
  * every GPU that loads libvc_accept.so holds until the process exits.  Limits:
  * B <= 4096 and B*(k+1)*S <= 6144, S = splits per row = min(ceil(1216 /
  * (B*(k+1))), ceil(V / 2048)), at least 1 (e.g. B=8, k=16, V=32768 uses
- * 1224); larger calls return VC_ERR_CAPACITY with the reason.  The first call
- * on a device looks up the array's device address (cudaGetSymbolAddress) for
- * that device: make that first call before any stream capture.  The address
- * is kept for the life of the process, so a cudaDeviceReset after that first
- * call is unsupported (the kept address would be stale).  Each call
+ * 1224); larger calls return VC_ERR_CAPACITY with the reason.  Every call
+ * looks up the array's address on the current device (cudaGetSymbolAddress,
+ * a host query that allocates nothing), so a context made after a
+ * cudaDeviceReset gets its own.  The first call on a device also loads the
+ * library's module there: make it before any stream capture.  Each call
  * zeroes the counters it needs on the stream before its kernel.  All calls
  * share the one array: calls that overlap on the GPU (other streams, other
  * host threads) race and return wrong results.  No cudaMalloc / cudaFree or

@@ -13,7 +13,6 @@
 // folds the partials in split order, so ties resolve to the lowest index,
 // and writes n_acc / next_tok / argmax.  HBM-bound: B*(k+1)*V*4 bytes read.
 #include <cfloat>
-#include <mutex>
 
 #include "vc_internal.h"
 
@@ -219,23 +218,14 @@ struct NoAllocScratch {
 };
 static __device__ __align__(256) NoAllocScratch g_accept_scratch;
 
-// Device address of g_accept_scratch for each device, looked up on first use.
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
-std::mutex g_scratch_mu;
-
+// Device address of g_accept_scratch on the current device, looked up on
+// every call (a host-side query, no allocation and no synchronisation), so
+// that a new context after a device reset gets its own address.
 vc_status_t scratch_address(NoAllocScratch** out) {
-  int dev = 0;
-  VC_CUDA_CHECK(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= kMaxDevices) VC_FAIL(VC_ERR_UNSUPPORTED, "device index %d >= %d", dev, kMaxDevices);
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_accept_scratch);
-    if (e != cudaSuccess) VC_FAIL(VC_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-    g_scratch_addr[dev] = p;
-  }
-  *out = static_cast<NoAllocScratch*>(g_scratch_addr[dev]);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_accept_scratch);
+  if (e != cudaSuccess) VC_FAIL(VC_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+  *out = static_cast<NoAllocScratch*>(p);
   return VC_OK;
 }
 }  // namespace
