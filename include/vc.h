@@ -286,7 +286,10 @@ vc_status_t vc_draft_attn_partition(const vc_shape_t* s, int32_t max_packed, int
  * A call that ran out raises the barrier time-out bit of
  * vc_draft_attn_device_status, leaves its output undefined and its workspace
  * dirty: zero the workspace before reusing it.  No wait is unbounded and no
- * fault is raised. */
+ * fault is raised.  With a short bound, do not chain calls
+ * (VC_DRAFT_CHAINED): a chained call's producer fills its ring and then waits
+ * for consumers that themselves wait for the previous call, and that wait
+ * counts against the bound. */
 vc_status_t vc_draft_attn_test_hooks(int64_t wait_cycles, int32_t withhold_first_stage);
 
 /* ----------------------------------------------------- libvc_verify_attn
