@@ -642,7 +642,8 @@ __device__ void arrive_and_combine(const DraftArgs& a, unsigned int* flag, int b
 
 // ------------------------------------------------------------------ bf16 tail
 // The bf16 tail tokens 0 .. tail_len + step - 1 and the current token of slice
-// bh, taken by the consumer warps of a tail CTA.  Warp w takes the tokens t = w
+// bh, taken by the consumer warps of the stream CTA the slice's tail is
+// assigned to (of a tail CTA when there are no packed groups).  Warp w takes the tokens t = w
 // (mod kWarps), 8 in flight, K and V rows straight from global memory (each
 // lane D/32 channels), with an online-softmax state per head in registers;
 // the warps' (max, sum, output) go to the warp-merge region and
