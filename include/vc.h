@@ -240,14 +240,15 @@ vc_status_t vc_quant_kv_device_status(uint32_t* status);
  * share a workspace must not overlap on the GPU, other than as chained calls
  * (below), which order their workspace accesses themselves.
  * flags: 0, or VC_DRAFT_CHAINED for a call enqueued directly after another
- * vc_draft_attn call on the same stream (the draft steps of a round, layer
- * after layer).  Such a call is launched with programmatic dependent launch:
- * its CTAs may start while the previous call's last CTAs run, and before
- * that call has finished they read only this call's packed cache (kc, ksz,
- * vc, vsz, packed_len); queries, k_cur/v_cur, the tail, the workspace and
- * out are touched only after it.  The caller guarantees that the packed
- * cache was complete before the previous call was enqueued (no draft call
- * writes one).  Other bits: VC_ERR_INVALID_ARG.
+ * vc_draft_attn call on the same stream, with no other work between them
+ * (the draft steps of a round, layer after layer).  Such a call is launched
+ * with programmatic dependent launch: its CTAs may start while the previous
+ * call's last CTAs run, and before that call has finished they read only
+ * this call's packed cache (kc, ksz, vc, vsz, packed_len), which no draft
+ * call writes; queries, k_cur/v_cur, the tail, the workspace and out are
+ * touched only after it.  So work that writes a packed cache (pack, append,
+ * staging) goes before a chain's first, unchained call.  Other bits:
+ * VC_ERR_INVALID_ARG.
  * Reads B, Hq, Hkv, d, bits, softmax_scale. */
 #define VC_DRAFT_CHAINED 1u
 vc_status_t vc_draft_attn_workspace_size(const vc_shape_t* s, int32_t max_packed, size_t* bytes);
