@@ -54,7 +54,7 @@ typedef struct CUstream_st* vc_stream_t; /* ABI-identical to cudaStream_t */
 typedef enum {
   VC_OK = 0,
   VC_ERR_INVALID_ARG = 1, /* NULL / misaligned pointer, negative or inconsistent size */
-  VC_ERR_UNSUPPORTED = 2, /* valid but not built: bits not in {2,4}, d not in {64,128}, G > 8 ... */
+  VC_ERR_UNSUPPORTED = 2, /* valid but not built: bits not in {2,4,8}, d not in {64,128}, G > 8 ... */
   VC_ERR_CUDA = 3,        /* a CUDA runtime call failed (text in vc_last_error) */
   VC_ERR_TIMEOUT = 4,     /* a bounded wait expired (host event wait or device barrier) */
   VC_ERR_WORKSPACE = 5,   /* workspace pointer NULL or smaller than *_workspace_size() */
